@@ -1,0 +1,324 @@
+/*
+ * libbiv -- batch-invariant transformer forward for one GB300 (sm_103a).
+ *
+ * Every call computes each output row from that row's own inputs (and its own
+ * sequence's KV cache or SSM state) with one fixed reduction order, so a
+ * token's logprob does not change with batch size, batch mix, prefill vs
+ * chunked prefill vs decode, eager vs CUDA-Graph replay, or rollout vs
+ * trainer recompute.  The requirement and the rules that achieve it (one
+ * computation path, one quantisation rule, one tie-break, one accumulation
+ * order per op) come from "Finish RL Training Faster: Bitwise-Consistent,
+ * High-Performance, Agent-Driven", sections "零差异需要一个精确的比较对象" and
+ * "让训练前向使用推理的数值", and from "No More Train-Inference Mismatch:
+ * Bitwise Consistent On-Policy Reinforcement Learning with vLLM and
+ * TorchTitan", section "方法细节".
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or synchronises (except biv_poll_error), and only
+ *    launches kernels on the given stream.  Weights may be updated in place
+ *    between calls (captured graphs keep reading the same addresses).
+ *  - bf16 tensors are passed as uint16_t* (raw bfloat16 payloads); FP8 tensors
+ *    as uint8_t* (OCP E4M3FN codes).  Row-major; *_stride arguments are in
+ *    ELEMENTS between consecutive rows.
+ *  - Pointers used with 16-byte vector or TMA access must be 16-byte aligned
+ *    and row strides must keep rows 16-byte aligned; the host check returns
+ *    BIV_ERR_INVALID otherwise, without launching anything.
+ *  - Zero-sized work (rows == 0, T == 0 ...) returns BIV_OK and launches nothing.
+ *  - On error the status is returned and biv_last_error() describes it.
+ *  - mode BIV_MODE_FAST switches the split-K / split-KV choice to one that
+ *    depends on the batch (the non-invariant comparator); results then change
+ *    with batch size.  BIV_MODE_INVARIANT never lets the batch enter a
+ *    reduction.
+ */
+#ifndef BIV_H
+#define BIV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* biv_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  BIV_OK = 0,
+  BIV_ERR_INVALID = 1,     /* bad argument: nothing was launched */
+  BIV_ERR_UNSUPPORTED = 2, /* valid but not implemented shape/dtype combination */
+  BIV_ERR_WORKSPACE = 3,   /* workspace pointer NULL or smaller than required */
+  BIV_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
+  BIV_ERR_TIMEOUT = 5      /* a device-side wait gave up (see biv_poll_error) */
+} biv_status;
+
+typedef enum { BIV_MODE_INVARIANT = 0, BIV_MODE_FAST = 1 } biv_mode;
+typedef enum { BIV_BF16 = 0, BIV_F32 = 1, BIV_E4M3 = 2 } biv_dtype;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int biv_version(void);
+
+/* Thread-local description of the last error on this thread; never NULL. */
+const char* biv_last_error(void);
+
+/* Number of SMs of the current device (0 if no device). */
+int biv_device_sm_count(void);
+
+/* Reads and clears the device error word that bounded device-side waits set
+ * when they give up.  Synchronises the given stream.  *code receives the word
+ * (0 = no timeout).  Returns BIV_ERR_TIMEOUT when the word was non-zero. */
+biv_status biv_poll_error(biv_stream_t stream, int* code);
+
+/* Test hook for the timeout path: launches one CTA that waits on an mbarrier
+ * nothing will ever arrive on, for at most `limit_ns` nanoseconds, then sets
+ * the device error word and returns.  Never hangs, never traps. */
+biv_status biv_selftest_timeout(uint64_t limit_ns, biv_stream_t stream);
+
+/* ---------------------------------------------------------------- embed --
+ * h[t, :] = table[ids[t], :]   ids int32 [T] (0 <= id < vocab, checked on the
+ * device: an out-of-range id writes a zero row and sets the error word);
+ * table bf16 [vocab, d]; h bf16 [T, d] with row stride h_stride. */
+biv_status biv_embed(const int32_t* ids, const uint16_t* table, int vocab, int T, int d,
+                     uint16_t* h, int64_t h_stride, biv_stream_t stream);
+
+/* ------------------------------------------------------------ RMSNorm ----
+ * Fused residual add + RMSNorm ("No More Train-Inference Mismatch", section
+ * "方法细节": fused RMSNorm with residual).  With residual != NULL:
+ *   r' = bf16(x + r) (written back to residual), y = bf16(r' * inv * w);
+ * with residual == NULL: y = bf16(x * inv * w); inv = 1/sqrt(mean(v^2) + eps)
+ * where v is r' (or x), summed in FP32 in a fixed tree that depends on d
+ * only.  x, residual, y bf16 [rows, d] with their own row strides; w bf16 [d].
+ * d must be a multiple of 8 and <= 8192; y may alias x. */
+biv_status biv_add_rmsnorm(const uint16_t* x, int64_t x_stride, uint16_t* residual,
+                           int64_t r_stride, const uint16_t* w, uint16_t* y, int64_t y_stride,
+                           int rows, int d, float eps, biv_stream_t stream);
+
+/* ------------------------------------------------------------ SiLU-mul ----
+ * y = bf16(silu(g) * u), silu(g) = g / (1 + exp(-g)) in FP32, for
+ * gate_up = [g | u] bf16 [rows, 2I] ("No More Train-Inference Mismatch",
+ * section "方法细节": fused SiLU MLP).  y bf16 [rows, I].  I % 8 == 0. */
+biv_status biv_silu_mul(const uint16_t* gate_up, int64_t gu_stride, uint16_t* y,
+                        int64_t y_stride, int rows, int I, biv_stream_t stream);
+
+/* --------------------------------------------------------- RoPE table ----
+ * cos_sin float32 [2, max_pos, D/2]: cos then sin of pos * theta^(-2i/D),
+ * computed in double precision on the device and rounded to FP32. */
+biv_status biv_rope_table(double theta, int D, int max_pos, float* cos_sin,
+                          biv_stream_t stream);
+
+/* ---------------------------------------------------- QK-norm + RoPE ----
+ * In place on the q and k heads of a packed qkv buffer [T, (Hq+2Hkv)*D]:
+ * q at columns [0, Hq*D), k at [Hq*D, (Hq+Hkv)*D).  For each (token, head):
+ * optional per-head RMSNorm with gain q_w / k_w bf16 [D] (NULL = skip, the
+ * norm output rounded to bf16), then rotate-half RoPE with pairs
+ * (i, i+D/2) at position pos[t] (int32 [T], 0 <= pos < max_pos), FP32
+ * arithmetic, bf16 result.  D in {64, 80, 128}. */
+biv_status biv_qk_norm_rope(uint16_t* qkv, int64_t row_stride, int T, int Hq, int Hkv, int D,
+                            const uint16_t* q_w, const uint16_t* k_w, const float* cos_sin,
+                            int max_pos, const int32_t* pos, float eps, biv_stream_t stream);
+
+/* ------------------------------------------------------- KV cache store --
+ * Paged KV cache, page size `page` tokens: slot s = page_id*page + offset.
+ * k, v rows: bf16 [T, Hkv, D] at k + t*row_stride, v + t*row_stride.
+ * slot int64 [T] (slot < 0 = skip the row).
+ *
+ * biv_kv_store_bf16: k_cache/v_cache bf16 [pages, page, Hkv, D].
+ * biv_kv_fp8_quant ("Finish RL Training Faster", section
+ *   "让训练前向使用推理的数值": the cache stays FP8 and every path makes the same
+ *   round trip): per (token, kv head), separately for K and V,
+ *   s = amax/448 (IEEE division; 1 when amax = 0),
+ *   code = e4m3_rne_satfinite(x / s); codes uint8 [pages, page, Hkv, D],
+ *   scales float32 [pages, page, Hkv]. */
+biv_status biv_kv_store_bf16(const uint16_t* k, const uint16_t* v, int64_t row_stride,
+                             const int64_t* slot, int T, int Hkv, int D, uint16_t* k_cache,
+                             uint16_t* v_cache, biv_stream_t stream);
+biv_status biv_kv_fp8_quant(const uint16_t* k, const uint16_t* v, int64_t row_stride,
+                            const int64_t* slot, int T, int Hkv, int D, uint8_t* k_codes,
+                            uint8_t* v_codes, float* k_scales, float* v_scales,
+                            biv_stream_t stream);
+
+/* Gather + dequantise: for each sequence i, tokens [0, ctx_len[i]) of its
+ * pages (block_table int32 [nseq, max_pages]) are written as
+ * bf16(float(code) * s) to out bf16 [sum ctx, Hkv, D] starting at row
+ * out_row0[i] (int64 [nseq]).  Same formula as the attention loader. */
+biv_status biv_kv_fp8_gather(const uint8_t* codes, const float* scales,
+                             const int32_t* block_table, int max_pages, const int32_t* ctx_len,
+                             const int64_t* out_row0, int nseq, int Hkv, int D, int page,
+                             uint16_t* out, biv_stream_t stream);
+
+/* ----------------------------------------------------------- attention --
+ * One paged GQA attention kernel for prefill, chunked prefill and decode rows
+ * ("Finish RL Training Faster", section "让训练前向使用推理的数值": every path
+ * gathers, dequantises and enters the same attention operator).
+ * Row t (a token of sequence row_seq[t] at absolute position row_pos[t])
+ * attends to keys at positions <= row_pos[t] of its sequence, read from the
+ * paged cache through block_table.  Keys are visited in 64-token tiles aligned
+ * to absolute positions, grouped into splits of kv_split tokens (a model
+ * constant); each split keeps an online softmax (FP32), P is rounded to bf16
+ * for P.V, and the splits are merged in ascending order in FP32.  With
+ * topk_idx != NULL (sparse attention) the keys of row t are the positions
+ * topk_idx[t, 0..topk) (ascending, -1 = none) and splits run over that list.
+ * qblocks int32 [nqblocks, 2] = (first row, row count): rows of a block must
+ * belong to one sequence (sparse: one row per block).  The grouping into
+ * blocks does not change any result bit.  Output bf16 [T, Hq, D]. */
+typedef struct {
+  const uint16_t* q;        /* [T, Hq, D] rows at q + t*q_stride */
+  int64_t q_stride;
+  uint16_t* out;            /* [T, Hq, D] rows at out + t*out_stride */
+  int64_t out_stride;
+  int T, Hq, Hkv, D;        /* D in {64, 80, 128}; Hq % Hkv == 0 */
+  const int32_t* row_seq;   /* [T] */
+  const int32_t* row_pos;   /* [T] */
+  const int32_t* qblocks;   /* [nqblocks, 2] */
+  int nqblocks;
+  int max_rows_per_block;   /* host bound on the row count of any block */
+  int kv_dtype;             /* BIV_BF16 or BIV_E4M3 */
+  const void* k_cache;      /* [pages, page, Hkv, D] bf16 or e4m3 */
+  const void* v_cache;
+  const float* k_scale;     /* [pages, page, Hkv] (E4M3 only) */
+  const float* v_scale;
+  const int32_t* block_table; /* [nseq, max_pages] */
+  int max_pages;
+  int page;                 /* must be 64 */
+  int kv_split;             /* tokens per split, multiple of 64 (INVARIANT: model constant) */
+  int max_ctx;              /* host bound: max over rows of row_pos+1 (dense) */
+  const int32_t* topk_idx;  /* optional [T, topk] */
+  int64_t topk_stride;
+  int topk;
+  float scale;              /* softmax scale, usually 1/sqrt(D) */
+  int mode;                 /* biv_mode; FAST picks kv_split from the batch */
+} biv_attn_desc;
+
+biv_status biv_attention_workspace(const biv_attn_desc* desc, size_t* bytes);
+biv_status biv_attention(const biv_attn_desc* desc, void* workspace, size_t workspace_bytes,
+                         biv_stream_t stream);
+
+/* ---------------------------------------------------------------- GEMM --
+ * C[M, N] = A[M, K] . B[N, K]^T on the tcgen05 tensor cores, FP32
+ * accumulation in TMEM ("Finish RL Training Faster", section
+ * "让训练前向使用推理的数值": one batch-invariant GEMM schedule).  A and B are
+ * K-major (row-major with K contiguous).  INVARIANT mode: each output element
+ * is one ascending pass over K in 64-wide blocks (bf16) or 128-wide blocks
+ * (FP8), never split, whatever M is.
+ *  - bf16 x bf16 -> bf16 or f32 (c_dtype).
+ *  - e4m3 x e4m3 -> bf16 with block scales: per 128-wide K block kb,
+ *    acc += (sa[m,kb]*sb[g][n/128,kb]) * (FP8 products summed over the
+ *    block), promoted to FP32 every block, blocks in ascending order.
+ * Grouped (MoE) when groups > 1: rows [off[g], off[g+1]) of A use weight
+ * group g (B rows g*N .. g*N+N-1, sb + g*ceil(N/128)*ceil(K/128)).
+ * K % 8 == 0 (bf16) / K % 16 == 0 (e4m3); lda, ldb keep rows 16-byte
+ * aligned; ldc keeps rows 16-byte aligned for vector stores. */
+typedef struct {
+  int M, N, K;
+  int a_dtype, b_dtype, c_dtype;
+  const void* A; int64_t lda;
+  const void* B; int64_t ldb;
+  void* C; int64_t ldc;
+  const float* sa; int64_t ld_sa;   /* FP8: [M, ld_sa >= ceil(K/128)] */
+  const float* sb;                  /* FP8: [groups, ceil(N/128), ceil(K/128)] */
+  const int32_t* group_offsets;     /* optional device [groups+1] */
+  int groups;                       /* 0/1 = plain */
+  int mode;                         /* biv_mode */
+} biv_gemm_desc;
+
+biv_status biv_gemm_workspace(const biv_gemm_desc* desc, size_t* bytes);
+biv_status biv_gemm(const biv_gemm_desc* desc, void* workspace, size_t workspace_bytes,
+                    biv_stream_t stream);
+
+/* Per-token activation quantisation for the FP8 GEMM: groups of 128 along K,
+ * s = amax/448 (1 when amax = 0), code = e4m3_rne_satfinite(x/s).
+ * x bf16 [rows, K]; codes uint8 [rows, K] (row stride K); scales float32
+ * [rows, ceil(K/128)].  K % 16 == 0. */
+biv_status biv_act_quant_fp8(const uint16_t* x, int64_t x_stride, int rows, int K,
+                             uint8_t* codes, float* scales, biv_stream_t stream);
+
+/* -------------------------------------------------------------- Top-K ---
+ * Sparse-attention selection ("Finish RL Training Faster", section
+ * "让训练前向使用推理的数值": fixed tie-break and fixed position order): per row
+ * r, among indices j < valid_len[r] with scores[r, j] > -inf, the k largest
+ * scores, equal scores resolved toward the LOWER index; the chosen indices
+ * are written to idx int32 [rows, k] in ASCENDING index order, padded with
+ * -1.  -0.0 and +0.0 compare equal; NaN scores are not allowed.
+ * 0 < k <= n <= 40960, ld >= n. */
+biv_status biv_topk(const float* scores, int64_t ld, const int32_t* valid_len, int rows, int n,
+                    int k, int32_t* idx, biv_stream_t stream);
+
+/* MoE router: per row, the k largest of E logits (ties -> lower expert id),
+ * written in rank order (logit descending, id ascending) to idx int32
+ * [rows, k]; w float32 [rows, k] = softmax probability of each chosen expert
+ * over all E (not renormalised).  E <= 1024, k <= 32. */
+biv_status biv_router_topk(const float* logits, int64_t ld, int rows, int E, int k, int32_t* idx,
+                           float* w, biv_stream_t stream);
+
+/* Deterministic dispatch: experts idx int32 [T, k] -> offsets int32 [E+1]
+ * (rows of expert e = [offsets[e], offsets[e+1])) and perm int32 [T*k]
+ * (entry t*k+s of expert e placed at offsets[e] + rank of (t, s) among that
+ * expert's entries in ascending (t, s) order); src_row int32 [T, k] is the
+ * inverse (row of entry (t, s) in the grouped layout).  T*k <= 1<<20. */
+biv_status biv_moe_dispatch(const int32_t* idx, int T, int k, int E, int32_t* offsets,
+                            int32_t* perm, int32_t* src_row, biv_stream_t stream);
+
+/* Row gather for grouped GEMM inputs: dst[i, :] = src[perm[i] / k_div, :] for
+ * byte rows of `row_bytes` (multiple of 16), i < n. */
+biv_status biv_gather_rows(const void* src, int64_t src_stride_bytes, const int32_t* perm,
+                           int k_div, int n, int row_bytes, void* dst, int64_t dst_stride_bytes,
+                           biv_stream_t stream);
+
+/* FP32 fixed-slot combine ("Finish RL Training Faster", section
+ * "让训练前向使用推理的数值": expert outputs merged in FP32 in slot order):
+ * out[t] = bf16( sum_{s=0..k-1, in order} w[t,s]*float(y_row(t,s)) + float(shared[t]) )
+ * with y_row(t,s) = y[src_row[t*k+s]] when src_row != NULL, else y[t*k+s];
+ * y bf16 [*, d], shared bf16 [T, d] or NULL, out bf16 [T, d]. */
+biv_status biv_moe_combine(const uint16_t* y, const int32_t* src_row, const float* w,
+                           const uint16_t* shared, uint16_t* out, int T, int k, int d,
+                           biv_stream_t stream);
+
+/* ------------------------------------------------------------ log-prob --
+ * lp[t] = z[t, target[t]] - (m + log sum_v exp(z[t, v] - m)), m = max_v z,
+ * in FP32 with a reduction order that depends on V only (the logprob of
+ * every sampled token, "Finish RL Training Faster", section
+ * "零差异需要一个精确的比较对象").  logits float32 [T, V] rows at ld. */
+biv_status biv_logprob(const float* logits, int64_t ld, const int32_t* target, int T, int V,
+                       float* lp, biv_stream_t stream);
+
+/* ------------------------------------------------------------- SSD scan --
+ * Mamba-2 SSD over chunks of `chunk` positions aligned to absolute positions
+ * ("Finish RL Training Faster", section "一致性有多个层面": decode replays the
+ * prefill chunk order).  For each sequence i, rows [row0[i], row0[i]+n[i])
+ * of x/dt/B/C are its next n[i] tokens, starting at absolute position pos0[i].
+ * Per sequence the library keeps, in caller memory:
+ *   state  float32 [nseq, H, P, N]: the state at the start of the open chunk;
+ *   buf_x  bf16 [nseq, chunk, H, P], buf_B/buf_C bf16 [nseq, chunk, N],
+ *   buf_dt float32 [nseq, chunk, H]: the open chunk's rows so far.
+ * Every output row y_t is computed from its chunk's start state and the
+ * chunk's rows <= t with one code path, so prefill, chunked prefill and
+ * token-by-token decode give the same bits.  When a chunk closes its end
+ * state replaces `state`.  Set state to zero for a new sequence (pos0 = 0).
+ * H*P, N: P in {64}, N in {128}; chunk in {64, 128, 256}. */
+typedef struct {
+  const uint16_t* x; int64_t x_stride;   /* [rows, H, P] */
+  const float* dt;   int64_t dt_stride;  /* [rows, H] (after softplus) */
+  const float* A;                        /* [H], negative */
+  const uint16_t* B; int64_t B_stride;   /* [rows, N] */
+  const uint16_t* C; int64_t C_stride;   /* [rows, N] */
+  const float* D;                        /* [H] */
+  uint16_t* y; int64_t y_stride;         /* [rows, H, P] */
+  int H, P, N, chunk;
+  int nseq;
+  const int32_t* row0;                   /* [nseq] */
+  const int32_t* n;                      /* [nseq] */
+  const int32_t* pos0;                   /* [nseq] */
+  int max_n;                             /* host bound on n[i] */
+  float* state;
+  uint16_t* buf_x;
+  uint16_t* buf_B;
+  uint16_t* buf_C;
+  float* buf_dt;
+} biv_ssd_desc;
+
+biv_status biv_ssd_scan(const biv_ssd_desc* desc, biv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BIV_H */

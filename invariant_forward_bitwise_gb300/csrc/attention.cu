@@ -1,0 +1,517 @@
+// One paged attention operator for prefill, chunked prefill, decode and
+// trainer recompute ("Finish RL Training Faster", section "让训练前向使用推理的数值":
+// every path gathers, dequantises and enters the same attention operator).
+//
+// A CTA handles one query block (rows of one sequence), one KV head and one
+// KV split.  Its 64 query vectors are (row, q-head-of-the-group) pairs, 16 per
+// warp.  Keys are visited in 64-token tiles aligned to absolute positions (one
+// cache page), inside splits of kv_split tokens.  Per vector and split:
+// online softmax in FP32 (exp2 domain), P rounded to bf16 for P.V, the
+// denominator summed from the same rounded P.  Splits are merged in ascending
+// order.  A vector's arithmetic is the same whatever other rows share its CTA:
+// tiles past its own position are fully masked and leave (m, l, acc) bitwise
+// unchanged, and masked slots are zero in shared memory.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace biv {
+namespace {
+
+constexpr int kTile = 64;   // keys per tile = one page
+constexpr int kNV = 64;     // query vectors per CTA (4 warps x 16)
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct AttnCfg {
+  static constexpr int LD = D + 8;                   // padded smem row (elements)
+  static constexpr int Q_BYTES = kNV * LD * 2;
+  static constexpr int KV_BYTES = kTile * LD * 2;
+  static constexpr int SMEM = Q_BYTES + 4 * KV_BYTES + kTile * 4 * 2;
+  static constexpr int DK = D / 16;                  // k-steps of Q.K^T
+  static constexpr int DT = D / 8;                   // n-tiles of O
+};
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+struct AttnArgs {
+  const uint16_t* q; int64_t q_stride;
+  uint16_t* out; int64_t out_stride;
+  int T, Hq, Hkv, G;
+  const int32_t* row_seq; const int32_t* row_pos;
+  const int32_t* qblocks;
+  int fp8;
+  const void* kc; const void* vc;
+  const float* ks; const float* vs;
+  const int32_t* bt; int max_pages;
+  int kv_split;
+  const int32_t* topk_idx; int64_t topk_stride; int topk;
+  float scale_log2;
+  float* ws_o; float* ws_ml; int nsplit_grid;
+  int* err;
+};
+
+// Number of splits that hold keys of a row (fixed per row).
+__device__ __forceinline__ int row_splits(const AttnArgs& a, int pos) {
+  return a.topk_idx ? (a.topk + a.kv_split - 1) / a.kv_split : pos / a.kv_split + 1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
+  using Cfg = AttnCfg<D>;
+  constexpr int LD = Cfg::LD;
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* sQ = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* sK = reinterpret_cast<uint16_t*>(smem + Cfg::Q_BYTES);          // [2][64][LD]
+  uint16_t* sV = sK + 2 * kTile * LD;                                        // [2][64][LD]
+  int32_t* sPos = reinterpret_cast<int32_t*>(sV + 2 * kTile * LD);          // [2][64]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int blk = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
+  const int r0 = a.qblocks[2 * blk], nr = a.qblocks[2 * blk + 1];
+  const int nv = nr * a.G;
+  const int seq = a.row_seq[r0];
+  const bool sparse = a.topk_idx != nullptr;
+
+  // block's largest position (rows of a block are one sequence)
+  int maxpos = -1;
+  for (int r = 0; r < nr; ++r) maxpos = max(maxpos, a.row_pos[r0 + r]);
+
+  // key range of this split
+  int lo, hi;  // [lo, hi) in positions (dense) or list indices (sparse)
+  if (sparse) {
+    lo = split * a.kv_split;
+    hi = min(a.topk, lo + a.kv_split);
+  } else {
+    lo = split * a.kv_split;
+    hi = min(maxpos + 1, lo + a.kv_split);
+  }
+  if (lo >= hi) return;  // uniform: nothing of this block lives in this split
+  const int ntiles = (hi - lo + kTile - 1) / kTile;
+
+  // ---- load Q (zero for vectors past nv)
+  {
+    constexpr int CPR = D / 8;  // 16-byte chunks per vector
+    for (int i = tid; i < kNV * CPR; i += 128) {
+      const int v = i / CPR, c = i % CPR;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (v < nv) {
+        const int r = v / a.G, j = v % a.G;
+        const uint16_t* src = a.q + int64_t(r0 + r) * a.q_stride + int64_t(h * a.G + j) * D;
+        val = reinterpret_cast<const uint4*>(src)[c];
+      }
+      *reinterpret_cast<uint4*>(sQ + v * LD + c * 8) = val;
+    }
+  }
+
+  // ---- tile loader (dense: the page of absolute tile t; sparse: listed keys)
+  const int64_t kv_row = int64_t(a.Hkv) * D;  // elements between consecutive cache slots
+  auto load_tile = [&](int buf, int t) {
+    const int base = lo + t * kTile;
+    int32_t* pos_buf = sPos + buf * kTile;
+    if (tid < kTile) {
+      int p;
+      if (sparse) {
+        const int li = base + tid;
+        p = li < hi ? a.topk_idx[int64_t(r0) * a.topk_stride + li] : -1;
+      } else {
+        p = base + tid;
+        if (p >= hi) p = -1;
+      }
+      pos_buf[tid] = p;
+    }
+    __syncthreads();
+    uint16_t* dK = sK + buf * kTile * LD;
+    uint16_t* dV = sV + buf * kTile * LD;
+    if (!a.fp8) {
+      constexpr int CPR = D / 8;
+      for (int i = tid; i < kTile * CPR * 2; i += 128) {
+        const int which = i / (kTile * CPR);
+        const int rem = i % (kTile * CPR);
+        const int j = rem / CPR, c = rem % CPR;
+        const int p = pos_buf[j];
+        const uint16_t* src = static_cast<const uint16_t*>(which ? a.vc : a.kc);
+        const uint16_t* gp = src;
+        if (p >= 0) {
+          const int64_t slot = int64_t(a.bt[int64_t(seq) * a.max_pages + p / kTile]) * kTile + p % kTile;
+          gp = src + slot * kv_row + int64_t(h) * D + c * 8;
+        }
+        cp_async16(smem_u32((which ? dV : dK) + j * LD + c * 8), gp, p >= 0);
+      }
+    } else {
+      constexpr int CPR = D / 16;  // 16 codes per chunk
+      for (int i = tid; i < kTile * CPR * 2; i += 128) {
+        const int which = i / (kTile * CPR);
+        const int rem = i % (kTile * CPR);
+        const int j = rem / CPR, c = rem % CPR;
+        const int p = pos_buf[j];
+        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+        if (p >= 0) {
+          const int64_t slot = int64_t(a.bt[int64_t(seq) * a.max_pages + p / kTile]) * kTile + p % kTile;
+          const uint8_t* codes = static_cast<const uint8_t*>(which ? a.vc : a.kc) + slot * kv_row + int64_t(h) * D;
+          const float sc = (which ? a.vs : a.ks)[slot * a.Hkv + h];
+          const uint4 cv = reinterpret_cast<const uint4*>(codes)[c];
+          const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
+          uint32_t packed[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float f0 = e4m32f(uint8_t(w[q] & 0xFF)) * sc;
+            const float f1 = e4m32f(uint8_t((w[q] >> 8) & 0xFF)) * sc;
+            const float f2 = e4m32f(uint8_t((w[q] >> 16) & 0xFF)) * sc;
+            const float f3 = e4m32f(uint8_t(w[q] >> 24)) * sc;
+            packed[2 * q] = pack_bf2(f0, f1);
+            packed[2 * q + 1] = pack_bf2(f2, f3);
+          }
+          o0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          o1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        }
+        uint16_t* dst = (which ? dV : dK) + j * LD + c * 16;
+        reinterpret_cast<uint4*>(dst)[0] = o0;
+        reinterpret_cast<uint4*>(dst)[1] = o1;
+      }
+    }
+  };
+
+  // per-thread rows: g and g+8 of this warp's 16 vectors
+  const int g = lane >> 2, cq = lane & 3;
+  int vpos[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int v = warp * 16 + g + 8 * i;
+    vpos[i] = v < nv ? a.row_pos[r0 + v / a.G] : -1;
+  }
+
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float acc[Cfg::DT][4];
+#pragma unroll
+  for (int i = 0; i < Cfg::DT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+  load_tile(0, 0);
+  cp_async_commit();
+  __syncthreads();
+
+  // Q fragments (A operand), loaded once
+  uint32_t qf[Cfg::DK][4];
+  {
+    const uint32_t qbase = smem_u32(sQ + (warp * 16 + (lane & 15)) * LD + (lane >> 4) * 8);
+#pragma unroll
+    for (int kk = 0; kk < Cfg::DK; ++kk)
+      ldsm_x4(qbase + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+  }
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int buf = t & 1;
+    if (t + 1 < ntiles) {
+      load_tile(buf ^ 1, t + 1);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const uint16_t* tK = sK + buf * kTile * LD;
+    const uint16_t* tV = sV + buf * kTile * LD;
+    const int32_t* tP = sPos + buf * kTile;
+    if (warp * 16 >= nv) {  // no live vector in this warp: only help with loads
+      __syncthreads();
+      continue;
+    }
+
+    // S = Q . K^T  (16 x 64 per warp)
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < Cfg::DK; ++kk) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t b0, b1, b2, b3;
+        const int key = np * 16 + (lane & 7) + (lane >> 4) * 8;
+        const int dim = kk * 16 + ((lane >> 3) & 1) * 8;
+        ldsm_x4(smem_u32(tK + key * LD + dim), b0, b1, b2, b3);
+        mma_bf16(s[2 * np], qf[kk], b0, b1);
+        mma_bf16(s[2 * np + 1], qf[kk], b2, b3);
+      }
+    }
+    // mask, online softmax
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = e >> 1;
+        const int kp = tP[nt * 8 + 2 * cq + (e & 1)];
+        const bool vis = kp >= 0 && kp <= vpos[i];
+        const float x = vis ? s[nt][e] * a.scale_log2 : -INFINITY;
+        s[nt][e] = x;
+        mx[i] = fmaxf(mx[i], x);
+      }
+    }
+    float alpha[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+      const float mn = fmaxf(m[i], mx[i]);
+      alpha[i] = (mn == -INFINITY) ? 1.f : exp2f(m[i] - mn);
+      m[i] = mn;
+    }
+    uint32_t pf[4][4];  // P as bf16 A fragments, 4 k-steps of 16 keys
+    float rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = e >> 1;
+        const float pe = (m[i] == -INFINITY) ? 0.f : exp2f(s[nt][e] - m[i]);
+        p[e] = bf2f(f2bf(pe));
+        rs[i] += p[e];
+      }
+      const int ks = nt >> 1, hi2 = nt & 1;
+      pf[ks][hi2 * 2 + 0] = pack_bf2(p[0], p[1]);
+      pf[ks][hi2 * 2 + 1] = pack_bf2(p[2], p[3]);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
+      rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
+      l[i] = l[i] * alpha[i] + rs[i];
+    }
+#pragma unroll
+    for (int dt = 0; dt < Cfg::DT; ++dt) {
+      acc[dt][0] *= alpha[0];
+      acc[dt][1] *= alpha[0];
+      acc[dt][2] *= alpha[1];
+      acc[dt][3] *= alpha[1];
+    }
+    // O += P . V
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      // A fragment order: (row g, k 0-7), (row g+8, k 0-7), (row g, k 8-15), (row g+8, k 8-15)
+      const uint32_t af[4] = {pf[ks][0], pf[ks][1], pf[ks][2], pf[ks][3]};
+#pragma unroll
+      for (int dp = 0; dp < Cfg::DT / 2; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        const int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int dim = dp * 16 + (lane >> 4) * 8;
+        ldsm_x4_t(smem_u32(tV + key * LD + dim), b0, b1, b2, b3);
+        mma_bf16(acc[2 * dp], af, b0, b1);
+        mma_bf16(acc[2 * dp + 1], af, b2, b3);
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- epilogue: single-split rows write the final output, others partials
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int v = warp * 16 + g + 8 * i;
+    if (v >= nv) continue;
+    const int row = r0 + v / a.G;
+    const int head = h * a.G + v % a.G;
+    const int ns = row_splits(a, vpos[i]);
+    if (split >= ns) continue;
+    if (ns == 1) {
+      const float inv_l = l[i] > 0.f ? 1.0f / l[i] : 0.f;
+      uint16_t* dst = a.out + int64_t(row) * a.out_stride + int64_t(head) * D;
+#pragma unroll
+      for (int dt = 0; dt < Cfg::DT; ++dt) {
+        const float o0 = acc[dt][2 * i] * inv_l + 0.0f;
+        const float o1 = acc[dt][2 * i + 1] * inv_l + 0.0f;
+        *reinterpret_cast<uint32_t*>(dst + dt * 8 + 2 * cq) = pack_bf2(o0, o1);
+      }
+    } else {
+      const int64_t slot = (int64_t(row) * a.Hq + head) * a.nsplit_grid + split;
+      float* wo = a.ws_o + slot * D;
+#pragma unroll
+      for (int dt = 0; dt < Cfg::DT; ++dt)
+        *reinterpret_cast<float2*>(wo + dt * 8 + 2 * cq) = make_float2(acc[dt][2 * i], acc[dt][2 * i + 1]);
+      if (cq == 0) {
+        a.ws_ml[2 * slot] = m[i];
+        a.ws_ml[2 * slot + 1] = l[i];
+      }
+    }
+  }
+}
+
+// Merge the splits of rows that have more than one, in ascending split order:
+// w_s = 2^(m_s - M), O = sum w_s o_s, L = sum w_s l_s, out = O / L.
+template <int D>
+__global__ void attn_merge_kernel(const AttnArgs a) {
+  const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= int64_t(a.T) * a.Hq) return;
+  const int row = int(gw / a.Hq), head = int(gw % a.Hq);
+  const int ns = row_splits(a, a.row_pos[row]);
+  if (ns <= 1) return;
+  const int64_t base = (int64_t(row) * a.Hq + head) * a.nsplit_grid;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, a.ws_ml[2 * (base + s)]);
+  constexpr int PER = (D + 31) / 32;
+  float O[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) O[j] = 0.f;
+  float L = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float ms = a.ws_ml[2 * (base + s)];
+    if (ms == -INFINITY) continue;
+    const float w = exp2f(ms - M);
+    L += w * a.ws_ml[2 * (base + s) + 1];
+    const float* o = a.ws_o + (base + s) * D;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int d = lane + 32 * j;
+      if (d < D) O[j] += w * o[d];
+    }
+  }
+  uint16_t* dst = a.out + int64_t(row) * a.out_stride + int64_t(head) * D;
+  const float inv = L > 0.f ? 1.0f / L : 0.f;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int d = lane + 32 * j;
+    if (d < D) dst[d] = f2bf(O[j] * inv + 0.0f);
+  }
+}
+
+int plan_split(const biv_attn_desc& d) {
+  if (d.mode != BIV_MODE_FAST) return d.kv_split;
+  // FAST: choose the split from the batch so that the grid fills the GPU
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  const int span = d.topk_idx ? d.topk : d.max_ctx;
+  const int64_t ctas = int64_t(d.nqblocks) * d.Hkv;
+  int split = span;
+  while (split > 256 && ctas * ((span + split - 1) / split) < 2 * sms) split /= 2;
+  return std::max(64, (split + 63) / 64 * 64);
+}
+
+biv_status validate(const biv_attn_desc* d) {
+  BIV_REQUIRE(d, "attention: null descriptor");
+  BIV_REQUIRE(d->D == 64 || d->D == 80 || d->D == 128, "attention: D=%d unsupported", d->D);
+  BIV_REQUIRE(d->T >= 0 && d->Hq > 0 && d->Hkv > 0 && d->Hq % d->Hkv == 0, "attention: bad heads");
+  const int G = d->Hq / d->Hkv;
+  BIV_REQUIRE(G <= kNV, "attention: q heads per kv head above %d", kNV);
+  BIV_REQUIRE(d->page == kTile, "attention: page size must be %d", kTile);
+  BIV_REQUIRE(d->kv_split >= kTile && d->kv_split % kTile == 0, "attention: kv_split must be a multiple of 64");
+  BIV_REQUIRE(d->kv_dtype == BIV_BF16 || d->kv_dtype == BIV_E4M3, "attention: kv dtype");
+  BIV_REQUIRE(d->kv_dtype == BIV_BF16 || (d->k_scale && d->v_scale), "attention: FP8 needs scales");
+  BIV_REQUIRE(d->max_rows_per_block >= 1 && d->max_rows_per_block * G <= kNV,
+              "attention: max_rows_per_block * (Hq/Hkv) must be <= %d", kNV);
+  BIV_REQUIRE(!d->topk_idx || (d->max_rows_per_block == 1 && d->topk > 0),
+              "attention: sparse mode takes one row per block");
+  BIV_REQUIRE(d->topk_idx || d->max_ctx >= 1, "attention: max_ctx >= 1 required");
+  BIV_REQUIRE(d->nqblocks >= 0 && d->nqblocks <= 0x7fffffff, "attention: bad nqblocks");
+  BIV_REQUIRE(d->mode == BIV_MODE_INVARIANT || d->mode == BIV_MODE_FAST, "attention: bad mode");
+  return BIV_OK;
+}
+
+size_t ws_bytes(const biv_attn_desc& d, int split) {
+  const int span = d.topk_idx ? d.topk : d.max_ctx;
+  const int64_t ns = (span + split - 1) / split;
+  if (ns <= 1) return 0;
+  return size_t(d.T) * d.Hq * ns * (d.D + 2) * sizeof(float);
+}
+
+template <int D>
+biv_status launch(const biv_attn_desc& d, const AttnArgs& a, cudaStream_t s) {
+  using Cfg = AttnCfg<D>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM) != cudaSuccess)
+      return set_error(BIV_ERR_CUDA, "attention: cannot set shared memory size");
+    attr = true;
+  }
+  dim3 grid(d.nqblocks, d.Hkv, a.nsplit_grid);
+  attn_kernel<D><<<grid, 128, Cfg::SMEM, s>>>(a);
+  biv_status st = check_launch("attention");
+  if (st != BIV_OK || a.nsplit_grid <= 1) return st;
+  const int64_t warps = int64_t(d.T) * d.Hq;
+  attn_merge_kernel<D><<<unsigned((warps * 32 + 255) / 256), 256, 0, s>>>(a);
+  return check_launch("attention_merge");
+}
+
+}  // namespace
+}  // namespace biv
+
+using namespace biv;
+
+extern "C" {
+
+biv_status biv_attention_workspace(const biv_attn_desc* d, size_t* bytes) {
+  biv_status st = validate(d);
+  if (st != BIV_OK) return st;
+  BIV_REQUIRE(bytes, "attention_workspace: null output");
+  *bytes = ws_bytes(*d, plan_split(*d));
+  return BIV_OK;
+}
+
+biv_status biv_attention(const biv_attn_desc* d, void* ws, size_t wsb, biv_stream_t stream) {
+  biv_status st = validate(d);
+  if (st != BIV_OK) return st;
+  if (d->T == 0 || d->nqblocks == 0) return BIV_OK;
+  BIV_REQUIRE(d->q && d->out && d->row_seq && d->row_pos && d->qblocks && d->k_cache &&
+                  d->v_cache && d->block_table,
+              "attention: null pointer");
+  BIV_REQUIRE(aligned16(d->q) && aligned16(d->out) && (d->q_stride * 2) % 16 == 0 &&
+                  (d->out_stride * 2) % 16 == 0 && aligned16(d->k_cache) && aligned16(d->v_cache),
+              "attention: q/out/cache must keep rows 16-byte aligned");
+  const int split = plan_split(*d);
+  const size_t need = ws_bytes(*d, split);
+  if (need && (!ws || wsb < need))
+    return set_error(BIV_ERR_WORKSPACE, "attention: workspace of %zu bytes needed", need);
+  const int span = d->topk_idx ? d->topk : d->max_ctx;
+  AttnArgs a;
+  a.q = d->q; a.q_stride = d->q_stride;
+  a.out = d->out; a.out_stride = d->out_stride;
+  a.T = d->T; a.Hq = d->Hq; a.Hkv = d->Hkv; a.G = d->Hq / d->Hkv;
+  a.row_seq = d->row_seq; a.row_pos = d->row_pos; a.qblocks = d->qblocks;
+  a.fp8 = d->kv_dtype == BIV_E4M3;
+  a.kc = d->k_cache; a.vc = d->v_cache; a.ks = d->k_scale; a.vs = d->v_scale;
+  a.bt = d->block_table; a.max_pages = d->max_pages;
+  a.kv_split = split;
+  a.topk_idx = d->topk_idx; a.topk_stride = d->topk_stride; a.topk = d->topk;
+  a.scale_log2 = d->scale * kLog2e;
+  a.nsplit_grid = (span + split - 1) / split;
+  a.ws_o = static_cast<float*>(ws);
+  a.ws_ml = a.ws_o ? a.ws_o + size_t(d->T) * d->Hq * a.nsplit_grid * d->D : nullptr;
+  a.err = device_error_word();
+  BIV_REQUIRE(a.nsplit_grid <= 65535, "attention: too many splits");
+  cudaStream_t s = as_cuda(stream);
+  switch (d->D) {
+    case 64: return launch<64>(*d, a, s);
+    case 80: return launch<80>(*d, a, s);
+    default: return launch<128>(*d, a, s);
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,695 @@
+// Row-wise memory-bound kernels of the invariant forward.  Each output row is
+// computed by one fixed thread/warp arrangement that depends only on the row
+// length (never on the number of rows), with reductions in a fixed tree, so a
+// row's bits do not depend on the batch it is in.
+#include "common.cuh"
+
+namespace biv {
+
+namespace {
+
+constexpr int kNormThreads = 256;  // fixed: the RMSNorm tree depends on d only
+constexpr int kLogprobThreads = 512;
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]),
+                    pack_bf2(f[6], f[7]));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ------------------------------------------------------------------ embed --
+__global__ void embed_kernel(const int32_t* __restrict__ ids, const uint16_t* __restrict__ table,
+                             int vocab, int d, uint16_t* __restrict__ h, int64_t h_stride,
+                             int* err) {
+  const int t = blockIdx.x;
+  const int id = ids[t];
+  uint4* dst = reinterpret_cast<uint4*>(h + int64_t(t) * h_stride);
+  const int chunks = d / 8;
+  if (id < 0 || id >= vocab) {
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) raise_error(err, kErrBadIndex);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(table + int64_t(id) * d);
+  for (int c = threadIdx.x; c < chunks; c += blockDim.x) dst[c] = __ldg(src + c);
+}
+
+// ------------------------------------------------------- add + RMSNorm ----
+// One CTA of kNormThreads per row.  Thread t owns 8-element chunks
+// t, t+256, ...; sum of squares: per-thread in chunk order, warp xor tree,
+// then the 8 warp sums added in warp order.
+template <int CPT>  // chunks per thread (ceil(d/8/256))
+__global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
+    const uint16_t* __restrict__ x, int64_t xs, uint16_t* __restrict__ r, int64_t rs,
+    const uint16_t* __restrict__ w, uint16_t* __restrict__ y, int64_t ys, int d, float eps) {
+  __shared__ float warp_ss[kNormThreads / 32];
+  const int row = blockIdx.x;
+  const int chunks = d / 8;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + int64_t(row) * xs);
+  uint4* rr = r ? reinterpret_cast<uint4*>(r + int64_t(row) * rs) : nullptr;
+  float v[CPT][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < CPT; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    if (c < chunks) {
+      unpack8(xr[c], v[i]);
+      if (rr) {
+        float rv[8];
+        unpack8(rr[c], rv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[i][j] = bf2f(f2bf(v[i][j] + rv[j]));
+        rr[c] = pack8(v[i]);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(v[i][j], v[i][j], ss);
+    }
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) warp_ss[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) tot += warp_ss[i];
+  const float inv = 1.0f / sqrtf(tot / float(d) + eps);
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  uint4* yr = reinterpret_cast<uint4*>(y + int64_t(row) * ys);
+#pragma unroll
+  for (int i = 0; i < CPT; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    if (c < chunks) {
+      float wv[8], o[8];
+      unpack8(__ldg(wr + c), wv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[j] = (v[i][j] * inv) * wv[j];
+      yr[c] = pack8(o);
+    }
+  }
+}
+
+// ------------------------------------------------------------- SiLU-mul ----
+__global__ void silu_mul_kernel(const uint16_t* __restrict__ gu, int64_t gs,
+                                uint16_t* __restrict__ y, int64_t ys, int rows, int I) {
+  const int cpr = I / 8;
+  const int64_t total = int64_t(rows) * cpr;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int row = int(i / cpr), c = int(i % cpr);
+    const uint4* g = reinterpret_cast<const uint4*>(gu + int64_t(row) * gs);
+    float gv[8], uv[8], o[8];
+    unpack8(g[c], gv);
+    unpack8(g[cpr + c], uv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = (gv[j] / (1.0f + expf(-gv[j]))) * uv[j];
+    reinterpret_cast<uint4*>(y + int64_t(row) * ys)[c] = pack8(o);
+  }
+}
+
+// ------------------------------------------------------------ RoPE table --
+__global__ void rope_table_kernel(double theta, int D, int max_pos, float* cos_sin) {
+  const int half = D / 2;
+  const int64_t n = int64_t(max_pos) * half;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int p = int(i / half), j = int(i % half);
+    const double inv_freq = pow(theta, -(2.0 * j) / double(D));
+    const double ang = double(p) * inv_freq;
+    cos_sin[i] = float(cos(ang));
+    cos_sin[n + i] = float(sin(ang));
+  }
+}
+
+// ------------------------------------------------------- QK-norm + RoPE ----
+// One warp per (token, head).  Lane l owns the rotation pairs p = l, l+32
+// (p < D/2) holding elements p and p + D/2.
+__global__ void qk_norm_rope_kernel(uint16_t* __restrict__ qkv, int64_t rs, int T, int Hq,
+                                    int Hkv, int D, const uint16_t* __restrict__ qw,
+                                    const uint16_t* __restrict__ kw,
+                                    const float* __restrict__ cos_sin, int max_pos,
+                                    const int32_t* __restrict__ pos, float eps, int* err) {
+  const int heads = Hq + Hkv;
+  const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= int64_t(T) * heads) return;
+  const int t = int(gw / heads), h = int(gw % heads);
+  const bool is_q = h < Hq;
+  const uint16_t* wn = is_q ? qw : kw;
+  uint16_t* v = qkv + int64_t(t) * rs + int64_t(h) * D;
+  const int half = D / 2;
+  int p = pos[t];
+  if (p < 0 || p >= max_pos) {
+    if (lane == 0) raise_error(err, kErrBadIndex);
+    p = 0;
+  }
+  float a[2], b[2];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int j = lane + 32 * i;
+    a[i] = b[i] = 0.f;
+    if (j < half) {
+      a[i] = bf2f(v[j]);
+      b[i] = bf2f(v[j + half]);
+      ss = fmaf(a[i], a[i], ss);
+      ss = fmaf(b[i], b[i], ss);
+    }
+  }
+  if (wn) {
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / float(D) + eps);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int j = lane + 32 * i;
+      if (j < half) {
+        a[i] = bf2f(f2bf((a[i] * inv) * bf2f(wn[j])));
+        b[i] = bf2f(f2bf((b[i] * inv) * bf2f(wn[j + half])));
+      }
+    }
+  }
+  const int64_t n = int64_t(max_pos) * half;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int j = lane + 32 * i;
+    if (j < half) {
+      const float c = cos_sin[int64_t(p) * half + j];
+      const float s = cos_sin[n + int64_t(p) * half + j];
+      v[j] = f2bf(a[i] * c - b[i] * s);
+      v[j + half] = f2bf(b[i] * c + a[i] * s);
+    }
+  }
+}
+
+// --------------------------------------------------------------- KV store --
+__global__ void kv_store_bf16_kernel(const uint16_t* __restrict__ k,
+                                     const uint16_t* __restrict__ v, int64_t rs,
+                                     const int64_t* __restrict__ slot, int T, int Hkv, int D,
+                                     uint16_t* __restrict__ kc, uint16_t* __restrict__ vc) {
+  const int cpv = D / 8;  // 16-byte chunks per head vector
+  const int64_t total = int64_t(T) * Hkv * cpv * 2;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    int64_t r = i;
+    const int c = int(r % cpv); r /= cpv;
+    const int h = int(r % Hkv); r /= Hkv;
+    const int which = int(r % 2); r /= 2;
+    const int t = int(r);
+    const int64_t s = slot[t];
+    if (s < 0) continue;
+    const uint16_t* src = (which ? v : k) + int64_t(t) * rs + int64_t(h) * D;
+    uint16_t* dst = (which ? vc : kc) + (s * Hkv + h) * D;
+    reinterpret_cast<uint4*>(dst)[c] = reinterpret_cast<const uint4*>(src)[c];
+  }
+}
+
+// One warp per (token, kv head, K|V): amax, scale, codes.
+__global__ void kv_fp8_quant_kernel(const uint16_t* __restrict__ k,
+                                    const uint16_t* __restrict__ v, int64_t rs,
+                                    const int64_t* __restrict__ slot, int T, int Hkv, int D,
+                                    uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
+                                    float* __restrict__ ks, float* __restrict__ vs) {
+  const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= int64_t(T) * Hkv * 2) return;
+  const int which = int(gw % 2);
+  const int h = int((gw / 2) % Hkv);
+  const int t = int(gw / 2 / Hkv);
+  const int64_t s = slot[t];
+  if (s < 0) return;
+  const uint16_t* src = (which ? v : k) + int64_t(t) * rs + int64_t(h) * D;
+  float x[4];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = lane + 32 * i;
+    x[i] = j < D ? bf2f(src[j]) : 0.f;
+    amax = fmaxf(amax, fabsf(x[i]));
+  }
+  amax = warp_max(amax);
+  const float sc = amax == 0.f ? 1.0f : amax / 448.0f;
+  uint8_t* dst = (which ? vc : kc) + (s * Hkv + h) * D;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = lane + 32 * i;
+    if (j < D) dst[j] = f2e4m3(x[i] / sc);
+  }
+  if (lane == 0) (which ? vs : ks)[s * Hkv + h] = sc;
+}
+
+__global__ void kv_fp8_gather_kernel(const uint8_t* __restrict__ codes,
+                                     const float* __restrict__ scales,
+                                     const int32_t* __restrict__ bt, int max_pages,
+                                     const int32_t* __restrict__ ctx,
+                                     const int64_t* __restrict__ row0, int Hkv, int D, int page,
+                                     uint16_t* __restrict__ out) {
+  const int i = blockIdx.y;
+  const int n = ctx[i];
+  const int per_tok = Hkv * D;
+  for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < int64_t(n) * per_tok;
+       e += int64_t(gridDim.x) * blockDim.x) {
+    const int t = int(e / per_tok);
+    const int hd = int(e % per_tok);
+    const int64_t s = int64_t(bt[int64_t(i) * max_pages + t / page]) * page + t % page;
+    const float sc = scales[s * Hkv + hd / D];
+    out[(row0[i] + t) * per_tok + hd] = f2bf(e4m32f(codes[s * per_tok + hd]) * sc);
+  }
+}
+
+// ---------------------------------------------------- activation quant ----
+// One warp per (row, 128-wide group).
+__global__ void act_quant_kernel(const uint16_t* __restrict__ x, int64_t xs, int rows, int K,
+                                 uint8_t* __restrict__ codes, float* __restrict__ scales) {
+  const int groups = (K + 127) / 128;
+  const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= int64_t(rows) * groups) return;
+  const int row = int(gw / groups), g = int(gw % groups);
+  const uint16_t* src = x + int64_t(row) * xs + g * 128;
+  float v[4];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = lane * 4 + i;
+    v[i] = (g * 128 + j < K) ? bf2f(src[j]) : 0.f;
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = warp_max(amax);
+  const float sc = amax == 0.f ? 1.0f : amax / 448.0f;
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) packed |= uint32_t(f2e4m3(v[i] / sc)) << (8 * i);
+  uint8_t* dst = codes + int64_t(row) * K + g * 128 + lane * 4;
+  if (g * 128 + lane * 4 + 4 <= K) {
+    *reinterpret_cast<uint32_t*>(dst) = packed;
+  } else {
+    for (int i = 0; i < 4; ++i)
+      if (g * 128 + lane * 4 + i < K) dst[i] = uint8_t(packed >> (8 * i));
+  }
+  if (lane == 0) scales[int64_t(row) * groups + g] = sc;
+}
+
+// -------------------------------------------------------------- logprob ----
+// One CTA of 512 threads per row.  Thread t folds float4 chunks t, t+512, ...
+// into an online (max, sumexp) pair; pairs are then merged by a warp xor tree
+// and the 16 warp results in warp order.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  const float a = (m == -INFINITY) ? 0.f : s * expf(m - mn);
+  const float b = (m2 == -INFINITY) ? 0.f : s2 * expf(m2 - mn);
+  m = mn;
+  s = a + b;
+}
+
+__global__ void __launch_bounds__(kLogprobThreads) logprob_kernel(
+    const float* __restrict__ z, int64_t ld, const int32_t* __restrict__ target, int V,
+    float* __restrict__ lp, int* err) {
+  __shared__ float sm_m[kLogprobThreads / 32], sm_s[kLogprobThreads / 32];
+  const int row = blockIdx.x;
+  const float4* zr = reinterpret_cast<const float4*>(z + int64_t(row) * ld);
+  const int chunks = V / 4;
+  float m = -INFINITY, s = 0.f;
+  for (int c = threadIdx.x; c < chunks; c += kLogprobThreads) {
+    const float4 q = __ldcs(zr + c);
+    const float cm = fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w));
+    if (cm > m) {
+      s = (m == -INFINITY) ? 0.f : s * expf(m - cm);
+      m = cm;
+    }
+    s += expf(q.x - m);
+    s += expf(q.y - m);
+    s += expf(q.z - m);
+    s += expf(q.w - m);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    sm_m[threadIdx.x >> 5] = m;
+    sm_s[threadIdx.x >> 5] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = sm_m[0], S = sm_s[0];
+    for (int i = 1; i < kLogprobThreads / 32; ++i) lse_merge(M, S, sm_m[i], sm_s[i]);
+    int tg = target[row];
+    if (tg < 0 || tg >= V) {
+      raise_error(err, kErrBadIndex);
+      lp[row] = NAN;
+      return;
+    }
+    lp[row] = z[int64_t(row) * ld + tg] - (M + logf(S));
+  }
+}
+
+// ---------------------------------------------------------------- router --
+// One warp per row; logits staged in shared memory.
+constexpr int kRouterWarps = 4;
+__global__ void router_kernel(const float* __restrict__ logits, int64_t ld, int rows, int E,
+                              int k, int32_t* __restrict__ idx, float* __restrict__ w) {
+  extern __shared__ float sm_router[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kRouterWarps + warp;
+  if (row >= rows) return;
+  float* z = sm_router + warp * E;
+  const float* src = logits + int64_t(row) * ld;
+  float m = -INFINITY;
+  for (int e = lane; e < E; e += 32) {
+    z[e] = src[e];
+    m = fmaxf(m, z[e]);
+  }
+  m = warp_max(m);
+  float den = 0.f;
+  for (int e = lane; e < E; e += 32) den += expf(z[e] - m);
+  den = warp_sum(den);
+  __syncwarp();
+  uint32_t taken_lo = 0;  // selection bookkeeping in shared memory below
+  for (int s = 0; s < k; ++s) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {
+      const float v = z[e];
+      if (isnan(v)) continue;  // chosen entries are marked NaN
+      if (v > bv || (v == bv && e < bi)) {
+        bv = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (v2 > bv || (v2 == bv && i2 < bi)) {
+        bv = v2;
+        bi = i2;
+      }
+    }
+    if (lane == 0) {
+      idx[int64_t(row) * k + s] = bi;
+      w[int64_t(row) * k + s] = expf(bv - m) / den;
+    }
+    __syncwarp();
+    if (lane == (bi & 31)) z[bi] = NAN;
+    __syncwarp();
+  }
+  (void)taken_lo;
+}
+
+// ------------------------------------------------------------- dispatch ----
+// One CTA; each warp owns experts warp, warp+32, ...  Pass 1 counts, thread 0
+// forms the exclusive prefix, pass 2 places entries in ascending (t, s) order.
+__global__ void __launch_bounds__(1024) moe_dispatch_kernel(const int32_t* __restrict__ idx,
+                                                            int n, int E,
+                                                            int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ perm,
+                                                            int32_t* __restrict__ src_row) {
+  extern __shared__ int sm_counts[];  // [E+1]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int e = warp; e < E; e += nw) {
+    int cnt = 0;
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      const bool hit = i < n && idx[i] == e;
+      cnt += __popc(__ballot_sync(0xffffffffu, hit));
+    }
+    if (lane == 0) sm_counts[e] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      const int c = sm_counts[e];
+      sm_counts[e] = acc;
+      offsets[e] = acc;
+      acc += c;
+    }
+    offsets[E] = acc;
+  }
+  __syncthreads();
+  for (int e = warp; e < E; e += nw) {
+    int at = sm_counts[e];
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      const bool hit = i < n && idx[i] == e;
+      const uint32_t bal = __ballot_sync(0xffffffffu, hit);
+      if (hit) {
+        const int r = at + __popc(bal & ((1u << lane) - 1u));
+        perm[r] = i;
+        src_row[i] = r;
+      }
+      at += __popc(bal);
+    }
+  }
+}
+
+__global__ void gather_rows_kernel(const uint8_t* __restrict__ src, int64_t ss,
+                                   const int32_t* __restrict__ perm, int k_div, int n,
+                                   int row_bytes, uint8_t* __restrict__ dst, int64_t ds) {
+  const int cpr = row_bytes / 16;
+  const int64_t total = int64_t(n) * cpr;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int r = int(i / cpr), c = int(i % cpr);
+    const int64_t s = perm[r] / k_div;
+    reinterpret_cast<uint4*>(dst + r * ds)[c] = reinterpret_cast<const uint4*>(src + s * ss)[c];
+  }
+}
+
+// --------------------------------------------------------------- combine --
+__global__ void moe_combine_kernel(const uint16_t* __restrict__ y,
+                                   const int32_t* __restrict__ src_row,
+                                   const float* __restrict__ w, const uint16_t* __restrict__ sh,
+                                   uint16_t* __restrict__ out, int T, int k, int d) {
+  const int cpr = d / 8;
+  const int64_t total = int64_t(T) * cpr;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int t = int(i / cpr), c = int(i % cpr);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < k; ++s) {
+      const int64_t e = int64_t(t) * k + s;
+      const int64_t r = src_row ? int64_t(src_row[e]) : e;
+      float v[8];
+      unpack8(reinterpret_cast<const uint4*>(y + r * d)[c], v);
+      const float ws = w[e];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(ws, v[j], acc[j]);
+    }
+    if (sh) {
+      float v[8];
+      unpack8(reinterpret_cast<const uint4*>(sh + int64_t(t) * d)[c], v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] += v[j];
+    }
+    reinterpret_cast<uint4*>(out + int64_t(t) * d)[c] = pack8(acc);
+  }
+}
+
+int grid_for(int64_t work, int threads) {
+  const int64_t want = (work + threads - 1) / threads;
+  const int64_t cap = int64_t(sm_count() > 0 ? sm_count() : 148) * 16;
+  return int(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+bool row_ok(const void* p, int64_t stride_elems, int elem_bytes) {
+  return aligned16(p) && ((stride_elems * elem_bytes) % 16 == 0);
+}
+
+}  // namespace
+}  // namespace biv
+
+using namespace biv;
+
+extern "C" {
+
+biv_status biv_embed(const int32_t* ids, const uint16_t* table, int vocab, int T, int d,
+                     uint16_t* h, int64_t h_stride, biv_stream_t stream) {
+  BIV_REQUIRE(T >= 0 && d > 0 && d % 8 == 0 && vocab > 0, "embed: bad sizes T=%d d=%d", T, d);
+  if (T == 0) return BIV_OK;
+  BIV_REQUIRE(ids && aligned16(table) && row_ok(h, h_stride, 2), "embed: bad pointer/stride");
+  embed_kernel<<<T, 128, 0, as_cuda(stream)>>>(ids, table, vocab, d, h, h_stride,
+                                              device_error_word());
+  return check_launch("embed");
+}
+
+biv_status biv_add_rmsnorm(const uint16_t* x, int64_t xs, uint16_t* r, int64_t rs,
+                           const uint16_t* w, uint16_t* y, int64_t ys, int rows, int d, float eps,
+                           biv_stream_t stream) {
+  BIV_REQUIRE(rows >= 0 && d > 0 && d % 8 == 0 && d <= 8192, "add_rmsnorm: bad d=%d", d);
+  if (rows == 0) return BIV_OK;
+  BIV_REQUIRE(row_ok(x, xs, 2) && row_ok(y, ys, 2) && aligned16(w) && (!r || row_ok(r, rs, 2)),
+              "add_rmsnorm: pointers/strides must keep rows 16-byte aligned");
+  const int cpt = (d / 8 + kNormThreads - 1) / kNormThreads;
+  cudaStream_t s = as_cuda(stream);
+  switch (cpt) {
+    case 1: add_rmsnorm_kernel<1><<<rows, kNormThreads, 0, s>>>(x, xs, r, rs, w, y, ys, d, eps); break;
+    case 2: add_rmsnorm_kernel<2><<<rows, kNormThreads, 0, s>>>(x, xs, r, rs, w, y, ys, d, eps); break;
+    case 3: add_rmsnorm_kernel<3><<<rows, kNormThreads, 0, s>>>(x, xs, r, rs, w, y, ys, d, eps); break;
+    default: add_rmsnorm_kernel<4><<<rows, kNormThreads, 0, s>>>(x, xs, r, rs, w, y, ys, d, eps); break;
+  }
+  return check_launch("add_rmsnorm");
+}
+
+biv_status biv_silu_mul(const uint16_t* gu, int64_t gs, uint16_t* y, int64_t ys, int rows, int I,
+                        biv_stream_t stream) {
+  BIV_REQUIRE(rows >= 0 && I > 0 && I % 8 == 0, "silu_mul: I=%d must be a multiple of 8", I);
+  if (rows == 0) return BIV_OK;
+  BIV_REQUIRE(row_ok(gu, gs, 2) && row_ok(y, ys, 2), "silu_mul: misaligned rows");
+  const int64_t work = int64_t(rows) * (I / 8);
+  silu_mul_kernel<<<grid_for(work, 256), 256, 0, as_cuda(stream)>>>(gu, gs, y, ys, rows, I);
+  return check_launch("silu_mul");
+}
+
+biv_status biv_rope_table(double theta, int D, int max_pos, float* cos_sin, biv_stream_t stream) {
+  BIV_REQUIRE(D > 0 && D % 2 == 0 && max_pos > 0 && cos_sin && theta > 0, "rope_table: bad args");
+  const int64_t n = int64_t(max_pos) * (D / 2);
+  rope_table_kernel<<<grid_for(n, 256), 256, 0, as_cuda(stream)>>>(theta, D, max_pos, cos_sin);
+  return check_launch("rope_table");
+}
+
+biv_status biv_qk_norm_rope(uint16_t* qkv, int64_t rs, int T, int Hq, int Hkv, int D,
+                            const uint16_t* q_w, const uint16_t* k_w, const float* cos_sin,
+                            int max_pos, const int32_t* pos, float eps, biv_stream_t stream) {
+  BIV_REQUIRE(D == 64 || D == 80 || D == 128, "qk_norm_rope: D=%d unsupported", D);
+  BIV_REQUIRE(T >= 0 && Hq > 0 && Hkv > 0 && max_pos > 0, "qk_norm_rope: bad sizes");
+  BIV_REQUIRE((q_w == nullptr) == (k_w == nullptr), "qk_norm_rope: give both gains or neither");
+  if (T == 0) return BIV_OK;
+  BIV_REQUIRE(qkv && cos_sin && pos, "qk_norm_rope: null pointer");
+  const int64_t warps = int64_t(T) * (Hq + Hkv);
+  const int threads = 256;
+  const int64_t blocks = (warps * 32 + threads - 1) / threads;
+  qk_norm_rope_kernel<<<unsigned(blocks), threads, 0, as_cuda(stream)>>>(
+      qkv, rs, T, Hq, Hkv, D, q_w, k_w, cos_sin, max_pos, pos, eps, device_error_word());
+  return check_launch("qk_norm_rope");
+}
+
+biv_status biv_kv_store_bf16(const uint16_t* k, const uint16_t* v, int64_t rs, const int64_t* slot,
+                             int T, int Hkv, int D, uint16_t* kc, uint16_t* vc,
+                             biv_stream_t stream) {
+  BIV_REQUIRE(T >= 0 && Hkv > 0 && D % 8 == 0, "kv_store_bf16: bad sizes");
+  if (T == 0) return BIV_OK;
+  BIV_REQUIRE(row_ok(k, rs, 2) && row_ok(v, rs, 2) && aligned16(kc) && aligned16(vc) && slot,
+              "kv_store_bf16: misaligned");
+  const int64_t work = int64_t(T) * Hkv * (D / 8) * 2;
+  kv_store_bf16_kernel<<<grid_for(work, 256), 256, 0, as_cuda(stream)>>>(k, v, rs, slot, T, Hkv,
+                                                                         D, kc, vc);
+  return check_launch("kv_store_bf16");
+}
+
+biv_status biv_kv_fp8_quant(const uint16_t* k, const uint16_t* v, int64_t rs, const int64_t* slot,
+                            int T, int Hkv, int D, uint8_t* kc, uint8_t* vc, float* ks, float* vs,
+                            biv_stream_t stream) {
+  BIV_REQUIRE(T >= 0 && Hkv > 0 && D > 0 && D <= 128, "kv_fp8_quant: bad sizes");
+  if (T == 0) return BIV_OK;
+  BIV_REQUIRE(k && v && slot && kc && vc && ks && vs, "kv_fp8_quant: null pointer");
+  const int64_t warps = int64_t(T) * Hkv * 2;
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  kv_fp8_quant_kernel<<<unsigned(blocks), 256, 0, as_cuda(stream)>>>(k, v, rs, slot, T, Hkv, D,
+                                                                     kc, vc, ks, vs);
+  return check_launch("kv_fp8_quant");
+}
+
+biv_status biv_kv_fp8_gather(const uint8_t* codes, const float* scales, const int32_t* bt,
+                             int max_pages, const int32_t* ctx, const int64_t* row0, int nseq,
+                             int Hkv, int D, int page, uint16_t* out, biv_stream_t stream) {
+  BIV_REQUIRE(nseq >= 0 && Hkv > 0 && D > 0 && page > 0 && max_pages > 0,
+              "kv_fp8_gather: bad sizes");
+  if (nseq == 0) return BIV_OK;
+  BIV_REQUIRE(nseq <= 65535, "kv_fp8_gather: nseq above 65535");
+  BIV_REQUIRE(codes && scales && bt && ctx && row0 && out, "kv_fp8_gather: null pointer");
+  dim3 grid(64, nseq);
+  kv_fp8_gather_kernel<<<grid, 256, 0, as_cuda(stream)>>>(codes, scales, bt, max_pages, ctx, row0,
+                                                          Hkv, D, page, out);
+  return check_launch("kv_fp8_gather");
+}
+
+biv_status biv_act_quant_fp8(const uint16_t* x, int64_t xs, int rows, int K, uint8_t* codes,
+                             float* scales, biv_stream_t stream) {
+  BIV_REQUIRE(rows >= 0 && K > 0 && K % 16 == 0, "act_quant_fp8: K=%d must be a multiple of 16", K);
+  if (rows == 0) return BIV_OK;
+  BIV_REQUIRE(x && codes && scales, "act_quant_fp8: null pointer");
+  const int64_t warps = int64_t(rows) * ((K + 127) / 128);
+  act_quant_kernel<<<unsigned((warps * 32 + 255) / 256), 256, 0, as_cuda(stream)>>>(
+      x, xs, rows, K, codes, scales);
+  return check_launch("act_quant_fp8");
+}
+
+biv_status biv_logprob(const float* z, int64_t ld, const int32_t* target, int T, int V, float* lp,
+                       biv_stream_t stream) {
+  BIV_REQUIRE(T >= 0 && V > 0 && V % 4 == 0, "logprob: V=%d must be a multiple of 4", V);
+  if (T == 0) return BIV_OK;
+  BIV_REQUIRE(row_ok(z, ld, 4) && target && lp, "logprob: logits rows must be 16-byte aligned");
+  logprob_kernel<<<T, kLogprobThreads, 0, as_cuda(stream)>>>(z, ld, target, V, lp,
+                                                           device_error_word());
+  return check_launch("logprob");
+}
+
+biv_status biv_router_topk(const float* logits, int64_t ld, int rows, int E, int k, int32_t* idx,
+                           float* w, biv_stream_t stream) {
+  BIV_REQUIRE(rows >= 0 && E > 0 && E <= 1024 && k > 0 && k <= 32 && k <= E,
+              "router_topk: bad sizes E=%d k=%d", E, k);
+  if (rows == 0) return BIV_OK;
+  BIV_REQUIRE(logits && idx && w, "router_topk: null pointer");
+  const int blocks = (rows + kRouterWarps - 1) / kRouterWarps;
+  router_kernel<<<blocks, 32 * kRouterWarps, kRouterWarps * E * sizeof(float), as_cuda(stream)>>>(
+      logits, ld, rows, E, k, idx, w);
+  return check_launch("router_topk");
+}
+
+biv_status biv_moe_dispatch(const int32_t* idx, int T, int k, int E, int32_t* offsets,
+                            int32_t* perm, int32_t* src_row, biv_stream_t stream) {
+  BIV_REQUIRE(T >= 0 && k > 0 && E > 0 && E <= 4096 && int64_t(T) * k <= (1 << 20),
+              "moe_dispatch: bad sizes");
+  BIV_REQUIRE(idx && offsets && perm && src_row, "moe_dispatch: null pointer");
+  moe_dispatch_kernel<<<1, 1024, (E + 1) * sizeof(int), as_cuda(stream)>>>(idx, T * k, E, offsets,
+                                                                          perm, src_row);
+  return check_launch("moe_dispatch");
+}
+
+biv_status biv_gather_rows(const void* src, int64_t ss, const int32_t* perm, int k_div, int n,
+                           int row_bytes, void* dst, int64_t ds, biv_stream_t stream) {
+  BIV_REQUIRE(n >= 0 && k_div > 0 && row_bytes > 0 && row_bytes % 16 == 0,
+              "gather_rows: bad sizes");
+  if (n == 0) return BIV_OK;
+  BIV_REQUIRE(aligned16(src) && aligned16(dst) && ss % 16 == 0 && ds % 16 == 0 && perm,
+              "gather_rows: misaligned");
+  const int64_t work = int64_t(n) * (row_bytes / 16);
+  gather_rows_kernel<<<grid_for(work, 256), 256, 0, as_cuda(stream)>>>(
+      static_cast<const uint8_t*>(src), ss, perm, k_div, n, row_bytes,
+      static_cast<uint8_t*>(dst), ds);
+  return check_launch("gather_rows");
+}
+
+biv_status biv_moe_combine(const uint16_t* y, const int32_t* src_row, const float* w,
+                           const uint16_t* sh, uint16_t* out, int T, int k, int d,
+                           biv_stream_t stream) {
+  BIV_REQUIRE(T >= 0 && k > 0 && d > 0 && d % 8 == 0, "moe_combine: bad sizes");
+  if (T == 0) return BIV_OK;
+  BIV_REQUIRE(aligned16(y) && aligned16(out) && w && (!sh || aligned16(sh)),
+              "moe_combine: misaligned");
+  const int64_t work = int64_t(T) * (d / 8);
+  moe_combine_kernel<<<grid_for(work, 256), 256, 0, as_cuda(stream)>>>(y, src_row, w, sh, out, T,
+                                                                       k, d);
+  return check_launch("moe_combine");
+}
+
+}  // extern "C"

@@ -1,0 +1,201 @@
+"""Paged attention: parity with the oracle's plain softmax, and bitwise
+invariance of a row across prefill blocks, decode, block partitions and batch
+mix (one attention operator for every path)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import ops
+from oracle.codecs import bf16_to_f32
+
+pytestmark = pytest.mark.gpu
+REL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def B():
+    from invariant_forward_bitwise_gb300 import biv, build
+    build.build()
+    biv.load()
+    return biv
+
+
+def host_f32(t):
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return bf16_to_f32(t.view(torch.int16).numpy().view(np.uint16))
+    return t.float().numpy()
+
+
+def bits(t):
+    return t.detach().contiguous().view(torch.uint8).cpu().numpy()
+
+
+def rel_err(got, ref):
+    ref = np.asarray(ref, np.float64)
+    return float(np.max(np.abs(np.asarray(got, np.float64) - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+class Paged:
+    """Sequences' K/V in a shuffled paged cache (64-token pages)."""
+
+    def __init__(self, B, g, lens, Hkv, D, fp8=False):
+        self.B, self.lens, self.Hkv, self.D, self.fp8 = B, lens, Hkv, D, fp8
+        npages = [(L + 63) // 64 for L in lens]
+        total = sum(npages) + 3
+        perm = g.permutation(total)
+        self.bt = np.zeros((len(lens), max(npages)), np.int32)
+        at = 0
+        for i, n in enumerate(npages):
+            self.bt[i, :n] = perm[at:at + n]
+            at += n
+        self.k = [synth.normal_bf16(g, (L, Hkv, D)) for L in lens]
+        self.v = [synth.normal_bf16(g, (L, Hkv, D)) for L in lens]
+        shape = (total, 64, Hkv, D)
+        if fp8:
+            self.kc = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+            self.vc = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+            self.ks = torch.zeros(shape[:3], dtype=torch.float32, device="cuda")
+            self.vs = torch.zeros(shape[:3], dtype=torch.float32, device="cuda")
+        else:
+            # stale NaN everywhere that no token wrote: masked slots must not leak
+            self.kc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+            self.vc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+            self.ks = self.vs = None
+        for i, L in enumerate(lens):
+            pos = np.arange(L)
+            slot = (self.bt[i][pos // 64].astype(np.int64) * 64 + pos % 64)
+            kd, vd = self.k[i].cuda().reshape(L, -1), self.v[i].cuda().reshape(L, -1)
+            if fp8:
+                B.biv_kv_fp8_quant(kd, vd, Hkv * D, torch.from_numpy(slot).cuda(), L, Hkv, D,
+                                   self.kc, self.vc, self.ks, self.vs)
+            else:
+                B.biv_kv_store_bf16(kd, vd, Hkv * D, torch.from_numpy(slot).cuda(), L, Hkv, D,
+                                    self.kc, self.vc)
+        self.bt_d = torch.from_numpy(self.bt).cuda()
+
+    def oracle_kv(self, i):
+        k = self.k[i].float().numpy()
+        v = self.v[i].float().numpy()
+        if self.fp8:
+            k, v = ops.kv_roundtrip(k), ops.kv_roundtrip(v)
+        return k, v
+
+
+def run_attn(B, pc, q, rows, blocks, Hq, kv_split=1024, mode=0, topk_idx=None, topk=0):
+    """rows: list of (seq, pos); blocks: list of (first row, count)."""
+    T = len(rows)
+    D = pc.D
+    out = torch.full((T, Hq * D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    row_seq = torch.tensor([r[0] for r in rows], dtype=torch.int32, device="cuda")
+    row_pos = torch.tensor([r[1] for r in rows], dtype=torch.int32, device="cuda")
+    qb = torch.tensor(np.array(blocks, np.int32).ravel(), dtype=torch.int32, device="cuda")
+    d = B.AttnDesc()
+    d.q, d.q_stride = q.data_ptr(), q.stride(0)
+    d.out, d.out_stride = out.data_ptr(), out.stride(0)
+    d.T, d.Hq, d.Hkv, d.D = T, Hq, pc.Hkv, D
+    d.row_seq, d.row_pos = row_seq.data_ptr(), row_pos.data_ptr()
+    d.qblocks, d.nqblocks = qb.data_ptr(), len(blocks)
+    d.max_rows_per_block = max(b[1] for b in blocks)
+    d.kv_dtype = B.E4M3 if pc.fp8 else B.BF16
+    d.k_cache, d.v_cache = pc.kc.data_ptr(), pc.vc.data_ptr()
+    d.k_scale = pc.ks.data_ptr() if pc.fp8 else None
+    d.v_scale = pc.vs.data_ptr() if pc.fp8 else None
+    d.block_table, d.max_pages = pc.bt_d.data_ptr(), pc.bt.shape[1]
+    d.page, d.kv_split = 64, kv_split
+    d.max_ctx = max(r[1] for r in rows) + 1
+    if topk_idx is not None:
+        d.topk_idx, d.topk_stride, d.topk = topk_idx.data_ptr(), topk_idx.stride(0), topk
+    d.scale = 1.0 / math.sqrt(D)
+    d.mode = mode
+    n = B.biv_attention_workspace(d)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda") if n else None
+    B.biv_attention(d, ws)
+    torch.cuda.synchronize()
+    return out
+
+
+def blocks_of(rows, per):
+    out, i = [], 0
+    while i < len(rows):
+        j = i
+        while j < len(rows) and j - i < per and rows[j][0] == rows[i][0]:
+            j += 1
+        out.append((i, j - i))
+        i = j
+    return out
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,fp8,split", [(128, 16, 8, False, 1024), (128, 16, 8, True, 128),
+                                                 (64, 4, 2, False, 64), (80, 32, 4, False, 192),
+                                                 (128, 32, 1, True, 256)])
+def test_prefill_parity_and_decode_invariance(B, D, Hq, Hkv, fp8, split):
+    g = synth.rng(D + Hq + split)
+    lens = [37, 300, 64, 129]
+    pc = Paged(B, g, lens, Hkv, D, fp8)
+    G = Hq // Hkv
+    rows = [(i, p) for i, L in enumerate(lens) for p in range(L)]
+    q = synth.normal_bf16(g, (len(rows), Hq * D)).cuda()
+    per = max(1, 64 // G)
+    out = run_attn(B, pc, q, rows, blocks_of(rows, per), Hq, kv_split=split)
+    got = host_f32(out).reshape(len(rows), Hq, D)
+    qh = host_f32(q).reshape(len(rows), Hq, D)
+    at = 0
+    for i, L in enumerate(lens):
+        k, v = pc.oracle_kv(i)
+        ref = ops.attention(qh[at:at + L], k, v, np.arange(L), np.arange(L), 1.0 / math.sqrt(D))
+        assert rel_err(got[at:at + L], ref) < REL, i
+        at += L
+    # decode: one row per sequence at its last position, one row per block
+    last = [sum(lens[:i + 1]) - 1 for i in range(len(lens))]
+    drows = [rows[j] for j in last]
+    qd = q[torch.tensor(last, device="cuda")]
+    dout = run_attn(B, pc, qd, drows, [(j, 1) for j in range(len(drows))], Hq, kv_split=split)
+    assert np.array_equal(bits(dout), bits(out[torch.tensor(last, device="cuda")]))
+    # another block partition of the same prefill rows
+    out2 = run_attn(B, pc, q, rows, blocks_of(rows, max(1, per // 3)), Hq, kv_split=split)
+    assert np.array_equal(bits(out2), bits(out))
+
+
+def test_fast_mode_close_not_required_equal(B):
+    g = synth.rng(3)
+    lens = [2000, 900]
+    pc = Paged(B, g, lens, 8, 128)
+    rows = [(0, 1999), (1, 899)]
+    q = synth.normal_bf16(g, (2, 16 * 128)).cuda()
+    inv = run_attn(B, pc, q, rows, [(0, 1), (1, 1)], 16)
+    fast = run_attn(B, pc, q, rows, [(0, 1), (1, 1)], 16, mode=B.MODE_FAST)
+    assert rel_err(host_f32(fast), host_f32(inv)) < 1e-2
+
+
+def test_sparse_topk_attention(B):
+    g = synth.rng(4)
+    L, D, Hq = 700, 128, 32
+    pc = Paged(B, g, [L], 1, D)
+    qpos = [699, 650, 100]
+    topk = 256
+    idx = np.full((3, topk), -1, np.int32)
+    for r, p in enumerate(qpos):
+        cand = g.permutation(p + 1)[:min(topk, p + 1) - (r == 0) * 10]
+        idx[r, :cand.size] = np.sort(cand)
+    rows = [(0, p) for p in qpos]
+    q = synth.normal_bf16(g, (3, Hq * D)).cuda()
+    out = run_attn(B, pc, q, rows, [(0, 1), (1, 1), (2, 1)], Hq, kv_split=128,
+                   topk_idx=torch.from_numpy(idx).cuda(), topk=topk)
+    k, v = pc.oracle_kv(0)
+    ref = ops.sparse_attention(host_f32(q).reshape(3, Hq, D), k, v, idx, np.array(qpos), 1 / math.sqrt(D))
+    assert rel_err(host_f32(out).reshape(3, Hq, D), ref) < REL
+    # the same row alone
+    one = run_attn(B, pc, q[1:2], rows[1:2], [(0, 1)], Hq, kv_split=128,
+                   topk_idx=torch.from_numpy(idx[1:2]).cuda(), topk=topk)
+    assert np.array_equal(bits(one), bits(out[1:2]))
+    # dense top-k that lists every position equals causal attention
+    full = np.tile(np.arange(topk, dtype=np.int32), (1, 1))
+    rows2 = [(0, 200)]
+    o_sparse = run_attn(B, pc, q[:1], rows2, [(0, 1)], Hq, kv_split=128,
+                        topk_idx=torch.from_numpy(np.where(full <= 200, full, -1)).cuda(), topk=topk)
+    o_dense = run_attn(B, pc, q[:1], rows2, [(0, 1)], Hq, kv_split=128)
+    assert rel_err(host_f32(o_sparse), host_f32(o_dense)) < 1e-2

@@ -1,0 +1,384 @@
+"""Per-op parity of the CUDA path against the CPU oracle, plus bitwise row
+invariance (a row computed alone equals the same row inside any batch).
+
+Tolerances: integer/byte outputs bit-exact; floating-point outputs within the
+relative error 1e-2 of the oracle (max |gpu - oracle| / max |oracle| per
+output tensor), the per-op bar of the method's statement.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import ops
+from oracle.codecs import bf16_to_f32, e4m3_to_f32
+
+pytestmark = pytest.mark.gpu
+
+REL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def B():
+    from invariant_forward_bitwise_gb300 import biv, build
+    build.build()
+    biv.load()
+    return biv
+
+
+def dev(x, dtype=None):
+    t = torch.as_tensor(x)
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def host_f32(t):
+    """bf16/float CUDA tensor -> float32 numpy (bf16 decoded by the oracle codec)."""
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return bf16_to_f32(t.view(torch.int16).numpy().view(np.uint16))
+    return t.float().numpy()
+
+
+def rel_err(got, ref):
+    ref = np.asarray(ref, np.float64)
+    den = max(np.max(np.abs(ref)), 1e-30)
+    return float(np.max(np.abs(np.asarray(got, np.float64) - ref)) / den)
+
+
+def bits(t):
+    return t.detach().contiguous().view(torch.uint8).cpu().numpy()
+
+
+def rnd_bf16(g, *shape, std=1.0):
+    return synth.normal_bf16(g, shape, std)
+
+
+# ------------------------------------------------------------------ RMSNorm --
+@pytest.mark.parametrize("d", [256, 2048, 2560, 4096, 128, 8192])
+def test_add_rmsnorm_parity_and_row_invariance(B, d):
+    g = synth.rng(d)
+    rows = 37
+    x, r, w = rnd_bf16(g, rows, d), rnd_bf16(g, rows, d), rnd_bf16(g, d)
+    xd, rd, wd = dev(x), dev(r), dev(w)
+    y = torch.empty_like(xd)
+    B.biv_add_rmsnorm(xd, rd, wd, y, 1e-6)
+    r_ref, y_ref = ops.add_rmsnorm(x.float().numpy(), r.float().numpy(), w.float().numpy(), 1e-6)
+    assert np.array_equal(host_f32(rd), r_ref)          # bf16(x + r) is exact
+    assert rel_err(host_f32(y), y_ref) < REL
+    # no-residual form
+    y2 = torch.empty_like(xd)
+    B.biv_add_rmsnorm(xd, None, wd, y2, 1e-6)
+    assert rel_err(host_f32(y2), ops.rmsnorm(x.float().numpy(), w.float().numpy(), 1e-6)) < REL
+    # row 11 alone == row 11 in the batch, bit for bit
+    r1 = dev(r[11:12])
+    y1 = torch.empty_like(xd[11:12])
+    B.biv_add_rmsnorm(xd[11:12], r1, wd, y1, 1e-6)
+    assert np.array_equal(bits(y1), bits(y[11:12])) and np.array_equal(bits(r1), bits(rd[11:12]))
+
+
+def test_silu_mul_parity(B):
+    g = synth.rng(5)
+    gu = rnd_bf16(g, 19, 2 * 688, std=2.0)
+    y = torch.empty(19, 688, dtype=torch.bfloat16, device="cuda")
+    B.biv_silu_mul(dev(gu), y)
+    assert rel_err(host_f32(y), ops.silu_mul(gu.float().numpy())) < REL
+
+
+def test_embed_and_bad_id(B):
+    g = synth.rng(6)
+    table = rnd_bf16(g, 100, 64)
+    ids = np.array([3, 0, 99, 42], np.int32)
+    h = torch.empty(4, 64, dtype=torch.bfloat16, device="cuda")
+    B.biv_embed(dev(ids), dev(table), h)
+    assert np.array_equal(bits(h), bits(table[ids]))
+    assert B.biv_poll_error() == 0
+    B.biv_embed(dev(np.array([1, 100], np.int32)), dev(table), h[:2])
+    assert B.biv_poll_error() == 2                      # bad index reported, then cleared
+    assert B.biv_poll_error() == 0
+
+
+# --------------------------------------------------------------------- RoPE --
+@pytest.mark.parametrize("D,qk", [(128, True), (64, False), (80, False)])
+def test_qk_norm_rope_parity(B, D, qk):
+    g = synth.rng(7)
+    T, Hq, Hkv, max_pos = 9, 4, 2, 5000
+    qkv = rnd_bf16(g, T, (Hq + 2 * Hkv) * D)
+    pos = np.array([0, 1, 5, 77, 128, 1000, 4095, 4999, 3], np.int32)
+    qw = rnd_bf16(g, D) if qk else None
+    kw = rnd_bf16(g, D) if qk else None
+    tab = torch.empty(2 * max_pos * (D // 2), dtype=torch.float32, device="cuda")
+    B.biv_rope_table(1e6, D, max_pos, tab)
+    cos, sin = ops.rope_table(1e6, D, max_pos)
+    got_tab = tab.cpu().numpy().reshape(2, max_pos, D // 2)
+    assert np.max(np.abs(got_tab[0] - cos)) < 1e-6 and np.max(np.abs(got_tab[1] - sin)) < 1e-6
+    qd = dev(qkv)
+    B.biv_qk_norm_rope(qd, T, Hq, Hkv, D, dev(qw) if qk else None, dev(kw) if qk else None, tab,
+                       max_pos, dev(pos), 1e-6)
+    x = qkv.float().numpy()
+    q = x[:, :Hq * D].reshape(T, Hq, D)
+    k = x[:, Hq * D:(Hq + Hkv) * D].reshape(T, Hkv, D)
+    qr = ops.qk_norm_rope(q, pos, qw.float().numpy() if qk else None, 1e-6, cos, sin)
+    kr = ops.qk_norm_rope(k, pos, kw.float().numpy() if qk else None, 1e-6, cos, sin)
+    got = host_f32(qd)
+    assert rel_err(got[:, :Hq * D].reshape(T, Hq, D), qr) < REL
+    assert rel_err(got[:, Hq * D:(Hq + Hkv) * D].reshape(T, Hkv, D), kr) < REL
+    assert np.array_equal(got[:, (Hq + Hkv) * D:], x[:, (Hq + Hkv) * D:])   # v untouched
+
+
+# ------------------------------------------------------------------- FP8 KV --
+@pytest.mark.parametrize("D", [128, 64, 80])
+def test_kv_fp8_quant_codes_bit_exact_and_gather(B, D):
+    g = synth.rng(8)
+    T, Hkv, page = 70, 2, 64
+    k, v = rnd_bf16(g, T, Hkv * D, std=3.0), rnd_bf16(g, T, Hkv * D)
+    k[5] = 0   # amax = 0 row -> scale 1, codes 0
+    pages = 4
+    slot = np.arange(T, dtype=np.int64) + 64 * 1      # start on page 1
+    kc = torch.zeros(pages, page, Hkv, D, dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros(pages, page, Hkv, dtype=torch.float32, device="cuda")
+    vs = torch.zeros_like(ks)
+    kd, vd = dev(k), dev(v)
+    B.biv_kv_fp8_quant(kd, vd, Hkv * D, dev(slot), T, Hkv, D, kc, vc, ks, vs)
+    c_ref, s_ref = ops.fp8_quant_rows(k.float().numpy().reshape(T, Hkv, D))
+    got_c = kc.view(-1, Hkv, D)[64:64 + T].cpu().numpy()
+    got_s = ks.view(-1, Hkv)[64:64 + T].cpu().numpy()
+    assert np.array_equal(got_c, c_ref) and np.array_equal(got_s, s_ref)
+    # gather + dequant of 2 sequences sharing the pages
+    bt = dev(np.array([[1, 2, 0, 0], [1, 0, 0, 0]], np.int32))
+    ctx = dev(np.array([T, 10], np.int32))
+    row0 = dev(np.array([0, T], np.int64))
+    out = torch.empty(T + 10, Hkv, D, dtype=torch.bfloat16, device="cuda")
+    B.biv_kv_fp8_gather(kc, ks, bt, ctx, row0, Hkv, D, page, out)
+    ref = ops.fp8_dequant_rows(c_ref, s_ref)
+    assert np.array_equal(host_f32(out[:T]), ref) and np.array_equal(host_f32(out[T:]), ref[:10])
+
+
+def test_kv_store_bf16(B):
+    g = synth.rng(9)
+    T, Hkv, D = 5, 2, 64
+    qkv = rnd_bf16(g, T, 4 * Hkv * D)
+    kd = dev(qkv)
+    kc = torch.zeros(2, 64, Hkv, D, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    slot = dev(np.array([0, 1, -1, 70, 127], np.int64))
+    B.biv_kv_store_bf16(kd[:, :Hkv * D], kd[:, Hkv * D:], 4 * Hkv * D, slot, T, Hkv, D, kc, vc)
+    kcf = kc.view(-1, Hkv * D)
+    assert torch.equal(kcf[70], kd[3, :Hkv * D]) and torch.equal(kcf[2], torch.zeros_like(kcf[2]))
+    assert torch.equal(vc.view(-1, Hkv * D)[127], kd[4, Hkv * D:2 * Hkv * D])
+
+
+# ------------------------------------------------------------------ logprob --
+@pytest.mark.parametrize("V", [4096, 151936])
+def test_logprob_parity_and_invariance(B, V):
+    g = synth.rng(10)
+    T = 13
+    z = (synth.normal_f32(g, (T, V)) * 3).astype(np.float32)
+    tgt = g.integers(0, V, size=T).astype(np.int32)
+    lp = torch.empty(T, dtype=torch.float32, device="cuda")
+    zd = dev(z)
+    B.biv_logprob(zd, dev(tgt), lp)
+    ref = ops.logprob(z, tgt)
+    assert np.max(np.abs(lp.cpu().numpy() - ref)) < 1e-4
+    lp1 = torch.empty(1, dtype=torch.float32, device="cuda")
+    B.biv_logprob(zd[7:8], dev(tgt[7:8]), lp1)
+    assert np.array_equal(bits(lp1), bits(lp[7:8]))
+    # uniform logits: exactly -log V up to float rounding
+    B.biv_logprob(torch.zeros(2, V, device="cuda"), dev(np.array([0, 1], np.int32)), lp[:2])
+    assert np.allclose(lp[:2].cpu().numpy(), -math.log(V), atol=1e-5)
+
+
+# --------------------------------------------------------------------- GEMM --
+GEMM_SHAPES = [(1, 64, 64), (5, 96, 80), (130, 512, 256), (200, 688, 256), (77, 256, 688),
+               (257, 1000, 320), (64, 4096, 2048), (300, 2048, 6144)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_gemm_bf16_parity(B, M, N, K, out):
+    g = synth.rng(M * 7 + N + K)
+    a, b = rnd_bf16(g, M, K), rnd_bf16(g, N, K, std=0.05)
+    ad, bd = dev(a), dev(b)
+    c = torch.full((M, N), float("nan"), dtype=torch.bfloat16 if out == "bf16" else torch.float32,
+                   device="cuda")
+    B.biv_gemm(B.gemm_desc(ad, bd, c))
+    ref = ops.gemm(a.float().numpy(), b.float().numpy(), out=out)
+    got = host_f32(c)
+    assert np.isfinite(got).all()
+    assert rel_err(got, ref) < REL
+
+
+@pytest.mark.parametrize("N,K", [(512, 256), (4096, 2048), (151936 // 8, 2048)])
+def test_gemm_row_invariance(B, N, K):
+    """Any row's bits are the same alone, in a batch of 300, or at another
+    position of the 128-row tile."""
+    g = synth.rng(N + K)
+    M = 300
+    a, b = rnd_bf16(g, M, K), rnd_bf16(g, N, K, std=0.05)
+    ad, bd = dev(a), dev(b)
+    full = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    B.biv_gemm(B.gemm_desc(ad, bd, full))
+    for r in [0, 1, 127, 128, 200, 299]:
+        one = torch.empty(1, N, dtype=torch.float32, device="cuda")
+        B.biv_gemm(B.gemm_desc(ad[r:r + 1], bd, one))
+        assert np.array_equal(bits(one), bits(full[r:r + 1])), r
+    # shifted batch: row r lands at another tile position
+    sub = torch.empty(M - 45, N, dtype=torch.float32, device="cuda")
+    B.biv_gemm(B.gemm_desc(ad[45:], bd, sub))
+    assert np.array_equal(bits(sub), bits(full[45:]))
+
+
+def test_gemm_fast_mode_is_close_but_batch_dependent(B):
+    g = synth.rng(11)
+    M, N, K = 3, 2048, 6144
+    a, b = rnd_bf16(g, M, K), rnd_bf16(g, N, K, std=0.05)
+    ad, bd = dev(a), dev(b)
+    inv = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    B.biv_gemm(B.gemm_desc(ad, bd, inv))
+    d = B.gemm_desc(ad, bd, torch.empty(M, N, dtype=torch.float32, device="cuda"), mode=B.MODE_FAST)
+    fast = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    d = B.gemm_desc(ad, bd, fast, mode=B.MODE_FAST)
+    n = B.biv_gemm_workspace(d)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+    B.biv_gemm(d, ws)
+    assert n > 0                                     # FAST splits K at small M
+    assert rel_err(fast.cpu().numpy(), inv.cpu().numpy()) < 1e-4
+
+
+def test_gemm_fp8_block_scaled_parity(B):
+    g = synth.rng(12)
+    M, N, K = 200, 384, 512
+    a = rnd_bf16(g, M, K)
+    codes_b, sb = synth.fp8_block_weights(g, 1, N, K)
+    ad = dev(a)
+    ac = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    sa = torch.empty(M, K // 128, dtype=torch.float32, device="cuda")
+    B.biv_act_quant_fp8(ad, ac, sa)
+    ac_ref, sa_ref = ops.act_quant_fp8(a.float().numpy())
+    assert np.array_equal(ac.cpu().numpy(), ac_ref) and np.array_equal(sa.cpu().numpy(), sa_ref)
+    bc = dev(codes_b[0].view(torch.uint8))
+    c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    B.biv_gemm(B.gemm_desc(ac, bc, c, sa=sa, sb=dev(sb[0])))
+    ref = ops.gemm_fp8_block(ac_ref, sa_ref, synth.fp8_bits(codes_b[0]), sb[0])
+    assert rel_err(host_f32(c), ref) < REL
+    one = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
+    B.biv_gemm(B.gemm_desc(ac[150:151], bc, one, sa=sa[150:151], sb=dev(sb[0])))
+    assert np.array_equal(bits(one), bits(c[150:151]))
+
+
+def test_gemm_fp8_grouped(B):
+    g = synth.rng(13)
+    G, N, K = 4, 256, 384
+    counts = [130, 0, 7, 257]
+    M = sum(counts)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    a = rnd_bf16(g, M, K)
+    codes_b, sb = synth.fp8_block_weights(g, G, N, K)
+    ac = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    sa = torch.empty(M, K // 128, dtype=torch.float32, device="cuda")
+    B.biv_act_quant_fp8(dev(a), ac, sa)
+    c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    bc = dev(codes_b.view(torch.uint8).reshape(G * N, K))
+    B.biv_gemm(B.gemm_desc(ac, bc, c, sa=sa, sb=dev(sb), group_offsets=dev(offs), groups=G, M=M))
+    ac_h, sa_h = ac.cpu().numpy(), sa.cpu().numpy()
+    got = host_f32(c)
+    for e in range(G):
+        lo, hi = offs[e], offs[e + 1]
+        if hi == lo:
+            continue
+        ref = ops.gemm_fp8_block(ac_h[lo:hi], sa_h[lo:hi], synth.fp8_bits(codes_b[e]), sb[e])
+        assert rel_err(got[lo:hi], ref) < REL, e
+
+
+# -------------------------------------------------------------------- Top-K --
+def test_topk_brute_force_ties(B):
+    g = synth.rng(14)
+    R, n, k = 40, 1000, 37
+    s = g.integers(0, 4, size=(R, n)).astype(np.float32)
+    s[3] = -np.inf
+    s[4, :500] = -np.inf
+    s[5, 7] = -0.0
+    s[6] = 0.0
+    nv = g.integers(0, n + 1, size=R).astype(np.int32)
+    nv[:8] = n
+    nv[8] = 10
+    idx = torch.empty(R, k, dtype=torch.int32, device="cuda")
+    B.biv_topk(dev(s), dev(nv), k, idx)
+    assert np.array_equal(idx.cpu().numpy(), ops.topk_positions(s, nv, k))
+
+
+def test_topk_indexer_shape(B):
+    g = synth.rng(15)
+    R, n, k = 64, 32768, 2048
+    s = synth.normal_f32(g, (R, n))
+    s[:, ::3] = np.round(s[:, ::3], 1)          # plenty of ties
+    nv = (n - R + np.arange(R)).astype(np.int32)
+    idx = torch.empty(R, k, dtype=torch.int32, device="cuda")
+    sd = dev(s)
+    B.biv_topk(sd, dev(nv), k, idx)
+    got = idx.cpu().numpy()
+    for r in [0, 17, 63]:
+        assert np.array_equal(got[r], ops.topk_positions(s[r:r + 1], nv[r:r + 1], k)[0])
+    # a row alone gives the same indices
+    one = torch.empty(1, k, dtype=torch.int32, device="cuda")
+    B.biv_topk(sd[40:41], dev(nv[40:41]), k, one)
+    assert np.array_equal(one.cpu().numpy()[0], got[40])
+
+
+def test_router_topk(B):
+    g = synth.rng(16)
+    R, E, k = 300, 64, 6
+    z = (g.integers(-3, 4, size=(R, E)) * 0.5).astype(np.float32)
+    idx = torch.empty(R, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(R, k, dtype=torch.float32, device="cuda")
+    B.biv_router_topk(dev(z), k, idx, w)
+    ri, rw = ops.router_topk(z, k)
+    assert np.array_equal(idx.cpu().numpy(), ri)
+    assert np.max(np.abs(w.cpu().numpy() - rw)) < 1e-6
+
+
+def test_moe_dispatch_gather_combine(B):
+    g = synth.rng(17)
+    T, k, E, d = 50, 6, 8, 64
+    idx = np.stack([g.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    src = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    B.biv_moe_dispatch(dev(idx), E, offs, perm, src)
+    flat = idx.ravel()
+    ref_perm = np.concatenate([np.nonzero(flat == e)[0] for e in range(E)]).astype(np.int32)
+    assert np.array_equal(perm.cpu().numpy(), ref_perm)
+    assert np.array_equal(offs.cpu().numpy(), np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=E))]))
+    inv = np.empty_like(ref_perm)
+    inv[ref_perm] = np.arange(T * k)
+    assert np.array_equal(src.cpu().numpy(), inv)
+    # gather token rows into expert order, combine back in slot order
+    h = rnd_bf16(g, T, d)
+    hg = torch.empty(T * k, d, dtype=torch.bfloat16, device="cuda")
+    B.biv_gather_rows(dev(h), perm, k, T * k, hg)
+    assert np.array_equal(bits(hg), bits(h[torch.from_numpy(ref_perm // k).long()]))
+    y = rnd_bf16(g, T * k, d)
+    w = np.abs(synth.normal_f32(g, (T, k)))
+    sh = rnd_bf16(g, T, d)
+    out = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    B.biv_moe_combine(dev(y), src, dev(w), dev(sh), out)
+    y_slots = y.float().numpy()[inv].reshape(T, k, d)
+    assert rel_err(host_f32(out), ops.moe_combine(y_slots, w, sh.float().numpy())) < REL
+    onehot = np.zeros((T, k), np.float32)
+    onehot[:, 2] = 1
+    B.biv_moe_combine(dev(y), src, dev(onehot), None, out)
+    assert np.array_equal(host_f32(out), y_slots[:, 2])
+
+
+def test_device_wait_timeout_reports_and_recovers(B):
+    assert B.biv_poll_error() == 0
+    B.biv_selftest_timeout(2_000_000)        # 2 ms bounded wait that nobody satisfies
+    assert B.biv_poll_error() == 1           # timeout reported, word cleared
+    assert B.biv_poll_error() == 0
+    x = torch.ones(4, 64, dtype=torch.bfloat16, device="cuda")
+    B.biv_add_rmsnorm(x, None, x[0], x.clone(), 1e-6)   # context still usable
+    torch.cuda.synchronize()
