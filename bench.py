@@ -243,12 +243,8 @@ def main():
     diff_max = float(np.max(np.abs(la - lb)))
     clocks = Clocks(local)
     ms, ck, timer = timed(inv, args.steps, args.warmup, clocks)
-    ms_t = torch.tensor([ms], device="cuda")
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms = float(ms_t.item())
     tokens_per_step = 2 * resp_tokens
-    value = tokens_per_step * world / (ms / 1e3)
+    ms, value = reduce_over_ranks(ms, tokens_per_step, world, device="cuda")
 
     peaks = load_peaks()
     roof = timer.roofline(peaks)
@@ -289,6 +285,19 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def reduce_over_ranks(ms: float, tokens_per_step: int, world: int, device=None):
+    """Replicas: every rank runs its own sequences (weak scaling).  The step
+    time is the max over ranks; whole-job throughput counts all ranks' tokens
+    over that time."""
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    return ms, tokens_per_step * world / (ms / 1e3)
 
 
 class KernelTimer:

@@ -15,6 +15,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -211,6 +212,143 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int spli
   }
 }
 
+// ----------------------------------------------------- persistent bf16 ----
+// Same per-element schedule as gemm_bf16_kernel (ascending 64-wide K blocks,
+// four K=16 MMAs each, FP32 accumulator in TMEM), so the two give identical
+// bits.  Persistent grid; warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2..5 = epilogue.  The accumulator is double-buffered in TMEM so
+// the epilogue of tile j overlaps the main loop of tile j+1.  Tiles are walked
+// M-fastest so that CTAs running together share the weight tile in L2.
+template <int BN>
+struct PersistCfg {
+  static constexpr int BK = 64;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+};
+
+template <int BN, bool F32OUT>
+__global__ void __launch_bounds__(192, 1)
+    gemm_bf16_persistent(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB, void* C, int64_t ldc, int M,
+                         int N, int K, int vec_ok, int* err) {
+  using Cfg = PersistCfg<BN>;
+  constexpr int S = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * Cfg::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+  const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KB = (K + Cfg::BK - 1) / Cfg::BK;
+  const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+  const int tiles = tiles_m * tiles_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(tfull0 + 8 * j, 1);
+      mbar_init(tempty0 + 8 * j, 4);
+    }
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  int issued = 0;
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    bool ok = true;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int it = issued, s = it % S;
+        if (it >= S && !mbar_wait(empty0 + 8 * s, ((it / S) - 1) & 1, err)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(full0 + 8 * s, Cfg::STAGE);
+        tma_load_2d(smem_u32(sA + s * Cfg::A_BYTES), &tmA, full0 + 8 * s, kb * Cfg::BK, m0);
+        tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full0 + 8 * s, kb * Cfg::BK, n0);
+        issued = it + 1;
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = idesc_mma(1u, BM, BN);
+    int it = 0, j = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++j) {
+      const int b = j & 1;
+      if (j >= 2 && !mbar_wait(tempty0 + 8 * b, ((j >> 1) - 1) & 1, err)) break;
+      tc_fence_after();
+      const uint32_t dt = tmem + b * BN;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % S;
+        if (!mbar_wait(full0 + 8 * s, (it / S) & 1, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + s * Cfg::A_BYTES);
+        const uint32_t b0 = smem_u32(sB + s * Cfg::B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < Cfg::BK / 16; ++kk)
+          umma_f16(dt, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
+                   (kb | kk) != 0 ? 1u : 0u);
+        umma_commit(empty0 + 8 * s);
+      }
+      umma_commit(tfull0 + 8 * b);
+    }
+  } else if (warp >= 2) {
+    const int q = warp & 3;
+    int j = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
+      const int b = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * b, (j >> 1) & 1, err))) break;
+      tc_fence_after();
+      const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+      const int row = m0 + q * 32 + lane;
+      const uint32_t trow = tmem + b * BN + (uint32_t(q * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        if (n0 + c0 >= N) break;  // warp-uniform
+        uint32_t r[32];
+        tmem_ld32(trow + c0, r);
+        tmem_ld_wait();
+        if (row < M) store_row32<F32OUT>(C, ldc, row, n0 + c0, N, r, vec_ok != 0);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * b);
+    }
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = max(0, issued - S); i < issued; ++i)
+      mbar_wait(full0 + 8 * (i % S), (i / S) & 1, err, 100000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+}
+
 // ------------------------------------------------------------- FP8 kernel --
 // 6 warps: warp 0 = TMA producer, warp 1 = MMA issuer (+TMEM owner),
 // warps 2..5 = promotion/epilogue (lane quarter = warp % 4).  For each
@@ -390,7 +528,15 @@ struct Plan {
   int bn = 128;
   int splits = 1;
   int kb_per_split = 0;
+  bool persistent = false;
 };
+
+// Set BIV_GEMM_PERSISTENT=0 to force the one-tile-per-CTA kernel (used by the
+// tests that check both kernels give the same bits).
+bool persistent_allowed() {
+  const char* e = getenv("BIV_GEMM_PERSISTENT");
+  return !(e && e[0] == '0');
+}
 
 // INVARIANT: the tile width depends on N only; K is never split.
 // FAST: for small M, narrow tiles and a K split sized to fill the GPU.
@@ -399,7 +545,13 @@ Plan plan_bf16(const biv_gemm_desc& d) {
   const int KB = (d.K + 63) / 64;
   p.bn = d.N >= 8192 ? 256 : (d.N >= 128 ? 128 : (d.N > 32 ? 64 : 32));
   p.kb_per_split = KB;
+  // Many tiles: persistent kernel (identical per-element schedule, so this
+  // choice may depend on M without touching any result bit).
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  const int64_t tiles = int64_t((d.N + p.bn - 1) / p.bn) * ((d.M + BM - 1) / BM);
+  p.persistent = tiles >= 2 * sms && persistent_allowed();
   if (d.mode == BIV_MODE_FAST && d.M <= 256) {
+    p.persistent = false;
     p.bn = d.N >= 128 ? 64 : 32;
     const int tiles = ((d.N + p.bn - 1) / p.bn) * ((d.M + BM - 1) / BM);
     const int sms = sm_count() > 0 ? sm_count() : 148;
@@ -432,9 +584,38 @@ biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_g
   return check_launch("gemm_bf16");
 }
 
+template <int BN, bool F32OUT>
+biv_status launch_bf16_persistent(const CUtensorMap& ta, const CUtensorMap& tb,
+                                  const biv_gemm_desc& d, cudaStream_t s) {
+  using Cfg = PersistCfg<BN>;
+  auto kern = gemm_bf16_persistent<BN, F32OUT>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+        cudaSuccess)
+      return set_error(BIV_ERR_CUDA, "gemm: cannot set shared memory size");
+    attr = true;
+  }
+  const int eb = F32OUT ? 4 : 2;
+  const int vec_ok = aligned16(d.C) && (d.ldc * eb) % 16 == 0;
+  const int tiles = ((d.N + BN - 1) / BN) * ((d.M + BM - 1) / BM);
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  const int grid = std::min(tiles, sms);
+  kern<<<grid, 192, Cfg::SMEM, s>>>(ta, tb, d.C, d.ldc, d.M, d.N, d.K, vec_ok, device_error_word());
+  return check_launch("gemm_bf16_persistent");
+}
+
 template <bool F32OUT>
 biv_status dispatch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_gemm_desc& d,
                          const Plan& p, float* partial, cudaStream_t s) {
+  if (p.persistent) {
+    switch (p.bn) {
+      case 256: return launch_bf16_persistent<256, F32OUT>(ta, tb, d, s);
+      case 128: return launch_bf16_persistent<128, F32OUT>(ta, tb, d, s);
+      case 64: return launch_bf16_persistent<64, F32OUT>(ta, tb, d, s);
+      default: return launch_bf16_persistent<32, F32OUT>(ta, tb, d, s);
+    }
+  }
   switch (p.bn) {
     case 256: return launch_bf16<256, F32OUT>(ta, tb, d, p, partial, s);
     case 128: return launch_bf16<128, F32OUT>(ta, tb, d, p, partial, s);

@@ -71,8 +71,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sh = 8 * byte;
       for (int b = lane; b < 256; b += 32) whist[warp * 256 + b] = 0;
       __syncwarp();
-      for (int j = tid; j < n; j += kThreads) {
-        const uint32_t key = keys[j];
+      // uniform trip count: every lane of a warp reaches the ballot/match
+      for (int base = 0; base < n; base += kThreads) {
+        const int j = base + tid;
+        const uint32_t key = j < n ? keys[j] : 0u;
         const bool hit = key != 0 && (key & mask) == want;
         const uint32_t bin = (key >> sh) & 255u;
         const uint32_t act = __ballot_sync(0xffffffffu, hit);

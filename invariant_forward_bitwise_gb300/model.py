@@ -125,6 +125,8 @@ class DenseModel:
         self.lm_rows = torch.zeros(T, **i32)
         self.targets = torch.zeros(T, **i32)
         self.ws = torch.empty(16, dtype=torch.uint8, device=device)
+        self._old_ws: List[torch.Tensor] = []
+        self.audit: Optional[list] = None  # when a list: residual stream copied after each layer
         self.launches = 0        # libbiv launches of the last step()
         self.kernel_timer = None  # optional event brackets around GEMM/attention
         self.h2d_bytes = 0       # host->device bytes of step inputs copied so far
@@ -148,14 +150,15 @@ class DenseModel:
             t.close(tok)
         self.launches += 2 if need else 1
 
-    def _attn_desc(self, kv: PagedKV, layer: int, spec: StepSpec):
+    def _attn_desc(self, kv: PagedKV, layer: int, spec: StepSpec, qblocks=None):
         cfg = self.cfg
         d = biv.AttnDesc()
         d.q, d.q_stride = self.qkv.data_ptr(), self.qkv.stride(0)
         d.out, d.out_stride = self.o.data_ptr(), self.o.stride(0)
         d.T, d.Hq, d.Hkv, d.D = spec.T, cfg.q_heads, cfg.kv_heads, cfg.head_dim
         d.row_seq, d.row_pos = self.row_seq.data_ptr(), self.row_pos.data_ptr()
-        d.qblocks, d.nqblocks = self.qblocks.data_ptr(), spec.nqblocks
+        d.qblocks = (self.qblocks if qblocks is None else qblocks).data_ptr()
+        d.nqblocks = spec.nqblocks
         d.max_rows_per_block = spec.max_rows_per_block
         d.kv_dtype = biv.E4M3 if kv.fp8 else biv.BF16
         d.k_cache, d.v_cache = kv.k[layer].data_ptr(), kv.v[layer].data_ptr()
@@ -193,13 +196,19 @@ class DenseModel:
             d.mode = self.mode
             need = max(need, biv.biv_gemm_workspace(d))
         if need > self.ws.numel():
+            # captured graphs keep the address they saw: never free a workspace
+            self._old_ws.append(self.ws)
             self.ws = torch.empty(need, dtype=torch.uint8, device=self.ws.device)
 
     # -- the forward ------------------------------------------------------------
-    def step(self, kv: PagedKV, spec: StepSpec):
+    def step(self, kv: PagedKV, spec: StepSpec, qblocks=None, lm_rows=None):
         """Rows [0, spec.T) of the static inputs through the model; logprobs of
-        targets[0, T_lm) for rows lm_rows[0, T_lm) land in lp[0, T_lm)."""
+        targets[0, T_lm) for rows lm_rows[0, T_lm) land in lp[0, T_lm).
+        ``qblocks`` / ``lm_rows`` default to the shared step buffers; captured
+        decode graphs pass constant buffers of their own."""
         cfg, W, T = self.cfg, self.W, spec.T
+        qblocks = self.qblocks if qblocks is None else qblocks
+        lm_rows = self.lm_rows if lm_rows is None else lm_rows
         Hq, Hkv, D = cfg.q_heads, cfg.kv_heads, cfg.head_dim
         eps = cfg.eps
         r, y = self.r[:T], self.y[:T]
@@ -220,7 +229,7 @@ class DenseModel:
                                      kv.ks[l], kv.vs[l])
             else:
                 biv.biv_kv_store_bf16(kq, vq, self.qkv.stride(0), self.slot, T, Hkv, D, kv.k[l], kv.v[l])
-            ad = self._attn_desc(kv, l, spec)
+            ad = self._attn_desc(kv, l, spec, qblocks)
             need = biv.biv_attention_workspace(ad)
             t = self._timer()
             tok = t.bracket("attention_prefill", spec.attn_flops, "flop") if t and spec.attn_flops else None
@@ -235,11 +244,13 @@ class DenseModel:
             nxt = W[f"l{l + 1}.attn_norm"] if l + 1 < cfg.layers else W["final_norm"]
             biv.biv_add_rmsnorm(self.a[:T], r, nxt, y, eps)
             self.launches += 6 + (2 if need else 1)
+            if self.audit is not None and not torch.cuda.is_current_stream_capturing():
+                self.audit.append(("layer", l, r.clone()))
         # LM head + logprob over the rows that produce a logprob
         Tl = spec.T_lm
         if Tl == 0:
             return
-        biv.biv_gather_rows(y, self.lm_rows, 1, Tl, self.ylm)
+        biv.biv_gather_rows(y, lm_rows, 1, Tl, self.ylm)
         self.launches += 1
         for c0 in range(0, Tl, self.lm_chunk):
             n = min(self.lm_chunk, Tl - c0)
@@ -389,6 +400,14 @@ class DecodeGraphs:
         self.m, self.kv, self.use = model, kv, use_graphs
         self.graphs: Dict[int, torch.cuda.CUDAGraph] = {}
         self.launches: Dict[int, int] = {}
+        # decode rows are one per block and all produce a logprob: constant
+        # buffers owned by the graphs (the eager prefill path reuses the
+        # model's shared qblocks / lm_rows buffers between replays)
+        nmax = self.BUCKETS[-1]
+        dev = model.ids.device
+        self.qblocks = torch.stack([torch.arange(nmax, dtype=torch.int32),
+                                    torch.ones(nmax, dtype=torch.int32)], 1).to(dev)
+        self.lm_rows = torch.arange(nmax, dtype=torch.int32, device=dev)
 
     def spec(self, Tb: int) -> StepSpec:
         return StepSpec(T=Tb, nqblocks=Tb, max_rows_per_block=1, max_ctx=self.m.max_pos, T_lm=Tb)
@@ -415,28 +434,21 @@ class DecodeGraphs:
         m.targets[:Tb].copy_(torch.from_numpy(tg), non_blocking=True)
         m.h2d_bytes += Tb * (4 + 4 + 4 + 8 + 4)
         spec = self.spec(Tb)
-        if Tb not in self.graphs:
-            qb = np.stack([np.arange(Tb), np.ones(Tb)], 1).astype(np.int32)
-            m.qblocks[:Tb].copy_(torch.from_numpy(qb))
-            m.lm_rows[:Tb].copy_(torch.arange(Tb, dtype=torch.int32))
-            if self.use:
-                m.reserve(self.kv, [spec])
-                s = torch.cuda.Stream()
-                s.wait_stream(torch.cuda.current_stream())
-                with torch.cuda.stream(s):
-                    m.step(self.kv, spec)           # warm-up (also a real step of these rows)
-                torch.cuda.current_stream().wait_stream(s)
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    m.step(self.kv, spec)
-                self.graphs[Tb] = g
-                self.launches[Tb] = m.launches
-        if not self.use:
-            qb = np.stack([np.arange(Tb), np.ones(Tb)], 1).astype(np.int32)
-            m.qblocks[:Tb].copy_(torch.from_numpy(qb), non_blocking=True)
-            m.lm_rows[:Tb].copy_(torch.arange(Tb, dtype=torch.int32), non_blocking=True)
+        if self.use and Tb not in self.graphs:
             m.reserve(self.kv, [spec])
-            m.step(self.kv, spec)
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                m.step(self.kv, spec, self.qblocks, self.lm_rows)   # warm-up: a real step of these rows
+            torch.cuda.current_stream().wait_stream(s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                m.step(self.kv, spec, self.qblocks, self.lm_rows)
+            self.graphs[Tb] = g
+            self.launches[Tb] = m.launches
+        elif not self.use:
+            m.reserve(self.kv, [spec])
+            m.step(self.kv, spec, self.qblocks, self.lm_rows)
         else:
             self.graphs[Tb].replay()
             t = m._timer()

@@ -33,6 +33,7 @@ class DenseOracle:
     def __init__(self, cfg, W: Dict[str, np.ndarray], max_pos: int = 4096):
         self.cfg = cfg
         self.W = W
+        self.audit = None  # when a list: residual stream after each layer
         self.cos, self.sin = ops.rope_table(cfg.rope_theta, cfg.head_dim, max_pos)
         self.scale = F32(1.0 / np.sqrt(cfg.head_dim))
 
@@ -73,6 +74,8 @@ class DenseOracle:
             m = ops.gemm(ops.silu_mul(gu), W[f"l{l}.wd"])
             nxt = W[f"l{l + 1}.attn_norm"] if l + 1 < cfg.layers else W["final_norm"]
             r, y = ops.add_rmsnorm(m, r, nxt, cfg.eps)
+            if self.audit is not None:
+                self.audit.append(("layer", l, r.copy()))
         return ops.gemm(y, W["lm_head"], out="f32")
 
     def new_cache(self) -> list:

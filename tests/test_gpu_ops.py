@@ -382,3 +382,42 @@ def test_device_wait_timeout_reports_and_recovers(B):
     x = torch.ones(4, 64, dtype=torch.bfloat16, device="cuda")
     B.biv_add_rmsnorm(x, None, x[0], x.clone(), 1e-6)   # context still usable
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("M,N,K,out", [(4096, 2048, 2048, "bf16"), (2304, 12288, 512, "bf16"),
+                                       (1200, 151936 // 4, 256, "f32")])
+def test_gemm_persistent_equals_one_tile_kernel(B, monkeypatch, M, N, K, out):
+    """Large M runs the persistent kernel; forcing the one-tile-per-CTA kernel
+    must give the same bits (same per-element K schedule)."""
+    g = synth.rng(M + N)
+    a, b = rnd_bf16(g, M, K), rnd_bf16(g, N, K, std=0.05)
+    ad, bd = dev(a), dev(b)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    c1 = torch.empty(M, N, dtype=dt, device="cuda")
+    B.biv_gemm(B.gemm_desc(ad, bd, c1))
+    monkeypatch.setenv("BIV_GEMM_PERSISTENT", "0")
+    c2 = torch.empty(M, N, dtype=dt, device="cuda")
+    B.biv_gemm(B.gemm_desc(ad, bd, c2))
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(c1), bits(c2))
+    rows = np.array([0, 1, 777, M - 1])
+    ref = ops.gemm(a.float().numpy()[rows], b.float().numpy(), out=out)
+    assert rel_err(host_f32(c1)[rows], ref) < REL
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 512, 192), (100, 512, 128), (7, 8192, 192), (64, 12288, 64)])
+def test_tcgen05_result_independent_of_tile_width(B, M, N, K):
+    """The hardware property the tile planner relies on: with the same K
+    schedule, an output element has the same bits whether its CTA's MMA is
+    N=64 wide (FAST mode at small M, no K split for K <= 192) or 128/256 wide
+    (INVARIANT mode)."""
+    g = synth.rng(M * N + K)
+    a, b = rnd_bf16(g, M, K), rnd_bf16(g, N, K, std=0.05)
+    ad, bd = dev(a), dev(b)
+    c1 = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    c2 = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    B.biv_gemm(B.gemm_desc(ad, bd, c1))
+    d = B.gemm_desc(ad, bd, c2, mode=B.MODE_FAST)
+    assert B.biv_gemm_workspace(d) == 0
+    B.biv_gemm(d)
+    assert np.array_equal(bits(c1), bits(c2))
