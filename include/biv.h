@@ -154,10 +154,11 @@ biv_status biv_kv_fp8_gather(const uint8_t* codes, const float* scales,
  * attends to keys at positions <= row_pos[t] of its sequence, read from the
  * paged cache through block_table.  Keys are visited in 64-token tiles aligned
  * to absolute positions, grouped into splits of kv_split tokens (a model
- * constant); each split keeps an online softmax (FP32), P is rounded to bf16
- * for P.V, and the splits are merged in ascending order in FP32.  With
- * topk_idx != NULL (sparse attention) the keys of row t are the positions
- * topk_idx[t, 0..topk) (ascending, -1 = none) and splits run over that list.
+ * constant); each split keeps an online softmax (FP32), P enters P.V as a
+ * bf16 hi + lo pair (about 16 significant bits), and the splits are merged
+ * in ascending order in FP32.  With topk_idx != NULL (sparse attention) the
+ * keys of row t are the positions topk_idx[t, 0..topk) (ascending, -1 =
+ * none) and splits run over that list.
  * qblocks int32 [nqblocks, 2] = (first row, row count): rows of a block must
  * belong to one sequence (sparse: one row per block).  The grouping into
  * blocks does not change any result bit.  Output bf16 [T, Hq, D]. */

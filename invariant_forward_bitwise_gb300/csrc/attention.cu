@@ -6,8 +6,9 @@
 // KV split.  Its 64 query vectors are (row, q-head-of-the-group) pairs, 16 per
 // warp.  Keys are visited in 64-token tiles aligned to absolute positions (one
 // cache page), inside splits of kv_split tokens.  Per vector and split:
-// online softmax in FP32 (exp2 domain), P rounded to bf16 for P.V, the
-// denominator summed from the same rounded P.  Splits are merged in ascending
+// online softmax in FP32 (exp2 domain), P split into a bf16 hi + lo pair
+// for P.V (two MMAs into one FP32 accumulator), the denominator summed from
+// the FP32 P.  Splits are merged in ascending
 // order.  A vector's arithmetic is the same whatever other rows share its CTA:
 // tiles past its own position are fully masked and leave (m, l, acc) bitwise
 // unchanged, and masked slots are zero in shared memory.
@@ -285,21 +286,27 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
       alpha[i] = (mn == -INFINITY) ? 1.f : exp2f(m[i] - mn);
       m[i] = mn;
     }
-    uint32_t pf[4][4];  // P as bf16 A fragments, 4 k-steps of 16 keys
+    // P as two bf16 A fragments per k-step: P = hi + lo, hi = bf16(p),
+    // lo = bf16(p - hi), so P.V carries ~16 significant bits of p while V stays
+    // exact bf16.  The denominator sums the FP32 p.
+    uint32_t pf[4][4], pl[4][4];
     float rs[2] = {0.f, 0.f};
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      float p[4];
+      float ph[4], plo[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = e >> 1;
         const float pe = (m[i] == -INFINITY) ? 0.f : exp2f(s[nt][e] - m[i]);
-        p[e] = bf2f(f2bf(pe));
-        rs[i] += p[e];
+        ph[e] = bf2f(f2bf(pe));
+        plo[e] = pe - ph[e];
+        rs[i] += pe;
       }
       const int ks = nt >> 1, hi2 = nt & 1;
-      pf[ks][hi2 * 2 + 0] = pack_bf2(p[0], p[1]);
-      pf[ks][hi2 * 2 + 1] = pack_bf2(p[2], p[3]);
+      pf[ks][hi2 * 2 + 0] = pack_bf2(ph[0], ph[1]);
+      pf[ks][hi2 * 2 + 1] = pack_bf2(ph[2], ph[3]);
+      pl[ks][hi2 * 2 + 0] = pack_bf2(plo[0], plo[1]);
+      pl[ks][hi2 * 2 + 1] = pack_bf2(plo[2], plo[3]);
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -319,6 +326,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
     for (int ks = 0; ks < 4; ++ks) {
       // A fragment order: (row g, k 0-7), (row g+8, k 0-7), (row g, k 8-15), (row g+8, k 8-15)
       const uint32_t af[4] = {pf[ks][0], pf[ks][1], pf[ks][2], pf[ks][3]};
+      const uint32_t al[4] = {pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3]};
 #pragma unroll
       for (int dp = 0; dp < Cfg::DT / 2; ++dp) {
         uint32_t b0, b1, b2, b3;
@@ -327,6 +335,8 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
         ldsm_x4_t(smem_u32(tV + key * LD + dim), b0, b1, b2, b3);
         mma_bf16(acc[2 * dp], af, b0, b1);
         mma_bf16(acc[2 * dp + 1], af, b2, b3);
+        mma_bf16(acc[2 * dp], al, b0, b1);
+        mma_bf16(acc[2 * dp + 1], al, b2, b3);
       }
     }
     __syncthreads();
