@@ -194,6 +194,21 @@ biv_status biv_attention_workspace(const biv_attn_desc* desc, size_t* bytes);
 biv_status biv_attention(const biv_attn_desc* desc, void* workspace, size_t workspace_bytes,
                          biv_stream_t stream);
 
+/* Allocation-free variant of biv_attention (the paper has no counterpart: it
+ * exists for callers that cannot call cudaMalloc, e.g. code running inside
+ * another runtime's memory budget or a hook that must not allocate).  Same
+ * arguments and results as biv_attention, but the split partials go to a
+ * fixed 64 MiB device array inside the library instead of a caller
+ * workspace.  Every GPU that loads the library holds that array until the
+ * process exits.  The first call on a device looks the array's address up
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  A call whose scratch need (biv_attention_workspace)
+ * exceeds 64 MiB returns BIV_ERR_WORKSPACE and launches nothing.  All calls
+ * share the one array: calls whose work can overlap on the GPU (different
+ * streams, no ordering between them) race and must not be issued.  Nothing
+ * in the array needs to start at zero. */
+biv_status biv_attention_noalloc(const biv_attn_desc* desc, biv_stream_t stream);
+
 /* ---------------------------------------------------------------- GEMM --
  * C[M, N] = A[M, K] . B[N, K]^T on the tcgen05 tensor cores, FP32
  * accumulation in TMEM ("Finish RL Training Faster", section

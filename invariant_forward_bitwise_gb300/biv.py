@@ -22,7 +22,7 @@ EXPORTS = [
     "biv_version", "biv_last_error", "biv_device_sm_count", "biv_poll_error",
     "biv_selftest_timeout", "biv_embed", "biv_add_rmsnorm", "biv_silu_mul", "biv_rope_table",
     "biv_qk_norm_rope", "biv_kv_store_bf16", "biv_kv_fp8_quant", "biv_kv_fp8_gather",
-    "biv_attention_workspace", "biv_attention", "biv_gemm_workspace", "biv_gemm",
+    "biv_attention_workspace", "biv_attention", "biv_attention_noalloc", "biv_gemm_workspace", "biv_gemm",
     "biv_act_quant_fp8", "biv_topk", "biv_router_topk", "biv_moe_dispatch", "biv_gather_rows",
     "biv_moe_combine", "biv_logprob", "biv_ssd_scan",
 ]
@@ -103,6 +103,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "biv_kv_fp8_quant": ([P, P, I64, P, I, I, I, P, P, P, P, P], I),
         "biv_kv_fp8_gather": ([P, P, P, I, P, P, I, I, I, I, P, P], I),
         "biv_attention_workspace": ([P, P], I), "biv_attention": ([P, P, C.c_size_t, P], I),
+        "biv_attention_noalloc": ([P, P], I),
         "biv_gemm_workspace": ([P, P], I), "biv_gemm": ([P, P, C.c_size_t, P], I),
         "biv_act_quant_fp8": ([P, I64, I, I, P, P, P], I),
         "biv_topk": ([P, I64, P, I, I, I, P, P], I),
@@ -232,6 +233,11 @@ def biv_attention_workspace(desc: AttnDesc) -> int:
 def biv_attention(desc: AttnDesc, ws: Optional[torch.Tensor], stream=None):
     _check(load().biv_attention(C.byref(desc), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                 _stream(stream)), "biv_attention")
+
+
+def biv_attention_noalloc(desc: AttnDesc, stream=None):
+    """biv_attention without a caller workspace (see include/biv.h)."""
+    _check(load().biv_attention_noalloc(C.byref(desc), _stream(stream)), "biv_attention_noalloc")
 
 
 def gemm_desc(A, B, Cout, mode=MODE_INVARIANT, sa=None, sb=None, group_offsets=None, groups=0,

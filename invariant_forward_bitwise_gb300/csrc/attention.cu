@@ -13,6 +13,7 @@
 // tiles past its own position are fully masked and leave (m, l, acc) bitwise
 // unchanged, and masked slots are zero in shared memory.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -525,3 +526,61 @@ biv_status biv_attention(const biv_attn_desc* d, void* ws, size_t wsb, biv_strea
 }
 
 }  // extern "C"
+
+// --------------------------------------------------------------------------
+// Allocation-free attention.  Some callers cannot call cudaMalloc at all: a
+// host process that runs under a memory-budget sandbox, an inference server
+// whose allocator is owned by another runtime, or a driver-level hook that
+// must not allocate while the caller holds a lock.  For them the split
+// partials live in one fixed device array that the library owns.  It is
+// reserved on every GPU that loads the library and held until the process
+// exits.
+namespace biv {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB per device
+static __device__ __align__(256) uint8_t g_attn_noalloc_scratch[kNoAllocScratchBytes];
+
+// The host cannot use the array's name as a device address: it is looked up
+// once per device, with that device current.
+void* noalloc_scratch_ptr(biv_status* st) {
+  static std::mutex mu;
+  static void* ptr[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *st = set_error(BIV_ERR_CUDA, "attention_noalloc: no current CUDA device");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      *st = set_error(BIV_ERR_CUDA, "attention_noalloc: cudaGetSymbolAddress failed: %s",
+                      cudaGetErrorString(e));
+      return nullptr;
+    }
+    ptr[dev] = p;
+  }
+  *st = BIV_OK;
+  return ptr[dev];
+}
+
+}  // namespace
+}  // namespace biv
+
+extern "C" biv_status biv_attention_noalloc(const biv_attn_desc* d, biv_stream_t stream) {
+  biv_status st = validate(d);
+  if (st != BIV_OK) return st;
+  const size_t need = ws_bytes(*d, plan_split(*d));
+  if (need > kNoAllocScratchBytes)
+    return set_error(BIV_ERR_WORKSPACE,
+                     "attention_noalloc: this call needs %zu bytes of scratch, above the fixed "
+                     "%zu-byte array; use biv_attention with a caller workspace",
+                     need, kNoAllocScratchBytes);
+  void* scratch = noalloc_scratch_ptr(&st);
+  if (st != BIV_OK) return st;
+  // Every slot of the partials that the merge reads is written earlier in the
+  // same call, so nothing in the array has to start at zero.
+  return biv_attention(d, scratch, kNoAllocScratchBytes, stream);
+}
