@@ -188,6 +188,8 @@ typedef struct {
   int topk;
   float scale;              /* softmax scale, usually 1/sqrt(D) */
   int mode;                 /* biv_mode; FAST picks kv_split from the batch */
+  int num_pages;            /* pages the cache arrays hold (bf16 caches: lets the
+                               kernel fetch whole pages by TMA); 0 = unknown */
 } biv_attn_desc;
 
 biv_status biv_attention_workspace(const biv_attn_desc* desc, size_t* bytes);

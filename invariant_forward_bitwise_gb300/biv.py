@@ -59,7 +59,7 @@ class AttnDesc(C.Structure):
                 ("block_table", C.c_void_p), ("max_pages", C.c_int),
                 ("page", C.c_int), ("kv_split", C.c_int), ("max_ctx", C.c_int),
                 ("topk_idx", C.c_void_p), ("topk_stride", C.c_int64), ("topk", C.c_int),
-                ("scale", C.c_float), ("mode", C.c_int)]
+                ("scale", C.c_float), ("mode", C.c_int), ("num_pages", C.c_int)]
 
 
 class SSDDesc(C.Structure):

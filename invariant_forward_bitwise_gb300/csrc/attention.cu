@@ -3,16 +3,23 @@
 // every path gathers, dequantises and enters the same attention operator).
 //
 // A CTA handles one query block (rows of one sequence), one KV head and one
-// KV split.  Its 64 query vectors are (row, q-head-of-the-group) pairs, 16 per
+// KV split.  Its query vectors are (row, q-head-of-the-group) pairs, 16 per
 // warp.  Keys are visited in 64-token tiles aligned to absolute positions (one
 // cache page), inside splits of kv_split tokens.  Per vector and split:
-// online softmax in FP32 (exp2 domain), P split into a bf16 hi + lo pair
-// for P.V (two MMAs into one FP32 accumulator), the denominator summed from
-// the FP32 P.  Splits are merged in ascending
-// order.  A vector's arithmetic is the same whatever other rows share its CTA:
-// tiles past its own position are fully masked and leave (m, l, acc) bitwise
-// unchanged, and masked slots are zero in shared memory.
+// online softmax in FP32 (exp2 domain), P split into a bf16 hi + lo pair for
+// P.V (two MMAs into one FP32 accumulator), the denominator summed from the
+// FP32 P.  Splits are merged in ascending order.  A vector's arithmetic is the
+// same whatever other rows share its CTA and whatever the CTA shape: each warp
+// runs one instruction sequence for its 16 vectors, tiles past a vector's own
+// position are fully masked and leave (m, l, acc) bitwise unchanged, and
+// masked V slots are zero in shared memory.
+//
+// Loads: dense bf16 pages (D = 64 or 128) arrive by TMA, one 2-D bulk copy
+// per 64-dim half of K and V, 128-byte swizzled, completed on an mbarrier;
+// FP8 pages (dequantised on the way in), sparse gathers and D = 80 use
+// cp.async / plain loads into padded rows.
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -21,17 +28,30 @@ namespace biv {
 namespace {
 
 constexpr int kTile = 64;   // keys per tile = one page
-constexpr int kNV = 64;     // query vectors per CTA (4 warps x 16)
+constexpr int kNV = 64;     // most query vectors a CTA takes (4 warps x 16)
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+// NW warps per CTA (16 query vectors each), ST-stage K/V pipeline, TMA or
+// thread-issued loads.  Decode blocks (<= 16 vectors) run NW = 1, ST = 3;
+// prefill blocks NW = 4, ST = 2.
+template <int D, int NW, int ST, bool TMA>
 struct AttnCfg {
-  static constexpr int LD = D + 8;                   // padded smem row (elements)
-  static constexpr int Q_BYTES = kNV * LD * 2;
-  static constexpr int KV_BYTES = kTile * LD * 2;
-  static constexpr int SMEM = Q_BYTES + 4 * KV_BYTES + kTile * 4 * 2;
+  static constexpr int LD = D + 8;                   // padded row (elements), thread-loaded tiles
+  static constexpr int NV = NW * 16;                 // query vectors per CTA
+  static constexpr int NT = NW * 32;                 // threads per CTA
+  static constexpr int KVB = TMA ? kTile * D * 2 : kTile * LD * 2;  // one K or V stage
+  static constexpr int Q_BYTES = NV * LD * 2;
+  static constexpr int SMEM = 1024 + 2 * ST * KVB + Q_BYTES + ST * kTile * 4 + ST * 8;
   static constexpr int DK = D / 16;                  // k-steps of Q.K^T
   static constexpr int DT = D / 8;                   // n-tiles of O
+  // byte offset of (row, dim) inside a K/V stage (dim a multiple of 8)
+  __device__ static __forceinline__ uint32_t off(int row, int dim) {
+    if (TMA) {
+      const int c = (dim & 63) >> 3;
+      return uint32_t((dim >> 6) * 8192 + row * 128 + ((c ^ (row & 7)) << 4));
+    }
+    return uint32_t((row * LD + dim) * 2);
+  }
 };
 
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -66,6 +86,7 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 struct AttnArgs {
+  CUtensorMap tmK, tmV;      // bf16 caches as [pages*64, Hkv*D] (TMA path only)
   const uint16_t* q; int64_t q_stride;
   uint16_t* out; int64_t out_stride;
   int T, Hq, Hkv, G;
@@ -87,15 +108,18 @@ __device__ __forceinline__ int row_splits(const AttnArgs& a, int pos) {
   return a.topk_idx ? (a.topk + a.kv_split - 1) / a.kv_split : pos / a.kv_split + 1;
 }
 
-template <int D>
-__global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
-  using Cfg = AttnCfg<D>;
-  constexpr int LD = Cfg::LD;
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* sQ = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* sK = reinterpret_cast<uint16_t*>(smem + Cfg::Q_BYTES);          // [2][64][LD]
-  uint16_t* sV = sK + 2 * kTile * LD;                                        // [2][64][LD]
-  int32_t* sPos = reinterpret_cast<int32_t*>(sV + 2 * kTile * LD);          // [2][64]
+template <int D, int NW, int ST, bool TMA>
+__global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ AttnArgs a) {
+  using Cfg = AttnCfg<D, NW, ST, TMA>;
+  constexpr int LD = Cfg::LD, NV = Cfg::NV, NT = Cfg::NT, KVB = Cfg::KVB;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sK = base;                                   // [ST] stages of KVB bytes
+  uint8_t* sV = base + ST * KVB;
+  uint16_t* sQ = reinterpret_cast<uint16_t*>(base + 2 * ST * KVB);
+  int32_t* sPos = reinterpret_cast<int32_t*>(base + 2 * ST * KVB + Cfg::Q_BYTES);  // [ST][64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sPos + ST * kTile);                 // [ST]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int blk = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
@@ -108,22 +132,21 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   int maxpos = -1;
   for (int r = 0; r < nr; ++r) maxpos = max(maxpos, a.row_pos[r0 + r]);
 
-  // key range of this split
-  int lo, hi;  // [lo, hi) in positions (dense) or list indices (sparse)
-  if (sparse) {
-    lo = split * a.kv_split;
-    hi = min(a.topk, lo + a.kv_split);
-  } else {
-    lo = split * a.kv_split;
-    hi = min(maxpos + 1, lo + a.kv_split);
-  }
+  // key range of this split: [lo, hi) in positions (dense) or list indices (sparse)
+  const int lo = split * a.kv_split;
+  const int hi = sparse ? min(a.topk, lo + a.kv_split) : min(maxpos + 1, lo + a.kv_split);
   if (lo >= hi) return;  // uniform: nothing of this block lives in this split
   const int ntiles = (hi - lo + kTile - 1) / kTile;
+
+  if (TMA && tid == 0) {
+    for (int s = 0; s < ST; ++s) mbar_init(smem_u32(bars + s), 1);
+    fence_barrier_init();
+  }
 
   // ---- load Q (zero for vectors past nv)
   {
     constexpr int CPR = D / 8;  // 16-byte chunks per vector
-    for (int i = tid; i < kNV * CPR; i += 128) {
+    for (int i = tid; i < NV * CPR; i += NT) {
       const int v = i / CPR, c = i % CPR;
       uint4 val = make_uint4(0, 0, 0, 0);
       if (v < nv) {
@@ -138,25 +161,39 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   // ---- tile loader (dense: the page of absolute tile t; sparse: listed keys)
   const int64_t kv_row = int64_t(a.Hkv) * D;  // elements between consecutive cache slots
   auto load_tile = [&](int buf, int t) {
-    const int base = lo + t * kTile;
+    const int tbase = lo + t * kTile;
+    if (TMA) {
+      if (tid == 0) {
+        const uint32_t bar = smem_u32(bars + buf);
+        const int page = a.bt[int64_t(seq) * a.max_pages + tbase / kTile];
+        fence_proxy_async();  // earlier generic accesses to this stage come first
+        mbar_expect_tx(bar, 2 * KVB);
+#pragma unroll
+        for (int hh = 0; hh < D / 64; ++hh) {
+          tma_load_2d(smem_u32(sK + buf * KVB + hh * 8192), &a.tmK, bar, h * D + hh * 64, page * kTile);
+          tma_load_2d(smem_u32(sV + buf * KVB + hh * 8192), &a.tmV, bar, h * D + hh * 64, page * kTile);
+        }
+      }
+      return;
+    }
     int32_t* pos_buf = sPos + buf * kTile;
-    if (tid < kTile) {
+    for (int j = tid; j < kTile; j += NT) {
       int p;
       if (sparse) {
-        const int li = base + tid;
+        const int li = tbase + j;
         p = li < hi ? a.topk_idx[int64_t(r0) * a.topk_stride + li] : -1;
       } else {
-        p = base + tid;
+        p = tbase + j;
         if (p >= hi) p = -1;
       }
-      pos_buf[tid] = p;
+      pos_buf[j] = p;
     }
     __syncthreads();
-    uint16_t* dK = sK + buf * kTile * LD;
-    uint16_t* dV = sV + buf * kTile * LD;
+    uint8_t* dK = sK + buf * KVB;
+    uint8_t* dV = sV + buf * KVB;
     if (!a.fp8) {
       constexpr int CPR = D / 8;
-      for (int i = tid; i < kTile * CPR * 2; i += 128) {
+      for (int i = tid; i < kTile * CPR * 2; i += NT) {
         const int which = i / (kTile * CPR);
         const int rem = i % (kTile * CPR);
         const int j = rem / CPR, c = rem % CPR;
@@ -167,11 +204,11 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
           const int64_t slot = int64_t(a.bt[int64_t(seq) * a.max_pages + p / kTile]) * kTile + p % kTile;
           gp = src + slot * kv_row + int64_t(h) * D + c * 8;
         }
-        cp_async16(smem_u32((which ? dV : dK) + j * LD + c * 8), gp, p >= 0);
+        cp_async16(smem_u32((which ? dV : dK) + Cfg::off(j, c * 8)), gp, p >= 0);
       }
     } else {
       constexpr int CPR = D / 16;  // 16 codes per chunk
-      for (int i = tid; i < kTile * CPR * 2; i += 128) {
+      for (int i = tid; i < kTile * CPR * 2; i += NT) {
         const int which = i / (kTile * CPR);
         const int rem = i % (kTile * CPR);
         const int j = rem / CPR, c = rem % CPR;
@@ -196,9 +233,9 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
           o0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
           o1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
         }
-        uint16_t* dst = (which ? dV : dK) + j * LD + c * 16;
-        reinterpret_cast<uint4*>(dst)[0] = o0;
-        reinterpret_cast<uint4*>(dst)[1] = o1;
+        uint8_t* dst = (which ? dV : dK);
+        *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16)) = o0;
+        *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16 + 8)) = o1;
       }
     }
   };
@@ -217,9 +254,13 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
 #pragma unroll
   for (int i = 0; i < Cfg::DT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-  load_tile(0, 0);
-  cp_async_commit();
-  __syncthreads();
+  __syncthreads();  // Q stored, barriers initialised
+  // prologue: tiles 0 .. ST-2 in flight (one cp.async group each, even if empty)
+#pragma unroll
+  for (int s0 = 0; s0 < ST - 1; ++s0) {
+    if (s0 < ntiles) load_tile(s0, s0);
+    if (!TMA) cp_async_commit();
+  }
 
   // Q fragments (A operand), loaded once
   uint32_t qf[Cfg::DK][4];
@@ -231,22 +272,33 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   }
 
   for (int t = 0; t < ntiles; ++t) {
-    const int buf = t & 1;
-    if (t + 1 < ntiles) {
-      load_tile(buf ^ 1, t + 1);
-      cp_async_commit();
-      cp_async_wait<1>();
+    const int buf = t % ST;
+    const int tbase = lo + t * kTile;
+    if (TMA) {
+      mbar_wait(smem_u32(bars + buf), (t / ST) & 1, a.err);
+      // slots past the split's end in its last page hold no key of this
+      // sequence: zero their V rows (P is 0 there, and 0 * stale must be 0)
+      const int first_bad = hi - tbase;
+      if (first_bad < kTile) {
+        for (int i = tid; i < (kTile - first_bad) * (D / 8); i += NT) {
+          const int j = first_bad + i / (D / 8), c = i % (D / 8);
+          *reinterpret_cast<uint4*>(sV + buf * KVB + Cfg::off(j, c * 8)) = make_uint4(0, 0, 0, 0);
+        }
+      }
     } else {
-      cp_async_wait<0>();
+      cp_async_wait<ST - 2>();  // tile t has landed
     }
     __syncthreads();
-    const uint16_t* tK = sK + buf * kTile * LD;
-    const uint16_t* tV = sV + buf * kTile * LD;
-    const int32_t* tP = sPos + buf * kTile;
+    // refill the stage that tile t-1 used (its compute ended at the last sync)
+    if (t + ST - 1 < ntiles) load_tile((t + ST - 1) % ST, t + ST - 1);
+    if (!TMA) cp_async_commit();
     if (warp * 16 >= nv) {  // no live vector in this warp: only help with loads
       __syncthreads();
       continue;
     }
+    const uint32_t tK = smem_u32(sK + buf * KVB);
+    const uint32_t tV = smem_u32(sV + buf * KVB);
+    const int32_t* tP = sPos + buf * kTile;
 
     // S = Q . K^T  (16 x 64 per warp)
     float s[8][4];
@@ -259,7 +311,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
         uint32_t b0, b1, b2, b3;
         const int key = np * 16 + (lane & 7) + (lane >> 4) * 8;
         const int dim = kk * 16 + ((lane >> 3) & 1) * 8;
-        ldsm_x4(smem_u32(tK + key * LD + dim), b0, b1, b2, b3);
+        ldsm_x4(tK + Cfg::off(key, dim), b0, b1, b2, b3);
         mma_bf16(s[2 * np], qf[kk], b0, b1);
         mma_bf16(s[2 * np + 1], qf[kk], b2, b3);
       }
@@ -271,7 +323,8 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = e >> 1;
-        const int kp = tP[nt * 8 + 2 * cq + (e & 1)];
+        const int col = nt * 8 + 2 * cq + (e & 1);
+        const int kp = sparse ? tP[col] : (tbase + col < hi ? tbase + col : -1);
         const bool vis = kp >= 0 && kp <= vpos[i];
         const float x = vis ? s[nt][e] * a.scale_log2 : -INFINITY;
         s[nt][e] = x;
@@ -333,7 +386,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
         uint32_t b0, b1, b2, b3;
         const int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
         const int dim = dp * 16 + (lane >> 4) * 8;
-        ldsm_x4_t(smem_u32(tV + key * LD + dim), b0, b1, b2, b3);
+        ldsm_x4_t(tV + Cfg::off(key, dim), b0, b1, b2, b3);
         mma_bf16(acc[2 * dp], af, b0, b1);
         mma_bf16(acc[2 * dp + 1], af, b2, b3);
         mma_bf16(acc[2 * dp], al, b0, b1);
@@ -378,7 +431,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
 // Merge the splits of rows that have more than one, in ascending split order:
 // w_s = 2^(m_s - M), O = sum w_s o_s, L = sum w_s l_s, out = O / L.
 template <int D>
-__global__ void attn_merge_kernel(const AttnArgs a) {
+__global__ void attn_merge_kernel(const __grid_constant__ AttnArgs a) {
   const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= int64_t(a.T) * a.Hq) return;
@@ -452,19 +505,49 @@ size_t ws_bytes(const biv_attn_desc& d, int split) {
   return size_t(d.T) * d.Hq * ns * (d.D + 2) * sizeof(float);
 }
 
-template <int D>
-biv_status launch(const biv_attn_desc& d, const AttnArgs& a, cudaStream_t s) {
-  using Cfg = AttnCfg<D>;
+template <int D, int NW, int ST, bool TMA>
+biv_status launch_cfg(const biv_attn_desc& d, const AttnArgs& a, cudaStream_t s) {
+  using Cfg = AttnCfg<D, NW, ST, TMA>;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_kernel<D, NW, ST, TMA>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
       return set_error(BIV_ERR_CUDA, "attention: cannot set shared memory size");
     attr = true;
   }
   dim3 grid(d.nqblocks, d.Hkv, a.nsplit_grid);
-  attn_kernel<D><<<grid, 128, Cfg::SMEM, s>>>(a);
-  biv_status st = check_launch("attention");
+  attn_kernel<D, NW, ST, TMA><<<grid, Cfg::NT, Cfg::SMEM, s>>>(a);
+  return check_launch("attention");
+}
+
+// bf16 cache of one layer as a 2-D tensor [num_pages*64 slots, Hkv*D], boxes of
+// 64 slots x 64 dims (128 bytes, 128-byte swizzle)
+bool make_kv_map(CUtensorMap* m, const void* base, int num_pages, int Hkv, int D) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cuuint64_t(Hkv) * D, cuuint64_t(num_pages) * kTile};
+  cuuint64_t strides[1] = {cuuint64_t(Hkv) * D * 2};
+  cuuint32_t box[2] = {64, kTile};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
+  // The CTA shape and the loader follow the call; a vector's arithmetic does not.
+  const bool small = d.max_rows_per_block * a.G <= 16;
+  biv_status st;
+  bool tma = false;
+  if constexpr (D % 64 == 0) {
+    tma = !a.fp8 && !a.topk_idx && d.num_pages > 0 &&
+          make_kv_map(&a.tmK, d.k_cache, d.num_pages, d.Hkv, D) &&
+          make_kv_map(&a.tmV, d.v_cache, d.num_pages, d.Hkv, D);
+    if (tma)
+      st = small ? launch_cfg<D, 1, 3, true>(d, a, s) : launch_cfg<D, 4, 2, true>(d, a, s);
+  }
+  if (!tma) st = small ? launch_cfg<D, 1, 3, false>(d, a, s) : launch_cfg<D, 4, 2, false>(d, a, s);
   if (st != BIV_OK || a.nsplit_grid <= 1) return st;
   const int64_t warps = int64_t(d.T) * d.Hq;
   attn_merge_kernel<D><<<unsigned((warps * 32 + 255) / 256), 256, 0, s>>>(a);
@@ -502,6 +585,7 @@ biv_status biv_attention(const biv_attn_desc* d, void* ws, size_t wsb, biv_strea
     return set_error(BIV_ERR_WORKSPACE, "attention: workspace of %zu bytes needed", need);
   const int span = d->topk_idx ? d->topk : d->max_ctx;
   AttnArgs a;
+  memset(&a, 0, sizeof(a));
   a.q = d->q; a.q_stride = d->q_stride;
   a.out = d->out; a.out_stride = d->out_stride;
   a.T = d->T; a.Hq = d->Hq; a.Hkv = d->Hkv; a.G = d->Hq / d->Hkv;

@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include <cstdarg>
@@ -25,6 +26,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 int sm_count();
 // device error word: bounded waits that give up set it (never trap)
 int* device_error_word();
+// the driver's cuTensorMapEncodeTiled, resolved once at run time (nullptr if absent)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 #define BIV_REQUIRE(cond, ...)                                   \
   do {                                                           \

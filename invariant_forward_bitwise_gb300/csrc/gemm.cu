@@ -495,24 +495,10 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ------------------------------------------------------------------- host --
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // 2-D K-major tensor map: dims {K, rows}, box {box_k, box_rows}, 128B swizzle.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
               int64_t K, int64_t rows, int64_t ld, int box_k, int box_rows) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
   cuuint64_t strides[1] = {cuuint64_t(ld * elem_bytes)};
@@ -545,10 +531,15 @@ Plan plan_bf16(const biv_gemm_desc& d) {
   const int KB = (d.K + 63) / 64;
   p.bn = d.N >= 8192 ? 256 : (d.N >= 128 ? 128 : (d.N > 32 ? 64 : 32));
   p.kb_per_split = KB;
-  // Many tiles: persistent kernel (identical per-element schedule, so this
-  // choice may depend on M without touching any result bit).
+  // The tile width (MMA instruction N) and the one-tile vs persistent kernel
+  // do not change any element's K schedule, and tcgen05 gives the same bits
+  // for every instruction N, so both may follow M.  Enough 128x256 tiles to
+  // fill the GPU: the widest tile on the persistent kernel (least shared-memory
+  // traffic per FLOP).
   const int sms = sm_count() > 0 ? sm_count() : 148;
-  const int64_t tiles = int64_t((d.N + p.bn - 1) / p.bn) * ((d.M + BM - 1) / BM);
+  const int64_t mt = (d.M + BM - 1) / BM;
+  if (d.N >= 256 && int64_t((d.N + 255) / 256) * mt >= sms) p.bn = 256;
+  const int64_t tiles = int64_t((d.N + p.bn - 1) / p.bn) * mt;
   p.persistent = tiles >= 2 * sms && persistent_allowed();
   if (d.mode == BIV_MODE_FAST && d.M <= 256) {
     p.persistent = false;

@@ -168,6 +168,7 @@ class DenseModel:
         d.page, d.kv_split, d.max_ctx = PAGE, cfg.kv_split, spec.max_ctx
         d.scale = 1.0 / math.sqrt(cfg.head_dim)
         d.mode = self.mode
+        d.num_pages = kv.pages
         return d
 
     def reserve(self, kv: PagedKV, specs: Sequence[StepSpec]):
@@ -237,10 +238,17 @@ class DenseModel:
             if tok:
                 t.close(tok)
             self._gemm(self.o, W[p + "wo"], self.a, T)
+            aud = self.audit is not None and not torch.cuda.is_current_stream_capturing()
+            if aud:
+                self.audit.append(("qkv", l, self.qkv[:T].clone()))
+                self.audit.append(("attn_o", l, self.o[:T].clone()))
+                self.audit.append(("attn_proj", l, self.a[:T].clone()))
             biv.biv_add_rmsnorm(self.a[:T], r, W[p + "mlp_norm"], y, eps)
             self._gemm(y, W[p + "wgu"], self.gu, T)
             biv.biv_silu_mul(self.gu[:T], self.act[:T])
             self._gemm(self.act, W[p + "wd"], self.a, T)
+            if self.audit is not None and not torch.cuda.is_current_stream_capturing():
+                self.audit.append(("mlp_out", l, self.a[:T].clone()))
             nxt = W[f"l{l + 1}.attn_norm"] if l + 1 < cfg.layers else W["final_norm"]
             biv.biv_add_rmsnorm(self.a[:T], r, nxt, y, eps)
             self.launches += 6 + (2 if need else 1)

@@ -59,7 +59,13 @@ class DenseOracle:
         kp = np.concatenate([kp, pos]) if kp is not None else pos
         kv[l] = (kc, vc, kp)
         o = ops.attention(q, kc, vc, pos, kp, self.scale)
-        return ops.gemm(o.reshape(T, Hq * D), W[p + "wo"])
+        a = ops.gemm(o.reshape(T, Hq * D), W[p + "wo"])
+        if self.audit is not None:
+            qk = np.concatenate([q.reshape(T, -1), k.reshape(T, -1), v.reshape(T, -1)], 1)
+            self.audit.append(("qkv", l, qk))
+            self.audit.append(("attn_o", l, o.reshape(T, Hq * D)))
+            self.audit.append(("attn_proj", l, a))
+        return a
 
     def forward_rows(self, tokens: np.ndarray, pos: np.ndarray, kv: list) -> np.ndarray:
         """Run rows (one sequence, consecutive positions) through the model,
@@ -72,11 +78,31 @@ class DenseOracle:
             r, y = ops.add_rmsnorm(a, r, W[f"l{l}.mlp_norm"], cfg.eps)
             gu = ops.gemm(y, W[f"l{l}.wgu"])
             m = ops.gemm(ops.silu_mul(gu), W[f"l{l}.wd"])
+            if self.audit is not None:
+                self.audit.append(("mlp_out", l, m))
             nxt = W[f"l{l + 1}.attn_norm"] if l + 1 < cfg.layers else W["final_norm"]
             r, y = ops.add_rmsnorm(m, r, nxt, cfg.eps)
             if self.audit is not None:
                 self.audit.append(("layer", l, r.copy()))
         return ops.gemm(y, W["lm_head"], out="f32")
+
+    def layer_from(self, l: int, r_prev: np.ndarray, pos: np.ndarray) -> np.ndarray:
+        """One decoder layer on its own: from the residual stream entering layer
+        l (all positions of one sequence, a full prefill), the residual leaving
+        it.  Used to check each layer of a long model against its own input."""
+        cfg, W = self.cfg, self.W
+        kv = self.new_cache()
+        y = ops.rmsnorm(r_prev, W[f"l{l}.attn_norm"], cfg.eps)
+        a = self._attn_block(l, y, pos, kv)
+        r, y = ops.add_rmsnorm(a, r_prev, W[f"l{l}.mlp_norm"], cfg.eps)
+        gu = ops.gemm(y, W[f"l{l}.wgu"])
+        m = ops.gemm(ops.silu_mul(gu), W[f"l{l}.wd"])
+        return ops.bf16_round(m + r)
+
+    def head_from(self, r_last: np.ndarray, targets: np.ndarray) -> np.ndarray:
+        """Final norm, LM head and logprob from the last layer's residual."""
+        y = ops.rmsnorm(r_last, self.W["final_norm"], self.cfg.eps)
+        return ops.logprob(ops.gemm(y, self.W["lm_head"], out="f32"), targets)
 
     def new_cache(self) -> list:
         return [(None, None, None) for _ in range(self.cfg.layers)]

@@ -85,7 +85,7 @@ class Paged:
         return k, v
 
 
-def run_attn(B, pc, q, rows, blocks, Hq, kv_split=1024, mode=0, topk_idx=None, topk=0):
+def run_attn(B, pc, q, rows, blocks, Hq, kv_split=1024, mode=0, topk_idx=None, topk=0, tma=True):
     """rows: list of (seq, pos); blocks: list of (first row, count)."""
     T = len(rows)
     D = pc.D
@@ -111,6 +111,7 @@ def run_attn(B, pc, q, rows, blocks, Hq, kv_split=1024, mode=0, topk_idx=None, t
         d.topk_idx, d.topk_stride, d.topk = topk_idx.data_ptr(), topk_idx.stride(0), topk
     d.scale = 1.0 / math.sqrt(D)
     d.mode = mode
+    d.num_pages = pc.kc.shape[0] if tma else 0
     n = B.biv_attention_workspace(d)
     ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda") if n else None
     B.biv_attention(d, ws)
@@ -199,3 +200,21 @@ def test_sparse_topk_attention(B):
                         topk_idx=torch.from_numpy(np.where(full <= 200, full, -1)).cuda(), topk=topk)
     o_dense = run_attn(B, pc, q[:1], rows2, [(0, 1)], Hq, kv_split=128)
     assert rel_err(host_f32(o_sparse), host_f32(o_dense)) < 1e-2
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_tma_loader_equals_thread_loader(B, D):
+    """Whole-page TMA loads and thread-issued loads feed the same arithmetic."""
+    g = synth.rng(50 + D)
+    lens = [200, 77]
+    pc = Paged(B, g, lens, 2, D)
+    rows = [(i, p) for i, L in enumerate(lens) for p in range(L)]
+    q = synth.normal_bf16(g, (len(rows), 4 * D)).cuda()
+    blocks = blocks_of(rows, 32)
+    a = run_attn(B, pc, q, rows, blocks, 4, kv_split=128, tma=True)
+    b = run_attn(B, pc, q, rows, blocks, 4, kv_split=128, tma=False)
+    assert np.array_equal(bits(a), bits(b))
+    last = [sum(lens[:i + 1]) - 1 for i in range(len(lens))]
+    dec = run_attn(B, pc, q[torch.tensor(last, device="cuda")], [rows[j] for j in last],
+                   [(j, 1) for j in range(len(last))], 4, kv_split=128, tma=True)
+    assert np.array_equal(bits(dec), bits(a[torch.tensor(last, device="cuda")]))

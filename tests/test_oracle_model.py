@@ -81,3 +81,21 @@ def test_planted_rope_sign_error_is_caught(monkeypatch):
 
     assert rel_gap(ops.rope) < 0.05 * np.abs(q).sum() * np.abs(k).max()
     assert rel_gap(bad_rope) > rel_gap(ops.rope) * 10
+
+
+def test_layer_by_layer_entry_points_chain_to_the_forward():
+    """Chaining layer_from from the embedding reproduces the full forward's
+    residuals, and head_from reproduces its logprobs."""
+    cfg = synth.TINY
+    orc = _oracle(cfg, random_gains=True, lm_scale=10.0)
+    s = synth.tiny_sequences(cfg, n=1, lo=30, hi=30, seed=8)[0]
+    orc.audit = []
+    full = orc.prefill_logprobs(s.tokens)
+    res = [x for t, l, x in orc.audit if t == "layer"]
+    orc.audit = None
+    pos = np.arange(s.length - 1)
+    r = orc.W["embed"][s.tokens[:-1]]
+    for l in range(cfg.layers):
+        r = orc.layer_from(l, r, pos)
+        assert np.array_equal(r, res[l])
+    assert np.array_equal(orc.head_from(r, s.tokens[1:]), full)

@@ -61,6 +61,7 @@ def _case(B, seed, lens, Hq=16, Hkv=8, D=128, kv_split=128):
     d.block_table, d.max_pages = keep["bt"].data_ptr(), bt.shape[1]
     d.page, d.kv_split, d.max_ctx = 64, kv_split, max(lens)
     d.scale = 1.0 / math.sqrt(D)
+    d.num_pages = total
     return d, keep
 
 
