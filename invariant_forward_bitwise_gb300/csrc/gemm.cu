@@ -96,7 +96,11 @@ template <int BN, bool F32OUT>
 __global__ void __launch_bounds__(128, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, void* C, int64_t ldc, int M, int N,
-                     int K, int kb_per_split, float* partial, int vec_ok, int* err) {
+                     int K, int kb_per_split, float* partial, int vec_ok, int a_box_bytes,
+                     int* err) {
+  // a_box_bytes: bytes of A that TMA writes per stage (rows of the A box x 128);
+  // when M < 128 only the first rows are loaded, rows past them never feed a
+  // stored output row.
   using Cfg = Bf16Cfg<BN>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(128, 1)
     for (int i = 0; i < nkb; ++i) {
       const int s = i % S;
       if (i >= S && !mbar_wait(empty0 + 8 * s, ((i / S) - 1) & 1, err)) break;
-      mbar_expect_tx(full0 + 8 * s, Cfg::STAGE);
+      mbar_expect_tx(full0 + 8 * s, uint32_t(a_box_bytes + Cfg::B_BYTES));
       const int kx = (kb0 + i) * Cfg::BK;
       tma_load_2d(smem_u32(sA + s * Cfg::A_BYTES), &tmA, full0 + 8 * s, kx, m0);
       tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full0 + 8 * s, kx, n0);
@@ -515,10 +519,35 @@ struct Plan {
   int splits = 1;
   int kb_per_split = 0;
   bool persistent = false;
+  int m_box = BM;  // rows of the A TMA box
 };
 
-// Set BIV_GEMM_PERSISTENT=0 to force the one-tile-per-CTA kernel (used by the
-// tests that check both kernels give the same bits).
+// Few output tiles (decode-sized M): pick the tile width with the best
+// modelled weight-streaming rate.  Per 64-wide K block a CTA moves through
+// shared memory the A box (m_box rows), the B tile (TMA write) and the MMA's
+// operand reads (128 A rows + BN B rows, 4 times 32 bytes each), so the weight
+// share of that traffic is BN / (m_box + 2 BN + 128); CTAs beyond the SM
+// count add nothing.
+int pick_small_m_bn(int M, int N, int m_box, int sms) {
+  const int tiles_m = (M + BM - 1) / BM;
+  int best = 128;
+  double best_score = -1.0;
+  for (int bn : {256, 128, 64, 32}) {
+    if (bn > 32 && bn / 2 >= N) continue;
+    const double rate = double(bn) / double(m_box + 2 * bn + 128);
+    const int64_t ctas = int64_t((N + bn - 1) / bn) * tiles_m;
+    const double score = double(std::min<int64_t>(ctas, sms)) * rate;
+    if (score > best_score * 1.0001) {
+      best_score = score;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+// Test overrides: BIV_GEMM_PERSISTENT=0 forces the one-tile-per-CTA kernel and
+// BIV_GEMM_TILE_N=32|64|128|256 forces the tile width; the tests use them to
+// check that neither choice changes a result bit.
 bool persistent_allowed() {
   const char* e = getenv("BIV_GEMM_PERSISTENT");
   return !(e && e[0] == '0');
@@ -538,12 +567,22 @@ Plan plan_bf16(const biv_gemm_desc& d) {
   // traffic per FLOP).
   const int sms = sm_count() > 0 ? sm_count() : 148;
   const int64_t mt = (d.M + BM - 1) / BM;
-  if (d.N >= 256 && int64_t((d.N + 255) / 256) * mt >= sms) p.bn = 256;
+  if (d.N >= 256 && int64_t((d.N + 255) / 256) * mt >= sms) {
+    p.bn = 256;
+  } else {
+    p.m_box = d.M <= BM ? std::max(16, (d.M + 15) / 16 * 16) : BM;
+    p.bn = pick_small_m_bn(d.M, d.N, p.m_box, sms);
+  }
+  if (const char* e = getenv("BIV_GEMM_TILE_N")) {  // test override of the tile width
+    const int bn = atoi(e);
+    if (bn == 32 || bn == 64 || bn == 128 || bn == 256) p.bn = bn;
+  }
   const int64_t tiles = int64_t((d.N + p.bn - 1) / p.bn) * mt;
   p.persistent = tiles >= 2 * sms && persistent_allowed();
   if (d.mode == BIV_MODE_FAST && d.M <= 256) {
+    // the batch-dependent comparator: same modelled tile, plus a K split that
+    // fills the GPU (this is what makes its bits depend on M)
     p.persistent = false;
-    p.bn = d.N >= 128 ? 64 : 32;
     const int tiles = ((d.N + p.bn - 1) / p.bn) * ((d.M + BM - 1) / BM);
     const int sms = sm_count() > 0 ? sm_count() : 148;
     int splits = (2 * sms + tiles - 1) / tiles;
@@ -570,7 +609,7 @@ biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_g
   const int vec_ok = aligned16(d.C) && (d.ldc * eb) % 16 == 0;
   dim3 grid((d.N + BN - 1) / BN, (d.M + BM - 1) / BM, p.splits);
   kern<<<grid, 128, Cfg::SMEM, s>>>(ta, tb, d.C, d.ldc, d.M, d.N, d.K, p.kb_per_split,
-                                    p.splits > 1 ? partial : nullptr, vec_ok,
+                                    p.splits > 1 ? partial : nullptr, vec_ok, p.m_box * 128,
                                     device_error_word());
   return check_launch("gemm_bf16");
 }
@@ -693,7 +732,8 @@ biv_status biv_gemm(const biv_gemm_desc* d, void* ws, size_t ws_bytes, biv_strea
     const size_t need = p.splits > 1 ? size_t(p.splits) * d->M * d->N * sizeof(float) : 0;
     if (need && (!ws || ws_bytes < need))
       return set_error(BIV_ERR_WORKSPACE, "gemm: workspace of %zu bytes needed", need);
-    if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->A, d->K, d->M, d->lda, 64, BM) ||
+    if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->A, d->K, d->M, d->lda, 64,
+                  p.persistent ? BM : p.m_box) ||
         !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->B, d->K, d->N, d->ldb, 64, p.bn))
       return set_error(BIV_ERR_CUDA, "gemm: tensor map encoding failed");
     float* partial = static_cast<float*>(ws);

@@ -1,0 +1,99 @@
+"""Per-kernel micro-benchmark of libbiv on Qwen3-1.7B-shaped cases.
+
+  python -m invariant_forward_bitwise_gb300.kernel_bench CASE [REPS]
+
+CASE is one of attn_decode (256 sequences x 700 context, one decode row each),
+attn_prefill (8 sequences x 1024 tokens), gemm_prefill (M 8192, N 2048,
+K 6144), gemm_decode (M 64, N 2048, K 6144), lm_head (M 4096, N 151936,
+K 2048), ssd_prefill (16384 tokens, 64 heads) and ssd_decode (one token).
+Each case times REPS calls with CUDA events after one warm-up call and
+prints the time and the rate against the case's algorithmic bytes or FLOPs;
+it is also the command that the ncu summaries in profiles/ capture.
+"""
+import math
+import os
+import sys
+
+import numpy as np
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import synth  # noqa: E402
+from invariant_forward_bitwise_gb300 import biv, build  # noqa: E402
+
+build.build()
+biv.load()
+case = sys.argv[1]
+reps = int(sys.argv[2]) if len(sys.argv) > 2 else 3
+g = synth.rng(0)
+
+def timeit(fn, n=reps):
+    fn(); torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n): fn()
+    e1.record(); torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+if case.startswith("ssd"):
+    H, P, N, Q = 64, 64, 128, 256
+    T = 16384 if case == "ssd_prefill" else 1
+    x, dt, A, Bm, Cm, D = synth.ssd_inputs(g, T)
+    st = torch.zeros(1, H, P, N, device="cuda"); bx = torch.zeros(1, Q, H, P, dtype=torch.bfloat16, device="cuda")
+    bB = torch.zeros(1, Q, N, dtype=torch.bfloat16, device="cuda"); bC = torch.zeros_like(bB)
+    bdt = torch.zeros(1, Q, H, device="cuda")
+    xd = x.reshape(T, H * P).cuda(); dtd = torch.from_numpy(dt).cuda(); Ad = torch.from_numpy(A).cuda()
+    Bd, Cd, Dd = Bm.cuda(), Cm.cuda(), torch.from_numpy(D).cuda()
+    y = torch.empty(T, H * P, dtype=torch.bfloat16, device="cuda")
+    keep = [torch.tensor([v], dtype=torch.int32, device="cuda") for v in (0, T, 0 if T > 1 else 200)]
+    d = biv.SSDDesc()
+    d.x, d.x_stride, d.dt, d.dt_stride, d.A, d.D = xd.data_ptr(), xd.stride(0), dtd.data_ptr(), dtd.stride(0), Ad.data_ptr(), Dd.data_ptr()
+    d.B, d.B_stride, d.C, d.C_stride, d.y, d.y_stride = Bd.data_ptr(), Bd.stride(0), Cd.data_ptr(), Cd.stride(0), y.data_ptr(), y.stride(0)
+    d.H, d.P, d.N, d.chunk, d.nseq = H, P, N, Q, 1
+    d.row0, d.n, d.pos0, d.max_n = keep[0].data_ptr(), keep[1].data_ptr(), keep[2].data_ptr(), T
+    d.state, d.buf_x, d.buf_B, d.buf_C, d.buf_dt = st.data_ptr(), bx.data_ptr(), bB.data_ptr(), bC.data_ptr(), bdt.data_ptr()
+    ms = timeit(lambda: biv.biv_ssd_scan(d))
+    print(f"{case} T={T}: {ms*1e3:.1f} us  ({T/(ms/1e3):.0f} tokens/s per sequence)")
+elif case.startswith("attn"):
+    Hq, Hkv, D = 16, 8, 128
+    B, ctx = (256, 700) if case == "attn_decode" else (8, 1024)
+    pages_per = (ctx + 63) // 64
+    P = B * pages_per
+    kc = (torch.randn(P, 64, Hkv, D, device="cuda") * 0.5).to(torch.bfloat16)
+    vc = (torch.randn(P, 64, Hkv, D, device="cuda") * 0.5).to(torch.bfloat16)
+    bt = torch.arange(P, dtype=torch.int32, device="cuda").view(B, pages_per)
+    if case == "attn_decode":
+        rows = [(i, ctx - 1) for i in range(B)]
+        blocks = [(i, 1) for i in range(B)]
+    else:
+        rows = [(i, p) for i in range(B) for p in range(ctx)]
+        blocks = [(i * ctx + j, 32) for i in range(B) for j in range(0, ctx, 32)]
+    T = len(rows)
+    q = torch.randn(T, Hq * D, device="cuda").to(torch.bfloat16)
+    out = torch.empty_like(q)
+    seq = torch.tensor([r[0] for r in rows], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([r[1] for r in rows], dtype=torch.int32, device="cuda")
+    qb = torch.tensor(np.array(blocks, np.int32).ravel(), device="cuda")
+    d = biv.AttnDesc()
+    d.q, d.q_stride, d.out, d.out_stride = q.data_ptr(), q.stride(0), out.data_ptr(), out.stride(0)
+    d.T, d.Hq, d.Hkv, d.D = T, Hq, Hkv, D
+    d.row_seq, d.row_pos, d.qblocks, d.nqblocks = seq.data_ptr(), pos.data_ptr(), qb.data_ptr(), len(blocks)
+    d.max_rows_per_block = max(b[1] for b in blocks)
+    d.kv_dtype = biv.BF16
+    d.k_cache, d.v_cache, d.block_table, d.max_pages = kc.data_ptr(), vc.data_ptr(), bt.data_ptr(), pages_per
+    d.page, d.kv_split, d.max_ctx, d.scale, d.num_pages = 64, 1024, ctx, 1 / math.sqrt(D), P
+    n = biv.biv_attention_workspace(d)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+    ms = timeit(lambda: biv.biv_attention(d, ws))
+    kv_bytes = B * ctx * Hkv * D * 2 * 2
+    flops = 4.0 * sum(p + 1 for _, p in rows) * Hq * D
+    print(f"{case}: {ms*1e3:.1f} us  KV {kv_bytes/1e6:.0f} MB -> {kv_bytes/(ms/1e3)/1e9:.0f} GB/s;  {flops/(ms/1e3)/1e12:.1f} TFLOP/s")
+else:
+    M, N, K = {"gemm_prefill": (8192, 2048, 6144), "gemm_decode": (64, 2048, 6144),
+               "lm_head": (4096, 151936, 2048)}[case]
+    a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+    b = (torch.randn(N, K, device="cuda") * 0.02).to(torch.bfloat16)
+    c = torch.empty(M, N, device="cuda", dtype=torch.float32 if case == "lm_head" else torch.bfloat16)
+    d = biv.gemm_desc(a, b, c)
+    ms = timeit(lambda: biv.biv_gemm(d))
+    print(f"{case} M={M} N={N} K={K}: {ms*1e3:.1f} us  {2*M*N*K/(ms/1e3)/1e12:.0f} TFLOP/s  weights {N*K*2/(ms/1e3)/1e9:.0f} GB/s")

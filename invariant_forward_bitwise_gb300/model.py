@@ -402,7 +402,10 @@ class DecodeGraphs:
     result discarded), which cannot change a live row's bits because no
     reduction crosses rows."""
 
-    BUCKETS = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024)
+    # padded batch sizes with a captured graph each (finer steps where the
+    # padding would waste most)
+    BUCKETS = (1, 2, 4, 8, 16, 24, 32, 48, 64, 80, 96, 112, 128, 160, 192, 224, 256, 288, 320,
+               384, 448, 512, 640, 768, 1024)
 
     def __init__(self, model: DenseModel, kv: PagedKV, use_graphs: bool = True):
         self.m, self.kv, self.use = model, kv, use_graphs
@@ -500,4 +503,77 @@ def rollout(model: DenseModel, kv: PagedKV, seqs, max_tokens: int, use_graphs: b
             out[i][pos[j] + 1 - seqs[i].prompt_len] = v[j]
     for i in slots:
         kv.release(i)
+    return out
+
+
+# ---------------------------------------------------- continuous batching ----
+def serve_mixed(model: DenseModel, kv: PagedKV, seqs, chunk: int = 512, max_decode: int = 256,
+                max_tokens: Optional[int] = None):
+    """Continuous batching: every step carries one prefill chunk (<= ``chunk``
+    tokens) of the next admitted sequence together with one decode row for
+    each live sequence whose prompt is done (at most ``max_decode``).  A
+    sequence is admitted when a decode slot is free and leaves when its last
+    token is consumed.  Returns per sequence the logprobs of its response
+    tokens; they are the same bits as a rollout or a recompute of it alone."""
+    run = Runner(model)
+    out = [np.zeros(s.length - s.prompt_len, np.float32) for s in seqs]
+    free = list(range(len(seqs)))[::-1]
+    slot_of, cur = {}, {}
+    queue = list(range(len(seqs)))
+    prefill_next = {}        # seq -> next prompt position to prefill
+    decoding = []            # seqs whose prompt is done and that still decode
+    while queue or prefill_next or decoding:
+        if queue and not prefill_next and len(decoding) < max_decode:
+            i = queue.pop(0)
+            slot_of[i] = free.pop()
+            kv.admit(slot_of[i], seqs[i].length)
+            kv.sync_table()
+            prefill_next[i] = 0
+        seq_slot, pos, ids, lm_rows, targets, owner = [], [], [], [], [], []
+        done_after_step = []
+        for i in decoding:
+            p = cur[i]
+            lm_rows.append(len(ids))
+            targets.append(int(seqs[i].tokens[p + 1]))
+            owner.append((i, p))
+            seq_slot.append(slot_of[i]); pos.append(p); ids.append(int(seqs[i].tokens[p]))
+        for i, p0 in list(prefill_next.items()):
+            s = seqs[i]
+            p1 = min(s.prompt_len, p0 + chunk)
+            for p in range(p0, p1):
+                if p >= s.prompt_len - 1:
+                    lm_rows.append(len(ids))
+                    targets.append(int(s.tokens[p + 1]))
+                    owner.append((i, p))
+                seq_slot.append(slot_of[i]); pos.append(p); ids.append(int(s.tokens[p]))
+            if p1 == s.prompt_len:
+                del prefill_next[i]
+                cur[i] = s.prompt_len
+                if cur[i] < s.length - 1:
+                    decoding.append(i)
+                else:
+                    done_after_step.append(i)
+            else:
+                prefill_next[i] = p1
+        if not ids:
+            continue
+        spec = run.load_rows(kv, seq_slot, pos, ids, lm_rows, targets)
+        model.reserve(kv, [spec])
+        model.step(kv, spec)
+        lp = model.lp[:len(lm_rows)].cpu().numpy()
+        for (i, p), v in zip(owner, lp):
+            out[i][p + 1 - seqs[i].prompt_len] = v
+        nxt = []
+        for i in decoding:
+            if (i, cur[i]) in set(owner):
+                cur[i] += 1
+            if cur[i] < seqs[i].length - 1:
+                nxt.append(i)
+            else:
+                kv.release(slot_of[i])
+                free.append(slot_of[i])
+        decoding = nxt
+        for i in done_after_step:
+            kv.release(slot_of[i])
+            free.append(slot_of[i])
     return out

@@ -191,3 +191,16 @@ def test_fast_mode_differs_but_stays_close():
     a = rollout(m_inv, kv, seqs, max_tokens=1024)
     b = rollout(m_fast, kv2, seqs, max_tokens=1024)
     assert stats(a, b)["max"] <= TOL_LP
+
+
+@pytest.mark.parametrize("kv_fp8", [False, True], ids=["bf16kv", "fp8kv"])
+def test_continuous_batching_equals_recompute(kv_fp8):
+    """Mixed steps (a prefill chunk of one sequence next to decode rows of the
+    others, sequences arriving and leaving) give the recompute's bits."""
+    from invariant_forward_bitwise_gb300.model import recompute, serve_mixed
+    cfg = synth.replace(synth.TINY, kv_fp8=kv_fp8)
+    W, m, kv = make(cfg)
+    seqs = synth.tiny_sequences(cfg, n=8, lo=40, hi=128, seed=21)
+    rec = recompute(m, kv, seqs, max_tokens=1024)
+    mixed = serve_mixed(m, kv, seqs, chunk=16, max_decode=3)
+    assert stats(rec, mixed) == ZERO

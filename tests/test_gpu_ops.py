@@ -405,19 +405,24 @@ def test_gemm_persistent_equals_one_tile_kernel(B, monkeypatch, M, N, K, out):
     assert rel_err(host_f32(c1)[rows], ref) < REL
 
 
-@pytest.mark.parametrize("M,N,K", [(3, 512, 192), (100, 512, 128), (7, 8192, 192), (64, 12288, 64)])
-def test_tcgen05_result_independent_of_tile_width(B, M, N, K):
+@pytest.mark.parametrize("M,N,K", [(3, 512, 192), (100, 512, 2048), (7, 8192, 688), (300, 12288, 64),
+                                   (4096, 1024, 256)])
+def test_tcgen05_result_independent_of_tile_width(B, monkeypatch, M, N, K):
     """The hardware property the tile planner relies on: with the same K
-    schedule, an output element has the same bits whether its CTA's MMA is
-    N=64 wide (FAST mode at small M, no K split for K <= 192) or 128/256 wide
-    (INVARIANT mode)."""
+    schedule an output element has the same bits whatever the MMA instruction
+    width (tile N) of its CTA, on the one-tile and the persistent kernel."""
     g = synth.rng(M * N + K)
     a, b = rnd_bf16(g, M, K), rnd_bf16(g, N, K, std=0.05)
     ad, bd = dev(a), dev(b)
-    c1 = torch.empty(M, N, dtype=torch.float32, device="cuda")
-    c2 = torch.empty(M, N, dtype=torch.float32, device="cuda")
-    B.biv_gemm(B.gemm_desc(ad, bd, c1))
-    d = B.gemm_desc(ad, bd, c2, mode=B.MODE_FAST)
-    assert B.biv_gemm_workspace(d) == 0
-    B.biv_gemm(d)
-    assert np.array_equal(bits(c1), bits(c2))
+    outs = []
+    for bn in ["32", "64", "128", "256"]:
+        monkeypatch.setenv("BIV_GEMM_TILE_N", bn)
+        c = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        B.biv_gemm(B.gemm_desc(ad, bd, c))
+        outs.append(bits(c))
+    monkeypatch.delenv("BIV_GEMM_TILE_N")
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    ref = ops.gemm(a.float().numpy()[:5], b.float().numpy(), out="f32")
+    got = outs[0].view(np.float32).reshape(M, N)[:5]
+    assert rel_err(got, ref) < REL
