@@ -48,6 +48,10 @@ def parse():
     ap.add_argument("--no-fast", action="store_true", help="skip the non-invariant comparator")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="decode without CUDA-graph replay (for per-launch profilers)")
+    ap.add_argument("--prompt-max", type=int, default=512, help="cap prompt length (profiling runs)")
+    ap.add_argument("--resp-max", type=int, default=1024, help="cap response length (profiling runs)")
     return ap.parse_args()
 
 
@@ -192,7 +196,9 @@ def main():
     biv.load()
 
     cfg = synth.QWEN3_1P7B if args.layers == 28 else synth.scaled_dense(synth.QWEN3_1P7B, args.layers)
-    seqs = synth.rollout_sequences(cfg, prompts=args.prompts, responses=args.responses, seed=1 + rank)
+    seqs = synth.rollout_sequences(cfg, prompts=args.prompts, responses=args.responses,
+                                   prompt_lo=min(64, args.prompt_max), prompt_hi=args.prompt_max,
+                                   resp_lo=min(128, args.resp_max), resp_hi=args.resp_max, seed=1 + rank)
     W = synth.dense_weights(cfg, seed=0)
     max_len = max(s.length for s in seqs)
     max_pos = (max_len + 63) // 64 * 64
@@ -204,7 +210,7 @@ def main():
         kv_roll = PagedKV(cfg, pages=pages_roll, max_seqs=len(seqs), max_pages=max_pos // 64)
         group_pages = (args.max_tokens // 64 + 64) * 2
         kv_rec = PagedKV(cfg, pages=group_pages, max_seqs=len(seqs), max_pages=max_pos // 64)
-        dg = DecodeGraphs(m, kv_roll, use_graphs=True)
+        dg = DecodeGraphs(m, kv_roll, use_graphs=not args.eager)
         return m, kv_roll, kv_rec, dg
 
     def one_step(arm, collect=False):

@@ -19,6 +19,7 @@
 // FP8 pages (dequantised on the way in), sparse gathers and D = 80 use
 // cp.async / plain loads into padded rows.
 #include <algorithm>
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -32,8 +33,9 @@ constexpr int kNV = 64;     // most query vectors a CTA takes (4 warps x 16)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // NW warps per CTA (16 query vectors each), ST-stage K/V pipeline, TMA or
-// thread-issued loads.  Decode blocks (<= 16 vectors) run NW = 1, ST = 3;
-// prefill blocks NW = 4, ST = 2.
+// thread-issued loads.  Decode blocks (<= 16 vectors) run NW = 1, prefill
+// blocks NW = 4, both with a 2-stage pipeline (measured on GB300: 2 stages let
+// 3 one-warp decode CTAs share an SM and beat 3 stages with 2 CTAs).
 template <int D, int NW, int ST, bool TMA>
 struct AttnCfg {
   static constexpr int LD = D + 8;                   // padded row (elements), thread-loaded tiles
@@ -316,19 +318,36 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
         mma_bf16(s[2 * np + 1], qf[kk], b2, b3);
       }
     }
-    // mask, online softmax
+    // mask, online softmax.  A dense tile that every live row of the warp sees
+    // whole needs no per-element test (the result is the same either way).
     float mx[2] = {-INFINITY, -INFINITY};
+    const int row_lo = min(vpos[0] < 0 ? INT_MAX : vpos[0], vpos[1] < 0 ? INT_MAX : vpos[1]);
+    const bool whole = !sparse && tbase + kTile <= hi &&
+                       __all_sync(0xffffffffu, row_lo >= tbase + kTile - 1);
+    if (whole) {
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = e >> 1;
-        const int col = nt * 8 + 2 * cq + (e & 1);
-        const int kp = sparse ? tP[col] : (tbase + col < hi ? tbase + col : -1);
-        const bool vis = kp >= 0 && kp <= vpos[i];
-        const float x = vis ? s[nt][e] * a.scale_log2 : -INFINITY;
-        s[nt][e] = x;
-        mx[i] = fmaxf(mx[i], x);
+        for (int e = 0; e < 4; ++e) {
+          const int i = e >> 1;
+          const float x = vpos[i] >= 0 ? s[nt][e] * a.scale_log2 : -INFINITY;
+          s[nt][e] = x;
+          mx[i] = fmaxf(mx[i], x);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = e >> 1;
+          const int col = nt * 8 + 2 * cq + (e & 1);
+          const int kp = sparse ? tP[col] : (tbase + col < hi ? tbase + col : -1);
+          const bool vis = kp >= 0 && kp <= vpos[i];
+          const float x = vis ? s[nt][e] * a.scale_log2 : -INFINITY;
+          s[nt][e] = x;
+          mx[i] = fmaxf(mx[i], x);
+        }
       }
     }
     float alpha[2];
@@ -368,12 +387,15 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
       rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
       l[i] = l[i] * alpha[i] + rs[i];
     }
+    // rescale only when some row's max moved (a factor of exactly 1 is a no-op)
+    if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
-    for (int dt = 0; dt < Cfg::DT; ++dt) {
-      acc[dt][0] *= alpha[0];
-      acc[dt][1] *= alpha[0];
-      acc[dt][2] *= alpha[1];
-      acc[dt][3] *= alpha[1];
+      for (int dt = 0; dt < Cfg::DT; ++dt) {
+        acc[dt][0] *= alpha[0];
+        acc[dt][1] *= alpha[0];
+        acc[dt][2] *= alpha[1];
+        acc[dt][3] *= alpha[1];
+      }
     }
     // O += P . V
 #pragma unroll
@@ -545,9 +567,9 @@ biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
           make_kv_map(&a.tmK, d.k_cache, d.num_pages, d.Hkv, D) &&
           make_kv_map(&a.tmV, d.v_cache, d.num_pages, d.Hkv, D);
     if (tma)
-      st = small ? launch_cfg<D, 1, 3, true>(d, a, s) : launch_cfg<D, 4, 2, true>(d, a, s);
+      st = small ? launch_cfg<D, 1, 2, true>(d, a, s) : launch_cfg<D, 4, 2, true>(d, a, s);
   }
-  if (!tma) st = small ? launch_cfg<D, 1, 3, false>(d, a, s) : launch_cfg<D, 4, 2, false>(d, a, s);
+  if (!tma) st = small ? launch_cfg<D, 1, 2, false>(d, a, s) : launch_cfg<D, 4, 2, false>(d, a, s);
   if (st != BIV_OK || a.nsplit_grid <= 1) return st;
   const int64_t warps = int64_t(d.T) * d.Hq;
   attn_merge_kernel<D><<<unsigned((warps * 32 + 255) / 256), 256, 0, s>>>(a);

@@ -238,7 +238,9 @@ template <int BN, bool F32OUT>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_persistent(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, void* C, int64_t ldc, int M,
-                         int N, int K, int vec_ok, int* err) {
+                         int N, int K, int vec_ok, int n_fastest, int* err) {
+  // n_fastest: walk N tiles first (CTAs running together share an A tile and
+  // B is re-read from L2) when B is the smaller operand; else M first.
   using Cfg = PersistCfg<BN>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -282,7 +284,8 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch_desc(&tmB);
     bool ok = true;
     for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+      const int m0 = (n_fastest ? t / tiles_n : t % tiles_m) * BM;
+      const int n0 = (n_fastest ? t % tiles_n : t / tiles_m) * BN;
       for (int kb = 0; kb < KB; ++kb) {
         const int it = issued, s = it % S;
         if (it >= S && !mbar_wait(empty0 + 8 * s, ((it / S) - 1) & 1, err)) {
@@ -328,7 +331,8 @@ __global__ void __launch_bounds__(192, 1)
       const int b = j & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * b, (j >> 1) & 1, err))) break;
       tc_fence_after();
-      const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+      const int m0 = (n_fastest ? t / tiles_n : t % tiles_m) * BM;
+      const int n0 = (n_fastest ? t % tiles_n : t / tiles_m) * BN;
       const int row = m0 + q * 32 + lane;
       const uint32_t trow = tmem + b * BN + (uint32_t(q * 32) << 16);
 #pragma unroll 1
@@ -585,8 +589,9 @@ Plan plan_bf16(const biv_gemm_desc& d) {
     p.persistent = false;
     const int tiles = ((d.N + p.bn - 1) / p.bn) * ((d.M + BM - 1) / BM);
     const int sms = sm_count() > 0 ? sm_count() : 148;
-    int splits = (2 * sms + tiles - 1) / tiles;
-    splits = std::max(1, std::min(splits, KB / 4));
+    // split K only when the tiles leave most SMs idle; aim at one wave
+    int splits = tiles * 2 <= sms ? (sms + tiles - 1) / tiles : 1;
+    splits = std::max(1, std::min(splits, KB / 8));
     p.kb_per_split = (KB + splits - 1) / splits;
     p.splits = (KB + p.kb_per_split - 1) / p.kb_per_split;
   }
@@ -631,7 +636,9 @@ biv_status launch_bf16_persistent(const CUtensorMap& ta, const CUtensorMap& tb,
   const int tiles = ((d.N + BN - 1) / BN) * ((d.M + BM - 1) / BM);
   const int sms = sm_count() > 0 ? sm_count() : 148;
   const int grid = std::min(tiles, sms);
-  kern<<<grid, 192, Cfg::SMEM, s>>>(ta, tb, d.C, d.ldc, d.M, d.N, d.K, vec_ok, device_error_word());
+  const int n_fastest = d.N <= d.M;
+  kern<<<grid, 192, Cfg::SMEM, s>>>(ta, tb, d.C, d.ldc, d.M, d.N, d.K, vec_ok, n_fastest,
+                                    device_error_word());
   return check_launch("gemm_bf16_persistent");
 }
 

@@ -22,6 +22,7 @@ namespace {
 
 constexpr int kP = 64, kN = 128, kMaxQ = 256;
 constexpr int kLDC = kN + 8;  // padded C rows (bank spread for per-row reads)
+constexpr int kFewRows = 4;   // at most this many new rows in a chunk: (row, p) threads
 
 struct SsdSmem {
   uint16_t B[kMaxQ][kN];
@@ -30,6 +31,7 @@ struct SsdSmem {
   float dt[kMaxQ];
   float L[kMaxQ];
   float h[kP][kN];
+  float W[4][kMaxQ];  // term weights of the new rows (few-row path)
 };
 
 __global__ void __launch_bounds__(256, 1) ssd_kernel(const biv_ssd_desc d) {
@@ -98,9 +100,38 @@ __global__ void __launch_bounds__(256, 1) ssd_kernel(const biv_ssd_desc d) {
     }
     __syncthreads();
 
-    // outputs of the new rows
+    // outputs of the new rows.  Few new rows (decode): threads over (row, p)
+    // with the term weights w(t, s) staged in shared memory; many rows: one
+    // thread per row.  Both evaluate every output with the same operations in
+    // the same order (the weights, then the s sum, the n sum and the skip
+    // term as fma chains), so they give the same bits.
+    const int nnew = last - first;
+    if (nnew <= kFewRows) {
+      for (int e = tid; e < nnew * kMaxQ; e += 256) {
+        const int j = e / kMaxQ, sidx = e % kMaxQ;
+        const int rj = first - s0 + j;
+        if (sidx > rj) continue;
+        float cb = 0.f;
+#pragma unroll 8
+        for (int q = 0; q < kN; ++q) cb = fmaf(bf2f(S.C[rj][q]), bf2f(S.B[sidx][q]), cb);
+        S.W[j][sidx] = expf(S.L[rj] - S.L[sidx]) * cb;
+      }
+      __syncthreads();
+      if (tid < nnew * kP) {
+        const int j = tid / kP, pp = tid % kP;
+        const int rj = first - s0 + j;
+        float acc = 0.f;
+        for (int sidx = 0; sidx <= rj; ++sidx)
+          acc = fmaf(S.W[j][sidx], S.dt[sidx] * bf2f(S.x[sidx][pp]), acc);
+        const float eL = expf(S.L[rj]);
+        for (int q = 0; q < kN; ++q) acc = fmaf(eL * S.h[pp][q], bf2f(S.C[rj][q]), acc);
+        const int t = s0 + rj;
+        uint16_t* y = d.y + int64_t(row0 + (t - pos0)) * d.y_stride + int64_t(h) * kP;
+        y[pp] = f2bf(fmaf(Dh, bf2f(S.x[rj][pp]), acc));
+      }
+    }
     const int r = tid;
-    if (r < cnt && s0 + r >= first) {
+    if (nnew > kFewRows && r < cnt && s0 + r >= first) {
       const int t = s0 + r;
       const float Lt = S.L[r];
       float acc[kP];

@@ -88,6 +88,24 @@ elif case.startswith("attn"):
     kv_bytes = B * ctx * Hkv * D * 2 * 2
     flops = 4.0 * sum(p + 1 for _, p in rows) * Hq * D
     print(f"{case}: {ms*1e3:.1f} us  KV {kv_bytes/1e6:.0f} MB -> {kv_bytes/(ms/1e3)/1e9:.0f} GB/s;  {flops/(ms/1e3)/1e12:.1f} TFLOP/s")
+elif case == "gemm_sweep":
+    # weights rotate through enough copies to exceed L2, as in a decode step
+    # where every layer's weights are cold
+    shapes = {"qkv": (4096, 2048), "o": (2048, 2048), "gate_up": (12288, 2048),
+              "down": (2048, 6144), "lm_head": (151936, 2048)}
+    for name, (N, K) in shapes.items():
+        copies = max(1, -(-300_000_000 // (N * K * 2)))
+        bs = [(torch.randn(N, K, device="cuda") * 0.02).to(torch.bfloat16) for _ in range(copies)]
+        for M in (1, 16, 64, 128, 256, 512):
+            a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+            c = torch.empty(M, N, device="cuda",
+                            dtype=torch.float32 if name == "lm_head" else torch.bfloat16)
+            ds = [biv.gemm_desc(a, b, c) for b in bs]
+            n = copies * max(1, 8 // copies)
+            ms = timeit(lambda: [biv.biv_gemm(ds[i % copies]) for i in range(n)], 1) / n
+            print(f"{name:8s} M={M:4d} N={N:6d} K={K}: {ms*1e3:8.1f} us  weights {N*K*2/(ms/1e3)/1e9:6.0f} GB/s"
+                  f"  {2*M*N*K/(ms/1e3)/1e12:6.1f} TFLOP/s", flush=True)
+        del bs
 else:
     M, N, K = {"gemm_prefill": (8192, 2048, 6144), "gemm_decode": (64, 2048, 6144),
                "lm_head": (4096, 151936, 2048)}[case]

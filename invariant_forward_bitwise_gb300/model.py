@@ -138,14 +138,14 @@ class DenseModel:
             return None
         return t
 
-    def _gemm(self, A, Bw, Cout, M):
+    def _gemm(self, A, Bw, Cout, M, stream=None):
         d = biv.gemm_desc(A, Bw, Cout, mode=self.mode, M=M)
         need = biv.biv_gemm_workspace(d)
         if need > self.ws.numel():
             raise RuntimeError(f"workspace too small ({need} > {self.ws.numel()}); call reserve()")
         t = self._timer()
         tok = t.bracket("gemm_bf16", 2.0 * M * d.N * d.K, "flop") if t else None
-        biv.biv_gemm(d, self.ws if need else None)
+        biv.biv_gemm(d, self.ws if need else None, stream=stream)
         if tok:
             t.close(tok)
         self.launches += 2 if need else 1
@@ -208,49 +208,51 @@ class DenseModel:
         ``qblocks`` / ``lm_rows`` default to the shared step buffers; captured
         decode graphs pass constant buffers of their own."""
         cfg, W, T = self.cfg, self.W, spec.T
+        st = torch.cuda.current_stream()  # fetched once: every call below runs on it
         qblocks = self.qblocks if qblocks is None else qblocks
         lm_rows = self.lm_rows if lm_rows is None else lm_rows
         Hq, Hkv, D = cfg.q_heads, cfg.kv_heads, cfg.head_dim
         eps = cfg.eps
         r, y = self.r[:T], self.y[:T]
         self.launches = 0
-        biv.biv_embed(self.ids[:T], W["embed"], r)
-        biv.biv_add_rmsnorm(r, None, W["l0.attn_norm"], y, eps)
+        biv.biv_embed(self.ids[:T], W["embed"], r, stream=st)
+        biv.biv_add_rmsnorm(r, None, W["l0.attn_norm"], y, eps, stream=st)
         self.launches += 2
         for l in range(cfg.layers):
             p = f"l{l}."
-            self._gemm(y, W[p + "wqkv"], self.qkv, T)
+            self._gemm(y, W[p + "wqkv"], self.qkv, T, st)
             biv.biv_qk_norm_rope(self.qkv, T, Hq, Hkv, D, W.get(p + "q_norm") if cfg.qk_norm else None,
                                  W.get(p + "k_norm") if cfg.qk_norm else None, self.rope, self.max_pos,
-                                 self.row_pos, eps)
+                                 self.row_pos, eps, stream=st)
             kq = self.qkv[:, Hq * D:]
             vq = self.qkv[:, (Hq + Hkv) * D:]
             if kv.fp8:
                 biv.biv_kv_fp8_quant(kq, vq, self.qkv.stride(0), self.slot, T, Hkv, D, kv.k[l], kv.v[l],
-                                     kv.ks[l], kv.vs[l])
+                                     kv.ks[l], kv.vs[l], stream=st)
             else:
-                biv.biv_kv_store_bf16(kq, vq, self.qkv.stride(0), self.slot, T, Hkv, D, kv.k[l], kv.v[l])
+                biv.biv_kv_store_bf16(kq, vq, self.qkv.stride(0), self.slot, T, Hkv, D, kv.k[l], kv.v[l],
+                                      stream=st)
             ad = self._attn_desc(kv, l, spec, qblocks)
             need = biv.biv_attention_workspace(ad)
             t = self._timer()
             tok = t.bracket("attention_prefill", spec.attn_flops, "flop") if t and spec.attn_flops else None
-            biv.biv_attention(ad, self.ws if need else None)
+            biv.biv_attention(ad, self.ws if need else None, stream=st)
             if tok:
                 t.close(tok)
-            self._gemm(self.o, W[p + "wo"], self.a, T)
+            self._gemm(self.o, W[p + "wo"], self.a, T, st)
             aud = self.audit is not None and not torch.cuda.is_current_stream_capturing()
             if aud:
                 self.audit.append(("qkv", l, self.qkv[:T].clone()))
                 self.audit.append(("attn_o", l, self.o[:T].clone()))
                 self.audit.append(("attn_proj", l, self.a[:T].clone()))
-            biv.biv_add_rmsnorm(self.a[:T], r, W[p + "mlp_norm"], y, eps)
-            self._gemm(y, W[p + "wgu"], self.gu, T)
-            biv.biv_silu_mul(self.gu[:T], self.act[:T])
-            self._gemm(self.act, W[p + "wd"], self.a, T)
+            biv.biv_add_rmsnorm(self.a[:T], r, W[p + "mlp_norm"], y, eps, stream=st)
+            self._gemm(y, W[p + "wgu"], self.gu, T, st)
+            biv.biv_silu_mul(self.gu[:T], self.act[:T], stream=st)
+            self._gemm(self.act, W[p + "wd"], self.a, T, st)
             if self.audit is not None and not torch.cuda.is_current_stream_capturing():
                 self.audit.append(("mlp_out", l, self.a[:T].clone()))
             nxt = W[f"l{l + 1}.attn_norm"] if l + 1 < cfg.layers else W["final_norm"]
-            biv.biv_add_rmsnorm(self.a[:T], r, nxt, y, eps)
+            biv.biv_add_rmsnorm(self.a[:T], r, nxt, y, eps, stream=st)
             self.launches += 6 + (2 if need else 1)
             if self.audit is not None and not torch.cuda.is_current_stream_capturing():
                 self.audit.append(("layer", l, r.clone()))
@@ -258,12 +260,12 @@ class DenseModel:
         Tl = spec.T_lm
         if Tl == 0:
             return
-        biv.biv_gather_rows(y, lm_rows, 1, Tl, self.ylm)
+        biv.biv_gather_rows(y, lm_rows, 1, Tl, self.ylm, stream=st)
         self.launches += 1
         for c0 in range(0, Tl, self.lm_chunk):
             n = min(self.lm_chunk, Tl - c0)
-            self._gemm(self.ylm[c0:c0 + n], W["lm_head"], self.logits, n)
-            biv.biv_logprob(self.logits, self.targets[c0:c0 + n], self.lp[c0:c0 + n], T=n)
+            self._gemm(self.ylm[c0:c0 + n], W["lm_head"], self.logits, n, st)
+            biv.biv_logprob(self.logits, self.targets[c0:c0 + n], self.lp[c0:c0 + n], T=n, stream=st)
             self.launches += 1
         t = self._timer()
         if t:
