@@ -214,18 +214,29 @@ biv_status biv_attention_noalloc(const biv_attn_desc* desc, biv_stream_t stream)
 /* ---------------------------------------------------------------- GEMM --
  * C[M, N] = A[M, K] . B[N, K]^T on the tcgen05 tensor cores, FP32
  * accumulation in TMEM ("Finish RL Training Faster", section
- * "让训练前向使用推理的数值": one batch-invariant GEMM schedule).  A and B are
- * K-major (row-major with K contiguous).  INVARIANT mode: each output element
- * is one ascending pass over K in 64-wide blocks (bf16) or 128-wide blocks
- * (FP8), never split, whatever M is.
- *  - bf16 x bf16 -> bf16 or f32 (c_dtype).
+ * "让训练前向使用推理的数值": one batch-invariant GEMM schedule with a fixed K
+ * split).  A and B are K-major (row-major with K contiguous).  INVARIANT
+ * mode, whatever M is:
+ *  - bf16 x bf16 -> bf16 or f32 (c_dtype): with KB = ceil(K/64), K is cut
+ *    into chunks of ceil(KB/8) blocks of 64 (at most 8 chunks, the last may
+ *    be shorter); each chunk P_c is accumulated in FP32 from zero in
+ *    ascending K steps of 16; the output is the left fold r = P_0,
+ *    r = r + P_1, ... in FP32, rounded once to c_dtype.
  *  - e4m3 x e4m3 -> bf16 with block scales: per 128-wide K block kb,
  *    acc += (sa[m,kb]*sb[g][n/128,kb]) * (FP8 products summed over the
  *    block), promoted to FP32 every block, blocks in ascending order.
  * Grouped (MoE) when groups > 1: rows [off[g], off[g+1]) of A use weight
  * group g (B rows g*N .. g*N+N-1, sb + g*ceil(N/128)*ceil(K/128)).
  * K % 8 == 0 (bf16) / K % 16 == 0 (e4m3); lda, ldb keep rows 16-byte
- * aligned; ldc keeps rows 16-byte aligned for vector stores. */
+ * aligned; ldc keeps rows 16-byte aligned for vector stores.
+ * FAST mode (bf16): no K chunks when M fills the GPU, a K split sized to the
+ * GPU when it does not (results depend on M; the comparator).
+ * Workspace (bf16, when biv_gemm_workspace reports > 0: few output tiles,
+ * where the chunks of one tile run on different SMs and a second kernel
+ * folds them): device memory, 16-byte aligned, owned by the caller, no
+ * initial value needed.  Calls that can overlap on the GPU need separate
+ * workspaces.
+ * Returns BIV_ERR_WORKSPACE when the workspace is missing or too small. */
 typedef struct {
   int M, N, K;
   int a_dtype, b_dtype, c_dtype;

@@ -7,7 +7,7 @@ from __future__ import annotations
 
 import ctypes as C
 import os
-from typing import Optional
+from typing import Dict, Optional
 
 import torch
 
@@ -266,7 +266,27 @@ def biv_gemm_workspace(desc: GemmDesc) -> int:
     return n.value
 
 
+_gemm_scratch: Dict[int, torch.Tensor] = {}
+
+
+def gemm_scratch(nbytes: int, device=None) -> torch.Tensor:
+    """A GEMM workspace of at least nbytes, cached per device (for callers on
+    one stream)."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    t = _gemm_scratch.get(dev.index)
+    if t is None or t.numel() < nbytes:
+        t = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        _gemm_scratch[dev.index] = t
+    return t
+
+
 def biv_gemm(desc: GemmDesc, ws: Optional[torch.Tensor] = None, stream=None):
+    """ws: a workspace of biv_gemm_workspace(desc) bytes; when None and the
+    plan needs one, a cached per-device scratch buffer is used."""
+    if ws is None:
+        need = biv_gemm_workspace(desc)
+        if need:
+            ws = gemm_scratch(need)
     _check(load().biv_gemm(C.byref(desc), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                            _stream(stream)), "biv_gemm")
 

@@ -20,6 +20,7 @@
 // cp.async / plain loads into padded rows.
 #include <algorithm>
 #include <climits>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -33,9 +34,8 @@ constexpr int kNV = 64;     // most query vectors a CTA takes (4 warps x 16)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // NW warps per CTA (16 query vectors each), ST-stage K/V pipeline, TMA or
-// thread-issued loads.  Decode blocks (<= 16 vectors) run NW = 1, prefill
-// blocks NW = 4, both with a 2-stage pipeline (measured on GB300: 2 stages let
-// 3 one-warp decode CTAs share an SM and beat 3 stages with 2 CTAs).
+// thread-issued loads.  Decode blocks (<= 16 vectors) run NW = 1 with one TMA
+// stage (six CTAs per SM), prefill blocks NW = 4 with two stages.
 template <int D, int NW, int ST, bool TMA>
 struct AttnCfg {
   static constexpr int LD = D + 8;                   // padded row (elements), thread-loaded tiles
@@ -112,6 +112,8 @@ __device__ __forceinline__ int row_splits(const AttnArgs& a, int pos) {
 
 template <int D, int NW, int ST, bool TMA>
 __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ AttnArgs a) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
   using Cfg = AttnCfg<D, NW, ST, TMA>;
   constexpr int LD = Cfg::LD, NV = Cfg::NV, NT = Cfg::NT, KVB = Cfg::KVB;
   extern __shared__ uint8_t smem_raw[];
@@ -257,9 +259,11 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
   for (int i = 0; i < Cfg::DT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
   __syncthreads();  // Q stored, barriers initialised
-  // prologue: tiles 0 .. ST-2 in flight (one cp.async group each, even if empty)
+  // prologue.  TMA: tiles 0 .. ST-1 in flight, a stage is refilled right
+  // after the tile that used it.  Threads: tiles 0 .. ST-2 in flight (one
+  // cp.async group each, even if empty), refilled at the top of the loop.
 #pragma unroll
-  for (int s0 = 0; s0 < ST - 1; ++s0) {
+  for (int s0 = 0; s0 < (TMA ? ST : ST - 1); ++s0) {
     if (s0 < ntiles) load_tile(s0, s0);
     if (!TMA) cp_async_commit();
   }
@@ -291,9 +295,11 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
       cp_async_wait<ST - 2>();  // tile t has landed
     }
     __syncthreads();
-    // refill the stage that tile t-1 used (its compute ended at the last sync)
-    if (t + ST - 1 < ntiles) load_tile((t + ST - 1) % ST, t + ST - 1);
-    if (!TMA) cp_async_commit();
+    if (!TMA) {
+      // refill the stage that tile t-1 used (its compute ended at the last sync)
+      if (t + ST - 1 < ntiles) load_tile((t + ST - 1) % ST, t + ST - 1);
+      cp_async_commit();
+    }
     if (warp * 16 >= nv) {  // no live vector in this warp: only help with loads
       __syncthreads();
       continue;
@@ -306,16 +312,21 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
     float s[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+    // per k-step: all fragment loads first, then the MMAs (independent
+    // accumulators back to back; each accumulator still sees ascending k)
 #pragma unroll
     for (int kk = 0; kk < Cfg::DK; ++kk) {
+      uint32_t kf[4][4];
 #pragma unroll
       for (int np = 0; np < 4; ++np) {
-        uint32_t b0, b1, b2, b3;
         const int key = np * 16 + (lane & 7) + (lane >> 4) * 8;
         const int dim = kk * 16 + ((lane >> 3) & 1) * 8;
-        ldsm_x4(tK + Cfg::off(key, dim), b0, b1, b2, b3);
-        mma_bf16(s[2 * np], qf[kk], b0, b1);
-        mma_bf16(s[2 * np + 1], qf[kk], b2, b3);
+        ldsm_x4(tK + Cfg::off(key, dim), kf[np][0], kf[np][1], kf[np][2], kf[np][3]);
+      }
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        mma_bf16(s[2 * np], qf[kk], kf[np][0], kf[np][1]);
+        mma_bf16(s[2 * np + 1], qf[kk], kf[np][2], kf[np][3]);
       }
     }
     // mask, online softmax.  A dense tile that every live row of the warp sees
@@ -403,19 +414,30 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
       // A fragment order: (row g, k 0-7), (row g+8, k 0-7), (row g, k 8-15), (row g+8, k 8-15)
       const uint32_t af[4] = {pf[ks][0], pf[ks][1], pf[ks][2], pf[ks][3]};
       const uint32_t al[4] = {pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3]};
+      // V fragments of this k-step first, then every accumulator's hi MMA,
+      // then every lo MMA (per accumulator still hi before lo, ks ascending)
+      constexpr int DPS = Cfg::DT / 2;
+      uint32_t vf[DPS][4];
 #pragma unroll
-      for (int dp = 0; dp < Cfg::DT / 2; ++dp) {
-        uint32_t b0, b1, b2, b3;
+      for (int dp = 0; dp < DPS; ++dp) {
         const int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
         const int dim = dp * 16 + (lane >> 4) * 8;
-        ldsm_x4_t(tV + Cfg::off(key, dim), b0, b1, b2, b3);
-        mma_bf16(acc[2 * dp], af, b0, b1);
-        mma_bf16(acc[2 * dp + 1], af, b2, b3);
-        mma_bf16(acc[2 * dp], al, b0, b1);
-        mma_bf16(acc[2 * dp + 1], al, b2, b3);
+        ldsm_x4_t(tV + Cfg::off(key, dim), vf[dp][0], vf[dp][1], vf[dp][2], vf[dp][3]);
+      }
+#pragma unroll
+      for (int dp = 0; dp < DPS; ++dp) {
+        mma_bf16(acc[2 * dp], af, vf[dp][0], vf[dp][1]);
+        mma_bf16(acc[2 * dp + 1], af, vf[dp][2], vf[dp][3]);
+      }
+#pragma unroll
+      for (int dp = 0; dp < DPS; ++dp) {
+        mma_bf16(acc[2 * dp], al, vf[dp][0], vf[dp][1]);
+        mma_bf16(acc[2 * dp + 1], al, vf[dp][2], vf[dp][3]);
       }
     }
     __syncthreads();
+    // TMA: every warp is done with tile t's stage: refill it with tile t+ST
+    if (TMA && t + ST < ntiles) load_tile(buf, t + ST);
   }
 
   // ---- epilogue: single-split rows write the final output, others partials
@@ -454,6 +476,8 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
 // w_s = 2^(m_s - M), O = sum w_s o_s, L = sum w_s l_s, out = O / L.
 template <int D>
 __global__ void attn_merge_kernel(const __grid_constant__ AttnArgs a) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
   const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= int64_t(a.T) * a.Hq) return;
@@ -538,7 +562,7 @@ biv_status launch_cfg(const biv_attn_desc& d, const AttnArgs& a, cudaStream_t s)
     attr = true;
   }
   dim3 grid(d.nqblocks, d.Hkv, a.nsplit_grid);
-  attn_kernel<D, NW, ST, TMA><<<grid, Cfg::NT, Cfg::SMEM, s>>>(a);
+  launch_pdl(attn_kernel<D, NW, ST, TMA>, grid, Cfg::NT, Cfg::SMEM, s, a);
   return check_launch("attention");
 }
 
@@ -556,6 +580,17 @@ bool make_kv_map(CUtensorMap* m, const void* base, int num_pages, int Hkv, int D
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Pipeline depth of the one-warp TMA decode CTAs (BIV_ATTN_DECODE_STAGES =
+// 1, 2 or 3; a tuning override, the depth changes no result bit).  Default 1:
+// a CTA is latency-bound on its own instruction stream, so six one-stage CTAs
+// per SM move more KV than three two-stage ones (measured on GB300: 5.9 vs
+// 4.6 TB/s on 256 sequences x 700 tokens).
+int decode_stages() {
+  const char* e = getenv("BIV_ATTN_DECODE_STAGES");
+  const int v = e ? atoi(e) : 1;
+  return (v >= 1 && v <= 3) ? v : 1;
+}
+
 template <int D>
 biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
   // The CTA shape and the loader follow the call; a vector's arithmetic does not.
@@ -566,13 +601,22 @@ biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
     tma = !a.fp8 && !a.topk_idx && d.num_pages > 0 &&
           make_kv_map(&a.tmK, d.k_cache, d.num_pages, d.Hkv, D) &&
           make_kv_map(&a.tmV, d.v_cache, d.num_pages, d.Hkv, D);
-    if (tma)
-      st = small ? launch_cfg<D, 1, 2, true>(d, a, s) : launch_cfg<D, 4, 2, true>(d, a, s);
+    if (tma) {
+      const int ds = decode_stages();
+      if (!small)
+        st = launch_cfg<D, 4, 2, true>(d, a, s);
+      else if (ds == 1)
+        st = launch_cfg<D, 1, 1, true>(d, a, s);
+      else if (ds == 3)
+        st = launch_cfg<D, 1, 3, true>(d, a, s);
+      else
+        st = launch_cfg<D, 1, 2, true>(d, a, s);
+    }
   }
   if (!tma) st = small ? launch_cfg<D, 1, 2, false>(d, a, s) : launch_cfg<D, 4, 2, false>(d, a, s);
   if (st != BIV_OK || a.nsplit_grid <= 1) return st;
   const int64_t warps = int64_t(d.T) * d.Hq;
-  attn_merge_kernel<D><<<unsigned((warps * 32 + 255) / 256), 256, 0, s>>>(a);
+  launch_pdl(attn_merge_kernel<D>, unsigned((warps * 32 + 255) / 256), 256, 0, s, a);
   return check_launch("attention_merge");
 }
 

@@ -13,6 +13,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <utility>
 
 #include "biv.h"
 
@@ -29,6 +30,30 @@ int* device_error_word();
 // the driver's cuTensorMapEncodeTiled, resolved once at run time (nullptr if absent)
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// Programmatic dependent launch.  Kernels of the forward chain are launched
+// with programmatic stream serialization: a kernel may be scheduled while its
+// predecessor in the stream still runs, executes griddepcontrol.wait before it
+// touches any memory the predecessor writes or reads (weights excepted), and
+// lets its own successor be scheduled early (griddepcontrol.launch_dependents).
+// BIV_PDL=0 turns the attribute off (plain stream order).
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 #define BIV_REQUIRE(cond, ...)                                   \
   do {                                                           \
     if (!(cond)) return ::biv::set_error(BIV_ERR_INVALID, __VA_ARGS__); \
@@ -40,6 +65,14 @@ enum : int { kErrNone = 0, kErrTimeout = 1, kErrBadIndex = 2 };
 
 __device__ __forceinline__ void raise_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
+}
+
+// wait until the stream predecessor has completed and its memory is visible
+// (a no-op when the kernel was launched without the attribute)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// let the stream successor be scheduled once every CTA of this grid got here
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -181,6 +214,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
         "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+// 32 lanes x 16 columns of 32-bit from TMEM
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 }

@@ -1,21 +1,27 @@
 // Batch-invariant GEMM on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
-// C[M,N] = A[M,K] . B[N,K]^T, both operands K-major.  One CTA owns a 128 x BN
-// output tile; TMA streams 128-byte-swizzled K-slabs of A and B into a
-// shared-memory ring; one thread issues tcgen05.mma (M=128, N=BN) into an FP32
-// accumulator in TMEM; the four warps read it back (tcgen05.ld) and store.
+// C[M,N] = A[M,K] . B[N,K]^T, both operands K-major.  TMA streams
+// 128-byte-swizzled K slabs of A and B into a shared-memory ring; one thread
+// issues tcgen05.mma (M=128, N=BN) into FP32 accumulators in TMEM; epilogue
+// warps read them back (tcgen05.ld), fold and store.
 //
 // Invariance ("Finish RL Training Faster", section "让训练前向使用推理的数值":
-// one batch-invariant GEMM schedule): every output element is accumulated over
-// K in ascending 64-wide (bf16) / 128-wide (FP8) blocks, each block as a fixed
-// sequence of K=16 / K=32 MMA steps, with no split of K in INVARIANT mode.
-// Nothing about M enters that sequence: rows past M are TMA zero-fill and are
-// not stored.  FAST mode splits K when M is small (batch-dependent), the
-// comparator the pages measure against.
+// one batch-invariant GEMM schedule with a fixed K split): K is cut into
+// chunks whose boundaries depend on K only (at most 8 for bf16, 128-element
+// blocks for FP8); each chunk is accumulated from zero as a fixed sequence of
+// K=16 / K=32 MMA steps, and the chunk results are added in ascending chunk
+// order in FP32 (FP8: each scaled by its block scales first).  Nothing about
+// M enters that arithmetic: rows past M are TMA zero-fill and are not stored,
+// and the tile width, the persistent-CTA walk and whether chunks are folded
+// inside one CTA or by a second kernel only decide where the same additions
+// run.  FAST mode (the
+// batch-dependent comparator the pages measure against) does not chunk large
+// M and splits K to fill the GPU when M is small.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -24,17 +30,6 @@ namespace biv {
 namespace {
 
 constexpr int BM = 128;
-
-template <int BN>
-struct Bf16Cfg {
-  static constexpr int BK = 64;                       // 64 bf16 = one 128-byte swizzle row
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (192 * 1024) / STAGE > 8 ? 8 : (192 * 1024) / STAGE;
-  static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
-  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
-};
 
 template <int BN>
 struct Fp8Cfg {
@@ -88,174 +83,119 @@ __device__ __forceinline__ void store_row32(void* C, int64_t ldc, int row, int n
   }
 }
 
-// ------------------------------------------------------------ bf16 kernel --
-// grid (ceil(N/BN), ceil(M/128), splits).  Split z covers K-blocks
-// [z*kb_per_split, min(KB, (z+1)*kb_per_split)); with splits > 1 the FP32
-// partial tile goes to partial[z][M][N] instead of C.
-template <int BN, bool F32OUT>
-__global__ void __launch_bounds__(128, 1)
-    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, void* C, int64_t ldc, int M, int N,
-                     int K, int kb_per_split, float* partial, int vec_ok, int a_box_bytes,
-                     int* err) {
-  // a_box_bytes: bytes of A that TMA writes per stage (rows of the A box x 128);
-  // when M < 128 only the first rows are loaded, rows past them never feed a
-  // stored output row.
-  using Cfg = Bf16Cfg<BN>;
-  constexpr int S = Cfg::STAGES;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + S * Cfg::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), done = smem_u32(bars + 2 * S);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
-  const int KB = (K + Cfg::BK - 1) / Cfg::BK;
-  const int kb0 = blockIdx.z * kb_per_split;
-  const int nkb = min(KB, kb0 + kb_per_split) - kb0;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
-    }
-    mbar_init(done, 1);
-    fence_barrier_init();
-  }
-  __syncwarp();
-  if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  int issued = 0;
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % S;
-      if (i >= S && !mbar_wait(empty0 + 8 * s, ((i / S) - 1) & 1, err)) break;
-      mbar_expect_tx(full0 + 8 * s, uint32_t(a_box_bytes + Cfg::B_BYTES));
-      const int kx = (kb0 + i) * Cfg::BK;
-      tma_load_2d(smem_u32(sA + s * Cfg::A_BYTES), &tmA, full0 + 8 * s, kx, m0);
-      tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full0 + 8 * s, kx, n0);
-      issued = i + 1;
-    }
-  } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = idesc_mma(1u, BM, BN);
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % S;
-      if (!mbar_wait(full0 + 8 * s, (i / S) & 1, err)) break;
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(sA + s * Cfg::A_BYTES);
-      const uint32_t b0 = smem_u32(sB + s * Cfg::B_BYTES);
+// Store W consecutive FP32 register values of one row (static indexing only).
+template <int W, bool F32OUT>
+__device__ __forceinline__ void store_row_regs(void* C, int64_t ldc, int row, int n, int N,
+                                               const float (&r)[W], bool vec_ok) {
+  if (vec_ok && n + W <= N) {
+    if (F32OUT) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(C) + int64_t(row) * ldc + n);
 #pragma unroll
-      for (int kk = 0; kk < Cfg::BK / 16; ++kk)
-        umma_f16(tmem, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
-                 (i | kk) != 0 ? 1u : 0u);
-      umma_commit(empty0 + 8 * s);
-    }
-    umma_commit(done);
-  }
-  __syncwarp();
-  const bool have = __all_sync(0xffffffffu, mbar_wait(done, 0, err));
-  tc_fence_after();
-
-  if (have) {
-    const int row = m0 + warp * 32 + lane;
-    const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      if (n0 + c0 >= N) break;  // warp-uniform
-      uint32_t r[32];
-      tmem_ld32(trow + c0, r);
-      tmem_ld_wait();
-      if (row < M) {
-        if (partial) {
-          float* dst = partial + (int64_t(blockIdx.z) * M + row) * N + n0 + c0;
+      for (int j = 0; j < W / 4; ++j)
+        dst[j] = make_float4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(C) + int64_t(row) * ldc + n);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (n0 + c0 + j < N) dst[j] = __uint_as_float(r[j]);
-        } else {
-          store_row32<F32OUT>(C, ldc, row, n0 + c0, N, r, vec_ok != 0);
-        }
+      for (int j = 0; j < W / 8; ++j)
+        dst[j] = make_uint4(pack_bf2(r[8 * j], r[8 * j + 1]), pack_bf2(r[8 * j + 2], r[8 * j + 3]),
+                            pack_bf2(r[8 * j + 4], r[8 * j + 5]), pack_bf2(r[8 * j + 6], r[8 * j + 7]));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      if (n + j < N) {
+        if (F32OUT)
+          static_cast<float*>(C)[int64_t(row) * ldc + n + j] = r[j];
+        else
+          static_cast<uint16_t*>(C)[int64_t(row) * ldc + n + j] = f2bf(r[j]);
       }
     }
   }
-  // the producer makes sure its copies have landed before the CTA exits
-  if (warp == 0 && lane == 0) {
-    for (int i = max(0, issued - S); i < issued; ++i)
-      mbar_wait(full0 + 8 * (i % S), (i / S) & 1, err, 100000000ull);
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, Cfg::TMEM_COLS);
 }
 
-// Deterministic split-K reduction: partials summed in ascending split order.
-template <bool F32OUT>
-__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, int M, int N,
-                                     void* C, int64_t ldc) {
-  const int64_t total = int64_t(M) * N;
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    float acc = partial[i];
-    for (int z = 1; z < splits; ++z) acc += partial[int64_t(z) * total + i];
-    const int64_t row = i / N, col = i % N;
-    if (F32OUT)
-      static_cast<float*>(C)[row * ldc + col] = acc;
-    else
-      static_cast<uint16_t*>(C)[row * ldc + col] = f2bf(acc);
-  }
-}
+// ------------------------------------------------------------ bf16 kernel --
+// The K schedule of every bf16 GEMM.  K is cut into at most 8 chunks of
+// kc_blocks x 64 elements whose boundaries depend on K only.  Each chunk's
+// partial P_c is accumulated by tcgen05 from zero in ascending K steps of 16;
+// the output is the FP32 left fold r = P_0, r = r + P_1, ..., rounded once to
+// the output type.  Two ways of running that schedule give the same bits:
+//  - fold mode: a work item is a whole 128 x BN tile; the epilogue warps fold
+//    its chunks in registers as the MMA warp finishes them;
+//  - partial mode: a work item is one (tile, chunk) pair and its P_c goes to
+//    the workspace; gemm_fold_kernel then folds every element's partials in
+//    chunk order.  This spreads a few output tiles (decode-sized M) over every
+//    SM without changing any element's arithmetic.
+//
+// Persistent CTAs, 320 threads: warp 0 = TMA producer, warp 1 = MMA issuer
+// and TMEM owner, warps 2..9 = epilogue.  Epilogue warp w reads TMEM lanes
+// 32*(w%4).. (its lane quarter) and columns [h*BN/2, (h+1)*BN/2) with
+// h = (w-2)/4.  TMEM holds two BN-column accumulators (chunk double buffer).
+// Shared memory: S stages of B (BN x 64) then S stages of A (m_box x 64), and
+// a pad after the last A stage: the M=128 MMA reads 128 A rows, the rows past
+// m_box never feed a stored output row.
+struct GemmArgs {
+  void* C;
+  int64_t ldc;
+  int M, N, K;
+  int kc_blocks;        // K blocks of 64 per chunk
+  int m_box;            // rows of the A box (multiple of 16, <= 128)
+  int stages;           // pipeline depth (<= kMaxStages)
+  int partial;          // 1: partial mode
+  float4* ws;           // partial mode: [tiles][chunks][BN/4][m_box] float4 groups
+  int vec_ok;           // C rows 16-byte aligned
+  int n_fastest;        // fold mode: walk N tiles first
+  int* err;
+};
 
-// ----------------------------------------------------- persistent bf16 ----
-// Same per-element schedule as gemm_bf16_kernel (ascending 64-wide K blocks,
-// four K=16 MMAs each, FP32 accumulator in TMEM), so the two give identical
-// bits.  Persistent grid; warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
-// owner, warps 2..5 = epilogue.  The accumulator is double-buffered in TMEM so
-// the epilogue of tile j overlaps the main loop of tile j+1.  Tiles are walked
-// M-fastest so that CTAs running together share the weight tile in L2.
+constexpr int kMaxStages = 16;
+constexpr int kMaxChunks = 8;   // the invariant schedule cuts K into at most 8 chunks
+constexpr int kEpiWarps = 8;
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+
 template <int BN>
-struct PersistCfg {
-  static constexpr int BK = 64;
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
-  static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+struct GemmSmem {
+  static constexpr int B_STAGE = BN * 128;
+  // bytes of dynamic shared memory for `stages` stages of an m_box-row A box
+  static size_t bytes(int stages, int m_box) {
+    return 1024 + size_t(stages) * (B_STAGE + m_box * 128) + (128 - m_box) * 128 +
+           (2 * kMaxStages + 4) * 8 + 16;
+  }
 };
 
 template <int BN, bool F32OUT>
-__global__ void __launch_bounds__(192, 1)
-    gemm_bf16_persistent(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB, void* C, int64_t ldc, int M,
-                         int N, int K, int vec_ok, int n_fastest, int* err) {
-  // n_fastest: walk N tiles first (CTAs running together share an A tile and
-  // B is re-read from L2) when B is the smaller operand; else M first.
-  using Cfg = PersistCfg<BN>;
-  constexpr int S = Cfg::STAGES;
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+  constexpr int B_STAGE = GemmSmem<BN>::B_STAGE;
+  constexpr int HALF = BN / 2;
+  static_assert(HALF % 32 == 0, "epilogue reads 32-column groups");
+  // partial mode runs on tiles of at most 128 columns (register budget)
+  constexpr bool kPartialOk = BN <= 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + S * Cfg::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
-  const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
+  const int S = p.stages;
+  const int a_stage = p.m_box * 128;
+  uint8_t* sB = smem;
+  uint8_t* sA = smem + S * B_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + S * a_stage + (128 - p.m_box) * 128);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kMaxStages);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kMaxStages + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KB = (K + Cfg::BK - 1) / Cfg::BK;
-  const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+  const int KB = (p.K + 63) / 64;
+  const int chunks = (KB + p.kc_blocks - 1) / p.kc_blocks;
+  const int tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
   const int tiles = tiles_m * tiles_n;
+  const bool partial = kPartialOk && p.partial;
+  const int items = partial ? tiles * chunks : tiles;
+  // item -> tile and chunk range
+  auto item_tile = [&](int i) { return partial ? i / chunks : i; };
+  auto item_c0 = [&](int i) { return partial ? i % chunks : 0; };
+  auto item_c1 = [&](int i) { return partial ? i % chunks + 1 : chunks; };
+  auto tile_m0 = [&](int t) { return (p.n_fastest ? t / tiles_n : t % tiles_m) * BM; };
+  auto tile_n0 = [&](int t) { return (p.n_fastest ? t % tiles_n : t / tiles_m) * BN; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -264,97 +204,218 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(tfull0 + 8 * j, 1);
-      mbar_init(tempty0 + 8 * j, 4);
+      mbar_init(tempty0 + 8 * j, kEpiWarps);
     }
     fence_barrier_init();
   }
   __syncwarp();
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_alloc(smem_u32(tmem_slot), 2 * BN);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();  // TMEM is held: the next kernel in the stream may be scheduled
 
   int issued = 0;
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      const int m0 = (n_fastest ? t / tiles_n : t % tiles_m) * BM;
-      const int n0 = (n_fastest ? t % tiles_n : t / tiles_m) * BN;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int it = issued, s = it % S;
-        if (it >= S && !mbar_wait(empty0 + 8 * s, ((it / S) - 1) & 1, err)) {
-          ok = false;
-          break;
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      const uint32_t tx = uint32_t(a_stage + B_STAGE);
+      // The weights (B) of the first stages do not depend on the previous
+      // kernel: fetch them before waiting for it, then A and the rest.
+      int pre = 0;
+      {
+        const int i = blockIdx.x, n0 = tile_n0(item_tile(i));
+        const int kb0 = item_c0(i) * p.kc_blocks;
+        pre = min(S, min(KB, item_c1(i) * p.kc_blocks) - kb0);
+        for (int s = 0; s < pre; ++s) {
+          mbar_expect_tx(full0 + 8 * s, tx);
+          tma_load_2d(smem_u32(sB + s * B_STAGE), &tmB, full0 + 8 * s, (kb0 + s) * 64, n0);
         }
-        mbar_expect_tx(full0 + 8 * s, Cfg::STAGE);
-        tma_load_2d(smem_u32(sA + s * Cfg::A_BYTES), &tmA, full0 + 8 * s, kb * Cfg::BK, m0);
-        tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full0 + 8 * s, kb * Cfg::BK, n0);
-        issued = it + 1;
+      }
+      pdl_wait();
+      bool ok = true;
+      for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
+        const int t = item_tile(i), m0 = tile_m0(t), n0 = tile_n0(t);
+        const int kb1 = min(KB, item_c1(i) * p.kc_blocks);
+        for (int kb = item_c0(i) * p.kc_blocks; kb < kb1; ++kb) {
+          const int s = issued % S;
+          if (issued >= pre) {
+            if (issued >= S && !mbar_wait(empty0 + 8 * s, ((issued / S) - 1) & 1, p.err)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(full0 + 8 * s, tx);
+            tma_load_2d(smem_u32(sB + s * B_STAGE), &tmB, full0 + 8 * s, kb * 64, n0);
+          }
+          tma_load_2d(smem_u32(sA + s * a_stage), &tmA, full0 + 8 * s, kb * 64, m0);
+          ++issued;
+        }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = idesc_mma(1u, BM, BN);
-    int it = 0, j = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++j) {
-      const int b = j & 1;
-      if (j >= 2 && !mbar_wait(tempty0 + 8 * b, ((j >> 1) - 1) & 1, err)) break;
-      tc_fence_after();
-      const uint32_t dt = tmem + b * BN;
-      for (int kb = 0; kb < KB; ++kb, ++it) {
-        const int s = it % S;
-        if (!mbar_wait(full0 + 8 * s, (it / S) & 1, err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + s * Cfg::A_BYTES);
-        const uint32_t b0 = smem_u32(sB + s * Cfg::B_BYTES);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_mma(1u, BM, BN);
+      int it = 0, j = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
+        for (int c = item_c0(i); c < item_c1(i) && ok; ++c, ++j) {
+          const int b = j & 1;
+          if (j >= 2 && !mbar_wait(tempty0 + 8 * b, ((j >> 1) - 1) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t dt = tmem + b * BN;
+          const int kb0 = c * p.kc_blocks, kb1 = min(KB, kb0 + p.kc_blocks);
+          for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = it % S;
+            if (!mbar_wait(full0 + 8 * s, (it / S) & 1, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + s * a_stage);
+            const uint32_t b0 = smem_u32(sB + s * B_STAGE);
 #pragma unroll
-        for (int kk = 0; kk < Cfg::BK / 16; ++kk)
-          umma_f16(dt, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
-                   (kb | kk) != 0 ? 1u : 0u);
-        umma_commit(empty0 + 8 * s);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_f16(dt, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
+                       (kb != kb0 || kk != 0) ? 1u : 0u);
+            umma_commit(empty0 + 8 * s);
+          }
+          if (ok) umma_commit(tfull0 + 8 * b);
+        }
       }
-      umma_commit(tfull0 + 8 * b);
     }
-  } else if (warp >= 2) {
-    const int q = warp & 3;
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int q = warp & 3, col0 = ((warp - 2) >> 2) * HALF;
+    float r[HALF];
     int j = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
-      const int b = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * b, (j >> 1) & 1, err))) break;
-      tc_fence_after();
-      const int m0 = (n_fastest ? t / tiles_n : t % tiles_m) * BM;
-      const int n0 = (n_fastest ? t % tiles_n : t / tiles_m) * BN;
+    bool ok = true;
+    for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
+      const int t = item_tile(i), m0 = tile_m0(t), n0 = tile_n0(t);
       const int row = m0 + q * 32 + lane;
-      const uint32_t trow = tmem + b * BN + (uint32_t(q * 32) << 16);
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        if (n0 + c0 >= N) break;  // warp-uniform
-        uint32_t r[32];
-        tmem_ld32(trow + c0, r);
-        tmem_ld_wait();
-        if (row < M) store_row32<F32OUT>(C, ldc, row, n0 + c0, N, r, vec_ok != 0);
+      const int lrow = q * 32 + lane;        // row inside the tile
+      const bool live = row < p.M;
+      for (int c = item_c0(i); c < item_c1(i); ++c, ++j) {
+        const int b = j & 1;
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * b, (j >> 1) & 1, p.err)))
+          ok = false;
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ta = tmem + b * BN + col0 + (uint32_t(q * 32) << 16);
+        // partial layout: float4 group (column/4) major, row minor, so that a
+        // warp's 32 rows land in 512 contiguous bytes
+        float4* dst = partial && live
+                          ? p.ws + ((int64_t(t) * chunks + c) * (BN / 4) + col0 / 4) * p.m_box + lrow
+                          : nullptr;
+        // tcgen05.ld is warp-collective: every lane issues it, live row or not
+        if (partial) {
+#pragma unroll
+          for (int g = 0; g < HALF / 32; ++g) {
+            uint32_t v[32];
+            tmem_ld32(ta + g * 32, v);
+            tmem_ld_wait();
+            if (dst) {
+#pragma unroll
+              for (int x = 0; x < 32; x += 4)
+                dst[int64_t((g * 32 + x) / 4) * p.m_box] =
+                    make_float4(__uint_as_float(v[x]), __uint_as_float(v[x + 1]),
+                                __uint_as_float(v[x + 2]), __uint_as_float(v[x + 3]));
+            }
+          }
+        } else {
+          // 16-column loads keep the running sum plus one load in registers
+#pragma unroll
+          for (int g = 0; g < HALF / 16; ++g) {
+            uint32_t v[16];
+            tmem_ld16(ta + g * 16, v);
+            tmem_ld_wait();
+            if (c == 0) {
+#pragma unroll
+              for (int x = 0; x < 16; ++x) r[g * 16 + x] = __uint_as_float(v[x]);
+            } else {
+#pragma unroll
+              for (int x = 0; x < 16; ++x) r[g * 16 + x] = r[g * 16 + x] + __uint_as_float(v[x]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8 * b);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * b);
+      if (partial) continue;  // gemm_fold_kernel finishes the tile
+      if (!ok) break;
+      if (live) store_row_regs<HALF, F32OUT>(p.C, p.ldc, row, n0 + col0, p.N, r, p.vec_ok != 0);
     }
   }
+  // the producer makes sure its copies have landed before the CTA exits
   if (warp == 0 && lane == 0) {
     for (int i = max(0, issued - S); i < issued; ++i)
-      mbar_wait(full0 + 8 * (i % S), (i / S) & 1, err, 100000000ull);
+      mbar_wait(full0 + 8 * (i % S), (i / S) & 1, p.err, 100000000ull);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem, 2 * BN);
+}
+
+// Partial mode, second half: every output element's chunk partials folded in
+// chunk order, r = P_0, r = r + P_1, ..., rounded once.  One thread per
+// (tile, 4-column group, row); consecutive threads take consecutive rows, so
+// the partial reads are contiguous.  Tiles are in M-fastest order.
+template <bool F32OUT>
+__global__ void __launch_bounds__(256) gemm_fold_kernel(const float4* __restrict__ ws, void* C,
+                                                        int64_t ldc, int M, int N, int BN,
+                                                        int m_box, int tiles_m, int chunks,
+                                                        int64_t groups, int vec_ok) {
+  pdl_wait();  // the partials of the GEMM kernel before this one
+  pdl_trigger();
+  const int cgs = BN / 4;
+  const int64_t cstride = int64_t(cgs) * m_box;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < groups;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int lrow = int(i % m_box);
+    const int64_t rest = i / m_box;
+    const int cg = int(rest % cgs);
+    const int t = int(rest / cgs);
+    const int row = (t % tiles_m) * BM + lrow, n = (t / tiles_m) * BN + cg * 4;
+    if (row >= M || n >= N) continue;
+    const float4* src = ws + (int64_t(t) * chunks * cgs + cg) * m_box + lrow;
+    float4 v[kMaxChunks];
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c)
+      if (c < chunks) v[c] = __ldcg(src + c * cstride);
+    float r[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+#pragma unroll
+    for (int c = 1; c < kMaxChunks; ++c) {
+      if (c < chunks) {
+        r[0] = r[0] + v[c].x;
+        r[1] = r[1] + v[c].y;
+        r[2] = r[2] + v[c].z;
+        r[3] = r[3] + v[c].w;
+      }
+    }
+    if (F32OUT) {
+      float* dst = static_cast<float*>(C) + int64_t(row) * ldc + n;
+      if (vec_ok && n + 4 <= N) {
+        *reinterpret_cast<float4*>(dst) = make_float4(r[0], r[1], r[2], r[3]);
+      } else {
+        for (int j = 0; j < 4 && n + j < N; ++j) dst[j] = r[j];
+      }
+    } else {
+      uint16_t* dst = static_cast<uint16_t*>(C) + int64_t(row) * ldc + n;
+      if (vec_ok && n + 4 <= N) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf2(r[0], r[1]), pack_bf2(r[2], r[3]));
+      } else {
+        for (int j = 0; j < 4 && n + j < N; ++j) dst[j] = f2bf(r[j]);
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------- FP8 kernel --
@@ -519,145 +580,119 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void
 }
 
 struct Plan {
-  int bn = 128;
-  int splits = 1;
-  int kb_per_split = 0;
-  bool persistent = false;
-  int m_box = BM;  // rows of the A TMA box
+  int bn = 256;
+  int kc_blocks = 1;  // K blocks (of 64) per chunk
+  int chunks = 1;
+  bool partial = false;
+  int m_box = BM;     // rows of the A TMA box
+  int stages = 4;
+  int64_t tiles = 0;
+  size_t ws_bytes = 0;
 };
 
-// Few output tiles (decode-sized M): pick the tile width with the best
-// modelled weight-streaming rate.  Per 64-wide K block a CTA moves through
-// shared memory the A box (m_box rows), the B tile (TMA write) and the MMA's
-// operand reads (128 A rows + BN B rows, 4 times 32 bytes each), so the weight
-// share of that traffic is BN / (m_box + 2 BN + 128); CTAs beyond the SM
-// count add nothing.
-int pick_small_m_bn(int M, int N, int m_box, int sms) {
-  const int tiles_m = (M + BM - 1) / BM;
-  int best = 128;
-  double best_score = -1.0;
-  for (int bn : {256, 128, 64, 32}) {
-    if (bn > 32 && bn / 2 >= N) continue;
-    const double rate = double(bn) / double(m_box + 2 * bn + 128);
-    const int64_t ctas = int64_t((N + bn - 1) / bn) * tiles_m;
-    const double score = double(std::min<int64_t>(ctas, sms)) * rate;
-    if (score > best_score * 1.0001) {
-      best_score = score;
-      best = bn;
-    }
-  }
-  return best;
+constexpr size_t kSmemBudget = 225 * 1024;
+
+// Test overrides: BIV_GEMM_TILE_N=64|128|256 forces the tile width and
+// BIV_GEMM_FOLD=cta|partial the fold mode; the tests use them to check that
+// neither choice changes a result bit.
+int env_tile_n() {
+  const char* e = getenv("BIV_GEMM_TILE_N");
+  const int bn = e ? atoi(e) : 0;
+  return (bn == 64 || bn == 128 || bn == 256) ? bn : 0;
+}
+int env_fold() {  // 0 = planner, 1 = fold in the CTA, 2 = partials
+  const char* e = getenv("BIV_GEMM_FOLD");
+  if (!e) return 0;
+  if (!strcmp(e, "cta")) return 1;
+  if (!strcmp(e, "partial")) return 2;
+  return 0;
 }
 
-// Test overrides: BIV_GEMM_PERSISTENT=0 forces the one-tile-per-CTA kernel and
-// BIV_GEMM_TILE_N=32|64|128|256 forces the tile width; the tests use them to
-// check that neither choice changes a result bit.
-bool persistent_allowed() {
-  const char* e = getenv("BIV_GEMM_PERSISTENT");
-  return !(e && e[0] == '0');
-}
-
-// INVARIANT: the tile width depends on N only; K is never split.
-// FAST: for small M, narrow tiles and a K split sized to fill the GPU.
+// INVARIANT: K cut into min(8, K blocks) chunks of ceil(KB/8) blocks for every
+// M; the tile width and the fold mode follow M (neither changes a bit).
+// FAST (the batch-dependent comparator): no chunking for large M, and for
+// small M a K split sized to fill the GPU.
 Plan plan_bf16(const biv_gemm_desc& d) {
   Plan p;
   const int KB = (d.K + 63) / 64;
-  p.bn = d.N >= 8192 ? 256 : (d.N >= 128 ? 128 : (d.N > 32 ? 64 : 32));
-  p.kb_per_split = KB;
-  // The tile width (MMA instruction N) and the one-tile vs persistent kernel
-  // do not change any element's K schedule, and tcgen05 gives the same bits
-  // for every instruction N, so both may follow M.  Enough 128x256 tiles to
-  // fill the GPU: the widest tile on the persistent kernel (least shared-memory
-  // traffic per FLOP).
   const int sms = sm_count() > 0 ? sm_count() : 148;
-  const int64_t mt = (d.M + BM - 1) / BM;
-  if (d.N >= 256 && int64_t((d.N + 255) / 256) * mt >= sms) {
-    p.bn = 256;
+  const int64_t tiles_m = (d.M + BM - 1) / BM;
+  p.m_box = d.M <= BM ? std::max(16, (d.M + 15) / 16 * 16) : BM;
+  const int64_t tiles256 = int64_t((d.N + 255) / 256) * tiles_m;
+  const int64_t tiles128 = int64_t((d.N + 127) / 128) * tiles_m;
+  const bool wide = tiles256 >= sms;   // enough 128x256 tiles to fill the GPU
+  bool partial = !wide && tiles128 * 2 <= sms;
+  if (d.mode == BIV_MODE_INVARIANT) {
+    p.kc_blocks = (KB + kMaxChunks - 1) / kMaxChunks;
+  } else if (partial) {
+    const int64_t want = (sms + tiles128 - 1) / tiles128;
+    const int splits = int(std::max<int64_t>(1, std::min<int64_t>({want, int64_t(kMaxChunks), KB / 2})));
+    p.kc_blocks = (KB + splits - 1) / splits;
   } else {
-    p.m_box = d.M <= BM ? std::max(16, (d.M + 15) / 16 * 16) : BM;
-    p.bn = pick_small_m_bn(d.M, d.N, p.m_box, sms);
+    p.kc_blocks = KB;
   }
-  if (const char* e = getenv("BIV_GEMM_TILE_N")) {  // test override of the tile width
-    const int bn = atoi(e);
-    if (bn == 32 || bn == 64 || bn == 128 || bn == 256) p.bn = bn;
-  }
-  const int64_t tiles = int64_t((d.N + p.bn - 1) / p.bn) * mt;
-  p.persistent = tiles >= 2 * sms && persistent_allowed();
-  if (d.mode == BIV_MODE_FAST && d.M <= 256) {
-    // the batch-dependent comparator: same modelled tile, plus a K split that
-    // fills the GPU (this is what makes its bits depend on M)
-    p.persistent = false;
-    const int tiles = ((d.N + p.bn - 1) / p.bn) * ((d.M + BM - 1) / BM);
-    const int sms = sm_count() > 0 ? sm_count() : 148;
-    // split K only when the tiles leave most SMs idle; aim at one wave
-    int splits = tiles * 2 <= sms ? (sms + tiles - 1) / tiles : 1;
-    splits = std::max(1, std::min(splits, KB / 8));
-    p.kb_per_split = (KB + splits - 1) / splits;
-    p.splits = (KB + p.kb_per_split - 1) / p.kb_per_split;
-  }
+  p.chunks = (KB + p.kc_blocks - 1) / p.kc_blocks;
+  p.bn = wide ? 256 : 128;
+  if (const int bn = env_tile_n()) p.bn = bn;
+  if (const int f = env_fold()) partial = f == 2;
+  p.tiles = int64_t((d.N + p.bn - 1) / p.bn) * tiles_m;
+  // partial mode: more than one chunk, tiles of at most 128 columns
+  p.partial = partial && p.chunks > 1 && p.bn <= 128;
+  const int a_stage = p.m_box * 128, b_stage = p.bn * 128;
+  const size_t fixed = 1024 + size_t(128 - p.m_box) * 128 + (2 * kMaxStages + 4) * 8 + 16;
+  p.stages = int(std::min<size_t>(kMaxStages, (kSmemBudget - fixed) / (a_stage + b_stage)));
+  if (p.partial) p.ws_bytes = size_t(p.tiles) * p.chunks * p.m_box * p.bn * sizeof(float);
   return p;
 }
 
 template <int BN, bool F32OUT>
 biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_gemm_desc& d,
-                       const Plan& p, float* partial, cudaStream_t s) {
-  using Cfg = Bf16Cfg<BN>;
+                       const Plan& pl, void* ws, cudaStream_t s) {
   auto kern = gemm_bf16_kernel<BN, F32OUT>;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSmemBudget)) != cudaSuccess)
       return set_error(BIV_ERR_CUDA, "gemm: cannot set shared memory size");
     attr = true;
   }
   const int eb = F32OUT ? 4 : 2;
-  const int vec_ok = aligned16(d.C) && (d.ldc * eb) % 16 == 0;
-  dim3 grid((d.N + BN - 1) / BN, (d.M + BM - 1) / BM, p.splits);
-  kern<<<grid, 128, Cfg::SMEM, s>>>(ta, tb, d.C, d.ldc, d.M, d.N, d.K, p.kb_per_split,
-                                    p.splits > 1 ? partial : nullptr, vec_ok, p.m_box * 128,
-                                    device_error_word());
-  return check_launch("gemm_bf16");
-}
-
-template <int BN, bool F32OUT>
-biv_status launch_bf16_persistent(const CUtensorMap& ta, const CUtensorMap& tb,
-                                  const biv_gemm_desc& d, cudaStream_t s) {
-  using Cfg = PersistCfg<BN>;
-  auto kern = gemm_bf16_persistent<BN, F32OUT>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
-        cudaSuccess)
-      return set_error(BIV_ERR_CUDA, "gemm: cannot set shared memory size");
-    attr = true;
-  }
-  const int eb = F32OUT ? 4 : 2;
-  const int vec_ok = aligned16(d.C) && (d.ldc * eb) % 16 == 0;
-  const int tiles = ((d.N + BN - 1) / BN) * ((d.M + BM - 1) / BM);
+  GemmArgs a;
+  a.C = d.C;
+  a.ldc = d.ldc;
+  a.M = d.M;
+  a.N = d.N;
+  a.K = d.K;
+  a.kc_blocks = pl.kc_blocks;
+  a.m_box = pl.m_box;
+  a.stages = pl.stages;
+  a.partial = pl.partial ? 1 : 0;
+  a.ws = pl.partial ? static_cast<float4*>(ws) : nullptr;
+  a.vec_ok = aligned16(d.C) && (d.ldc * eb) % 16 == 0;
+  a.n_fastest = !pl.partial && d.N <= d.M;
+  a.err = device_error_word();
+  const int64_t items = pl.partial ? pl.tiles * pl.chunks : pl.tiles;
   const int sms = sm_count() > 0 ? sm_count() : 148;
-  const int grid = std::min(tiles, sms);
-  const int n_fastest = d.N <= d.M;
-  kern<<<grid, 192, Cfg::SMEM, s>>>(ta, tb, d.C, d.ldc, d.M, d.N, d.K, vec_ok, n_fastest,
-                                    device_error_word());
-  return check_launch("gemm_bf16_persistent");
+  const int grid = int(std::min<int64_t>(items, sms));
+  const size_t smem = GemmSmem<BN>::bytes(pl.stages, pl.m_box);
+  launch_pdl(kern, grid, kGemmThreads, smem, s, ta, tb, a);
+  biv_status st = check_launch("gemm_bf16");
+  if (st != BIV_OK || !pl.partial) return st;
+  const int64_t tiles_m = (d.M + BM - 1) / BM;
+  const int64_t groups = pl.tiles * (BN / 4) * pl.m_box;
+  const int blocks = int(std::min<int64_t>((groups + 255) / 256, int64_t(sms) * 8));
+  launch_pdl(gemm_fold_kernel<F32OUT>, blocks, 256, 0, s, static_cast<const float4*>(ws), d.C,
+             d.ldc, d.M, d.N, BN, pl.m_box, int(tiles_m), pl.chunks, groups, a.vec_ok);
+  return check_launch("gemm_fold");
 }
 
 template <bool F32OUT>
 biv_status dispatch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_gemm_desc& d,
-                         const Plan& p, float* partial, cudaStream_t s) {
-  if (p.persistent) {
-    switch (p.bn) {
-      case 256: return launch_bf16_persistent<256, F32OUT>(ta, tb, d, s);
-      case 128: return launch_bf16_persistent<128, F32OUT>(ta, tb, d, s);
-      case 64: return launch_bf16_persistent<64, F32OUT>(ta, tb, d, s);
-      default: return launch_bf16_persistent<32, F32OUT>(ta, tb, d, s);
-    }
-  }
+                         const Plan& p, void* ws, cudaStream_t s) {
   switch (p.bn) {
-    case 256: return launch_bf16<256, F32OUT>(ta, tb, d, p, partial, s);
-    case 128: return launch_bf16<128, F32OUT>(ta, tb, d, p, partial, s);
-    case 64: return launch_bf16<64, F32OUT>(ta, tb, d, p, partial, s);
-    default: return launch_bf16<32, F32OUT>(ta, tb, d, p, partial, s);
+    case 256: return launch_bf16<256, F32OUT>(ta, tb, d, p, ws, s);
+    case 128: return launch_bf16<128, F32OUT>(ta, tb, d, p, ws, s);
+    default: return launch_bf16<64, F32OUT>(ta, tb, d, p, ws, s);
   }
 }
 
@@ -720,11 +755,7 @@ biv_status biv_gemm_workspace(const biv_gemm_desc* d, size_t* bytes) {
   biv_status st = validate(d);
   if (st != BIV_OK) return st;
   BIV_REQUIRE(bytes, "gemm_workspace: null output");
-  *bytes = 0;
-  if (d->a_dtype == BIV_BF16) {
-    const Plan p = plan_bf16(*d);
-    if (p.splits > 1) *bytes = size_t(p.splits) * d->M * d->N * sizeof(float);
-  }
+  *bytes = d->a_dtype == BIV_BF16 ? plan_bf16(*d).ws_bytes : 0;
   return BIV_OK;
 }
 
@@ -736,24 +767,15 @@ biv_status biv_gemm(const biv_gemm_desc* d, void* ws, size_t ws_bytes, biv_strea
   CUtensorMap ta, tb;
   if (d->a_dtype == BIV_BF16) {
     const Plan p = plan_bf16(*d);
-    const size_t need = p.splits > 1 ? size_t(p.splits) * d->M * d->N * sizeof(float) : 0;
-    if (need && (!ws || ws_bytes < need))
-      return set_error(BIV_ERR_WORKSPACE, "gemm: workspace of %zu bytes needed", need);
-    if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->A, d->K, d->M, d->lda, 64,
-                  p.persistent ? BM : p.m_box) ||
+    if (p.ws_bytes && (!ws || ws_bytes < p.ws_bytes))
+      return set_error(BIV_ERR_WORKSPACE, "gemm: workspace of %zu bytes needed", p.ws_bytes);
+    if (p.ws_bytes && !aligned16(ws))
+      return set_error(BIV_ERR_INVALID, "gemm: workspace must be 16-byte aligned");
+    if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->A, d->K, d->M, d->lda, 64, p.m_box) ||
         !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->B, d->K, d->N, d->ldb, 64, p.bn))
       return set_error(BIV_ERR_CUDA, "gemm: tensor map encoding failed");
-    float* partial = static_cast<float*>(ws);
-    st = d->c_dtype == BIV_F32 ? dispatch_bf16<true>(ta, tb, *d, p, partial, s)
-                               : dispatch_bf16<false>(ta, tb, *d, p, partial, s);
-    if (st != BIV_OK || p.splits == 1) return st;
-    const int64_t total = int64_t(d->M) * d->N;
-    const int blocks = int(std::min<int64_t>((total + 255) / 256, int64_t(sm_count() * 16 + 1)));
-    if (d->c_dtype == BIV_F32)
-      splitk_reduce_kernel<true><<<blocks, 256, 0, s>>>(partial, p.splits, d->M, d->N, d->C, d->ldc);
-    else
-      splitk_reduce_kernel<false><<<blocks, 256, 0, s>>>(partial, p.splits, d->M, d->N, d->C, d->ldc);
-    return check_launch("gemm_splitk_reduce");
+    return d->c_dtype == BIV_F32 ? dispatch_bf16<true>(ta, tb, *d, p, ws, s)
+                                 : dispatch_bf16<false>(ta, tb, *d, p, ws, s);
   }
   // FP8 block-scaled (optionally grouped)
   const int groups = d->groups > 1 ? d->groups : 1;
@@ -766,3 +788,4 @@ biv_status biv_gemm(const biv_gemm_desc* d, void* ws, size_t ws_bytes, biv_strea
 }
 
 }  // extern "C"
+

@@ -39,6 +39,8 @@ __device__ __forceinline__ float warp_max(float v) {
 __global__ void embed_kernel(const int32_t* __restrict__ ids, const uint16_t* __restrict__ table,
                              int vocab, int d, uint16_t* __restrict__ h, int64_t h_stride,
                              int* err) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
   const int t = blockIdx.x;
   const int id = ids[t];
   uint4* dst = reinterpret_cast<uint4*>(h + int64_t(t) * h_stride);
@@ -60,6 +62,8 @@ template <int CPT>  // chunks per thread (ceil(d/8/256))
 __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
     const uint16_t* __restrict__ x, int64_t xs, uint16_t* __restrict__ r, int64_t rs,
     const uint16_t* __restrict__ w, uint16_t* __restrict__ y, int64_t ys, int d, float eps) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
   __shared__ float warp_ss[kNormThreads / 32];
   const int row = blockIdx.x;
   const int chunks = d / 8;
@@ -108,6 +112,8 @@ __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
 // ------------------------------------------------------------- SiLU-mul ----
 __global__ void silu_mul_kernel(const uint16_t* __restrict__ gu, int64_t gs,
                                 uint16_t* __restrict__ y, int64_t ys, int rows, int I) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
   const int cpr = I / 8;
   const int64_t total = int64_t(rows) * cpr;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
@@ -145,6 +151,8 @@ __global__ void qk_norm_rope_kernel(uint16_t* __restrict__ qkv, int64_t rs, int 
                                     const uint16_t* __restrict__ kw,
                                     const float* __restrict__ cos_sin, int max_pos,
                                     const int32_t* __restrict__ pos, float eps, int* err) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
   const int heads = Hq + Hkv;
   const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -202,6 +210,8 @@ __global__ void kv_store_bf16_kernel(const uint16_t* __restrict__ k,
                                      const uint16_t* __restrict__ v, int64_t rs,
                                      const int64_t* __restrict__ slot, int T, int Hkv, int D,
                                      uint16_t* __restrict__ kc, uint16_t* __restrict__ vc) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
   const int cpv = D / 8;  // 16-byte chunks per head vector
   const int64_t total = int64_t(T) * Hkv * cpv * 2;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
@@ -225,6 +235,8 @@ __global__ void kv_fp8_quant_kernel(const uint16_t* __restrict__ k,
                                     const int64_t* __restrict__ slot, int T, int Hkv, int D,
                                     uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
                                     float* __restrict__ ks, float* __restrict__ vs) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
   const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= int64_t(T) * Hkv * 2) return;
@@ -320,6 +332,8 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
 __global__ void __launch_bounds__(kLogprobThreads) logprob_kernel(
     const float* __restrict__ z, int64_t ld, const int32_t* __restrict__ target, int V,
     float* __restrict__ lp, int* err) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
   __shared__ float sm_m[kLogprobThreads / 32], sm_s[kLogprobThreads / 32];
   const int row = blockIdx.x;
   const float4* zr = reinterpret_cast<const float4*>(z + int64_t(row) * ld);
@@ -464,6 +478,8 @@ __global__ void __launch_bounds__(1024) moe_dispatch_kernel(const int32_t* __res
 __global__ void gather_rows_kernel(const uint8_t* __restrict__ src, int64_t ss,
                                    const int32_t* __restrict__ perm, int k_div, int n,
                                    int row_bytes, uint8_t* __restrict__ dst, int64_t ds) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
   const int cpr = row_bytes / 16;
   const int64_t total = int64_t(n) * cpr;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
@@ -526,8 +542,8 @@ biv_status biv_embed(const int32_t* ids, const uint16_t* table, int vocab, int T
   BIV_REQUIRE(T >= 0 && d > 0 && d % 8 == 0 && vocab > 0, "embed: bad sizes T=%d d=%d", T, d);
   if (T == 0) return BIV_OK;
   BIV_REQUIRE(ids && aligned16(table) && row_ok(h, h_stride, 2), "embed: bad pointer/stride");
-  embed_kernel<<<T, 128, 0, as_cuda(stream)>>>(ids, table, vocab, d, h, h_stride,
-                                              device_error_word());
+  launch_pdl(embed_kernel, T, 128, 0, as_cuda(stream), ids, table, vocab, d, h, h_stride,
+             device_error_word());
   return check_launch("embed");
 }
 
@@ -541,10 +557,10 @@ biv_status biv_add_rmsnorm(const uint16_t* x, int64_t xs, uint16_t* r, int64_t r
   const int cpt = (d / 8 + kNormThreads - 1) / kNormThreads;
   cudaStream_t s = as_cuda(stream);
   switch (cpt) {
-    case 1: add_rmsnorm_kernel<1><<<rows, kNormThreads, 0, s>>>(x, xs, r, rs, w, y, ys, d, eps); break;
-    case 2: add_rmsnorm_kernel<2><<<rows, kNormThreads, 0, s>>>(x, xs, r, rs, w, y, ys, d, eps); break;
-    case 3: add_rmsnorm_kernel<3><<<rows, kNormThreads, 0, s>>>(x, xs, r, rs, w, y, ys, d, eps); break;
-    default: add_rmsnorm_kernel<4><<<rows, kNormThreads, 0, s>>>(x, xs, r, rs, w, y, ys, d, eps); break;
+    case 1: launch_pdl(add_rmsnorm_kernel<1>, rows, kNormThreads, 0, s, x, xs, r, rs, w, y, ys, d, eps); break;
+    case 2: launch_pdl(add_rmsnorm_kernel<2>, rows, kNormThreads, 0, s, x, xs, r, rs, w, y, ys, d, eps); break;
+    case 3: launch_pdl(add_rmsnorm_kernel<3>, rows, kNormThreads, 0, s, x, xs, r, rs, w, y, ys, d, eps); break;
+    default: launch_pdl(add_rmsnorm_kernel<4>, rows, kNormThreads, 0, s, x, xs, r, rs, w, y, ys, d, eps); break;
   }
   return check_launch("add_rmsnorm");
 }
@@ -555,7 +571,7 @@ biv_status biv_silu_mul(const uint16_t* gu, int64_t gs, uint16_t* y, int64_t ys,
   if (rows == 0) return BIV_OK;
   BIV_REQUIRE(row_ok(gu, gs, 2) && row_ok(y, ys, 2), "silu_mul: misaligned rows");
   const int64_t work = int64_t(rows) * (I / 8);
-  silu_mul_kernel<<<grid_for(work, 256), 256, 0, as_cuda(stream)>>>(gu, gs, y, ys, rows, I);
+  launch_pdl(silu_mul_kernel, grid_for(work, 256), 256, 0, as_cuda(stream), gu, gs, y, ys, rows, I);
   return check_launch("silu_mul");
 }
 
@@ -577,8 +593,8 @@ biv_status biv_qk_norm_rope(uint16_t* qkv, int64_t rs, int T, int Hq, int Hkv, i
   const int64_t warps = int64_t(T) * (Hq + Hkv);
   const int threads = 256;
   const int64_t blocks = (warps * 32 + threads - 1) / threads;
-  qk_norm_rope_kernel<<<unsigned(blocks), threads, 0, as_cuda(stream)>>>(
-      qkv, rs, T, Hq, Hkv, D, q_w, k_w, cos_sin, max_pos, pos, eps, device_error_word());
+  launch_pdl(qk_norm_rope_kernel, unsigned(blocks), threads, 0, as_cuda(stream), qkv, rs, T, Hq,
+             Hkv, D, q_w, k_w, cos_sin, max_pos, pos, eps, device_error_word());
   return check_launch("qk_norm_rope");
 }
 
@@ -590,8 +606,8 @@ biv_status biv_kv_store_bf16(const uint16_t* k, const uint16_t* v, int64_t rs, c
   BIV_REQUIRE(row_ok(k, rs, 2) && row_ok(v, rs, 2) && aligned16(kc) && aligned16(vc) && slot,
               "kv_store_bf16: misaligned");
   const int64_t work = int64_t(T) * Hkv * (D / 8) * 2;
-  kv_store_bf16_kernel<<<grid_for(work, 256), 256, 0, as_cuda(stream)>>>(k, v, rs, slot, T, Hkv,
-                                                                         D, kc, vc);
+  launch_pdl(kv_store_bf16_kernel, grid_for(work, 256), 256, 0, as_cuda(stream), k, v, rs, slot, T,
+             Hkv, D, kc, vc);
   return check_launch("kv_store_bf16");
 }
 
@@ -603,8 +619,8 @@ biv_status biv_kv_fp8_quant(const uint16_t* k, const uint16_t* v, int64_t rs, co
   BIV_REQUIRE(k && v && slot && kc && vc && ks && vs, "kv_fp8_quant: null pointer");
   const int64_t warps = int64_t(T) * Hkv * 2;
   const int64_t blocks = (warps * 32 + 255) / 256;
-  kv_fp8_quant_kernel<<<unsigned(blocks), 256, 0, as_cuda(stream)>>>(k, v, rs, slot, T, Hkv, D,
-                                                                     kc, vc, ks, vs);
+  launch_pdl(kv_fp8_quant_kernel, unsigned(blocks), 256, 0, as_cuda(stream), k, v, rs, slot, T, Hkv,
+             D, kc, vc, ks, vs);
   return check_launch("kv_fp8_quant");
 }
 
@@ -638,8 +654,8 @@ biv_status biv_logprob(const float* z, int64_t ld, const int32_t* target, int T,
   BIV_REQUIRE(T >= 0 && V > 0 && V % 4 == 0, "logprob: V=%d must be a multiple of 4", V);
   if (T == 0) return BIV_OK;
   BIV_REQUIRE(row_ok(z, ld, 4) && target && lp, "logprob: logits rows must be 16-byte aligned");
-  logprob_kernel<<<T, kLogprobThreads, 0, as_cuda(stream)>>>(z, ld, target, V, lp,
-                                                           device_error_word());
+  launch_pdl(logprob_kernel, T, kLogprobThreads, 0, as_cuda(stream), z, ld, target, V, lp,
+             device_error_word());
   return check_launch("logprob");
 }
 
@@ -673,9 +689,9 @@ biv_status biv_gather_rows(const void* src, int64_t ss, const int32_t* perm, int
   BIV_REQUIRE(aligned16(src) && aligned16(dst) && ss % 16 == 0 && ds % 16 == 0 && perm,
               "gather_rows: misaligned");
   const int64_t work = int64_t(n) * (row_bytes / 16);
-  gather_rows_kernel<<<grid_for(work, 256), 256, 0, as_cuda(stream)>>>(
-      static_cast<const uint8_t*>(src), ss, perm, k_div, n, row_bytes,
-      static_cast<uint8_t*>(dst), ds);
+  launch_pdl(gather_rows_kernel, grid_for(work, 256), 256, 0, as_cuda(stream),
+             static_cast<const uint8_t*>(src), ss, perm, k_div, n, row_bytes,
+             static_cast<uint8_t*>(dst), ds);
   return check_launch("gather_rows");
 }
 

@@ -1,5 +1,6 @@
 // Host runtime of libbiv: error strings, device error word, SM count, the
 // timeout self-test, and the cached driver entry point for TMA descriptors.
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
@@ -52,6 +53,14 @@ biv_status check_launch(const char* what) {
   if (e != cudaSuccess)
     return set_error(BIV_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
   return BIV_OK;
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("BIV_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
 }
 
 int sm_count() {

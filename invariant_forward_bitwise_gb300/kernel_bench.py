@@ -27,6 +27,24 @@ case = sys.argv[1]
 reps = int(sys.argv[2]) if len(sys.argv) > 2 else 3
 g = synth.rng(0)
 
+def graph_time(fn, n):
+    """Device time of one fn() when n calls run back to back from a CUDA graph
+    (no host launch cost between them)."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(n):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
 def timeit(fn, n=reps):
     fn(); torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -88,6 +106,19 @@ elif case.startswith("attn"):
     kv_bytes = B * ctx * Hkv * D * 2 * 2
     flops = 4.0 * sum(p + 1 for _, p in rows) * Hq * D
     print(f"{case}: {ms*1e3:.1f} us  KV {kv_bytes/1e6:.0f} MB -> {kv_bytes/(ms/1e3)/1e9:.0f} GB/s;  {flops/(ms/1e3)/1e12:.1f} TFLOP/s")
+elif case == "gemm_prefill_layer":
+    # the four decoder-layer GEMMs at a 16384-row prefill step
+    M = 16384
+    for name, (N, K) in {"qkv": (4096, 2048), "o": (2048, 2048), "gate_up": (12288, 2048),
+                         "down": (2048, 6144)}.items():
+        a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+        b = (torch.randn(N, K, device="cuda") * 0.02).to(torch.bfloat16)
+        c = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        d = biv.gemm_desc(a, b, c)
+        ms = graph_time(lambda: biv.biv_gemm(d), reps)
+        print(f"{name:8s} M={M} N={N:6d} K={K}: {ms*1e3:8.1f} us  {2*M*N*K/(ms/1e3)/1e12:6.0f} TFLOP/s",
+              flush=True)
+        del a, b, c
 elif case == "gemm_sweep":
     # weights rotate through enough copies to exceed L2, as in a decode step
     # where every layer's weights are cold
@@ -102,7 +133,7 @@ elif case == "gemm_sweep":
                             dtype=torch.float32 if name == "lm_head" else torch.bfloat16)
             ds = [biv.gemm_desc(a, b, c) for b in bs]
             n = copies * max(1, 8 // copies)
-            ms = timeit(lambda: [biv.biv_gemm(ds[i % copies]) for i in range(n)], 1) / n
+            ms = graph_time(lambda: [biv.biv_gemm(ds[i % copies]) for i in range(n)], 1) / n
             print(f"{name:8s} M={M:4d} N={N:6d} K={K}: {ms*1e3:8.1f} us  weights {N*K*2/(ms/1e3)/1e9:6.0f} GB/s"
                   f"  {2*M*N*K/(ms/1e3)/1e12:6.1f} TFLOP/s", flush=True)
         del bs

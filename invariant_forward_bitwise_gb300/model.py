@@ -124,7 +124,8 @@ class DenseModel:
         self.qblocks = torch.zeros(T, 2, **i32)
         self.lm_rows = torch.zeros(T, **i32)
         self.targets = torch.zeros(T, **i32)
-        self.ws = torch.empty(16, dtype=torch.uint8, device=device)
+        self.ws = torch.empty(16, dtype=torch.uint8, device=device)     # attention partials
+        self.gws = torch.empty(256, dtype=torch.uint8, device=device)   # GEMM chunk partials
         self._old_ws: List[torch.Tensor] = []
         self.audit: Optional[list] = None  # when a list: residual stream copied after each layer
         self.launches = 0        # libbiv launches of the last step()
@@ -141,14 +142,14 @@ class DenseModel:
     def _gemm(self, A, Bw, Cout, M, stream=None):
         d = biv.gemm_desc(A, Bw, Cout, mode=self.mode, M=M)
         need = biv.biv_gemm_workspace(d)
-        if need > self.ws.numel():
-            raise RuntimeError(f"workspace too small ({need} > {self.ws.numel()}); call reserve()")
+        if need > self.gws.numel():
+            raise RuntimeError(f"GEMM workspace too small ({need} > {self.gws.numel()}); call reserve()")
         t = self._timer()
         tok = t.bracket("gemm_bf16", 2.0 * M * d.N * d.K, "flop") if t else None
-        biv.biv_gemm(d, self.ws if need else None, stream=stream)
+        biv.biv_gemm(d, self.gws, stream=stream)
         if tok:
             t.close(tok)
-        self.launches += 2 if need else 1
+        self.launches += 1
 
     def _attn_desc(self, kv: PagedKV, layer: int, spec: StepSpec, qblocks=None):
         cfg = self.cfg
@@ -172,8 +173,9 @@ class DenseModel:
         return d
 
     def reserve(self, kv: PagedKV, specs: Sequence[StepSpec]):
-        """Size the shared workspace for the given step shapes (before capture)."""
-        need = 16
+        """Size the attention and GEMM workspaces for the given step shapes
+        (before capture)."""
+        need, gneed = 16, 256
         cfg = self.cfg
         for s in specs:
             need = max(need, biv.biv_attention_workspace(self._attn_desc(kv, 0, s)))
@@ -186,7 +188,7 @@ class DenseModel:
                 d.lda = d.ldb = K
                 d.ldc = N
                 d.mode = self.mode
-                need = max(need, biv.biv_gemm_workspace(d))
+                gneed = max(gneed, biv.biv_gemm_workspace(d))
             d = biv.GemmDesc()
             d.M, d.N, d.K = min(s.T_lm, self.lm_chunk), cfg.vocab, cfg.hidden
             d.a_dtype = d.b_dtype = biv.BF16
@@ -195,11 +197,14 @@ class DenseModel:
             d.lda = d.ldb = cfg.hidden
             d.ldc = cfg.vocab
             d.mode = self.mode
-            need = max(need, biv.biv_gemm_workspace(d))
+            gneed = max(gneed, biv.biv_gemm_workspace(d))
+        # captured graphs keep the address they saw: never free a workspace
         if need > self.ws.numel():
-            # captured graphs keep the address they saw: never free a workspace
             self._old_ws.append(self.ws)
             self.ws = torch.empty(need, dtype=torch.uint8, device=self.ws.device)
+        if gneed > self.gws.numel():
+            self._old_ws.append(self.gws)
+            self.gws = torch.empty(gneed, dtype=torch.uint8, device=self.gws.device)
 
     # -- the forward ------------------------------------------------------------
     def step(self, kv: PagedKV, spec: StepSpec, qblocks=None, lm_rows=None):

@@ -218,3 +218,20 @@ def test_tma_loader_equals_thread_loader(B, D):
     dec = run_attn(B, pc, q[torch.tensor(last, device="cuda")], [rows[j] for j in last],
                    [(j, 1) for j in range(len(last))], 4, kv_split=128, tma=True)
     assert np.array_equal(bits(dec), bits(a[torch.tensor(last, device="cuda")]))
+
+
+@pytest.mark.parametrize("stages", ["2", "3"])
+def test_decode_pipeline_depth_changes_no_bit(B, monkeypatch, stages):
+    """The one-warp decode CTAs' TMA pipeline depth is a tuning choice: 1, 2 or
+    3 stages give the same bits, over several 64-key tiles and splits."""
+    g = synth.rng(77)
+    lens = [700, 130, 1500]
+    pc = Paged(B, g, lens, 8, 128)
+    last = [(i, L - 1) for i, L in enumerate(lens)]
+    q = synth.normal_bf16(g, (len(last), 16 * 128)).cuda()
+    blocks = [(j, 1) for j in range(len(last))]
+    ref = run_attn(B, pc, q, last, blocks, 16, kv_split=1024, tma=True)
+    monkeypatch.setenv("BIV_ATTN_DECODE_STAGES", stages)
+    got = run_attn(B, pc, q, last, blocks, 16, kv_split=1024, tma=True)
+    monkeypatch.delenv("BIV_ATTN_DECODE_STAGES")
+    assert np.array_equal(bits(got), bits(ref))

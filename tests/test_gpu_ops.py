@@ -384,25 +384,58 @@ def test_device_wait_timeout_reports_and_recovers(B):
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("M,N,K,out", [(4096, 2048, 2048, "bf16"), (2304, 12288, 512, "bf16"),
+@pytest.mark.parametrize("M,N,K,out", [(1, 2048, 2048, "bf16"), (77, 4096, 6144, "f32"),
+                                       (300, 1000, 520, "bf16"), (4096, 2048, 2048, "bf16"),
                                        (1200, 151936 // 4, 256, "f32")])
-def test_gemm_persistent_equals_one_tile_kernel(B, monkeypatch, M, N, K, out):
-    """Large M runs the persistent kernel; forcing the one-tile-per-CTA kernel
-    must give the same bits (same per-element K schedule)."""
-    g = synth.rng(M + N)
+def test_gemm_chunk_fold_in_cta_equals_fold_across_ctas(B, monkeypatch, M, N, K, out):
+    """The fixed K-chunk schedule folded inside one CTA (registers) and across
+    CTAs (per-chunk partials, folded in chunk order by a second kernel) must
+    give the same bits, call after call on one workspace."""
+    g = synth.rng(M + N + K)
     a, b = rnd_bf16(g, M, K), rnd_bf16(g, N, K, std=0.05)
     ad, bd = dev(a), dev(b)
     dt = torch.bfloat16 if out == "bf16" else torch.float32
-    c1 = torch.empty(M, N, dtype=dt, device="cuda")
-    B.biv_gemm(B.gemm_desc(ad, bd, c1))
-    monkeypatch.setenv("BIV_GEMM_PERSISTENT", "0")
-    c2 = torch.empty(M, N, dtype=dt, device="cuda")
-    B.biv_gemm(B.gemm_desc(ad, bd, c2))
-    torch.cuda.synchronize()
-    assert np.array_equal(bits(c1), bits(c2))
-    rows = np.array([0, 1, 777, M - 1])
+    res = []
+    for fold in ["cta", "partial", "partial"]:
+        monkeypatch.setenv("BIV_GEMM_FOLD", fold)
+        monkeypatch.setenv("BIV_GEMM_TILE_N", "128")
+        c = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
+        d = B.gemm_desc(ad, bd, c)
+        n = B.biv_gemm_workspace(d)
+        assert (n > 0) == (fold == "partial" and K > 64)
+        ws = torch.full((max(n, 256),), 0xFF, dtype=torch.uint8, device="cuda")  # no initial value needed
+        B.biv_gemm(d, ws)
+        B.biv_gemm(d, ws)
+        torch.cuda.synchronize()
+        res.append(bits(c))
+    monkeypatch.delenv("BIV_GEMM_FOLD")
+    monkeypatch.delenv("BIV_GEMM_TILE_N")
+    c = torch.empty(M, N, dtype=dt, device="cuda")
+    B.biv_gemm(B.gemm_desc(ad, bd, c))                  # the planner's own choice
+    res.append(bits(c))
+    for r in res[1:]:
+        assert np.array_equal(r, res[0])
+    rows = np.unique(np.array([0, M // 2, M - 1]))
     ref = ops.gemm(a.float().numpy()[rows], b.float().numpy(), out=out)
-    assert rel_err(host_f32(c1)[rows], ref) < REL
+    assert rel_err(host_f32(c)[rows], ref) < REL
+
+
+def test_gemm_shared_workspace_across_shapes(B):
+    """Calls of different shapes (different tile counts and chunk counts) on
+    one workspace give what each gives on a fresh one."""
+    g = synth.rng(5150)
+    shapes = [(100, 512, 2048), (7, 8192, 688), (64, 2048, 6144), (3, 4096, 2048), (100, 512, 2048)]
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    for M, N, K in shapes:
+        a, b = dev(rnd_bf16(g, M, K)), dev(rnd_bf16(g, N, K, std=0.05))
+        c1 = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        c2 = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        d1, d2 = B.gemm_desc(a, b, c1), B.gemm_desc(a, b, c2)
+        assert B.biv_gemm_workspace(d1) > 0
+        B.biv_gemm(d1, ws)
+        B.biv_gemm(d2, torch.zeros(B.biv_gemm_workspace(d2), dtype=torch.uint8, device="cuda"))
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(c1), bits(c2)), (M, N, K)
 
 
 @pytest.mark.parametrize("M,N,K", [(3, 512, 192), (100, 512, 2048), (7, 8192, 688), (300, 12288, 64),
@@ -410,12 +443,12 @@ def test_gemm_persistent_equals_one_tile_kernel(B, monkeypatch, M, N, K, out):
 def test_tcgen05_result_independent_of_tile_width(B, monkeypatch, M, N, K):
     """The hardware property the tile planner relies on: with the same K
     schedule an output element has the same bits whatever the MMA instruction
-    width (tile N) of its CTA, on the one-tile and the persistent kernel."""
+    width (tile N) of its CTA, whichever way the chunks are folded."""
     g = synth.rng(M * N + K)
     a, b = rnd_bf16(g, M, K), rnd_bf16(g, N, K, std=0.05)
     ad, bd = dev(a), dev(b)
     outs = []
-    for bn in ["32", "64", "128", "256"]:
+    for bn in ["64", "128", "256"]:
         monkeypatch.setenv("BIV_GEMM_TILE_N", bn)
         c = torch.empty(M, N, dtype=torch.float32, device="cuda")
         B.biv_gemm(B.gemm_desc(ad, bd, c))
