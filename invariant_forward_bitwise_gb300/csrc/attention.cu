@@ -33,19 +33,24 @@ constexpr int kTile = 64;   // keys per tile = one page
 constexpr int kNV = 64;     // most query vectors a CTA takes (4 warps x 16)
 constexpr float kLog2e = 1.4426950408889634f;
 
-// NW warps per CTA (16 query vectors each), ST-stage K/V pipeline, TMA or
-// thread-issued loads.  Decode blocks (<= 16 vectors) run NW = 1 with one TMA
-// stage (six CTAs per SM), prefill blocks NW = 4 with two stages.
-template <int D, int NW, int ST, bool TMA>
+// NW warps per CTA, ST-stage K/V pipeline, TMA or thread-issued loads, and
+// DS: 1 = each warp owns 16 query vectors (prefill blocks); DS = NW = every
+// warp forms the same S and softmax for one group of 16 vectors and takes
+// 1/DS of the head dimension in P.V (decode blocks: shorter dependency chains
+// per warp, the same arithmetic for every output element).
+template <int D, int NW, int ST, bool TMA, int DS>
 struct AttnCfg {
+  static_assert(DS == 1 || DS == NW, "D split: one warp per D slice");
   static constexpr int LD = D + 8;                   // padded row (elements), thread-loaded tiles
-  static constexpr int NV = NW * 16;                 // query vectors per CTA
+  static constexpr int NV = DS > 1 ? 16 : NW * 16;   // query vectors per CTA
   static constexpr int NT = NW * 32;                 // threads per CTA
   static constexpr int KVB = TMA ? kTile * D * 2 : kTile * LD * 2;  // one K or V stage
   static constexpr int Q_BYTES = NV * LD * 2;
   static constexpr int SMEM = 1024 + 2 * ST * KVB + Q_BYTES + ST * kTile * 4 + ST * 8;
   static constexpr int DK = D / 16;                  // k-steps of Q.K^T
   static constexpr int DT = D / 8;                   // n-tiles of O
+  static constexpr int DTW = DT / DS;                // n-tiles of O per warp
+  static_assert(DTW % 2 == 0, "P.V runs n-tile pairs");
   // byte offset of (row, dim) inside a K/V stage (dim a multiple of 8)
   __device__ static __forceinline__ uint32_t off(int row, int dim) {
     if (TMA) {
@@ -110,12 +115,13 @@ __device__ __forceinline__ int row_splits(const AttnArgs& a, int pos) {
   return a.topk_idx ? (a.topk + a.kv_split - 1) / a.kv_split : pos / a.kv_split + 1;
 }
 
-template <int D, int NW, int ST, bool TMA>
+template <int D, int NW, int ST, bool TMA, int DS>
 __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ AttnArgs a) {
   pdl_wait();     // stream predecessor done, its writes visible
   pdl_trigger();
-  using Cfg = AttnCfg<D, NW, ST, TMA>;
+  using Cfg = AttnCfg<D, NW, ST, TMA, DS>;
   constexpr int LD = Cfg::LD, NV = Cfg::NV, NT = Cfg::NT, KVB = Cfg::KVB;
+  constexpr int DTW = Cfg::DTW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -244,19 +250,22 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
     }
   };
 
-  // per-thread rows: g and g+8 of this warp's 16 vectors
+  // per-thread rows: g and g+8 of the warp's 16 vectors (vw: their group);
+  // O n-tiles dt0 .. dt0+DTW-1 of the head dimension
+  const int vw = DS > 1 ? 0 : warp;
+  const int dt0 = DS > 1 ? warp * DTW : 0;
   const int g = lane >> 2, cq = lane & 3;
   int vpos[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const int v = warp * 16 + g + 8 * i;
+    const int v = vw * 16 + g + 8 * i;
     vpos[i] = v < nv ? a.row_pos[r0 + v / a.G] : -1;
   }
 
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-  float acc[Cfg::DT][4];
+  float acc[DTW][4];
 #pragma unroll
-  for (int i = 0; i < Cfg::DT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  for (int i = 0; i < DTW; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
   __syncthreads();  // Q stored, barriers initialised
   // prologue.  TMA: tiles 0 .. ST-1 in flight, a stage is refilled right
@@ -271,7 +280,7 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
   // Q fragments (A operand), loaded once
   uint32_t qf[Cfg::DK][4];
   {
-    const uint32_t qbase = smem_u32(sQ + (warp * 16 + (lane & 15)) * LD + (lane >> 4) * 8);
+    const uint32_t qbase = smem_u32(sQ + (vw * 16 + (lane & 15)) * LD + (lane >> 4) * 8);
 #pragma unroll
     for (int kk = 0; kk < Cfg::DK; ++kk)
       ldsm_x4(qbase + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
@@ -300,7 +309,7 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
       if (t + ST - 1 < ntiles) load_tile((t + ST - 1) % ST, t + ST - 1);
       cp_async_commit();
     }
-    if (warp * 16 >= nv) {  // no live vector in this warp: only help with loads
+    if (vw * 16 >= nv) {  // no live vector in this warp: only help with loads
       __syncthreads();
       continue;
     }
@@ -401,7 +410,7 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
     // rescale only when some row's max moved (a factor of exactly 1 is a no-op)
     if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
-      for (int dt = 0; dt < Cfg::DT; ++dt) {
+      for (int dt = 0; dt < DTW; ++dt) {
         acc[dt][0] *= alpha[0];
         acc[dt][1] *= alpha[0];
         acc[dt][2] *= alpha[1];
@@ -416,12 +425,12 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
       const uint32_t al[4] = {pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3]};
       // V fragments of this k-step first, then every accumulator's hi MMA,
       // then every lo MMA (per accumulator still hi before lo, ks ascending)
-      constexpr int DPS = Cfg::DT / 2;
+      constexpr int DPS = DTW / 2;
       uint32_t vf[DPS][4];
 #pragma unroll
       for (int dp = 0; dp < DPS; ++dp) {
         const int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int dim = dp * 16 + (lane >> 4) * 8;
+        const int dim = (dt0 / 2 + dp) * 16 + (lane >> 4) * 8;
         ldsm_x4_t(tV + Cfg::off(key, dim), vf[dp][0], vf[dp][1], vf[dp][2], vf[dp][3]);
       }
 #pragma unroll
@@ -443,7 +452,7 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
   // ---- epilogue: single-split rows write the final output, others partials
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const int v = warp * 16 + g + 8 * i;
+    const int v = vw * 16 + g + 8 * i;
     if (v >= nv) continue;
     const int row = r0 + v / a.G;
     const int head = h * a.G + v % a.G;
@@ -453,18 +462,19 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
       const float inv_l = l[i] > 0.f ? 1.0f / l[i] : 0.f;
       uint16_t* dst = a.out + int64_t(row) * a.out_stride + int64_t(head) * D;
 #pragma unroll
-      for (int dt = 0; dt < Cfg::DT; ++dt) {
+      for (int dt = 0; dt < DTW; ++dt) {
         const float o0 = acc[dt][2 * i] * inv_l + 0.0f;
         const float o1 = acc[dt][2 * i + 1] * inv_l + 0.0f;
-        *reinterpret_cast<uint32_t*>(dst + dt * 8 + 2 * cq) = pack_bf2(o0, o1);
+        *reinterpret_cast<uint32_t*>(dst + (dt0 + dt) * 8 + 2 * cq) = pack_bf2(o0, o1);
       }
     } else {
       const int64_t slot = (int64_t(row) * a.Hq + head) * a.nsplit_grid + split;
       float* wo = a.ws_o + slot * D;
 #pragma unroll
-      for (int dt = 0; dt < Cfg::DT; ++dt)
-        *reinterpret_cast<float2*>(wo + dt * 8 + 2 * cq) = make_float2(acc[dt][2 * i], acc[dt][2 * i + 1]);
-      if (cq == 0) {
+      for (int dt = 0; dt < DTW; ++dt)
+        *reinterpret_cast<float2*>(wo + (dt0 + dt) * 8 + 2 * cq) =
+            make_float2(acc[dt][2 * i], acc[dt][2 * i + 1]);
+      if (cq == 0 && dt0 == 0) {
         a.ws_ml[2 * slot] = m[i];
         a.ws_ml[2 * slot + 1] = l[i];
       }
@@ -551,19 +561,27 @@ size_t ws_bytes(const biv_attn_desc& d, int split) {
   return size_t(d.T) * d.Hq * ns * (d.D + 2) * sizeof(float);
 }
 
-template <int D, int NW, int ST, bool TMA>
+template <int D, int NW, int ST, bool TMA, int DS = 1>
 biv_status launch_cfg(const biv_attn_desc& d, const AttnArgs& a, cudaStream_t s) {
-  using Cfg = AttnCfg<D, NW, ST, TMA>;
+  using Cfg = AttnCfg<D, NW, ST, TMA, DS>;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attn_kernel<D, NW, ST, TMA>,
+    if (cudaFuncSetAttribute(attn_kernel<D, NW, ST, TMA, DS>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
       return set_error(BIV_ERR_CUDA, "attention: cannot set shared memory size");
     attr = true;
   }
   dim3 grid(d.nqblocks, d.Hkv, a.nsplit_grid);
-  launch_pdl(attn_kernel<D, NW, ST, TMA>, grid, Cfg::NT, Cfg::SMEM, s, a);
+  launch_pdl(attn_kernel<D, NW, ST, TMA, DS>, grid, Cfg::NT, Cfg::SMEM, s, a);
   return check_launch("attention");
+}
+
+// Decode CTAs (TMA loads): DS warps split the head dimension, ST stages.
+template <int D, int DS>
+biv_status launch_decode(const biv_attn_desc& d, const AttnArgs& a, int st, cudaStream_t s) {
+  if (st == 1) return launch_cfg<D, DS, 1, true, DS>(d, a, s);
+  if (st == 2) return launch_cfg<D, DS, 2, true, DS>(d, a, s);
+  return launch_cfg<D, DS, 3, true, DS>(d, a, s);
 }
 
 // bf16 cache of one layer as a 2-D tensor [num_pages*64 slots, Hkv*D], boxes of
@@ -580,15 +598,32 @@ bool make_kv_map(CUtensorMap* m, const void* base, int num_pages, int Hkv, int D
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Pipeline depth of the one-warp TMA decode CTAs (BIV_ATTN_DECODE_STAGES =
-// 1, 2 or 3; a tuning override, the depth changes no result bit).  Default 1:
-// a CTA is latency-bound on its own instruction stream, so six one-stage CTAs
-// per SM move more KV than three two-stage ones (measured on GB300: 5.9 vs
-// 4.6 TB/s on 256 sequences x 700 tokens).
-int decode_stages() {
-  const char* e = getenv("BIV_ATTN_DECODE_STAGES");
-  const int v = e ? atoi(e) : 1;
-  return (v >= 1 && v <= 3) ? v : 1;
+// Decode CTAs (at most 16 query vectors, TMA loads): the pipeline depth and
+// the number of warps that split the head dimension change no result bit,
+// only speed.  A CTA is latency-bound on its own instruction stream, so many
+// shallow one-warp CTAs per SM move the most KV when the grid is large
+// (measured on GB300, 256 sequences x 700 tokens: one stage 5.8 TB/s, two
+// 4.6, three 3.5); a small grid (few sequences) is faster with two warps
+// sharing the head dimension and two stages (4 sequences: 27 vs 30 us).
+// BIV_ATTN_DECODE_STAGES (1-3) and BIV_ATTN_DECODE_DSPLIT (1, 2, 4) override
+// the choice (tuning and tests).
+int env_int(const char* name, int lo, int hi) {
+  const char* e = getenv(name);
+  const int v = e ? atoi(e) : 0;
+  return (v >= lo && v <= hi) ? v : 0;
+}
+bool decode_grid_small(int64_t ctas) {
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  return ctas < 2 * int64_t(sms);
+}
+int decode_stages(int64_t ctas) {
+  if (const int v = env_int("BIV_ATTN_DECODE_STAGES", 1, 3)) return v;
+  return decode_grid_small(ctas) ? 2 : 1;
+}
+int decode_dsplit(int64_t ctas) {
+  const int v = env_int("BIV_ATTN_DECODE_DSPLIT", 1, 4);
+  if (v == 1 || v == 2 || v == 4) return v;
+  return decode_grid_small(ctas) ? 2 : 1;
 }
 
 template <int D>
@@ -602,15 +637,16 @@ biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
           make_kv_map(&a.tmK, d.k_cache, d.num_pages, d.Hkv, D) &&
           make_kv_map(&a.tmV, d.v_cache, d.num_pages, d.Hkv, D);
     if (tma) {
-      const int ds = decode_stages();
-      if (!small)
+      if (!small) {
         st = launch_cfg<D, 4, 2, true>(d, a, s);
-      else if (ds == 1)
-        st = launch_cfg<D, 1, 1, true>(d, a, s);
-      else if (ds == 3)
-        st = launch_cfg<D, 1, 3, true>(d, a, s);
-      else
-        st = launch_cfg<D, 1, 2, true>(d, a, s);
+      } else {
+        const int64_t ctas = int64_t(d.nqblocks) * d.Hkv * a.nsplit_grid;
+        const int stages = decode_stages(ctas);
+        const int dsplit = decode_dsplit(ctas);
+        st = dsplit == 1   ? launch_decode<D, 1>(d, a, stages, s)
+             : dsplit == 4 ? launch_decode<D, 4>(d, a, stages, s)
+                           : launch_decode<D, 2>(d, a, stages, s);
+      }
     }
   }
   if (!tma) st = small ? launch_cfg<D, 1, 2, false>(d, a, s) : launch_cfg<D, 4, 2, false>(d, a, s);

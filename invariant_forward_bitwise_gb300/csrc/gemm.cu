@@ -152,13 +152,18 @@ constexpr int kMaxChunks = 8;   // the invariant schedule cuts K into at most 8 
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
+// Epilogue staging: per epilogue warp a 32 x 33 FP32 block, used to turn its
+// row-per-lane results into row-contiguous (coalesced) global stores.
+constexpr int kStagePitch = 33;
+constexpr size_t kStagingBytes = size_t(kEpiWarps) * 32 * kStagePitch * 4;
+
 template <int BN>
 struct GemmSmem {
   static constexpr int B_STAGE = BN * 128;
   // bytes of dynamic shared memory for `stages` stages of an m_box-row A box
   static size_t bytes(int stages, int m_box) {
     return 1024 + size_t(stages) * (B_STAGE + m_box * 128) + (128 - m_box) * 128 +
-           (2 * kMaxStages + 4) * 8 + 16;
+           (2 * kMaxStages + 4) * 8 + 16 + kStagingBytes;
   }
 };
 
@@ -182,6 +187,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tfull0 = smem_u32(bars + 2 * kMaxStages);
   const uint32_t tempty0 = smem_u32(bars + 2 * kMaxStages + 2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 4);
+  float* staging = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) +
+                                            (2 * kMaxStages + 4) * 8 + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = (p.K + 63) / 64;
@@ -351,7 +358,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (partial) continue;  // gemm_fold_kernel finishes the tile
       if (!ok) break;
-      if (live) store_row_regs<HALF, F32OUT>(p.C, p.ldc, row, n0 + col0, p.N, r, p.vec_ok != 0);
+      // store through the warp's staging block: lane l writes its row, then
+      // the warp reads it back as 16-byte row pieces (W columns per lane,
+      // LPR lanes per row), so a store instruction writes RPI whole row
+      // segments instead of 32 scattered pieces
+      constexpr int W = F32OUT ? 4 : 8;
+      constexpr int LPR = 32 / W, RPI = 32 / LPR;
+      float* stg = staging + (warp - 2) * 32 * kStagePitch;
+      const int rows = min(32, p.M - (m0 + q * 32));   // live rows of this warp
+      const int sub = lane % LPR, rsub = lane / LPR;
+#pragma unroll
+      for (int blk = 0; blk < HALF / 32; ++blk) {
+        __syncwarp();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) stg[lane * kStagePitch + x] = r[blk * 32 + x];
+        __syncwarp();
+        const int n = n0 + col0 + blk * 32 + sub * W;
+#pragma unroll
+        for (int it = 0; it < 32 / RPI; ++it) {
+          const int j = it * RPI + rsub;
+          if (j >= rows || n >= p.N) continue;
+          float v[W];
+#pragma unroll
+          for (int e = 0; e < W; ++e) v[e] = stg[j * kStagePitch + sub * W + e];
+          const int64_t off = int64_t(m0 + q * 32 + j) * p.ldc + n;
+          if (p.vec_ok && n + W <= p.N) {
+            if (F32OUT)
+              *reinterpret_cast<float4*>(static_cast<float*>(p.C) + off) =
+                  make_float4(v[0], v[1], v[2], v[3]);
+            else
+              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.C) + off) =
+                  make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]),
+                             pack_bf2(v[6], v[7]));
+          } else {
+            for (int e = 0; e < W && n + e < p.N; ++e) {
+              if (F32OUT)
+                static_cast<float*>(p.C)[off + e] = v[e];
+              else
+                static_cast<uint16_t*>(p.C)[off + e] = f2bf(v[e]);
+            }
+          }
+        }
+      }
     }
   }
   // the producer makes sure its copies have landed before the CTA exits
@@ -590,7 +638,7 @@ struct Plan {
   size_t ws_bytes = 0;
 };
 
-constexpr size_t kSmemBudget = 225 * 1024;
+constexpr size_t kSmemBudget = 227 * 1024;  // the per-CTA maximum
 
 // Test overrides: BIV_GEMM_TILE_N=64|128|256 forces the tile width and
 // BIV_GEMM_FOLD=cta|partial the fold mode; the tests use them to check that
@@ -639,7 +687,8 @@ Plan plan_bf16(const biv_gemm_desc& d) {
   // partial mode: more than one chunk, tiles of at most 128 columns
   p.partial = partial && p.chunks > 1 && p.bn <= 128;
   const int a_stage = p.m_box * 128, b_stage = p.bn * 128;
-  const size_t fixed = 1024 + size_t(128 - p.m_box) * 128 + (2 * kMaxStages + 4) * 8 + 16;
+  const size_t fixed = 1024 + size_t(128 - p.m_box) * 128 + (2 * kMaxStages + 4) * 8 + 16 +
+                       kStagingBytes;
   p.stages = int(std::min<size_t>(kMaxStages, (kSmemBudget - fixed) / (a_stage + b_stage)));
   if (p.partial) p.ws_bytes = size_t(p.tiles) * p.chunks * p.m_box * p.bn * sizeof(float);
   return p;

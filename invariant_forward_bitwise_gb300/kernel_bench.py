@@ -3,9 +3,14 @@
   python -m invariant_forward_bitwise_gb300.kernel_bench CASE [REPS]
 
 CASE is one of attn_decode (256 sequences x 700 context, one decode row each),
+attn_decode4 (the same for 4 sequences),
 attn_prefill (8 sequences x 1024 tokens), gemm_prefill (M 8192, N 2048,
 K 6144), gemm_decode (M 64, N 2048, K 6144), lm_head (M 4096, N 151936,
-K 2048), ssd_prefill (16384 tokens, 64 heads) and ssd_decode (one token).
+K 2048), ssd_prefill (16384 tokens, 64 heads), ssd_decode (one token), topk_indexer
+(4096 rows x 32768 scores, top 2048), moe_block (4096 tokens through the
+64-expert FP8 block) and decode_step (one decode step of the 28-layer model
+at batch BIV_BENCH_BATCH, default 64, from its CUDA graph and eagerly; the
+eager step runs inside cudaProfilerStart/Stop for an ncu launch list).
 Each case times REPS calls with CUDA events after one warm-up call and
 prints the time and the rate against the case's algorithmic bytes or FLOPs;
 it is also the command that the ncu summaries in profiles/ capture.
@@ -53,7 +58,82 @@ def timeit(fn, n=reps):
     e1.record(); torch.cuda.synchronize()
     return e0.elapsed_time(e1) / n
 
-if case.startswith("ssd"):
+def fp8_codes(*shape):
+    """e4m3 codes of N(0, 64) draws (clipped to the finite range), as uint8."""
+    x = (torch.randn(*shape, device="cuda") * 64).clamp(-448, 448)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+def block_scales(*shape):
+    return (0.02 / 64) * torch.exp2(torch.rand(*shape, device="cuda") * 2 - 1)
+
+if case == "decode_step":
+    # one decode step of the 28-layer Qwen3-1.7B shape at batch B (every
+    # sequence at position 700): prefill fills the caches, then the step is
+    # timed replayed from its CUDA graph, and run once eagerly inside
+    # cudaProfilerStart/Stop (for ncu --profile-from-start off)
+    from invariant_forward_bitwise_gb300.model import DecodeGraphs, DenseModel, PagedKV, Runner, prefill_rows
+    Bn = int(os.environ.get("BIV_BENCH_BATCH", "64"))
+    cfg = synth.QWEN3_1P7B
+    m = DenseModel(cfg, synth.dense_weights(cfg, seed=0), max_rows=16384, max_pos=1536)
+    kv = PagedKV(cfg, pages=Bn * 12 + 8, max_seqs=Bn, max_pages=24)
+    ctx = 700
+    for i in range(Bn):
+        kv.admit(i, 768)
+    kv.sync_table()
+    run = Runner(m)
+    toks = g.integers(0, cfg.vocab, size=(Bn, ctx + 1)).astype(np.int32)
+    for i0 in range(0, Bn, 16):
+        ii = list(range(i0, min(Bn, i0 + 16)))
+        seqs = [synth.Sequence(toks[i], 1) for i in ii]
+        rows = prefill_rows(seqs, ii, [0] * len(ii), [ctx] * len(ii), [10**9] * len(ii))
+        spec = run.load_rows(kv, *rows[:5])
+        m.reserve(kv, [spec])
+        m.step(kv, spec)
+    args = (list(range(Bn)), [ctx] * Bn, [1] * Bn, [2] * Bn)
+    for use in (True, False):
+        dg = DecodeGraphs(m, kv, use_graphs=use)
+        for _ in range(3):
+            dg.run(*args)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            dg.run(*args)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        kvb = Bn * ctx * 28 * cfg.kv_heads * cfg.head_dim * 2 * 2
+        print(f"decode_step {'graph' if use else 'eager'} batch {Bn}: {ms:.3f} ms  "
+              f"(weights 3.44 GB + KV {kvb/1e9:.2f} GB -> {(3.44e9 + kvb)/(ms/1e3)/1e9:.0f} GB/s)", flush=True)
+    torch.cuda.cudart().cudaProfilerStart()
+    dg.run(*args)
+    torch.cuda.synchronize()
+    torch.cuda.cudart().cudaProfilerStop()
+elif case == "topk_indexer":
+    # 4096 query rows over a 32768-key context, top 2048 per row
+    R, n, k = 4096, 32768, 2048
+    scores = torch.randn(R, n, device="cuda")
+    valid = torch.arange(n - R, n, dtype=torch.int32, device="cuda") + 1
+    idx = torch.empty(R, k, dtype=torch.int32, device="cuda")
+    ms = graph_time(lambda: biv.biv_topk(scores, valid, k, idx), reps)
+    rd = R * n * 4
+    print(f"topk_indexer {R}x{n} k={k}: {ms*1e3:.1f} us  scores {rd/1e6:.0f} MB -> {rd/(ms/1e3)/1e9:.0f} GB/s")
+elif case == "moe_block":
+    # 4096 tokens, hidden 4096, 64 routed experts top-6 + 1 shared, expert I 1408
+    from invariant_forward_bitwise_gb300.moe import MoEBlock
+    T, E, k, d, I = 4096, 64, 6, 4096, 1408
+    wr = (torch.randn(E, d, device="cuda") * 0.05).to(torch.bfloat16)
+    blk = MoEBlock(wr, fp8_codes(E, 2 * I, d), block_scales(E, 2 * I // 128, d // 128),
+                   fp8_codes(E, d, I), block_scales(E, d // 128, I // 128),
+                   fp8_codes(2 * I, d), block_scales(2 * I // 128, d // 128),
+                   fp8_codes(d, I), block_scales(d // 128, I // 128), top_k=k, max_tokens=T)
+    h = torch.randn(T, d, device="cuda").to(torch.bfloat16)
+    ms = graph_time(lambda: blk.forward(h), reps)
+    flops = 2.0 * T * (k + 1) * 3 * d * I
+    wbytes = (E + 1) * 3 * d * I
+    print(f"moe_block T={T} E={E} top{k}: {ms*1e3:.1f} us  expert FP8 {flops/(ms/1e3)/1e12:.0f} TFLOP/s  "
+          f"weights {wbytes/1e6:.0f} MB")
+elif case.startswith("ssd"):
     H, P, N, Q = 64, 64, 128, 256
     T = 16384 if case == "ssd_prefill" else 1
     x, dt, A, Bm, Cm, D = synth.ssd_inputs(g, T)
@@ -74,13 +154,13 @@ if case.startswith("ssd"):
     print(f"{case} T={T}: {ms*1e3:.1f} us  ({T/(ms/1e3):.0f} tokens/s per sequence)")
 elif case.startswith("attn"):
     Hq, Hkv, D = 16, 8, 128
-    B, ctx = (256, 700) if case == "attn_decode" else (8, 1024)
+    B, ctx = {"attn_decode": (256, 700), "attn_decode4": (4, 700)}.get(case, (8, 1024))
     pages_per = (ctx + 63) // 64
     P = B * pages_per
     kc = (torch.randn(P, 64, Hkv, D, device="cuda") * 0.5).to(torch.bfloat16)
     vc = (torch.randn(P, 64, Hkv, D, device="cuda") * 0.5).to(torch.bfloat16)
     bt = torch.arange(P, dtype=torch.int32, device="cuda").view(B, pages_per)
-    if case == "attn_decode":
+    if case.startswith("attn_decode"):
         rows = [(i, ctx - 1) for i in range(B)]
         blocks = [(i, 1) for i in range(B)]
     else:
@@ -102,7 +182,7 @@ elif case.startswith("attn"):
     d.page, d.kv_split, d.max_ctx, d.scale, d.num_pages = 64, 1024, ctx, 1 / math.sqrt(D), P
     n = biv.biv_attention_workspace(d)
     ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
-    ms = timeit(lambda: biv.biv_attention(d, ws))
+    ms = graph_time(lambda: biv.biv_attention(d, ws), reps)
     kv_bytes = B * ctx * Hkv * D * 2 * 2
     flops = 4.0 * sum(p + 1 for _, p in rows) * Hq * D
     print(f"{case}: {ms*1e3:.1f} us  KV {kv_bytes/1e6:.0f} MB -> {kv_bytes/(ms/1e3)/1e9:.0f} GB/s;  {flops/(ms/1e3)/1e12:.1f} TFLOP/s")

@@ -149,7 +149,7 @@ class DenseModel:
         biv.biv_gemm(d, self.gws, stream=stream)
         if tok:
             t.close(tok)
-        self.launches += 1
+        self.launches += 2 if need else 1   # chunk partials add the fold kernel
 
     def _attn_desc(self, kv: PagedKV, layer: int, spec: StepSpec, qblocks=None):
         cfg = self.cfg
@@ -258,7 +258,8 @@ class DenseModel:
                 self.audit.append(("mlp_out", l, self.a[:T].clone()))
             nxt = W[f"l{l + 1}.attn_norm"] if l + 1 < cfg.layers else W["final_norm"]
             biv.biv_add_rmsnorm(self.a[:T], r, nxt, y, eps, stream=st)
-            self.launches += 6 + (2 if need else 1)
+            # qk_norm_rope, KV store, attention (+ split merge), 2 x add_rmsnorm, silu_mul
+            self.launches += 6 + (1 if need else 0)
             if self.audit is not None and not torch.cuda.is_current_stream_capturing():
                 self.audit.append(("layer", l, r.clone()))
         # LM head + logprob over the rows that produce a logprob

@@ -220,18 +220,29 @@ def test_tma_loader_equals_thread_loader(B, D):
     assert np.array_equal(bits(dec), bits(a[torch.tensor(last, device="cuda")]))
 
 
-@pytest.mark.parametrize("stages", ["2", "3"])
-def test_decode_pipeline_depth_changes_no_bit(B, monkeypatch, stages):
-    """The one-warp decode CTAs' TMA pipeline depth is a tuning choice: 1, 2 or
-    3 stages give the same bits, over several 64-key tiles and splits."""
-    g = synth.rng(77)
+@pytest.mark.parametrize("stages,dsplit", [("1", "1"), ("2", "2"), ("3", "4"), ("1", "4")])
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_cta_shape_changes_no_bit(B, monkeypatch, stages, dsplit, D):
+    """The decode CTAs' TMA pipeline depth and the number of warps that split
+    the head dimension are speed choices: every one gives the bits of one
+    warp with a two-stage pipeline, over several 64-key tiles and splits."""
+    g = synth.rng(77 + D)
     lens = [700, 130, 1500]
-    pc = Paged(B, g, lens, 8, 128)
+    pc = Paged(B, g, lens, 8, D)
     last = [(i, L - 1) for i, L in enumerate(lens)]
-    q = synth.normal_bf16(g, (len(last), 16 * 128)).cuda()
+    q = synth.normal_bf16(g, (len(last), 16 * D)).cuda()
     blocks = [(j, 1) for j in range(len(last))]
+    monkeypatch.setenv("BIV_ATTN_DECODE_STAGES", "2")
+    monkeypatch.setenv("BIV_ATTN_DECODE_DSPLIT", "1")
     ref = run_attn(B, pc, q, last, blocks, 16, kv_split=1024, tma=True)
     monkeypatch.setenv("BIV_ATTN_DECODE_STAGES", stages)
+    monkeypatch.setenv("BIV_ATTN_DECODE_DSPLIT", dsplit)
     got = run_attn(B, pc, q, last, blocks, 16, kv_split=1024, tma=True)
-    monkeypatch.delenv("BIV_ATTN_DECODE_STAGES")
     assert np.array_equal(bits(got), bits(ref))
+    # and the prefill CTA shape gives the same row bits (one operator for both)
+    rows = [(i, p) for i, L in enumerate(lens) for p in range(L)]
+    qp = synth.normal_bf16(g, (len(rows), 16 * D)).cuda()
+    full = run_attn(B, pc, qp, rows, blocks_of(rows, 32), 16, kv_split=1024, tma=True)
+    idx = [sum(lens[:i + 1]) - 1 for i in range(len(lens))]
+    dec = run_attn(B, pc, qp[torch.tensor(idx, device="cuda")], last, blocks, 16, kv_split=1024, tma=True)
+    assert np.array_equal(bits(dec), bits(full[torch.tensor(idx, device="cuda")]))
