@@ -218,8 +218,8 @@ biv_status biv_attention_noalloc(const biv_attn_desc* desc, biv_stream_t stream)
  * split).  A and B are K-major (row-major with K contiguous).  INVARIANT
  * mode, whatever M is:
  *  - bf16 x bf16 -> bf16 or f32 (c_dtype): with KB = ceil(K/64), K is cut
- *    into chunks of ceil(KB/8) blocks of 64 (at most 8 chunks, the last may
- *    be shorter); each chunk P_c is accumulated in FP32 from zero in
+ *    into chunks of max(8, ceil(KB/8)) blocks of 64 (at most 8 chunks, the
+ *    last may be shorter); each chunk P_c is accumulated in FP32 from zero in
  *    ascending K steps of 16; the output is the left fold r = P_0,
  *    r = r + P_1, ... in FP32, rounded once to c_dtype.
  *  - e4m3 x e4m3 -> bf16 with block scales: per 128-wide K block kb,
@@ -268,7 +268,7 @@ biv_status biv_act_quant_fp8(const uint16_t* x, int64_t x_stride, int rows, int 
  * scores, equal scores resolved toward the LOWER index; the chosen indices
  * are written to idx int32 [rows, k] in ASCENDING index order, padded with
  * -1.  -0.0 and +0.0 compare equal; NaN scores are not allowed.
- * 0 < k <= n <= 40960, ld >= n. */
+ * 0 < k <= n <= 32768, ld >= n. */
 biv_status biv_topk(const float* scores, int64_t ld, const int32_t* valid_len, int rows, int n,
                     int k, int32_t* idx, biv_stream_t stream);
 
@@ -343,8 +343,18 @@ typedef struct {
   uint16_t* buf_B;
   uint16_t* buf_C;
   float* buf_dt;
+  void* workspace;                       /* optional, biv_ssd_workspace bytes, 16-byte aligned */
+  size_t workspace_bytes;
 } biv_ssd_desc;
 
+/* Workspace of the parallel path (0 when no sequence has more than 4 new rows,
+ * where one CTA per (sequence, head) runs the chunk).  With a large enough
+ * workspace a call with many new rows runs every (sequence, chunk, head) in
+ * parallel and hands states on chunk to chunk; without one it runs the
+ * per-(sequence, head) path.  Both evaluate every row with the same FP32
+ * operations in the same order, so the choice changes no bit.  The workspace
+ * needs no initial value. */
+biv_status biv_ssd_workspace(const biv_ssd_desc* desc, size_t* bytes);
 biv_status biv_ssd_scan(const biv_ssd_desc* desc, biv_stream_t stream);
 
 #ifdef __cplusplus

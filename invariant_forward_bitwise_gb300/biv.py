@@ -24,7 +24,7 @@ EXPORTS = [
     "biv_qk_norm_rope", "biv_kv_store_bf16", "biv_kv_fp8_quant", "biv_kv_fp8_gather",
     "biv_attention_workspace", "biv_attention", "biv_attention_noalloc", "biv_gemm_workspace", "biv_gemm",
     "biv_act_quant_fp8", "biv_topk", "biv_router_topk", "biv_moe_dispatch", "biv_gather_rows",
-    "biv_moe_combine", "biv_logprob", "biv_ssd_scan",
+    "biv_moe_combine", "biv_logprob", "biv_ssd_workspace", "biv_ssd_scan",
 ]
 
 
@@ -75,7 +75,8 @@ class SSDDesc(C.Structure):
                 ("row0", C.c_void_p), ("n", C.c_void_p), ("pos0", C.c_void_p),
                 ("max_n", C.c_int),
                 ("state", C.c_void_p), ("buf_x", C.c_void_p), ("buf_B", C.c_void_p),
-                ("buf_C", C.c_void_p), ("buf_dt", C.c_void_p)]
+                ("buf_C", C.c_void_p), ("buf_dt", C.c_void_p),
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
 
 
 _lib: Optional[C.CDLL] = None
@@ -112,7 +113,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "biv_gather_rows": ([P, I64, P, I, I, I, P, I64, P], I),
         "biv_moe_combine": ([P, P, P, P, P, I, I, I, P], I),
         "biv_logprob": ([P, I64, P, I, I, P, P], I),
-        "biv_ssd_scan": ([P, P], I),
+        "biv_ssd_workspace": ([P, P], I), "biv_ssd_scan": ([P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name, None)
@@ -270,8 +271,8 @@ _gemm_scratch: Dict[int, torch.Tensor] = {}
 
 
 def gemm_scratch(nbytes: int, device=None) -> torch.Tensor:
-    """A GEMM workspace of at least nbytes, cached per device (for callers on
-    one stream)."""
+    """A scratch workspace of at least nbytes (GEMM chunk partials, SSD
+    intermediates), cached per device (for callers on one stream)."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
     t = _gemm_scratch.get(dev.index)
     if t is None or t.numel() < nbytes:
@@ -330,5 +331,18 @@ def biv_logprob(logits, target, lp, T=None, stream=None):
                               _stream(stream)), "biv_logprob")
 
 
+def biv_ssd_workspace(desc: SSDDesc) -> int:
+    n = C.c_size_t(0)
+    _check(load().biv_ssd_workspace(C.byref(desc), C.byref(n)), "biv_ssd_workspace")
+    return n.value
+
+
 def biv_ssd_scan(desc: SSDDesc, stream=None):
+    """When desc.workspace is unset and the call has many new rows, a cached
+    per-device scratch buffer serves as the workspace (callers on one stream)."""
+    if not desc.workspace:
+        need = biv_ssd_workspace(desc)
+        if need:
+            ws = gemm_scratch(need)
+            desc.workspace, desc.workspace_bytes = ws.data_ptr(), ws.numel()
     _check(load().biv_ssd_scan(C.byref(desc), _stream(stream)), "biv_ssd_scan")

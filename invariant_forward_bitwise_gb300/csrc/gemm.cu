@@ -148,7 +148,12 @@ struct GemmArgs {
 };
 
 constexpr int kMaxStages = 16;
-constexpr int kMaxChunks = 8;   // the invariant schedule cuts K into at most 8 chunks
+// The invariant schedule cuts K into at most 8 chunks of at least 8 blocks of
+// 64 (shorter chunks make the register fold of wide tiles stall the MMA:
+// measured on GB300 at M = 16384, K = 2048, 256-element chunks ran 22% below
+// one unchunked pass).
+constexpr int kMaxChunks = 8;
+constexpr int kMinChunkBlocks = 8;
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
@@ -174,6 +179,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr int B_STAGE = GemmSmem<BN>::B_STAGE;
   constexpr int HALF = BN / 2;
   static_assert(HALF % 32 == 0, "epilogue reads 32-column groups");
+  // two BN-column accumulators, allocated as a power of two
+  constexpr uint32_t kTmemCols = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
   // partial mode runs on tiles of at most 128 columns (register budget)
   constexpr bool kPartialOk = BN <= 128;
   extern __shared__ uint8_t smem_raw[];
@@ -217,7 +224,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   __syncwarp();
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 2 * BN);
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -409,7 +416,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 2 * BN);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 // Partial mode, second half: every output element's chunk partials folded in
@@ -639,6 +646,10 @@ struct Plan {
 };
 
 constexpr size_t kSmemBudget = 227 * 1024;  // the per-CTA maximum
+// The wide tile of the register-fold mode (measured on GB300 at M = 16384:
+// 256 columns beat 192 although each epilogue thread then keeps 128 running
+// sums and spills a few registers).
+constexpr int kWideN = 256;
 
 // Test overrides: BIV_GEMM_TILE_N=64|128|256 forces the tile width and
 // BIV_GEMM_FOLD=cta|partial the fold mode; the tests use them to check that
@@ -646,7 +657,7 @@ constexpr size_t kSmemBudget = 227 * 1024;  // the per-CTA maximum
 int env_tile_n() {
   const char* e = getenv("BIV_GEMM_TILE_N");
   const int bn = e ? atoi(e) : 0;
-  return (bn == 64 || bn == 128 || bn == 256) ? bn : 0;
+  return (bn == 64 || bn == 128 || bn == 192 || bn == 256) ? bn : 0;
 }
 int env_fold() {  // 0 = planner, 1 = fold in the CTA, 2 = partials
   const char* e = getenv("BIV_GEMM_FOLD");
@@ -656,8 +667,8 @@ int env_fold() {  // 0 = planner, 1 = fold in the CTA, 2 = partials
   return 0;
 }
 
-// INVARIANT: K cut into min(8, K blocks) chunks of ceil(KB/8) blocks for every
-// M; the tile width and the fold mode follow M (neither changes a bit).
+// INVARIANT: K cut into chunks of max(8, ceil(KB/8)) blocks for every M; the
+// tile width and the fold mode follow M (neither changes a bit).
 // FAST (the batch-dependent comparator): no chunking for large M, and for
 // small M a K split sized to fill the GPU.
 Plan plan_bf16(const biv_gemm_desc& d) {
@@ -666,12 +677,12 @@ Plan plan_bf16(const biv_gemm_desc& d) {
   const int sms = sm_count() > 0 ? sm_count() : 148;
   const int64_t tiles_m = (d.M + BM - 1) / BM;
   p.m_box = d.M <= BM ? std::max(16, (d.M + 15) / 16 * 16) : BM;
-  const int64_t tiles256 = int64_t((d.N + 255) / 256) * tiles_m;
+  const int64_t tiles_wide = int64_t((d.N + kWideN - 1) / kWideN) * tiles_m;
   const int64_t tiles128 = int64_t((d.N + 127) / 128) * tiles_m;
-  const bool wide = tiles256 >= sms;   // enough 128x256 tiles to fill the GPU
+  const bool wide = tiles_wide >= sms;   // enough 128 x kWideN tiles to fill the GPU
   bool partial = !wide && tiles128 * 2 <= sms;
   if (d.mode == BIV_MODE_INVARIANT) {
-    p.kc_blocks = (KB + kMaxChunks - 1) / kMaxChunks;
+    p.kc_blocks = std::max(kMinChunkBlocks, (KB + kMaxChunks - 1) / kMaxChunks);
   } else if (partial) {
     const int64_t want = (sms + tiles128 - 1) / tiles128;
     const int splits = int(std::max<int64_t>(1, std::min<int64_t>({want, int64_t(kMaxChunks), KB / 2})));
@@ -680,7 +691,7 @@ Plan plan_bf16(const biv_gemm_desc& d) {
     p.kc_blocks = KB;
   }
   p.chunks = (KB + p.kc_blocks - 1) / p.kc_blocks;
-  p.bn = wide ? 256 : 128;
+  p.bn = wide ? kWideN : 128;
   if (const int bn = env_tile_n()) p.bn = bn;
   if (const int f = env_fold()) partial = f == 2;
   p.tiles = int64_t((d.N + p.bn - 1) / p.bn) * tiles_m;
@@ -740,6 +751,7 @@ biv_status dispatch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv
                          const Plan& p, void* ws, cudaStream_t s) {
   switch (p.bn) {
     case 256: return launch_bf16<256, F32OUT>(ta, tb, d, p, ws, s);
+    case 192: return launch_bf16<192, F32OUT>(ta, tb, d, p, ws, s);
     case 128: return launch_bf16<128, F32OUT>(ta, tb, d, p, ws, s);
     default: return launch_bf16<64, F32OUT>(ta, tb, d, p, ws, s);
   }

@@ -396,7 +396,6 @@ __global__ void router_kernel(const float* __restrict__ logits, int64_t ld, int 
   for (int e = lane; e < E; e += 32) den += expf(z[e] - m);
   den = warp_sum(den);
   __syncwarp();
-  uint32_t taken_lo = 0;  // selection bookkeeping in shared memory below
   for (int s = 0; s < k; ++s) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
@@ -425,53 +424,59 @@ __global__ void router_kernel(const float* __restrict__ logits, int64_t ld, int 
     if (lane == (bi & 31)) z[bi] = NAN;
     __syncwarp();
   }
-  (void)taken_lo;
 }
 
 // ------------------------------------------------------------- dispatch ----
-// One CTA; each warp owns experts warp, warp+32, ...  Pass 1 counts, thread 0
-// forms the exclusive prefix, pass 2 places entries in ascending (t, s) order.
+// One CTA per expert e: count every expert's entries (shared-memory counters,
+// order-free integers), take e's start as the sum of the counts below it, then
+// walk the entries in ascending (t, s) order in blocks of 1024 and place e's
+// entries by a block-wide ballot scan, so the layout is unique.
 __global__ void __launch_bounds__(1024) moe_dispatch_kernel(const int32_t* __restrict__ idx,
                                                             int n, int E,
                                                             int32_t* __restrict__ offsets,
                                                             int32_t* __restrict__ perm,
                                                             int32_t* __restrict__ src_row) {
-  extern __shared__ int sm_counts[];  // [E+1]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int e = warp; e < E; e += nw) {
-    int cnt = 0;
-    for (int base = 0; base < n; base += 32) {
-      const int i = base + lane;
-      const bool hit = i < n && idx[i] == e;
-      cnt += __popc(__ballot_sync(0xffffffffu, hit));
-    }
-    if (lane == 0) sm_counts[e] = cnt;
+  extern __shared__ int sm_counts[];  // [E]
+  __shared__ int wcount[32];
+  __shared__ int s_start;
+  const int e = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int x = tid; x < E; x += blockDim.x) sm_counts[x] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int v = idx[i];
+    if (v >= 0 && v < E) atomicAdd(sm_counts + v, 1);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     int acc = 0;
-    for (int e = 0; e < E; ++e) {
-      const int c = sm_counts[e];
-      sm_counts[e] = acc;
-      offsets[e] = acc;
-      acc += c;
-    }
-    offsets[E] = acc;
+    for (int x = 0; x < e; ++x) acc += sm_counts[x];
+    s_start = acc;
+    offsets[e] = acc;
+    if (e == E - 1) offsets[E] = acc + sm_counts[e];
   }
   __syncthreads();
-  for (int e = warp; e < E; e += nw) {
-    int at = sm_counts[e];
-    for (int base = 0; base < n; base += 32) {
-      const int i = base + lane;
-      const bool hit = i < n && idx[i] == e;
-      const uint32_t bal = __ballot_sync(0xffffffffu, hit);
-      if (hit) {
-        const int r = at + __popc(bal & ((1u << lane) - 1u));
-        perm[r] = i;
-        src_row[i] = r;
-      }
-      at += __popc(bal);
+  int at = s_start;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + tid;
+    const bool hit = i < n && idx[i] == e;
+    const uint32_t bal = __ballot_sync(0xffffffffu, hit);
+    if (lane == 0) wcount[warp] = __popc(bal);
+    __syncthreads();
+    int pre = 0, tot = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int c = wcount[w];
+      pre += w < warp ? c : 0;
+      tot += c;
     }
+    if (hit) {
+      const int r = at + pre + __popc(bal & lt);
+      perm[r] = i;
+      src_row[i] = r;
+    }
+    at += tot;
+    __syncthreads();
   }
 }
 
@@ -676,8 +681,8 @@ biv_status biv_moe_dispatch(const int32_t* idx, int T, int k, int E, int32_t* of
   BIV_REQUIRE(T >= 0 && k > 0 && E > 0 && E <= 4096 && int64_t(T) * k <= (1 << 20),
               "moe_dispatch: bad sizes");
   BIV_REQUIRE(idx && offsets && perm && src_row, "moe_dispatch: null pointer");
-  moe_dispatch_kernel<<<1, 1024, (E + 1) * sizeof(int), as_cuda(stream)>>>(idx, T * k, E, offsets,
-                                                                          perm, src_row);
+  moe_dispatch_kernel<<<E, 1024, E * sizeof(int), as_cuda(stream)>>>(idx, T * k, E, offsets,
+                                                                    perm, src_row);
   return check_launch("moe_dispatch");
 }
 

@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(256, 1) ssd_kernel(const biv_ssd_desc d) {
     if (tid == 0) {
       float acc = 0.f;
       for (int r = 0; r < cnt; ++r) {
-        acc += S.dt[r] * A;
+        acc = fmaf(S.dt[r], A, acc);
         S.L[r] = acc;
       }
     }
@@ -170,8 +170,8 @@ __global__ void __launch_bounds__(256, 1) ssd_kernel(const biv_ssd_desc d) {
         const int p = e / kN, q = e % kN;
         float acc = 0.f;
         for (int s = 0; s < Q; ++s)
-          acc = fmaf(expf(Lend - S.L[s]) * S.dt[s] * bf2f(S.x[s][p]), bf2f(S.B[s][q]), acc);
-        S.h[p][q] = eEnd * S.h[p][q] + acc;
+          acc = fmaf((expf(Lend - S.L[s]) * S.dt[s]) * bf2f(S.x[s][p]), bf2f(S.B[s][q]), acc);
+        S.h[p][q] = fmaf(eEnd, S.h[p][q], acc);
       }
       closed_any = true;
     } else {
@@ -196,6 +196,344 @@ __global__ void __launch_bounds__(256, 1) ssd_kernel(const biv_ssd_desc d) {
     for (int e = tid; e < kP * kN; e += 256) state[e] = S.h[e / kN][e % kN];
 }
 
+// --------------------------------------------------- many-row path ----
+// The same per-row formulas as ssd_kernel, spread over the GPU for calls with
+// many new rows.  Every (sequence, chunk) pair the call touches and every head
+// run in parallel; only the chunk-to-chunk state hand-over is sequential, and
+// it is an elementwise fma per state entry:
+//   ssd_cb_kernel     cb(t, s) = sum_q C_t[q] B_s[q] (fma chain), all heads share it
+//   ssd_intra_kernel  intra(t, p) = sum_{s<=t} w(t,s) * (dt_s x_s[p]);  for a closing
+//                     chunk dH(p, q) = sum_s ((e^{Lend-L_s} dt_s) x_s[p]) B_s[q], e^{Lend}
+//   ssd_state_kernel  start state of each chunk; h <- fma(e^{Lend}, h, dH) per closed chunk
+//   ssd_out_kernel    y = fma(D, x, intra + sum_q (e^{L_t} h[p][q]) C_t[q]); buffers of
+//                     an open last chunk
+// All sums run in the orders ssd_kernel uses, so either path gives the same bits.
+struct SsdGeom {
+  int n, pos0, row0, c, s0, first, last;  // chunk c = pos0/Q + blockIdx.y
+  __device__ bool load(const biv_ssd_desc& d, int i, int cr) {
+    n = d.n[i];
+    if (n <= 0) return false;
+    pos0 = d.pos0[i];
+    row0 = d.row0[i];
+    c = pos0 / d.chunk + cr;
+    s0 = c * d.chunk;
+    if (s0 >= pos0 + n) return false;
+    first = max(s0, pos0);
+    last = min(s0 + d.chunk, pos0 + n);
+    return true;
+  }
+};
+
+struct SsdWs {  // carve-up of the many-row workspace
+  float* cb;    // [nseq][maxc][Q][Q]
+  float* acc;   // [nseq][max_n][H][P]
+  float* dH;    // [nseq][maxc][H][P][N]
+  float* eEnd;  // [nseq][maxc][H]
+  float* hst;   // [nseq][maxc][H][P][N]
+};
+
+__host__ __device__ inline int ssd_max_chunks(int max_n, int Q) { return (max_n + Q - 1) / Q + 1; }
+
+__host__ __device__ inline SsdWs ssd_ws(void* base, const biv_ssd_desc& d) {
+  const int64_t mc = ssd_max_chunks(d.max_n, d.chunk), Q = d.chunk;
+  float* p = static_cast<float*>(base);
+  SsdWs w;
+  w.cb = p;
+  p += int64_t(d.nseq) * mc * Q * Q;
+  w.acc = p;
+  p += int64_t(d.nseq) * d.max_n * d.H * kP;
+  w.dH = p;
+  p += int64_t(d.nseq) * mc * d.H * kP * kN;
+  w.eEnd = p;
+  p += (int64_t(d.nseq) * mc * d.H + 3) / 4 * 4;
+  w.hst = p;
+  p += int64_t(d.nseq) * mc * d.H * kP * kN;
+  return w;
+}
+
+inline size_t ssd_ws_bytes(const biv_ssd_desc& d) {
+  const int64_t mc = ssd_max_chunks(d.max_n, d.chunk), Q = d.chunk;
+  const int64_t floats = int64_t(d.nseq) * mc * Q * Q + int64_t(d.nseq) * d.max_n * d.H * kP +
+                         2 * int64_t(d.nseq) * mc * d.H * kP * kN +
+                         (int64_t(d.nseq) * mc * d.H + 3) / 4 * 4;
+  return size_t(floats) * sizeof(float);
+}
+
+// bf16 row of the chunk, local index r: the open chunk's buffer below `first`,
+// the call's input at and above it
+__device__ __forceinline__ const uint16_t* chunk_row(const SsdGeom& g, int r, const uint16_t* buf,
+                                                     int64_t buf_stride, const uint16_t* in,
+                                                     int64_t in_stride) {
+  const int t = g.s0 + r;
+  return t < g.first ? buf + int64_t(r) * buf_stride : in + int64_t(g.row0 + (t - g.pos0)) * in_stride;
+}
+
+constexpr int kCbRows = 32;   // rows t per ssd_cb_kernel CTA
+constexpr int kLDB = kN + 2;  // padded B rows: consecutive rows start one bank apart
+
+struct CbSmem {
+  uint16_t B[kMaxQ][kLDB];
+  uint16_t C[kCbRows][kN];
+};
+
+__global__ void __launch_bounds__(256) ssd_cb_kernel(const biv_ssd_desc d, SsdWs w) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  CbSmem& S = *reinterpret_cast<CbSmem*>(smem_raw);
+  auto& sB = S.B;
+  auto& sC = S.C;
+  const int i = blockIdx.x, cr = blockIdx.y, tb = blockIdx.z, tid = threadIdx.x;
+  SsdGeom g;
+  if (!g.load(d, i, cr)) return;
+  const int t_lo = max(g.first - g.s0, tb * kCbRows), t_hi = min(g.last - g.s0, tb * kCbRows + kCbRows);
+  if (t_lo >= t_hi) return;
+  const uint16_t* bB = d.buf_B + int64_t(i) * d.chunk * kN;
+  const uint16_t* bC = d.buf_C + int64_t(i) * d.chunk * kN;
+  for (int e = tid; e < t_hi * (kN / 2); e += 256) {
+    const int r = e / (kN / 2), q2 = e % (kN / 2);
+    const uint16_t* src = chunk_row(g, r, bB, kN, d.B, d.B_stride);
+    *reinterpret_cast<uint32_t*>(&sB[r][2 * q2]) = reinterpret_cast<const uint32_t*>(src)[q2];
+  }
+  for (int e = tid; e < (t_hi - t_lo) * (kN / 8); e += 256) {
+    const int r = t_lo + e / (kN / 8), q = e % (kN / 8);
+    const uint16_t* src = chunk_row(g, r, bC, kN, d.C, d.C_stride);
+    *reinterpret_cast<uint4*>(&sC[r - t_lo][q * 8]) = reinterpret_cast<const uint4*>(src)[q];
+  }
+  __syncthreads();
+  const int sidx = tid;  // thread = key row s
+  float* out = w.cb + (int64_t(i) * ssd_max_chunks(d.max_n, d.chunk) + cr) * d.chunk * d.chunk;
+  for (int t = t_lo; t < t_hi; ++t) {
+    if (sidx > t) continue;
+    float cb = 0.f;
+#pragma unroll 16
+    for (int q = 0; q < kN; q += 2) {
+      const uint32_t b2 = *reinterpret_cast<const uint32_t*>(&sB[sidx][q]);
+      const uint32_t c2 = *reinterpret_cast<const uint32_t*>(&sC[t - t_lo][q]);
+      cb = fmaf(bf2f(uint16_t(c2 & 0xFFFF)), bf2f(uint16_t(b2 & 0xFFFF)), cb);
+      cb = fmaf(bf2f(uint16_t(c2 >> 16)), bf2f(uint16_t(b2 >> 16)), cb);
+    }
+    out[int64_t(t) * d.chunk + sidx] = cb;
+  }
+}
+
+struct IntraSmem {
+  uint16_t x[kMaxQ][kP];
+  uint16_t B[kMaxQ][kN];
+  float dt[kMaxQ];
+  float L[kMaxQ];
+  float u[kMaxQ][kP];
+};
+
+// rows 0 .. cnt-1 of the chunk: dt and x of head h (buffer below `first`)
+__device__ void load_dt_x(const biv_ssd_desc& d, const SsdGeom& g, int i, int h, int cnt, float* dt,
+                          uint16_t (*x)[kP]) {
+  const int H = d.H, tid = threadIdx.x;
+  const float* bdt = d.buf_dt + int64_t(i) * d.chunk * H;
+  const uint16_t* bx = d.buf_x + int64_t(i) * d.chunk * H * kP;
+  for (int r = tid; r < cnt; r += blockDim.x) {
+    const int t = g.s0 + r;
+    dt[r] = t < g.first ? bdt[int64_t(r) * H + h] : d.dt[int64_t(g.row0 + (t - g.pos0)) * d.dt_stride + h];
+  }
+  for (int e = tid; e < cnt * (kP / 8); e += blockDim.x) {
+    const int r = e / (kP / 8), q = e % (kP / 8);
+    const int t = g.s0 + r;
+    const uint16_t* src = t < g.first ? bx + (int64_t(r) * H + h) * kP
+                                      : d.x + int64_t(g.row0 + (t - g.pos0)) * d.x_stride + int64_t(h) * kP;
+    *reinterpret_cast<uint4*>(&x[r][q * 8]) = reinterpret_cast<const uint4*>(src)[q];
+  }
+}
+
+// the chunk's decay prefix L_r = L_{r-1} + dt_r A (one thread, in order)
+__device__ void decay_prefix(const float* dt, float A, int cnt, float* L) {
+  if (threadIdx.x == 0) {
+    float acc = 0.f;
+    for (int r = 0; r < cnt; ++r) {
+      acc = fmaf(dt[r], A, acc);
+      L[r] = acc;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256, 1) ssd_intra_kernel(const biv_ssd_desc d, SsdWs w) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  IntraSmem& S = *reinterpret_cast<IntraSmem*>(smem_raw);
+  const int i = blockIdx.x, cr = blockIdx.y, h = blockIdx.z, tid = threadIdx.x;
+  SsdGeom g;
+  if (!g.load(d, i, cr)) return;
+  const int Q = d.chunk, cnt = g.last - g.s0;
+  const int64_t ci = int64_t(i) * ssd_max_chunks(d.max_n, Q) + cr;
+  load_dt_x(d, g, i, h, cnt, S.dt, S.x);
+  __syncthreads();
+  decay_prefix(S.dt, d.A[h], cnt, S.L);
+  __syncthreads();
+  // intra-chunk sums of the new rows, one thread per row
+  const int r = tid;
+  if (r < cnt && g.s0 + r >= g.first) {
+    const float* cbr = w.cb + (ci * Q + r) * Q;
+    const float Lt = S.L[r];
+    float acc[kP];
+#pragma unroll
+    for (int p = 0; p < kP; ++p) acc[p] = 0.f;
+    for (int sidx = 0; sidx <= r; ++sidx) {
+      const float wts = expf(Lt - S.L[sidx]) * cbr[sidx];
+      const float dts = S.dt[sidx];
+#pragma unroll
+      for (int p = 0; p < kP; ++p) acc[p] = fmaf(wts, dts * bf2f(S.x[sidx][p]), acc[p]);
+    }
+    float4* dst = reinterpret_cast<float4*>(
+        w.acc + ((int64_t(i) * d.max_n + (g.s0 + r - g.pos0)) * d.H + h) * kP);
+#pragma unroll
+    for (int p = 0; p < kP; p += 4) dst[p / 4] = make_float4(acc[p], acc[p + 1], acc[p + 2], acc[p + 3]);
+  }
+  if (g.last != g.s0 + Q) return;  // the chunk stays open: no hand-over yet
+  // closing chunk: dH and e^{Lend}
+  const float Lend = S.L[Q - 1];
+  const uint16_t* bB = d.buf_B + int64_t(i) * Q * kN;
+  for (int e = tid; e < Q * (kN / 8); e += 256) {
+    const int rr = e / (kN / 8), q = e % (kN / 8);
+    const uint16_t* src = chunk_row(g, rr, bB, kN, d.B, d.B_stride);
+    *reinterpret_cast<uint4*>(&S.B[rr][q * 8]) = reinterpret_cast<const uint4*>(src)[q];
+  }
+  for (int e = tid; e < Q * kP; e += 256) {
+    const int sidx = e / kP, p = e % kP;
+    S.u[sidx][p] = (expf(Lend - S.L[sidx]) * S.dt[sidx]) * bf2f(S.x[sidx][p]);
+  }
+  __syncthreads();
+  const int q = tid % kN, p0 = tid / kN;  // this thread: column q, rows p0, p0+2, ...
+  float acc[kP / 2];
+#pragma unroll
+  for (int k = 0; k < kP / 2; ++k) acc[k] = 0.f;
+  for (int sidx = 0; sidx < Q; ++sidx) {
+    const float bq = bf2f(S.B[sidx][q]);
+#pragma unroll
+    for (int k = 0; k < kP / 2; ++k) acc[k] = fmaf(S.u[sidx][p0 + 2 * k], bq, acc[k]);
+  }
+  float* dH = w.dH + (ci * d.H + h) * kP * kN;
+#pragma unroll
+  for (int k = 0; k < kP / 2; ++k) dH[(p0 + 2 * k) * kN + q] = acc[k];
+  if (tid == 0) w.eEnd[ci * d.H + h] = expf(Lend);
+}
+
+// chunk start states and the sequence's state after the call
+__global__ void __launch_bounds__(256) ssd_state_kernel(const biv_ssd_desc d, SsdWs w) {
+  const int i = blockIdx.x, h = blockIdx.y, e = blockIdx.z * 256 + threadIdx.x;
+  const int n = d.n[i];
+  if (n <= 0 || e >= kP * kN) return;
+  const int pos0 = d.pos0[i], Q = d.chunk;
+  const int mc = ssd_max_chunks(d.max_n, Q);
+  float* state = d.state + (int64_t(i) * d.H + h) * kP * kN;
+  float hv = state[e];
+  bool closed = false;
+  for (int cr = 0; cr < mc; ++cr) {
+    const int s0 = (pos0 / Q + cr) * Q;
+    if (s0 >= pos0 + n) break;
+    const int64_t ci = int64_t(i) * mc + cr;
+    w.hst[(ci * d.H + h) * kP * kN + e] = hv;
+    if (s0 + Q <= pos0 + n) {
+      hv = fmaf(w.eEnd[ci * d.H + h], hv, w.dH[(ci * d.H + h) * kP * kN + e]);
+      closed = true;
+    }
+  }
+  if (closed) state[e] = hv;
+}
+
+struct OutSmem {
+  float h[kP][kN];
+  uint16_t x[kMaxQ][kP];
+  uint16_t C[kMaxQ][kLDB];  // rows one bank apart: thread r reads row r
+  float dt[kMaxQ];
+  float L[kMaxQ];
+};
+
+__global__ void __launch_bounds__(256, 1) ssd_out_kernel(const biv_ssd_desc d, SsdWs w) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  OutSmem& S = *reinterpret_cast<OutSmem*>(smem_raw);
+  const int i = blockIdx.x, cr = blockIdx.y, h = blockIdx.z, tid = threadIdx.x;
+  SsdGeom g;
+  if (!g.load(d, i, cr)) return;
+  const int Q = d.chunk, H = d.H, cnt = g.last - g.s0;
+  const int64_t ci = int64_t(i) * ssd_max_chunks(d.max_n, Q) + cr;
+  load_dt_x(d, g, i, h, cnt, S.dt, S.x);
+  const float* hs = w.hst + (ci * H + h) * kP * kN;
+  for (int e = tid; e < kP * kN; e += 256) S.h[e / kN][e % kN] = hs[e];
+  const int fr = g.first - g.s0;
+  for (int e = tid; e < (cnt - fr) * (kN / 2); e += 256) {
+    const int r = fr + e / (kN / 2), q2 = e % (kN / 2);
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(d.C + int64_t(g.row0 + (g.s0 + r - g.pos0)) * d.C_stride) + q2;
+    *reinterpret_cast<uint32_t*>(&S.C[r][2 * q2]) = *src;
+  }
+  __syncthreads();
+  decay_prefix(S.dt, d.A[h], cnt, S.L);
+  __syncthreads();
+  const int r = tid;
+  if (r < cnt && r >= fr) {
+    const int j = g.s0 + r - g.pos0;  // new-row index of the call
+    const float4* src = reinterpret_cast<const float4*>(w.acc + ((int64_t(i) * d.max_n + j) * H + h) * kP);
+    float acc[kP];
+#pragma unroll
+    for (int p = 0; p < kP; p += 4) {
+      const float4 v = src[p / 4];
+      acc[p] = v.x; acc[p + 1] = v.y; acc[p + 2] = v.z; acc[p + 3] = v.w;
+    }
+    const float eL = expf(S.L[r]);
+#pragma unroll 2
+    for (int q = 0; q < kN; ++q) {
+      const float cq = bf2f(S.C[r][q]);
+#pragma unroll
+      for (int p = 0; p < kP; ++p) acc[p] = fmaf(eL * S.h[p][q], cq, acc[p]);
+    }
+    const float Dh = d.D[h];
+    uint16_t* y = d.y + int64_t(g.row0 + j) * d.y_stride + int64_t(h) * kP;
+#pragma unroll
+    for (int p = 0; p < kP; p += 2) {
+      const float o0 = fmaf(Dh, bf2f(S.x[r][p]), acc[p]);
+      const float o1 = fmaf(Dh, bf2f(S.x[r][p + 1]), acc[p + 1]);
+      *reinterpret_cast<uint32_t*>(y + p) = pack_bf2(o0, o1);
+    }
+  }
+  if (g.last == g.s0 + Q) return;
+  // the chunk stays open: keep its new rows for the next call
+  uint16_t* bx = d.buf_x + int64_t(i) * Q * H * kP;
+  float* bdt = d.buf_dt + int64_t(i) * Q * H;
+  for (int e = tid; e < (cnt - fr) * (kP / 8); e += 256) {
+    const int rr = fr + e / (kP / 8), q = e % (kP / 8);
+    reinterpret_cast<uint4*>(bx + (int64_t(rr) * H + h) * kP)[q] = *reinterpret_cast<const uint4*>(&S.x[rr][q * 8]);
+  }
+  for (int rr = fr + tid; rr < cnt; rr += 256) bdt[int64_t(rr) * H + h] = S.dt[rr];
+  if (h == 0) {
+    uint16_t* bB = d.buf_B + int64_t(i) * Q * kN;
+    uint16_t* bC = d.buf_C + int64_t(i) * Q * kN;
+    for (int e = tid; e < (cnt - fr) * (kN / 8); e += 256) {
+      const int rr = fr + e / (kN / 8), q = e % (kN / 8);
+      const int64_t row = g.row0 + (g.s0 + rr - g.pos0);
+      reinterpret_cast<uint4*>(bB + int64_t(rr) * kN)[q] = reinterpret_cast<const uint4*>(d.B + row * d.B_stride)[q];
+      reinterpret_cast<uint4*>(bC + int64_t(rr) * kN)[q] = reinterpret_cast<const uint4*>(d.C + row * d.C_stride)[q];
+    }
+  }
+}
+
+template <typename Kern>
+biv_status set_smem(Kern kern, size_t bytes, bool& done) {
+  if (!done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) !=
+        cudaSuccess)
+      return set_error(BIV_ERR_CUDA, "ssd_scan: cannot set shared memory size");
+    done = true;
+  }
+  return BIV_OK;
+}
+
+biv_status validate_ssd(const biv_ssd_desc* d) {
+  BIV_REQUIRE(d, "ssd_scan: null descriptor");
+  BIV_REQUIRE(d->P == kP && d->N == kN, "ssd_scan: supports P=%d, N=%d", kP, kN);
+  BIV_REQUIRE(d->chunk == 64 || d->chunk == 128 || d->chunk == 256, "ssd_scan: chunk in {64,128,256}");
+  BIV_REQUIRE(d->H > 0 && d->H <= 65535 && d->nseq >= 0 && d->nseq <= 65535 && d->max_n >= 0,
+              "ssd_scan: bad sizes");
+  return BIV_OK;
+}
+
+// many new rows in some sequence: the parallel path (when given its workspace)
+bool many_rows(const biv_ssd_desc& d) { return d.max_n > kFewRows; }
+
 }  // namespace
 }  // namespace biv
 
@@ -203,11 +541,17 @@ using namespace biv;
 
 extern "C" {
 
+biv_status biv_ssd_workspace(const biv_ssd_desc* d, size_t* bytes) {
+  biv_status st = validate_ssd(d);
+  if (st != BIV_OK) return st;
+  BIV_REQUIRE(bytes, "ssd_workspace: null output");
+  *bytes = many_rows(*d) ? ssd_ws_bytes(*d) : 0;
+  return BIV_OK;
+}
+
 biv_status biv_ssd_scan(const biv_ssd_desc* d, biv_stream_t stream) {
-  BIV_REQUIRE(d, "ssd_scan: null descriptor");
-  BIV_REQUIRE(d->P == kP && d->N == kN, "ssd_scan: supports P=%d, N=%d", kP, kN);
-  BIV_REQUIRE(d->chunk == 64 || d->chunk == 128 || d->chunk == 256, "ssd_scan: chunk in {64,128,256}");
-  BIV_REQUIRE(d->H > 0 && d->H <= 65535 && d->nseq >= 0 && d->nseq <= 0x7fffffff, "ssd_scan: bad sizes");
+  biv_status st = validate_ssd(d);
+  if (st != BIV_OK) return st;
   if (d->nseq == 0) return BIV_OK;
   BIV_REQUIRE(d->x && d->dt && d->A && d->B && d->C && d->D && d->y && d->row0 && d->n && d->pos0 &&
                   d->state && d->buf_x && d->buf_B && d->buf_C && d->buf_dt,
@@ -216,16 +560,28 @@ biv_status biv_ssd_scan(const biv_ssd_desc* d, biv_stream_t stream) {
                   aligned16(d->buf_B) && aligned16(d->buf_C) && (d->x_stride * 2) % 16 == 0 &&
                   (d->B_stride * 2) % 16 == 0 && (d->C_stride * 2) % 16 == 0,
               "ssd_scan: x/B/C rows must be 16-byte aligned");
-  const int smem = int(sizeof(SsdSmem));
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(ssd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return set_error(BIV_ERR_CUDA, "ssd_scan: cannot set shared memory size");
-    attr = true;
+  cudaStream_t s = as_cuda(stream);
+  const size_t need = many_rows(*d) ? ssd_ws_bytes(*d) : 0;
+  if (need && d->workspace && d->workspace_bytes >= need && aligned16(d->workspace)) {
+    static bool a1 = false, a2 = false, a3 = false;
+    if ((st = set_smem(ssd_cb_kernel, sizeof(CbSmem), a1)) != BIV_OK) return st;
+    if ((st = set_smem(ssd_intra_kernel, sizeof(IntraSmem), a2)) != BIV_OK) return st;
+    if ((st = set_smem(ssd_out_kernel, sizeof(OutSmem), a3)) != BIV_OK) return st;
+    const SsdWs w = ssd_ws(d->workspace, *d);
+    const int mc = ssd_max_chunks(d->max_n, d->chunk);
+    ssd_cb_kernel<<<dim3(d->nseq, mc, d->chunk / kCbRows), 256, sizeof(CbSmem), s>>>(*d, w);
+    if ((st = check_launch("ssd_cb")) != BIV_OK) return st;
+    ssd_intra_kernel<<<dim3(d->nseq, mc, d->H), 256, sizeof(IntraSmem), s>>>(*d, w);
+    if ((st = check_launch("ssd_intra")) != BIV_OK) return st;
+    ssd_state_kernel<<<dim3(d->nseq, d->H, kP * kN / 256), 256, 0, s>>>(*d, w);
+    if ((st = check_launch("ssd_state")) != BIV_OK) return st;
+    ssd_out_kernel<<<dim3(d->nseq, mc, d->H), 256, sizeof(OutSmem), s>>>(*d, w);
+    return check_launch("ssd_out");
   }
+  static bool a0 = false;
+  if ((st = set_smem(ssd_kernel, sizeof(SsdSmem), a0)) != BIV_OK) return st;
   dim3 grid(d->nseq, d->H);
-  ssd_kernel<<<grid, 256, smem, as_cuda(stream)>>>(*d);
+  ssd_kernel<<<grid, 256, sizeof(SsdSmem), s>>>(*d);
   return check_launch("ssd_scan");
 }
 

@@ -5,7 +5,7 @@
 CASE is one of attn_decode (256 sequences x 700 context, one decode row each),
 attn_decode4 (the same for 4 sequences),
 attn_prefill (8 sequences x 1024 tokens), gemm_prefill (M 8192, N 2048,
-K 6144), gemm_decode (M 64, N 2048, K 6144), lm_head (M 4096, N 151936,
+K 6144), gemm_qkv (M 16384, N 4096, K 2048), gemm_decode (M 64, N 2048, K 6144), lm_head (M 4096, N 151936,
 K 2048), ssd_prefill (16384 tokens, 64 heads), ssd_decode (one token), topk_indexer
 (4096 rows x 32768 scores, top 2048), moe_block (4096 tokens through the
 64-expert FP8 block) and decode_step (one decode step of the 28-layer model
@@ -194,7 +194,8 @@ elif case == "gemm_prefill_layer":
         a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
         b = (torch.randn(N, K, device="cuda") * 0.02).to(torch.bfloat16)
         c = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
-        d = biv.gemm_desc(a, b, c)
+        mode = biv.MODE_FAST if os.environ.get("BIV_BENCH_MODE") == "fast" else biv.MODE_INVARIANT
+        d = biv.gemm_desc(a, b, c, mode=mode)
         ms = graph_time(lambda: biv.biv_gemm(d), reps)
         print(f"{name:8s} M={M} N={N:6d} K={K}: {ms*1e3:8.1f} us  {2*M*N*K/(ms/1e3)/1e12:6.0f} TFLOP/s",
               flush=True)
@@ -218,8 +219,8 @@ elif case == "gemm_sweep":
                   f"  {2*M*N*K/(ms/1e3)/1e12:6.1f} TFLOP/s", flush=True)
         del bs
 else:
-    M, N, K = {"gemm_prefill": (8192, 2048, 6144), "gemm_decode": (64, 2048, 6144),
-               "lm_head": (4096, 151936, 2048)}[case]
+    M, N, K = {"gemm_prefill": (8192, 2048, 6144), "gemm_qkv": (16384, 4096, 2048),
+               "gemm_decode": (64, 2048, 6144), "lm_head": (4096, 151936, 2048)}[case]
     a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
     b = (torch.randn(N, K, device="cuda") * 0.02).to(torch.bfloat16)
     c = torch.empty(M, N, device="cuda", dtype=torch.float32 if case == "lm_head" else torch.bfloat16)
