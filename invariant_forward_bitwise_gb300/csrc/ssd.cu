@@ -315,12 +315,16 @@ __global__ void __launch_bounds__(256) ssd_cb_kernel(const biv_ssd_desc d, SsdWs
   }
 }
 
+constexpr int kST = 32;            // key rows s per weight tile
+constexpr int kWP = kST + 1;        // padded weight-tile row: rows one bank apart
+
 struct IntraSmem {
   uint16_t x[kMaxQ][kP];
   uint16_t B[kMaxQ][kN];
   float dt[kMaxQ];
   float L[kMaxQ];
-  float u[kMaxQ][kP];
+  float v[kMaxQ][kP];      // dt_s * x_s[p]; for a closing chunk reused as u[s][p]
+  float wt[kMaxQ][kWP];    // w(t, s) of one tile of kST key rows
 };
 
 // rows 0 .. cnt-1 of the chunk: dt and x of head h (buffer below `first`)
@@ -353,63 +357,122 @@ __device__ void decay_prefix(const float* dt, float A, int cnt, float* L) {
   }
 }
 
-__global__ void __launch_bounds__(256, 1) ssd_intra_kernel(const biv_ssd_desc d, SsdWs w) {
+constexpr int kSsdThreads = 512;   // many-row path CTAs: 16 warps per SM hide shared-memory latency
+
+__global__ void __launch_bounds__(kSsdThreads, 1) ssd_intra_kernel(const biv_ssd_desc d, SsdWs w) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   IntraSmem& S = *reinterpret_cast<IntraSmem*>(smem_raw);
   const int i = blockIdx.x, cr = blockIdx.y, h = blockIdx.z, tid = threadIdx.x;
   SsdGeom g;
   if (!g.load(d, i, cr)) return;
-  const int Q = d.chunk, cnt = g.last - g.s0;
+  const int Q = d.chunk, cnt = g.last - g.s0, fr = g.first - g.s0;
   const int64_t ci = int64_t(i) * ssd_max_chunks(d.max_n, Q) + cr;
   load_dt_x(d, g, i, h, cnt, S.dt, S.x);
   __syncthreads();
   decay_prefix(S.dt, d.A[h], cnt, S.L);
-  __syncthreads();
-  // intra-chunk sums of the new rows, one thread per row
-  const int r = tid;
-  if (r < cnt && g.s0 + r >= g.first) {
-    const float* cbr = w.cb + (ci * Q + r) * Q;
-    const float Lt = S.L[r];
-    float acc[kP];
-#pragma unroll
-    for (int p = 0; p < kP; ++p) acc[p] = 0.f;
-    for (int sidx = 0; sidx <= r; ++sidx) {
-      const float wts = expf(Lt - S.L[sidx]) * cbr[sidx];
-      const float dts = S.dt[sidx];
-#pragma unroll
-      for (int p = 0; p < kP; ++p) acc[p] = fmaf(wts, dts * bf2f(S.x[sidx][p]), acc[p]);
-    }
-    float4* dst = reinterpret_cast<float4*>(
-        w.acc + ((int64_t(i) * d.max_n + (g.s0 + r - g.pos0)) * d.H + h) * kP);
-#pragma unroll
-    for (int p = 0; p < kP; p += 4) dst[p / 4] = make_float4(acc[p], acc[p + 1], acc[p + 2], acc[p + 3]);
+  for (int e = tid; e < cnt * kP; e += kSsdThreads) {
+    const int sidx = e / kP, p = e % kP;
+    S.v[sidx][p] = S.dt[sidx] * bf2f(S.x[sidx][p]);
   }
+  __syncthreads();
+  // intra-chunk sums of the new rows [fr, cnt).  Thread (k, quarter) owns
+  // rows fr+k and cnt-1-k (balanced: their key counts add up to the same
+  // total) and 16 columns p; keys go by tiles of kST in ascending order, each
+  // tile's weights formed once in shared memory.
+  constexpr int PC = kP / 4;
+  const int nnew = cnt - fr;
+  const int k = tid & 127, pc = (tid >> 7) * PC;
+  const int ra = fr + k, rb = cnt - 1 - k;
+  const bool has_a = k < (nnew + 1) / 2, has_b = has_a && rb != ra;
+  float acc_a[PC], acc_b[PC];
+#pragma unroll
+  for (int c = 0; c < PC; ++c) acc_a[c] = acc_b[c] = 0.f;
+  const float* cbase = w.cb + ci * Q * Q;
+  for (int s0 = 0; s0 < cnt; s0 += kST) {
+    // weights of the tile: the C.B products of rows max(fr, s0) .. cnt-1 come
+    // in row by row (one warp reads a row's kST = 32 values, coalesced), then
+    // each becomes w = e^{L_r - L_s} * cb in place
+    const int rlo = max(fr, s0);
+    for (int e = tid; e < (cnt - rlo) * kST; e += kSsdThreads) {
+      const int r = rlo + e / kST, c = e % kST, sidx = s0 + c;
+      S.wt[r][c] = sidx <= r ? expf(S.L[r] - S.L[sidx]) * cbase[int64_t(r) * Q + sidx] : 0.f;
+    }
+    __syncthreads();
+    const int cmax = min(kST, cnt - s0);
+    if (has_a && ra >= s0) {
+      const int ce = min(cmax, ra - s0 + 1);
+      for (int c = 0; c < ce; ++c) {
+        const float wv = S.wt[ra][c];
+        const float4* vr = reinterpret_cast<const float4*>(&S.v[s0 + c][pc]);
+#pragma unroll
+        for (int j = 0; j < PC / 4; ++j) {
+          const float4 v4 = vr[j];
+          acc_a[4 * j] = fmaf(wv, v4.x, acc_a[4 * j]);
+          acc_a[4 * j + 1] = fmaf(wv, v4.y, acc_a[4 * j + 1]);
+          acc_a[4 * j + 2] = fmaf(wv, v4.z, acc_a[4 * j + 2]);
+          acc_a[4 * j + 3] = fmaf(wv, v4.w, acc_a[4 * j + 3]);
+        }
+      }
+    }
+    if (has_b && rb >= s0) {
+      const int ce = min(cmax, rb - s0 + 1);
+      for (int c = 0; c < ce; ++c) {
+        const float wv = S.wt[rb][c];
+        const float4* vr = reinterpret_cast<const float4*>(&S.v[s0 + c][pc]);
+#pragma unroll
+        for (int j = 0; j < PC / 4; ++j) {
+          const float4 v4 = vr[j];
+          acc_b[4 * j] = fmaf(wv, v4.x, acc_b[4 * j]);
+          acc_b[4 * j + 1] = fmaf(wv, v4.y, acc_b[4 * j + 1]);
+          acc_b[4 * j + 2] = fmaf(wv, v4.z, acc_b[4 * j + 2]);
+          acc_b[4 * j + 3] = fmaf(wv, v4.w, acc_b[4 * j + 3]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  auto put = [&](int r, const float (&acc)[PC]) {
+    float4* dst = reinterpret_cast<float4*>(
+        w.acc + ((int64_t(i) * d.max_n + (g.s0 + r - g.pos0)) * d.H + h) * kP + pc);
+#pragma unroll
+    for (int j = 0; j < PC / 4; ++j)
+      dst[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+  };
+  if (has_a) put(ra, acc_a);
+  if (has_b) put(rb, acc_b);
   if (g.last != g.s0 + Q) return;  // the chunk stays open: no hand-over yet
   // closing chunk: dH and e^{Lend}
   const float Lend = S.L[Q - 1];
   const uint16_t* bB = d.buf_B + int64_t(i) * Q * kN;
-  for (int e = tid; e < Q * (kN / 8); e += 256) {
+  for (int e = tid; e < Q * (kN / 8); e += kSsdThreads) {
     const int rr = e / (kN / 8), q = e % (kN / 8);
     const uint16_t* src = chunk_row(g, rr, bB, kN, d.B, d.B_stride);
     *reinterpret_cast<uint4*>(&S.B[rr][q * 8]) = reinterpret_cast<const uint4*>(src)[q];
   }
-  for (int e = tid; e < Q * kP; e += 256) {
+  for (int e = tid; e < Q * kP; e += kSsdThreads) {  // u[s][p] = (e^{Lend-L_s} dt_s) x_s[p]
     const int sidx = e / kP, p = e % kP;
-    S.u[sidx][p] = (expf(Lend - S.L[sidx]) * S.dt[sidx]) * bf2f(S.x[sidx][p]);
+    S.v[sidx][p] = (expf(Lend - S.L[sidx]) * S.dt[sidx]) * bf2f(S.x[sidx][p]);
   }
   __syncthreads();
-  const int q = tid % kN, p0 = tid / kN;  // this thread: column q, rows p0, p0+2, ...
-  float acc[kP / 2];
+  const int q = tid % kN, pb = (tid / kN) * PC;  // this thread: column q, rows pb .. pb+15
+  float acc[PC];
 #pragma unroll
-  for (int k = 0; k < kP / 2; ++k) acc[k] = 0.f;
+  for (int c = 0; c < PC; ++c) acc[c] = 0.f;
   for (int sidx = 0; sidx < Q; ++sidx) {
     const float bq = bf2f(S.B[sidx][q]);
+    const float4* ur = reinterpret_cast<const float4*>(&S.v[sidx][pb]);
 #pragma unroll
-    for (int k = 0; k < kP / 2; ++k) acc[k] = fmaf(S.u[sidx][p0 + 2 * k], bq, acc[k]);
+    for (int j = 0; j < PC / 4; ++j) {
+      const float4 u4 = ur[j];
+      acc[4 * j] = fmaf(u4.x, bq, acc[4 * j]);
+      acc[4 * j + 1] = fmaf(u4.y, bq, acc[4 * j + 1]);
+      acc[4 * j + 2] = fmaf(u4.z, bq, acc[4 * j + 2]);
+      acc[4 * j + 3] = fmaf(u4.w, bq, acc[4 * j + 3]);
+    }
   }
   float* dH = w.dH + (ci * d.H + h) * kP * kN;
 #pragma unroll
-  for (int k = 0; k < kP / 2; ++k) dH[(p0 + 2 * k) * kN + q] = acc[k];
+  for (int c = 0; c < PC; ++c) dH[(pb + c) * kN + q] = acc[c];
   if (tid == 0) w.eEnd[ci * d.H + h] = expf(Lend);
 }
 
@@ -436,15 +499,17 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const biv_ssd_desc d, Ss
   if (closed) state[e] = hv;
 }
 
+constexpr int kHP = kP + 4;  // transposed state rows (16-byte aligned)
+
 struct OutSmem {
-  float h[kP][kN];
+  float hT[kN][kHP];          // chunk start state, transposed: hT[q][p] = h[p][q]
   uint16_t x[kMaxQ][kP];
   uint16_t C[kMaxQ][kLDB];  // rows one bank apart: thread r reads row r
   float dt[kMaxQ];
   float L[kMaxQ];
 };
 
-__global__ void __launch_bounds__(256, 1) ssd_out_kernel(const biv_ssd_desc d, SsdWs w) {
+__global__ void __launch_bounds__(kSsdThreads, 1) ssd_out_kernel(const biv_ssd_desc d, SsdWs w) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   OutSmem& S = *reinterpret_cast<OutSmem*>(smem_raw);
   const int i = blockIdx.x, cr = blockIdx.y, h = blockIdx.z, tid = threadIdx.x;
@@ -454,9 +519,9 @@ __global__ void __launch_bounds__(256, 1) ssd_out_kernel(const biv_ssd_desc d, S
   const int64_t ci = int64_t(i) * ssd_max_chunks(d.max_n, Q) + cr;
   load_dt_x(d, g, i, h, cnt, S.dt, S.x);
   const float* hs = w.hst + (ci * H + h) * kP * kN;
-  for (int e = tid; e < kP * kN; e += 256) S.h[e / kN][e % kN] = hs[e];
+  for (int e = tid; e < kP * kN; e += kSsdThreads) S.hT[e % kN][e / kN] = hs[e];
   const int fr = g.first - g.s0;
-  for (int e = tid; e < (cnt - fr) * (kN / 2); e += 256) {
+  for (int e = tid; e < (cnt - fr) * (kN / 2); e += kSsdThreads) {
     const int r = fr + e / (kN / 2), q2 = e % (kN / 2);
     const uint32_t* src = reinterpret_cast<const uint32_t*>(d.C + int64_t(g.row0 + (g.s0 + r - g.pos0)) * d.C_stride) + q2;
     *reinterpret_cast<uint32_t*>(&S.C[r][2 * q2]) = *src;
@@ -464,13 +529,15 @@ __global__ void __launch_bounds__(256, 1) ssd_out_kernel(const biv_ssd_desc d, S
   __syncthreads();
   decay_prefix(S.dt, d.A[h], cnt, S.L);
   __syncthreads();
-  const int r = tid;
+  // thread (row r, half): the 32 columns p of its half
+  constexpr int PH = kP / 2;
+  const int r = tid % kMaxQ, p0 = (tid / kMaxQ) * PH;
   if (r < cnt && r >= fr) {
     const int j = g.s0 + r - g.pos0;  // new-row index of the call
-    const float4* src = reinterpret_cast<const float4*>(w.acc + ((int64_t(i) * d.max_n + j) * H + h) * kP);
-    float acc[kP];
+    const float4* src = reinterpret_cast<const float4*>(w.acc + ((int64_t(i) * d.max_n + j) * H + h) * kP + p0);
+    float acc[PH];
 #pragma unroll
-    for (int p = 0; p < kP; p += 4) {
+    for (int p = 0; p < PH; p += 4) {
       const float4 v = src[p / 4];
       acc[p] = v.x; acc[p + 1] = v.y; acc[p + 2] = v.z; acc[p + 3] = v.w;
     }
@@ -478,15 +545,22 @@ __global__ void __launch_bounds__(256, 1) ssd_out_kernel(const biv_ssd_desc d, S
 #pragma unroll 2
     for (int q = 0; q < kN; ++q) {
       const float cq = bf2f(S.C[r][q]);
+      const float4* hq = reinterpret_cast<const float4*>(&S.hT[q][p0]);
 #pragma unroll
-      for (int p = 0; p < kP; ++p) acc[p] = fmaf(eL * S.h[p][q], cq, acc[p]);
+      for (int jj = 0; jj < PH / 4; ++jj) {
+        const float4 h4 = hq[jj];
+        acc[4 * jj] = fmaf(eL * h4.x, cq, acc[4 * jj]);
+        acc[4 * jj + 1] = fmaf(eL * h4.y, cq, acc[4 * jj + 1]);
+        acc[4 * jj + 2] = fmaf(eL * h4.z, cq, acc[4 * jj + 2]);
+        acc[4 * jj + 3] = fmaf(eL * h4.w, cq, acc[4 * jj + 3]);
+      }
     }
     const float Dh = d.D[h];
-    uint16_t* y = d.y + int64_t(g.row0 + j) * d.y_stride + int64_t(h) * kP;
+    uint16_t* y = d.y + int64_t(g.row0 + j) * d.y_stride + int64_t(h) * kP + p0;
 #pragma unroll
-    for (int p = 0; p < kP; p += 2) {
-      const float o0 = fmaf(Dh, bf2f(S.x[r][p]), acc[p]);
-      const float o1 = fmaf(Dh, bf2f(S.x[r][p + 1]), acc[p + 1]);
+    for (int p = 0; p < PH; p += 2) {
+      const float o0 = fmaf(Dh, bf2f(S.x[r][p0 + p]), acc[p]);
+      const float o1 = fmaf(Dh, bf2f(S.x[r][p0 + p + 1]), acc[p + 1]);
       *reinterpret_cast<uint32_t*>(y + p) = pack_bf2(o0, o1);
     }
   }
@@ -494,15 +568,15 @@ __global__ void __launch_bounds__(256, 1) ssd_out_kernel(const biv_ssd_desc d, S
   // the chunk stays open: keep its new rows for the next call
   uint16_t* bx = d.buf_x + int64_t(i) * Q * H * kP;
   float* bdt = d.buf_dt + int64_t(i) * Q * H;
-  for (int e = tid; e < (cnt - fr) * (kP / 8); e += 256) {
+  for (int e = tid; e < (cnt - fr) * (kP / 8); e += kSsdThreads) {
     const int rr = fr + e / (kP / 8), q = e % (kP / 8);
     reinterpret_cast<uint4*>(bx + (int64_t(rr) * H + h) * kP)[q] = *reinterpret_cast<const uint4*>(&S.x[rr][q * 8]);
   }
-  for (int rr = fr + tid; rr < cnt; rr += 256) bdt[int64_t(rr) * H + h] = S.dt[rr];
+  for (int rr = fr + tid; rr < cnt; rr += kSsdThreads) bdt[int64_t(rr) * H + h] = S.dt[rr];
   if (h == 0) {
     uint16_t* bB = d.buf_B + int64_t(i) * Q * kN;
     uint16_t* bC = d.buf_C + int64_t(i) * Q * kN;
-    for (int e = tid; e < (cnt - fr) * (kN / 8); e += 256) {
+    for (int e = tid; e < (cnt - fr) * (kN / 8); e += kSsdThreads) {
       const int rr = fr + e / (kN / 8), q = e % (kN / 8);
       const int64_t row = g.row0 + (g.s0 + rr - g.pos0);
       reinterpret_cast<uint4*>(bB + int64_t(rr) * kN)[q] = reinterpret_cast<const uint4*>(d.B + row * d.B_stride)[q];
@@ -571,11 +645,11 @@ biv_status biv_ssd_scan(const biv_ssd_desc* d, biv_stream_t stream) {
     const int mc = ssd_max_chunks(d->max_n, d->chunk);
     ssd_cb_kernel<<<dim3(d->nseq, mc, d->chunk / kCbRows), 256, sizeof(CbSmem), s>>>(*d, w);
     if ((st = check_launch("ssd_cb")) != BIV_OK) return st;
-    ssd_intra_kernel<<<dim3(d->nseq, mc, d->H), 256, sizeof(IntraSmem), s>>>(*d, w);
+    ssd_intra_kernel<<<dim3(d->nseq, mc, d->H), kSsdThreads, sizeof(IntraSmem), s>>>(*d, w);
     if ((st = check_launch("ssd_intra")) != BIV_OK) return st;
     ssd_state_kernel<<<dim3(d->nseq, d->H, kP * kN / 256), 256, 0, s>>>(*d, w);
     if ((st = check_launch("ssd_state")) != BIV_OK) return st;
-    ssd_out_kernel<<<dim3(d->nseq, mc, d->H), 256, sizeof(OutSmem), s>>>(*d, w);
+    ssd_out_kernel<<<dim3(d->nseq, mc, d->H), kSsdThreads, sizeof(OutSmem), s>>>(*d, w);
     return check_launch("ssd_out");
   }
   static bool a0 = false;
