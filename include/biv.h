@@ -55,6 +55,18 @@ typedef enum {
 typedef enum { BIV_MODE_INVARIANT = 0, BIV_MODE_FAST = 1 } biv_mode;
 typedef enum { BIV_BF16 = 0, BIV_F32 = 1, BIV_E4M3 = 2 } biv_dtype;
 
+/* Chunk partials that a bf16 biv_gemm left in its workspace: the output
+ * element (row, col) is RN(((p[0] + p[1]) + p[2]) + ...) with p[c] =
+ * p + c*chunk_stride + row*ld + col, rounded once to the GEMM's output type;
+ * chunks == 0 means the call wrote C itself. */
+typedef struct {
+  const float* p;
+  int chunks;
+  int64_t ld;
+  int64_t chunk_stride;
+} biv_partials;
+
+
 /* Library version (major*10000 + minor*100 + patch). */
 int biv_version(void);
 
@@ -92,6 +104,14 @@ biv_status biv_embed(const int32_t* ids, const uint16_t* table, int vocab, int T
 biv_status biv_add_rmsnorm(const uint16_t* x, int64_t x_stride, uint16_t* residual,
                            int64_t r_stride, const uint16_t* w, uint16_t* y, int64_t y_stride,
                            int rows, int d, float eps, biv_stream_t stream);
+
+/* The same, with x given as the chunk partials of the GEMM that produced it
+ * (biv_gemm with defer_fold): x = the GEMM's rounded output, formed here
+ * instead of by the GEMM's fold kernel, so the result is the same bit for
+ * bit and one launch and one round trip of x are saved. */
+biv_status biv_add_rmsnorm_partials(const biv_partials* x, uint16_t* residual, int64_t r_stride,
+                                    const uint16_t* w, uint16_t* y, int64_t y_stride, int rows,
+                                    int d, float eps, biv_stream_t stream);
 
 /* ------------------------------------------------------------ SiLU-mul ----
  * y = bf16(silu(g) * u), silu(g) = g / (1 + exp(-g)) in FP32, for
@@ -136,6 +156,21 @@ biv_status biv_kv_fp8_quant(const uint16_t* k, const uint16_t* v, int64_t row_st
                             const int64_t* slot, int T, int Hkv, int D, uint8_t* k_codes,
                             uint8_t* v_codes, float* k_scales, float* v_scales,
                             biv_stream_t stream);
+
+/* QKV finalize: biv_qk_norm_rope followed by biv_kv_store_bf16 (kv_dtype
+ * BIV_BF16) or biv_kv_fp8_quant (BIV_E4M3) of the k and v heads, in one
+ * pass with the same per-element operations, so the same bits.  When
+ * qkv_partials is non-NULL with chunks > 0, the packed qkv [T, (Hq+2Hkv)*D]
+ * is first formed from the QKV GEMM's chunk partials (biv_gemm with
+ * defer_fold) and written to qkv; otherwise qkv holds it already.  After the
+ * call qkv holds roped q and k and the plain v; k/v of rows with slot >= 0
+ * are in the cache (bf16 [slots, Hkv, D], or e4m3 codes with per-(token,
+ * head) scales). */
+biv_status biv_qkv_finalize(uint16_t* qkv, int64_t row_stride, const biv_partials* qkv_partials,
+                            int T, int Hq, int Hkv, int D, const uint16_t* q_w, const uint16_t* k_w,
+                            const float* cos_sin, int max_pos, const int32_t* pos, float eps,
+                            const int64_t* slot, int kv_dtype, void* k_cache, void* v_cache,
+                            float* k_scale, float* v_scale, biv_stream_t stream);
 
 /* Gather + dequantise: for each sequence i, tokens [0, ctx_len[i]) of its
  * pages (block_table int32 [nseq, max_pages]) are written as
@@ -248,7 +283,14 @@ typedef struct {
   const int32_t* group_offsets;     /* optional device [groups+1] */
   int groups;                       /* 0/1 = plain */
   int mode;                         /* biv_mode */
+  int defer_fold;                   /* 1: when the call leaves chunk partials in the
+                                       workspace (biv_gemm_partials says so), skip the
+                                       fold: a consumer op reads them; C is not written */
 } biv_gemm_desc;
+
+/* Fills *out with the partials layout of a call (chunks = 0 when the plan
+ * folds inside the GEMM).  Pure host computation, no launch. */
+biv_status biv_gemm_partials(const biv_gemm_desc* desc, const void* workspace, biv_partials* out);
 
 biv_status biv_gemm_workspace(const biv_gemm_desc* desc, size_t* bytes);
 biv_status biv_gemm(const biv_gemm_desc* desc, void* workspace, size_t workspace_bytes,

@@ -20,9 +20,10 @@ BF16, F32, E4M3 = 0, 1, 2
 
 EXPORTS = [
     "biv_version", "biv_last_error", "biv_device_sm_count", "biv_poll_error",
-    "biv_selftest_timeout", "biv_embed", "biv_add_rmsnorm", "biv_silu_mul", "biv_rope_table",
-    "biv_qk_norm_rope", "biv_kv_store_bf16", "biv_kv_fp8_quant", "biv_kv_fp8_gather",
-    "biv_attention_workspace", "biv_attention", "biv_attention_noalloc", "biv_gemm_workspace", "biv_gemm",
+    "biv_selftest_timeout", "biv_embed", "biv_add_rmsnorm", "biv_add_rmsnorm_partials", "biv_silu_mul",
+    "biv_rope_table", "biv_qk_norm_rope", "biv_kv_store_bf16", "biv_kv_fp8_quant", "biv_qkv_finalize",
+    "biv_kv_fp8_gather", "biv_attention_workspace", "biv_attention", "biv_attention_noalloc",
+    "biv_gemm_workspace", "biv_gemm_partials", "biv_gemm",
     "biv_act_quant_fp8", "biv_topk", "biv_router_topk", "biv_moe_dispatch", "biv_gather_rows",
     "biv_moe_combine", "biv_logprob", "biv_ssd_workspace", "biv_ssd_scan",
 ]
@@ -43,7 +44,13 @@ class GemmDesc(C.Structure):
                 ("sa", C.c_void_p), ("ld_sa", C.c_int64),
                 ("sb", C.c_void_p),
                 ("group_offsets", C.c_void_p), ("groups", C.c_int),
-                ("mode", C.c_int)]
+                ("mode", C.c_int), ("defer_fold", C.c_int)]
+
+
+class Partials(C.Structure):
+    """Chunk partials a GEMM left for its consumer (see include/biv.h)."""
+    _fields_ = [("p", C.c_void_p), ("chunks", C.c_int), ("ld", C.c_int64),
+                ("chunk_stride", C.c_int64)]
 
 
 class AttnDesc(C.Structure):
@@ -97,6 +104,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "biv_selftest_timeout": ([C.c_uint64, P], I),
         "biv_embed": ([P, P, I, I, I, P, I64, P], I),
         "biv_add_rmsnorm": ([P, I64, P, I64, P, P, I64, I, I, F, P], I),
+        "biv_add_rmsnorm_partials": ([P, P, I64, P, P, I64, I, I, F, P], I),
+        "biv_qkv_finalize": ([P, I64, P, I, I, I, I, P, P, P, I, P, F, P, I, P, P, P, P, P], I),
+        "biv_gemm_partials": ([P, P, P], I),
         "biv_silu_mul": ([P, I64, P, I64, I, I, P], I),
         "biv_rope_table": ([D_, I, I, P, P], I),
         "biv_qk_norm_rope": ([P, I64, I, I, I, I, P, P, P, I, P, F, P], I),
@@ -202,6 +212,31 @@ def biv_silu_mul(gate_up, y, stream=None):
 def biv_rope_table(theta, D, max_pos, out, stream=None):
     assert out.dtype == torch.float32 and out.numel() >= 2 * max_pos * (D // 2)
     _check(load().biv_rope_table(float(theta), D, max_pos, _p(out), _stream(stream)), "biv_rope_table")
+
+
+def biv_add_rmsnorm_partials(xp: "Partials", residual, w, y, rows, eps, stream=None):
+    """x given as GEMM chunk partials; rows/d from the arguments."""
+    _bf16_ok(residual, w, y)
+    d = y.shape[-1]
+    _check(load().biv_add_rmsnorm_partials(C.byref(xp), _p(residual),
+                                           _rs(residual) if residual is not None else 0, _p(w), _p(y),
+                                           _rs(y), rows, d, float(eps), _stream(stream)),
+           "biv_add_rmsnorm_partials")
+
+
+def biv_qkv_finalize(qkv, T, Hq, Hkv, D, q_w, k_w, cos_sin, max_pos, pos, eps, slot, kv_dtype,
+                     k_cache, v_cache, k_scale=None, v_scale=None, partials: Optional["Partials"] = None,
+                     stream=None):
+    _check(load().biv_qkv_finalize(_p(qkv), _rs(qkv), C.byref(partials) if partials is not None else None,
+                                   T, Hq, Hkv, D, _p(q_w), _p(k_w), _p(cos_sin), max_pos, _p(pos),
+                                   float(eps), _p(slot), kv_dtype, _p(k_cache), _p(v_cache), _p(k_scale),
+                                   _p(v_scale), _stream(stream)), "biv_qkv_finalize")
+
+
+def biv_gemm_partials(desc: GemmDesc, ws: Optional[torch.Tensor]) -> "Partials":
+    out = Partials()
+    _check(load().biv_gemm_partials(C.byref(desc), _p(ws), C.byref(out)), "biv_gemm_partials")
+    return out
 
 
 def biv_qk_norm_rope(qkv, T, Hq, Hkv, D, q_w, k_w, cos_sin, max_pos, pos, eps, stream=None):

@@ -122,7 +122,8 @@ __device__ __forceinline__ void store_row_regs(void* C, int64_t ldc, int row, in
 //  - fold mode: a work item is a whole 128 x BN tile; the epilogue warps fold
 //    its chunks in registers as the MMA warp finishes them;
 //  - partial mode: a work item is one (tile, chunk) pair and its P_c goes to
-//    the workspace; gemm_fold_kernel then folds every element's partials in
+//    the workspace (row-major per chunk); gemm_fold_kernel, or a consumer op
+//    that reads the partials directly, folds every element's partials in
 //    chunk order.  This spreads a few output tiles (decode-sized M) over every
 //    SM without changing any element's arithmetic.
 //
@@ -141,7 +142,8 @@ struct GemmArgs {
   int m_box;            // rows of the A box (multiple of 16, <= 128)
   int stages;           // pipeline depth (<= kMaxStages)
   int partial;          // 1: partial mode
-  float4* ws;           // partial mode: [tiles][chunks][BN/4][m_box] float4 groups
+  float* ws;            // partial mode: [chunks][M][ldp] FP32
+  int64_t ldp;          // partial row pitch (N rounded up to the tile width)
   int vec_ok;           // C rows 16-byte aligned
   int n_fastest;        // fold mode: walk N tiles first
   int* err;
@@ -314,7 +316,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
       const int t = item_tile(i), m0 = tile_m0(t), n0 = tile_n0(t);
       const int row = m0 + q * 32 + lane;
-      const int lrow = q * 32 + lane;        // row inside the tile
       const bool live = row < p.M;
       for (int c = item_c0(i); c < item_c1(i); ++c, ++j) {
         const int b = j & 1;
@@ -323,11 +324,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t ta = tmem + b * BN + col0 + (uint32_t(q * 32) << 16);
-        // partial layout: float4 group (column/4) major, row minor, so that a
-        // warp's 32 rows land in 512 contiguous bytes
-        float4* dst = partial && live
-                          ? p.ws + ((int64_t(t) * chunks + c) * (BN / 4) + col0 / 4) * p.m_box + lrow
-                          : nullptr;
+        float* dst = partial && live ? p.ws + (int64_t(c) * p.M + row) * p.ldp + n0 + col0 : nullptr;
         // tcgen05.ld is warp-collective: every lane issues it, live row or not
         if (partial) {
 #pragma unroll
@@ -338,7 +335,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (dst) {
 #pragma unroll
               for (int x = 0; x < 32; x += 4)
-                dst[int64_t((g * 32 + x) / 4) * p.m_box] =
+                *reinterpret_cast<float4*>(dst + g * 32 + x) =
                     make_float4(__uint_as_float(v[x]), __uint_as_float(v[x + 1]),
                                 __uint_as_float(v[x + 2]), __uint_as_float(v[x + 3]));
             }
@@ -420,31 +417,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // Partial mode, second half: every output element's chunk partials folded in
-// chunk order, r = P_0, r = r + P_1, ..., rounded once.  One thread per
-// (tile, 4-column group, row); consecutive threads take consecutive rows, so
-// the partial reads are contiguous.  Tiles are in M-fastest order.
+// chunk order, r = P_0, r = r + P_1, ..., rounded once.  One thread per 4
+// consecutive columns of a row (coalesced reads of each chunk's rows).
 template <bool F32OUT>
-__global__ void __launch_bounds__(256) gemm_fold_kernel(const float4* __restrict__ ws, void* C,
-                                                        int64_t ldc, int M, int N, int BN,
-                                                        int m_box, int tiles_m, int chunks,
-                                                        int64_t groups, int vec_ok) {
+__global__ void __launch_bounds__(256) gemm_fold_kernel(const float* __restrict__ ws, void* C,
+                                                        int64_t ldc, int M, int N, int64_t ldp,
+                                                        int chunks, int vec_ok) {
   pdl_wait();  // the partials of the GEMM kernel before this one
   pdl_trigger();
-  const int cgs = BN / 4;
-  const int64_t cstride = int64_t(cgs) * m_box;
+  const int gpr = (N + 3) / 4;  // 4-column groups per row
+  const int64_t groups = int64_t(M) * gpr;
+  const int64_t cstride = int64_t(M) * ldp;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < groups;
        i += int64_t(gridDim.x) * blockDim.x) {
-    const int lrow = int(i % m_box);
-    const int64_t rest = i / m_box;
-    const int cg = int(rest % cgs);
-    const int t = int(rest / cgs);
-    const int row = (t % tiles_m) * BM + lrow, n = (t / tiles_m) * BN + cg * 4;
-    if (row >= M || n >= N) continue;
-    const float4* src = ws + (int64_t(t) * chunks * cgs + cg) * m_box + lrow;
+    const int row = int(i / gpr), n = int(i % gpr) * 4;
+    const float* src = ws + int64_t(row) * ldp + n;
     float4 v[kMaxChunks];
 #pragma unroll
     for (int c = 0; c < kMaxChunks; ++c)
-      if (c < chunks) v[c] = __ldcg(src + c * cstride);
+      if (c < chunks) v[c] = __ldcg(reinterpret_cast<const float4*>(src + c * cstride));
     float r[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
 #pragma unroll
     for (int c = 1; c < kMaxChunks; ++c) {
@@ -642,6 +633,7 @@ struct Plan {
   int m_box = BM;     // rows of the A TMA box
   int stages = 4;
   int64_t tiles = 0;
+  int64_t ldp = 0;    // partial row pitch
   size_t ws_bytes = 0;
 };
 
@@ -701,7 +693,8 @@ Plan plan_bf16(const biv_gemm_desc& d) {
   const size_t fixed = 1024 + size_t(128 - p.m_box) * 128 + (2 * kMaxStages + 4) * 8 + 16 +
                        kStagingBytes;
   p.stages = int(std::min<size_t>(kMaxStages, (kSmemBudget - fixed) / (a_stage + b_stage)));
-  if (p.partial) p.ws_bytes = size_t(p.tiles) * p.chunks * p.m_box * p.bn * sizeof(float);
+  p.ldp = int64_t((d.N + p.bn - 1) / p.bn) * p.bn;
+  if (p.partial) p.ws_bytes = size_t(p.chunks) * d.M * p.ldp * sizeof(float);
   return p;
 }
 
@@ -727,7 +720,8 @@ biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_g
   a.m_box = pl.m_box;
   a.stages = pl.stages;
   a.partial = pl.partial ? 1 : 0;
-  a.ws = pl.partial ? static_cast<float4*>(ws) : nullptr;
+  a.ws = pl.partial ? static_cast<float*>(ws) : nullptr;
+  a.ldp = pl.ldp;
   a.vec_ok = aligned16(d.C) && (d.ldc * eb) % 16 == 0;
   a.n_fastest = !pl.partial && d.N <= d.M;
   a.err = device_error_word();
@@ -737,12 +731,11 @@ biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_g
   const size_t smem = GemmSmem<BN>::bytes(pl.stages, pl.m_box);
   launch_pdl(kern, grid, kGemmThreads, smem, s, ta, tb, a);
   biv_status st = check_launch("gemm_bf16");
-  if (st != BIV_OK || !pl.partial) return st;
-  const int64_t tiles_m = (d.M + BM - 1) / BM;
-  const int64_t groups = pl.tiles * (BN / 4) * pl.m_box;
+  if (st != BIV_OK || !pl.partial || d.defer_fold) return st;
+  const int64_t groups = int64_t(d.M) * ((d.N + 3) / 4);
   const int blocks = int(std::min<int64_t>((groups + 255) / 256, int64_t(sms) * 8));
-  launch_pdl(gemm_fold_kernel<F32OUT>, blocks, 256, 0, s, static_cast<const float4*>(ws), d.C,
-             d.ldc, d.M, d.N, BN, pl.m_box, int(tiles_m), pl.chunks, groups, a.vec_ok);
+  launch_pdl(gemm_fold_kernel<F32OUT>, blocks, 256, 0, s, static_cast<const float*>(ws), d.C,
+             d.ldc, d.M, d.N, pl.ldp, pl.chunks, a.vec_ok);
   return check_launch("gemm_fold");
 }
 
@@ -817,6 +810,21 @@ biv_status biv_gemm_workspace(const biv_gemm_desc* d, size_t* bytes) {
   if (st != BIV_OK) return st;
   BIV_REQUIRE(bytes, "gemm_workspace: null output");
   *bytes = d->a_dtype == BIV_BF16 ? plan_bf16(*d).ws_bytes : 0;
+  return BIV_OK;
+}
+
+biv_status biv_gemm_partials(const biv_gemm_desc* d, const void* ws, biv_partials* out) {
+  biv_status st = validate(d);
+  if (st != BIV_OK) return st;
+  BIV_REQUIRE(out, "gemm_partials: null output");
+  memset(out, 0, sizeof(*out));
+  if (d->a_dtype != BIV_BF16) return BIV_OK;
+  const Plan p = plan_bf16(*d);
+  if (!p.partial) return BIV_OK;
+  out->p = static_cast<const float*>(ws);
+  out->chunks = p.chunks;
+  out->ld = p.ldp;
+  out->chunk_stride = int64_t(d->M) * p.ldp;
   return BIV_OK;
 }
 

@@ -58,10 +58,30 @@ __global__ void embed_kernel(const int32_t* __restrict__ ids, const uint16_t* __
 // One CTA of kNormThreads per row.  Thread t owns 8-element chunks
 // t, t+256, ...; sum of squares: per-thread in chunk order, warp xor tree,
 // then the 8 warp sums added in warp order.
+// 8 consecutive bf16 outputs of a GEMM whose chunk partials were left for the
+// consumer: fold the partials in chunk order, round once (what the GEMM's own
+// fold kernel stores)
+__device__ __forceinline__ void fold8(const biv_partials& xp, int64_t row, int col, float (&f)[8]) {
+  const float* src = xp.p + row * xp.ld + col;
+  float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+  float4 b = __ldcg(reinterpret_cast<const float4*>(src + 4));
+  for (int c = 1; c < xp.chunks; ++c) {
+    const float* sc = src + c * xp.chunk_stride;
+    const float4 a2 = __ldcg(reinterpret_cast<const float4*>(sc));
+    const float4 b2 = __ldcg(reinterpret_cast<const float4*>(sc + 4));
+    a.x = a.x + a2.x; a.y = a.y + a2.y; a.z = a.z + a2.z; a.w = a.w + a2.w;
+    b.x = b.x + b2.x; b.y = b.y + b2.y; b.z = b.z + b2.z; b.w = b.w + b2.w;
+  }
+  const float t[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) f[j] = bf2f(f2bf(t[j]));
+}
+
 template <int CPT>  // chunks per thread (ceil(d/8/256))
 __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
-    const uint16_t* __restrict__ x, int64_t xs, uint16_t* __restrict__ r, int64_t rs,
-    const uint16_t* __restrict__ w, uint16_t* __restrict__ y, int64_t ys, int d, float eps) {
+    const uint16_t* __restrict__ x, int64_t xs, const biv_partials xp, uint16_t* __restrict__ r,
+    int64_t rs, const uint16_t* __restrict__ w, uint16_t* __restrict__ y, int64_t ys, int d,
+    float eps) {
   pdl_wait();     // stream predecessor done, its writes visible
   pdl_trigger();
   __shared__ float warp_ss[kNormThreads / 32];
@@ -75,7 +95,10 @@ __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
   for (int i = 0; i < CPT; ++i) {
     const int c = threadIdx.x + i * kNormThreads;
     if (c < chunks) {
-      unpack8(xr[c], v[i]);
+      if (xp.chunks > 0)
+        fold8(xp, row, c * 8, v[i]);
+      else
+        unpack8(xr[c], v[i]);
       if (rr) {
         float rv[8];
         unpack8(rr[c], rv);
@@ -144,6 +167,14 @@ __global__ void rope_table_kernel(double theta, int D, int max_pos, float* cos_s
 }
 
 // ------------------------------------------------------- QK-norm + RoPE ----
+// The rotation of one pair (a, b) at angle (c, s), rounded to bf16: the one
+// instruction sequence every kernel that applies RoPE uses.
+__device__ __forceinline__ void rope_pair(float a, float b, float c, float s, uint16_t& oa,
+                                          uint16_t& ob) {
+  oa = f2bf(fmaf(a, c, -(b * s)));
+  ob = f2bf(fmaf(b, c, a * s));
+}
+
 // One warp per (token, head).  Lane l owns the rotation pairs p = l, l+32
 // (p < D/2) holding elements p and p + D/2.
 __global__ void qk_norm_rope_kernel(uint16_t* __restrict__ qkv, int64_t rs, int T, int Hq,
@@ -199,8 +230,7 @@ __global__ void qk_norm_rope_kernel(uint16_t* __restrict__ qkv, int64_t rs, int 
     if (j < half) {
       const float c = cos_sin[int64_t(p) * half + j];
       const float s = cos_sin[n + int64_t(p) * half + j];
-      v[j] = f2bf(a[i] * c - b[i] * s);
-      v[j + half] = f2bf(b[i] * c + a[i] * s);
+      rope_pair(a[i], b[i], c, s, v[j], v[j + half]);
     }
   }
 }
@@ -263,6 +293,132 @@ __global__ void kv_fp8_quant_kernel(const uint16_t* __restrict__ k,
     if (j < D) dst[j] = f2e4m3(x[i] / sc);
   }
   if (lane == 0) (which ? vs : ks)[s * Hkv + h] = sc;
+}
+
+// QKV finalize: one warp per (token, head) over the q, k and v heads.  It
+// computes what the QKV GEMM's fold, qk_norm_rope and kv_store_bf16 /
+// kv_fp8_quant compute one after another, with the same operations per
+// element, in one pass: fold the GEMM's chunk partials (when given) and round
+// to bf16; QK-RMSNorm and RoPE on q and k heads; write q, k, v back into qkv;
+// store k and v of rows with a cache slot into the paged cache (bf16, or e4m3
+// codes with scale amax/448 per (token, head)).
+__global__ void qkv_finalize_kernel(uint16_t* __restrict__ qkv, int64_t rs, const biv_partials xp,
+                                    int T, int Hq, int Hkv, int D, const uint16_t* __restrict__ qw,
+                                    const uint16_t* __restrict__ kw,
+                                    const float* __restrict__ cos_sin, int max_pos,
+                                    const int32_t* __restrict__ pos, float eps,
+                                    const int64_t* __restrict__ slot, int fp8, void* kc, void* vc,
+                                    float* ks, float* vs, int* err) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
+  const int heads = Hq + 2 * Hkv;
+  const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= int64_t(T) * heads) return;
+  const int t = int(gw / heads), h = int(gw % heads);
+  const int kind = h < Hq ? 0 : (h < Hq + Hkv ? 1 : 2);  // q, k, v
+  uint16_t* v = qkv + int64_t(t) * rs + int64_t(h) * D;
+  const int half = D / 2;
+  auto load = [&](int e) -> float {
+    if (xp.chunks == 0) return bf2f(v[e]);
+    const float* src = xp.p + int64_t(t) * xp.ld + int64_t(h) * D + e;
+    float acc = __ldcg(src);
+    for (int c = 1; c < xp.chunks; ++c) acc = acc + __ldcg(src + c * xp.chunk_stride);
+    return bf2f(f2bf(acc));
+  };
+  float a[2], b[2];
+  uint16_t oa[2], ob[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int j = lane + 32 * i;
+    a[i] = b[i] = 0.f;
+    if (j < half) {
+      a[i] = load(j);
+      b[i] = load(j + half);
+    }
+    oa[i] = f2bf(a[i]);
+    ob[i] = f2bf(b[i]);
+  }
+  if (kind < 2) {
+    const uint16_t* wn = kind == 0 ? qw : kw;
+    int p = pos[t];
+    if (p < 0 || p >= max_pos) {
+      if (lane == 0) raise_error(err, kErrBadIndex);
+      p = 0;
+    }
+    if (wn) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (lane + 32 * i < half) {
+          ss = fmaf(a[i], a[i], ss);
+          ss = fmaf(b[i], b[i], ss);
+        }
+      }
+      ss = warp_sum(ss);
+      const float inv = 1.0f / sqrtf(ss / float(D) + eps);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int j = lane + 32 * i;
+        if (j < half) {
+          a[i] = bf2f(f2bf((a[i] * inv) * bf2f(wn[j])));
+          b[i] = bf2f(f2bf((b[i] * inv) * bf2f(wn[j + half])));
+        }
+      }
+    }
+    const int64_t n = int64_t(max_pos) * half;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int j = lane + 32 * i;
+      if (j < half) {
+        const float c = cos_sin[int64_t(p) * half + j];
+        const float s = cos_sin[n + int64_t(p) * half + j];
+        rope_pair(a[i], b[i], c, s, oa[i], ob[i]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int j = lane + 32 * i;
+    if (j < half) {
+      v[j] = oa[i];
+      v[j + half] = ob[i];
+    }
+  }
+  if (kind == 0) return;
+  const int64_t sl = slot[t];
+  if (sl < 0) return;
+  const int hk = h - Hq - (kind == 2 ? Hkv : 0);
+  const int64_t base = (sl * Hkv + hk) * D;
+  if (!fp8) {
+    uint16_t* dst = static_cast<uint16_t*>(kind == 1 ? kc : vc) + base;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int j = lane + 32 * i;
+      if (j < half) {
+        dst[j] = oa[i];
+        dst[j + half] = ob[i];
+      }
+    }
+    return;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (lane + 32 * i < half) amax = fmaxf(amax, fmaxf(fabsf(bf2f(oa[i])), fabsf(bf2f(ob[i]))));
+  }
+  amax = warp_max(amax);
+  const float sc = amax == 0.f ? 1.0f : amax / 448.0f;
+  uint8_t* dst = static_cast<uint8_t*>(kind == 1 ? kc : vc) + base;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int j = lane + 32 * i;
+    if (j < half) {
+      dst[j] = f2e4m3(bf2f(oa[i]) / sc);
+      dst[j + half] = f2e4m3(bf2f(ob[i]) / sc);
+    }
+  }
+  if (lane == 0) (kind == 1 ? ks : vs)[sl * Hkv + hk] = sc;
 }
 
 __global__ void kv_fp8_gather_kernel(const uint8_t* __restrict__ codes,
@@ -552,22 +708,48 @@ biv_status biv_embed(const int32_t* ids, const uint16_t* table, int vocab, int T
   return check_launch("embed");
 }
 
-biv_status biv_add_rmsnorm(const uint16_t* x, int64_t xs, uint16_t* r, int64_t rs,
-                           const uint16_t* w, uint16_t* y, int64_t ys, int rows, int d, float eps,
-                           biv_stream_t stream) {
+}  // extern "C"
+
+namespace biv {
+namespace {
+biv_status add_rmsnorm_impl(const uint16_t* x, int64_t xs, const biv_partials& xp, uint16_t* r,
+                            int64_t rs, const uint16_t* w, uint16_t* y, int64_t ys, int rows, int d,
+                            float eps, biv_stream_t stream) {
   BIV_REQUIRE(rows >= 0 && d > 0 && d % 8 == 0 && d <= 8192, "add_rmsnorm: bad d=%d", d);
   if (rows == 0) return BIV_OK;
-  BIV_REQUIRE(row_ok(x, xs, 2) && row_ok(y, ys, 2) && aligned16(w) && (!r || row_ok(r, rs, 2)),
+  BIV_REQUIRE((xp.chunks > 0 || row_ok(x, xs, 2)) && row_ok(y, ys, 2) && aligned16(w) &&
+                  (!r || row_ok(r, rs, 2)),
               "add_rmsnorm: pointers/strides must keep rows 16-byte aligned");
+  BIV_REQUIRE(xp.chunks == 0 || (xp.chunks <= 8 && aligned16(xp.p) && xp.ld % 4 == 0 &&
+                                 xp.chunk_stride % 4 == 0),
+              "add_rmsnorm: bad partials");
   const int cpt = (d / 8 + kNormThreads - 1) / kNormThreads;
   cudaStream_t s = as_cuda(stream);
   switch (cpt) {
-    case 1: launch_pdl(add_rmsnorm_kernel<1>, rows, kNormThreads, 0, s, x, xs, r, rs, w, y, ys, d, eps); break;
-    case 2: launch_pdl(add_rmsnorm_kernel<2>, rows, kNormThreads, 0, s, x, xs, r, rs, w, y, ys, d, eps); break;
-    case 3: launch_pdl(add_rmsnorm_kernel<3>, rows, kNormThreads, 0, s, x, xs, r, rs, w, y, ys, d, eps); break;
-    default: launch_pdl(add_rmsnorm_kernel<4>, rows, kNormThreads, 0, s, x, xs, r, rs, w, y, ys, d, eps); break;
+    case 1: launch_pdl(add_rmsnorm_kernel<1>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
+    case 2: launch_pdl(add_rmsnorm_kernel<2>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
+    case 3: launch_pdl(add_rmsnorm_kernel<3>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
+    default: launch_pdl(add_rmsnorm_kernel<4>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
   }
   return check_launch("add_rmsnorm");
+}
+}  // namespace
+}  // namespace biv
+
+extern "C" {
+
+biv_status biv_add_rmsnorm(const uint16_t* x, int64_t xs, uint16_t* r, int64_t rs,
+                           const uint16_t* w, uint16_t* y, int64_t ys, int rows, int d, float eps,
+                           biv_stream_t stream) {
+  const biv_partials none = {nullptr, 0, 0, 0};
+  return add_rmsnorm_impl(x, xs, none, r, rs, w, y, ys, rows, d, eps, stream);
+}
+
+biv_status biv_add_rmsnorm_partials(const biv_partials* x, uint16_t* r, int64_t rs,
+                                    const uint16_t* w, uint16_t* y, int64_t ys, int rows, int d,
+                                    float eps, biv_stream_t stream) {
+  BIV_REQUIRE(x && x->p && x->chunks > 0, "add_rmsnorm_partials: no partials");
+  return add_rmsnorm_impl(nullptr, 0, *x, r, rs, w, y, ys, rows, d, eps, stream);
 }
 
 biv_status biv_silu_mul(const uint16_t* gu, int64_t gs, uint16_t* y, int64_t ys, int rows, int I,
@@ -601,6 +783,32 @@ biv_status biv_qk_norm_rope(uint16_t* qkv, int64_t rs, int T, int Hq, int Hkv, i
   launch_pdl(qk_norm_rope_kernel, unsigned(blocks), threads, 0, as_cuda(stream), qkv, rs, T, Hq,
              Hkv, D, q_w, k_w, cos_sin, max_pos, pos, eps, device_error_word());
   return check_launch("qk_norm_rope");
+}
+
+biv_status biv_qkv_finalize(uint16_t* qkv, int64_t rs, const biv_partials* qkv_partials, int T,
+                            int Hq, int Hkv, int D, const uint16_t* q_w, const uint16_t* k_w,
+                            const float* cos_sin, int max_pos, const int32_t* pos, float eps,
+                            const int64_t* slot, int kv_dtype, void* k_cache, void* v_cache,
+                            float* k_scale, float* v_scale, biv_stream_t stream) {
+  BIV_REQUIRE(D == 64 || D == 80 || D == 128, "qkv_finalize: D=%d unsupported", D);
+  BIV_REQUIRE(T >= 0 && Hq > 0 && Hkv > 0 && max_pos > 0, "qkv_finalize: bad sizes");
+  BIV_REQUIRE((q_w == nullptr) == (k_w == nullptr), "qkv_finalize: give both gains or neither");
+  BIV_REQUIRE(kv_dtype == BIV_BF16 || kv_dtype == BIV_E4M3, "qkv_finalize: kv dtype");
+  if (T == 0) return BIV_OK;
+  BIV_REQUIRE(qkv && cos_sin && pos && slot && k_cache && v_cache, "qkv_finalize: null pointer");
+  BIV_REQUIRE(kv_dtype == BIV_BF16 || (k_scale && v_scale), "qkv_finalize: FP8 needs scales");
+  biv_partials xp = {nullptr, 0, 0, 0};
+  if (qkv_partials && qkv_partials->chunks > 0) {
+    xp = *qkv_partials;
+    BIV_REQUIRE(xp.p && xp.chunks <= 8, "qkv_finalize: bad partials");
+  }
+  const int64_t warps = int64_t(T) * (Hq + 2 * Hkv);
+  const int threads = 256;
+  const int64_t blocks = (warps * 32 + threads - 1) / threads;
+  launch_pdl(qkv_finalize_kernel, unsigned(blocks), threads, 0, as_cuda(stream), qkv, rs, xp, T, Hq,
+             Hkv, D, q_w, k_w, cos_sin, max_pos, pos, eps, slot, kv_dtype == BIV_E4M3 ? 1 : 0,
+             k_cache, v_cache, k_scale, v_scale, device_error_word());
+  return check_launch("qkv_finalize");
 }
 
 biv_status biv_kv_store_bf16(const uint16_t* k, const uint16_t* v, int64_t rs, const int64_t* slot,

@@ -139,17 +139,30 @@ class DenseModel:
             return None
         return t
 
-    def _gemm(self, A, Bw, Cout, M, stream=None):
+    def _gemm(self, A, Bw, Cout, M, stream=None, defer=False):
+        """Cout = A . Bw^T.  With defer=True a plan that leaves chunk partials
+        skips its fold kernel and returns the partials for the consumer op
+        (Cout is then not written); otherwise returns None."""
         d = biv.gemm_desc(A, Bw, Cout, mode=self.mode, M=M)
         need = biv.biv_gemm_workspace(d)
         if need > self.gws.numel():
             raise RuntimeError(f"GEMM workspace too small ({need} > {self.gws.numel()}); call reserve()")
+        d.defer_fold = 1 if (defer and need) else 0
         t = self._timer()
         tok = t.bracket("gemm_bf16", 2.0 * M * d.N * d.K, "flop") if t else None
         biv.biv_gemm(d, self.gws, stream=stream)
         if tok:
             t.close(tok)
-        self.launches += 2 if need else 1   # chunk partials add the fold kernel
+        self.launches += 2 if (need and not d.defer_fold) else 1   # partials add the fold kernel
+        return biv.biv_gemm_partials(d, self.gws) if d.defer_fold else None
+
+    @staticmethod
+    def _add_rmsnorm(x, xp, r, w, y, T, eps, st):
+        """Residual add + RMSNorm of x[:T] (a GEMM output, or its chunk partials xp)."""
+        if xp is not None:
+            biv.biv_add_rmsnorm_partials(xp, r, w, y, T, eps, stream=st)
+        else:
+            biv.biv_add_rmsnorm(x[:T], r, w, y, eps, stream=st)
 
     def _attn_desc(self, kv: PagedKV, layer: int, spec: StepSpec, qblocks=None):
         cfg = self.cfg
@@ -223,20 +236,19 @@ class DenseModel:
         biv.biv_embed(self.ids[:T], W["embed"], r, stream=st)
         biv.biv_add_rmsnorm(r, None, W["l0.attn_norm"], y, eps, stream=st)
         self.launches += 2
+        # GEMMs whose plan leaves chunk partials hand them straight to the next
+        # op (the same bits, one launch fewer); the per-op audit wants every
+        # GEMM output stored, so it keeps the folds
+        defer = self.audit is None
         for l in range(cfg.layers):
             p = f"l{l}."
-            self._gemm(y, W[p + "wqkv"], self.qkv, T, st)
-            biv.biv_qk_norm_rope(self.qkv, T, Hq, Hkv, D, W.get(p + "q_norm") if cfg.qk_norm else None,
+            qp = self._gemm(y, W[p + "wqkv"], self.qkv, T, st, defer=defer)
+            # QK-norm + RoPE and the k/v cache store in one pass
+            biv.biv_qkv_finalize(self.qkv, T, Hq, Hkv, D, W.get(p + "q_norm") if cfg.qk_norm else None,
                                  W.get(p + "k_norm") if cfg.qk_norm else None, self.rope, self.max_pos,
-                                 self.row_pos, eps, stream=st)
-            kq = self.qkv[:, Hq * D:]
-            vq = self.qkv[:, (Hq + Hkv) * D:]
-            if kv.fp8:
-                biv.biv_kv_fp8_quant(kq, vq, self.qkv.stride(0), self.slot, T, Hkv, D, kv.k[l], kv.v[l],
-                                     kv.ks[l], kv.vs[l], stream=st)
-            else:
-                biv.biv_kv_store_bf16(kq, vq, self.qkv.stride(0), self.slot, T, Hkv, D, kv.k[l], kv.v[l],
-                                      stream=st)
+                                 self.row_pos, eps, self.slot, biv.E4M3 if kv.fp8 else biv.BF16,
+                                 kv.k[l], kv.v[l], kv.ks[l] if kv.fp8 else None,
+                                 kv.vs[l] if kv.fp8 else None, partials=qp, stream=st)
             ad = self._attn_desc(kv, l, spec, qblocks)
             need = biv.biv_attention_workspace(ad)
             t = self._timer()
@@ -244,22 +256,22 @@ class DenseModel:
             biv.biv_attention(ad, self.ws if need else None, stream=st)
             if tok:
                 t.close(tok)
-            self._gemm(self.o, W[p + "wo"], self.a, T, st)
+            op = self._gemm(self.o, W[p + "wo"], self.a, T, st, defer=defer)
             aud = self.audit is not None and not torch.cuda.is_current_stream_capturing()
             if aud:
                 self.audit.append(("qkv", l, self.qkv[:T].clone()))
                 self.audit.append(("attn_o", l, self.o[:T].clone()))
                 self.audit.append(("attn_proj", l, self.a[:T].clone()))
-            biv.biv_add_rmsnorm(self.a[:T], r, W[p + "mlp_norm"], y, eps, stream=st)
+            self._add_rmsnorm(self.a, op, r, W[p + "mlp_norm"], y, T, eps, st)
             self._gemm(y, W[p + "wgu"], self.gu, T, st)
             biv.biv_silu_mul(self.gu[:T], self.act[:T], stream=st)
-            self._gemm(self.act, W[p + "wd"], self.a, T, st)
+            dp = self._gemm(self.act, W[p + "wd"], self.a, T, st, defer=defer)
             if self.audit is not None and not torch.cuda.is_current_stream_capturing():
                 self.audit.append(("mlp_out", l, self.a[:T].clone()))
             nxt = W[f"l{l + 1}.attn_norm"] if l + 1 < cfg.layers else W["final_norm"]
-            biv.biv_add_rmsnorm(self.a[:T], r, nxt, y, eps, stream=st)
-            # qk_norm_rope, KV store, attention (+ split merge), 2 x add_rmsnorm, silu_mul
-            self.launches += 6 + (1 if need else 0)
+            self._add_rmsnorm(self.a, dp, r, nxt, y, T, eps, st)
+            # qkv finalize, attention (+ split merge), 2 x add_rmsnorm, silu_mul
+            self.launches += 5 + (1 if need else 0)
             if self.audit is not None and not torch.cuda.is_current_stream_capturing():
                 self.audit.append(("layer", l, r.clone()))
         # LM head + logprob over the rows that produce a logprob

@@ -156,6 +156,10 @@ def test_qwen3_full_depth_per_layer_parity(kv_fp8, capsys):
     m.audit, audit = None, m.audit
     res = [x for t, l, x in audit if t == "layer"]
     assert len(res) == cfg.layers
+    # without the audit the GEMMs leave their chunk partials to the next op
+    # (fold fused into QKV finalize and add+RMSNorm): the same bits
+    m.step(kv, spec)
+    assert np.array_equal(m.lp[:spec.T_lm].cpu().numpy().view(np.uint32), lp.view(np.uint32))
 
     def h32(t):
         return bf16_to_f32(t.cpu().view(torch.int16).numpy().view(np.uint16))

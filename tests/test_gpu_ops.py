@@ -459,3 +459,91 @@ def test_tcgen05_result_independent_of_tile_width(B, monkeypatch, M, N, K):
     ref = ops.gemm(a.float().numpy()[:5], b.float().numpy(), out="f32")
     got = outs[0].view(np.float32).reshape(M, N)[:5]
     assert rel_err(got, ref) < REL
+
+
+# ------------------------------------------------- fused GEMM consumers --
+def _deferred_gemm(B, ad, bd, M, N, ws):
+    """GEMM whose fold is left to the consumer; returns the partials (chunks
+    > 0) -- the shapes below are chosen so that the plan leaves partials."""
+    c = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    d = B.gemm_desc(ad, bd, c)
+    assert 0 < B.biv_gemm_workspace(d) <= ws.numel()
+    d.defer_fold = 1
+    B.biv_gemm(d, ws)
+    P = B.biv_gemm_partials(d, ws)
+    assert P.chunks > 1
+    return P
+
+
+@pytest.mark.parametrize("M,d_model,K", [(1, 2048, 2048), (37, 2048, 6144), (64, 1024, 3072)])
+def test_add_rmsnorm_from_partials_equals_folded_gemm(B, M, d_model, K):
+    """Residual add + RMSNorm reading the GEMM's chunk partials (the fold done
+    in the consumer) gives the bits of the GEMM folding them itself followed
+    by the plain op."""
+    g = synth.rng(M * 7 + K)
+    a, b = rnd_bf16(g, M, K), rnd_bf16(g, d_model, K, std=0.05)
+    r, w = rnd_bf16(g, M, d_model), rnd_bf16(g, d_model)
+    ad, bd, wd = dev(a), dev(b), dev(w)
+    ws = torch.full((64 << 20,), 0xFF, dtype=torch.uint8, device="cuda")
+    c = torch.empty(M, d_model, dtype=torch.bfloat16, device="cuda")
+    B.biv_gemm(B.gemm_desc(ad, bd, c), ws)
+    r1, y1 = dev(r), torch.empty(M, d_model, dtype=torch.bfloat16, device="cuda")
+    B.biv_add_rmsnorm(c, r1, wd, y1, 1e-6)
+    P = _deferred_gemm(B, ad, bd, M, d_model, ws)
+    r2, y2 = dev(r), torch.empty_like(y1)
+    B.biv_add_rmsnorm_partials(P, r2, wd, y2, M, 1e-6)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(r2), bits(r1)) and np.array_equal(bits(y2), bits(y1))
+
+
+@pytest.mark.parametrize("kv_fp8", [False, True], ids=["bf16kv", "fp8kv"])
+@pytest.mark.parametrize("D,qk,fold", [(128, True, False), (128, True, True), (64, False, True)])
+def test_qkv_finalize_equals_separate_ops(B, kv_fp8, D, qk, fold):
+    """QK-norm + RoPE + k/v cache store in one kernel (optionally folding the
+    QKV GEMM's chunk partials first) gives the bits of the separate ops: the
+    normed, rotated q and k rows, v untouched, the same cache codes/scales."""
+    g = synth.rng(D + 3 * qk + 5 * fold + 11 * kv_fp8)
+    T, Hq, Hkv, max_pos, K = 9, 4, 2, 5000, 2048
+    W3 = (Hq + 2 * Hkv) * D
+    pos = np.array([0, 1, 5, 77, 128, 1000, 4095, 4999, 3], np.int32)
+    slot = np.array([64, 65, 3, 130, 200, 7, 66, 140, 0], np.int64)
+    qw = dev(rnd_bf16(g, D)) if qk else None
+    kw = dev(rnd_bf16(g, D)) if qk else None
+    tab = torch.empty(2 * max_pos * (D // 2), dtype=torch.float32, device="cuda")
+    B.biv_rope_table(1e6, D, max_pos, tab)
+    pages, page = 4, 64
+    cdt = torch.uint8 if kv_fp8 else torch.bfloat16
+
+    def caches():
+        kc = torch.zeros(pages, page, Hkv, D, dtype=cdt, device="cuda")
+        ks = torch.zeros(pages, page, Hkv, dtype=torch.float32, device="cuda") if kv_fp8 else None
+        return kc, torch.zeros_like(kc), ks, (torch.zeros_like(ks) if kv_fp8 else None)
+
+    ws = torch.full((64 << 20,), 0xFF, dtype=torch.uint8, device="cuda")
+    if fold:
+        a, b = dev(rnd_bf16(g, T, K)), dev(rnd_bf16(g, W3, K, std=0.05))
+        q1 = torch.empty(T, W3, dtype=torch.bfloat16, device="cuda")
+        B.biv_gemm(B.gemm_desc(a, b, q1), ws)
+    else:
+        q1 = dev(rnd_bf16(g, T, W3))
+    q2 = q1.clone()
+    # separate ops
+    kc1, vc1, ks1, vs1 = caches()
+    B.biv_qk_norm_rope(q1, T, Hq, Hkv, D, qw, kw, tab, max_pos, dev(pos), 1e-6)
+    kq, vq = q1[:, Hq * D:], q1[:, (Hq + Hkv) * D:]
+    if kv_fp8:
+        B.biv_kv_fp8_quant(kq, vq, q1.stride(0), dev(slot), T, Hkv, D, kc1, vc1, ks1, vs1)
+    else:
+        B.biv_kv_store_bf16(kq, vq, q1.stride(0), dev(slot), T, Hkv, D, kc1, vc1)
+    # fused
+    kc2, vc2, ks2, vs2 = caches()
+    P = None
+    if fold:
+        q2.fill_(float("nan"))
+        P = _deferred_gemm(B, a, b, T, W3, ws)
+    B.biv_qkv_finalize(q2, T, Hq, Hkv, D, qw, kw, tab, max_pos, dev(pos), 1e-6, dev(slot),
+                       B.E4M3 if kv_fp8 else B.BF16, kc2, vc2, ks2, vs2, partials=P)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(q2), bits(q1))
+    for x, y in [(kc2, kc1), (vc2, vc1)] + ([(ks2, ks1), (vs2, vs1)] if kv_fp8 else []):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
