@@ -213,9 +213,11 @@ def main():
         dg = DecodeGraphs(m, kv_roll, use_graphs=not args.eager)
         return m, kv_roll, kv_rec, dg
 
-    def one_step(arm, collect=False):
+    def one_step(arm, collect=False, mid=None):
         m, kv_roll, kv_rec, dg = arm
         a = rollout(m, kv_roll, seqs, args.max_tokens, graphs=dg, collect=collect)
+        if mid is not None:
+            mid.record(torch.cuda.current_stream())
         b = recompute(m, kv_rec, seqs, args.max_tokens)
         return a, b
 
@@ -230,9 +232,12 @@ def main():
         st = torch.cuda.current_stream()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         arm[0].kernel_timer = timer = KernelTimer()
+        # step boundaries and the rollout/recompute boundary of each step
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
         e0.record(st)
-        for _ in range(steps):
-            one_step(arm)
+        for i in range(steps):
+            one_step(arm, mid=ev[2 * i])
+            ev[2 * i + 1].record(st)
         e1.record(st)
         torch.cuda.synchronize()
         arm[0].kernel_timer = None
@@ -240,6 +245,9 @@ def main():
             dist.barrier()
         ck = clocks.stop() if clocks else None
         ms = e0.elapsed_time(e1) / steps
+        starts = [e0] + ev[1::2][:-1]
+        roll = sum(a.elapsed_time(b) for a, b in zip(starts, ev[0::2])) / steps
+        timer.phases = {"rollout_ms": roll, "recompute_ms": ms - roll}
         return ms, ck, timer
 
     inv = build_arm(biv.MODE_INVARIANT)
@@ -259,8 +267,8 @@ def main():
         del inv
         torch.cuda.empty_cache()
         fast_arm = build_arm(biv.MODE_FAST)
-        ms_f, _, _ = timed(fast_arm, max(1, args.steps), 1)
-        fast = {"value": tokens_per_step / (ms_f / 1e3), "ms_per_step": ms_f,
+        ms_f, _, t_f = timed(fast_arm, max(1, args.steps), 1)
+        fast = {"value": tokens_per_step / (ms_f / 1e3), "ms_per_step": ms_f, "phases": t_f.phases,
                 "invariant_over_fast": (tokens_per_step / (ms / 1e3)) / (tokens_per_step / (ms_f / 1e3))}
         del fast_arm
         torch.cuda.empty_cache()
@@ -287,7 +295,7 @@ def main():
                 "logprob_diff_rollout_vs_recompute": diff_max,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": ck,
                 "gpu_launches": timer.launches, "fast_comparator": fast,
-                "kernels": timer.summary(peaks)}
+                "kernels": timer.summary(peaks), "phases": timer.phases}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

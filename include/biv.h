@@ -120,6 +120,14 @@ biv_status biv_add_rmsnorm_partials(const biv_partials* x, uint16_t* residual, i
 biv_status biv_silu_mul(const uint16_t* gate_up, int64_t gu_stride, uint16_t* y,
                         int64_t y_stride, int rows, int I, biv_stream_t stream);
 
+/* The same, with gate_up given as the chunk partials of the GEMM that
+ * produced it (biv_gemm with defer_fold; partial columns [0, I) are g and
+ * [I, 2I) are u): folded here to the GEMM's bf16 output, so y is the same bit
+ * for bit.  BIV_ERR_ARG on chunks outside 1..8, a partial base not 16-byte
+ * aligned, or ld / chunk_stride not multiples of 4 or ld < 2I. */
+biv_status biv_silu_mul_partials(const biv_partials* gate_up, uint16_t* y, int64_t y_stride,
+                                 int rows, int I, biv_stream_t stream);
+
 /* --------------------------------------------------------- RoPE table ----
  * cos_sin float32 [2, max_pos, D/2]: cos then sin of pos * theta^(-2i/D),
  * computed in double precision on the device and rounded to FP32. */

@@ -21,7 +21,7 @@ BF16, F32, E4M3 = 0, 1, 2
 EXPORTS = [
     "biv_version", "biv_last_error", "biv_device_sm_count", "biv_poll_error",
     "biv_selftest_timeout", "biv_embed", "biv_add_rmsnorm", "biv_add_rmsnorm_partials", "biv_silu_mul",
-    "biv_rope_table", "biv_qk_norm_rope", "biv_kv_store_bf16", "biv_kv_fp8_quant", "biv_qkv_finalize",
+    "biv_rope_table", "biv_qk_norm_rope", "biv_kv_store_bf16", "biv_kv_fp8_quant", "biv_qkv_finalize", "biv_silu_mul_partials",
     "biv_kv_fp8_gather", "biv_attention_workspace", "biv_attention", "biv_attention_noalloc",
     "biv_gemm_workspace", "biv_gemm_partials", "biv_gemm",
     "biv_act_quant_fp8", "biv_topk", "biv_router_topk", "biv_moe_dispatch", "biv_gather_rows",
@@ -108,6 +108,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "biv_qkv_finalize": ([P, I64, P, I, I, I, I, P, P, P, I, P, F, P, I, P, P, P, P, P], I),
         "biv_gemm_partials": ([P, P, P], I),
         "biv_silu_mul": ([P, I64, P, I64, I, I, P], I),
+        "biv_silu_mul_partials": ([P, P, I64, I, I, P], I),
         "biv_rope_table": ([D_, I, I, P, P], I),
         "biv_qk_norm_rope": ([P, I64, I, I, I, I, P, P, P, I, P, F, P], I),
         "biv_kv_store_bf16": ([P, P, I64, P, I, I, I, P, P, P], I),
@@ -222,6 +223,13 @@ def biv_add_rmsnorm_partials(xp: "Partials", residual, w, y, rows, eps, stream=N
                                            _rs(residual) if residual is not None else 0, _p(w), _p(y),
                                            _rs(y), rows, d, float(eps), _stream(stream)),
            "biv_add_rmsnorm_partials")
+
+
+def biv_silu_mul_partials(gp: "Partials", y, rows, stream=None):
+    """gate_up given as GEMM chunk partials; I = y.shape[-1]."""
+    _bf16_ok(y)
+    _check(load().biv_silu_mul_partials(C.byref(gp), _p(y), _rs(y), rows, y.shape[-1],
+                                        _stream(stream)), "biv_silu_mul_partials")
 
 
 def biv_qkv_finalize(qkv, T, Hq, Hkv, D, q_w, k_w, cos_sin, max_pos, pos, eps, slot, kv_dtype,

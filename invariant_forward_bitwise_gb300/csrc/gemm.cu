@@ -638,6 +638,11 @@ struct Plan {
 };
 
 constexpr size_t kSmemBudget = 227 * 1024;  // the per-CTA maximum
+// At most this many rows, partial mode is taken whenever 128-column tiles
+// leave an SM idle (measured on GB300, 12288 x 2048 weights: M = 1 and 64 ran
+// 14.5 and 16.6 us as partials, 17.2 and 18.2 us folded in 96 CTAs; at M = 128
+// the partials' own traffic made folding faster)
+constexpr int kPartialRows = 64;
 // The wide tile of the register-fold mode (measured on GB300 at M = 16384:
 // 256 columns beat 192 although each epilogue thread then keeps 128 running
 // sums and spills a few registers).
@@ -672,7 +677,9 @@ Plan plan_bf16(const biv_gemm_desc& d) {
   const int64_t tiles_wide = int64_t((d.N + kWideN - 1) / kWideN) * tiles_m;
   const int64_t tiles128 = int64_t((d.N + 127) / 128) * tiles_m;
   const bool wide = tiles_wide >= sms;   // enough 128 x kWideN tiles to fill the GPU
-  bool partial = !wide && tiles128 * 2 <= sms;
+  // partials when whole 128-column tiles leave most SMs idle, and for the
+  // few-row (weight-streaming) shapes whenever they leave any SM idle
+  bool partial = !wide && (tiles128 * 2 <= sms || (d.M <= kPartialRows && tiles128 < sms));
   if (d.mode == BIV_MODE_INVARIANT) {
     p.kc_blocks = std::max(kMinChunkBlocks, (KB + kMaxChunks - 1) / kMaxChunks);
   } else if (partial) {
@@ -683,7 +690,23 @@ Plan plan_bf16(const biv_gemm_desc& d) {
     p.kc_blocks = KB;
   }
   p.chunks = (KB + p.kc_blocks - 1) / p.kc_blocks;
-  p.bn = wide ? kWideN : 128;
+  if (wide) {
+    p.bn = kWideN;
+  } else if (partial && p.chunks > 1) {
+    p.bn = 128;
+  } else {
+    // fold mode below one full wave of wide tiles: the width with the least
+    // A + B rows streamed by the busiest CTA (rounds of tiles x rows per tile)
+    int64_t best = -1;
+    for (const int bn : {128, 192, 256}) {
+      const int64_t t = int64_t((d.N + bn - 1) / bn) * tiles_m;
+      const int64_t cost = (t + sms - 1) / sms * (p.m_box + bn);
+      if (best < 0 || cost < best) {
+        best = cost;
+        p.bn = bn;
+      }
+    }
+  }
   if (const int bn = env_tile_n()) p.bn = bn;
   if (const int f = env_fold()) partial = f == 2;
   p.tiles = int64_t((d.N + p.bn - 1) / p.bn) * tiles_m;

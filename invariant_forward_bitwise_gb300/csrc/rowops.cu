@@ -61,23 +61,36 @@ __global__ void embed_kernel(const int32_t* __restrict__ ids, const uint16_t* __
 // 8 consecutive bf16 outputs of a GEMM whose chunk partials were left for the
 // consumer: fold the partials in chunk order, round once (what the GEMM's own
 // fold kernel stores)
+// GEMM chunk partials hold at most this many chunks (the GEMM's schedule)
+constexpr int kMaxPartialChunks = 8;
+
+// 8 consecutive columns of one row folded over the chunks in chunk order and
+// rounded to bf16 (what the GEMM's own fold stores).  Every chunk's loads are
+// issued before the first add so that the chunks' latencies overlap.
 __device__ __forceinline__ void fold8(const biv_partials& xp, int64_t row, int col, float (&f)[8]) {
   const float* src = xp.p + row * xp.ld + col;
-  float4 a = __ldcg(reinterpret_cast<const float4*>(src));
-  float4 b = __ldcg(reinterpret_cast<const float4*>(src + 4));
-  for (int c = 1; c < xp.chunks; ++c) {
-    const float* sc = src + c * xp.chunk_stride;
-    const float4 a2 = __ldcg(reinterpret_cast<const float4*>(sc));
-    const float4 b2 = __ldcg(reinterpret_cast<const float4*>(sc + 4));
-    a.x = a.x + a2.x; a.y = a.y + a2.y; a.z = a.z + a2.z; a.w = a.w + a2.w;
-    b.x = b.x + b2.x; b.y = b.y + b2.y; b.z = b.z + b2.z; b.w = b.w + b2.w;
+  float4 a[kMaxPartialChunks], b[kMaxPartialChunks];
+#pragma unroll
+  for (int c = 0; c < kMaxPartialChunks; ++c) {
+    if (c < xp.chunks) {
+      const float* sc = src + c * xp.chunk_stride;
+      a[c] = __ldcg(reinterpret_cast<const float4*>(sc));
+      b[c] = __ldcg(reinterpret_cast<const float4*>(sc + 4));
+    }
   }
-  const float t[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float t[8] = {a[0].x, a[0].y, a[0].z, a[0].w, b[0].x, b[0].y, b[0].z, b[0].w};
+#pragma unroll
+  for (int c = 1; c < kMaxPartialChunks; ++c) {
+    if (c < xp.chunks) {
+      t[0] = t[0] + a[c].x; t[1] = t[1] + a[c].y; t[2] = t[2] + a[c].z; t[3] = t[3] + a[c].w;
+      t[4] = t[4] + b[c].x; t[5] = t[5] + b[c].y; t[6] = t[6] + b[c].z; t[7] = t[7] + b[c].w;
+    }
+  }
 #pragma unroll
   for (int j = 0; j < 8; ++j) f[j] = bf2f(f2bf(t[j]));
 }
 
-template <int CPT>  // chunks per thread (ceil(d/8/256))
+template <int CPT, bool PARTIAL>  // chunks per thread (ceil(d/8/256)); x as partials
 __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
     const uint16_t* __restrict__ x, int64_t xs, const biv_partials xp, uint16_t* __restrict__ r,
     int64_t rs, const uint16_t* __restrict__ w, uint16_t* __restrict__ y, int64_t ys, int d,
@@ -95,7 +108,7 @@ __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
   for (int i = 0; i < CPT; ++i) {
     const int c = threadIdx.x + i * kNormThreads;
     if (c < chunks) {
-      if (xp.chunks > 0)
+      if (PARTIAL)
         fold8(xp, row, c * 8, v[i]);
       else
         unpack8(xr[c], v[i]);
@@ -133,7 +146,10 @@ __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
 }
 
 // ------------------------------------------------------------- SiLU-mul ----
-__global__ void silu_mul_kernel(const uint16_t* __restrict__ gu, int64_t gs,
+// gate_up given as bf16 rows, or (gp.chunks > 0) as the chunk partials of the
+// GEMM that produced it, folded here to the same bf16 values
+template <bool PARTIAL>
+__global__ void silu_mul_kernel(const uint16_t* __restrict__ gu, int64_t gs, const biv_partials gp,
                                 uint16_t* __restrict__ y, int64_t ys, int rows, int I) {
   pdl_wait();     // stream predecessor done, its writes visible
   pdl_trigger();
@@ -142,10 +158,15 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ gu, int64_t gs,
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
        i += int64_t(gridDim.x) * blockDim.x) {
     const int row = int(i / cpr), c = int(i % cpr);
-    const uint4* g = reinterpret_cast<const uint4*>(gu + int64_t(row) * gs);
     float gv[8], uv[8], o[8];
-    unpack8(g[c], gv);
-    unpack8(g[cpr + c], uv);
+    if (PARTIAL) {
+      fold8(gp, row, c * 8, gv);
+      fold8(gp, row, I + c * 8, uv);
+    } else {
+      const uint4* g = reinterpret_cast<const uint4*>(gu + int64_t(row) * gs);
+      unpack8(g[c], gv);
+      unpack8(g[cpr + c], uv);
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) o[j] = (gv[j] / (1.0f + expf(-gv[j]))) * uv[j];
     reinterpret_cast<uint4*>(y + int64_t(row) * ys)[c] = pack8(o);
@@ -302,6 +323,7 @@ __global__ void kv_fp8_quant_kernel(const uint16_t* __restrict__ k,
 // to bf16; QK-RMSNorm and RoPE on q and k heads; write q, k, v back into qkv;
 // store k and v of rows with a cache slot into the paged cache (bf16, or e4m3
 // codes with scale amax/448 per (token, head)).
+template <bool PARTIAL>
 __global__ void qkv_finalize_kernel(uint16_t* __restrict__ qkv, int64_t rs, const biv_partials xp,
                                     int T, int Hq, int Hkv, int D, const uint16_t* __restrict__ qw,
                                     const uint16_t* __restrict__ kw,
@@ -319,23 +341,51 @@ __global__ void qkv_finalize_kernel(uint16_t* __restrict__ qkv, int64_t rs, cons
   const int kind = h < Hq ? 0 : (h < Hq + Hkv ? 1 : 2);  // q, k, v
   uint16_t* v = qkv + int64_t(t) * rs + int64_t(h) * D;
   const int half = D / 2;
-  auto load = [&](int e) -> float {
-    if (xp.chunks == 0) return bf2f(v[e]);
-    const float* src = xp.p + int64_t(t) * xp.ld + int64_t(h) * D + e;
-    float acc = __ldcg(src);
-    for (int c = 1; c < xp.chunks; ++c) acc = acc + __ldcg(src + c * xp.chunk_stride);
-    return bf2f(f2bf(acc));
-  };
   float a[2], b[2];
   uint16_t oa[2], ob[2];
+  if (!PARTIAL) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int j = lane + 32 * i;
+      a[i] = j < half ? bf2f(v[j]) : 0.f;
+      b[i] = j < half ? bf2f(v[j + half]) : 0.f;
+    }
+  } else {
+    // the GEMM's fold: chunk-order FP32 sum, rounded to bf16; all loads are
+    // issued before the first add
+    const float* src = xp.p + int64_t(t) * xp.ld + int64_t(h) * D;
+    float pa[2][kMaxPartialChunks], pb[2][kMaxPartialChunks];
+#pragma unroll
+    for (int c = 0; c < kMaxPartialChunks; ++c) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int j = lane + 32 * i;
+        if (c < xp.chunks && j < half) {
+          pa[i][c] = __ldcg(src + c * xp.chunk_stride + j);
+          pb[i][c] = __ldcg(src + c * xp.chunk_stride + j + half);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      a[i] = b[i] = 0.f;
+      if (lane + 32 * i < half) {
+        a[i] = pa[i][0];
+        b[i] = pb[i][0];
+#pragma unroll
+        for (int c = 1; c < kMaxPartialChunks; ++c) {
+          if (c < xp.chunks) {
+            a[i] = a[i] + pa[i][c];
+            b[i] = b[i] + pb[i][c];
+          }
+        }
+        a[i] = bf2f(f2bf(a[i]));
+        b[i] = bf2f(f2bf(b[i]));
+      }
+    }
+  }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const int j = lane + 32 * i;
-    a[i] = b[i] = 0.f;
-    if (j < half) {
-      a[i] = load(j);
-      b[i] = load(j + half);
-    }
     oa[i] = f2bf(a[i]);
     ob[i] = f2bf(b[i]);
   }
@@ -377,12 +427,14 @@ __global__ void qkv_finalize_kernel(uint16_t* __restrict__ qkv, int64_t rs, cons
       }
     }
   }
+  if (PARTIAL || kind < 2) {  // v rows already hold their values unless folded here
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int j = lane + 32 * i;
-    if (j < half) {
-      v[j] = oa[i];
-      v[j + half] = ob[i];
+    for (int i = 0; i < 2; ++i) {
+      const int j = lane + 32 * i;
+      if (j < half) {
+        v[j] = oa[i];
+        v[j + half] = ob[i];
+      }
     }
   }
   if (kind == 0) return;
@@ -712,6 +764,20 @@ biv_status biv_embed(const int32_t* ids, const uint16_t* table, int vocab, int T
 
 namespace biv {
 namespace {
+template <bool PARTIAL>
+biv_status launch_add_rmsnorm(int cpt, const uint16_t* x, int64_t xs, const biv_partials& xp,
+                              uint16_t* r, int64_t rs, const uint16_t* w, uint16_t* y, int64_t ys,
+                              int rows, int d, float eps, biv_stream_t stream) {
+  cudaStream_t s = as_cuda(stream);
+  switch (cpt) {
+    case 1: launch_pdl(add_rmsnorm_kernel<1, PARTIAL>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
+    case 2: launch_pdl(add_rmsnorm_kernel<2, PARTIAL>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
+    case 3: launch_pdl(add_rmsnorm_kernel<3, PARTIAL>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
+    default: launch_pdl(add_rmsnorm_kernel<4, PARTIAL>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
+  }
+  return check_launch("add_rmsnorm");
+}
+
 biv_status add_rmsnorm_impl(const uint16_t* x, int64_t xs, const biv_partials& xp, uint16_t* r,
                             int64_t rs, const uint16_t* w, uint16_t* y, int64_t ys, int rows, int d,
                             float eps, biv_stream_t stream) {
@@ -720,18 +786,12 @@ biv_status add_rmsnorm_impl(const uint16_t* x, int64_t xs, const biv_partials& x
   BIV_REQUIRE((xp.chunks > 0 || row_ok(x, xs, 2)) && row_ok(y, ys, 2) && aligned16(w) &&
                   (!r || row_ok(r, rs, 2)),
               "add_rmsnorm: pointers/strides must keep rows 16-byte aligned");
-  BIV_REQUIRE(xp.chunks == 0 || (xp.chunks <= 8 && aligned16(xp.p) && xp.ld % 4 == 0 &&
+  BIV_REQUIRE(xp.chunks == 0 || (xp.chunks <= kMaxPartialChunks && aligned16(xp.p) && xp.ld % 4 == 0 &&
                                  xp.chunk_stride % 4 == 0),
               "add_rmsnorm: bad partials");
   const int cpt = (d / 8 + kNormThreads - 1) / kNormThreads;
-  cudaStream_t s = as_cuda(stream);
-  switch (cpt) {
-    case 1: launch_pdl(add_rmsnorm_kernel<1>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
-    case 2: launch_pdl(add_rmsnorm_kernel<2>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
-    case 3: launch_pdl(add_rmsnorm_kernel<3>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
-    default: launch_pdl(add_rmsnorm_kernel<4>, rows, kNormThreads, 0, s, x, xs, xp, r, rs, w, y, ys, d, eps); break;
-  }
-  return check_launch("add_rmsnorm");
+  if (xp.chunks > 0) return launch_add_rmsnorm<true>(cpt, x, xs, xp, r, rs, w, y, ys, rows, d, eps, stream);
+  return launch_add_rmsnorm<false>(cpt, x, xs, xp, r, rs, w, y, ys, rows, d, eps, stream);
 }
 }  // namespace
 }  // namespace biv
@@ -758,7 +818,26 @@ biv_status biv_silu_mul(const uint16_t* gu, int64_t gs, uint16_t* y, int64_t ys,
   if (rows == 0) return BIV_OK;
   BIV_REQUIRE(row_ok(gu, gs, 2) && row_ok(y, ys, 2), "silu_mul: misaligned rows");
   const int64_t work = int64_t(rows) * (I / 8);
-  launch_pdl(silu_mul_kernel, grid_for(work, 256), 256, 0, as_cuda(stream), gu, gs, y, ys, rows, I);
+  const biv_partials none = {nullptr, 0, 0, 0};
+  launch_pdl(silu_mul_kernel<false>, grid_for(work, 256), 256, 0, as_cuda(stream), gu, gs, none, y,
+             ys, rows, I);
+  return check_launch("silu_mul");
+}
+
+biv_status biv_silu_mul_partials(const biv_partials* gu, uint16_t* y, int64_t ys, int rows, int I,
+                                 biv_stream_t stream) {
+  BIV_REQUIRE(rows >= 0 && I > 0 && I % 8 == 0, "silu_mul: I=%d must be a multiple of 8", I);
+  BIV_REQUIRE(gu && gu->p && gu->chunks > 0 && gu->chunks <= kMaxPartialChunks &&
+                  aligned16(gu->p) && gu->ld % 4 == 0 && gu->chunk_stride % 4 == 0 &&
+                  gu->ld >= 2 * int64_t(I),
+              "silu_mul_partials: bad partials");
+  if (rows == 0) return BIV_OK;
+  BIV_REQUIRE(row_ok(y, ys, 2), "silu_mul: misaligned rows");
+  const int64_t work = int64_t(rows) * (I / 8);
+  // 128-thread CTAs: the partials variant keeps every chunk's loads in
+  // registers (about 170 per thread), so smaller CTAs spread over more SMs
+  launch_pdl(silu_mul_kernel<true>, grid_for(work, 128), 128, 0, as_cuda(stream), nullptr,
+             int64_t(0), *gu, y, ys, rows, I);
   return check_launch("silu_mul");
 }
 
@@ -800,14 +879,15 @@ biv_status biv_qkv_finalize(uint16_t* qkv, int64_t rs, const biv_partials* qkv_p
   biv_partials xp = {nullptr, 0, 0, 0};
   if (qkv_partials && qkv_partials->chunks > 0) {
     xp = *qkv_partials;
-    BIV_REQUIRE(xp.p && xp.chunks <= 8, "qkv_finalize: bad partials");
+    BIV_REQUIRE(xp.p && xp.chunks <= kMaxPartialChunks, "qkv_finalize: bad partials");
   }
   const int64_t warps = int64_t(T) * (Hq + 2 * Hkv);
   const int threads = 256;
   const int64_t blocks = (warps * 32 + threads - 1) / threads;
-  launch_pdl(qkv_finalize_kernel, unsigned(blocks), threads, 0, as_cuda(stream), qkv, rs, xp, T, Hq,
-             Hkv, D, q_w, k_w, cos_sin, max_pos, pos, eps, slot, kv_dtype == BIV_E4M3 ? 1 : 0,
-             k_cache, v_cache, k_scale, v_scale, device_error_word());
+  launch_pdl(xp.chunks > 0 ? qkv_finalize_kernel<true> : qkv_finalize_kernel<false>,
+             unsigned(blocks), threads, 0, as_cuda(stream), qkv, rs, xp, T, Hq, Hkv, D, q_w, k_w,
+             cos_sin, max_pos, pos, eps, slot, kv_dtype == BIV_E4M3 ? 1 : 0, k_cache, v_cache,
+             k_scale, v_scale, device_error_word());
   return check_launch("qkv_finalize");
 }
 

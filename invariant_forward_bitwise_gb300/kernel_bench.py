@@ -203,20 +203,31 @@ elif case == "gemm_prefill_layer":
 elif case == "gemm_sweep":
     # weights rotate through enough copies to exceed L2, as in a decode step
     # where every layer's weights are cold
+    # BIV_BENCH_MS: comma-separated M values; BIV_BENCH_DEFER=1 times the GEMM
+    # kernel alone when it leaves chunk partials (the consumer op folds them)
     shapes = {"qkv": (4096, 2048), "o": (2048, 2048), "gate_up": (12288, 2048),
               "down": (2048, 6144), "lm_head": (151936, 2048)}
+    ms_list = [int(x) for x in os.environ.get("BIV_BENCH_MS", "1,16,64,128,256,512").split(",")]
+    defer = os.environ.get("BIV_BENCH_DEFER") == "1"
+    if os.environ.get("BIV_BENCH_SHAPES"):
+        shapes = {k: shapes[k] for k in os.environ["BIV_BENCH_SHAPES"].split(",")}
     for name, (N, K) in shapes.items():
         copies = max(1, -(-300_000_000 // (N * K * 2)))
         bs = [(torch.randn(N, K, device="cuda") * 0.02).to(torch.bfloat16) for _ in range(copies)]
-        for M in (1, 16, 64, 128, 256, 512):
+        for M in ms_list:
             a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
             c = torch.empty(M, N, device="cuda",
                             dtype=torch.float32 if name == "lm_head" else torch.bfloat16)
             ds = [biv.gemm_desc(a, b, c) for b in bs]
+            need = biv.biv_gemm_workspace(ds[0])
+            for d in ds:
+                d.defer_fold = int(defer)
+            ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
             n = copies * max(1, 8 // copies)
-            ms = graph_time(lambda: [biv.biv_gemm(ds[i % copies]) for i in range(n)], 1) / n
+            ms = graph_time(lambda: [biv.biv_gemm(ds[i % copies], ws) for i in range(n)], 1) / n
             print(f"{name:8s} M={M:4d} N={N:6d} K={K}: {ms*1e3:8.1f} us  weights {N*K*2/(ms/1e3)/1e9:6.0f} GB/s"
-                  f"  {2*M*N*K/(ms/1e3)/1e12:6.1f} TFLOP/s", flush=True)
+                  f"  {2*M*N*K/(ms/1e3)/1e12:6.1f} TFLOP/s  {'partials' if need else 'in-CTA fold'}",
+                  flush=True)
         del bs
 else:
     M, N, K = {"gemm_prefill": (8192, 2048, 6144), "gemm_qkv": (16384, 4096, 2048),

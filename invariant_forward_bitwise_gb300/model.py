@@ -263,8 +263,11 @@ class DenseModel:
                 self.audit.append(("attn_o", l, self.o[:T].clone()))
                 self.audit.append(("attn_proj", l, self.a[:T].clone()))
             self._add_rmsnorm(self.a, op, r, W[p + "mlp_norm"], y, T, eps, st)
-            self._gemm(y, W[p + "wgu"], self.gu, T, st)
-            biv.biv_silu_mul(self.gu[:T], self.act[:T], stream=st)
+            gp = self._gemm(y, W[p + "wgu"], self.gu, T, st, defer=defer)
+            if gp is not None:
+                biv.biv_silu_mul_partials(gp, self.act[:T], T, stream=st)
+            else:
+                biv.biv_silu_mul(self.gu[:T], self.act[:T], stream=st)
             dp = self._gemm(self.act, W[p + "wd"], self.a, T, st, defer=defer)
             if self.audit is not None and not torch.cuda.is_current_stream_capturing():
                 self.audit.append(("mlp_out", l, self.a[:T].clone()))

@@ -547,3 +547,22 @@ def test_qkv_finalize_equals_separate_ops(B, kv_fp8, D, qk, fold):
     assert np.array_equal(bits(q2), bits(q1))
     for x, y in [(kc2, kc1), (vc2, vc1)] + ([(ks2, ks1), (vs2, vs1)] if kv_fp8 else []):
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+
+
+@pytest.mark.parametrize("M,I", [(1, 6144), (64, 6144), (5, 688)])
+def test_silu_mul_from_partials_equals_folded_gemm(B, M, I):
+    """SiLU-mul reading the gate/up GEMM's chunk partials gives the bits of
+    the GEMM folding them itself followed by the plain op."""
+    g = synth.rng(M + I)
+    K = 2048
+    a, b = dev(rnd_bf16(g, M, K)), dev(rnd_bf16(g, 2 * I, K, std=0.05))
+    ws = torch.full((64 << 20,), 0xFF, dtype=torch.uint8, device="cuda")
+    gu = torch.empty(M, 2 * I, dtype=torch.bfloat16, device="cuda")
+    B.biv_gemm(B.gemm_desc(a, b, gu), ws)
+    y1 = torch.empty(M, I, dtype=torch.bfloat16, device="cuda")
+    B.biv_silu_mul(gu, y1)
+    P = _deferred_gemm(B, a, b, M, 2 * I, ws)
+    y2 = torch.full_like(y1, float("nan"))
+    B.biv_silu_mul_partials(P, y2, M)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(y2), bits(y1))
