@@ -329,6 +329,33 @@ def test_topk_indexer_shape(B):
     assert np.array_equal(one.cpu().numpy()[0], got[40])
 
 
+def test_topk_range_refinement_distributions(B):
+    """Rows whose keys sit in one bin, two values, the extremes of the float
+    range (+inf, the largest and smallest normals, denormals), only negative
+    scores, a ragged valid length: every row equals the oracle's selection."""
+    g = synth.rng(16)
+    R, n, k = 12, 5000, 300
+    s = synth.normal_f32(g, (R, n))
+    s[0] = 1.5                                            # one key value
+    s[1] = np.where(g.random(n) < 0.5, 2.0, -2.0)         # two values
+    s[2] = np.float32(3.4e38) * np.sign(s[2])             # +-max normal
+    s[2, ::7] = np.inf
+    s[3] = np.float32(1e-40) * g.integers(-3, 4, n)        # denormals and zeros
+    s[4] = -np.abs(s[4]) - 1.0                            # all negative
+    s[5] = np.ldexp(np.float32(1.0), g.integers(-120, 120, n)).astype(np.float32)  # exponents spread
+    s[6] = np.float32(1.0) + np.float32(2.0 ** -23) * g.integers(0, 40, n)  # adjacent keys
+    s[7, :] = -np.inf
+    s[7, 10:20] = 0.5                                     # fewer valid than k
+    s[8] = np.round(s[8] * 4) / 4                         # many ties at the threshold
+    nv = np.full(R, n, np.int32)
+    nv[9] = 1234
+    nv[10] = k                                            # exactly k valid
+    nv[11] = 0
+    idx = torch.empty(R, k, dtype=torch.int32, device="cuda")
+    B.biv_topk(dev(s), dev(nv), k, idx)
+    assert np.array_equal(idx.cpu().numpy(), ops.topk_positions(s, nv, k))
+
+
 def test_router_topk(B):
     g = synth.rng(16)
     R, E, k = 300, 64, 6
