@@ -168,14 +168,18 @@ template <int BN>
 struct GemmSmem {
   static constexpr int B_STAGE = BN * 128;
   // bytes of dynamic shared memory for `stages` stages of an m_box-row A box
-  static size_t bytes(int stages, int m_box) {
+  // (the store staging blocks only in fold mode)
+  static size_t bytes(int stages, int m_box, bool staging) {
     return 1024 + size_t(stages) * (B_STAGE + m_box * 128) + (128 - m_box) * 128 +
-           (2 * kMaxStages + 4) * 8 + 16 + kStagingBytes;
+           (2 * kMaxStages + 4) * 8 + 16 + (staging ? kStagingBytes : 0);
   }
 };
 
-template <int BN, bool F32OUT>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// PARTIAL: the partial-mode instantiation.  Its epilogue keeps no running
+// sum, so it is compiled for half the register file; with PDL the next
+// kernel's CTAs can then start on the same SMs while it runs.
+template <int BN, bool F32OUT, bool PARTIAL>
+__global__ void __launch_bounds__(kGemmThreads, PARTIAL ? 2 : 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
   constexpr int B_STAGE = GemmSmem<BN>::B_STAGE;
@@ -204,7 +208,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int chunks = (KB + p.kc_blocks - 1) / p.kc_blocks;
   const int tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
   const int tiles = tiles_m * tiles_n;
-  const bool partial = kPartialOk && p.partial;
+  static_assert(!PARTIAL || kPartialOk, "partial mode needs tiles of at most 128 columns");
+  constexpr bool partial = PARTIAL;
   const int items = partial ? tiles * chunks : tiles;
   // item -> tile and chunk range
   auto item_tile = [&](int i) { return partial ? i / chunks : i; };
@@ -310,7 +315,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3, col0 = ((warp - 2) >> 2) * HALF;
-    float r[HALF];
+    float r[PARTIAL ? 1 : HALF];
     int j = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
@@ -638,6 +643,9 @@ struct Plan {
 };
 
 constexpr size_t kSmemBudget = 227 * 1024;  // the per-CTA maximum
+// Partial mode leaves 32 KB of the SM's shared memory free, so that with PDL
+// the next kernel's (small) CTAs can start beside the GEMM's.
+constexpr size_t kSmemBudgetPartial = kSmemBudget - 32 * 1024;
 // At most this many rows, partial mode is taken whenever 128-column tiles
 // leave an SM idle (measured on GB300, 12288 x 2048 weights: M = 1 and 64 ran
 // 14.5 and 16.6 us as partials, 17.2 and 18.2 us folded in 96 CTAs; at M = 128
@@ -713,9 +721,9 @@ Plan plan_bf16(const biv_gemm_desc& d) {
   // partial mode: more than one chunk, tiles of at most 128 columns
   p.partial = partial && p.chunks > 1 && p.bn <= 128;
   const int a_stage = p.m_box * 128, b_stage = p.bn * 128;
-  const size_t fixed = 1024 + size_t(128 - p.m_box) * 128 + (2 * kMaxStages + 4) * 8 + 16 +
-                       kStagingBytes;
-  p.stages = int(std::min<size_t>(kMaxStages, (kSmemBudget - fixed) / (a_stage + b_stage)));
+  const size_t fixed = GemmSmem<128>::bytes(0, p.m_box, !p.partial);
+  const size_t budget = p.partial ? kSmemBudgetPartial : kSmemBudget;
+  p.stages = int(std::min<size_t>(kMaxStages, (budget - fixed) / (a_stage + b_stage)));
   p.ldp = int64_t((d.N + p.bn - 1) / p.bn) * p.bn;
   if (p.partial) p.ws_bytes = size_t(p.chunks) * d.M * p.ldp * sizeof(float);
   return p;
@@ -724,13 +732,16 @@ Plan plan_bf16(const biv_gemm_desc& d) {
 template <int BN, bool F32OUT>
 biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_gemm_desc& d,
                        const Plan& pl, void* ws, cudaStream_t s) {
-  auto kern = gemm_bf16_kernel<BN, F32OUT>;
-  static bool attr = false;
-  if (!attr) {
+  // partial mode writes FP32 partials whatever C's type: one instantiation
+  constexpr bool kPartialOk = BN <= 128;
+  auto kern = (kPartialOk && pl.partial) ? gemm_bf16_kernel<BN, false, kPartialOk>
+                                         : gemm_bf16_kernel<BN, F32OUT, false>;
+  static bool attr[2] = {false, false};
+  if (!attr[pl.partial]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kSmemBudget)) != cudaSuccess)
       return set_error(BIV_ERR_CUDA, "gemm: cannot set shared memory size");
-    attr = true;
+    attr[pl.partial] = true;
   }
   const int eb = F32OUT ? 4 : 2;
   GemmArgs a;
@@ -751,7 +762,7 @@ biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_g
   const int64_t items = pl.partial ? pl.tiles * pl.chunks : pl.tiles;
   const int sms = sm_count() > 0 ? sm_count() : 148;
   const int grid = int(std::min<int64_t>(items, sms));
-  const size_t smem = GemmSmem<BN>::bytes(pl.stages, pl.m_box);
+  const size_t smem = GemmSmem<BN>::bytes(pl.stages, pl.m_box, !pl.partial);
   launch_pdl(kern, grid, kGemmThreads, smem, s, ta, tb, a);
   biv_status st = check_launch("gemm_bf16");
   if (st != BIV_OK || !pl.partial || d.defer_fold) return st;
