@@ -90,6 +90,24 @@ __device__ __forceinline__ void fold8(const biv_partials& xp, int64_t row, int c
   for (int j = 0; j < 8; ++j) f[j] = bf2f(f2bf(t[j]));
 }
 
+// 4 consecutive columns of one row folded like fold8.
+__device__ __forceinline__ void fold4(const biv_partials& xp, int64_t row, int col, float (&f)[4]) {
+  const float* src = xp.p + row * xp.ld + col;
+  float4 a[kMaxPartialChunks];
+#pragma unroll
+  for (int c = 0; c < kMaxPartialChunks; ++c)
+    if (c < xp.chunks) a[c] = __ldcg(reinterpret_cast<const float4*>(src + c * xp.chunk_stride));
+  float t[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
+#pragma unroll
+  for (int c = 1; c < kMaxPartialChunks; ++c) {
+    if (c < xp.chunks) {
+      t[0] = t[0] + a[c].x; t[1] = t[1] + a[c].y; t[2] = t[2] + a[c].z; t[3] = t[3] + a[c].w;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) f[j] = bf2f(f2bf(t[j]));
+}
+
 template <int CPT, bool PARTIAL>  // chunks per thread (ceil(d/8/256)); x as partials
 __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
     const uint16_t* __restrict__ x, int64_t xs, const biv_partials xp, uint16_t* __restrict__ r,
@@ -146,10 +164,8 @@ __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
 }
 
 // ------------------------------------------------------------- SiLU-mul ----
-// gate_up given as bf16 rows, or (gp.chunks > 0) as the chunk partials of the
-// GEMM that produced it, folded here to the same bf16 values
-template <bool PARTIAL>
-__global__ void silu_mul_kernel(const uint16_t* __restrict__ gu, int64_t gs, const biv_partials gp,
+// gate_up given as bf16 rows: one thread per 8 columns.
+__global__ void silu_mul_kernel(const uint16_t* __restrict__ gu, int64_t gs,
                                 uint16_t* __restrict__ y, int64_t ys, int rows, int I) {
   pdl_wait();     // stream predecessor done, its writes visible
   pdl_trigger();
@@ -158,18 +174,35 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ gu, int64_t gs, con
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
        i += int64_t(gridDim.x) * blockDim.x) {
     const int row = int(i / cpr), c = int(i % cpr);
+    const uint4* g = reinterpret_cast<const uint4*>(gu + int64_t(row) * gs);
     float gv[8], uv[8], o[8];
-    if (PARTIAL) {
-      fold8(gp, row, c * 8, gv);
-      fold8(gp, row, I + c * 8, uv);
-    } else {
-      const uint4* g = reinterpret_cast<const uint4*>(gu + int64_t(row) * gs);
-      unpack8(g[c], gv);
-      unpack8(g[cpr + c], uv);
-    }
+    unpack8(g[c], gv);
+    unpack8(g[cpr + c], uv);
 #pragma unroll
     for (int j = 0; j < 8; ++j) o[j] = (gv[j] / (1.0f + expf(-gv[j]))) * uv[j];
     reinterpret_cast<uint4*>(y + int64_t(row) * ys)[c] = pack8(o);
+  }
+}
+
+// gate_up given as the chunk partials of the GEMM that produced it, folded
+// here to the same bf16 values: one thread per 4 columns (the chunk loads of
+// both halves stay in registers)
+__global__ void silu_mul_partials_kernel(const biv_partials gp, uint16_t* __restrict__ y,
+                                         int64_t ys, int rows, int I) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
+  const int cpr = I / 4;
+  const int64_t total = int64_t(rows) * cpr;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int row = int(i / cpr), c = int(i % cpr);
+    float gv[4], uv[4], o[4];
+    fold4(gp, row, c * 4, gv);
+    fold4(gp, row, I + c * 4, uv);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = (gv[j] / (1.0f + expf(-gv[j]))) * uv[j];
+    reinterpret_cast<uint2*>(y + int64_t(row) * ys)[c] = make_uint2(pack_bf2(o[0], o[1]),
+                                                                     pack_bf2(o[2], o[3]));
   }
 }
 
@@ -818,9 +851,8 @@ biv_status biv_silu_mul(const uint16_t* gu, int64_t gs, uint16_t* y, int64_t ys,
   if (rows == 0) return BIV_OK;
   BIV_REQUIRE(row_ok(gu, gs, 2) && row_ok(y, ys, 2), "silu_mul: misaligned rows");
   const int64_t work = int64_t(rows) * (I / 8);
-  const biv_partials none = {nullptr, 0, 0, 0};
-  launch_pdl(silu_mul_kernel<false>, grid_for(work, 256), 256, 0, as_cuda(stream), gu, gs, none, y,
-             ys, rows, I);
+  launch_pdl(silu_mul_kernel, grid_for(work, 256), 256, 0, as_cuda(stream), gu, gs, y, ys, rows,
+             I);
   return check_launch("silu_mul");
 }
 
@@ -833,11 +865,9 @@ biv_status biv_silu_mul_partials(const biv_partials* gu, uint16_t* y, int64_t ys
               "silu_mul_partials: bad partials");
   if (rows == 0) return BIV_OK;
   BIV_REQUIRE(row_ok(y, ys, 2), "silu_mul: misaligned rows");
-  const int64_t work = int64_t(rows) * (I / 8);
-  // 128-thread CTAs: the partials variant keeps every chunk's loads in
-  // registers (about 170 per thread), so smaller CTAs spread over more SMs
-  launch_pdl(silu_mul_kernel<true>, grid_for(work, 128), 128, 0, as_cuda(stream), nullptr,
-             int64_t(0), *gu, y, ys, rows, I);
+  const int64_t work = int64_t(rows) * (I / 4);
+  launch_pdl(silu_mul_partials_kernel, grid_for(work, 256), 256, 0, as_cuda(stream), *gu, y, ys,
+             rows, I);
   return check_launch("silu_mul");
 }
 
