@@ -58,3 +58,55 @@ def test_host_validation_without_gpu(lib_path):
     assert st == biv.BIV_ERR_INVALID
     # zero-sized work is a no-op
     assert lib.biv_silu_mul(None, 0, None, 0, 0, 8, None) == biv.BIV_OK
+
+
+def _gemm_plan(lib, biv, M, N, K):
+    """Workspace bytes and partials layout the planner picks (host only)."""
+    import ctypes as C
+    d = biv.GemmDesc()
+    d.M, d.N, d.K = M, N, K
+    d.a_dtype = d.b_dtype = d.c_dtype = biv.BF16
+    d.lda, d.ldb, d.ldc = K, K, N
+    d.A, d.B, d.C = 0x100000, 0x200000, 0x300000   # never dereferenced: no launch here
+    n = C.c_size_t(0)
+    assert lib.biv_gemm_workspace(C.byref(d), C.byref(n)) == biv.BIV_OK, lib.biv_last_error()
+    p = biv.Partials()
+    ws = C.c_void_p(0x1000) if n.value else None
+    assert lib.biv_gemm_partials(C.byref(d), ws, C.byref(p)) == biv.BIV_OK, lib.biv_last_error()
+    return n.value, p
+
+
+def test_gemm_plan_on_host(lib_path):
+    """The K-chunk schedule depends on K alone (max(8, ceil(KB/8)) blocks of
+    64 per chunk); few-row calls leave their chunks to a fold across CTAs,
+    and the workspace holds exactly chunks x M x ldp FP32 partials."""
+    from invariant_forward_bitwise_gb300 import biv
+    lib = biv.load(lib_path)
+    for M in (1, 16, 64):
+        for N, K, chunks in ((12288, 2048, 4), (2048, 6144, 8), (4096, 2048, 4), (2048, 2048, 4)):
+            n, p = _gemm_plan(lib, biv, M, N, K)
+            ldp = (N + 127) // 128 * 128
+            assert (p.chunks, p.ld, p.chunk_stride) == (chunks, ldp, M * ldp), (M, N, K)
+            assert n == chunks * M * ldp * 4
+    # one chunk (K <= 512): nothing to fold across CTAs
+    assert _gemm_plan(lib, biv, 1, 4096, 512)[0] == 0
+    # prefill-sized calls fold inside the CTA: no workspace
+    for N, K in ((12288, 2048), (2048, 6144), (151936, 2048)):
+        n, p = _gemm_plan(lib, biv, 16384, N, K)
+        assert n == 0 and p.chunks == 0
+
+
+def test_partials_consumers_reject_bad_layouts(lib_path):
+    """The ops that fold GEMM partials check the layout on the host."""
+    import ctypes as C
+    from invariant_forward_bitwise_gb300 import biv
+    lib = biv.load(lib_path)
+    bad = [biv.Partials(0x1000, 9, 2048, 64 * 2048),      # more than 8 chunks
+           biv.Partials(0x1004, 4, 2048, 64 * 2048),      # base not 16-byte aligned
+           biv.Partials(0x1000, 4, 2047, 64 * 2047)]      # row pitch not a multiple of 4
+    for p in bad:
+        st = lib.biv_add_rmsnorm_partials(C.byref(p), None, 0, C.c_void_p(0x2000), C.c_void_p(0x3000),
+                                          2048, 4, 2048, C.c_float(1e-6), None)
+        assert st == biv.BIV_ERR_INVALID
+        st = lib.biv_silu_mul_partials(C.byref(p), C.c_void_p(0x3000), 1024, 4, 1024, None)
+        assert st == biv.BIV_ERR_INVALID
