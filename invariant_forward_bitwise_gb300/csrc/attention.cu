@@ -115,8 +115,9 @@ __device__ __forceinline__ int row_splits(const AttnArgs& a, int pos) {
   return a.topk_idx ? (a.topk + a.kv_split - 1) / a.kv_split : pos / a.kv_split + 1;
 }
 
-template <int D, int NW, int ST, bool TMA, int DS>
-__global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ AttnArgs a) {
+// MINB: CTAs per SM the register allocation must allow (0: no bound)
+template <int D, int NW, int ST, bool TMA, int DS, int MINB>
+__global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_constant__ AttnArgs a) {
   pdl_wait();     // stream predecessor done, its writes visible
   pdl_trigger();
   using Cfg = AttnCfg<D, NW, ST, TMA, DS>;
@@ -561,18 +562,18 @@ size_t ws_bytes(const biv_attn_desc& d, int split) {
   return size_t(d.T) * d.Hq * ns * (d.D + 2) * sizeof(float);
 }
 
-template <int D, int NW, int ST, bool TMA, int DS = 1>
+template <int D, int NW, int ST, bool TMA, int DS = 1, int MINB = 0>
 biv_status launch_cfg(const biv_attn_desc& d, const AttnArgs& a, cudaStream_t s) {
   using Cfg = AttnCfg<D, NW, ST, TMA, DS>;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attn_kernel<D, NW, ST, TMA, DS>,
+    if (cudaFuncSetAttribute(attn_kernel<D, NW, ST, TMA, DS, MINB>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
       return set_error(BIV_ERR_CUDA, "attention: cannot set shared memory size");
     attr = true;
   }
   dim3 grid(d.nqblocks, d.Hkv, a.nsplit_grid);
-  launch_pdl(attn_kernel<D, NW, ST, TMA, DS>, grid, Cfg::NT, Cfg::SMEM, s, a);
+  launch_pdl(attn_kernel<D, NW, ST, TMA, DS, MINB>, grid, Cfg::NT, Cfg::SMEM, s, a);
   return check_launch("attention");
 }
 
@@ -638,7 +639,13 @@ biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
           make_kv_map(&a.tmV, d.v_cache, d.num_pages, d.Hkv, D);
     if (tma) {
       if (!small) {
-        st = launch_cfg<D, 4, 2, true>(d, a, s);
+        // Prefill CTAs: one TMA stage and registers capped for three CTAs
+        // per SM (measured on GB300, 8 sequences x 1024 tokens: 223 us,
+        // against 265 us for two stages at two CTAs per SM and 273 us for
+        // one stage at two).  BIV_ATTN_PREFILL_STAGES=2 selects the two-stage
+        // CTA (tests and tuning; no bit changes).
+        st = env_int("BIV_ATTN_PREFILL_STAGES", 2, 2) ? launch_cfg<D, 4, 2, true>(d, a, s)
+                                                      : launch_cfg<D, 4, 1, true, 1, 3>(d, a, s);
       } else {
         const int64_t ctas = int64_t(d.nqblocks) * d.Hkv * a.nsplit_grid;
         const int stages = decode_stages(ctas);

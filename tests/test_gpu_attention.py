@@ -161,6 +161,21 @@ def test_prefill_parity_and_decode_invariance(B, D, Hq, Hkv, fp8, split):
     assert np.array_equal(bits(out2), bits(out))
 
 
+def test_prefill_cta_shape_changes_no_bit(B, monkeypatch):
+    """The two-stage prefill CTA gives the bits of the default one-stage CTA."""
+    g = synth.rng(77)
+    lens = [300, 129]
+    Hq, Hkv, D = 16, 8, 128
+    pc = Paged(B, g, lens, Hkv, D, False)
+    rows = [(i, p) for i, L in enumerate(lens) for p in range(L)]
+    q = synth.normal_bf16(g, (len(rows), Hq * D)).cuda()
+    blocks = blocks_of(rows, 64 // (Hq // Hkv))
+    out1 = run_attn(B, pc, q, rows, blocks, Hq)
+    monkeypatch.setenv("BIV_ATTN_PREFILL_STAGES", "2")
+    out2 = run_attn(B, pc, q, rows, blocks, Hq)
+    assert np.array_equal(bits(out1), bits(out2))
+
+
 def test_fast_mode_close_not_required_equal(B):
     g = synth.rng(3)
     lens = [2000, 900]
