@@ -283,12 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t key[kPer];
     uint32_t cnt = 0, mn = 0xffffffffu, mx = 0;
-  #pragma unroll
+#pragma unroll
     for (int r = 0; r < kRounds; ++r) {
       const int j0 = r * kRoundSpan + 4 * tid;
       const float4 f = rowbuf4[j0 / 4];
       const float v[4] = {f.x, f.y, f.z, f.w};
-  #pragma unroll
+#pragma unroll
       for (int e = 0; e < 4; ++e) {
         const uint32_t kk = (j0 + e < nv && v[e] != -INFINITY) ? order_key(v[e]) : 0u;
         key[4 * r + e] = kk;
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t sel = 0;  // bit q: key slot q chosen
     if (total_valid <= uint32_t(k)) {
-  #pragma unroll
+#pragma unroll
       for (int q = 0; q < kPer; ++q) sel |= uint32_t(key[q] != 0) << q;
     } else {
       if (!range_done(g)) refine_regs(g, key, hist, wsum, s_sel);
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         // keys above the bin are chosen whatever the later rounds decide
         const uint32_t lo1 = g.lo, span1 = g.hi - g.lo;
-  #pragma unroll
+#pragma unroll
         for (int q = 0; q < kPer; ++q) {
           const uint32_t d = key[q] - lo1;
           if (d <= span1) {
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // more than 1024 keys share the bin: refine over the registers
         while (!range_done(g)) refine_regs(g, key, hist, wsum, s_sel);
         uint32_t eq = 0;
-  #pragma unroll
+#pragma unroll
         for (int q = 0; q < kPer; ++q) {
           sel |= uint32_t(key[q] > g.hi) << q;
           eq |= uint32_t(key[q] >= g.lo && key[q] <= g.hi) << q;
@@ -369,10 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {  // one key value: its lowest `rem` positions
           uint32_t lane_pre[kRounds];
           ordered_slots(eq, hist, wsum, lane_pre);
-  #pragma unroll
+#pragma unroll
           for (int r = 0; r < kRounds; ++r) {
             uint32_t rank = hist[r * kWarps + warp] + lane_pre[r];
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int q = 4 * r + e;
               if ((eq >> q) & 1u) {
@@ -389,12 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t lane_pre[kRounds];
     const uint32_t total_sel = ordered_slots(sel, hist, wsum, lane_pre);
     int32_t* out = idx + int64_t(row) * k;
-  #pragma unroll
+#pragma unroll
     for (int r = 0; r < kRounds; ++r) {
       const uint32_t nib = (sel >> (4 * r)) & 15u;
       if (nib) {
         uint32_t slot = hist[r * kWarps + warp] + lane_pre[r];
-  #pragma unroll
+#pragma unroll
         for (int e = 0; e < 4; ++e)
           if ((nib >> e) & 1u) out[slot++] = r * kRoundSpan + 4 * tid + e;
       }
