@@ -108,7 +108,10 @@ biv_status biv_add_rmsnorm(const uint16_t* x, int64_t x_stride, uint16_t* residu
 /* The same, with x given as the chunk partials of the GEMM that produced it
  * (biv_gemm with defer_fold): x = the GEMM's rounded output, formed here
  * instead of by the GEMM's fold kernel, so the result is the same bit for
- * bit and one launch and one round trip of x are saved. */
+ * bit and one launch and one round trip of x are saved.  The partials stay
+ * the caller's (the GEMM workspace) and are only read.  BIV_ERR_INVALID on
+ * x NULL or chunks outside 1..8, a partial base not 16-byte aligned, or
+ * ld / chunk_stride not multiples of 4. */
 biv_status biv_add_rmsnorm_partials(const biv_partials* x, uint16_t* residual, int64_t r_stride,
                                     const uint16_t* w, uint16_t* y, int64_t y_stride, int rows,
                                     int d, float eps, biv_stream_t stream);
@@ -123,8 +126,8 @@ biv_status biv_silu_mul(const uint16_t* gate_up, int64_t gu_stride, uint16_t* y,
 /* The same, with gate_up given as the chunk partials of the GEMM that
  * produced it (biv_gemm with defer_fold; partial columns [0, I) are g and
  * [I, 2I) are u): folded here to the GEMM's bf16 output, so y is the same bit
- * for bit.  BIV_ERR_ARG on chunks outside 1..8, a partial base not 16-byte
- * aligned, or ld / chunk_stride not multiples of 4 or ld < 2I. */
+ * for bit.  BIV_ERR_INVALID on chunks outside 1..8, a partial base not
+ * 16-byte aligned, or ld / chunk_stride not multiples of 4 or ld < 2I. */
 biv_status biv_silu_mul_partials(const biv_partials* gate_up, uint16_t* y, int64_t y_stride,
                                  int rows, int I, biv_stream_t stream);
 
@@ -173,7 +176,10 @@ biv_status biv_kv_fp8_quant(const uint16_t* k, const uint16_t* v, int64_t row_st
  * defer_fold) and written to qkv; otherwise qkv holds it already.  After the
  * call qkv holds roped q and k and the plain v; k/v of rows with slot >= 0
  * are in the cache (bf16 [slots, Hkv, D], or e4m3 codes with per-(token,
- * head) scales). */
+ * head) scales).  Sizes and the error behaviour are those of the separate
+ * ops (D in {64, 80, 128}; an out-of-range position is reported through
+ * biv_poll_error and read as 0); BIV_ERR_INVALID also on partials with
+ * more than 8 chunks. */
 biv_status biv_qkv_finalize(uint16_t* qkv, int64_t row_stride, const biv_partials* qkv_partials,
                             int T, int Hq, int Hkv, int D, const uint16_t* q_w, const uint16_t* k_w,
                             const float* cos_sin, int max_pos, const int32_t* pos, float eps,
