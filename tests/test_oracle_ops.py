@@ -169,6 +169,24 @@ def test_topk_positions_brute_force_with_ties():
             assert got[r].tolist() == _brute_topk(s[r], nv[r], k), (n, k, r)
 
 
+def test_topk_positions_brute_force_extreme_values():
+    """The oracle's selection on +inf, +-max normals, denormals, signed zeros
+    and adjacent floats equals a plain sort by (score desc, position asc)."""
+    g = np.random.default_rng(12)
+    n, k = 200, 37
+    rows = [np.float32(3.4e38) * np.sign(g.standard_normal(n)).astype(F32),
+            (np.float32(1e-40) * g.integers(-3, 4, n)).astype(F32),
+            (np.float32(1.0) + np.float32(2.0 ** -23) * g.integers(0, 9, n)).astype(F32),
+            np.ldexp(np.float32(1.0), g.integers(-126, 127, n)).astype(F32),
+            np.where(g.random(n) < 0.5, F32(0.0), F32(-0.0)).astype(F32)]
+    rows[0][::7] = np.inf
+    s = np.stack(rows)
+    nv = np.array([n, n, 150, n, n])
+    got = ops.topk_positions(s, nv, k)
+    for r in range(s.shape[0]):
+        assert got[r].tolist() == _brute_topk(s[r], nv[r], k), r
+
+
 def test_router_brute_force_and_softmax_weights():
     g = np.random.default_rng(11)
     z = g.integers(-2, 3, size=(16, 64)).astype(F32) * F32(0.5)
