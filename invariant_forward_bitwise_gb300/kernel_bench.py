@@ -14,6 +14,15 @@ eager step runs inside cudaProfilerStart/Stop for an ncu launch list).
 Each case times REPS calls with CUDA events after one warm-up call and
 prints the time and the rate against the case's algorithmic bytes or FLOPs;
 it is also the command that the ncu summaries in profiles/ capture.
+
+Further cases: gemm_sweep (the decoder GEMMs over decode batch sizes, weights
+rotated through copies larger than L2; BIV_BENCH_MS lists the M values,
+BIV_BENCH_SHAPES the GEMMs, BIV_BENCH_DEFER=1 times the GEMM kernel alone
+when it leaves chunk partials to the consumer op) and gemm_prefill_layer (the
+four GEMMs of a 16384-row prefill step; BIV_BENCH_MODE=fast runs the
+batch-dependent comparator).  The library's own tuning switches
+(BIV_GEMM_TILE_N, BIV_GEMM_FOLD, BIV_ATTN_DECODE_STAGES,
+BIV_ATTN_DECODE_DSPLIT, BIV_ATTN_PREFILL_STAGES, BIV_PDL) apply here too.
 """
 import math
 import os
