@@ -10,6 +10,7 @@ namespace {
 
 constexpr int kNormThreads = 256;  // fixed: the RMSNorm tree depends on d only
 constexpr int kLogprobThreads = 512;
+constexpr int kLogprobAhead = 8;  // logit chunks a thread loads before using them
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -580,8 +581,7 @@ __global__ void __launch_bounds__(kLogprobThreads) logprob_kernel(
   const float4* zr = reinterpret_cast<const float4*>(z + int64_t(row) * ld);
   const int chunks = V / 4;
   float m = -INFINITY, s = 0.f;
-  for (int c = threadIdx.x; c < chunks; c += kLogprobThreads) {
-    const float4 q = __ldcs(zr + c);
+  auto update = [&](const float4& q) {
     const float cm = fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w));
     if (cm > m) {
       s = (m == -INFINITY) ? 0.f : s * expf(m - cm);
@@ -591,6 +591,18 @@ __global__ void __launch_bounds__(kLogprobThreads) logprob_kernel(
     s += expf(q.y - m);
     s += expf(q.z - m);
     s += expf(q.w - m);
+  };
+  // the thread's chunks c, c + T, c + 2T, ... in that order; the loads of
+  // kLogprobAhead of them are issued before the first update
+  constexpr int kStep = kLogprobThreads * kLogprobAhead;
+  for (int c0 = threadIdx.x; c0 < chunks; c0 += kStep) {
+    float4 q[kLogprobAhead];
+#pragma unroll
+    for (int u = 0; u < kLogprobAhead; ++u)
+      if (c0 + u * kLogprobThreads < chunks) q[u] = __ldcs(zr + c0 + u * kLogprobThreads);
+#pragma unroll
+    for (int u = 0; u < kLogprobAhead; ++u)
+      if (c0 + u * kLogprobThreads < chunks) update(q[u]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
