@@ -1,0 +1,66 @@
+"""Host-side scheduling logic of the model harness (no GPU): query blocks,
+prefill rows and the decode-graph batch buckets."""
+import types
+
+import numpy as np
+import pytest
+
+import synth
+
+
+@pytest.fixture(scope="module")
+def model_mod():
+    from invariant_forward_bitwise_gb300 import model
+    return model
+
+
+def test_qblocks_cover_rows_in_order_within_one_sequence(model_mod):
+    g = np.random.default_rng(3)
+    row_seq = np.repeat(np.arange(7, dtype=np.int32), g.integers(1, 90, size=7))
+    for per in (1, 8, 32, 64):
+        qb = model_mod.qblocks_for(row_seq, per)
+        # consecutive, gap-free cover of every row, in order
+        assert qb[0, 0] == 0 and int(qb[-1].sum()) == row_seq.size
+        assert np.array_equal(qb[1:, 0], qb[:-1, 0] + qb[:-1, 1])
+        for r0, n in qb:
+            assert 1 <= n <= per
+            assert np.all(row_seq[r0:r0 + n] == row_seq[r0])   # one sequence per block
+        # a block ends early only at a sequence boundary
+        for (r0, n), (r1, _) in zip(qb[:-1], qb[1:]):
+            if n < per:
+                assert row_seq[r1] != row_seq[r0]
+
+
+def test_prefill_rows_emit_the_logprob_of_the_next_token(model_mod):
+    cfg = synth.TINY
+    seqs = synth.tiny_sequences(cfg, n=3, lo=10, hi=30, seed=4)
+    starts = [0, 3, 5]
+    ends = [s.length for s in seqs]
+    lm_from = [s.prompt_len - 1 for s in seqs]
+    seq_slot, pos, ids, lm_rows, targets, owner = model_mod.prefill_rows(
+        seqs, [10, 11, 12], starts, ends, lm_from)
+    assert len(pos) == sum(e - b for b, e in zip(starts, ends))
+    at = 0
+    for i, s in enumerate(seqs):
+        for p in range(starts[i], ends[i]):
+            assert (seq_slot[at], pos[at], ids[at]) == (10 + i, p, int(s.tokens[p]))
+            at += 1
+    # every logprob row predicts token p + 1 of its own sequence, from lm_from on
+    want = [(i, p) for i, s in enumerate(seqs) for p in range(max(starts[i], lm_from[i]), ends[i])
+            if p + 1 < s.length]
+    assert owner == want
+    for r, t, (i, p) in zip(lm_rows, targets, owner):
+        assert pos[r] == p and t == int(seqs[i].tokens[p + 1])
+
+
+def test_decode_buckets(model_mod):
+    DG = model_mod.DecodeGraphs
+    b = list(DG.BUCKETS)
+    assert b == sorted(set(b)) and b[0] == 1
+    fake = types.SimpleNamespace(BUCKETS=DG.BUCKETS)
+    for n in range(1, b[-1] + 1):
+        k = DG.bucket(fake, n)
+        assert k >= n and k in b
+        assert k == min(x for x in b if x >= n)                 # the smallest that fits
+    with pytest.raises(ValueError):
+        DG.bucket(fake, b[-1] + 1)
