@@ -161,10 +161,16 @@ def expert_mlp_fp8(x, wgu_codes, wgu_scale, wd_codes, wd_scale):
     return ops.gemm_fp8_block(aq2, sa2, wd_codes, wd_scale)
 
 
-def moe_block(h, router_w, experts: List[tuple], shared: tuple, top_k: int):
+def moe_block(h, router_w, experts: List[tuple], shared: tuple, top_k: int, logits=None):
     """Router logits (FP32 GEMM), Top-k routing, each selected expert per token
-    row, the shared expert, FP32 fixed-slot combine."""
-    logits = ops.gemm(h, router_w, out="f32")
+    row, the shared expert, FP32 fixed-slot combine.
+
+    ``logits`` (optional, FP32 [T, E]) routes by given router logits instead
+    of computing them: a comparison with another implementation can then route
+    both sides identically, so that a near-tie that rounds the other way in
+    one of them does not decide which experts the float comparison covers."""
+    if logits is None:
+        logits = ops.gemm(h, router_w, out="f32")
     idx, w = ops.router_topk(logits, top_k)
     T, d = h.shape
     y = np.zeros((T, top_k, d), F32)

@@ -7,16 +7,54 @@ float32 scales.
 """
 from __future__ import annotations
 
+import contextlib
+
 import numpy as np
 
 from .codecs import bf16_round, e4m3_to_f32, f32_to_e4m3
 
 F32 = np.float32
 
+# How the oracle forms a dot product.  "f64" (the default): in float64, rounded
+# once to FP32, so the result does not depend on how a library blocks the sum.
+# "f32": plain FP32 in ascending k, every product and every partial sum
+# rounded to FP32 -- the textbook order.  Both are correct FP32 evaluations of
+# the same definition; the second exists to measure how far two correct
+# evaluations drift apart through a deep model (the spread script in this
+# package), which bounds what any implementation can promise against either.
+_ACCUMULATION = ["f64"]
+
+
+@contextlib.contextmanager
+def accumulation(kind: str):
+    """Run the enclosed oracle calls with dot products formed as ``kind``
+    ("f64" or "f32")."""
+    if kind not in ("f64", "f32"):
+        raise ValueError(kind)
+    prev = _ACCUMULATION[0]
+    _ACCUMULATION[0] = kind
+    try:
+        yield
+    finally:
+        _ACCUMULATION[0] = prev
+
+
+def _dot_f32_ascending(a: np.ndarray, bt: np.ndarray) -> np.ndarray:
+    """acc = 0; for k = 0, 1, ...: acc = fp32(acc + fp32(a[:, k] * bt[k, :]))."""
+    a = np.ascontiguousarray(np.asarray(a, F32).T)
+    bt = np.ascontiguousarray(bt, F32)
+    acc = np.zeros((a.shape[1], bt.shape[1]), F32)
+    for k in range(a.shape[0]):
+        acc += a[k][:, None] * bt[k][None, :]
+    return acc
+
 
 # ----------------------------------------------------------------- GEMM ----
 def dot_f32(a: np.ndarray, bt: np.ndarray) -> np.ndarray:
-    """a @ bt with float64 accumulation, rounded once to FP32."""
+    """a @ bt as FP32 values: float64 accumulation rounded once to FP32, or
+    (inside ``accumulation("f32")``) plain FP32 accumulation in ascending k."""
+    if _ACCUMULATION[0] == "f32":
+        return _dot_f32_ascending(a, bt)
     return np.matmul(np.asarray(a, np.float64), np.asarray(bt, np.float64)).astype(F32)
 
 
