@@ -6,9 +6,10 @@
 // KV split.  Its query vectors are (row, q-head-of-the-group) pairs, 16 per
 // warp.  Keys are visited in 64-token tiles aligned to absolute positions (one
 // cache page), inside splits of kv_split tokens.  Per vector and split:
-// online softmax in FP32 (exp2 domain), P split into a bf16 hi + lo pair for
-// P.V (two MMAs into one FP32 accumulator), the denominator summed from the
-// FP32 P.  Splits are merged in ascending order.  A vector's arithmetic is the
+// online softmax in FP32 (x = s * scale, p = exp(x - m), natural base), P
+// split into three bf16 parts hi + mid + lo that add up to the FP32 p exactly
+// (three MMAs into one FP32 accumulator, hi first), the denominator summed
+// from the FP32 p.  Splits are merged in ascending order.  A vector's arithmetic is the
 // same whatever other rows share its CTA and whatever the CTA shape: each warp
 // runs one instruction sequence for its 16 vectors, tiles past a vector's own
 // position are fully masked and leave (m, l, acc) bitwise unchanged, and
@@ -31,7 +32,6 @@ namespace {
 
 constexpr int kTile = 64;   // keys per tile = one page
 constexpr int kNV = 64;     // most query vectors a CTA takes (4 warps x 16)
-constexpr float kLog2e = 1.4426950408889634f;
 
 // NW warps per CTA, ST-stage K/V pipeline, TMA or thread-issued loads, and
 // DS: 1 = each warp owns 16 query vectors (prefill blocks); DS = NW = every
@@ -46,7 +46,7 @@ struct AttnCfg {
   static constexpr int NT = NW * 32;                 // threads per CTA
   static constexpr int KVB = TMA ? kTile * D * 2 : kTile * LD * 2;  // one K or V stage
   static constexpr int Q_BYTES = NV * LD * 2;
-  static constexpr int SMEM = 1024 + 2 * ST * KVB + Q_BYTES + ST * kTile * 4 + ST * 8;
+  static constexpr int SMEM = 1024 + 2 * ST * KVB + Q_BYTES + ST * kTile * 4 + 2 * ST * 8;
   static constexpr int DK = D / 16;                  // k-steps of Q.K^T
   static constexpr int DT = D / 8;                   // n-tiles of O
   static constexpr int DTW = DT / DS;                // n-tiles of O per warp
@@ -60,6 +60,21 @@ struct AttnCfg {
     return uint32_t((row * LD + dim) * 2);
   }
 };
+
+// two FP32 values as packed bf16 pairs hi, mid, lo with hi + mid + lo equal to
+// each value exactly (x0 in the low halves): hi = bf16(x), mid = bf16(x - hi),
+// lo = bf16(x - hi - mid); both differences are exact in FP32
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo_half, float hi_half) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo_half, hi_half);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ void split3(float x0, float x1, uint32_t& hi, uint32_t& mid,
+                                       uint32_t& lo) {
+  hi = cvt_bf16x2(x0, x1);
+  const float r0 = x0 - __uint_as_float(hi << 16), r1 = x1 - __uint_as_float(hi & 0xFFFF0000u);
+  mid = cvt_bf16x2(r0, r1);
+  lo = cvt_bf16x2(r0 - __uint_as_float(mid << 16), r1 - __uint_as_float(mid & 0xFFFF0000u));
+}
 
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -105,7 +120,7 @@ struct AttnArgs {
   const int32_t* bt; int max_pages;
   int kv_split;
   const int32_t* topk_idx; int64_t topk_stride; int topk;
-  float scale_log2;
+  float scale;
   float* ws_o; float* ws_ml; int nsplit_grid;
   int* err;
 };
@@ -113,6 +128,16 @@ struct AttnArgs {
 // Number of splits that hold keys of a row (fixed per row).
 __device__ __forceinline__ int row_splits(const AttnArgs& a, int pos) {
   return a.topk_idx ? (a.topk + a.kv_split - 1) / a.kv_split : pos / a.kv_split + 1;
+}
+
+// A dense row's position must lie inside the grid's splits (position + 1 <=
+// max_ctx rounded up to whole splits) and inside its block-table row.  A row
+// outside either bound raises kErrBadIndex, has its output set to NaN and
+// takes no part in the loads, the partials or the merge.
+__device__ __forceinline__ bool row_pos_ok(const AttnArgs& a, int pos) {
+  if (pos < 0) return false;
+  if (a.topk_idx) return true;
+  return pos < a.nsplit_grid * a.kv_split && pos < a.max_pages * kTile;
 }
 
 // MINB: CTAs per SM the register allocation must allow (0: no bound)
@@ -130,7 +155,9 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
   uint8_t* sV = base + ST * KVB;
   uint16_t* sQ = reinterpret_cast<uint16_t*>(base + 2 * ST * KVB);
   int32_t* sPos = reinterpret_cast<int32_t*>(base + 2 * ST * KVB + Cfg::Q_BYTES);  // [ST][64]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sPos + ST * kTile);                 // [ST]
+  // TMA: K of stage s completes on bars[s], V on bars[ST + s], so that K of
+  // the next tile streams in while this tile's softmax and P.V run
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sPos + ST * kTile);                 // [2 ST]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int blk = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
@@ -139,9 +166,19 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
   const int seq = a.row_seq[r0];
   const bool sparse = a.topk_idx != nullptr;
 
-  // block's largest position (rows of a block are one sequence)
+  // block's largest position (rows of a block are one sequence); rows whose
+  // position is out of bounds are reported and left out
   int maxpos = -1;
-  for (int r = 0; r < nr; ++r) maxpos = max(maxpos, a.row_pos[r0 + r]);
+  for (int r = 0; r < nr; ++r) {
+    const int p = a.row_pos[r0 + r];
+    if (row_pos_ok(a, p)) {
+      maxpos = max(maxpos, p);
+    } else if (split == 0) {
+      if (tid == 0) raise_error(a.err, kErrBadIndex);
+      uint16_t* dst = a.out + int64_t(r0 + r) * a.out_stride + int64_t(h * a.G) * D;
+      for (int i = tid; i < a.G * D; i += NT) dst[i] = 0x7FC0;  // bf16 NaN
+    }
+  }
 
   // key range of this split: [lo, hi) in positions (dense) or list indices (sparse)
   const int lo = split * a.kv_split;
@@ -150,7 +187,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
   const int ntiles = (hi - lo + kTile - 1) / kTile;
 
   if (TMA && tid == 0) {
-    for (int s = 0; s < ST; ++s) mbar_init(smem_u32(bars + s), 1);
+    for (int s = 0; s < 2 * ST; ++s) mbar_init(smem_u32(bars + s), 1);
     fence_barrier_init();
   }
 
@@ -171,20 +208,26 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
 
   // ---- tile loader (dense: the page of absolute tile t; sparse: listed keys)
   const int64_t kv_row = int64_t(a.Hkv) * D;  // elements between consecutive cache slots
+  // TMA: K (which = 0) or V (which = 1) of the page of absolute tile t, by
+  // thread 0, on that half's barrier of stage buf
+  auto load_half = [&](int buf, int t, int which) {
+    if (!TMA || tid != 0) return;
+    const int tbase = lo + t * kTile;
+    const uint32_t bar = smem_u32(bars + which * ST + buf);
+    const int page = a.bt[int64_t(seq) * a.max_pages + tbase / kTile];
+    uint8_t* dst = (which ? sV : sK) + buf * KVB;
+    fence_proxy_async();  // earlier generic accesses to this buffer come first
+    mbar_expect_tx(bar, KVB);
+#pragma unroll
+    for (int hh = 0; hh < D / 64; ++hh)
+      tma_load_2d(smem_u32(dst + hh * 8192), which ? &a.tmV : &a.tmK, bar, h * D + hh * 64,
+                  page * kTile);
+  };
   auto load_tile = [&](int buf, int t) {
     const int tbase = lo + t * kTile;
     if (TMA) {
-      if (tid == 0) {
-        const uint32_t bar = smem_u32(bars + buf);
-        const int page = a.bt[int64_t(seq) * a.max_pages + tbase / kTile];
-        fence_proxy_async();  // earlier generic accesses to this stage come first
-        mbar_expect_tx(bar, 2 * KVB);
-#pragma unroll
-        for (int hh = 0; hh < D / 64; ++hh) {
-          tma_load_2d(smem_u32(sK + buf * KVB + hh * 8192), &a.tmK, bar, h * D + hh * 64, page * kTile);
-          tma_load_2d(smem_u32(sV + buf * KVB + hh * 8192), &a.tmV, bar, h * D + hh * 64, page * kTile);
-        }
-      }
+      load_half(buf, t, 0);
+      load_half(buf, t, 1);
       return;
     }
     int32_t* pos_buf = sPos + buf * kTile;
@@ -193,6 +236,10 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
       if (sparse) {
         const int li = tbase + j;
         p = li < hi ? a.topk_idx[int64_t(r0) * a.topk_stride + li] : -1;
+        if (p >= a.max_pages * kTile) {   // a listed key outside the block table
+          raise_error(a.err, kErrBadIndex);
+          p = -1;
+        }
       } else {
         p = tbase + j;
         if (p >= hi) p = -1;
@@ -261,6 +308,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
   for (int i = 0; i < 2; ++i) {
     const int v = vw * 16 + g + 8 * i;
     vpos[i] = v < nv ? a.row_pos[r0 + v / a.G] : -1;
+    if (!row_pos_ok(a, vpos[i])) vpos[i] = -1;   // sees no key; output already NaN
   }
 
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
@@ -291,16 +339,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     const int buf = t % ST;
     const int tbase = lo + t * kTile;
     if (TMA) {
-      mbar_wait(smem_u32(bars + buf), (t / ST) & 1, a.err);
-      // slots past the split's end in its last page hold no key of this
-      // sequence: zero their V rows (P is 0 there, and 0 * stale must be 0)
-      const int first_bad = hi - tbase;
-      if (first_bad < kTile) {
-        for (int i = tid; i < (kTile - first_bad) * (D / 8); i += NT) {
-          const int j = first_bad + i / (D / 8), c = i % (D / 8);
-          *reinterpret_cast<uint4*>(sV + buf * KVB + Cfg::off(j, c * 8)) = make_uint4(0, 0, 0, 0);
-        }
-      }
+      mbar_wait(smem_u32(bars + buf), (t / ST) & 1, a.err);   // K of tile t
     } else {
       cp_async_wait<ST - 2>();  // tile t has landed
     }
@@ -310,10 +349,8 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
       if (t + ST - 1 < ntiles) load_tile((t + ST - 1) % ST, t + ST - 1);
       cp_async_commit();
     }
-    if (vw * 16 >= nv) {  // no live vector in this warp: only help with loads
-      __syncthreads();
-      continue;
-    }
+    // a warp with no live vector only takes part in the loads and barriers
+    const bool live = vw * 16 < nv;
     const uint32_t tK = smem_u32(sK + buf * KVB);
     const uint32_t tV = smem_u32(sV + buf * KVB);
     const int32_t* tP = sPos + buf * kTile;
@@ -322,6 +359,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     float s[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+    if (live) {
     // per k-step: all fragment loads first, then the MMAs (independent
     // accumulators back to back; each accumulator still sees ascending k)
 #pragma unroll
@@ -339,6 +377,12 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
         mma_bf16(s[2 * np + 1], qf[kk], kf[np][2], kf[np][3]);
       }
     }
+    }  // live
+    if (TMA) {
+      __syncthreads();                                  // every warp is done with K of tile t
+      if (t + ST < ntiles) load_half(buf, t + ST, 0);   // its buffer takes K of tile t+ST
+    }
+    if (live) {
     // mask, online softmax.  A dense tile that every live row of the warp sees
     // whole needs no per-element test (the result is the same either way).
     float mx[2] = {-INFINITY, -INFINITY};
@@ -351,7 +395,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = e >> 1;
-          const float x = vpos[i] >= 0 ? s[nt][e] * a.scale_log2 : -INFINITY;
+          const float x = vpos[i] >= 0 ? s[nt][e] * a.scale : -INFINITY;
           s[nt][e] = x;
           mx[i] = fmaxf(mx[i], x);
         }
@@ -365,7 +409,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
           const int col = nt * 8 + 2 * cq + (e & 1);
           const int kp = sparse ? tP[col] : (tbase + col < hi ? tbase + col : -1);
           const bool vis = kp >= 0 && kp <= vpos[i];
-          const float x = vis ? s[nt][e] * a.scale_log2 : -INFINITY;
+          const float x = vis ? s[nt][e] * a.scale : -INFINITY;
           s[nt][e] = x;
           mx[i] = fmaxf(mx[i], x);
         }
@@ -377,30 +421,20 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
       mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
       mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
       const float mn = fmaxf(m[i], mx[i]);
-      alpha[i] = (mn == -INFINITY) ? 1.f : exp2f(m[i] - mn);
+      alpha[i] = (mn == -INFINITY) ? 1.f : expf(m[i] - mn);
       m[i] = mn;
     }
-    // P as two bf16 A fragments per k-step: P = hi + lo, hi = bf16(p),
-    // lo = bf16(p - hi), so P.V carries ~16 significant bits of p while V stays
-    // exact bf16.  The denominator sums the FP32 p.
-    uint32_t pf[4][4], pl[4][4];
+    // p = exp(x - m) in FP32, kept in s; the denominator sums these FP32 p
     float rs[2] = {0.f, 0.f};
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      float ph[4], plo[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = e >> 1;
-        const float pe = (m[i] == -INFINITY) ? 0.f : exp2f(s[nt][e] - m[i]);
-        ph[e] = bf2f(f2bf(pe));
-        plo[e] = pe - ph[e];
+        const float pe = (m[i] == -INFINITY) ? 0.f : expf(s[nt][e] - m[i]);
+        s[nt][e] = pe;
         rs[i] += pe;
       }
-      const int ks = nt >> 1, hi2 = nt & 1;
-      pf[ks][hi2 * 2 + 0] = pack_bf2(ph[0], ph[1]);
-      pf[ks][hi2 * 2 + 1] = pack_bf2(ph[2], ph[3]);
-      pl[ks][hi2 * 2 + 0] = pack_bf2(plo[0], plo[1]);
-      pl[ks][hi2 * 2 + 1] = pack_bf2(plo[2], plo[3]);
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -418,14 +452,40 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
         acc[dt][3] *= alpha[1];
       }
     }
-    // O += P . V
+    }  // live
+    if (TMA) {
+      mbar_wait(smem_u32(bars + ST + buf), (t / ST) & 1, a.err);   // V of tile t
+      // slots past the split's end in its last page hold no key of this
+      // sequence: zero their V rows (P is 0 there, and 0 * stale must be 0)
+      const int first_bad = hi - tbase;
+      if (first_bad < kTile) {
+        for (int i = tid; i < (kTile - first_bad) * (D / 8); i += NT) {
+          const int j = first_bad + i / (D / 8), c = i % (D / 8);
+          *reinterpret_cast<uint4*>(sV + buf * KVB + Cfg::off(j, c * 8)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      __syncthreads();
+    }
+    if (live) {
+    // O += P . V with P = hi + mid + lo: hi = bf16(p), mid = bf16(p - hi),
+    // lo = bf16(p - hi - mid).  Both differences are exact in FP32 and the
+    // three parts hold p's 24 significant bits, so the products sum the FP32
+    // p against exact bf16 V.
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
       // A fragment order: (row g, k 0-7), (row g+8, k 0-7), (row g, k 8-15), (row g+8, k 8-15)
-      const uint32_t af[4] = {pf[ks][0], pf[ks][1], pf[ks][2], pf[ks][3]};
-      const uint32_t al[4] = {pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3]};
+      uint32_t af[4], am[4], al[4];
+#pragma unroll
+      for (int hi2 = 0; hi2 < 2; ++hi2) {
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+          const float p0 = s[2 * ks + hi2][2 * pr], p1 = s[2 * ks + hi2][2 * pr + 1];
+          split3(p0, p1, af[hi2 * 2 + pr], am[hi2 * 2 + pr], al[hi2 * 2 + pr]);
+        }
+      }
       // V fragments of this k-step first, then every accumulator's hi MMA,
-      // then every lo MMA (per accumulator still hi before lo, ks ascending)
+      // then every mid MMA, then every lo MMA (per accumulator hi, mid, lo,
+      // ks ascending)
       constexpr int DPS = DTW / 2;
       uint32_t vf[DPS][4];
 #pragma unroll
@@ -441,20 +501,26 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
       }
 #pragma unroll
       for (int dp = 0; dp < DPS; ++dp) {
+        mma_bf16(acc[2 * dp], am, vf[dp][0], vf[dp][1]);
+        mma_bf16(acc[2 * dp + 1], am, vf[dp][2], vf[dp][3]);
+      }
+#pragma unroll
+      for (int dp = 0; dp < DPS; ++dp) {
         mma_bf16(acc[2 * dp], al, vf[dp][0], vf[dp][1]);
         mma_bf16(acc[2 * dp + 1], al, vf[dp][2], vf[dp][3]);
       }
     }
+    }  // live
     __syncthreads();
-    // TMA: every warp is done with tile t's stage: refill it with tile t+ST
-    if (TMA && t + ST < ntiles) load_tile(buf, t + ST);
+    // TMA: every warp is done with V of tile t: its buffer takes V of tile t+ST
+    if (TMA && t + ST < ntiles) load_half(buf, t + ST, 1);
   }
 
   // ---- epilogue: single-split rows write the final output, others partials
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int v = vw * 16 + g + 8 * i;
-    if (v >= nv) continue;
+    if (v >= nv || vpos[i] < 0) continue;
     const int row = r0 + v / a.G;
     const int head = h * a.G + v % a.G;
     const int ns = row_splits(a, vpos[i]);
@@ -484,7 +550,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
 }
 
 // Merge the splits of rows that have more than one, in ascending split order:
-// w_s = 2^(m_s - M), O = sum w_s o_s, L = sum w_s l_s, out = O / L.
+// w_s = exp(m_s - M), O = sum w_s o_s, L = sum w_s l_s, out = O / L.
 template <int D>
 __global__ void attn_merge_kernel(const __grid_constant__ AttnArgs a) {
   pdl_wait();     // stream predecessor done, its writes visible
@@ -493,7 +559,9 @@ __global__ void attn_merge_kernel(const __grid_constant__ AttnArgs a) {
   const int lane = threadIdx.x & 31;
   if (gw >= int64_t(a.T) * a.Hq) return;
   const int row = int(gw / a.Hq), head = int(gw % a.Hq);
-  const int ns = row_splits(a, a.row_pos[row]);
+  const int pos = a.row_pos[row];
+  if (!row_pos_ok(a, pos)) return;   // reported by the attention kernel; output is NaN
+  const int ns = row_splits(a, pos);
   if (ns <= 1) return;
   const int64_t base = (int64_t(row) * a.Hq + head) * a.nsplit_grid;
   float M = -INFINITY;
@@ -506,7 +574,7 @@ __global__ void attn_merge_kernel(const __grid_constant__ AttnArgs a) {
   for (int s = 0; s < ns; ++s) {
     const float ms = a.ws_ml[2 * (base + s)];
     if (ms == -INFINITY) continue;
-    const float w = exp2f(ms - M);
+    const float w = expf(ms - M);
     L += w * a.ws_ml[2 * (base + s) + 1];
     const float* o = a.ws_o + (base + s) * D;
 #pragma unroll
@@ -704,7 +772,7 @@ biv_status biv_attention(const biv_attn_desc* d, void* ws, size_t wsb, biv_strea
   a.bt = d->block_table; a.max_pages = d->max_pages;
   a.kv_split = split;
   a.topk_idx = d->topk_idx; a.topk_stride = d->topk_stride; a.topk = d->topk;
-  a.scale_log2 = d->scale * kLog2e;
+  a.scale = d->scale;
   a.nsplit_grid = (span + split - 1) / split;
   a.ws_o = static_cast<float*>(ws);
   a.ws_ml = a.ws_o ? a.ws_o + size_t(d->T) * d->Hq * a.nsplit_grid * d->D : nullptr;
@@ -735,28 +803,67 @@ constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB per device
 static __device__ __align__(256) uint8_t g_attn_noalloc_scratch[kNoAllocScratchBytes];
 
 // The host cannot use the array's name as a device address: it is looked up
-// once per device, with that device current.
+// with the device current and cached per CUDA context.  Keying the cache on
+// the context (not only on the device ordinal) means that a context torn down
+// and created again (cudaDeviceReset, which reloads the module and so moves
+// the array) gets a fresh lookup instead of a stale address.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
 void* noalloc_scratch_ptr(biv_status* st) {
+  struct Entry { CUcontext ctx; int dev; void* ptr; };
   static std::mutex mu;
-  static void* ptr[64] = {};
+  static Entry cache[64];
+  static int used = 0;
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
     *st = set_error(BIV_ERR_CUDA, "attention_noalloc: no current CUDA device");
     return nullptr;
   }
+  CtxGetCurrentFn get_ctx = ctx_get_current();
+  if (!get_ctx) {
+    *st = set_error(BIV_ERR_CUDA, "attention_noalloc: cuCtxGetCurrent is not available");
+    return nullptr;
+  }
+  CUcontext ctx = nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!ptr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      *st = set_error(BIV_ERR_CUDA, "attention_noalloc: cudaGetSymbolAddress failed: %s",
-                      cudaGetErrorString(e));
-      return nullptr;
-    }
-    ptr[dev] = p;
+  if (get_ctx(&ctx) == CUDA_SUCCESS && ctx) {
+    for (int i = 0; i < used; ++i)
+      if (cache[i].ctx == ctx && cache[i].dev == dev) {
+        *st = BIV_OK;
+        return cache[i].ptr;
+      }
+  }
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_noalloc_scratch);
+  if (e != cudaSuccess || !p) {
+    *st = set_error(BIV_ERR_CUDA, "attention_noalloc: cudaGetSymbolAddress failed: %s",
+                    cudaGetErrorString(e));
+    return nullptr;
+  }
+  // the lookup makes the device's primary context current if none was
+  if (get_ctx(&ctx) == CUDA_SUCCESS && ctx) {
+    int slot = -1;
+    for (int i = 0; i < used; ++i)
+      if (cache[i].dev == dev) slot = i;       // a replaced context of this device
+    if (slot < 0 && used < 64) slot = used++;
+    if (slot >= 0) cache[slot] = Entry{ctx, dev, p};
   }
   *st = BIV_OK;
-  return ptr[dev];
+  return p;
 }
 
 }  // namespace

@@ -85,7 +85,8 @@ class Paged:
         return k, v
 
 
-def run_attn(B, pc, q, rows, blocks, Hq, kv_split=1024, mode=0, topk_idx=None, topk=0, tma=True):
+def run_attn(B, pc, q, rows, blocks, Hq, kv_split=1024, mode=0, topk_idx=None, topk=0, tma=True,
+             max_ctx=None):
     """rows: list of (seq, pos); blocks: list of (first row, count)."""
     T = len(rows)
     D = pc.D
@@ -106,7 +107,7 @@ def run_attn(B, pc, q, rows, blocks, Hq, kv_split=1024, mode=0, topk_idx=None, t
     d.v_scale = pc.vs.data_ptr() if pc.fp8 else None
     d.block_table, d.max_pages = pc.bt_d.data_ptr(), pc.bt.shape[1]
     d.page, d.kv_split = 64, kv_split
-    d.max_ctx = max(r[1] for r in rows) + 1
+    d.max_ctx = max(r[1] for r in rows) + 1 if max_ctx is None else max_ctx
     if topk_idx is not None:
         d.topk_idx, d.topk_stride, d.topk = topk_idx.data_ptr(), topk_idx.stride(0), topk
     d.scale = 1.0 / math.sqrt(D)
@@ -261,3 +262,42 @@ def test_decode_cta_shape_changes_no_bit(B, monkeypatch, stages, dsplit, D):
     idx = [sum(lens[:i + 1]) - 1 for i in range(len(lens))]
     dec = run_attn(B, pc, qp[torch.tensor(idx, device="cuda")], last, blocks, 16, kv_split=1024, tma=True)
     assert np.array_equal(bits(dec), bits(full[torch.tensor(idx, device="cuda")]))
+
+
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "threads"])
+def test_row_beyond_max_ctx_is_reported_and_isolated(B, tma):
+    """A row whose position lies past the splits that max_ctx provides for
+    (the caller broke the bound) is reported on the device error word and
+    gets NaN output; it touches no workspace slot, and the other rows of the
+    call keep the bits they have when the bound holds."""
+    g = synth.rng(41)
+    Hq, Hkv, D = 16, 8, 128
+    pc = Paged(B, g, [700], Hkv, D)
+    q = synth.normal_bf16(g, (3, Hq * D)).cuda()
+    rows = [(0, 699), (0, 100), (0, 200)]
+    blocks = [(0, 1), (1, 1), (2, 1)]
+    assert B.biv_poll_error() == 0
+    good = run_attn(B, pc, q, rows, blocks, Hq, kv_split=128, tma=tma)
+    assert B.biv_poll_error() == 0
+    for max_ctx in (201, 100):           # 2 splits; 1 split (no workspace at all)
+        bad = run_attn(B, pc, q, rows, blocks, Hq, kv_split=128, tma=tma, max_ctx=max_ctx)
+        assert B.biv_poll_error() == 2
+        assert B.biv_poll_error() == 0
+        assert torch.isnan(bad[0].float()).all()
+        ok = [1, 2] if max_ctx == 201 else [1]
+        assert np.array_equal(bits(bad[ok]), bits(good[ok]))
+
+
+@pytest.mark.parametrize("fp8", [False, True], ids=["bf16kv", "fp8kv"])
+def test_decode_row_at_16k_context_parity(B, fp8):
+    """One decode row of a 16384-token sequence: 16 splits of 1024 keys merged
+    in ascending order, against the oracle's plain softmax over every key."""
+    g = synth.rng(16384 + fp8)
+    Hq, Hkv, D, L = 16, 8, 128, 16384
+    pc = Paged(B, g, [L], Hkv, D, fp8=fp8)
+    q = synth.normal_bf16(g, (1, Hq * D)).cuda()
+    out = run_attn(B, pc, q, [(0, L - 1)], [(0, 1)], Hq, kv_split=1024)
+    k, v = pc.oracle_kv(0)
+    ref = ops.attention(host_f32(q).reshape(1, Hq, D), k, v, np.array([L - 1]), np.arange(L),
+                        1 / math.sqrt(D))
+    assert rel_err(host_f32(out).reshape(1, Hq, D), ref) < REL
