@@ -84,3 +84,36 @@ def f32_to_e4m3(x: np.ndarray) -> np.ndarray:
     code = np.where(a >= E4M3_MAX, 0x7E, code).astype(np.uint8)
     code = np.where(nan, np.uint8(0x7F), code).astype(np.uint8)
     return (code | np.where(neg, np.uint8(0x80), np.uint8(0))).astype(np.uint8)
+
+
+# ----------------------------------------------------------------- e2m1 ----
+# OCP 4-bit floating point "E2M1": sign, 2 exponent bits (bias 1), 1 mantissa
+# bit, no infinities or NaN.  Exponent field 0 is subnormal (0 and 0.5).
+
+def _e2m1_value(code: int) -> float:
+    s = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return s * m * 0.5
+    return s * (1.0 + m / 2.0) * 2.0 ** (e - 1)
+
+
+E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def e2m1_to_f32(codes: np.ndarray) -> np.ndarray:
+    """Decode e2m1 codes (low 4 bits of uint8) to float32 exactly."""
+    return E2M1_TABLE[np.asarray(codes, dtype=np.uint8) & 0xF].astype(np.float32)
+
+
+def nvfp4_dequant(codes: np.ndarray, scale_codes: np.ndarray, block: int = 16) -> np.ndarray:
+    """NVFP4 weights [N, K]: e2m1 codes [N, K] times one e4m3 scale per block
+    of 16 consecutive K elements (scale codes [N, K/16]), global scale 1.
+    A 2-significant-bit value times a 4-significant-bit scale has at most 6
+    significant bits, so the product is exact in FP32 and lies on the bf16
+    grid (unless it leaves bf16's exponent range, which e4m3 scales cannot
+    reach)."""
+    v = e2m1_to_f32(codes).astype(np.float64)
+    s = np.repeat(e4m3_to_f32(scale_codes).astype(np.float64), block, axis=-1)[..., :v.shape[-1]]
+    return (v * s).astype(np.float32)
