@@ -251,9 +251,10 @@ biv_status biv_attention(const biv_attn_desc* desc, void* workspace, size_t work
  * arguments and results as biv_attention, but the split partials go to a
  * fixed 64 MiB device array inside the library instead of a caller
  * workspace.  Every GPU that loads the library holds that array until the
- * process exits.  The first call on a device looks the array's address up
- * (once per device, with that device current); make that first call before
- * any stream capture.  A call whose scratch need (biv_attention_workspace)
+ * process exits.  The first call in a CUDA context looks the array's address
+ * up (with that context's device current) and caches it for that context;
+ * make that first call before any stream capture, and again after a device
+ * reset (a new context gets a fresh lookup on its first call).  A call whose scratch need (biv_attention_workspace)
  * exceeds 64 MiB returns BIV_ERR_WORKSPACE and launches nothing.  All calls
  * share the one array: calls whose work can overlap on the GPU (different
  * streams, no ordering between them) race and must not be issued.  Nothing
@@ -412,6 +413,60 @@ typedef struct {
  * needs no initial value. */
 biv_status biv_ssd_workspace(const biv_ssd_desc* desc, size_t* bytes);
 biv_status biv_ssd_scan(const biv_ssd_desc* desc, biv_stream_t stream);
+
+/* ------------------------------------------------- Mamba-2 mixer steps --
+ * The steps of a Mamba-2 layer around biv_ssd_scan ("Finish RL Training
+ * Faster", section "两组结果，要连同分母一起读": the Mamba-2 hybrid; section
+ * "一致性有多个层面": decode replays the prefill order bit for bit).
+ *
+ * biv_causal_conv1d: depthwise causal convolution of width 4 over the
+ * `channels` xBC columns of the in-projection output u (columns col_x ..),
+ * then SiLU, rounded to bf16 into out [T, channels]:
+ *   out[t, c] = bf16(silu(acc)), acc = b[c]; acc = acc + w[c, j] * x[t-3+j, c]
+ *   for j = 0..3 in FP32, product and sum each rounded (no fma);
+ * and, over the `heads` dt columns (col_dt ..), dt_out[t, h] =
+ * softplus(dt_raw + dt_bias[h]) in FP32 (x > 20 gives x).  Rows of sequence
+ * i (0 <= i < nseq) are rows row0[i] .. row0[i]+n[i]-1 of this call, at
+ * consecutive positions from pos0[i]; row_seq / row_pos give each row's i
+ * and position.  Inputs before a sequence's first row in the call come from
+ * state [nseq, 3, channels] bf16 (the three inputs that preceded it; zero for
+ * a new sequence, pos0 = 0), so prefill, chunked prefill and decode give the
+ * same bits.  After the call state[i] holds the last three inputs of every
+ * sequence with n[i] > 0.  conv_w bf16 [channels, 4], conv_b bf16
+ * [channels], dt_bias fp32 [heads].  channels and heads multiples of 8;
+ * u, out rows and state 16-byte aligned.  A row whose (row_seq, row_pos) is
+ * not one of its sequence's rows is reported through biv_poll_error and
+ * written as zeros. */
+typedef struct {
+  const uint16_t* u; int64_t u_stride;
+  int col_x, col_dt, channels, heads, width;   /* width must be 4 */
+  const uint16_t* conv_w; const uint16_t* conv_b; const float* dt_bias;
+  uint16_t* out; int64_t out_stride;
+  float* dt_out; int64_t dt_stride;
+  int T;
+  const int32_t* row_seq; const int32_t* row_pos;
+  int nseq;
+  const int32_t* row0; const int32_t* n; const int32_t* pos0;
+  uint16_t* state;
+} biv_conv_desc;
+biv_status biv_causal_conv1d(const biv_conv_desc* desc, biv_stream_t stream);
+
+/* Gated RMSNorm of the Mamba-2 output: g = y * silu(z) in FP32 (not
+ * rounded), out = bf16((g * inv) * w), inv = 1/sqrt(mean(g^2) + eps), the
+ * same per-row reduction tree as biv_add_rmsnorm.  y, z, out bf16 rows of d
+ * (d a multiple of 8, at most 8192), w bf16 [d]. */
+biv_status biv_gated_rmsnorm(const uint16_t* y, int64_t y_stride, const uint16_t* z,
+                             int64_t z_stride, const uint16_t* w, uint16_t* out,
+                             int64_t out_stride, int rows, int d, float eps, biv_stream_t stream);
+
+/* NVFP4 weights to bf16 ("Finish RL Training Faster", section
+ * "两组结果，要连同分母一起读": NVFP4 weights): out[n, k] = e2m1(codes[n, k])
+ * * e4m3(scales[n, k/16]), global scale 1.  codes uint8 [N, K] (one e2m1
+ * code per byte, low 4 bits), scales uint8 [N, K/16] (e4m3), out bf16
+ * [N, K]; the product is exact in bf16.  K a multiple of 16, codes and out
+ * 16-byte aligned. */
+biv_status biv_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, int N, int K,
+                             uint16_t* out, biv_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -26,6 +26,7 @@ EXPORTS = [
     "biv_gemm_workspace", "biv_gemm_partials", "biv_gemm",
     "biv_act_quant_fp8", "biv_topk", "biv_router_topk", "biv_moe_dispatch", "biv_gather_rows",
     "biv_moe_combine", "biv_logprob", "biv_ssd_workspace", "biv_ssd_scan",
+    "biv_causal_conv1d", "biv_gated_rmsnorm", "biv_nvfp4_dequant",
 ]
 
 
@@ -86,6 +87,20 @@ class SSDDesc(C.Structure):
                 ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
 
 
+class ConvDesc(C.Structure):
+    _fields_ = [("u", C.c_void_p), ("u_stride", C.c_int64),
+                ("col_x", C.c_int), ("col_dt", C.c_int), ("channels", C.c_int), ("heads", C.c_int),
+                ("width", C.c_int),
+                ("conv_w", C.c_void_p), ("conv_b", C.c_void_p), ("dt_bias", C.c_void_p),
+                ("out", C.c_void_p), ("out_stride", C.c_int64),
+                ("dt_out", C.c_void_p), ("dt_stride", C.c_int64),
+                ("T", C.c_int),
+                ("row_seq", C.c_void_p), ("row_pos", C.c_void_p),
+                ("nseq", C.c_int),
+                ("row0", C.c_void_p), ("n", C.c_void_p), ("pos0", C.c_void_p),
+                ("state", C.c_void_p)]
+
+
 _lib: Optional[C.CDLL] = None
 
 
@@ -125,6 +140,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "biv_moe_combine": ([P, P, P, P, P, I, I, I, P], I),
         "biv_logprob": ([P, I64, P, I, I, P, P], I),
         "biv_ssd_workspace": ([P, P], I), "biv_ssd_scan": ([P, P], I),
+        "biv_causal_conv1d": ([P, P], I),
+        "biv_gated_rmsnorm": ([P, I64, P, I64, P, P, I64, I, I, F, P], I),
+        "biv_nvfp4_dequant": ([P, P, I, I, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name, None)
@@ -389,3 +407,22 @@ def biv_ssd_scan(desc: SSDDesc, stream=None):
             ws = gemm_scratch(need)
             desc.workspace, desc.workspace_bytes = ws.data_ptr(), ws.numel()
     _check(load().biv_ssd_scan(C.byref(desc), _stream(stream)), "biv_ssd_scan")
+
+
+def biv_causal_conv1d(desc: ConvDesc, stream=None):
+    _check(load().biv_causal_conv1d(C.byref(desc), _stream(stream)), "biv_causal_conv1d")
+
+
+def biv_gated_rmsnorm(y, z, w, out, eps, rows=None, stream=None):
+    """y, z, out: 2-D bf16 views (rows of d); w bf16 [d]."""
+    _bf16_ok(y, z, w, out)
+    n = y.shape[0] if rows is None else rows
+    _check(load().biv_gated_rmsnorm(_p(y), _rs(y), _p(z), _rs(z), _p(w), _p(out), _rs(out), n,
+                                    y.shape[-1], eps, _stream(stream)), "biv_gated_rmsnorm")
+
+
+def biv_nvfp4_dequant(codes, scales, out, stream=None):
+    """codes uint8 [N, K], scales uint8 [N, K/16] (e4m3) -> out bf16 [N, K]."""
+    N, K = codes.shape
+    _check(load().biv_nvfp4_dequant(_p(codes), _p(scales), N, K, _p(out), _stream(stream)),
+           "biv_nvfp4_dequant")

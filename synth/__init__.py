@@ -107,6 +107,61 @@ class SSDConfig:
 SSD_LAYER = SSDConfig()
 
 
+@dataclass(frozen=True)
+class HybridConfig:
+    """Mamba-2 / attention hybrid: ``pattern`` lists the mixers of the stack
+    ("M" Mamba-2, "A" GQA attention), each followed by a SiLU-gated MLP."""
+
+    name: str
+    d_model: int
+    ssd_heads: int
+    ssd_head_dim: int
+    state: int
+    chunk: int
+    q_heads: int
+    kv_heads: int
+    head_dim: int
+    intermediate: int
+    vocab: int
+    pattern: str = "MMMMA"
+    eps: float = 1e-6
+    rope_theta: float = 1e6
+    page: int = 64
+    kv_split: int = 1024
+    kv_fp8: bool = False
+    conv_width: int = 4
+
+    @property
+    def d_inner(self) -> int:
+        return self.ssd_heads * self.ssd_head_dim
+
+    @property
+    def conv_channels(self) -> int:
+        return self.d_inner + 2 * self.state
+
+    @property
+    def in_proj_width(self) -> int:
+        return 2 * self.d_inner + 2 * self.state + self.ssd_heads
+
+    @property
+    def qkv_width(self) -> int:
+        return (self.q_heads + 2 * self.kv_heads) * self.head_dim
+
+    @property
+    def layers(self) -> int:          # attention layers (the ones with a KV cache)
+        return self.pattern.count("A")
+
+
+# one hybrid unit at the Nemotron-style width (vocabulary: a reading, the
+# pages give none)
+HYBRID = HybridConfig(name="mamba2-hybrid-unit-d2560", d_model=2560, ssd_heads=64, ssd_head_dim=64,
+                      state=128, chunk=256, q_heads=32, kv_heads=4, head_dim=80, intermediate=6912,
+                      vocab=131072)
+HYBRID_TINY = HybridConfig(name="mamba2-hybrid-tiny", d_model=256, ssd_heads=8, ssd_head_dim=64,
+                           state=128, chunk=256, q_heads=4, kv_heads=2, head_dim=80, intermediate=512,
+                           vocab=4096)
+
+
 # --------------------------------------------------------------------------
 # random sources
 # --------------------------------------------------------------------------
@@ -260,3 +315,171 @@ def ssd_inputs(g: np.random.Generator, T: int, cfg: SSDConfig = SSD_LAYER):
     A = (-g.uniform(1.0, 16.0, size=H)).astype(np.float32)
     D = normal_f32(g, (H,))
     return x, dt, A, B, C, D
+
+
+# --------------------------------------------------------------------------
+# device-side draws for throughput workloads (no oracle comparison)
+# --------------------------------------------------------------------------
+def device_generator(seed: int, device="cuda") -> torch.Generator:
+    """torch's counter-based CUDA generator (Philox), seeded."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    return gen
+
+
+def device_normal(gen: torch.Generator, shape, std: float = 1.0, dtype=torch.bfloat16) -> torch.Tensor:
+    """N(0, std^2) draws made on the device, narrowed by PyTorch's cast."""
+    return (torch.randn(*shape, generator=gen, device=gen.device) * std).to(dtype)
+
+
+def device_fp8_block_weights(gen: torch.Generator, groups: int, n: int, k: int):
+    """The recipe of ``fp8_block_weights`` drawn on the device: e4m3 codes of
+    N(0, 64) clipped to the finite range, one log-uniform fp32 scale (around
+    0.02 / 64) per 128x128 block.  Returns (codes uint8 [groups, n, k],
+    scales fp32 [groups, ceil(n/128), ceil(k/128)])."""
+    dev = gen.device
+    codes = torch.empty(groups, n, k, dtype=torch.uint8, device=dev)
+    for gi in range(groups):   # one group at a time keeps the fp32 draw small
+        x = (torch.randn(n, k, generator=gen, device=dev) * 64.0).clamp_(-448, 448)
+        codes[gi] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+    nb, kb = (n + 127) // 128, (k + 127) // 128
+    u = torch.rand(groups, nb, kb, generator=gen, device=dev) * 2.0 - 1.0
+    return codes, (0.02 / 64.0) * torch.exp2(u)
+
+
+# --------------------------------------------------------------------------
+# hybrid stack weights (NVFP4 linear layers)
+# --------------------------------------------------------------------------
+# magnitudes of the 8 non-negative e2m1 codes 0..7 (0, 0.5, 1, 1.5, 2, 3, 4, 6)
+# are drawn with these probabilities (a bell-shaped spread over the grid);
+# the sign bit (code bit 3) is a fair coin
+_E2M1_MAG_P = np.array([0.12, 0.22, 0.20, 0.16, 0.12, 0.10, 0.05, 0.03])
+
+
+def nvfp4_weights(g: np.random.Generator, n: int, k: int):
+    """NVFP4 weights drawn as codes: e2m1 codes uint8 [n, k] (one code per
+    byte, values 0..15) and e4m3 scale codes uint8 [n, ceil(k/16)] drawn
+    uniformly from 0x04..0x0F (scales 2^-7 .. 1.875 * 2^-6, so code x scale
+    has an RMS near 0.03).  No quantisation happens here: each side decodes
+    the codes with its own codec."""
+    mag = g.choice(8, size=(n, k), p=_E2M1_MAG_P).astype(np.uint8)
+    sign = (g.random(size=(n, k)) < 0.5).astype(np.uint8) << 3
+    sc = g.integers(0x04, 0x10, size=(n, (k + 15) // 16)).astype(np.uint8)
+    return torch.from_numpy(mag | sign), torch.from_numpy(sc)
+
+
+def hybrid_weights(cfg: HybridConfig, seed: int = 0, random_gains: bool = False,
+                   lm_scale: float = 1.0) -> Dict[str, object]:
+    """Random-init weights of the hybrid stack.  Linear layers are NVFP4
+    (a (codes, scale codes) pair per matrix, [N, K] K-major); the embedding
+    is bf16 N(0, 0.02); norm gains 1.0 (or 1 + N(0, 0.1)); conv weights bf16
+    N(0, 0.3) [channels, 4] and bias N(0, 0.1); dt_bias U[-6, -2.5], A =
+    -U[1, 16], D = N(1, 0.1) in fp32.  ``lm_scale`` multiplies the LM head's
+    scales by a power of two (exact) for a peaked variant."""
+    g = rng(seed)
+    d, I = cfg.d_model, cfg.intermediate
+    W: Dict[str, object] = {}
+    W["embed"] = normal_bf16(g, (cfg.vocab, d), 0.02)
+
+    def gain(n):
+        if random_gains:
+            return to_bf16(1.0 + normal_f32(g, (n,), 0.1))
+        return to_bf16(np.ones(n, np.float32))
+
+    for l, kind in enumerate(cfg.pattern):
+        p = f"l{l}."
+        W[p + "norm"] = gain(d)
+        if kind == "M":
+            W[p + "in_proj"] = nvfp4_weights(g, cfg.in_proj_width, d)
+            W[p + "conv_w"] = normal_bf16(g, (cfg.conv_channels, cfg.conv_width), 0.3)
+            W[p + "conv_b"] = normal_bf16(g, (cfg.conv_channels,), 0.1)
+            W[p + "dt_bias"] = torch.from_numpy(g.uniform(-6.0, -2.5, size=cfg.ssd_heads).astype(np.float32))
+            W[p + "A"] = torch.from_numpy((-g.uniform(1.0, 16.0, size=cfg.ssd_heads)).astype(np.float32))
+            W[p + "D"] = torch.from_numpy(normal_f32(g, (cfg.ssd_heads,), 0.1, 1.0))
+            W[p + "norm_w"] = gain(cfg.d_inner)
+            W[p + "out_proj"] = nvfp4_weights(g, d, cfg.d_inner)
+        else:
+            W[p + "wqkv"] = nvfp4_weights(g, cfg.qkv_width, d)
+            W[p + "wo"] = nvfp4_weights(g, d, cfg.q_heads * cfg.head_dim)
+        W[p + "mlp_norm"] = gain(d)
+        W[p + "wgu"] = nvfp4_weights(g, 2 * I, d)
+        W[p + "wd"] = nvfp4_weights(g, d, I)
+    W["final_norm"] = gain(d)
+    codes, sc = nvfp4_weights(g, cfg.vocab, d)
+    if lm_scale != 1.0:
+        e = int(round(np.log2(lm_scale)))
+        assert 2.0 ** e == lm_scale and 0 <= e <= 4, "lm_scale: a power of two up to 16"
+        sc = sc + np.uint8(8 * e)                  # e4m3: +1 in the exponent field doubles
+    W["lm_head"] = (codes, sc)
+    return W
+
+
+def hybrid_sequences(cfg: HybridConfig, n: int, lo: int, hi: int, seed: int = 1,
+                     prompt_frac: float = 0.75) -> List[Sequence]:
+    """n sequences, lengths uniform in [lo, hi], ids uniform; the prompt is
+    the first ``prompt_frac`` of each."""
+    g = rng(seed)
+    out = []
+    for _ in range(n):
+        L = int(g.integers(lo, hi + 1))
+        toks = g.integers(0, cfg.vocab, size=L, dtype=np.int64).astype(np.int32)
+        out.append(Sequence(toks, max(1, int(L * prompt_frac))))
+    return out
+
+
+def host_payload(W: Dict[str, object]) -> Dict[str, object]:
+    """Raw payloads for the oracle's own decoders: bf16 tensors as uint16
+    bits, fp32 as float32 arrays, NVFP4 pairs as (codes, scale codes) uint8."""
+    out = {}
+    for k, v in W.items():
+        if isinstance(v, tuple):
+            out[k] = (v[0].numpy().copy(), v[1].numpy().copy())
+        elif v.dtype == torch.bfloat16:
+            out[k] = bf16_bits(v)
+        else:
+            out[k] = v.numpy().astype(np.float32).copy()
+    return out
+
+
+def device_nvfp4_weights(gen: torch.Generator, n: int, k: int):
+    """The recipe of ``nvfp4_weights`` drawn on the device: e2m1 magnitudes
+    from the same categorical distribution (a uniform draw located in its
+    cumulative probabilities), a fair sign bit, e4m3 scale codes uniform over
+    0x04..0x0F."""
+    dev = gen.device
+    cdf = torch.tensor(np.cumsum(_E2M1_MAG_P)[:-1], dtype=torch.float32, device=dev)
+    mag = torch.searchsorted(cdf, torch.rand(n, k, generator=gen, device=dev), right=True)
+    sign = (torch.rand(n, k, generator=gen, device=dev) < 0.5).to(torch.uint8) << 3
+    sc = torch.randint(0x04, 0x10, (n, (k + 15) // 16), generator=gen, device=dev, dtype=torch.uint8)
+    return (mag.to(torch.uint8) | sign), sc
+
+
+def device_hybrid_weights(cfg: HybridConfig, seed: int = 0) -> Dict[str, object]:
+    """``hybrid_weights``' recipe (unit gains) drawn on the device, for
+    throughput runs at full width."""
+    gen = device_generator(seed)
+    dev = gen.device
+    d, I = cfg.d_model, cfg.intermediate
+    W: Dict[str, object] = {"embed": device_normal(gen, (cfg.vocab, d), 0.02)}
+    ones = lambda n: torch.ones(n, dtype=torch.bfloat16, device=dev)
+    for l, kind in enumerate(cfg.pattern):
+        p = f"l{l}."
+        W[p + "norm"] = ones(d)
+        if kind == "M":
+            W[p + "in_proj"] = device_nvfp4_weights(gen, cfg.in_proj_width, d)
+            W[p + "conv_w"] = device_normal(gen, (cfg.conv_channels, cfg.conv_width), 0.3)
+            W[p + "conv_b"] = device_normal(gen, (cfg.conv_channels,), 0.1)
+            W[p + "dt_bias"] = torch.rand(cfg.ssd_heads, generator=gen, device=dev) * 3.5 - 6.0
+            W[p + "A"] = -(torch.rand(cfg.ssd_heads, generator=gen, device=dev) * 15.0 + 1.0)
+            W[p + "D"] = 1.0 + 0.1 * torch.randn(cfg.ssd_heads, generator=gen, device=dev)
+            W[p + "norm_w"] = ones(cfg.d_inner)
+            W[p + "out_proj"] = device_nvfp4_weights(gen, d, cfg.d_inner)
+        else:
+            W[p + "wqkv"] = device_nvfp4_weights(gen, cfg.qkv_width, d)
+            W[p + "wo"] = device_nvfp4_weights(gen, d, cfg.q_heads * cfg.head_dim)
+        W[p + "mlp_norm"] = ones(d)
+        W[p + "wgu"] = device_nvfp4_weights(gen, 2 * I, d)
+        W[p + "wd"] = device_nvfp4_weights(gen, d, I)
+    W["final_norm"] = ones(d)
+    W["lm_head"] = device_nvfp4_weights(gen, cfg.vocab, d)
+    return W

@@ -1,0 +1,224 @@
+"""Mamba-2 / attention hybrid: the mixer's steps against the oracle, and the
+stack's invariance -- one prefill, a chunked prefill and a token-by-token
+decode that crosses a 256-token SSD chunk boundary give the same bits, and a
+sequence alone gives the bits it has in a batch ("Finish RL Training Faster",
+section "一致性有多个层面": decode replays the prefill chunk order)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import mamba
+from oracle.codecs import bf16_to_f32, nvfp4_dequant
+
+pytestmark = pytest.mark.gpu
+REL = 1e-2
+TOL_LP = 2e-2
+with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                       "accumulation_spread.json")) as _f:
+    SPREAD = json.load(_f)
+
+
+@pytest.fixture(scope="module")
+def B():
+    from invariant_forward_bitwise_gb300 import biv, build
+    build.build()
+    biv.load()
+    return biv
+
+
+def h32(t):
+    return bf16_to_f32(t.detach().cpu().view(torch.int16).numpy().view(np.uint16))
+
+
+def bits(t):
+    return t.detach().contiguous().view(torch.uint8).cpu().numpy()
+
+
+def rel_err(got, ref):
+    ref = np.asarray(ref, np.float64)
+    return float(np.max(np.abs(np.asarray(got, np.float64) - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def test_nvfp4_dequant_bit_exact(B):
+    g = synth.rng(1)
+    codes, sc = synth.nvfp4_weights(g, 300, 4096)
+    sc[:, :3] = torch.tensor([0x00, 0x7E, 0x01], dtype=torch.uint8)   # zero, 448, smallest subnormal
+    out = torch.empty(300, 4096, dtype=torch.bfloat16, device="cuda")
+    B.biv_nvfp4_dequant(codes.cuda(), sc.cuda(), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(h32(out), nvfp4_dequant(codes.numpy(), sc.numpy()))
+
+
+def _conv_call(B, u, col_x, col_dt, ch, H, w, b, dtb, out, dt, rows_of, state):
+    """rows_of: list per sequence of (row0, n, pos0); rows laid out in order."""
+    T = sum(n for _, n, _ in rows_of)
+    seq = np.concatenate([np.full(n, i, np.int32) for i, (_, n, _) in enumerate(rows_of)])
+    pos = np.concatenate([np.arange(p0, p0 + n, dtype=np.int32) for _, n, p0 in rows_of])
+    keep = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in
+            (seq, pos, np.array([r[0] for r in rows_of], np.int32), np.array([r[1] for r in rows_of], np.int32),
+             np.array([r[2] for r in rows_of], np.int32))]
+    c = B.ConvDesc()
+    c.u, c.u_stride, c.col_x, c.col_dt, c.channels, c.heads, c.width = (
+        u.data_ptr(), u.stride(0), col_x, col_dt, ch, H, 4)
+    c.conv_w, c.conv_b, c.dt_bias = w.data_ptr(), b.data_ptr(), dtb.data_ptr()
+    c.out, c.out_stride, c.dt_out, c.dt_stride = out.data_ptr(), out.stride(0), dt.data_ptr(), dt.stride(0)
+    c.T = T
+    c.row_seq, c.row_pos = keep[0].data_ptr(), keep[1].data_ptr()
+    c.nseq = len(rows_of)
+    c.row0, c.n, c.pos0 = keep[2].data_ptr(), keep[3].data_ptr(), keep[4].data_ptr()
+    c.state = state.data_ptr()
+    B.biv_causal_conv1d(c)
+    torch.cuda.synchronize()
+
+
+def test_causal_conv1d_parity_and_state_replay(B):
+    g = synth.rng(2)
+    ch, H, T = 768, 8, 70
+    width = 2 * 512 + 256 + H
+    u = synth.normal_bf16(g, (T, width)).cuda()
+    w = synth.normal_bf16(g, (ch, 4), 0.3).cuda()
+    b = synth.normal_bf16(g, (ch,), 0.1).cuda()
+    dtb = torch.from_numpy(g.uniform(-6, -2.5, H).astype(np.float32)).cuda()
+    col_x, col_dt = 512, 512 + ch
+    out = torch.empty(T, ch, dtype=torch.bfloat16, device="cuda")
+    dt = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    state = torch.zeros(1, 3, ch, dtype=torch.bfloat16, device="cuda")
+    _conv_call(B, u, col_x, col_dt, ch, H, w, b, dtb, out, dt, [(0, T, 0)], state)
+    uf = h32(u)
+    ref, st_ref = mamba.conv1d_causal_silu(uf[:, col_x:col_x + ch], h32(w), h32(b))
+    got = h32(out)
+    assert rel_err(got, ref) < REL
+    assert np.mean(got != ref) < 0.01                       # equal but for rare silu ulps
+    assert np.array_equal(h32(state[0]), st_ref)
+    ref_dt = mamba.softplus(uf[:, col_dt:col_dt + H] + dtb.cpu().numpy()[None, :])
+    assert np.allclose(dt.cpu().numpy(), ref_dt, rtol=1e-6, atol=0)
+    # the same rows in pieces (state replay): 1 row, 2 rows, 40, then 1 at a time
+    out2 = torch.empty_like(out)
+    dt2 = torch.empty_like(dt)
+    state2 = torch.zeros_like(state)
+    a = 0
+    for n in [1, 2, 40] + [1] * 27:
+        _conv_call(B, u[a:a + n], col_x, col_dt, ch, H, w, b, dtb, out2[a:a + n], dt2[a:a + n],
+                   [(0, n, a)], state2)
+        a += n
+    assert a == T
+    assert np.array_equal(bits(out2), bits(out)) and np.array_equal(bits(dt2), bits(dt))
+    assert np.array_equal(bits(state2), bits(state))
+
+
+def test_gated_rmsnorm_parity(B):
+    g = synth.rng(3)
+    for d in (512, 4096):
+        y = synth.normal_bf16(g, (9, d)).cuda()
+        z = synth.normal_bf16(g, (9, d)).cuda()
+        w = synth.to_bf16(1 + synth.normal_f32(g, (d,), 0.1)).cuda()
+        out = torch.empty_like(y)
+        B.biv_gated_rmsnorm(y, z, w, out, 1e-6)
+        torch.cuda.synchronize()
+        ref = mamba.gated_rmsnorm(h32(y), h32(z), h32(w), 1e-6)
+        assert rel_err(h32(out), ref) < REL
+        one = torch.empty_like(y[:1])
+        B.biv_gated_rmsnorm(y[4:5], z[4:5], w, one, 1e-6)
+        assert np.array_equal(bits(one), bits(out[4:5]))     # a row alone = in the batch
+
+
+def _model(lm_scale, seed=0):
+    from invariant_forward_bitwise_gb300.hybrid import HybridModel, new_kv
+    cfg = synth.HYBRID_TINY
+    W = synth.hybrid_weights(cfg, seed=seed, random_gains=True, lm_scale=lm_scale)
+    m = HybridModel(cfg, W, max_rows=1024, max_seqs=4, max_pos=512)
+    return cfg, W, m, new_kv(cfg, 4, 512)
+
+
+@pytest.fixture(scope="module")
+def peaked(B):
+    return _model(8.0)
+
+
+def test_hybrid_prefill_chunked_decode_bitwise_across_chunk_boundary(peaked):
+    """Sequences of 280-300 tokens (one 256-token SSD chunk boundary inside):
+    one prefill; a chunked prefill of 100-row pieces; a 250-token prompt then
+    token-by-token decode across position 256; all in a batch and alone."""
+    from invariant_forward_bitwise_gb300.hybrid import run_sequences
+    cfg, W, m, kv = peaked
+    seqs = synth.hybrid_sequences(cfg, n=2, lo=280, hi=300, seed=5)
+    full = run_sequences(m, kv, seqs, [[s.length - 1] for s in seqs])
+    chunked = run_sequences(m, kv, seqs, [[100] * ((s.length - 1) // 100) + [(s.length - 1) % 100]
+                                          for s in seqs])
+    decode = run_sequences(m, kv, seqs, [[250] + [1] * (s.length - 1 - 250) for s in seqs])
+    alone = [run_sequences(m, kv, [s], [[250] + [1] * (s.length - 1 - 250)])[0] for s in seqs]
+    for a, b, c, e in zip(full, chunked, decode, alone):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+        assert np.array_equal(a.view(np.uint32), c.view(np.uint32))
+        assert np.array_equal(a.view(np.uint32), e.view(np.uint32))
+
+
+@pytest.mark.parametrize("lm_scale,case", [(1.0, "hybrid_tiny_flat"), (8.0, "hybrid_tiny_peaked")],
+                         ids=["flat", "peaked"])
+def test_hybrid_matches_oracle(B, lm_scale, case, capsys):
+    from invariant_forward_bitwise_gb300.hybrid import run_sequences
+    cfg, W, m, kv = _model(lm_scale)
+    seqs = synth.hybrid_sequences(cfg, n=2, lo=280, hi=300, seed=5)
+    got = run_sequences(m, kv, seqs, [[s.length - 1] for s in seqs])
+    orc = mamba.HybridOracle(cfg, mamba.decode_hybrid_weights(synth.host_payload(W)), max_pos=512)
+    worst = 0.0
+    for s, gl in zip(seqs, got):
+        ref = orc.prefill_logprobs(s.tokens)
+        worst = max(worst, float(np.max(np.abs(gl[s.prompt_len - 1:] - ref[s.prompt_len - 1:]))))
+    bound = max(TOL_LP, SPREAD[case]["max"])
+    with capsys.disabled():
+        print(f"\n[hybrid tiny lm x{lm_scale:g}] |dlp| max {worst:.4f} (bound {bound:.4f})")
+    assert worst <= bound
+
+
+def test_hybrid_save_reload_then_next_decode_step(B):
+    """Mid-decode, the hybrid's weights (decoded bf16), attention KV pages,
+    conv states, SSD states and the open chunks' row buffers go to host memory
+    and are loaded into a new model in fresh allocations; the next decode
+    steps (crossing the 256-token chunk boundary) give the original bits."""
+    from invariant_forward_bitwise_gb300.hybrid import HybridModel, new_kv
+    cfg = synth.HYBRID_TINY
+    W = synth.hybrid_weights(cfg, seed=2, random_gains=True, lm_scale=8.0)
+    m = HybridModel(cfg, W, max_rows=1024, max_seqs=4, max_pos=512)
+    kv = new_kv(cfg, 4, 512)
+    seqs = synth.hybrid_sequences(cfg, n=2, lo=290, hi=300, seed=8)
+    for i, s in enumerate(seqs):
+        kv.admit(i, s.length)
+        m.reset_slot(i)
+    kv.sync_table()
+
+    def step(model, cache, positions):
+        ids = [int(seqs[i].tokens[p]) for i, p in enumerate(positions)]
+        tg = [int(seqs[i].tokens[p + 1]) for i, p in enumerate(positions)]
+        spec = model.load(cache, list(range(len(positions))), positions, ids, list(range(len(ids))), tg)
+        model.step(cache, spec)
+        return model.lp[:len(ids)].cpu().numpy().copy()
+
+    # prefill 250 tokens of each, then 3 decode steps
+    ids = [int(t) for s in seqs for t in s.tokens[:250]]
+    spec = m.load(kv, [0] * 250 + [1] * 250, list(range(250)) * 2, ids, [], [])
+    m.step(kv, spec)
+    for p in range(250, 253):
+        step(m, kv, [p, p])
+    torch.cuda.synchronize()
+    host_w = {k: v.cpu().clone() for k, v in m.W.items()}
+    host_state = {l: {k: t.cpu().clone() for k, t in st.items()} for l, st in m.mstate.items()}
+    host_kv = (kv.k.cpu().clone(), kv.v.cpu().clone(), kv.bt_host.copy(),
+               {k: list(v) for k, v in kv.owned.items()}, list(kv.free))
+    a = [step(m, kv, [p, p]) for p in range(253, 262)]
+    m2 = HybridModel(cfg, host_w, max_rows=1024, max_seqs=4, max_pos=512)
+    for l, st in host_state.items():
+        for k, t in st.items():
+            m2.mstate[l][k].copy_(t)
+    kv2 = new_kv(cfg, 4, 512)
+    kv2.k.copy_(host_kv[0])
+    kv2.v.copy_(host_kv[1])
+    kv2.bt_host[:], kv2.owned, kv2.free = host_kv[2], host_kv[3], host_kv[4]
+    kv2.sync_table()
+    b = [step(m2, kv2, [p, p]) for p in range(253, 262)]
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
