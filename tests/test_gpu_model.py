@@ -4,8 +4,20 @@ Invariance (every statistic of the logprob diff, max/mean/std and k3, must be
 exactly 0): batch 1 vs batch 8, whole prefill vs chunked prefill, rollout
 (prompt prefill + token-by-token decode) vs trainer recompute (private cache),
 eager vs CUDA-Graph decode, graph replay after an in-place weight update vs
-eager at the new weights.  Parity: |lp_gpu - lp_oracle| <= 2e-2.
+eager at the new weights.
+
+Parity, free-running (each side feeds its own outputs forward):
+|lp_gpu - lp_oracle| <= max(2e-2, spread), where spread is the measured gap
+between two correct FP32 evaluation orders of the oracle itself on the same
+case (float64-then-rounded vs plain ascending-k dot products), stored in
+tests/golden/accumulation_spread.json by the script beside it.  Where bf16
+rounding flips are amplified (a x10 LM head, 28 layers of QK-norm attention,
+FP8 KV codes) that spread exceeds 2e-2, and no implementation that does not
+reproduce the oracle's exact roundings can promise less.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -17,6 +29,14 @@ from oracle.model import DenseOracle, decode_weights
 pytestmark = pytest.mark.gpu
 TOL_LP = 2e-2
 ZERO = {"max": 0.0, "mean": 0.0, "std": 0.0, "k3": 0.0}
+with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                       "accumulation_spread.json")) as _f:
+    SPREAD = json.load(_f)
+
+
+def lp_bound(case):
+    """2e-2, or the oracle's own order spread on this case if larger."""
+    return max(TOL_LP, SPREAD[case]["max"])
 
 
 def flat(lps):
@@ -49,18 +69,28 @@ def tiny(request):
     return cfg, W, m, kv, seqs
 
 
+@pytest.mark.parametrize("lm_scale", [1.0, 10.0], ids=["flat", "peaked"])
 @pytest.mark.parametrize("kv_fp8", [False, True], ids=["bf16kv", "fp8kv"])
-def test_recompute_matches_oracle(kv_fp8):
-    """Free-running parity at the config's own initialisation (N(0, 0.02))."""
+def test_recompute_matches_oracle(kv_fp8, lm_scale, capsys):
+    """Free-running parity at the config's own initialisation (N(0, 0.02)),
+    and with the x10 "peaked" LM head whose logprobs spread far from -log V
+    (the variant that exercises log-softmax)."""
     from invariant_forward_bitwise_gb300.model import recompute
     cfg = synth.replace(synth.TINY, kv_fp8=kv_fp8)
-    W, m, kv = make(cfg, lm_scale=1.0)
+    W, m, kv = make(cfg, lm_scale=lm_scale)
     seqs = synth.tiny_sequences(cfg, n=8, seed=1)
     got = recompute(m, kv, seqs, max_tokens=1024)
     orc = oracle_for(cfg, W)
-    for s, g in zip(seqs, got):
-        ref = orc.prefill_logprobs(s.tokens)[s.prompt_len - 1:]
-        assert np.max(np.abs(g - ref)) <= TOL_LP
+    refs = [orc.prefill_logprobs(s.tokens)[s.prompt_len - 1:] for s in seqs]
+    if lm_scale > 1.0:
+        assert np.std(np.concatenate(refs)) > 1.0        # really peaked
+        bound = lp_bound("tiny_peaked_fp8kv" if kv_fp8 else "tiny_peaked_bf16kv")
+    else:
+        bound = TOL_LP
+    worst = max(float(np.max(np.abs(g - r))) for g, r in zip(got, refs))
+    with capsys.disabled():
+        print(f"\n[tiny lm x{lm_scale:g} kv_fp8={kv_fp8}] |dlp| max {worst:.4f} (bound {bound:.4f})")
+    assert worst <= bound
 
 
 def test_batch1_vs_batch8_and_chunked(tiny):
@@ -100,6 +130,11 @@ def test_inplace_weight_update_under_graph():
     rec2 = recompute(m, kv, seqs, max_tokens=1024)                  # eager at new weights
     assert stats(after, rec2) == ZERO
     assert stats(before, after)["max"] > 0
+    # and the replayed graphs computed the model at the new weights
+    orc = oracle_for(cfg, W2)
+    for s, g in zip(seqs, after):
+        ref = orc.prefill_logprobs(s.tokens)[s.prompt_len - 1:]
+        assert np.max(np.abs(g - ref)) <= lp_bound("tiny_peaked_seed4")
 
 
 def test_reload_then_first_step():
@@ -125,9 +160,9 @@ def test_qwen3_shape_two_layers_invariance_and_parity():
     rol = rollout(m, kv, seqs, max_tokens=512)
     assert stats(rec, rol) == ZERO
     orc = oracle_for(cfg, W)
-    for s, g in zip(seqs, rec):
-        ref = orc.prefill_logprobs(s.tokens)[s.prompt_len - 1:]
-        assert np.max(np.abs(g - ref)) <= 3 * TOL_LP
+    worst = max(float(np.max(np.abs(g - orc.prefill_logprobs(s.tokens)[s.prompt_len - 1:])))
+                for s, g in zip(seqs, rec))
+    assert worst <= lp_bound("qwen3_2L"), worst
 
 
 @pytest.mark.parametrize("kv_fp8", [False, True], ids=["bf16kv", "fp8kv"])
@@ -135,8 +170,9 @@ def test_qwen3_full_depth_per_layer_parity(kv_fp8, capsys):
     """All 28 layers of the Qwen3-1.7B shape at full size, each checked against
     the oracle computing that layer from the GPU's own input residual (1e-2
     relative per layer output), plus the head from the GPU's last residual
-    (|dlp| <= 2e-2).  The free-running oracle gap is printed, not asserted:
-    it compounds bf16 rounding differences over depth."""
+    (|dlp| <= 2e-2), plus free-running parity on three sequences within the
+    oracle's own order spread at this depth (bf16 flips compound over 28
+    layers for any two correct evaluation orders)."""
     from invariant_forward_bitwise_gb300.model import PagedKV, Runner, prefill_rows, DenseModel
     from oracle.codecs import bf16_to_f32
     cfg = synth.replace(synth.QWEN3_1P7B, kv_fp8=kv_fp8)
@@ -177,11 +213,28 @@ def test_qwen3_full_depth_per_layer_parity(kv_fp8, capsys):
         r_prev = got                       # next layer starts from the GPU's residual
     head = orc.head_from(r_prev, s.tokens[1:])
     assert np.max(np.abs(lp - head)) <= TOL_LP
-    free = orc.prefill_logprobs(s.tokens)
+    # free-running: the three sequences of the spread measurement, all positions
+    seqs = synth.tiny_sequences(cfg, n=3, lo=48, hi=48, seed=11)
+    assert np.array_equal(seqs[0].tokens, s.tokens)
+    kv2 = PagedKV(cfg, pages=8, max_seqs=3, max_pages=4)
+    for i, q in enumerate(seqs):
+        kv2.admit(i, q.length)
+    kv2.sync_table()
+    rows = prefill_rows(seqs, [0, 1, 2], [0, 0, 0], [q.length - 1 for q in seqs], [0, 0, 0])
+    spec2 = run.load_rows(kv2, *rows[:5])
+    m.reserve(kv2, [spec2])
+    m.step(kv2, spec2)
+    lp3 = m.lp[:spec2.T_lm].cpu().numpy().reshape(3, -1)
+    assert np.array_equal(lp3[0].view(np.uint32), lp.view(np.uint32))   # batch of 3 = alone
+    gaps = [np.abs(lp3[i] - orc.prefill_logprobs(q.tokens)) for i, q in enumerate(seqs)]
+    case = "qwen3_28L_fp8kv" if kv_fp8 else "qwen3_28L_bf16kv"
+    fmax, fmean = max(float(g.max()) for g in gaps), float(np.mean([g.mean() for g in gaps]))
     with capsys.disabled():
         print(f"\n[qwen3 28L kv_fp8={kv_fp8}] worst per-layer rel err {worst:.2e}; "
               f"teacher-forced head |dlp| max {np.max(np.abs(lp - head)):.2e}; "
-              f"free-running |dlp| max {np.max(np.abs(lp - free)):.3f} mean {np.mean(np.abs(lp - free)):.4f}")
+              f"free-running |dlp| max {fmax:.3f} mean {fmean:.4f}; oracle order spread "
+              f"max {SPREAD[case]['max']:.3f} mean {SPREAD[case]['mean']:.4f}")
+    assert fmax <= lp_bound(case)
 
 
 def test_fast_mode_differs_but_stays_close():
@@ -208,3 +261,60 @@ def test_continuous_batching_equals_recompute(kv_fp8):
     rec = recompute(m, kv, seqs, max_tokens=1024)
     mixed = serve_mixed(m, kv, seqs, chunk=16, max_decode=3)
     assert stats(rec, mixed) == ZERO
+
+
+def _decode_steps(dg, kv, seqs, cur, nsteps):
+    """nsteps teacher-forced decode steps of the live sequences (slot i =
+    sequence i), advancing cur; returns the logprobs of each step."""
+    out = []
+    for _ in range(nsteps):
+        live = [i for i, s in enumerate(seqs) if cur[i] < s.length - 1]
+        if not live:
+            break
+        lp = dg.run(live, [cur[i] for i in live], [int(seqs[i].tokens[cur[i]]) for i in live],
+                    [int(seqs[i].tokens[cur[i] + 1]) for i in live])
+        out.append(lp.cpu().numpy().copy())
+        for i in live:
+            cur[i] += 1
+    return out
+
+
+@pytest.mark.parametrize("kv_fp8", [False, True], ids=["bf16kv", "fp8kv"])
+def test_save_reload_then_next_decode_step(kv_fp8):
+    """Mid-rollout, weights, KV pages (codes and scales), the block table and
+    the page ownership go to host memory; a new model and a new cache are
+    built from those copies in fresh allocations and their decode graphs are
+    captured anew.  The next decode steps give the original objects' bits."""
+    from invariant_forward_bitwise_gb300.model import (DecodeGraphs, DenseModel, PagedKV, Runner,
+                                                      _run_rows, prefill_rows)
+    cfg = synth.replace(synth.TINY, kv_fp8=kv_fp8)
+    W, m, kv = make(cfg, seed=5)
+    seqs = synth.tiny_sequences(cfg, n=3, lo=60, hi=90, seed=6)
+    for i, s in enumerate(seqs):
+        kv.admit(i, s.length)
+    kv.sync_table()
+    rows = prefill_rows(seqs, [0, 1, 2], [0] * 3, [s.prompt_len for s in seqs], [10 ** 9] * 3)
+    _run_rows(m, Runner(m), kv, rows, 1024, lambda k, v: None)
+    dg = DecodeGraphs(m, kv, use_graphs=True)
+    cur = [s.prompt_len for s in seqs]
+    _decode_steps(dg, kv, seqs, cur, 5)
+    torch.cuda.synchronize()
+    # snapshot to host
+    host_w = {k: v.cpu().clone() for k, v in m.W.items()}
+    host_kv = {n: getattr(kv, n).cpu().clone() for n in ("k", "v", "ks", "vs") if getattr(kv, n) is not None}
+    bt, owned, free = kv.bt_host.copy(), {k: list(v) for k, v in kv.owned.items()}, list(kv.free)
+    cur2 = list(cur)
+    # the original objects go on
+    a = _decode_steps(dg, kv, seqs, cur, 6)
+    # new allocations from the host copies, graphs captured again
+    m2 = DenseModel(cfg, host_w, max_rows=1024, max_pos=512)
+    kv2 = PagedKV(cfg, pages=kv.pages, max_seqs=kv.block_table.shape[0], max_pages=kv.max_pages)
+    for n, t in host_kv.items():
+        getattr(kv2, n).copy_(t)
+    kv2.bt_host[:], kv2.owned, kv2.free = bt, owned, free
+    kv2.sync_table()
+    dg2 = DecodeGraphs(m2, kv2, use_graphs=True)
+    b = _decode_steps(dg2, kv2, seqs, cur2, 6)
+    assert len(a) == len(b) == 6
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))

@@ -43,8 +43,11 @@ def _weights(g, E, d, I):
     return wr, wgu, sgu, wd, sd, shgu[0], shsgu[0], shd[0], shsd[0]
 
 
-@pytest.mark.parametrize("T,E,k,d,I", [(64, 8, 2, 512, 256), (200, 64, 6, 1024, 1408)])
+@pytest.mark.parametrize("T,E,k,d,I", [(64, 8, 2, 512, 256), (200, 64, 6, 1024, 1408),
+                                       (256, 64, 6, 4096, 1408)])
 def test_moe_block_parity_and_invariance(T, E, k, d, I):
+    """The last case is the MoE block's own width (hidden 4096, 64 experts
+    top-6 + shared, expert intermediate 1408) on 256 tokens."""
     from invariant_forward_bitwise_gb300 import build
     from invariant_forward_bitwise_gb300.moe import MoEBlock
     build.build()
@@ -55,17 +58,20 @@ def test_moe_block_parity_and_invariance(T, E, k, d, I):
     h = synth.normal_bf16(g, (T, d))
     out = blk.forward(h.cuda()).clone()
     logits = blk.logits[:T].cpu().numpy()
+    hf = h.float().numpy()
+    # router logits: the FP32 GEMM within FP32 rounding of the oracle's
+    assert rel_err(logits, ops.gemm(hf, W[0].float().numpy(), out="f32")) < 1e-5
     # routing: bit-exact against the oracle's rule on the same logits
     ri, rw = ops.router_topk(logits, k)
     assert np.array_equal(blk.idx[:T].cpu().numpy(), ri)
     assert np.max(np.abs(blk.w[:T].cpu().numpy() - rw)) < 1e-6
-    # block output against the oracle's block (same quantisation rules)
-    hf = h.float().numpy()
+    # block output against the oracle's block (same quantisation rules),
+    # routed by the same logits so that every token's experts are compared
     experts = [(synth.fp8_bits(W[1][e]), W[2][e], synth.fp8_bits(W[3][e]), W[4][e]) for e in range(E)]
     shared = (synth.fp8_bits(W[5]), W[6], synth.fp8_bits(W[7]), W[8])
-    ref, oi, ow = moe_block(hf, W[0].float().numpy(), experts, shared, k)
-    if np.array_equal(oi, ri):
-        assert rel_err(host_f32(out), ref) < REL
+    ref, oi, ow = moe_block(hf, W[0].float().numpy(), experts, shared, k, logits=logits)
+    assert np.array_equal(oi, ri)
+    assert rel_err(host_f32(out), ref) < REL
     # a token alone gives the bits it had inside the batch
     for t in [0, T // 2, T - 1]:
         one = blk.forward(h[t:t + 1].cuda())

@@ -321,8 +321,7 @@ def test_topk_indexer_shape(B):
     sd = dev(s)
     B.biv_topk(sd, dev(nv), k, idx)
     got = idx.cpu().numpy()
-    for r in [0, 17, 63]:
-        assert np.array_equal(got[r], ops.topk_positions(s[r:r + 1], nv[r:r + 1], k)[0])
+    assert np.array_equal(got, ops.topk_positions(s, nv, k))           # all 64 rows
     # a row alone gives the same indices
     one = torch.empty(1, k, dtype=torch.int32, device="cuda")
     B.biv_topk(sd[40:41], dev(nv[40:41]), k, one)
@@ -442,9 +441,8 @@ def test_gemm_chunk_fold_in_cta_equals_fold_across_ctas(B, monkeypatch, M, N, K,
     res.append(bits(c))
     for r in res[1:]:
         assert np.array_equal(r, res[0])
-    rows = np.unique(np.array([0, M // 2, M - 1]))
-    ref = ops.gemm(a.float().numpy()[rows], b.float().numpy(), out=out)
-    assert rel_err(host_f32(c)[rows], ref) < REL
+    ref = ops.gemm(a.float().numpy(), b.float().numpy(), out=out)     # every row
+    assert rel_err(host_f32(c), ref) < REL
 
 
 def test_gemm_shared_workspace_across_shapes(B):
@@ -483,8 +481,8 @@ def test_tcgen05_result_independent_of_tile_width(B, monkeypatch, M, N, K):
     monkeypatch.delenv("BIV_GEMM_TILE_N")
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
-    ref = ops.gemm(a.float().numpy()[:5], b.float().numpy(), out="f32")
-    got = outs[0].view(np.float32).reshape(M, N)[:5]
+    ref = ops.gemm(a.float().numpy(), b.float().numpy(), out="f32")   # every row
+    got = outs[0].view(np.float32).reshape(M, N)
     assert rel_err(got, ref) < REL
 
 

@@ -118,3 +118,19 @@ def test_ssd_batch_of_sequences_matches_alone(B):
         r0 = row0[i]
         y1 = SSDRunner(B, 1, H, Q).run(x[r0:r0 + L], dt[r0:r0 + L], A, Bm[r0:r0 + L], Cm[r0:r0 + L], D, [0], [L], [0])
         assert np.array_equal(bits(y1), bits(yb[r0:r0 + L])), i
+
+
+def test_ssd_16k_tokens_parity_across_chunk_boundaries(B):
+    """16384 tokens (64 chunks of 256) through the parallel many-row path,
+    against the oracle's sequential recurrence carried over every chunk."""
+    H, T, Q = 4, 16384, 256
+    x, dt, A, Bm, Cm, D = inputs(T, T, H)
+    r = SSDRunner(B, 1, H, Q)
+    y = r.run(x.reshape(T, H * 64).cuda(), torch.from_numpy(dt).cuda(), torch.from_numpy(A).cuda(),
+              Bm.cuda(), Cm.cuda(), torch.from_numpy(D).cuda(), [0], [T], [0])
+    ref, h = ssd_sequential(x.float().numpy(), dt, A, Bm.float().numpy(), Cm.float().numpy(), D)
+    got = bf16_to_f32(y.cpu().view(torch.int16).numpy().view(np.uint16)).reshape(T, H, 64)
+    assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) < REL
+    # the carried state after the last full chunk (= the final state here)
+    st = r.state[0].cpu().numpy()
+    assert np.max(np.abs(st - h)) / np.max(np.abs(h)) < REL
