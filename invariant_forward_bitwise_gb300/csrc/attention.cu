@@ -38,15 +38,21 @@ constexpr int kNV = 64;     // most query vectors a CTA takes (4 warps x 16)
 // warp forms the same S and softmax for one group of 16 vectors and takes
 // 1/DS of the head dimension in P.V (decode blocks: shorter dependency chains
 // per warp, the same arithmetic for every output element).
-template <int D, int NW, int ST, bool TMA, int DS>
+// F8: FP8 pages; their codes and scales land in a staging area by cp.async one
+// tile ahead and are dequantised shared-to-shared into the bf16 K/V tiles.
+template <int D, int NW, int ST, bool TMA, int DS, bool F8 = false>
 struct AttnCfg {
   static_assert(DS == 1 || DS == NW, "D split: one warp per D slice");
+  static_assert(!(F8 && TMA), "FP8 pages use the thread loader");
   static constexpr int LD = D + 8;                   // padded row (elements), thread-loaded tiles
   static constexpr int NV = DS > 1 ? 16 : NW * 16;   // query vectors per CTA
   static constexpr int NT = NW * 32;                 // threads per CTA
   static constexpr int KVB = TMA ? kTile * D * 2 : kTile * LD * 2;  // one K or V stage
   static constexpr int Q_BYTES = NV * LD * 2;
-  static constexpr int SMEM = 1024 + 2 * ST * KVB + Q_BYTES + ST * kTile * 4 + 2 * ST * 8;
+  static constexpr int F8_CODES = F8 ? 2 * kTile * D : 0;          // K then V codes
+  static constexpr int F8_STAGE = F8 ? F8_CODES + 2 * kTile * 4 : 0;  // + K then V scales
+  static constexpr int SMEM =
+      1024 + 2 * ST * KVB + Q_BYTES + ST * F8_STAGE + ST * kTile * 4 + 2 * ST * 8;
   static constexpr int DK = D / 16;                  // k-steps of Q.K^T
   static constexpr int DT = D / 8;                   // n-tiles of O
   static constexpr int DTW = DT / DS;                // n-tiles of O per warp
@@ -101,6 +107,16 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
                "r"(valid ? 16 : 0)
                : "memory");
 }
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+// two e4m3 codes (first in the low byte) -> their exact values
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(v), __NV_E4M3);
+  return __half22float2(__half2(h));
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -141,11 +157,11 @@ __device__ __forceinline__ bool row_pos_ok(const AttnArgs& a, int pos) {
 }
 
 // MINB: CTAs per SM the register allocation must allow (0: no bound)
-template <int D, int NW, int ST, bool TMA, int DS, int MINB>
+template <int D, int NW, int ST, bool TMA, int DS, int MINB, bool F8>
 __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_constant__ AttnArgs a) {
   pdl_wait();     // stream predecessor done, its writes visible
   pdl_trigger();
-  using Cfg = AttnCfg<D, NW, ST, TMA, DS>;
+  using Cfg = AttnCfg<D, NW, ST, TMA, DS, F8>;
   constexpr int LD = Cfg::LD, NV = Cfg::NV, NT = Cfg::NT, KVB = Cfg::KVB;
   constexpr int DTW = Cfg::DTW;
   extern __shared__ uint8_t smem_raw[];
@@ -154,7 +170,8 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
   uint8_t* sK = base;                                   // [ST] stages of KVB bytes
   uint8_t* sV = base + ST * KVB;
   uint16_t* sQ = reinterpret_cast<uint16_t*>(base + 2 * ST * KVB);
-  int32_t* sPos = reinterpret_cast<int32_t*>(base + 2 * ST * KVB + Cfg::Q_BYTES);  // [ST][64]
+  uint8_t* sF8 = base + 2 * ST * KVB + Cfg::Q_BYTES;    // [ST] FP8 staging (F8 only)
+  int32_t* sPos = reinterpret_cast<int32_t*>(sF8 + ST * Cfg::F8_STAGE);  // [ST][64]
   // TMA: K of stage s completes on bars[s], V on bars[ST + s], so that K of
   // the next tile streams in while this tile's softmax and P.V run
   uint64_t* bars = reinterpret_cast<uint64_t*>(sPos + ST * kTile);                 // [2 ST]
@@ -249,7 +266,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     __syncthreads();
     uint8_t* dK = sK + buf * KVB;
     uint8_t* dV = sV + buf * KVB;
-    if (!a.fp8) {
+    if constexpr (!F8) {
       constexpr int CPR = D / 8;
       for (int i = tid; i < kTile * CPR * 2; i += NT) {
         const int which = i / (kTile * CPR);
@@ -265,36 +282,59 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
         cp_async16(smem_u32((which ? dV : dK) + Cfg::off(j, c * 8)), gp, p >= 0);
       }
     } else {
-      constexpr int CPR = D / 16;  // 16 codes per chunk
+      // raw codes (16 per copy) and scales of the tile's keys into the
+      // stage's staging area; missing keys read as zero codes and scales
+      uint8_t* stg = sF8 + buf * Cfg::F8_STAGE;
+      constexpr int CPR = D / 16;
       for (int i = tid; i < kTile * CPR * 2; i += NT) {
         const int which = i / (kTile * CPR);
         const int rem = i % (kTile * CPR);
         const int j = rem / CPR, c = rem % CPR;
         const int p = pos_buf[j];
-        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+        const uint8_t* gp = static_cast<const uint8_t*>(which ? a.vc : a.kc);
         if (p >= 0) {
           const int64_t slot = int64_t(a.bt[int64_t(seq) * a.max_pages + p / kTile]) * kTile + p % kTile;
-          const uint8_t* codes = static_cast<const uint8_t*>(which ? a.vc : a.kc) + slot * kv_row + int64_t(h) * D;
-          const float sc = (which ? a.vs : a.ks)[slot * a.Hkv + h];
-          const uint4 cv = reinterpret_cast<const uint4*>(codes)[c];
-          const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
-          uint32_t packed[8];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float f0 = e4m32f(uint8_t(w[q] & 0xFF)) * sc;
-            const float f1 = e4m32f(uint8_t((w[q] >> 8) & 0xFF)) * sc;
-            const float f2 = e4m32f(uint8_t((w[q] >> 16) & 0xFF)) * sc;
-            const float f3 = e4m32f(uint8_t(w[q] >> 24)) * sc;
-            packed[2 * q] = pack_bf2(f0, f1);
-            packed[2 * q + 1] = pack_bf2(f2, f3);
-          }
-          o0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          o1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          gp += slot * kv_row + int64_t(h) * D + c * 16;
         }
-        uint8_t* dst = (which ? dV : dK);
-        *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16)) = o0;
-        *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16 + 8)) = o1;
+        cp_async16(smem_u32(stg + which * kTile * D + j * D + c * 16), gp, p >= 0);
       }
+      for (int i = tid; i < 2 * kTile; i += NT) {
+        const int which = i / kTile, j = i % kTile;
+        const int p = pos_buf[j];
+        const float* gp = which ? a.vs : a.ks;
+        if (p >= 0) {
+          const int64_t slot = int64_t(a.bt[int64_t(seq) * a.max_pages + p / kTile]) * kTile + p % kTile;
+          gp += slot * a.Hkv + h;
+        }
+        cp_async4(smem_u32(stg + Cfg::F8_CODES + i * 4), gp, p >= 0);
+      }
+    }
+  };
+  // FP8: the staged codes of stage buf -> bf16 K/V tiles, x = bf16(float(code) * s)
+  auto dequant_stage = [&](int buf) {
+    const uint8_t* stg = sF8 + buf * Cfg::F8_STAGE;
+    const float* scl = reinterpret_cast<const float*>(stg + Cfg::F8_CODES);
+    constexpr int CPR = D / 16;
+    for (int i = tid; i < kTile * CPR * 2; i += NT) {
+      const int which = i / (kTile * CPR);
+      const int rem = i % (kTile * CPR);
+      const int j = rem / CPR, c = rem % CPR;
+      const uint4 cv = *reinterpret_cast<const uint4*>(stg + which * kTile * D + j * D + c * 16);
+      const float sc = scl[which * kTile + j];
+      const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
+      uint32_t packed[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f01 = e4m3x2_to_float2(uint16_t(w[q] & 0xFFFFu));
+        const float2 f23 = e4m3x2_to_float2(uint16_t(w[q] >> 16));
+        packed[2 * q] = pack_bf2(f01.x * sc, f01.y * sc);
+        packed[2 * q + 1] = pack_bf2(f23.x * sc, f23.y * sc);
+      }
+      uint8_t* dst = (which ? sV : sK) + buf * KVB;
+      *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16)) =
+          make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16 + 8)) =
+          make_uint4(packed[4], packed[5], packed[6], packed[7]);
     }
   };
 
@@ -344,6 +384,10 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
       cp_async_wait<ST - 2>();  // tile t has landed
     }
     __syncthreads();
+    if constexpr (F8) {
+      dequant_stage(buf);
+      __syncthreads();
+    }
     if (!TMA) {
       // refill the stage that tile t-1 used (its compute ended at the last sync)
       if (t + ST - 1 < ntiles) load_tile((t + ST - 1) % ST, t + ST - 1);
@@ -630,18 +674,18 @@ size_t ws_bytes(const biv_attn_desc& d, int split) {
   return size_t(d.T) * d.Hq * ns * (d.D + 2) * sizeof(float);
 }
 
-template <int D, int NW, int ST, bool TMA, int DS = 1, int MINB = 0>
+template <int D, int NW, int ST, bool TMA, int DS = 1, int MINB = 0, bool F8 = false>
 biv_status launch_cfg(const biv_attn_desc& d, const AttnArgs& a, cudaStream_t s) {
-  using Cfg = AttnCfg<D, NW, ST, TMA, DS>;
+  using Cfg = AttnCfg<D, NW, ST, TMA, DS, F8>;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attn_kernel<D, NW, ST, TMA, DS, MINB>,
+    if (cudaFuncSetAttribute(attn_kernel<D, NW, ST, TMA, DS, MINB, F8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
       return set_error(BIV_ERR_CUDA, "attention: cannot set shared memory size");
     attr = true;
   }
   dim3 grid(d.nqblocks, d.Hkv, a.nsplit_grid);
-  launch_pdl(attn_kernel<D, NW, ST, TMA, DS, MINB>, grid, Cfg::NT, Cfg::SMEM, s, a);
+  launch_pdl(attn_kernel<D, NW, ST, TMA, DS, MINB, F8>, grid, Cfg::NT, Cfg::SMEM, s, a);
   return check_launch("attention");
 }
 
@@ -724,7 +768,18 @@ biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
       }
     }
   }
-  if (!tma) st = small ? launch_cfg<D, 1, 2, false>(d, a, s) : launch_cfg<D, 4, 2, false>(d, a, s);
+  if (!tma) {
+    if (a.fp8) {
+      // FP8 decode CTAs: four warps share the staged dequantisation and split
+      // the head dimension in P.V (D = 80 keeps one warp: its 10 output
+      // n-tiles do not split four ways)
+      constexpr int DSF = D % 64 == 0 ? 4 : 1;
+      st = small ? launch_cfg<D, DSF, 2, false, DSF, 0, true>(d, a, s)
+                 : launch_cfg<D, 4, 2, false, 1, 0, true>(d, a, s);
+    } else {
+      st = small ? launch_cfg<D, 1, 2, false>(d, a, s) : launch_cfg<D, 4, 2, false>(d, a, s);
+    }
+  }
   if (st != BIV_OK || a.nsplit_grid <= 1) return st;
   const int64_t warps = int64_t(d.T) * d.Hq;
   launch_pdl(attn_merge_kernel<D>, unsigned((warps * 32 + 255) / 256), 256, 0, s, a);

@@ -3,7 +3,8 @@
   python -m invariant_forward_bitwise_gb300.kernel_bench CASE [REPS]
 
 CASE is one of attn_decode (256 sequences x 700 context, one decode row each),
-attn_decode4 (the same for 4 sequences),
+attn_decode4 (the same for 4 sequences), attn_decode_fp8 (128 sequences x 4096
+context on the e4m3 cache),
 attn_prefill (8 sequences x 1024 tokens), gemm_prefill (M 8192, N 2048,
 K 6144), gemm_qkv (M 16384, N 4096, K 2048), gemm_decode (M 64, N 2048, K 6144), lm_head (M 4096, N 151936,
 K 2048), ssd_prefill (16384 tokens, 64 heads), ssd_decode (one token), topk_indexer
@@ -163,11 +164,19 @@ elif case.startswith("ssd"):
     print(f"{case} T={T}: {ms*1e3:.1f} us  ({T/(ms/1e3):.0f} tokens/s per sequence)")
 elif case.startswith("attn"):
     Hq, Hkv, D = 16, 8, 128
-    B, ctx = {"attn_decode": (256, 700), "attn_decode4": (4, 700)}.get(case, (8, 1024))
+    B, ctx = {"attn_decode": (256, 700), "attn_decode4": (4, 700),
+              "attn_decode_fp8": (128, 4096)}.get(case, (8, 1024))
+    fp8 = case.endswith("fp8")
     pages_per = (ctx + 63) // 64
     P = B * pages_per
-    kc = (torch.randn(P, 64, Hkv, D, device="cuda") * 0.5).to(torch.bfloat16)
-    vc = (torch.randn(P, 64, Hkv, D, device="cuda") * 0.5).to(torch.bfloat16)
+    if fp8:
+        kc = fp8_codes(P, 64, Hkv, D)
+        vc = fp8_codes(P, 64, Hkv, D)
+        ks = torch.rand(P, 64, Hkv, device="cuda") * 0.01
+        vs = torch.rand(P, 64, Hkv, device="cuda") * 0.01
+    else:
+        kc = (torch.randn(P, 64, Hkv, D, device="cuda") * 0.5).to(torch.bfloat16)
+        vc = (torch.randn(P, 64, Hkv, D, device="cuda") * 0.5).to(torch.bfloat16)
     bt = torch.arange(P, dtype=torch.int32, device="cuda").view(B, pages_per)
     if case.startswith("attn_decode"):
         rows = [(i, ctx - 1) for i in range(B)]
@@ -186,13 +195,15 @@ elif case.startswith("attn"):
     d.T, d.Hq, d.Hkv, d.D = T, Hq, Hkv, D
     d.row_seq, d.row_pos, d.qblocks, d.nqblocks = seq.data_ptr(), pos.data_ptr(), qb.data_ptr(), len(blocks)
     d.max_rows_per_block = max(b[1] for b in blocks)
-    d.kv_dtype = biv.BF16
+    d.kv_dtype = biv.E4M3 if fp8 else biv.BF16
+    if fp8:
+        d.k_scale, d.v_scale = ks.data_ptr(), vs.data_ptr()
     d.k_cache, d.v_cache, d.block_table, d.max_pages = kc.data_ptr(), vc.data_ptr(), bt.data_ptr(), pages_per
     d.page, d.kv_split, d.max_ctx, d.scale, d.num_pages = 64, 1024, ctx, 1 / math.sqrt(D), P
     n = biv.biv_attention_workspace(d)
     ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
     ms = graph_time(lambda: biv.biv_attention(d, ws), reps)
-    kv_bytes = B * ctx * Hkv * D * 2 * 2
+    kv_bytes = B * ctx * Hkv * (D * (1 if fp8 else 2) + (4 if fp8 else 0)) * 2
     flops = 4.0 * sum(p + 1 for _, p in rows) * Hq * D
     print(f"{case}: {ms*1e3:.1f} us  KV {kv_bytes/1e6:.0f} MB -> {kv_bytes/(ms/1e3)/1e9:.0f} GB/s;  {flops/(ms/1e3)/1e12:.1f} TFLOP/s")
 elif case == "gemm_prefill_layer":

@@ -484,18 +484,22 @@ class DecodeGraphs:
             m.reserve(self.kv, [spec])
             m.step(self.kv, spec, self.qblocks, self.lm_rows)
         else:
-            self.graphs[Tb].replay()
             t = m._timer()
+            tok = t.bracket_decode(pos) if t and hasattr(t, "bracket_decode") else None
+            self.graphs[Tb].replay()
+            if tok:
+                t.close(tok)
             if t:
                 t.launches += self.launches[Tb]
         return m.lp[:n]
 
 
 def rollout(model: DenseModel, kv: PagedKV, seqs, max_tokens: int, use_graphs: bool = True,
-            graphs: Optional[DecodeGraphs] = None, collect: bool = True):
+            graphs: Optional[DecodeGraphs] = None, collect: bool = True, after_prefill=None):
     """Rollout: prefill every prompt, then decode one teacher-forced token per
     live sequence per step.  Returns per sequence the logprobs of its response
-    tokens (the first one comes from the prompt's last row)."""
+    tokens (the first one comes from the prompt's last row).  ``after_prefill``
+    (optional) is called once the prompt prefill has been issued."""
     run = Runner(model)
     out = [np.zeros(s.length - s.prompt_len, np.float32) for s in seqs]
     slots = list(range(len(seqs)))
@@ -506,6 +510,8 @@ def rollout(model: DenseModel, kv: PagedKV, seqs, max_tokens: int, use_graphs: b
                         [s.prompt_len - 1 for s in seqs])
     _run_rows(model, run, kv, rows, max_tokens,
               lambda k, lpv: _scatter(out, list(range(len(seqs))), seqs, k, lpv))
+    if after_prefill is not None:
+        after_prefill()
     dg = graphs or DecodeGraphs(model, kv, use_graphs)
     cur = [s.prompt_len for s in seqs]
     pending = []
