@@ -734,8 +734,8 @@ def hybrid_unit(peaks, lengths=(16384, 32768, 57344), decode_steps=256, seed=9):
     dec_ms = e[1].elapsed_time(e[2])
     ntok = sum(lengths)
     # lower bounds.  Parameters per token: every linear layer's N*K plus the LM head
-    lin = sum(v[0].numel() for v in W.values() if isinstance(v, tuple))
-    nvfp4_bytes = sum(v[0].numel() * 0.5 + v[1].numel() for v in W.values() if isinstance(v, tuple))
+    lin = sum(2 * v[0].numel() for v in W.values() if isinstance(v, tuple))   # codes packed two per byte
+    nvfp4_bytes = sum(v[0].numel() + v[1].numel() for v in W.values() if isinstance(v, tuple))
     tf, bw = peaks["bf16_tflops_sustained"] * 1e12, peaks["hbm_gbs"] * 1e9
     alu = 152 * 128 * 2 * 2.07e9            # FP32 FMA rate from unit counts and the max clock
     H, P, N, Q = cfg.ssd_heads, cfg.ssd_head_dim, cfg.state, cfg.chunk

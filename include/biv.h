@@ -460,13 +460,34 @@ biv_status biv_gated_rmsnorm(const uint16_t* y, int64_t y_stride, const uint16_t
                              int64_t out_stride, int rows, int d, float eps, biv_stream_t stream);
 
 /* NVFP4 weights to bf16 ("Finish RL Training Faster", section
- * "两组结果，要连同分母一起读": NVFP4 weights): out[n, k] = e2m1(codes[n, k])
- * * e4m3(scales[n, k/16]), global scale 1.  codes uint8 [N, K] (one e2m1
- * code per byte, low 4 bits), scales uint8 [N, K/16] (e4m3), out bf16
- * [N, K]; the product is exact in bf16.  K a multiple of 16, codes and out
- * 16-byte aligned. */
+ * "两组结果，要连同分母一起读": NVFP4 weights): out[n, k] = e2m1(code[n, k])
+ * * e4m3(scales[n, k/16]), global scale 1.  codes uint8 [N, K/2] packed two
+ * per byte (element 2i in the low nibble of byte i), scales uint8 [N, K/16]
+ * (e4m3), out bf16 [N, K]; the product is exact in bf16.  K a multiple of
+ * 16, codes and out 16-byte aligned. */
 biv_status biv_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, int N, int K,
                              uint16_t* out, biv_stream_t stream);
+
+/* GEMM with NVFP4 weights (W4A16): C[M, N] = A[M, K] . W^T with W = the
+ * biv_nvfp4_dequant of (codes, scales), every output bit equal to biv_gemm
+ * on that bf16 W (same K-chunk schedule, same tcgen05 MMAs; "Finish RL
+ * Training Faster", section "两组结果，要连同分母一起读": NVFP4 weights, and
+ * section "让训练前向使用推理的数值": one schedule for every batch).  When
+ * the bf16 plan would spread a few output tiles' K chunks over the SMs
+ * (decode-sized M), the kernel streams the packed codes and scales by TMA
+ * and decodes them in shared memory: 0.5625 bytes of HBM per weight instead
+ * of 2 (K a multiple of 256).  Otherwise (many rows: compute-bound; or
+ * another K) the weights are decoded once into the workspace and the bf16
+ * GEMM runs.  A bf16 [M, K] row-major
+ * (lda >= K); codes/scales as for biv_nvfp4_dequant; C bf16 or f32 (c_dtype)
+ * [M, ldc].  K a multiple of 16; every pointer 16-byte aligned.  Workspace:
+ * biv_gemm_nvfp4_workspace bytes (0 possible), caller-owned, 16-byte
+ * aligned, no initial value; BIV_ERR_WORKSPACE when missing or too small. */
+biv_status biv_gemm_nvfp4_workspace(int M, int N, int K, int c_dtype, int mode, size_t* bytes);
+biv_status biv_gemm_nvfp4(const uint16_t* A, int64_t lda, const uint8_t* codes,
+                          const uint8_t* scales, int M, int N, int K, void* C, int64_t ldc,
+                          int c_dtype, int mode, void* workspace, size_t workspace_bytes,
+                          biv_stream_t stream);
 
 #ifdef __cplusplus
 }

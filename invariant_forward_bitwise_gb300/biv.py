@@ -27,6 +27,7 @@ EXPORTS = [
     "biv_act_quant_fp8", "biv_topk", "biv_router_topk", "biv_moe_dispatch", "biv_gather_rows",
     "biv_moe_combine", "biv_logprob", "biv_ssd_workspace", "biv_ssd_scan",
     "biv_causal_conv1d", "biv_gated_rmsnorm", "biv_nvfp4_dequant",
+    "biv_gemm_nvfp4_workspace", "biv_gemm_nvfp4",
 ]
 
 
@@ -143,6 +144,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "biv_causal_conv1d": ([P, P], I),
         "biv_gated_rmsnorm": ([P, I64, P, I64, P, P, I64, I, I, F, P], I),
         "biv_nvfp4_dequant": ([P, P, I, I, P, P], I),
+        "biv_gemm_nvfp4_workspace": ([I, I, I, I, I, P], I),
+        "biv_gemm_nvfp4": ([P, I64, P, P, I, I, I, P, I64, I, I, P, C.c_size_t, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name, None)
@@ -422,7 +425,28 @@ def biv_gated_rmsnorm(y, z, w, out, eps, rows=None, stream=None):
 
 
 def biv_nvfp4_dequant(codes, scales, out, stream=None):
-    """codes uint8 [N, K], scales uint8 [N, K/16] (e4m3) -> out bf16 [N, K]."""
-    N, K = codes.shape
+    """codes uint8 [N, K/2] (packed), scales uint8 [N, K/16] (e4m3) -> out bf16 [N, K]."""
+    N, K = out.shape
     _check(load().biv_nvfp4_dequant(_p(codes), _p(scales), N, K, _p(out), _stream(stream)),
            "biv_nvfp4_dequant")
+
+
+def biv_gemm_nvfp4_workspace(M, N, K, c_dtype=BF16, mode=MODE_INVARIANT) -> int:
+    n = C.c_size_t(0)
+    _check(load().biv_gemm_nvfp4_workspace(M, N, K, c_dtype, mode, C.byref(n)),
+           "biv_gemm_nvfp4_workspace")
+    return n.value
+
+
+def biv_gemm_nvfp4(A, codes, scales, Cout, M=None, mode=MODE_INVARIANT, ws=None, stream=None):
+    """Cout[M, N] = A[M, K] . dequant(codes, scales)^T; ws: a workspace of
+    biv_gemm_nvfp4_workspace bytes (a cached per-device scratch when None)."""
+    M = A.shape[0] if M is None else M
+    N, K = codes.shape[0], A.shape[1]
+    cdt = F32 if Cout.dtype == torch.float32 else BF16
+    need = biv_gemm_nvfp4_workspace(M, N, K, cdt, mode)
+    if ws is None and need:
+        ws = gemm_scratch(need)
+    _check(load().biv_gemm_nvfp4(_p(A), A.stride(0), _p(codes), _p(scales), M, N, K, _p(Cout),
+                                 Cout.stride(0), cdt, mode, _p(ws), ws.numel() if ws is not None else 0,
+                                 _stream(stream)), "biv_gemm_nvfp4")

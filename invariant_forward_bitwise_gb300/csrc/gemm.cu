@@ -146,6 +146,7 @@ struct GemmArgs {
   int64_t ldp;          // partial row pitch (N rounded up to the tile width)
   int vec_ok;           // C rows 16-byte aligned
   int n_fastest;        // fold mode: walk N tiles first
+  int b_after_wait;     // 1: B is written by the previous kernel (no early prefetch)
   int* err;
 };
 
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(kGemmThreads, PARTIAL ? 2 : 1)
       // The weights (B) of the first stages do not depend on the previous
       // kernel: fetch them before waiting for it, then A and the rest.
       int pre = 0;
-      {
+      if (!p.b_after_wait) {
         const int i = blockIdx.x, n0 = tile_n0(item_tile(i));
         const int kb0 = item_c0(i) * p.kc_blocks;
         pre = min(S, min(KB, item_c1(i) * p.kc_blocks) - kb0);
@@ -614,10 +615,275 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) tmem_dealloc(tmem, Cfg::TMEM_COLS);
 }
 
+// ------------------------------------------------------- NVFP4 weights --
+// Partial-mode GEMM whose B operand is stored as NVFP4: packed e2m1 codes
+// [N, K/2] (element 2i in the low nibble of byte i) and one e4m3 scale per 16
+// elements [N, K/16], global scale 1.  Each K block of 64 arrives as 4 KB of
+// codes and the 16-byte scale group holding its four scales; converter warps
+// decode it to bf16 (e2m1 x scale is exact in bf16) into the same
+// 128-byte-swizzled K-major tile that TMA writes for the bf16 path, and the
+// MMA runs the identical K schedule.  Every partial, and so every output, has
+// the bits of the bf16 GEMM on the decoded weights; HBM reads 0.5625 bytes
+// per weight instead of 2.
+// Two rings: R raw stages (A box, codes, scales; ~8 KB each, deep, so that
+// enough bytes are in flight) and kFp4Dec decoded bf16 tiles (16 KB each).
+// Warps: 0 = TMA producer, 1 = MMA issuer and TMEM owner, 2..9 = converters
+// (two threads per B row), 10..13 = epilogue (TMEM lane quarters).  A
+// converter looks each code byte (two elements) up in a 256-entry table of
+// bf16 pairs at scale 1 and multiplies the pair by the block scale in bf16
+// (exact: the product has at most 6 significant bits).  The table is held in
+// 32 interleaved copies so that lane L always reads bank L (measured: one
+// shared copy cost about 340 bank conflicts per 64-wide K block).
+constexpr int kFp4CodeBytes = 128 * 32;   // a K block: 128 rows x 64 codes
+constexpr int kFp4SclBytes = 128 * 16;    // a K block: 128 rows x one 16-scale group
+constexpr int kFp4Conv = 8;               // converter warps
+constexpr int kFp4Threads = 64 + 32 * kFp4Conv + 128;
+constexpr int kFp4Dec = 3;                // decoded bf16 tiles
+constexpr int kFp4MaxRaw = 32;            // raw stages at most
+
+size_t fp4_smem_bytes(int raw, int m_box) {
+  return 1024 + size_t(kFp4Dec) * 128 * 128 +
+         size_t(raw) * (m_box * 128 + kFp4CodeBytes + kFp4SclBytes) + (128 - m_box) * 128 +
+         (2 * kFp4MaxRaw + 2 * kFp4Dec + 4) * 8 + 16 + 256 * 32 * 4;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, __nv_bfloat162 b) {
+  const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), b);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__global__ void __launch_bounds__(kFp4Threads, 1)
+    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmC,
+                      const __grid_constant__ CUtensorMap tmS, const GemmArgs p) {
+  constexpr int BN = 128;
+  constexpr int B_TILE = BN * 128;
+  constexpr uint32_t kTmemCols = 256;   // two 128-column accumulators
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int R = p.stages;                                        // raw stages
+  const int a_stage = p.m_box * 128;
+  uint8_t* sB = smem;                                            // [kFp4Dec] decoded tiles
+  uint8_t* sA = sB + kFp4Dec * B_TILE;                           // [R] A boxes (+ pad)
+  uint8_t* sCode = sA + R * a_stage + (128 - p.m_box) * 128;     // [R] raw codes
+  uint8_t* sScl = sCode + R * kFp4CodeBytes;                     // [R] raw scale groups
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sScl + R * kFp4SclBytes);
+  // full[r]: A, codes and scales of raw stage r landed.  empty[r]: the MMA
+  // (A) and every converter warp (codes) are done with it.  dfull[b] /
+  // dempty[b]: decoded tile b written / read by the MMA.
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kFp4MaxRaw);
+  const uint32_t dfull0 = smem_u32(bars + 2 * kFp4MaxRaw);
+  const uint32_t dempty0 = smem_u32(bars + 2 * kFp4MaxRaw + kFp4Dec);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kFp4MaxRaw + 2 * kFp4Dec);
+  const uint32_t tempty0 = tfull0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kFp4MaxRaw + 2 * kFp4Dec + 4);
+  uint32_t* lut = tmem_slot + 4;   // [256][32]: byte (two codes) -> bf16 pair at scale 1
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KB = (p.K + 63) / 64;
+  const int chunks = (KB + p.kc_blocks - 1) / p.kc_blocks;
+  const int tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
+  const int items = tiles_m * tiles_n * chunks;
+  auto tile_m0 = [&](int t) { return (t % tiles_m) * BM; };
+  auto tile_n0 = [&](int t) { return (t / tiles_m) * BN; };
+  for (int e = threadIdx.x; e < 256 * 32; e += blockDim.x) {
+    const __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2(__nv_fp4x2_storage_t(e >> 5), __NV_E2M1);
+    const float2 f = __half22float2(__half2(hr));
+    lut[e] = pack_bf2(f.x, f.y);
+  }
+
+  if (threadIdx.x == 0) {
+    for (int r = 0; r < R; ++r) {
+      mbar_init(full0 + 8 * r, 1);
+      mbar_init(empty0 + 8 * r, 1 + kFp4Conv);
+    }
+    for (int b = 0; b < kFp4Dec; ++b) {
+      mbar_init(dfull0 + 8 * b, kFp4Conv);
+      mbar_init(dempty0 + 8 * b, 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(tfull0 + 8 * j, 1);
+      mbar_init(tempty0 + 8 * j, 4);
+    }
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+
+  int issued = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmC);
+      tma_prefetch_desc(&tmS);
+      const uint32_t tx = uint32_t(a_stage + kFp4CodeBytes + kFp4SclBytes);
+      auto load_b = [&](int r, int kb, int n0) {
+        mbar_expect_tx(full0 + 8 * r, tx);
+        tma_load_2d(smem_u32(sCode + r * kFp4CodeBytes), &tmC, full0 + 8 * r, kb * 32, n0);
+        tma_load_2d(smem_u32(sScl + r * kFp4SclBytes), &tmS, full0 + 8 * r, (kb >> 2) * 16, n0);
+      };
+      // weights of the first stages before waiting for the previous kernel
+      int pre = 0;
+      if (blockIdx.x < items) {
+        const int i = blockIdx.x, t = i / chunks, c = i % chunks;
+        const int kb0 = c * p.kc_blocks;
+        pre = min(R, min(KB, kb0 + p.kc_blocks) - kb0);
+        for (int r = 0; r < pre; ++r) load_b(r, kb0 + r, tile_n0(t));
+      }
+      pdl_wait();
+      bool ok = true;
+      for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
+        const int t = i / chunks, c = i % chunks, m0 = tile_m0(t), n0 = tile_n0(t);
+        const int kb1 = min(KB, (c + 1) * p.kc_blocks);
+        for (int kb = c * p.kc_blocks; kb < kb1; ++kb) {
+          const int r = issued % R;
+          if (issued >= pre) {
+            if (issued >= R && !mbar_wait(empty0 + 8 * r, ((issued / R) - 1) & 1, p.err)) {
+              ok = false;
+              break;
+            }
+            load_b(r, kb, n0);
+          }
+          tma_load_2d(smem_u32(sA + r * a_stage), &tmA, full0 + 8 * r, kb * 64, m0);
+          ++issued;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_mma(1u, BM, BN);
+      int it = 0, j = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++j) {
+        const int c = i % chunks, tb = j & 1;
+        if (j >= 2 && !mbar_wait(tempty0 + 8 * tb, ((j >> 1) - 1) & 1, p.err)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem + tb * BN;
+        const int kb0 = c * p.kc_blocks, kb1 = min(KB, kb0 + p.kc_blocks);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int r = it % R, b = it % kFp4Dec;
+          if (!mbar_wait(full0 + 8 * r, (it / R) & 1, p.err) ||
+              !mbar_wait(dfull0 + 8 * b, (it / kFp4Dec) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + r * a_stage);
+          const uint32_t b0 = smem_u32(sB + b * B_TILE);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f16(dt, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
+                     (kb != kb0 || kk != 0) ? 1u : 0u);
+          umma_commit(empty0 + 8 * r);
+          umma_commit(dempty0 + 8 * b);
+        }
+        if (ok) umma_commit(tfull0 + 8 * tb);
+      }
+    }
+  } else if (warp < 2 + kFp4Conv) {
+    // ---------------------------------------------------------- decode --
+    // two threads per B row: 16 bytes of codes (32 elements) and two scales
+    // of this K block -> half of one 128-byte swizzled bf16 row
+    const int rw = (threadIdx.x - 64) >> 1, hh = (threadIdx.x - 64) & 1;
+    int it = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
+      const int c = i % chunks;
+      const int kb1 = min(KB, (c + 1) * p.kc_blocks);
+      for (int kb = c * p.kc_blocks; kb < kb1; ++kb, ++it) {
+        const int r = it % R, b = it % kFp4Dec;
+        bool w_ok = mbar_wait(full0 + 8 * r, (it / R) & 1, p.err);
+        if (it >= kFp4Dec)
+          w_ok = w_ok && mbar_wait(dempty0 + 8 * b, ((it / kFp4Dec) - 1) & 1, p.err);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          ok = false;
+          break;
+        }
+        const uint4 cv =
+            *reinterpret_cast<const uint4*>(sCode + r * kFp4CodeBytes + rw * 32 + hh * 16);
+        const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(sScl + r * kFp4SclBytes + rw * 16 +
+                                                                  (kb & 3) * 4 + hh * 2);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * r);   // this warp is done with raw stage r
+        uint8_t* dst = sB + b * B_TILE + (rw >> 3) * 1024 + (rw & 7) * 128;
+        const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {              // 16 elements per e4m3 scale
+          const float sf = __half2float(__ushort_as_half(
+              __nv_cvt_fp8_to_halfraw(__nv_fp8_storage_t((sc2 >> (8 * g)) & 0xFFu), __NV_E4M3).x));
+          const __nv_bfloat162 s2 = __floats2bfloat162_rn(sf, sf);   // e4m3 is exact in bf16
+#pragma unroll
+          for (int q = 2 * g; q < 2 * g + 2; ++q) {  // 8 elements (one 16-byte chunk) per word
+            const uint32_t* lt = lut + lane;      // this lane's copy: bank = lane
+            const uint4 v = make_uint4(bf16x2_mul(lt[(w[q] & 0xFFu) << 5], s2),
+                                       bf16x2_mul(lt[((w[q] >> 8) & 0xFFu) << 5], s2),
+                                       bf16x2_mul(lt[((w[q] >> 16) & 0xFFu) << 5], s2),
+                                       bf16x2_mul(lt[(w[q] >> 24) << 5], s2));
+            const int chunk = hh * 4 + q;
+            *reinterpret_cast<uint4*>(dst + ((chunk ^ (rw & 7)) << 4)) = v;
+          }
+        }
+        fence_proxy_async();   // the generic writes above feed the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dfull0 + 8 * b);
+      }
+    }
+  } else {
+    // -------------------------------------------------------- epilogue --
+    const int q = warp & 3;
+    int j = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++j) {
+      const int t = i / chunks, c = i % chunks, m0 = tile_m0(t), n0 = tile_n0(t);
+      const int row = m0 + q * 32 + lane;
+      const int tb = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * tb, (j >> 1) & 1, p.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t ta = tmem + tb * BN + (uint32_t(q * 32) << 16);
+      float* dst = row < p.M ? p.ws + (int64_t(c) * p.M + row) * p.ldp + n0 : nullptr;
+#pragma unroll
+      for (int g = 0; g < BN / 32; ++g) {
+        uint32_t v[32];
+        tmem_ld32(ta + g * 32, v);
+        tmem_ld_wait();
+        if (dst) {
+#pragma unroll
+          for (int x = 0; x < 32; x += 4)
+            *reinterpret_cast<float4*>(dst + g * 32 + x) =
+                make_float4(__uint_as_float(v[x]), __uint_as_float(v[x + 1]),
+                            __uint_as_float(v[x + 2]), __uint_as_float(v[x + 3]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * tb);
+    }
+  }
+  // the producer makes sure its copies have landed before the CTA exits
+  if (warp == 0 && lane == 0) {
+    for (int i = max(0, issued - R); i < issued; ++i)
+      mbar_wait(full0 + 8 * (i % R), (i / R) & 1, p.err, 100000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------------------- host --
 // 2-D K-major tensor map: dims {K, rows}, box {box_k, box_rows}, 128B swizzle.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
-              int64_t K, int64_t rows, int64_t ld, int box_k, int box_rows) {
+              int64_t K, int64_t rows, int64_t ld, int box_k, int box_rows, bool swizzle = true) {
   auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
@@ -625,7 +891,8 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void
   cuuint32_t box[2] = {cuuint32_t(box_k), cuuint32_t(box_rows)};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -731,7 +998,7 @@ Plan plan_bf16(const biv_gemm_desc& d) {
 
 template <int BN, bool F32OUT>
 biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_gemm_desc& d,
-                       const Plan& pl, void* ws, cudaStream_t s) {
+                       const Plan& pl, void* ws, cudaStream_t s, bool b_after_wait) {
   // partial mode writes FP32 partials whatever C's type: one instantiation
   constexpr bool kPartialOk = BN <= 128;
   auto kern = (kPartialOk && pl.partial) ? gemm_bf16_kernel<BN, false, kPartialOk>
@@ -758,6 +1025,7 @@ biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_g
   a.ldp = pl.ldp;
   a.vec_ok = aligned16(d.C) && (d.ldc * eb) % 16 == 0;
   a.n_fastest = !pl.partial && d.N <= d.M;
+  a.b_after_wait = b_after_wait ? 1 : 0;
   a.err = device_error_word();
   const int64_t items = pl.partial ? pl.tiles * pl.chunks : pl.tiles;
   const int sms = sm_count() > 0 ? sm_count() : 148;
@@ -775,12 +1043,12 @@ biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_g
 
 template <bool F32OUT>
 biv_status dispatch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_gemm_desc& d,
-                         const Plan& p, void* ws, cudaStream_t s) {
+                         const Plan& p, void* ws, cudaStream_t s, bool b_after_wait = false) {
   switch (p.bn) {
-    case 256: return launch_bf16<256, F32OUT>(ta, tb, d, p, ws, s);
-    case 192: return launch_bf16<192, F32OUT>(ta, tb, d, p, ws, s);
-    case 128: return launch_bf16<128, F32OUT>(ta, tb, d, p, ws, s);
-    default: return launch_bf16<64, F32OUT>(ta, tb, d, p, ws, s);
+    case 256: return launch_bf16<256, F32OUT>(ta, tb, d, p, ws, s, b_after_wait);
+    case 192: return launch_bf16<192, F32OUT>(ta, tb, d, p, ws, s, b_after_wait);
+    case 128: return launch_bf16<128, F32OUT>(ta, tb, d, p, ws, s, b_after_wait);
+    default: return launch_bf16<64, F32OUT>(ta, tb, d, p, ws, s, b_after_wait);
   }
 }
 
@@ -832,12 +1100,154 @@ biv_status validate(const biv_gemm_desc* d) {
   return BIV_OK;
 }
 
+// The bf16 call that biv_gemm_nvfp4 matches bit for bit (B decoded to bf16).
+biv_gemm_desc nvfp4_as_bf16(const uint16_t* A, int64_t lda, const uint16_t* Bdec, int M, int N,
+                            int K, void* C, int64_t ldc, int c_dtype, int mode) {
+  biv_gemm_desc d;
+  memset(&d, 0, sizeof(d));
+  d.M = M; d.N = N; d.K = K;
+  d.a_dtype = d.b_dtype = BIV_BF16;
+  d.c_dtype = c_dtype;
+  d.A = A; d.lda = lda;
+  d.B = Bdec; d.ldb = K;
+  d.C = C; d.ldc = ldc;
+  d.mode = mode;
+  return d;
+}
+
+struct Fp4Plan {
+  Plan p;              // the bf16 plan of the same shape
+  bool native = false; // NVFP4 partial kernel (else: decode, then the bf16 GEMM)
+  int stages = 0;
+  size_t dec_bytes = 0, ws_bytes = 0;
+};
+
+Fp4Plan plan_nvfp4(const biv_gemm_desc& d) {
+  Fp4Plan f;
+  f.p = plan_bf16(d);
+  // the native kernel reads 16-byte scale groups by TMA: rows of K/16 bytes
+  // must be whole 16-byte units.  It runs every weight-streaming shape (at
+  // most kPartialRows rows) as partials, also those whose bf16 plan folds in
+  // the CTA (wide N, e.g. an LM head): partial and in-CTA fold give the same
+  // bits, and only the native kernel reads 4-bit weights.
+  const bool stream_rows = d.M <= kPartialRows && d.mode == BIV_MODE_INVARIANT;
+  f.native = d.K % 256 == 0 && ((f.p.partial && f.p.bn == 128) || stream_rows);
+  if (f.native && !(f.p.partial && f.p.bn == 128)) {
+    const int64_t tiles_m = (d.M + BM - 1) / BM;
+    f.p.partial = true;
+    f.p.bn = 128;
+    f.p.tiles = int64_t((d.N + 127) / 128) * tiles_m;
+    f.p.ldp = int64_t((d.N + 127) / 128) * 128;
+    f.p.ws_bytes = size_t(f.p.chunks) * d.M * f.p.ldp * sizeof(float);
+  }
+  if (f.native) {
+    const size_t per = size_t(f.p.m_box) * 128 + kFp4CodeBytes + kFp4SclBytes;
+    f.stages = int(std::min<size_t>(kFp4MaxRaw, (kSmemBudget - fp4_smem_bytes(0, f.p.m_box)) / per));
+    f.ws_bytes = f.p.ws_bytes;
+  } else {
+    f.dec_bytes = (size_t(d.N) * d.K * 2 + 255) / 256 * 256;
+    f.ws_bytes = f.dec_bytes + f.p.ws_bytes;
+  }
+  return f;
+}
+
 }  // namespace
 }  // namespace biv
 
 using namespace biv;
 
 extern "C" {
+
+biv_status biv_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, int N, int K,
+                             uint16_t* out, biv_stream_t stream);
+
+static biv_status nvfp4_check(const uint16_t* A, int64_t lda, const uint8_t* codes,
+                              const uint8_t* scales, int M, int N, int K, const void* C,
+                              int64_t ldc, int c_dtype, int mode) {
+  BIV_REQUIRE(M >= 0 && N > 0 && K > 0 && K % 16 == 0,
+              "gemm_nvfp4: K=%d must be a multiple of 16", K);
+  BIV_REQUIRE(c_dtype == BIV_BF16 || c_dtype == BIV_F32, "gemm_nvfp4: C is bf16 or f32");
+  BIV_REQUIRE(mode == BIV_MODE_INVARIANT || mode == BIV_MODE_FAST, "gemm_nvfp4: bad mode");
+  if (M == 0) return BIV_OK;
+  BIV_REQUIRE(A && codes && scales && C && aligned16(A) && aligned16(codes) && aligned16(scales) &&
+                  aligned16(C) && lda >= K && (lda * 2) % 16 == 0 && ldc >= N,
+              "gemm_nvfp4: null or misaligned operand");
+  return BIV_OK;
+}
+
+biv_status biv_gemm_nvfp4_workspace(int M, int N, int K, int c_dtype, int mode, size_t* bytes) {
+  BIV_REQUIRE(bytes, "gemm_nvfp4_workspace: null output");
+  BIV_REQUIRE(M >= 0 && N > 0 && K > 0 && K % 16 == 0, "gemm_nvfp4: K must be a multiple of 16");
+  BIV_REQUIRE(c_dtype == BIV_BF16 || c_dtype == BIV_F32, "gemm_nvfp4: C is bf16 or f32");
+  const biv_gemm_desc d = nvfp4_as_bf16(nullptr, K, nullptr, M, N, K, nullptr, N, c_dtype, mode);
+  *bytes = M == 0 ? 0 : plan_nvfp4(d).ws_bytes;
+  return BIV_OK;
+}
+
+biv_status biv_gemm_nvfp4(const uint16_t* A, int64_t lda, const uint8_t* codes,
+                          const uint8_t* scales, int M, int N, int K, void* C, int64_t ldc,
+                          int c_dtype, int mode, void* ws, size_t ws_bytes, biv_stream_t stream) {
+  biv_status st = nvfp4_check(A, lda, codes, scales, M, N, K, C, ldc, c_dtype, mode);
+  if (st != BIV_OK || M == 0) return st;
+  biv_gemm_desc d = nvfp4_as_bf16(A, lda, nullptr, M, N, K, C, ldc, c_dtype, mode);
+  const Fp4Plan f = plan_nvfp4(d);
+  if (f.ws_bytes && (!ws || ws_bytes < f.ws_bytes || !aligned16(ws)))
+    return set_error(BIV_ERR_WORKSPACE, "gemm_nvfp4: 16-byte aligned workspace of %zu bytes needed",
+                     f.ws_bytes);
+  cudaStream_t s = as_cuda(stream);
+  if (!f.native) {
+    // many rows: decode the weights once, then the bf16 GEMM (compute-bound
+    // here), its own partials after the decoded weights
+    uint16_t* dec = static_cast<uint16_t*>(ws);
+    st = biv_nvfp4_dequant(codes, scales, N, K, dec, stream);
+    if (st != BIV_OK) return st;
+    d.B = dec;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, f.p.m_box) ||
+        !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dec, K, N, K, 64, f.p.bn))
+      return set_error(BIV_ERR_CUDA, "gemm_nvfp4: tensor map encoding failed");
+    // the decoded weights come from the kernel just before: no early B prefetch
+    void* pws = static_cast<uint8_t*>(ws) + f.dec_bytes;
+    return c_dtype == BIV_F32 ? dispatch_bf16<true>(ta, tb, d, f.p, pws, s, true)
+                              : dispatch_bf16<false>(ta, tb, d, f.p, pws, s, true);
+  }
+  const Plan& p = f.p;
+  CUtensorMap ta, tc, ts;
+  if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, p.m_box) ||
+      !make_map(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, codes, K / 2, N, K / 2, 32, 128, false) ||
+      !make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, scales, K / 16, N, K / 16, 16, 128, false))
+    return set_error(BIV_ERR_CUDA, "gemm_nvfp4: tensor map encoding failed");
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSmemBudget)) != cudaSuccess)
+      return set_error(BIV_ERR_CUDA, "gemm_nvfp4: cannot set shared memory size");
+    attr = true;
+  }
+  const int eb = c_dtype == BIV_F32 ? 4 : 2;
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.C = C; a.ldc = ldc; a.M = M; a.N = N; a.K = K;
+  a.kc_blocks = p.kc_blocks; a.m_box = p.m_box; a.stages = f.stages; a.partial = 1;
+  a.ws = static_cast<float*>(ws); a.ldp = p.ldp;
+  a.vec_ok = aligned16(C) && (ldc * eb) % 16 == 0;
+  a.err = device_error_word();
+  const int64_t items = p.tiles * p.chunks;
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  launch_pdl(gemm_nvfp4_kernel, int(std::min<int64_t>(items, sms)), kFp4Threads,
+             fp4_smem_bytes(f.stages, p.m_box), s, ta, tc, ts, a);
+  st = check_launch("gemm_nvfp4");
+  if (st != BIV_OK) return st;
+  const int64_t groups = int64_t(M) * ((N + 3) / 4);
+  const int blocks = int(std::min<int64_t>((groups + 255) / 256, int64_t(sms) * 8));
+  if (c_dtype == BIV_F32)
+    launch_pdl(gemm_fold_kernel<true>, blocks, 256, 0, s, static_cast<const float*>(ws), C, ldc, M,
+               N, p.ldp, p.chunks, a.vec_ok);
+  else
+    launch_pdl(gemm_fold_kernel<false>, blocks, 256, 0, s, static_cast<const float*>(ws), C, ldc, M,
+               N, p.ldp, p.chunks, a.vec_ok);
+  return check_launch("gemm_nvfp4_fold");
+}
 
 biv_status biv_gemm_workspace(const biv_gemm_desc* d, size_t* bytes) {
   biv_status st = validate(d);

@@ -16,7 +16,8 @@
 //  * gated RMSNorm: g = y * silu(z) in FP32, out = bf16((g * inv) * w) with
 //    the same per-row reduction tree as the other norms (256 threads, per
 //    thread in chunk order, warp xor tree, warps in order).
-//  * NVFP4 decode: e2m1 code times its block's e4m3 scale, exact in bf16.
+//  * NVFP4 decode: packed e2m1 codes times their block's e4m3 scale, exact in
+//    bf16 (the same conversion the NVFP4 GEMM runs in shared memory).
 #include "common.cuh"
 
 namespace biv {
@@ -200,14 +201,9 @@ __global__ void __launch_bounds__(kGNThreads) gated_rmsnorm_kernel(
 }
 
 // ------------------------------------------------------------ NVFP4 ----
-// e2m1: sign bit 3, exponent bits 2-1 (bias 1), mantissa bit 0
-__device__ __forceinline__ float e2m1f(uint32_t c) {
-  const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
-  const float v = mag[c & 7u];
-  return (c & 8u) ? -v : v;
-}
-
-// one thread per 16-element block (one scale): 16 codes in, 16 bf16 out
+// one thread per 16-element block: 8 bytes of packed e2m1 codes (element 2i in
+// the low nibble of byte i) and the block's e4m3 scale -> 16 bf16 values.
+// e2m1 x e4m3 has at most 6 significant bits: exact in f16 and in bf16.
 __global__ void nvfp4_dequant_kernel(const uint8_t* __restrict__ codes,
                                      const uint8_t* __restrict__ scales, int N, int K,
                                      uint16_t* __restrict__ out) {
@@ -217,19 +213,24 @@ __global__ void nvfp4_dequant_kernel(const uint8_t* __restrict__ codes,
        e += int64_t(gridDim.x) * blockDim.x) {
     const int64_t n = e / kb;
     const int b = int(e % kb);
-    const float s = e4m32f(scales[n * kb + b]);
-    const uint4 cv = *reinterpret_cast<const uint4*>(codes + n * K + b * 16);
-    const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
-    float f[16];
+    const __half s = __ushort_as_half(
+        __nv_cvt_fp8_to_halfraw(__nv_fp8_storage_t(scales[n * kb + b]), __NV_E4M3).x);
+    const __half2 s2 = __halves2half2(s, s);
+    const uint2 cv = *reinterpret_cast<const uint2*>(codes + n * (K / 2) + b * 8);
+    const uint32_t w[2] = {cv.x, cv.y};
+    uint32_t o[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) f[4 * q + j] = e2m1f((w[q] >> (8 * j)) & 0xFFu) * s;
+      for (int j = 0; j < 4; ++j) {
+        const __half2_raw hr =
+            __nv_cvt_fp4x2_to_halfraw2(__nv_fp4x2_storage_t((w[q] >> (8 * j)) & 0xFFu), __NV_E2M1);
+        const float2 f = __half22float2(__hmul2(__half2(hr), s2));
+        o[4 * q + j] = pack_bf2(f.x, f.y);
+      }
     uint4* dst = reinterpret_cast<uint4*>(out + n * K + b * 16);
-    dst[0] = make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]),
-                        pack_bf2(f[6], f[7]));
-    dst[1] = make_uint4(pack_bf2(f[8], f[9]), pack_bf2(f[10], f[11]), pack_bf2(f[12], f[13]),
-                        pack_bf2(f[14], f[15]));
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
 }
 
@@ -308,7 +309,7 @@ biv_status biv_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, int N,
   BIV_REQUIRE(N >= 0 && K > 0 && K % 16 == 0, "nvfp4_dequant: K=%d must be a multiple of 16", K);
   if (N == 0) return BIV_OK;
   BIV_REQUIRE(codes && scales && out && aligned16(codes) && aligned16(out),
-              "nvfp4_dequant: pointers must be 16-byte aligned");
+              "nvfp4_dequant: codes and out must be 16-byte aligned");
   nvfp4_dequant_kernel<<<grid_of(int64_t(N) * (K / 16), 256), 256, 0, as_cuda(stream)>>>(
       codes, scales, N, K, out);
   return check_launch("nvfp4_dequant");

@@ -10,8 +10,10 @@ chunked SSD whose rows are computed from their chunk's start state and rows
 (prefill, chunked prefill and decode take one code path).  The attention
 mixers are the dense model's paged attention (RoPE, no QK-norm).  Every
 mixer is followed by a SiLU-gated MLP; norms are pre-norm with the residual
-add fused.  NVFP4 weights are decoded once, at load, to their exact bf16
-values by ``biv_nvfp4_dequant``.
+add fused.  Linear layers keep their NVFP4 weights (packed e2m1 codes and
+e4m3 block scales) on the device and run through ``biv_gemm_nvfp4``, whose
+every output bit equals the bf16 GEMM on the decoded weights: decode-sized
+steps stream the 4-bit codes, prefill-sized steps decode once per call.
 
 PyTorch holds device memory and streams; every arithmetic step runs in libbiv.
 """
@@ -40,13 +42,10 @@ class HybridModel:
         bf = dict(dtype=torch.bfloat16, device=device)
         f32 = dict(dtype=torch.float32, device=device)
         i32 = dict(dtype=torch.int32, device=device)
-        self.W: Dict[str, torch.Tensor] = {}
+        self.W: Dict[str, object] = {}
         for k, v in weights.items():
-            if isinstance(v, tuple):
-                codes, sc = v[0].to(device).contiguous(), v[1].to(device).contiguous()
-                out = torch.empty(codes.shape, **bf)
-                biv.biv_nvfp4_dequant(codes, sc, out)
-                self.W[k] = out
+            if isinstance(v, tuple):      # NVFP4: (packed codes [N, K/2], scales [N, K/16])
+                self.W[k] = (v[0].to(device).contiguous(), v[1].to(device).contiguous())
             else:
                 self.W[k] = v.to(device).contiguous()
         D, T = cfg.head_dim, max_rows
@@ -153,9 +152,16 @@ class HybridModel:
 
     # -- ops -------------------------------------------------------------------
     def _gemm(self, A, Bw, Cout, M, st):
-        d = biv.gemm_desc(A, Bw, Cout, mode=self.mode, M=M)
-        ws = self._grow("gws", biv.biv_gemm_workspace(d))
-        biv.biv_gemm(d, ws, stream=st)
+        if isinstance(Bw, tuple):
+            codes, sc = Bw
+            cdt = biv.F32 if Cout.dtype == torch.float32 else biv.BF16
+            ws = self._grow("gws", biv.biv_gemm_nvfp4_workspace(M, codes.shape[0], A.shape[1], cdt,
+                                                               self.mode))
+            biv.biv_gemm_nvfp4(A, codes, sc, Cout, M=M, mode=self.mode, ws=ws, stream=st)
+        else:
+            d = biv.gemm_desc(A, Bw, Cout, mode=self.mode, M=M)
+            ws = self._grow("gws", biv.biv_gemm_workspace(d))
+            biv.biv_gemm(d, ws, stream=st)
         self.launches += 1
 
     def _mamba(self, l, T, spec, st):

@@ -16,7 +16,8 @@ Each case times REPS calls with CUDA events after one warm-up call and
 prints the time and the rate against the case's algorithmic bytes or FLOPs;
 it is also the command that the ncu summaries in profiles/ capture.
 
-Further cases: gemm_sweep (the decoder GEMMs over decode batch sizes, weights
+Further cases: gemm_nvfp4 (the hybrid unit's linear layers at M = 1, 16, 64
+with NVFP4 weights against the same GEMM on bf16 weights), gemm_sweep (the decoder GEMMs over decode batch sizes, weights
 rotated through copies larger than L2; BIV_BENCH_MS lists the M values,
 BIV_BENCH_SHAPES the GEMMs, BIV_BENCH_DEFER=1 times the GEMM kernel alone
 when it leaves chunk partials to the consumer op) and gemm_prefill_layer (the
@@ -206,6 +207,34 @@ elif case.startswith("attn"):
     kv_bytes = B * ctx * Hkv * (D * (1 if fp8 else 2) + (4 if fp8 else 0)) * 2
     flops = 4.0 * sum(p + 1 for _, p in rows) * Hq * D
     print(f"{case}: {ms*1e3:.1f} us  KV {kv_bytes/1e6:.0f} MB -> {kv_bytes/(ms/1e3)/1e9:.0f} GB/s;  {flops/(ms/1e3)/1e12:.1f} TFLOP/s")
+elif case == "gemm_nvfp4":
+    # the hybrid unit's linear layers at decode batch sizes: NVFP4 weights
+    # (4-bit codes decoded in shared memory) against the same GEMM on bf16
+    # weights; weights rotate through copies larger than L2
+    shapes = {"in_proj": (8512, 2560), "out_proj": (2560, 4096), "gate_up": (13824, 2560),
+              "down": (2560, 6912), "lm_head": (131072, 2560)}
+    if os.environ.get("BIV_BENCH_SHAPES"):
+        shapes = {k: shapes[k] for k in os.environ["BIV_BENCH_SHAPES"].split(",")}
+    ms_list = [int(x) for x in os.environ.get("BIV_BENCH_MS", "1,16,64").split(",")]
+    gg = synth.device_generator(1)
+    for name, (N, K) in shapes.items():
+        copies = max(1, -(-300_000_000 // (N * K // 2)))
+        ws4 = [synth.device_nvfp4_weights(gg, N, K) for _ in range(copies)]
+        wb = torch.empty(N, K, dtype=torch.bfloat16, device="cuda")
+        biv.biv_nvfp4_dequant(ws4[0][0], ws4[0][1], wb)
+        wbs = [wb] + [wb.clone() for _ in range(max(0, -(-300_000_000 // (N * K * 2)) - 1))]
+        for M in ms_list:
+            a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+            c = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+            n4 = len(ws4) * max(1, 8 // len(ws4))
+            t4 = graph_time(lambda: [biv.biv_gemm_nvfp4(a, *ws4[i % len(ws4)], c) for i in range(n4)], 1) / n4
+            ds = [biv.gemm_desc(a, w, c) for w in wbs]
+            nb = len(ds) * max(1, 8 // len(ds))
+            tb = graph_time(lambda: [biv.biv_gemm(ds[i % len(ds)]) for i in range(nb)], 1) / nb
+            print(f"{name:8s} M={M:3d} N={N:6d} K={K}: nvfp4 {t4*1e3:7.1f} us "
+                  f"({N*K*0.5625/(t4/1e3)/1e9:5.0f} GB/s)  bf16 {tb*1e3:7.1f} us "
+                  f"({N*K*2/(tb/1e3)/1e9:5.0f} GB/s)", flush=True)
+        del ws4, wbs
 elif case == "gemm_prefill_layer":
     # the four decoder-layer GEMMs at a 16384-row prefill step
     M = 16384

@@ -107,13 +107,24 @@ def e2m1_to_f32(codes: np.ndarray) -> np.ndarray:
     return E2M1_TABLE[np.asarray(codes, dtype=np.uint8) & 0xF].astype(np.float32)
 
 
-def nvfp4_dequant(codes: np.ndarray, scale_codes: np.ndarray, block: int = 16) -> np.ndarray:
-    """NVFP4 weights [N, K]: e2m1 codes [N, K] times one e4m3 scale per block
-    of 16 consecutive K elements (scale codes [N, K/16]), global scale 1.
+def nvfp4_unpack(packed: np.ndarray) -> np.ndarray:
+    """Packed NVFP4 codes [N, K/2] -> one e2m1 code per element [N, K]:
+    element 2i is the low nibble of byte i, element 2i+1 the high nibble."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def nvfp4_dequant(packed: np.ndarray, scale_codes: np.ndarray, block: int = 16) -> np.ndarray:
+    """NVFP4 weights [N, K]: packed e2m1 codes [N, K/2] (nvfp4_unpack) times
+    one e4m3 scale per block of 16 consecutive K elements (scale codes
+    [N, K/16]), global scale 1.
     A 2-significant-bit value times a 4-significant-bit scale has at most 6
     significant bits, so the product is exact in FP32 and lies on the bf16
     grid (unless it leaves bf16's exponent range, which e4m3 scales cannot
     reach)."""
-    v = e2m1_to_f32(codes).astype(np.float64)
+    v = e2m1_to_f32(nvfp4_unpack(packed)).astype(np.float64)
     s = np.repeat(e4m3_to_f32(scale_codes).astype(np.float64), block, axis=-1)[..., :v.shape[-1]]
     return (v * s).astype(np.float32)

@@ -357,15 +357,18 @@ _E2M1_MAG_P = np.array([0.12, 0.22, 0.20, 0.16, 0.12, 0.10, 0.05, 0.03])
 
 
 def nvfp4_weights(g: np.random.Generator, n: int, k: int):
-    """NVFP4 weights drawn as codes: e2m1 codes uint8 [n, k] (one code per
-    byte, values 0..15) and e4m3 scale codes uint8 [n, ceil(k/16)] drawn
-    uniformly from 0x04..0x0F (scales 2^-7 .. 1.875 * 2^-6, so code x scale
-    has an RMS near 0.03).  No quantisation happens here: each side decodes
-    the codes with its own codec."""
+    """NVFP4 weights drawn as codes, in the packed storage: e2m1 codes uint8
+    [n, k/2] (two per byte, element 2i in the low nibble of byte i) and e4m3
+    scale codes uint8 [n, k/16] drawn uniformly from 0x04..0x0F (scales 2^-7 ..
+    1.875 * 2^-6, so code x scale has an RMS near 0.03).  No quantisation
+    happens here: each side decodes the codes with its own codec.  k is a
+    multiple of 16."""
     mag = g.choice(8, size=(n, k), p=_E2M1_MAG_P).astype(np.uint8)
     sign = (g.random(size=(n, k)) < 0.5).astype(np.uint8) << 3
-    sc = g.integers(0x04, 0x10, size=(n, (k + 15) // 16)).astype(np.uint8)
-    return torch.from_numpy(mag | sign), torch.from_numpy(sc)
+    c = mag | sign
+    packed = (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+    sc = g.integers(0x04, 0x10, size=(n, k // 16)).astype(np.uint8)
+    return torch.from_numpy(packed), torch.from_numpy(sc)
 
 
 def hybrid_weights(cfg: HybridConfig, seed: int = 0, random_gains: bool = False,
@@ -442,16 +445,18 @@ def host_payload(W: Dict[str, object]) -> Dict[str, object]:
 
 
 def device_nvfp4_weights(gen: torch.Generator, n: int, k: int):
-    """The recipe of ``nvfp4_weights`` drawn on the device: e2m1 magnitudes
-    from the same categorical distribution (a uniform draw located in its
-    cumulative probabilities), a fair sign bit, e4m3 scale codes uniform over
-    0x04..0x0F."""
+    """The recipe of ``nvfp4_weights`` drawn on the device (packed the same
+    way): e2m1 magnitudes from the same categorical distribution (a uniform
+    draw located in its cumulative probabilities), a fair sign bit, e4m3 scale
+    codes uniform over 0x04..0x0F."""
     dev = gen.device
     cdf = torch.tensor(np.cumsum(_E2M1_MAG_P)[:-1], dtype=torch.float32, device=dev)
     mag = torch.searchsorted(cdf, torch.rand(n, k, generator=gen, device=dev), right=True)
     sign = (torch.rand(n, k, generator=gen, device=dev) < 0.5).to(torch.uint8) << 3
-    sc = torch.randint(0x04, 0x10, (n, (k + 15) // 16), generator=gen, device=dev, dtype=torch.uint8)
-    return (mag.to(torch.uint8) | sign), sc
+    c = mag.to(torch.uint8) | sign
+    packed = c[:, 0::2] | (c[:, 1::2] << 4)
+    sc = torch.randint(0x04, 0x10, (n, k // 16), generator=gen, device=dev, dtype=torch.uint8)
+    return packed.contiguous(), sc
 
 
 def device_hybrid_weights(cfg: HybridConfig, seed: int = 0) -> Dict[str, object]:

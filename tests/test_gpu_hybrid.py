@@ -47,10 +47,41 @@ def test_nvfp4_dequant_bit_exact(B):
     g = synth.rng(1)
     codes, sc = synth.nvfp4_weights(g, 300, 4096)
     sc[:, :3] = torch.tensor([0x00, 0x7E, 0x01], dtype=torch.uint8)   # zero, 448, smallest subnormal
+    codes[0, :8] = torch.tensor([0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE], dtype=torch.uint8)
     out = torch.empty(300, 4096, dtype=torch.bfloat16, device="cuda")
     B.biv_nvfp4_dequant(codes.cuda(), sc.cuda(), out)
     torch.cuda.synchronize()
     assert np.array_equal(h32(out), nvfp4_dequant(codes.numpy(), sc.numpy()))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8512, 2560), (3, 2560, 4096), (64, 13824, 2560),
+                                   (16, 2560, 6912), (1, 4096, 256), (200, 2560, 2560),
+                                   (1024, 3200, 2560), (5, 256, 320)])
+def test_gemm_nvfp4_bitwise_equals_bf16_gemm_on_decoded_weights(B, M, N, K):
+    """The NVFP4 GEMM (4-bit codes streamed and decoded in shared memory for
+    decode-sized M; decode-then-bf16 for many rows) gives every bit of
+    biv_gemm on the bf16 weights that biv_nvfp4_dequant produces, for bf16
+    and f32 outputs, and a row alone has its bits in the batch."""
+    g = synth.rng(M * 7 + N + K)
+    codes, sc = synth.nvfp4_weights(g, N, K)
+    cd, sd = codes.cuda(), sc.cuda()
+    a = synth.normal_bf16(g, (M, K)).cuda()
+    w = torch.empty(N, K, dtype=torch.bfloat16, device="cuda")
+    B.biv_nvfp4_dequant(cd, sd, w)
+    for dt in (torch.bfloat16, torch.float32):
+        ref = torch.empty(M, N, dtype=dt, device="cuda")
+        B.biv_gemm(B.gemm_desc(a, w, ref))
+        got = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
+        B.biv_gemm_nvfp4(a, cd, sd, got)
+        B.biv_gemm_nvfp4(a, cd, sd, got)          # twice: the workspace needs no initial value
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(got), bits(ref)), dt
+    one = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
+    B.biv_gemm_nvfp4(a[M // 2:M // 2 + 1], cd, sd, one)
+    full = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    B.biv_gemm_nvfp4(a, cd, sd, full)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(one), bits(full[M // 2:M // 2 + 1]))
 
 
 def _conv_call(B, u, col_x, col_dt, ch, H, w, b, dtb, out, dt, rows_of, state):
@@ -205,7 +236,8 @@ def test_hybrid_save_reload_then_next_decode_step(B):
     for p in range(250, 253):
         step(m, kv, [p, p])
     torch.cuda.synchronize()
-    host_w = {k: v.cpu().clone() for k, v in m.W.items()}
+    host_w = {k: tuple(t.cpu().clone() for t in v) if isinstance(v, tuple) else v.cpu().clone()
+              for k, v in m.W.items()}
     host_state = {l: {k: t.cpu().clone() for k, t in st.items()} for l, st in m.mstate.items()}
     host_kv = (kv.k.cpu().clone(), kv.v.cpu().clone(), kv.bt_host.copy(),
                {k: list(v) for k, v in kv.owned.items()}, list(kv.free))

@@ -24,21 +24,28 @@ def test_e2m1_table_is_the_ocp_fp4_grid():
     assert np.signbit(v[8])                       # code 8 is -0
 
 
-def test_nvfp4_dequant_blocks_and_bf16_exactness():
+def _pack(codes):
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
+def test_nvfp4_dequant_blocks_packing_and_bf16_exactness():
     g = np.random.default_rng(0)
     codes = g.integers(0, 16, size=(5, 48)).astype(np.uint8)
     sc = g.integers(0, 0x7F, size=(5, 3)).astype(np.uint8)
-    w = nvfp4_dequant(codes, sc)
+    w = nvfp4_dequant(_pack(codes), sc)
     assert np.array_equal(bf16_round(w), w)        # on the bf16 grid
-    # element (n, k) uses the scale of its own block of 16 along k
+    # element (n, k) uses its own code and the scale of its block of 16 along k
     for n in range(5):
         for k in range(48):
             assert w[n, k] == F32(e2m1_to_f32(codes[n, k]) * e4m3_to_f32(sc[n, k // 16]))
-    # one-hot codes fix the block index: value 1.0 (code 2) at k = 17 picks scale 1
+    # one-hot codes fix the block index and the nibble order: value 1.0
+    # (code 2) at k = 17 (high nibble of byte 8) picks scale 1
     c1 = np.zeros((1, 48), np.uint8)
     c1[0, 17] = 2
+    assert _pack(c1)[0, 8] == 0x20
     s1 = np.array([[0x38, 0x40, 0x48]], np.uint8)   # 1.0, 2.0, 4.0
-    assert nvfp4_dequant(c1, s1)[0, 17] == 2.0
+    d1 = nvfp4_dequant(_pack(c1), s1)
+    assert d1[0, 17] == 2.0 and np.count_nonzero(d1) == 1
 
 
 def test_softplus_against_logaddexp():
