@@ -48,11 +48,13 @@ struct AttnCfg {
   static constexpr int NV = DS > 1 ? 16 : NW * 16;   // query vectors per CTA
   static constexpr int NT = NW * 32;                 // threads per CTA
   static constexpr int KVB = TMA ? kTile * D * 2 : kTile * LD * 2;  // one K or V stage
+  // bf16 K/V tile stages: FP8 keeps one (its staging area holds the prefetch)
+  static constexpr int TST = F8 ? 1 : ST;
   static constexpr int Q_BYTES = NV * LD * 2;
   static constexpr int F8_CODES = F8 ? 2 * kTile * D : 0;          // K then V codes
   static constexpr int F8_STAGE = F8 ? F8_CODES + 2 * kTile * 4 : 0;  // + K then V scales
   static constexpr int SMEM =
-      1024 + 2 * ST * KVB + Q_BYTES + ST * F8_STAGE + ST * kTile * 4 + 2 * ST * 8;
+      1024 + 2 * TST * KVB + Q_BYTES + ST * F8_STAGE + ST * kTile * 4 + 2 * ST * 8;
   static constexpr int DK = D / 16;                  // k-steps of Q.K^T
   static constexpr int DT = D / 8;                   // n-tiles of O
   static constexpr int DTW = DT / DS;                // n-tiles of O per warp
@@ -167,10 +169,11 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sK = base;                                   // [ST] stages of KVB bytes
-  uint8_t* sV = base + ST * KVB;
-  uint16_t* sQ = reinterpret_cast<uint16_t*>(base + 2 * ST * KVB);
-  uint8_t* sF8 = base + 2 * ST * KVB + Cfg::Q_BYTES;    // [ST] FP8 staging (F8 only)
+  constexpr int TST = Cfg::TST;
+  uint8_t* sK = base;                                   // [TST] stages of KVB bytes
+  uint8_t* sV = base + TST * KVB;
+  uint16_t* sQ = reinterpret_cast<uint16_t*>(base + 2 * TST * KVB);
+  uint8_t* sF8 = base + 2 * TST * KVB + Cfg::Q_BYTES;   // [ST] FP8 staging (F8 only)
   int32_t* sPos = reinterpret_cast<int32_t*>(sF8 + ST * Cfg::F8_STAGE);  // [ST][64]
   // TMA: K of stage s completes on bars[s], V on bars[ST + s], so that K of
   // the next tile streams in while this tile's softmax and P.V run
@@ -264,8 +267,8 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
       pos_buf[j] = p;
     }
     __syncthreads();
-    uint8_t* dK = sK + buf * KVB;
-    uint8_t* dV = sV + buf * KVB;
+    uint8_t* dK = sK + (buf % TST) * KVB;
+    uint8_t* dV = sV + (buf % TST) * KVB;
     if constexpr (!F8) {
       constexpr int CPR = D / 8;
       for (int i = tid; i < kTile * CPR * 2; i += NT) {
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
         packed[2 * q] = pack_bf2(f01.x * sc, f01.y * sc);
         packed[2 * q + 1] = pack_bf2(f23.x * sc, f23.y * sc);
       }
-      uint8_t* dst = (which ? sV : sK) + buf * KVB;
+      uint8_t* dst = (which ? sV : sK) + (buf % TST) * KVB;
       *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16)) =
           make_uint4(packed[0], packed[1], packed[2], packed[3]);
       *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16 + 8)) =
@@ -395,8 +398,8 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     }
     // a warp with no live vector only takes part in the loads and barriers
     const bool live = vw * 16 < nv;
-    const uint32_t tK = smem_u32(sK + buf * KVB);
-    const uint32_t tV = smem_u32(sV + buf * KVB);
+    const uint32_t tK = smem_u32(sK + (buf % TST) * KVB);
+    const uint32_t tV = smem_u32(sV + (buf % TST) * KVB);
     const int32_t* tP = sPos + buf * kTile;
 
     // S = Q . K^T  (16 x 64 per warp)
