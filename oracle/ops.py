@@ -17,19 +17,24 @@ F32 = np.float32
 
 # How the oracle forms a dot product.  "f64" (the default): in float64, rounded
 # once to FP32, so the result does not depend on how a library blocks the sum.
-# "f32": plain FP32 in ascending k, every product and every partial sum
-# rounded to FP32 -- the textbook order.  Both are correct FP32 evaluations of
-# the same definition; the second exists to measure how far two correct
-# evaluations drift apart through a deep model (the spread script in this
-# package), which bounds what any implementation can promise against either.
+# The others are plain FP32 evaluations of the same sums: "f32" in ascending
+# k and "f32_desc" in descending k, every product and every partial sum
+# rounded to FP32 (nearest), "f32_rz" in ascending k with every partial sum
+# rounded toward zero (IEEE's directed rounding; tensor-core accumulators
+# truncate in this way), and "f32_blas" the FP32 library matmul with its own
+# blocking.  All are correct FP32 evaluations of the same definition; the
+# alternatives exist to measure how far correct evaluations drift apart
+# through a deep model (tests/golden/make_accumulation_spread.py), which
+# bounds what any implementation can promise against the default.
 _ACCUMULATION = ["f64"]
+KINDS = ("f64", "f32", "f32_desc", "f32_rz", "f32_blas")
 
 
 @contextlib.contextmanager
 def accumulation(kind: str):
     """Run the enclosed oracle calls with dot products formed as ``kind``
-    ("f64" or "f32")."""
-    if kind not in ("f64", "f32"):
+    (one of KINDS)."""
+    if kind not in KINDS:
         raise ValueError(kind)
     prev = _ACCUMULATION[0]
     _ACCUMULATION[0] = kind
@@ -39,22 +44,51 @@ def accumulation(kind: str):
         _ACCUMULATION[0] = prev
 
 
-def _dot_f32_ascending(a: np.ndarray, bt: np.ndarray) -> np.ndarray:
-    """acc = 0; for k = 0, 1, ...: acc = fp32(acc + fp32(a[:, k] * bt[k, :]))."""
+def _dot_f32_sequential(a: np.ndarray, bt: np.ndarray, descending: bool = False) -> np.ndarray:
+    """acc = 0; for k = 0, 1, ... (or K-1, K-2, ...):
+    acc = fp32(acc + fp32(a[:, k] * bt[k, :]))."""
+    a = np.ascontiguousarray(np.asarray(a, F32).T)
+    bt = np.ascontiguousarray(bt, F32)
+    acc = np.zeros((a.shape[1], bt.shape[1]), F32)
+    ks = range(a.shape[0] - 1, -1, -1) if descending else range(a.shape[0])
+    for k in ks:
+        acc += a[k][:, None] * bt[k][None, :]
+    return acc
+
+
+def _to_f32_toward_zero(x: np.ndarray) -> np.ndarray:
+    """float64 -> float32 rounded toward zero: clear the 29 low mantissa bits
+    (exact for normal float32 results, which is all a dot product of bf16
+    values produces here)."""
+    u = np.ascontiguousarray(x, np.float64).view(np.uint64) & np.uint64(0xFFFFFFFFE0000000)
+    return u.view(np.float64).astype(F32)
+
+
+def _dot_f32_rz(a: np.ndarray, bt: np.ndarray) -> np.ndarray:
+    """acc = 0; for k ascending: acc = rz32(acc + fp32(a[:, k] * bt[k, :])),
+    the sum formed exactly in float64 (two FP32 values) then truncated."""
     a = np.ascontiguousarray(np.asarray(a, F32).T)
     bt = np.ascontiguousarray(bt, F32)
     acc = np.zeros((a.shape[1], bt.shape[1]), F32)
     for k in range(a.shape[0]):
-        acc += a[k][:, None] * bt[k][None, :]
+        prod = a[k][:, None] * bt[k][None, :]
+        acc = _to_f32_toward_zero(acc.astype(np.float64) + prod.astype(np.float64))
     return acc
 
 
 # ----------------------------------------------------------------- GEMM ----
 def dot_f32(a: np.ndarray, bt: np.ndarray) -> np.ndarray:
-    """a @ bt as FP32 values: float64 accumulation rounded once to FP32, or
-    (inside ``accumulation("f32")``) plain FP32 accumulation in ascending k."""
-    if _ACCUMULATION[0] == "f32":
-        return _dot_f32_ascending(a, bt)
+    """a @ bt as FP32 values: float64 accumulation rounded once to FP32, or,
+    inside ``accumulation(kind)``, one of the plain FP32 orders."""
+    kind = _ACCUMULATION[0]
+    if kind == "f32":
+        return _dot_f32_sequential(a, bt)
+    if kind == "f32_desc":
+        return _dot_f32_sequential(a, bt, descending=True)
+    if kind == "f32_rz":
+        return _dot_f32_rz(a, bt)
+    if kind == "f32_blas":
+        return np.matmul(np.asarray(a, F32), np.asarray(bt, F32))
     return np.matmul(np.asarray(a, np.float64), np.asarray(bt, np.float64)).astype(F32)
 
 

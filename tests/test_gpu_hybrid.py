@@ -200,7 +200,8 @@ def test_hybrid_matches_oracle(B, lm_scale, case, capsys):
     for s, gl in zip(seqs, got):
         ref = orc.prefill_logprobs(s.tokens)
         worst = max(worst, float(np.max(np.abs(gl[s.prompt_len - 1:] - ref[s.prompt_len - 1:]))))
-    bound = max(TOL_LP, SPREAD[case]["max"])
+    m = [o["max"] for o in SPREAD[case]["orders"].values()]
+    bound = max(TOL_LP, max(m) * max(m) / min(m))   # the envelope widened as in test_gpu_model
     with capsys.disabled():
         print(f"\n[hybrid tiny lm x{lm_scale:g}] |dlp| max {worst:.4f} (bound {bound:.4f})")
     assert worst <= bound

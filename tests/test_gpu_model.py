@@ -7,12 +7,14 @@ eager vs CUDA-Graph decode, graph replay after an in-place weight update vs
 eager at the new weights.
 
 Parity, free-running (each side feeds its own outputs forward):
-|lp_gpu - lp_oracle| <= max(2e-2, spread), where spread is the measured gap
-between two correct FP32 evaluation orders of the oracle itself on the same
-case (float64-then-rounded vs plain ascending-k dot products), stored in
+|lp_gpu - lp_oracle| <= max(2e-2, envelope), where the envelope is how far
+correct FP32 evaluation orders of the oracle itself drift from its default
+on the same case (ascending, descending, round-toward-zero and blocked
+library orders against float64-then-rounded dot products), widened by the
+variability of that maximum among the orders; the measurements are stored in
 tests/golden/accumulation_spread.json by the script beside it.  Where bf16
 rounding flips are amplified (a x10 LM head, 28 layers of QK-norm attention,
-FP8 KV codes) that spread exceeds 2e-2, and no implementation that does not
+FP8 KV codes) the envelope exceeds 2e-2, and no implementation that does not
 reproduce the oracle's exact roundings can promise less.
 """
 import json
@@ -35,8 +37,13 @@ with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
 
 
 def lp_bound(case):
-    """2e-2, or the oracle's own order spread on this case if larger."""
-    return max(TOL_LP, SPREAD[case]["max"])
+    """2e-2, or, where larger, the envelope of correct FP32 evaluation orders
+    of the oracle on this case widened by how much that statistic varies
+    among them: the largest max |dlogprob| any order shows, times the ratio
+    of the largest to the smallest order's maximum (a maximum over positions
+    is heavy-tailed; the orders' own maxima differ by up to about 1.6x)."""
+    m = [o["max"] for o in SPREAD[case]["orders"].values()]
+    return max(TOL_LP, max(m) * max(m) / min(m))
 
 
 def flat(lps):
@@ -235,6 +242,8 @@ def test_qwen3_full_depth_per_layer_parity(kv_fp8, capsys):
               f"free-running |dlp| max {fmax:.3f} mean {fmean:.4f}; oracle order spread "
               f"max {SPREAD[case]['max']:.3f} mean {SPREAD[case]['mean']:.4f}")
     assert fmax <= lp_bound(case)
+    means = [o["mean"] for o in SPREAD[case]["orders"].values()]
+    assert fmean <= max(means) * max(means) / min(means)
 
 
 def test_fast_mode_differs_but_stays_close():

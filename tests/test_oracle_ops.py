@@ -35,6 +35,29 @@ def test_gemm_within_fp32_bound_of_fp64():
         assert np.all(np.abs(cb - ref) <= bound + np.abs(ref) * 2.0 ** -8 + 1e-30)
 
 
+def test_gemm_accumulation_orders_within_fp32_bounds():
+    """Every FP32 order the oracle offers stays within K * 2^-23 * sum|a||b|
+    of the exact sum; round-toward-zero never rounds away from zero on
+    same-sign terms; integer sums are exact in every order."""
+    g = np.random.default_rng(30)
+    a, b = randn(g, 4, 700), randn(g, 6, 700)
+    ref = a.astype(np.float64) @ b.astype(np.float64).T
+    bound = 700 * 2.0 ** -23 * (np.abs(a).astype(np.float64) @ np.abs(b).astype(np.float64).T)
+    pos_a, pos_b = np.abs(a), np.abs(b)
+    pos_ref = pos_a.astype(np.float64) @ pos_b.astype(np.float64).T
+    ia = g.integers(-4, 5, size=(3, 50)).astype(F32)
+    ib = g.integers(-4, 5, size=(2, 50)).astype(F32)
+    for kind in ops.KINDS:
+        with ops.accumulation(kind):
+            assert np.all(np.abs(ops.gemm(a, b, out="f32") - ref) <= bound + 1e-30), kind
+            if kind == "f32_rz":
+                assert np.all(ops.gemm(pos_a, pos_b, out="f32") <= pos_ref)
+            assert np.array_equal(ops.gemm(ia, ib, out="f32"), (ia @ ib.T).astype(F32))
+    with pytest.raises(ValueError):
+        with ops.accumulation("f16"):
+            pass
+
+
 def test_gemm_integer_exact_and_orientation():
     g = np.random.default_rng(1)
     a = g.integers(-4, 5, size=(9, 13)).astype(F32)
