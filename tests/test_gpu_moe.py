@@ -123,3 +123,35 @@ def test_indexer_topk_sparse_attention_block():
     ref = ops.sparse_attention(host_f32(q).reshape(T, Hq, D)[rows], kv_k.float().numpy(),
                                kv_v.float().numpy(), ref_idx[rows], qpos[rows], 1 / math.sqrt(D))
     assert rel_err(host_f32(out).reshape(T, Hq, D)[rows], ref) < REL
+
+
+def test_expert_parallel_path_equals_block_on_one_rank():
+    """The expert-parallel path (ExpertRouter bookkeeping and NCCL
+    all-to-alls around the same kernels) on a one-rank group gives the
+    one-GPU block's bits; the two-rank exchange itself is covered over gloo
+    on CPU (tests/test_ep.py)."""
+    import socket
+    import torch.distributed as dist
+    from invariant_forward_bitwise_gb300 import build
+    from invariant_forward_bitwise_gb300.ep import ExpertParallelMoE, ExpertRouter
+    from invariant_forward_bitwise_gb300.moe import MoEBlock
+    build.build()
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        T, E, k, d, I = 96, 16, 4, 512, 256
+        g = synth.rng(4242)
+        W = _weights(g, E, d, I)
+        tw = [torch.from_numpy(x) if isinstance(x, np.ndarray) else x for x in W]
+        blk = MoEBlock(*tw, top_k=k, max_tokens=T)
+        ep = ExpertParallelMoE(ExpertRouter(E, 1, 0), *tw, top_k=k, max_tokens=T)
+        h = synth.normal_bf16(g, (T, d)).cuda()
+        a = blk.forward(h).clone()
+        b = ep.forward(h).clone()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(a), bits(b))
+    finally:
+        dist.destroy_process_group()
