@@ -489,6 +489,57 @@ biv_status biv_gemm_nvfp4(const uint16_t* A, int64_t lda, const uint8_t* codes,
                           int c_dtype, int mode, void* workspace, size_t workspace_bytes,
                           biv_stream_t stream);
 
+/* ------------------------------------------------------------ backward --
+ * Backward of the fused forward ops for a trainer that runs the inference
+ * ops' own backward ("No More Train-Inference Mismatch", section "方法细节"),
+ * the FP8 KV round trip passing gradients straight through ("Finish RL
+ * Training Faster", section "让训练前向使用推理的数值").  FP32 on the CUDA
+ * cores; every reduction has one order fixed by the shapes (per-row trees,
+ * ascending loops), so results repeat bit for bit, and a row's dx / dz / dq
+ * depends on that row (and, for dq, its keys) only.
+ *
+ * RMSNorm of x (bf16 rows of d, gain w bf16 [d]): dy, dx float32 rows;
+ * dx = inv*(w*dy) - x*(inv^3*sum(x*w*dy)/d), inv = 1/sqrt(mean(x^2)+eps);
+ * dw float32 [d] = sum over rows in ascending order of dy*x*inv.  Workspace:
+ * rows*d*4 bytes (caller-owned, no initial value). */
+biv_status biv_rmsnorm_backward(const uint16_t* x, int64_t x_stride, const uint16_t* w,
+                                const float* dy, int64_t dy_stride, float* dx, int64_t dx_stride,
+                                float* dw, int rows, int d, float eps, void* workspace,
+                                size_t workspace_bytes, biv_stream_t stream);
+
+/* SiLU-mul: gate_up bf16 [rows, 2I] ([gate | up]), dy float32 [rows, I] ->
+ * dgate_up float32 [rows, 2I]: dgate = dy*up*s*(1+gate*(1-s)), dup =
+ * dy*gate*s, s = 1/(1+exp(-gate)). */
+biv_status biv_silu_mul_backward(const uint16_t* gate_up, int64_t gate_up_stride, const float* dy,
+                                 int64_t dy_stride, float* dgate_up, int64_t dgate_up_stride,
+                                 int rows, int I, biv_stream_t stream);
+
+/* logprob: logits float32 [T, V] (ld), target int32 [T], dlp float32 [T] ->
+ * dz float32 [T, V] (ldz) = dlp*(onehot(target) - exp(z - lse)); lse from a
+ * per-row max and sum in a fixed order.  A target outside [0, V) is reported
+ * through biv_poll_error. */
+biv_status biv_logprob_backward(const float* logits, int64_t ld, const int32_t* target,
+                                const float* dlp, int T, int V, float* dz, int64_t ldz,
+                                biv_stream_t stream);
+
+/* Causal GQA attention of one sequence: q, dout bf16 [Tq, Hq, D]; k, v bf16
+ * [Tk, Hkv, D] (the cache's dequantised values: an FP8 round trip passes dk,
+ * dv through unchanged); key j is visible to row i iff k_pos[j] <= q_pos[i].
+ * dq float32 [Tq, Hq, D], dk, dv float32 [Tk, Hkv, D]: with p = softmax(s),
+ * s = q.k*scale, D_i = dout_i . o_i, ds = p*(dout.v - D): dq = sum_j ds k
+ * scale (keys ascending), dk = sum ds q scale and dv = sum p dout (rows
+ * ascending, q heads of the group ascending).  D <= 128.  workspace float32
+ * [2*Tq*Hq] (row statistics, no initial value). */
+typedef struct {
+  const uint16_t* q; const uint16_t* k; const uint16_t* v; const uint16_t* dout;
+  float* dq; float* dk; float* dv;
+  int Tq, Tk, Hq, Hkv, D;
+  const int32_t* q_pos; const int32_t* k_pos;
+  float scale;
+  float* workspace;
+} biv_attn_bwd_desc;
+biv_status biv_attention_backward(const biv_attn_bwd_desc* desc, biv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,6 +28,7 @@ EXPORTS = [
     "biv_moe_combine", "biv_logprob", "biv_ssd_workspace", "biv_ssd_scan",
     "biv_causal_conv1d", "biv_gated_rmsnorm", "biv_nvfp4_dequant",
     "biv_gemm_nvfp4_workspace", "biv_gemm_nvfp4",
+    "biv_rmsnorm_backward", "biv_silu_mul_backward", "biv_logprob_backward", "biv_attention_backward",
 ]
 
 
@@ -102,6 +103,14 @@ class ConvDesc(C.Structure):
                 ("state", C.c_void_p)]
 
 
+class AttnBwdDesc(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p), ("dout", C.c_void_p),
+                ("dq", C.c_void_p), ("dk", C.c_void_p), ("dv", C.c_void_p),
+                ("Tq", C.c_int), ("Tk", C.c_int), ("Hq", C.c_int), ("Hkv", C.c_int), ("D", C.c_int),
+                ("q_pos", C.c_void_p), ("k_pos", C.c_void_p), ("scale", C.c_float),
+                ("workspace", C.c_void_p)]
+
+
 _lib: Optional[C.CDLL] = None
 
 
@@ -146,6 +155,10 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "biv_nvfp4_dequant": ([P, P, I, I, P, P], I),
         "biv_gemm_nvfp4_workspace": ([I, I, I, I, I, P], I),
         "biv_gemm_nvfp4": ([P, I64, P, P, I, I, I, P, I64, I, I, P, C.c_size_t, P], I),
+        "biv_rmsnorm_backward": ([P, I64, P, P, I64, P, I64, P, I, I, F, P, C.c_size_t, P], I),
+        "biv_silu_mul_backward": ([P, I64, P, I64, P, I64, I, I, P], I),
+        "biv_logprob_backward": ([P, I64, P, P, I, I, P, I64, P], I),
+        "biv_attention_backward": ([P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name, None)
@@ -450,3 +463,39 @@ def biv_gemm_nvfp4(A, codes, scales, Cout, M=None, mode=MODE_INVARIANT, ws=None,
     _check(load().biv_gemm_nvfp4(_p(A), A.stride(0), _p(codes), _p(scales), M, N, K, _p(Cout),
                                  Cout.stride(0), cdt, mode, _p(ws), ws.numel() if ws is not None else 0,
                                  _stream(stream)), "biv_gemm_nvfp4")
+
+
+# ------------------------------------------------------------- backward --
+def biv_rmsnorm_backward(x, w, dy, dx, dw, eps, ws=None, stream=None):
+    """x bf16 [R, d], w bf16 [d], dy float32 [R, d] -> dx float32 [R, d], dw float32 [d]."""
+    R, d = x.shape
+    if ws is None:
+        ws = gemm_scratch(R * d * 4)
+    _check(load().biv_rmsnorm_backward(_p(x), x.stride(0), _p(w), _p(dy), dy.stride(0), _p(dx),
+                                       dx.stride(0), _p(dw), R, d, float(eps), _p(ws), ws.numel(),
+                                       _stream(stream)), "biv_rmsnorm_backward")
+
+
+def biv_silu_mul_backward(gate_up, dy, dgate_up, stream=None):
+    R, I = dy.shape
+    _check(load().biv_silu_mul_backward(_p(gate_up), gate_up.stride(0), _p(dy), dy.stride(0),
+                                        _p(dgate_up), dgate_up.stride(0), R, I, _stream(stream)),
+           "biv_silu_mul_backward")
+
+
+def biv_logprob_backward(logits, target, dlp, dz, stream=None):
+    T, V = logits.shape
+    _check(load().biv_logprob_backward(_p(logits), logits.stride(0), _p(target), _p(dlp), T, V, _p(dz),
+                                       dz.stride(0), _stream(stream)), "biv_logprob_backward")
+
+
+def biv_attention_backward(q, k, v, dout, q_pos, k_pos, scale, dq, dk, dv, stream=None):
+    """One sequence: q, dout bf16 [Tq, Hq, D]; k, v bf16 [Tk, Hkv, D]."""
+    Tq, Hq, D = q.shape
+    ws = gemm_scratch(2 * Tq * Hq * 4)
+    d = AttnBwdDesc()
+    d.q, d.k, d.v, d.dout = (t.data_ptr() for t in (q, k, v, dout))
+    d.dq, d.dk, d.dv = dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    d.Tq, d.Tk, d.Hq, d.Hkv, d.D = Tq, k.shape[0], Hq, k.shape[1], D
+    d.q_pos, d.k_pos, d.scale, d.workspace = q_pos.data_ptr(), k_pos.data_ptr(), float(scale), ws.data_ptr()
+    _check(load().biv_attention_backward(C.byref(d), _stream(stream)), "biv_attention_backward")
