@@ -336,8 +336,9 @@ def decode_step_bytes(cfg, W):
     ``pos``: every weight once (the tied LM head streams the embedding table
     once per step; the embedding gather reads only the rows' own entries), the
     cached K/V of positions 0..p of each row's sequence over all layers, the
-    row's own K/V write, and its logits row written by the LM head and read
-    back by the log-softmax."""
+    row's own K/V write, and the (max, sum exp) pairs of its 128-logit groups
+    that the LM head's epilogue writes and the combine reads (the FP32 logits
+    never reach memory)."""
     seen, wbytes = set(), 0
     for t in W.values():
         if id(t) not in seen:
@@ -345,7 +346,7 @@ def decode_step_bytes(cfg, W):
             wbytes += t.numel() * t.element_size()
     per_tok = cfg.kv_heads * cfg.head_dim * (1 if cfg.kv_fp8 else 2) + (4 * cfg.kv_heads if cfg.kv_fp8 else 0)
     kv_tok = 2 * cfg.layers * per_tok
-    extra = kv_tok + 2 * cfg.vocab * 4
+    extra = kv_tok + 2 * ((cfg.vocab + 127) // 128) * 8
 
     def work(pos):
         return float(wbytes + sum(int(p) + 1 for p in pos) * kv_tok + len(pos) * extra)

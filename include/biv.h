@@ -367,6 +367,29 @@ biv_status biv_moe_combine(const uint16_t* y, const int32_t* src_row, const floa
 biv_status biv_logprob(const float* logits, int64_t ld, const int32_t* target, int T, int V,
                        float* lp, biv_stream_t stream);
 
+/* LM head with the log-softmax gather in its epilogue: lp[t] = z[t, target[t]]
+ * - logsumexp_v z[t, v] for z = h . W^T, without writing the FP32 logits
+ * (same source as biv_logprob).  The GEMM is biv_gemm's bf16 schedule (K
+ * chunks in INVARIANT mode), folded in the CTA on 256-column tiles for every
+ * M.  Its epilogue reduces each row's logits in groups of 128 columns
+ * (group g = columns [128g, 128g+128) of V) to m_g = max z and
+ * s_g = sum exp(z - m_g), summed as four interleaved chains (column mod 4,
+ * ascending) added as (c0 + c1) + (c2 + c3); a second kernel forms
+ * M = max_g m_g and S = sum_g s_g * exp(m_g - M) (lane l of a warp takes
+ * groups l, l+32, ... in order, then a xor tree) and lp = z_t - (M + log S).
+ * Every step depends on V and the row only, so a row's lp has the same bits
+ * in every batch.
+ * h bf16 [M, K] rows at ldh; W bf16 [V, K] rows at ldw (K-major, 16-byte
+ * aligned rows); target int32 [M]; lp float32 [M].  V % 4 == 0, K % 8 == 0.
+ * A target outside [0, V) gives lp = NaN and the device error code 2.
+ * Workspace: device memory of biv_lm_head_logprob_workspace(M, V) bytes,
+ * 16-byte aligned, owned by the caller, no initial value needed; calls that
+ * can overlap on the GPU need separate workspaces. */
+biv_status biv_lm_head_logprob_workspace(int M, int V, size_t* bytes);
+biv_status biv_lm_head_logprob(const uint16_t* h, int64_t ldh, const uint16_t* W, int64_t ldw,
+                               int M, int V, int K, const int32_t* target, int mode, float* lp,
+                               void* workspace, size_t workspace_bytes, biv_stream_t stream);
+
 /* ------------------------------------------------------------- SSD scan --
  * Mamba-2 SSD over chunks of `chunk` positions aligned to absolute positions
  * ("Finish RL Training Faster", section "一致性有多个层面": decode replays the

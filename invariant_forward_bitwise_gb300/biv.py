@@ -25,7 +25,8 @@ EXPORTS = [
     "biv_kv_fp8_gather", "biv_attention_workspace", "biv_attention", "biv_attention_noalloc",
     "biv_gemm_workspace", "biv_gemm_partials", "biv_gemm",
     "biv_act_quant_fp8", "biv_topk", "biv_router_topk", "biv_moe_dispatch", "biv_gather_rows",
-    "biv_moe_combine", "biv_logprob", "biv_ssd_workspace", "biv_ssd_scan",
+    "biv_moe_combine", "biv_logprob", "biv_lm_head_logprob_workspace", "biv_lm_head_logprob",
+    "biv_ssd_workspace", "biv_ssd_scan",
     "biv_causal_conv1d", "biv_gated_rmsnorm", "biv_nvfp4_dequant",
     "biv_gemm_nvfp4_workspace", "biv_gemm_nvfp4",
     "biv_rmsnorm_backward", "biv_silu_mul_backward", "biv_logprob_backward", "biv_attention_backward",
@@ -149,6 +150,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "biv_gather_rows": ([P, I64, P, I, I, I, P, I64, P], I),
         "biv_moe_combine": ([P, P, P, P, P, I, I, I, P], I),
         "biv_logprob": ([P, I64, P, I, I, P, P], I),
+        "biv_lm_head_logprob_workspace": ([I, I, P], I),
+        "biv_lm_head_logprob": ([P, I64, P, I64, I, I, I, P, I, P, P, C.c_size_t, P], I),
         "biv_ssd_workspace": ([P, P], I), "biv_ssd_scan": ([P, P], I),
         "biv_causal_conv1d": ([P, P], I),
         "biv_gated_rmsnorm": ([P, I64, P, I64, P, P, I64, I, I, F, P], I),
@@ -406,6 +409,21 @@ def biv_logprob(logits, target, lp, T=None, stream=None):
     T = logits.shape[0] if T is None else T
     _check(load().biv_logprob(_p(logits), logits.stride(0), _p(target), T, logits.shape[1], _p(lp),
                               _stream(stream)), "biv_logprob")
+
+
+def biv_lm_head_logprob_workspace(M: int, V: int) -> int:
+    n = C.c_size_t(0)
+    _check(load().biv_lm_head_logprob_workspace(M, V, C.byref(n)), "biv_lm_head_logprob_workspace")
+    return n.value
+
+
+def biv_lm_head_logprob(h, W, target, lp, workspace, M=None, mode=0, stream=None):
+    """lp[:M] = log-softmax of (h[:M] . W^T) at target[:M], without FP32 logits."""
+    M = h.shape[0] if M is None else M
+    _check(load().biv_lm_head_logprob(_p(h), h.stride(0), _p(W), W.stride(0), M, W.shape[0], h.shape[1],
+                                      _p(target), mode, _p(lp), _p(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)),
+           "biv_lm_head_logprob")
 
 
 def biv_ssd_workspace(desc: SSDDesc) -> int:

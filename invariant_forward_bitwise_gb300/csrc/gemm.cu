@@ -147,10 +147,18 @@ struct GemmArgs {
   int vec_ok;           // C rows 16-byte aligned
   int n_fastest;        // fold mode: walk N tiles first
   int b_after_wait;     // 1: B is written by the previous kernel (no early prefetch)
+  // log-softmax epilogue (LSE instantiation): per row and 128-column group g
+  // of the output, (max, sum of exp(z - max)) to lse[row * ngroups + g]; the
+  // logit at target[row] to zt[row]
+  const int32_t* target;
+  float2* lse;
+  float* zt;
+  int ngroups;
   int* err;
 };
 
 constexpr int kMaxStages = 16;
+constexpr int kLseGroup = 128;   // logit columns per (max, sum exp) pair
 // The invariant schedule cuts K into at most 8 chunks of at least 8 blocks of
 // 64 (shorter chunks make the register fold of wide tiles stall the MMA:
 // measured on GB300 at M = 16384, K = 2048, 256-element chunks ran 22% below
@@ -179,7 +187,9 @@ struct GemmSmem {
 // PARTIAL: the partial-mode instantiation.  Its epilogue keeps no running
 // sum, so it is compiled for half the register file; with PDL the next
 // kernel's CTAs can then start on the same SMs while it runs.
-template <int BN, bool F32OUT, bool PARTIAL>
+// LSE: fold mode whose epilogue reduces each 128-column half tile of a row to
+// its (max, sum exp) pair instead of storing the FP32 logits.
+template <int BN, bool F32OUT, bool PARTIAL, bool LSE = false>
 __global__ void __launch_bounds__(kGemmThreads, PARTIAL ? 2 : 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
@@ -368,6 +378,34 @@ __global__ void __launch_bounds__(kGemmThreads, PARTIAL ? 2 : 1)
       }
       if (partial) continue;  // gemm_fold_kernel finishes the tile
       if (!ok) break;
+      if constexpr (LSE) {
+        static_assert(HALF == kLseGroup, "one 128-column group per epilogue thread");
+        // the row's logits z[nb .. nb+nv) of this half tile: their max, then
+        // sum exp(z - max) over four interleaved chains (x = e mod 4, x
+        // ascending) added as (c0 + c1) + (c2 + c3)
+        const int nb = n0 + col0, nv = min(HALF, p.N - nb);
+        if (live && nv > 0) {
+          float gm = -INFINITY;
+#pragma unroll
+          for (int x = 0; x < HALF; ++x)
+            if (x < nv) gm = fmaxf(gm, r[x]);
+          float cs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int x = 0; x < HALF; ++x)
+            if (x < nv) cs[x & 3] += expf(r[x] - gm);
+          p.lse[int64_t(row) * p.ngroups + nb / kLseGroup] =
+              make_float2(gm, (cs[0] + cs[1]) + (cs[2] + cs[3]));
+          const int tg = p.target[row];
+          if (tg >= nb && tg < nb + nv) {
+            float z = 0.f;
+#pragma unroll
+            for (int x = 0; x < HALF; ++x)
+              if (nb + x == tg) z = r[x];
+            p.zt[row] = z;
+          }
+        }
+        continue;
+      }
       // store through the warp's staging block: lane l writes its row, then
       // the warp reads it back as 16-byte row pieces (W columns per lane,
       // LPR lanes per row), so a store instruction writes RPI whole row
@@ -1302,3 +1340,144 @@ biv_status biv_gemm(const biv_gemm_desc* d, void* ws, size_t ws_bytes, biv_strea
 
 }  // extern "C"
 
+
+// ------------------------------------------- LM head + log-softmax gather --
+// The logprob of every sampled token ("Finish RL Training Faster", section
+// "零差异需要一个精确的比较对象") formed without writing the FP32 logits: the
+// LM-head GEMM's epilogue reduces each row's logits, in groups of 128
+// columns aligned to column 0, to (m_g, s_g) = (max, sum exp(z - m_g)) and
+// keeps the target's logit; lse_combine_kernel then forms
+// lp = z_t - (M + log S), M = max_g m_g, S = sum_g s_g * exp(m_g - M).
+namespace biv {
+namespace {
+
+constexpr int kLseWarps = 8;
+
+// One warp per row: lane l takes groups l, l+32, ... in ascending order; the
+// lane maxima and sums are combined by xor trees (the order depends on the
+// number of groups only).
+__global__ void __launch_bounds__(kLseWarps * 32)
+    lse_combine_kernel(const float2* __restrict__ lse, int ngroups, const float* __restrict__ zt,
+                       const int32_t* __restrict__ target, int M, int N, float* __restrict__ lp,
+                       int* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x * kLseWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const float2* g = lse + int64_t(row) * ngroups;
+  float mx = -INFINITY;
+  for (int i = lane; i < ngroups; i += 32) mx = fmaxf(mx, g[i].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float s = 0.f;
+  for (int i = lane; i < ngroups; i += 32) {
+    const float2 v = g[i];
+    s = fmaf(v.y, expf(v.x - mx), s);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) {
+    const int tg = target[row];
+    if (tg < 0 || tg >= N) {
+      raise_error(err, kErrBadIndex);
+      lp[row] = NAN;
+      return;
+    }
+    lp[row] = zt[row] - (mx + logf(s));
+  }
+}
+
+size_t lse_bytes(int M, int V, int* ngroups) {
+  const int ng = (V + kLseGroup - 1) / kLseGroup;
+  if (ngroups) *ngroups = ng;
+  return (size_t(M) * ng * sizeof(float2) + size_t(M) * sizeof(float) + 15) / 16 * 16;
+}
+
+// The fused head always folds in the CTA on 256-column tiles (two 128-column
+// groups per tile), whatever M: the groups, and so every bit, stay the same
+// for every batch.  K is chunked as in biv_gemm.
+Plan plan_lse(const biv_gemm_desc& d) {
+  Plan p;
+  const int KB = (d.K + 63) / 64;
+  p.m_box = d.M <= BM ? std::max(16, (d.M + 15) / 16 * 16) : BM;
+  p.kc_blocks = d.mode == BIV_MODE_INVARIANT
+                    ? std::max(kMinChunkBlocks, (KB + kMaxChunks - 1) / kMaxChunks)
+                    : KB;
+  p.chunks = (KB + p.kc_blocks - 1) / p.kc_blocks;
+  p.bn = kWideN;
+  p.partial = false;
+  p.tiles = int64_t((d.N + p.bn - 1) / p.bn) * ((d.M + BM - 1) / BM);
+  const size_t fixed = GemmSmem<kWideN>::bytes(0, p.m_box, true);
+  p.stages = int(std::min<size_t>(kMaxStages, (kSmemBudget - fixed) /
+                                                  (p.m_box * 128 + GemmSmem<kWideN>::B_STAGE)));
+  return p;
+}
+
+}  // namespace
+}  // namespace biv
+
+using namespace biv;
+
+extern "C" biv_status biv_lm_head_logprob_workspace(int M, int V, size_t* bytes) {
+  BIV_REQUIRE(bytes && M >= 0 && V > 0, "lm_head_logprob_workspace: bad arguments");
+  *bytes = lse_bytes(M, V, nullptr);
+  return BIV_OK;
+}
+
+extern "C" biv_status biv_lm_head_logprob(const uint16_t* h, int64_t ldh, const uint16_t* W,
+                                          int64_t ldw, int M, int V, int K,
+                                          const int32_t* target, int mode, float* lp,
+                                          void* workspace, size_t workspace_bytes,
+                                          biv_stream_t stream) {
+  BIV_REQUIRE(target && lp, "lm_head_logprob: null target or lp");
+  BIV_REQUIRE(V % 4 == 0, "lm_head_logprob: V=%d must be a multiple of 4", V);
+  biv_gemm_desc d;
+  memset(&d, 0, sizeof(d));
+  d.M = M; d.N = V; d.K = K;
+  d.a_dtype = BIV_BF16; d.b_dtype = BIV_BF16; d.c_dtype = BIV_F32;
+  d.A = h; d.lda = ldh; d.B = W; d.ldb = ldw;
+  d.C = lp; d.ldc = V;   // C is not written; validate() wants a non-null target
+  d.mode = mode;
+  biv_status st = validate(&d);
+  if (st != BIV_OK) return st;
+  if (M == 0) return BIV_OK;
+  int ng = 0;
+  const size_t need = lse_bytes(M, V, &ng);
+  if (!workspace || workspace_bytes < need)
+    return set_error(BIV_ERR_WORKSPACE, "lm_head_logprob: workspace of %zu bytes needed", need);
+  if (!aligned16(workspace))
+    return set_error(BIV_ERR_INVALID, "lm_head_logprob: workspace must be 16-byte aligned");
+  const Plan p = plan_lse(d);
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, K, M, ldh, 64, p.m_box) ||
+      !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, K, V, ldw, 64, p.bn))
+    return set_error(BIV_ERR_CUDA, "lm_head_logprob: tensor map encoding failed");
+  auto kern = gemm_bf16_kernel<kWideN, true, false, true>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSmemBudget)) != cudaSuccess)
+      return set_error(BIV_ERR_CUDA, "lm_head_logprob: cannot set shared memory size");
+    attr = true;
+  }
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.M = M; a.N = V; a.K = K;
+  a.kc_blocks = p.kc_blocks; a.m_box = p.m_box; a.stages = p.stages;
+  a.n_fastest = V <= M;
+  a.target = target;
+  a.lse = static_cast<float2*>(workspace);
+  a.zt = reinterpret_cast<float*>(static_cast<float2*>(workspace) + size_t(M) * ng);
+  a.ngroups = ng;
+  a.err = device_error_word();
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  cudaStream_t s = as_cuda(stream);
+  launch_pdl(kern, int(std::min<int64_t>(p.tiles, sms)), kGemmThreads,
+             GemmSmem<kWideN>::bytes(p.stages, p.m_box, true), s, ta, tb, a);
+  st = check_launch("lm_head_logprob gemm");
+  if (st != BIV_OK) return st;
+  launch_pdl(lse_combine_kernel, (M + kLseWarps - 1) / kLseWarps, kLseWarps * 32, 0, s,
+             static_cast<const float2*>(a.lse), ng, static_cast<const float*>(a.zt), target, M, V,
+             lp, a.err);
+  return check_launch("lm_head_logprob combine");
+}

@@ -93,7 +93,7 @@ class DenseModel:
     ``max_rows`` rows per step."""
 
     def __init__(self, cfg, weights: Dict[str, torch.Tensor], max_rows: int, max_pos: int,
-                 mode: int = biv.MODE_INVARIANT, lm_chunk: int = 4096, device="cuda"):
+                 mode: int = biv.MODE_INVARIANT, lm_chunk: int = 16384, device="cuda"):
         biv.load()
         self.cfg, self.mode, self.max_rows, self.max_pos = cfg, mode, max_rows, max_pos
         self.lm_chunk = min(lm_chunk, max_rows)
@@ -113,7 +113,9 @@ class DenseModel:
         self.gu = torch.empty(T, 2 * I, **bf)
         self.act = torch.empty(T, I, **bf)
         self.ylm = torch.empty(T, d, **bf)
-        self.logits = torch.empty(self.lm_chunk, cfg.vocab, dtype=torch.float32, device=device)
+        # LM head + log-softmax: per-row (max, sum exp) pairs of 128-logit groups
+        self.lse_ws = torch.empty(biv.biv_lm_head_logprob_workspace(self.lm_chunk, cfg.vocab),
+                                  dtype=torch.uint8, device=device)
         self.lp = torch.empty(T, dtype=torch.float32, device=device)
         # step inputs (static, so that captured graphs read fresh values)
         i32 = dict(dtype=torch.int32, device=device)
@@ -202,15 +204,6 @@ class DenseModel:
                 d.ldc = N
                 d.mode = self.mode
                 gneed = max(gneed, biv.biv_gemm_workspace(d))
-            d = biv.GemmDesc()
-            d.M, d.N, d.K = min(s.T_lm, self.lm_chunk), cfg.vocab, cfg.hidden
-            d.a_dtype = d.b_dtype = biv.BF16
-            d.c_dtype = biv.F32
-            d.A = d.B = d.C = self.y.data_ptr()
-            d.lda = d.ldb = cfg.hidden
-            d.ldc = cfg.vocab
-            d.mode = self.mode
-            gneed = max(gneed, biv.biv_gemm_workspace(d))
         # captured graphs keep the address they saw: never free a workspace
         if need > self.ws.numel():
             self._old_ws.append(self.ws)
@@ -285,9 +278,13 @@ class DenseModel:
         self.launches += 1
         for c0 in range(0, Tl, self.lm_chunk):
             n = min(self.lm_chunk, Tl - c0)
-            self._gemm(self.ylm[c0:c0 + n], W["lm_head"], self.logits, n, st)
-            biv.biv_logprob(self.logits, self.targets[c0:c0 + n], self.lp[c0:c0 + n], T=n, stream=st)
-            self.launches += 1
+            t = self._timer()
+            tok = t.bracket("gemm_bf16", 2.0 * n * cfg.vocab * cfg.hidden, "flop") if t else None
+            biv.biv_lm_head_logprob(self.ylm[c0:c0 + n], W["lm_head"], self.targets[c0:c0 + n],
+                                    self.lp[c0:c0 + n], self.lse_ws, M=n, mode=self.mode, stream=st)
+            if tok:
+                t.close(tok)
+            self.launches += 2
         t = self._timer()
         if t:
             t.launches += self.launches

@@ -192,6 +192,45 @@ def test_logprob_parity_and_invariance(B, V):
     assert np.allclose(lp[:2].cpu().numpy(), -math.log(V), atol=1e-5)
 
 
+@pytest.mark.parametrize("M,V,K", [(13, 4096, 256), (5, 4100, 96), (1, 151936, 2048),
+                                   (300, 151936, 2048)])
+def test_lm_head_logprob_parity_and_invariance(B, M, V, K):
+    """The fused LM head + log-softmax gather: within 1e-4 of the oracle's
+    logprob of the oracle's FP32 logits (peaked head, logit std about 3), a row
+    alone or inside another batch keeps its bits, and a bad target is NaN and
+    reported."""
+    g = synth.rng(M + V + K)
+    h, W = rnd_bf16(g, M, K), rnd_bf16(g, V, K, std=3.0 / math.sqrt(K))
+    tgt = g.integers(0, V, size=M).astype(np.int32)
+    hd, Wd, td = dev(h), dev(W), dev(tgt)
+    ws = torch.empty(B.biv_lm_head_logprob_workspace(M, V), dtype=torch.uint8, device="cuda")
+    lp = torch.full((M,), float("nan"), dtype=torch.float32, device="cuda")
+    B.biv_lm_head_logprob(hd, Wd, td, lp, ws)
+    assert B.biv_poll_error() == 0
+    got = lp.cpu().numpy()
+    rows = np.arange(M) if M * V <= 1 << 22 else np.unique(np.r_[0, 7, M // 2, M - 1] % M)
+    z = ops.gemm(h[rows].float().numpy(), W.float().numpy(), out="f32")
+    ref = ops.logprob(z, tgt[rows])
+    assert np.std(z) > 1.0
+    assert np.max(np.abs(got[rows] - ref)) < 1e-4
+    # a row alone, and a slice in the middle of the batch: the same bits
+    r = min(7, M - 1)
+    one = torch.empty(1, dtype=torch.float32, device="cuda")
+    B.biv_lm_head_logprob(hd[r:r + 1], Wd, td[r:r + 1], one, ws)
+    assert np.array_equal(bits(one), bits(lp[r:r + 1]))
+    if M > 4:
+        mid = torch.empty(M - 3, dtype=torch.float32, device="cuda")
+        B.biv_lm_head_logprob(hd[2:M - 1], Wd, td[2:M - 1], mid, ws)
+        assert np.array_equal(bits(mid), bits(lp[2:M - 1]))
+    # zero weights: every logit 0, lp = -log V up to rounding
+    B.biv_lm_head_logprob(hd[:1], torch.zeros_like(Wd), td[:1], one, ws)
+    assert abs(one.item() + math.log(V)) < 1e-5
+    # a target outside [0, V): NaN and error code 2, then cleared
+    B.biv_lm_head_logprob(hd[:1], Wd, dev(np.array([V], np.int32)), one, ws)
+    assert math.isnan(one.item()) and B.biv_poll_error() == 2
+    assert B.biv_poll_error() == 0
+
+
 # --------------------------------------------------------------------- GEMM --
 GEMM_SHAPES = [(1, 64, 64), (5, 96, 80), (130, 512, 256), (200, 688, 256), (77, 256, 688),
                (257, 1000, 320), (64, 4096, 2048), (300, 2048, 6144)]
