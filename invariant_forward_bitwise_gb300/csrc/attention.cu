@@ -31,7 +31,8 @@ namespace biv {
 namespace {
 
 constexpr int kTile = 64;   // keys per tile = one page
-constexpr int kNV = 64;     // most query vectors a CTA takes (4 warps x 16)
+constexpr int kNV = 64;     // most query vectors an attn_kernel CTA takes (4 warps x 16)
+constexpr int kNVTc = 128;  // most query vectors a block may hold (attn_tc_kernel)
 
 // NW warps per CTA, ST-stage K/V pipeline, TMA or thread-issued loads, and
 // DS: 1 = each warp owns 16 query vectors (prefill blocks); DS = NW = every
@@ -127,6 +128,7 @@ __device__ __forceinline__ void cp_async_wait() {
 
 struct AttnArgs {
   CUtensorMap tmK, tmV;      // bf16 caches as [pages*64, Hkv*D] (TMA path only)
+  CUtensorMap tmQ;           // q as [T][Hq][D], boxes of 64 dims x G heads x 128/G rows (tcgen05 path)
   const uint16_t* q; int64_t q_stride;
   uint16_t* out; int64_t out_stride;
   int T, Hq, Hkv, G;
@@ -487,7 +489,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     for (int i = 0; i < 2; ++i) {
       rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
       rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
-      l[i] = l[i] * alpha[i] + rs[i];
+      l[i] = __fmaf_rn(l[i], alpha[i], rs[i]);
     }
     // rescale only when some row's max moved (a factor of exactly 1 is a no-op)
     if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
@@ -596,6 +598,356 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
   }
 }
 
+// ---------------------------------------------------------------------------
+// Prefill attention on tcgen05.  A CTA takes up to 128 query vectors of one
+// query block and one KV head (the M = 128 rows of the MMA) over one KV split.
+// Per 64-key tile: S = Q . K^T into one of two TMEM buffers (K steps of 16
+// over the head dimension, ascending); the online softmax by four warps with
+// one thread per vector, doing attn_kernel's FP32 operations in attn_kernel's
+// order element for element; P's three bf16 parts into shared memory; and
+// O += P . V accumulated in TMEM (per 16-key step hi, mid, lo).  One K = 16
+// tcgen05 MMA rounds exactly as one mma.sync m16n8k16 on the same operands
+// and accumulator (checked bit for bit on GB300, including wide exponent
+// ranges and cancellation), so a vector's output has the same bits whichever
+// kernel runs it: prefill rows here, decode rows in attn_kernel.
+// V is read in place from its TMA tile ([key][dim], 128-byte swizzled) as an
+// MN-major operand.  O starts at +0 in TMEM and every P.V MMA accumulates,
+// as attn_kernel's register accumulators do.
+// Warps: 0 = TMA producer, 1 = MMA issuer and TMEM owner, 2..5 = softmax and
+// epilogue (TMEM lane quarter warp % 4, vector 32 * (warp % 4) + lane).
+template <int D>
+struct TcCfg {
+  static constexpr int NV = 128;                  // query vectors per CTA (MMA rows)
+  static constexpr int PANEL = NV * 128;          // one 64-dim panel of Q
+  static constexpr int Q_BYTES = NV * D * 2;
+  static constexpr int KV_BYTES = kTile * D * 2;  // one K or V tile
+  static constexpr int P_BYTES = NV * kTile * 2;  // one bf16 part of P
+  static constexpr int STK = 2, STV = 2;
+  static constexpr int NBARS = 15;
+  static constexpr int SMEM = 1024 + Q_BYTES + (STK + STV) * KV_BYTES + 3 * P_BYTES + NBARS * 8 + 16;
+  static constexpr uint32_t TMEM_COLS = 256;      // S double buffer (2 x 64) + O (D)
+  static constexpr uint32_t O_COL = 2 * kTile;
+  static constexpr int THREADS = 192;
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__ AttnArgs a) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
+  using Cfg = TcCfg<D>;
+  constexpr int KVB = Cfg::KV_BYTES, PB = Cfg::P_BYTES, STK = Cfg::STK, STV = Cfg::STV;
+  enum { Q_FULL = 0, K_FULL = 1, K_EMPTY = 3, V_FULL = 5, V_EMPTY = 7, S_FULL = 9, S_EMPTY = 11,
+         P_FULL = 13, PV_DONE = 14 };
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sQ = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  uint8_t* sK = sQ + Cfg::Q_BYTES;
+  uint8_t* sV = sK + STK * KVB;
+  uint8_t* sP = sV + STV * KVB;                    // parts hi, mid, lo
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 3 * PB);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NBARS);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int blk = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
+  const int r0 = a.qblocks[2 * blk], nr = a.qblocks[2 * blk + 1];
+  const int nv = nr * a.G;
+  const int seq = a.row_seq[r0];
+
+  // block's largest position; rows whose position is out of bounds are
+  // reported and left out (as in attn_kernel)
+  int maxpos = -1;
+  for (int r = 0; r < nr; ++r) {
+    const int p = a.row_pos[r0 + r];
+    if (row_pos_ok(a, p)) {
+      maxpos = max(maxpos, p);
+    } else if (split == 0) {
+      if (tid == 0) raise_error(a.err, kErrBadIndex);
+      uint16_t* dst = a.out + int64_t(r0 + r) * a.out_stride + int64_t(h * a.G) * D;
+      for (int i = tid; i < a.G * D; i += Cfg::THREADS) dst[i] = 0x7FC0;  // bf16 NaN
+    }
+  }
+  const int lo = split * a.kv_split;
+  const int hi = min(maxpos + 1, lo + a.kv_split);
+  if (lo >= hi) return;  // uniform: nothing of this block lives in this split
+  const int ntiles = (hi - lo + kTile - 1) / kTile;
+
+  if (tid == 0) {
+    mbar_init(bar(Q_FULL), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(K_FULL + s), 1);
+      mbar_init(bar(K_EMPTY + s), 1);
+      mbar_init(bar(V_FULL + s), 1);
+      mbar_init(bar(V_EMPTY + s), 1);
+      mbar_init(bar(S_FULL + s), 1);
+      mbar_init(bar(S_EMPTY + s), 4);
+    }
+    mbar_init(bar(P_FULL), 4);
+    mbar_init(bar(PV_DONE), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  int issued_k = 0, issued_v = 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      tma_prefetch_desc(&a.tmQ);
+      tma_prefetch_desc(&a.tmK);
+      tma_prefetch_desc(&a.tmV);
+      mbar_expect_tx(bar(Q_FULL), Cfg::Q_BYTES);
+#pragma unroll
+      for (int hh = 0; hh < D / 64; ++hh)
+        tma_load_3d(smem_u32(sQ + hh * Cfg::PANEL), &a.tmQ, bar(Q_FULL), hh * 64, h * a.G, r0);
+      for (int t = 0; t < ntiles; ++t) {
+        const int tbase = lo + t * kTile;
+        const int page = a.bt[int64_t(seq) * a.max_pages + tbase / kTile];
+        const int sk = t % STK, sv = t % STV;
+        if (t >= STK && !mbar_wait(bar(K_EMPTY + sk), ((t / STK) - 1) & 1, a.err)) break;
+        mbar_expect_tx(bar(K_FULL + sk), KVB);
+#pragma unroll
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_load_2d(smem_u32(sK + sk * KVB + hh * 8192), &a.tmK, bar(K_FULL + sk),
+                      h * D + hh * 64, page * kTile);
+        ++issued_k;
+        if (t >= STV && !mbar_wait(bar(V_EMPTY + sv), ((t / STV) - 1) & 1, a.err)) break;
+        mbar_expect_tx(bar(V_FULL + sv), KVB);
+#pragma unroll
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_load_2d(smem_u32(sV + sv * KVB + hh * 8192), &a.tmV, bar(V_FULL + sv),
+                      h * D + hh * 64, page * kTile);
+        ++issued_v;
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA --
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_mma(1u, Cfg::NV, kTile);
+      constexpr uint32_t idO = idesc_mma(1u, Cfg::NV, D) | (1u << 16);   // B = V, MN-major
+      const uint32_t q0 = smem_u32(sQ);
+      // S(t) = Q . K(t)^T into buffer t % 2 (free once the softmax of t-2 read it)
+      auto issue_s = [&](int t) -> bool {
+        const int sb = t & 1, sk = t % STK;
+        if (t >= 2 && !mbar_wait(bar(S_EMPTY + sb), ((t - 2) >> 1) & 1, a.err)) return false;
+        if (!mbar_wait(bar(K_FULL + sk), (t / STK) & 1, a.err)) return false;
+        tc_fence_after();
+        const uint32_t k0 = smem_u32(sK + sk * KVB);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_f16(tmem + sb * kTile, sdesc_k_sw128(q0 + (kk >> 2) * Cfg::PANEL + (kk & 3) * 32),
+                   sdesc_k_sw128(k0 + (kk >> 2) * 8192 + (kk & 3) * 32), idS, kk > 0 ? 1u : 0u);
+        umma_commit(bar(K_EMPTY + sk));
+        umma_commit(bar(S_FULL + sb));
+        return true;
+      };
+      bool ok = mbar_wait(bar(Q_FULL), 0, a.err) && issue_s(0);
+      for (int t = 0; t < ntiles && ok; ++t) {
+        if (t + 1 < ntiles && !(ok = issue_s(t + 1))) break;
+        // O += P(t) . V(t): per 16-key step the hi, mid and lo parts
+        if (!(ok = mbar_wait(bar(P_FULL), t & 1, a.err))) break;
+        tc_fence_after();
+        const int sv = t % STV;
+        const uint32_t v0 = smem_u32(sV + sv * KVB), p0 = smem_u32(sP);
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks) {
+          const uint64_t vd = sdesc_mn_sw128(v0 + ks * 2048, 8192, 1024);
+#pragma unroll
+          for (int part = 0; part < 3; ++part)
+            umma_f16(tmem + Cfg::O_COL, sdesc_k_sw128(p0 + part * PB + ks * 32), vd, idO, 1u);
+        }
+        umma_commit(bar(V_EMPTY + sv));
+        umma_commit(bar(PV_DONE));
+      }
+    }
+  } else {
+    // ------------------------------------------------- softmax, epilogue --
+    const int qtr = warp & 3;
+    const int v = qtr * 32 + lane;
+    const uint32_t lane_off = uint32_t(qtr * 32) << 16;
+    int vpos = v < nv ? a.row_pos[r0 + v / a.G] : -1;
+    if (!row_pos_ok(a, vpos)) vpos = -1;   // sees no key; output already NaN
+    float m = -INFINITY, l = 0.f;
+    {
+      uint32_t z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_st32(tmem + Cfg::O_COL + lane_off + c * 32, z);
+      tmem_st_wait();
+    }
+    uint8_t* myP = sP + (v >> 3) * 1024 + (v & 7) * 128;   // row v of each part
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int sb = t & 1, tbase = lo + t * kTile;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(S_FULL + sb), (t >> 1) & 1, a.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[kTile];
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tmem + sb * kTile + lane_off, ra);
+        tmem_ld32(tmem + sb * kTile + lane_off + 32, rb);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(ra[i]);
+          s[32 + i] = __uint_as_float(rb[i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(S_EMPTY + sb));
+      // mask: key tbase + j is seen when it lies below hi and at or before vpos
+      const int lim = vpos < 0 ? -1 : min(hi - 1, vpos) - tbase;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kTile; ++j) {
+        const float x = j <= lim ? s[j] * a.scale : -INFINITY;
+        s[j] = x;
+        mx = fmaxf(mx, x);
+      }
+      const float mn = fmaxf(m, mx);
+      const float alpha = (mn == -INFINITY) ? 1.f : expf(m - mn);
+      m = mn;
+      // p in FP32; the denominator as attn_kernel sums it: four chains (key
+      // mod 8 in {2c, 2c+1}, key ascending), then (c0 + c1) + (c2 + c3)
+      float cs[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t ph[kTile / 2], pm[kTile / 2], pl[kTile / 2];
+#pragma unroll
+      for (int nt = 0; nt < kTile / 8; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int j = nt * 8 + 2 * c;
+          const float p0 = (m == -INFINITY) ? 0.f : expf(s[j] - m);
+          const float p1 = (m == -INFINITY) ? 0.f : expf(s[j + 1] - m);
+          cs[c] += p0;
+          cs[c] += p1;
+          split3(p0, p1, ph[j / 2], pm[j / 2], pl[j / 2]);
+        }
+      }
+      l = __fmaf_rn(l, alpha, (cs[0] + cs[1]) + (cs[2] + cs[3]));
+      // P.V of tile t-1 is done: O and the P buffer are free
+      if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(PV_DONE), (t - 1) & 1, a.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int sv = t % STV;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(V_FULL + sv), (t / STV) & 1, a.err))) {
+        ok = false;
+        break;
+      }
+      // slots past the split's end in its last page hold no key of this
+      // sequence: zero their V rows (P is 0 there, and 0 * stale must be 0)
+      const int first_bad = hi - tbase;
+      if (first_bad < kTile) {
+        uint8_t* vt = sV + sv * KVB;
+        for (int i = tid - 64; i < (kTile - first_bad) * (D / 8); i += 128) {
+          const int j = first_bad + i / (D / 8), c = i % (D / 8);
+          const int dim = c * 8;
+          *reinterpret_cast<uint4*>(vt + (dim >> 6) * 8192 + j * 128 +
+                                    ((((dim & 63) >> 3) ^ (j & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      // rescale O when a row's max moved (a factor of exactly 1 is a no-op)
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + Cfg::O_COL + lane_off + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(tmem + Cfg::O_COL + lane_off + c * 32, r);
+        }
+        tmem_st_wait();
+      }
+      // P's parts: row v, keys 8c .. 8c+7 in 16-byte chunk c (128-byte swizzle)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t off = uint32_t((c ^ (v & 7)) << 4);
+        *reinterpret_cast<uint4*>(myP + off) =
+            make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
+        *reinterpret_cast<uint4*>(myP + PB + off) =
+            make_uint4(pm[4 * c], pm[4 * c + 1], pm[4 * c + 2], pm[4 * c + 3]);
+        *reinterpret_cast<uint4*>(myP + 2 * PB + off) =
+            make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(P_FULL));
+    }
+    // ---- epilogue: single-split rows write the final output, others partials
+    if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(PV_DONE), (ntiles - 1) & 1, a.err)))
+      ok = false;
+    tc_fence_after();
+    if (ok) {
+      const int row = r0 + v / a.G, head = h * a.G + v % a.G;
+      const int ns = (v < nv && vpos >= 0) ? row_splits(a, vpos) : 0;
+      const bool mine = split < ns;
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+      const int64_t slot = (int64_t(row) * a.Hq + head) * a.nsplit_grid + split;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + Cfg::O_COL + lane_off + c * 32, r);   // warp-collective
+        tmem_ld_wait();
+        if (!mine) continue;
+        if (ns == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(a.out + int64_t(row) * a.out_stride +
+                                                int64_t(head) * D + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float o0 = __uint_as_float(r[8 * q + 2 * e]) * inv_l + 0.0f;
+              const float o1 = __uint_as_float(r[8 * q + 2 * e + 1]) * inv_l + 0.0f;
+              pk[e] = pack_bf2(o0, o1);
+            }
+            dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        } else {
+          float4* wo = reinterpret_cast<float4*>(a.ws_o + slot * D + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            wo[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        }
+      }
+      if (mine && ns > 1) {
+        a.ws_ml[2 * slot] = m;
+        a.ws_ml[2 * slot + 1] = l;
+      }
+    }
+  }
+  // the producer makes sure its copies have landed before the CTA exits
+  if (warp == 0 && lane == 0) {
+    if (issued_k > 0) {
+      const int t = issued_k - 1;
+      mbar_wait(bar(K_FULL + t % STK), (t / STK) & 1, a.err, 100000000ull);
+    }
+    if (issued_v > 0) {
+      const int t = issued_v - 1;
+      mbar_wait(bar(V_FULL + t % STV), (t / STV) & 1, a.err, 100000000ull);
+    }
+    mbar_wait(bar(Q_FULL), 0, a.err, 100000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+}
+
 // Merge the splits of rows that have more than one, in ascending split order:
 // w_s = exp(m_s - M), O = sum w_s o_s, L = sum w_s l_s, out = O / L.
 template <int D>
@@ -660,8 +1012,8 @@ biv_status validate(const biv_attn_desc* d) {
   BIV_REQUIRE(d->kv_split >= kTile && d->kv_split % kTile == 0, "attention: kv_split must be a multiple of 64");
   BIV_REQUIRE(d->kv_dtype == BIV_BF16 || d->kv_dtype == BIV_E4M3, "attention: kv dtype");
   BIV_REQUIRE(d->kv_dtype == BIV_BF16 || (d->k_scale && d->v_scale), "attention: FP8 needs scales");
-  BIV_REQUIRE(d->max_rows_per_block >= 1 && d->max_rows_per_block * G <= kNV,
-              "attention: max_rows_per_block * (Hq/Hkv) must be <= %d", kNV);
+  BIV_REQUIRE(d->max_rows_per_block >= 1 && d->max_rows_per_block * G <= kNVTc,
+              "attention: max_rows_per_block * (Hq/Hkv) must be <= %d", kNVTc);
   BIV_REQUIRE(!d->topk_idx || (d->max_rows_per_block == 1 && d->topk > 0),
               "attention: sparse mode takes one row per block");
   BIV_REQUIRE(d->topk_idx || d->max_ctx >= 1, "attention: max_ctx >= 1 required");
@@ -742,17 +1094,60 @@ int decode_dsplit(int64_t ctas) {
   return decode_grid_small(ctas) ? 2 : 1;
 }
 
+// q as a 3-D tensor [T][Hq][D] with boxes of 64 dims x G heads x 128/G rows:
+// one box is 128 query vectors (row-major over (row, head of the group)) of
+// one 64-dim panel, 128-byte swizzled.  Rows past T read as zero.
+bool make_q_map(CUtensorMap* m, const void* q, int T, int Hq, int D, int64_t q_stride, int G) {
+  auto fn = tensor_map_encoder();
+  if (!fn || kNVTc % G != 0) return false;
+  cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(Hq), cuuint64_t(T)};
+  cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(q_stride) * 2};
+  cuuint32_t box[3] = {64, cuuint32_t(G), cuuint32_t(kNVTc / G)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+biv_status launch_tc(const biv_attn_desc& d, const AttnArgs& a, cudaStream_t s) {
+  using Cfg = TcCfg<D>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM) != cudaSuccess)
+      return set_error(BIV_ERR_CUDA, "attention: cannot set shared memory size");
+    attr = true;
+  }
+  dim3 grid(d.nqblocks, d.Hkv, a.nsplit_grid);
+  launch_pdl(attn_tc_kernel<D>, grid, Cfg::THREADS, Cfg::SMEM, s, a);
+  return check_launch("attention_tc");
+}
+
 template <int D>
 biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
-  // The CTA shape and the loader follow the call; a vector's arithmetic does not.
+  // The CTA shape, the loader and the tensor-core path follow the call; a
+  // vector's arithmetic does not.
   const bool small = d.max_rows_per_block * a.G <= 16;
+  const bool wide = d.max_rows_per_block * a.G > kNV;   // only attn_tc_kernel takes these
   biv_status st;
   bool tma = false;
   if constexpr (D % 64 == 0) {
     tma = !a.fp8 && !a.topk_idx && d.num_pages > 0 &&
           make_kv_map(&a.tmK, d.k_cache, d.num_pages, d.Hkv, D) &&
           make_kv_map(&a.tmV, d.v_cache, d.num_pages, d.Hkv, D);
-    if (tma) {
+    // prefill blocks on tcgen05 unless BIV_ATTN_PREFILL_TC=0 (tests compare
+    // the two kernels bit for bit)
+    const char* tc_env = getenv("BIV_ATTN_PREFILL_TC");
+    const bool tc = tma && !small && !(tc_env && atoi(tc_env) == 0) &&
+                    make_q_map(&a.tmQ, d.q, d.T, d.Hq, D, d.q_stride, a.G);
+    if (tc) {
+      st = launch_tc<D>(d, a, s);
+    } else if (wide) {
+      return set_error(BIV_ERR_UNSUPPORTED,
+                       "attention: blocks above %d query vectors need a bf16 cache, D 64 or 128, "
+                       "dense attention and Hq/Hkv dividing 128", kNV);
+    } else if (tma) {
       if (!small) {
         // Prefill CTAs: one TMA stage and registers capped for three CTAs
         // per SM (measured on GB300, 8 sequences x 1024 tokens: 223 us,
@@ -772,6 +1167,10 @@ biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
     }
   }
   if (!tma) {
+    if (wide)
+      return set_error(BIV_ERR_UNSUPPORTED,
+                       "attention: blocks above %d query vectors need a bf16 cache, D 64 or 128, "
+                       "dense attention and Hq/Hkv dividing 128", kNV);
     if (a.fp8) {
       // FP8 decode CTAs: four warps share the staged dequantisation and split
       // the head dimension in P.V (D = 80 keeps one warp: its 10 output

@@ -184,7 +184,9 @@ elif case.startswith("attn"):
         blocks = [(i, 1) for i in range(B)]
     else:
         rows = [(i, p) for i in range(B) for p in range(ctx)]
-        blocks = [(i * ctx + j, 32) for i in range(B) for j in range(0, ctx, 32)]
+        # blocks of 128 query vectors, as the model forms them for bf16 pages
+        per = int(os.environ.get("BIV_BENCH_BLOCK_ROWS", 128 // (Hq // Hkv)))
+        blocks = [(i * ctx + j, min(per, ctx - j)) for i in range(B) for j in range(0, ctx, per)]
     T = len(rows)
     q = torch.randn(T, Hq * D, device="cuda").to(torch.bfloat16)
     out = torch.empty_like(q)

@@ -310,7 +310,11 @@ class Runner:
     def __init__(self, model: DenseModel):
         self.m = model
         cfg = model.cfg
-        self.rows_per_block = max(1, 64 // (cfg.q_heads // cfg.kv_heads))
+        G = cfg.q_heads // cfg.kv_heads
+        # bf16 pages with D 64 / 128 run prefill blocks on the tcgen05 kernel,
+        # whose CTA takes 128 query vectors; other caches take 64 per CTA
+        nv = 128 if (not cfg.kv_fp8 and cfg.head_dim % 64 == 0 and 128 % G == 0) else 64
+        self.rows_per_block = max(1, nv // G)
 
     def load_rows(self, kv: PagedKV, seq_slot, pos, ids, lm_rows, targets, write_kv=None):
         m = self.m

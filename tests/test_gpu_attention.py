@@ -162,6 +162,30 @@ def test_prefill_parity_and_decode_invariance(B, D, Hq, Hkv, fp8, split):
     assert np.array_equal(bits(out2), bits(out))
 
 
+@pytest.mark.parametrize("D,Hq,Hkv,split", [(128, 16, 8, 1024), (128, 16, 8, 128), (64, 4, 2, 64),
+                                           (128, 8, 8, 256), (64, 32, 4, 192)])
+def test_tcgen05_prefill_equals_mma_sync_kernel(B, monkeypatch, D, Hq, Hkv, split):
+    """Prefill blocks of up to 128 query vectors on tcgen05 give the bits of
+    the mma.sync kernel on blocks of up to 64 (ragged lengths, stale NaN in
+    unwritten page slots, one to twelve KV splits merged), and stay within the
+    oracle's tolerance."""
+    g = synth.rng(D * 3 + Hq + split)
+    lens = [37, 300, 64, 129, 700]
+    pc = Paged(B, g, lens, Hkv, D)
+    G = Hq // Hkv
+    rows = [(i, p) for i, L in enumerate(lens) for p in range(L)]
+    q = synth.normal_bf16(g, (len(rows), Hq * D)).cuda()
+    out_tc = run_attn(B, pc, q, rows, blocks_of(rows, 128 // G), Hq, kv_split=split)
+    monkeypatch.setenv("BIV_ATTN_PREFILL_TC", "0")
+    out_ms = run_attn(B, pc, q, rows, blocks_of(rows, max(1, 64 // G)), Hq, kv_split=split)
+    assert np.array_equal(bits(out_tc), bits(out_ms))
+    at = sum(lens[:4])
+    k, v = pc.oracle_kv(4)
+    ref = ops.attention(host_f32(q).reshape(len(rows), Hq, D)[at:], k, v, np.arange(700),
+                        np.arange(700), 1.0 / math.sqrt(D))
+    assert rel_err(host_f32(out_tc).reshape(len(rows), Hq, D)[at:], ref) < REL
+
+
 def test_prefill_cta_shape_changes_no_bit(B, monkeypatch):
     """The two-stage prefill CTA gives the bits of the default one-stage CTA."""
     g = synth.rng(77)
