@@ -6,7 +6,9 @@
 // KV split.  Its query vectors are (row, q-head-of-the-group) pairs, 16 per
 // warp.  Keys are visited in 64-token tiles aligned to absolute positions (one
 // cache page), inside splits of kv_split tokens.  Per vector and split:
-// online softmax in FP32 (x = s * scale, p = exp(x - m), natural base), P
+// online softmax in FP32 in base 2 (x = s * scale * log2 e, rounded once;
+// p = 2^(x - m) by ex2.approx; the natural-base softmax up to rounding; m
+// moves lazily, see kLazy), P
 // split into three bf16 parts hi + mid + lo that add up to the FP32 p exactly
 // (three MMAs into one FP32 accumulator, hi first), the denominator summed
 // from the FP32 p.  Splits are merged in ascending order.  A vector's arithmetic is the
@@ -33,6 +35,10 @@ namespace {
 constexpr int kTile = 64;   // keys per tile = one page
 constexpr int kNV = 64;     // most query vectors an attn_kernel CTA takes (4 warps x 16)
 constexpr int kNVTc = 128;  // most query vectors a block may hold (attn_tc_kernel)
+// Lazy rescaling: a row's running max m (base-2 units) moves only when a tile's
+// max exceeds it by more than kLazy, so p = 2^(x - m) stays below 2^kLazy and
+// O, l are rescaled rarely.  Every kernel applies the same rule per row.
+constexpr float kLazy = 8.f;
 
 // NW warps per CTA, ST-stage K/V pipeline, TMA or thread-issued loads, and
 // DS: 1 = each warp owns 16 query vectors (prefill blocks); DS = NW = every
@@ -83,6 +89,13 @@ __device__ __forceinline__ void split3(float x0, float x1, uint32_t& hi, uint32_
   const float r0 = x0 - __uint_as_float(hi << 16), r1 = x1 - __uint_as_float(hi & 0xFFFF0000u);
   mid = cvt_bf16x2(r0, r1);
   lo = cvt_bf16x2(r0 - __uint_as_float(mid << 16), r1 - __uint_as_float(mid & 0xFFFF0000u));
+}
+
+// 2^x (PTX ex2.approx.ftz: 2^-inf = +0, results below 2^-126 flush to zero)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -140,7 +153,7 @@ struct AttnArgs {
   const int32_t* bt; int max_pages;
   int kv_split;
   const int32_t* topk_idx; int64_t topk_stride; int topk;
-  float scale;
+  float scale;               // softmax scale times log2(e): scores in base-2 units
   float* ws_o; float* ws_ml; int nsplit_grid;
   int* err;
 };
@@ -158,6 +171,29 @@ __device__ __forceinline__ bool row_pos_ok(const AttnArgs& a, int pos) {
   if (pos < 0) return false;
   if (a.topk_idx) return true;
   return pos < a.nsplit_grid * a.kv_split && pos < a.max_pages * kTile;
+}
+
+// The block's largest valid position (rows of a block are one sequence).
+// Rows whose position is out of bounds are reported (split 0) and their
+// output set to NaN; they take no part in the loads, the partials or the
+// merge.  One row per thread, so the positions load in parallel.
+template <int D>
+__device__ __forceinline__ int block_maxpos(const AttnArgs& a, int r0, int nr, int h, int split,
+                                            int* s_max) {
+  if (threadIdx.x == 0) *s_max = -1;
+  __syncthreads();
+  for (int r = threadIdx.x; r < nr; r += blockDim.x) {
+    const int p = a.row_pos[r0 + r];
+    if (row_pos_ok(a, p)) {
+      atomicMax(s_max, p);
+    } else if (split == 0) {
+      raise_error(a.err, kErrBadIndex);
+      uint16_t* dst = a.out + int64_t(r0 + r) * a.out_stride + int64_t(h * a.G) * D;
+      for (int i = 0; i < a.G * D; ++i) dst[i] = 0x7FC0;  // bf16 NaN
+    }
+  }
+  __syncthreads();
+  return *s_max;
 }
 
 // MINB: CTAs per SM the register allocation must allow (0: no bound)
@@ -188,19 +224,8 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
   const int seq = a.row_seq[r0];
   const bool sparse = a.topk_idx != nullptr;
 
-  // block's largest position (rows of a block are one sequence); rows whose
-  // position is out of bounds are reported and left out
-  int maxpos = -1;
-  for (int r = 0; r < nr; ++r) {
-    const int p = a.row_pos[r0 + r];
-    if (row_pos_ok(a, p)) {
-      maxpos = max(maxpos, p);
-    } else if (split == 0) {
-      if (tid == 0) raise_error(a.err, kErrBadIndex);
-      uint16_t* dst = a.out + int64_t(r0 + r) * a.out_stride + int64_t(h * a.G) * D;
-      for (int i = tid; i < a.G * D; i += NT) dst[i] = 0x7FC0;  // bf16 NaN
-    }
-  }
+  __shared__ int s_maxpos;
+  const int maxpos = block_maxpos<D>(a, r0, nr, h, split, &s_maxpos);
 
   // key range of this split: [lo, hi) in positions (dense) or list indices (sparse)
   const int lo = split * a.kv_split;
@@ -469,24 +494,27 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     for (int i = 0; i < 2; ++i) {
       mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
       mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
-      const float mn = fmaxf(m[i], mx[i]);
-      alpha[i] = (mn == -INFINITY) ? 1.f : expf(m[i] - mn);
+      const float mn = mx[i] > m[i] + kLazy ? mx[i] : m[i];
+      alpha[i] = mn == m[i] ? 1.f : ex2(m[i] - mn);
       m[i] = mn;
     }
     // p = exp(x - m) in FP32, kept in s; the denominator sums these FP32 p
-    float rs[2] = {0.f, 0.f};
+    // (per thread and row: one chain over the keys of each tile half, key
+    // ascending, the two added; then the quad's four sums as (0+1) + (2+3))
+    float rs[2] = {0.f, 0.f}, rb[2] = {0.f, 0.f};
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = e >> 1;
-        const float pe = (m[i] == -INFINITY) ? 0.f : expf(s[nt][e] - m[i]);
+        const float pe = (m[i] == -INFINITY) ? 0.f : ex2(s[nt][e] - m[i]);
         s[nt][e] = pe;
-        rs[i] += pe;
+        if (nt < 4) rs[i] += pe; else rb[i] += pe;
       }
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
+      rs[i] = rs[i] + rb[i];
       rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
       rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
       l[i] = __fmaf_rn(l[i], alpha[i], rs[i]);
@@ -602,19 +630,23 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
 // Prefill attention on tcgen05.  A CTA takes up to 128 query vectors of one
 // query block and one KV head (the M = 128 rows of the MMA) over one KV split.
 // Per 64-key tile: S = Q . K^T into one of two TMEM buffers (K steps of 16
-// over the head dimension, ascending); the online softmax by four warps with
-// one thread per vector, doing attn_kernel's FP32 operations in attn_kernel's
-// order element for element; P's three bf16 parts into shared memory; and
-// O += P . V accumulated in TMEM (per 16-key step hi, mid, lo).  One K = 16
-// tcgen05 MMA rounds exactly as one mma.sync m16n8k16 on the same operands
-// and accumulator (checked bit for bit on GB300, including wide exponent
-// ranges and cancellation), so a vector's output has the same bits whichever
-// kernel runs it: prefill rows here, decode rows in attn_kernel.
+// over the head dimension, ascending); the online softmax, doing attn_kernel's
+// FP32 operations in attn_kernel's order element for element; P's three bf16
+// parts into one of two shared-memory buffers; and O += P . V accumulated in
+// TMEM (per 16-key step hi, mid, lo).  One K = 16 tcgen05 MMA rounds exactly
+// as one mma.sync m16n8k16 on the same operands and accumulator (checked bit
+// for bit on GB300, including wide exponent ranges and cancellation), so a
+// vector's output has the same bits whichever kernel runs it: prefill rows
+// here, decode rows in attn_kernel.
 // V is read in place from its TMA tile ([key][dim], 128-byte swizzled) as an
-// MN-major operand.  O starts at +0 in TMEM and every P.V MMA accumulates,
-// as attn_kernel's register accumulators do.
-// Warps: 0 = TMA producer, 1 = MMA issuer and TMEM owner, 2..5 = softmax and
-// epilogue (TMEM lane quarter warp % 4, vector 32 * (warp % 4) + lane).
+// MN-major operand.  O starts at +0 in TMEM and every P.V MMA accumulates, as
+// attn_kernel's register accumulators do.
+// Warps: 0 = TMA producer, 1 = MMA issuer and TMEM owner, 2..9 = softmax and
+// epilogue.  Softmax warp w reads TMEM lane quarter w % 4 (vector
+// 32 * (w % 4) + lane) and tile half hf = (w - 2) / 4: keys [32 hf, 32 hf + 32)
+// of S, the same half of P, and head dimensions [hf D/2, (hf + 1) D/2) of O.
+// The two warps of a quarter exchange their row maxima and their denominator
+// chains through shared memory, with one named barrier per tile.
 template <int D>
 struct TcCfg {
   static constexpr int NV = 128;                  // query vectors per CTA (MMA rows)
@@ -623,28 +655,39 @@ struct TcCfg {
   static constexpr int KV_BYTES = kTile * D * 2;  // one K or V tile
   static constexpr int P_BYTES = NV * kTile * 2;  // one bf16 part of P
   static constexpr int STK = 2, STV = 2;
-  static constexpr int NBARS = 15;
-  static constexpr int SMEM = 1024 + Q_BYTES + (STK + STV) * KV_BYTES + 3 * P_BYTES + NBARS * 8 + 16;
+  static constexpr int NBARS = 21;   // 17 pipeline barriers + one exchange per lane quarter
+  // row exchange between the two halves: [2 tiles][2 halves][NV] maxima and
+  // [2 tiles][2 halves][4 chains][NV] denominator chains
+  static constexpr int XCH_BYTES = (2 * 2 * NV + 2 * 2 * 4 * NV) * 4;
+  // P: two buffers of three parts (the softmax of tile t+1 fills one while
+  // P.V of tile t reads the other)
+  static constexpr int SMEM =
+      1024 + Q_BYTES + (STK + STV) * KV_BYTES + 6 * P_BYTES + XCH_BYTES + NBARS * 8 + 16;
   static constexpr uint32_t TMEM_COLS = 256;      // S double buffer (2 x 64) + O (D)
   static constexpr uint32_t O_COL = 2 * kTile;
-  static constexpr int THREADS = 192;
+  static constexpr int SOFT_WARPS = 8;
+  static constexpr int THREADS = 64 + 32 * SOFT_WARPS;
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ AttnArgs a) {
   pdl_wait();     // stream predecessor done, its writes visible
   pdl_trigger();
   using Cfg = TcCfg<D>;
   constexpr int KVB = Cfg::KV_BYTES, PB = Cfg::P_BYTES, STK = Cfg::STK, STV = Cfg::STV;
+  constexpr int NV = Cfg::NV, SOFTW = Cfg::SOFT_WARPS;
   enum { Q_FULL = 0, K_FULL = 1, K_EMPTY = 3, V_FULL = 5, V_EMPTY = 7, S_FULL = 9, S_EMPTY = 11,
-         P_FULL = 13, PV_DONE = 14 };
+         P_FULL = 13, PV_DONE = 15 };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sQ = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
   uint8_t* sK = sQ + Cfg::Q_BYTES;
   uint8_t* sV = sK + STK * KVB;
-  uint8_t* sP = sV + STV * KVB;                    // parts hi, mid, lo
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 3 * PB);
+  uint8_t* sP = sV + STV * KVB;                    // [2][hi, mid, lo]
+  float* xmax = reinterpret_cast<float*>(sP + 6 * PB);   // [2][2][NV]
+  float* xsum = xmax + 2 * 2 * NV;                        // [2][2][4][NV]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xsum + 2 * 2 * 4 * NV);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NBARS);
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
@@ -654,19 +697,8 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
   const int nv = nr * a.G;
   const int seq = a.row_seq[r0];
 
-  // block's largest position; rows whose position is out of bounds are
-  // reported and left out (as in attn_kernel)
-  int maxpos = -1;
-  for (int r = 0; r < nr; ++r) {
-    const int p = a.row_pos[r0 + r];
-    if (row_pos_ok(a, p)) {
-      maxpos = max(maxpos, p);
-    } else if (split == 0) {
-      if (tid == 0) raise_error(a.err, kErrBadIndex);
-      uint16_t* dst = a.out + int64_t(r0 + r) * a.out_stride + int64_t(h * a.G) * D;
-      for (int i = tid; i < a.G * D; i += Cfg::THREADS) dst[i] = 0x7FC0;  // bf16 NaN
-    }
-  }
+  __shared__ int s_maxpos;
+  const int maxpos = block_maxpos<D>(a, r0, nr, h, split, &s_maxpos);
   const int lo = split * a.kv_split;
   const int hi = min(maxpos + 1, lo + a.kv_split);
   if (lo >= hi) return;  // uniform: nothing of this block lives in this split
@@ -680,10 +712,11 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       mbar_init(bar(V_FULL + s), 1);
       mbar_init(bar(V_EMPTY + s), 1);
       mbar_init(bar(S_FULL + s), 1);
-      mbar_init(bar(S_EMPTY + s), 4);
+      mbar_init(bar(S_EMPTY + s), SOFTW);
+      mbar_init(bar(P_FULL + s), SOFTW);
+      mbar_init(bar(PV_DONE + s), 1);
     }
-    mbar_init(bar(P_FULL), 4);
-    mbar_init(bar(PV_DONE), 1);
+    for (int q = 0; q < 4; ++q) mbar_init(bar(Cfg::NBARS - 4 + q), 2);   // one arrival per half
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -695,7 +728,6 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   int issued_k = 0, issued_v = 0;
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
@@ -751,10 +783,11 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       for (int t = 0; t < ntiles && ok; ++t) {
         if (t + 1 < ntiles && !(ok = issue_s(t + 1))) break;
         // O += P(t) . V(t): per 16-key step the hi, mid and lo parts
-        if (!(ok = mbar_wait(bar(P_FULL), t & 1, a.err))) break;
+        const int pb = t & 1;
+        if (!(ok = mbar_wait(bar(P_FULL + pb), (t >> 1) & 1, a.err))) break;
         tc_fence_after();
         const int sv = t % STV;
-        const uint32_t v0 = smem_u32(sV + sv * KVB), p0 = smem_u32(sP);
+        const uint32_t v0 = smem_u32(sV + sv * KVB), p0 = smem_u32(sP + pb * 3 * PB);
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks) {
           const uint64_t vd = sdesc_mn_sw128(v0 + ks * 2048, 8192, 1024);
@@ -763,80 +796,118 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
             umma_f16(tmem + Cfg::O_COL, sdesc_k_sw128(p0 + part * PB + ks * 32), vd, idO, 1u);
         }
         umma_commit(bar(V_EMPTY + sv));
-        umma_commit(bar(PV_DONE));
+        umma_commit(bar(PV_DONE + pb));
       }
     }
   } else {
     // ------------------------------------------------- softmax, epilogue --
-    const int qtr = warp & 3;
+    const int qtr = warp & 3, hf = (warp - 2) >> 2;
     const int v = qtr * 32 + lane;
     const uint32_t lane_off = uint32_t(qtr * 32) << 16;
+    constexpr int DH = D / 2;                      // O columns of one half
+    const uint32_t o_col = Cfg::O_COL + hf * DH;
+    const uint32_t xbar = bar(Cfg::NBARS - 4 + qtr);   // the quarter's exchange
     int vpos = v < nv ? a.row_pos[r0 + v / a.G] : -1;
     if (!row_pos_ok(a, vpos)) vpos = -1;   // sees no key; output already NaN
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+    float cs[4] = {0.f, 0.f, 0.f, 0.f};    // this half's denominator chains of the last tile
     {
       uint32_t z[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) z[i] = 0u;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_st32(tmem + Cfg::O_COL + lane_off + c * 32, z);
+      for (int c = 0; c < DH / 32; ++c) tmem_st32(tmem + o_col + lane_off + c * 32, z);
       tmem_st_wait();
     }
     uint8_t* myP = sP + (v >> 3) * 1024 + (v & 7) * 128;   // row v of each part
+    // rs of a tile from both halves' chains: c = A_c + B_c, (c0 + c1) + (c2 + c3)
+    auto tile_sum = [&](int slot) {
+      float c[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float other = xsum[((slot * 2 + (hf ^ 1)) * 4 + k) * NV + v];
+        c[k] = hf == 0 ? cs[k] + other : other + cs[k];
+      }
+      return (c[0] + c[1]) + (c[2] + c[3]);
+    };
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
-      const int sb = t & 1, tbase = lo + t * kTile;
+      const int sb = t & 1, tbase = lo + t * kTile, slot = t & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(S_FULL + sb), (t >> 1) & 1, a.err))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[kTile];
+      float s[32];
       {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(tmem + sb * kTile + lane_off, ra);
-        tmem_ld32(tmem + sb * kTile + lane_off + 32, rb);
+        uint32_t r[32];
+        tmem_ld32(tmem + sb * kTile + hf * 32 + lane_off, r);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(ra[i]);
-          s[32 + i] = __uint_as_float(rb[i]);
-        }
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(S_EMPTY + sb));
-      // mask: key tbase + j is seen when it lies below hi and at or before vpos
-      const int lim = vpos < 0 ? -1 : min(hi - 1, vpos) - tbase;
-      float mx = -INFINITY;
+      // mask: key tbase + j is seen when it lies below hi and at or before
+      // vpos; this half holds keys j = 32 hf + i
+      const int lim = (vpos < 0 ? -1 : min(hi - 1, vpos) - tbase) - hf * 32;
+      float m8[8];
 #pragma unroll
-      for (int j = 0; j < kTile; ++j) {
-        const float x = j <= lim ? s[j] * a.scale : -INFINITY;
-        s[j] = x;
-        mx = fmaxf(mx, x);
-      }
-      const float mn = fmaxf(m, mx);
-      const float alpha = (mn == -INFINITY) ? 1.f : expf(m - mn);
-      m = mn;
-      // p in FP32; the denominator as attn_kernel sums it: four chains (key
-      // mod 8 in {2c, 2c+1}, key ascending), then (c0 + c1) + (c2 + c3)
-      float cs[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t ph[kTile / 2], pm[kTile / 2], pl[kTile / 2];
+      for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+      if (lim >= 31) {
 #pragma unroll
-      for (int nt = 0; nt < kTile / 8; ++nt) {
+        for (int i = 0; i < 32; ++i) {
+          s[i] = s[i] * a.scale;
+          m8[i & 7] = fmaxf(m8[i & 7], s[i]);
+        }
+      } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int j = nt * 8 + 2 * c;
-          const float p0 = (m == -INFINITY) ? 0.f : expf(s[j] - m);
-          const float p1 = (m == -INFINITY) ? 0.f : expf(s[j + 1] - m);
-          cs[c] += p0;
-          cs[c] += p1;
-          split3(p0, p1, ph[j / 2], pm[j / 2], pl[j / 2]);
+        for (int i = 0; i < 32; ++i) {
+          const float x = i <= lim ? s[i] * a.scale : -INFINITY;
+          s[i] = x;
+          m8[i & 7] = fmaxf(m8[i & 7], x);
         }
       }
-      l = __fmaf_rn(l, alpha, (cs[0] + cs[1]) + (cs[2] + cs[3]));
-      // P.V of tile t-1 is done: O and the P buffer are free
-      if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(PV_DONE), (t - 1) & 1, a.err))) {
+      // the row's max over both halves (exact in any order)
+      xmax[(slot * 2 + hf) * NV + v] = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar);
+      if (!__all_sync(0xffffffffu, mbar_wait(xbar, t & 1, a.err))) {
+        ok = false;
+        break;
+      }
+      const float mx = fmaxf(xmax[(slot * 2) * NV + v], xmax[(slot * 2 + 1) * NV + v]);
+      // the denominator of tile t-1, now that the other half's chains are in
+      if (t > 0) l = __fmaf_rn(l, alpha_prev, tile_sum(slot ^ 1));
+      const float mn = mx > m + kLazy ? mx : m;
+      const float alpha = mn == m ? 1.f : ex2(m - mn);
+      m = mn;
+      // p = 2^(x - m) in FP32, kept in s (no key seen yet: every x is -inf and
+      // p = 0); chain c sums keys 8 nt + 2c, 8 nt + 2c + 1 of this half, nt
+      // ascending (attn_kernel: each thread's chain over one tile half)
+      const float mm = (m == -INFINITY) ? 0.f : m;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) cs[k] = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int i = nt * 8 + 2 * c;
+          s[i] = ex2(s[i] - mm);
+          s[i + 1] = ex2(s[i + 1] - mm);
+          cs[c] += s[i];
+          cs[c] += s[i + 1];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) xsum[((slot * 2 + hf) * 4 + k) * NV + v] = cs[k];
+      alpha_prev = alpha;
+      // P buffer t % 2 is free once P.V of tile t-2 is done
+      const int pb = t & 1;
+      if (t >= 2 &&
+          !__all_sync(0xffffffffu, mbar_wait(bar(PV_DONE + pb), ((t - 2) >> 1) & 1, a.err))) {
         ok = false;
         break;
       }
@@ -851,44 +922,62 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       const int first_bad = hi - tbase;
       if (first_bad < kTile) {
         uint8_t* vt = sV + sv * KVB;
-        for (int i = tid - 64; i < (kTile - first_bad) * (D / 8); i += 128) {
+        for (int i = tid - 64; i < (kTile - first_bad) * (D / 8); i += 32 * SOFTW) {
           const int j = first_bad + i / (D / 8), c = i % (D / 8);
           const int dim = c * 8;
           *reinterpret_cast<uint4*>(vt + (dim >> 6) * 8192 + j * 128 +
                                     ((((dim & 63) >> 3) ^ (j & 7)) << 4)) = make_uint4(0, 0, 0, 0);
         }
       }
-      // rescale O when a row's max moved (a factor of exactly 1 is a no-op)
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      // rescale this half of O when a row's max moved (a factor of exactly 1
+      // is a no-op; before the first P.V, O is +0 and stays +0), after P.V of
+      // tile t-1
+      if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(bar(PV_DONE + (pb ^ 1)), ((t - 1) >> 1) & 1, a.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < DH / 32; ++c) {
           uint32_t r[32];
-          tmem_ld32(tmem + Cfg::O_COL + lane_off + c * 32, r);
+          tmem_ld32(tmem + o_col + lane_off + c * 32, r);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(tmem + Cfg::O_COL + lane_off + c * 32, r);
+          tmem_st32(tmem + o_col + lane_off + c * 32, r);
         }
         tmem_st_wait();
       }
-      // P's parts: row v, keys 8c .. 8c+7 in 16-byte chunk c (128-byte swizzle)
+      // this half of P's parts: row v, keys 8 gc .. 8 gc + 7 in 16-byte chunk gc
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t off = uint32_t((c ^ (v & 7)) << 4);
-        *reinterpret_cast<uint4*>(myP + off) =
-            make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
-        *reinterpret_cast<uint4*>(myP + PB + off) =
-            make_uint4(pm[4 * c], pm[4 * c + 1], pm[4 * c + 2], pm[4 * c + 3]);
-        *reinterpret_cast<uint4*>(myP + 2 * PB + off) =
-            make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t ph[4], pm[4], pl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          split3(s[8 * cc + 2 * e], s[8 * cc + 2 * e + 1], ph[e], pm[e], pl[e]);
+        const int gc = hf * 4 + cc;
+        uint8_t* dst = myP + pb * 3 * PB + ((gc ^ (v & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+        *reinterpret_cast<uint4*>(dst + PB) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
+        *reinterpret_cast<uint4*>(dst + 2 * PB) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
       }
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(P_FULL));
+      if (lane == 0) mbar_arrive(bar(P_FULL + pb));
     }
+    // the last tile's denominator (its chains cross once more)
+    if (ok) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar);
+      if (!__all_sync(0xffffffffu, mbar_wait(xbar, ntiles & 1, a.err))) ok = false;
+    }
+    if (ok) l = __fmaf_rn(l, alpha_prev, tile_sum((ntiles - 1) & 1));
     // ---- epilogue: single-split rows write the final output, others partials
-    if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(PV_DONE), (ntiles - 1) & 1, a.err)))
+    if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(PV_DONE + ((ntiles - 1) & 1)),
+                                                 ((ntiles - 1) >> 1) & 1, a.err)))
       ok = false;
     tc_fence_after();
     if (ok) {
@@ -898,14 +987,15 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       const int64_t slot = (int64_t(row) * a.Hq + head) * a.nsplit_grid + split;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DH / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + Cfg::O_COL + lane_off + c * 32, r);   // warp-collective
+        tmem_ld32(tmem + o_col + lane_off + c * 32, r);   // warp-collective
         tmem_ld_wait();
         if (!mine) continue;
+        const int d0 = hf * DH + c * 32;
         if (ns == 1) {
           uint4* dst = reinterpret_cast<uint4*>(a.out + int64_t(row) * a.out_stride +
-                                                int64_t(head) * D + c * 32);
+                                                int64_t(head) * D + d0);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t pk[4];
@@ -918,14 +1008,14 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
             dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         } else {
-          float4* wo = reinterpret_cast<float4*>(a.ws_o + slot * D + c * 32);
+          float4* wo = reinterpret_cast<float4*>(a.ws_o + slot * D + d0);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             wo[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
         }
       }
-      if (mine && ns > 1) {
+      if (mine && ns > 1 && hf == 0) {
         a.ws_ml[2 * slot] = m;
         a.ws_ml[2 * slot + 1] = l;
       }
@@ -973,7 +1063,7 @@ __global__ void attn_merge_kernel(const __grid_constant__ AttnArgs a) {
   for (int s = 0; s < ns; ++s) {
     const float ms = a.ws_ml[2 * (base + s)];
     if (ms == -INFINITY) continue;
-    const float w = expf(ms - M);
+    const float w = ex2(ms - M);
     L += w * a.ws_ml[2 * (base + s) + 1];
     const float* o = a.ws_o + (base + s) * D;
 #pragma unroll
@@ -1229,7 +1319,7 @@ biv_status biv_attention(const biv_attn_desc* d, void* ws, size_t wsb, biv_strea
   a.bt = d->block_table; a.max_pages = d->max_pages;
   a.kv_split = split;
   a.topk_idx = d->topk_idx; a.topk_stride = d->topk_stride; a.topk = d->topk;
-  a.scale = d->scale;
+  a.scale = float(double(d->scale) * 1.4426950408889634);   // log2(e)
   a.nsplit_grid = (span + split - 1) / split;
   a.ws_o = static_cast<float*>(ws);
   a.ws_ml = a.ws_o ? a.ws_o + size_t(d->T) * d->Hq * a.nsplit_grid * d->D : nullptr;
