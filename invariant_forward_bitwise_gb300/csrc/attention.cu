@@ -632,8 +632,8 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
 // Per 64-key tile: S = Q . K^T into one of two TMEM buffers (K steps of 16
 // over the head dimension, ascending); the online softmax, doing attn_kernel's
 // FP32 operations in attn_kernel's order element for element; P's three bf16
-// parts into one of two shared-memory buffers; and O += P . V accumulated in
-// TMEM (per 16-key step hi, mid, lo).  One K = 16 tcgen05 MMA rounds exactly
+// parts into one of two TMEM buffers; and O += P . V accumulated in TMEM with
+// P read from TMEM as the A operand (per 16-key step hi, mid, lo).  One K = 16 tcgen05 MMA rounds exactly
 // as one mma.sync m16n8k16 on the same operands and accumulator (checked bit
 // for bit on GB300, including wide exponent ranges and cancellation), so a
 // vector's output has the same bits whichever kernel runs it: prefill rows
@@ -653,18 +653,19 @@ struct TcCfg {
   static constexpr int PANEL = NV * 128;          // one 64-dim panel of Q
   static constexpr int Q_BYTES = NV * D * 2;
   static constexpr int KV_BYTES = kTile * D * 2;  // one K or V tile
-  static constexpr int P_BYTES = NV * kTile * 2;  // one bf16 part of P
-  static constexpr int STK = 2, STV = 2;
-  static constexpr int NBARS = 21;   // 17 pipeline barriers + one exchange per lane quarter
+  static constexpr int STK = 3, STV = 3;
+  static constexpr int NBARS = 21 + 4;   // pipeline barriers + one exchange per lane quarter
   // row exchange between the two halves: [2 tiles][2 halves][NV] maxima and
   // [2 tiles][2 halves][4 chains][NV] denominator chains
   static constexpr int XCH_BYTES = (2 * 2 * NV + 2 * 2 * 4 * NV) * 4;
-  // P: two buffers of three parts (the softmax of tile t+1 fills one while
-  // P.V of tile t reads the other)
-  static constexpr int SMEM =
-      1024 + Q_BYTES + (STK + STV) * KV_BYTES + 6 * P_BYTES + XCH_BYTES + NBARS * 8 + 16;
-  static constexpr uint32_t TMEM_COLS = 256;      // S double buffer (2 x 64) + O (D)
+  static constexpr int SMEM = 1024 + Q_BYTES + (STK + STV) * KV_BYTES + XCH_BYTES + NBARS * 8 + 16;
+  // TMEM: S double buffer (2 x 64 columns), O (D), and P as the A operand of
+  // P.V: two buffers (the softmax of tile t+1 fills one while P.V of tile t
+  // reads the other) of three parts, each 64 bf16 keys packed in 32 columns
+  static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 2 * kTile;
+  static constexpr uint32_t P_COL = O_COL + 128;
+  static_assert(P_COL + 6 * 32 <= TMEM_COLS, "TMEM budget");
   static constexpr int SOFT_WARPS = 8;
   static constexpr int THREADS = 64 + 32 * SOFT_WARPS;
 };
@@ -675,17 +676,18 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   pdl_wait();     // stream predecessor done, its writes visible
   pdl_trigger();
   using Cfg = TcCfg<D>;
-  constexpr int KVB = Cfg::KV_BYTES, PB = Cfg::P_BYTES, STK = Cfg::STK, STV = Cfg::STV;
+  constexpr int KVB = Cfg::KV_BYTES, STK = Cfg::STK, STV = Cfg::STV;
   constexpr int NV = Cfg::NV, SOFTW = Cfg::SOFT_WARPS;
-  enum { Q_FULL = 0, K_FULL = 1, K_EMPTY = 3, V_FULL = 5, V_EMPTY = 7, S_FULL = 9, S_EMPTY = 11,
-         P_FULL = 13, PV_DONE = 15 };
+  enum { Q_FULL = 0, K_FULL = 1, K_EMPTY = K_FULL + STK, V_FULL = K_EMPTY + STK,
+         V_EMPTY = V_FULL + STV, S_FULL = V_EMPTY + STV, S_EMPTY = S_FULL + 2, P_FULL = S_EMPTY + 2,
+         PV_DONE = P_FULL + 2, XCH = PV_DONE + 2 };
+  static_assert(XCH + 4 == Cfg::NBARS, "barrier count");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sQ = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
   uint8_t* sK = sQ + Cfg::Q_BYTES;
   uint8_t* sV = sK + STK * KVB;
-  uint8_t* sP = sV + STV * KVB;                    // [2][hi, mid, lo]
-  float* xmax = reinterpret_cast<float*>(sP + 6 * PB);   // [2][2][NV]
+  float* xmax = reinterpret_cast<float*>(sV + STV * KVB);   // [2][2][NV]
   float* xsum = xmax + 2 * 2 * NV;                        // [2][2][4][NV]
   uint64_t* bars = reinterpret_cast<uint64_t*>(xsum + 2 * 2 * 4 * NV);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NBARS);
@@ -706,17 +708,21 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 
   if (tid == 0) {
     mbar_init(bar(Q_FULL), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < STK; ++s) {
       mbar_init(bar(K_FULL + s), 1);
       mbar_init(bar(K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < STV; ++s) {
       mbar_init(bar(V_FULL + s), 1);
       mbar_init(bar(V_EMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(S_FULL + s), 1);
       mbar_init(bar(S_EMPTY + s), SOFTW);
       mbar_init(bar(P_FULL + s), SOFTW);
       mbar_init(bar(PV_DONE + s), 1);
     }
-    for (int q = 0; q < 4; ++q) mbar_init(bar(Cfg::NBARS - 4 + q), 2);   // one arrival per half
+    for (int q = 0; q < 4; ++q) mbar_init(bar(XCH + q), 2);   // one arrival per half
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -738,19 +744,28 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 #pragma unroll
       for (int hh = 0; hh < D / 64; ++hh)
         tma_load_3d(smem_u32(sQ + hh * Cfg::PANEL), &a.tmQ, bar(Q_FULL), hh * 64, h * a.G, r0);
-      for (int t = 0; t < ntiles; ++t) {
-        const int tbase = lo + t * kTile;
-        const int page = a.bt[int64_t(seq) * a.max_pages + tbase / kTile];
-        const int sk = t % STK, sv = t % STV;
-        if (t >= STK && !mbar_wait(bar(K_EMPTY + sk), ((t / STK) - 1) & 1, a.err)) break;
+      // K runs two tiles ahead of V (S(t+2) is issued before P.V(t)), so a K
+      // load never queues behind a V stage that P.V still holds
+      auto page_of = [&](int t) { return a.bt[int64_t(seq) * a.max_pages + (lo + t * kTile) / kTile]; };
+      auto load_k = [&](int t) -> bool {
+        const int sk = t % STK;
+        if (t >= STK && !mbar_wait(bar(K_EMPTY + sk), ((t / STK) - 1) & 1, a.err)) return false;
         mbar_expect_tx(bar(K_FULL + sk), KVB);
+        const int page = page_of(t);
 #pragma unroll
         for (int hh = 0; hh < D / 64; ++hh)
           tma_load_2d(smem_u32(sK + sk * KVB + hh * 8192), &a.tmK, bar(K_FULL + sk),
                       h * D + hh * 64, page * kTile);
         ++issued_k;
+        return true;
+      };
+      bool ok = load_k(0) && (ntiles < 2 || load_k(1));
+      for (int t = 0; t < ntiles && ok; ++t) {
+        if (t + 2 < ntiles && !(ok = load_k(t + 2))) break;
+        const int sv = t % STV;
         if (t >= STV && !mbar_wait(bar(V_EMPTY + sv), ((t / STV) - 1) & 1, a.err)) break;
         mbar_expect_tx(bar(V_FULL + sv), KVB);
+        const int page = page_of(t);
 #pragma unroll
         for (int hh = 0; hh < D / 64; ++hh)
           tma_load_2d(smem_u32(sV + sv * KVB + hh * 8192), &a.tmV, bar(V_FULL + sv),
@@ -779,21 +794,24 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         umma_commit(bar(S_FULL + sb));
         return true;
       };
-      bool ok = mbar_wait(bar(Q_FULL), 0, a.err) && issue_s(0);
+      // S runs two tiles ahead of P.V: S(t+2) enters the pipe as soon as the
+      // softmax of tile t has read S(t) from the same buffer, ahead of
+      // P.V(t), so a tile's softmax never waits behind a P.V
+      bool ok = mbar_wait(bar(Q_FULL), 0, a.err) && issue_s(0) && (ntiles < 2 || issue_s(1));
       for (int t = 0; t < ntiles && ok; ++t) {
-        if (t + 1 < ntiles && !(ok = issue_s(t + 1))) break;
+        if (t + 2 < ntiles && !(ok = issue_s(t + 2))) break;
         // O += P(t) . V(t): per 16-key step the hi, mid and lo parts
         const int pb = t & 1;
         if (!(ok = mbar_wait(bar(P_FULL + pb), (t >> 1) & 1, a.err))) break;
         tc_fence_after();
         const int sv = t % STV;
-        const uint32_t v0 = smem_u32(sV + sv * KVB), p0 = smem_u32(sP + pb * 3 * PB);
+        const uint32_t v0 = smem_u32(sV + sv * KVB), p0 = tmem + Cfg::P_COL + pb * 3 * 32;
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks) {
           const uint64_t vd = sdesc_mn_sw128(v0 + ks * 2048, 8192, 1024);
 #pragma unroll
           for (int part = 0; part < 3; ++part)
-            umma_f16(tmem + Cfg::O_COL, sdesc_k_sw128(p0 + part * PB + ks * 32), vd, idO, 1u);
+            umma_f16_ts(tmem + Cfg::O_COL, p0 + part * 32 + ks * 8, vd, idO, 1u);
         }
         umma_commit(bar(V_EMPTY + sv));
         umma_commit(bar(PV_DONE + pb));
@@ -806,7 +824,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     const uint32_t lane_off = uint32_t(qtr * 32) << 16;
     constexpr int DH = D / 2;                      // O columns of one half
     const uint32_t o_col = Cfg::O_COL + hf * DH;
-    const uint32_t xbar = bar(Cfg::NBARS - 4 + qtr);   // the quarter's exchange
+    const uint32_t xbar = bar(XCH + qtr);   // the quarter's exchange
     int vpos = v < nv ? a.row_pos[r0 + v / a.G] : -1;
     if (!row_pos_ok(a, vpos)) vpos = -1;   // sees no key; output already NaN
     float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
@@ -819,7 +837,6 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       for (int c = 0; c < DH / 32; ++c) tmem_st32(tmem + o_col + lane_off + c * 32, z);
       tmem_st_wait();
     }
-    uint8_t* myP = sP + (v >> 3) * 1024 + (v & 7) * 128;   // row v of each part
     // rs of a tile from both halves' chains: c = A_c + B_c, (c0 + c1) + (c2 + c3)
     auto tile_sum = [&](int slot) {
       float c[4];
@@ -950,20 +967,19 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         }
         tmem_st_wait();
       }
-      // this half of P's parts: row v, keys 8 gc .. 8 gc + 7 in 16-byte chunk gc
+      // this half of P's parts into TMEM: lane v, column 16 hf + c holds keys
+      // 32 hf + 2c (low half) and 32 hf + 2c + 1
+      {
+        uint32_t ph[16], pm[16], pl[16];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t ph[4], pm[4], pl[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          split3(s[8 * cc + 2 * e], s[8 * cc + 2 * e + 1], ph[e], pm[e], pl[e]);
-        const int gc = hf * 4 + cc;
-        uint8_t* dst = myP + pb * 3 * PB + ((gc ^ (v & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-        *reinterpret_cast<uint4*>(dst + PB) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
-        *reinterpret_cast<uint4*>(dst + 2 * PB) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        for (int c = 0; c < 16; ++c) split3(s[2 * c], s[2 * c + 1], ph[c], pm[c], pl[c]);
+        const uint32_t pc = tmem + Cfg::P_COL + pb * 3 * 32 + hf * 16 + lane_off;
+        tmem_st16(pc, ph);
+        tmem_st16(pc + 32, pm);
+        tmem_st16(pc + 64, pl);
+        tmem_st_wait();
       }
-      fence_proxy_async();
+      if (first_bad < kTile) fence_proxy_async();   // zeroed V rows, for the MMA
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(P_FULL + pb));
