@@ -147,6 +147,7 @@ struct GemmArgs {
   int vec_ok;           // C rows 16-byte aligned
   int n_fastest;        // fold mode: walk N tiles first
   int b_after_wait;     // 1: B is written by the previous kernel (no early prefetch)
+  int kpb;              // K blocks of 64 per pipeline stage (2: 3-D maps, two panels per copy)
   // log-softmax epilogue (LSE instantiation): per row and 128-column group g
   // of the output, (max, sum of exp(z - max)) to lse[row * ngroups + g]; the
   // logit at target[row] to zt[row]
@@ -178,8 +179,8 @@ struct GemmSmem {
   static constexpr int B_STAGE = BN * 128;
   // bytes of dynamic shared memory for `stages` stages of an m_box-row A box
   // (the store staging blocks only in fold mode)
-  static size_t bytes(int stages, int m_box, bool staging) {
-    return 1024 + size_t(stages) * (B_STAGE + m_box * 128) + (128 - m_box) * 128 +
+  static size_t bytes(int stages, int m_box, bool staging, int kpb = 1) {
+    return 1024 + size_t(stages) * kpb * (B_STAGE + m_box * 128) + (128 - m_box) * 128 +
            (2 * kMaxStages + 4) * 8 + 16 + (staging ? kStagingBytes : 0);
   }
 };
@@ -203,9 +204,11 @@ __global__ void __launch_bounds__(kGemmThreads, PARTIAL ? 2 : 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int S = p.stages;
-  const int a_stage = p.m_box * 128;
+  // a stage holds kpb K blocks of 64: [block][rows][128 B] for A and for B
+  const int a_blk = p.m_box * 128, b_blk = B_STAGE;
+  const int a_stage = a_blk * p.kpb, b_stage = b_blk * p.kpb;
   uint8_t* sB = smem;
-  uint8_t* sA = smem + S * B_STAGE;
+  uint8_t* sA = smem + S * b_stage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sA + S * a_stage + (128 - p.m_box) * 128);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
   const uint32_t tfull0 = smem_u32(bars + 2 * kMaxStages);
@@ -256,36 +259,47 @@ __global__ void __launch_bounds__(kGemmThreads, PARTIAL ? 2 : 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
-      const uint32_t tx = uint32_t(a_stage + B_STAGE);
+      const uint32_t tx = uint32_t(a_stage + b_stage);
+      // one stage = K blocks [kb, kb + kpb) of one chunk (a chunk's odd last
+      // block leaves the stage's second block unused)
+      auto load = [&](const CUtensorMap* map, uint8_t* dst, int kb, int row0, uint32_t bar) {
+        if (p.kpb == 2)
+          tma_load_3d(smem_u32(dst), map, bar, 0, row0, kb);
+        else
+          tma_load_2d(smem_u32(dst), map, bar, kb * 64, row0);
+      };
       // The weights (B) of the first stages do not depend on the previous
       // kernel: fetch them before waiting for it, then A and the rest.
       int pre = 0;
       if (!p.b_after_wait) {
         const int i = blockIdx.x, n0 = tile_n0(item_tile(i));
-        const int kb0 = item_c0(i) * p.kc_blocks;
-        pre = min(S, min(KB, item_c1(i) * p.kc_blocks) - kb0);
-        for (int s = 0; s < pre; ++s) {
-          mbar_expect_tx(full0 + 8 * s, tx);
-          tma_load_2d(smem_u32(sB + s * B_STAGE), &tmB, full0 + 8 * s, (kb0 + s) * 64, n0);
+        for (int c = item_c0(i); c < item_c1(i) && pre < S; ++c) {
+          const int kb1 = min(KB, (c + 1) * p.kc_blocks);
+          for (int kb = c * p.kc_blocks; kb < kb1 && pre < S; kb += p.kpb, ++pre) {
+            mbar_expect_tx(full0 + 8 * pre, tx);
+            load(&tmB, sB + pre * b_stage, kb, n0, full0 + 8 * pre);
+          }
         }
       }
       pdl_wait();
       bool ok = true;
       for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
         const int t = item_tile(i), m0 = tile_m0(t), n0 = tile_n0(t);
-        const int kb1 = min(KB, item_c1(i) * p.kc_blocks);
-        for (int kb = item_c0(i) * p.kc_blocks; kb < kb1; ++kb) {
-          const int s = issued % S;
-          if (issued >= pre) {
-            if (issued >= S && !mbar_wait(empty0 + 8 * s, ((issued / S) - 1) & 1, p.err)) {
-              ok = false;
-              break;
+        for (int c = item_c0(i); c < item_c1(i) && ok; ++c) {
+          const int kb1 = min(KB, (c + 1) * p.kc_blocks);
+          for (int kb = c * p.kc_blocks; kb < kb1; kb += p.kpb) {
+            const int s = issued % S;
+            if (issued >= pre) {
+              if (issued >= S && !mbar_wait(empty0 + 8 * s, ((issued / S) - 1) & 1, p.err)) {
+                ok = false;
+                break;
+              }
+              mbar_expect_tx(full0 + 8 * s, tx);
+              load(&tmB, sB + s * b_stage, kb, n0, full0 + 8 * s);
             }
-            mbar_expect_tx(full0 + 8 * s, tx);
-            tma_load_2d(smem_u32(sB + s * B_STAGE), &tmB, full0 + 8 * s, kb * 64, n0);
+            load(&tmA, sA + s * a_stage, kb, m0, full0 + 8 * s);
+            ++issued;
           }
-          tma_load_2d(smem_u32(sA + s * a_stage), &tmA, full0 + 8 * s, kb * 64, m0);
-          ++issued;
         }
       }
     }
@@ -304,19 +318,22 @@ __global__ void __launch_bounds__(kGemmThreads, PARTIAL ? 2 : 1)
           tc_fence_after();
           const uint32_t dt = tmem + b * BN;
           const int kb0 = c * p.kc_blocks, kb1 = min(KB, kb0 + p.kc_blocks);
-          for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          for (int kb = kb0; kb < kb1; kb += p.kpb, ++it) {
             const int s = it % S;
             if (!mbar_wait(full0 + 8 * s, (it / S) & 1, p.err)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + s * a_stage);
-            const uint32_t b0 = smem_u32(sB + s * B_STAGE);
+            const int nb = min(p.kpb, kb1 - kb);
+            for (int q = 0; q < nb; ++q) {
+              const uint32_t a0 = smem_u32(sA + s * a_stage + q * a_blk);
+              const uint32_t b0 = smem_u32(sB + s * b_stage + q * b_blk);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_f16(dt, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
-                       (kb != kb0 || kk != 0) ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk)
+                umma_f16(dt, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
+                         (kb + q != kb0 || kk != 0) ? 1u : 0u);
+            }
             umma_commit(empty0 + 8 * s);
           }
           if (ok) umma_commit(tfull0 + 8 * b);
@@ -935,8 +952,29 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void
   return r == CUDA_SUCCESS;
 }
 
+// A bf16 K-major operand [rows, K] as a 3-D tensor {64, rows, K/64}: a box
+// {64, box_rows, 2} brings two consecutive K blocks in one copy, landing as
+// [block][row][128 B] with 128-byte swizzling (two ordinary stages back to
+// back).  Measured on GB300, one producer thread moves about 25 bytes per SM
+// clock in 2-D boxes of 128-byte rows, whatever the pipeline depth, and
+// twice that when each row brings two adjacent K blocks.  K % 64 == 0, so no
+// block reads past a row.
+bool make_map2k(CUtensorMap* m, const void* base, int64_t K, int64_t rows, int64_t ld,
+                int box_rows) {
+  auto fn = tensor_map_encoder();
+  if (!fn || K % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, cuuint64_t(rows), cuuint64_t(K / 64)};
+  cuuint64_t strides[2] = {cuuint64_t(ld * 2), 128};
+  cuuint32_t box[3] = {64, cuuint32_t(box_rows), 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct Plan {
   int bn = 256;
+  int kpb = 1;        // K blocks per pipeline stage
   int kc_blocks = 1;  // K blocks (of 64) per chunk
   int chunks = 1;
   bool partial = false;
@@ -975,6 +1013,23 @@ int env_fold() {  // 0 = planner, 1 = fold in the CTA, 2 = partials
   if (!strcmp(e, "cta")) return 1;
   if (!strcmp(e, "partial")) return 2;
   return 0;
+}
+
+// Two K blocks per stage when K is a whole number of blocks (BIV_GEMM_KPB=1
+// keeps one; the tests check that neither changes a bit).
+int kpb_for(int K) {
+  const char* e = getenv("BIV_GEMM_KPB");
+  if (e && atoi(e) == 1) return 1;
+  return (K % 64 == 0 && K >= 128) ? 2 : 1;
+}
+
+// Tensor maps of a bf16 call: 3-D two-block boxes when the plan takes them.
+bool make_bf16_maps(CUtensorMap* ta, CUtensorMap* tb, const void* A, int64_t lda, int64_t M,
+                    const void* B, int64_t ldb, int64_t N, int64_t K, const Plan& p) {
+  if (p.kpb == 2)
+    return make_map2k(ta, A, K, M, lda, p.m_box) && make_map2k(tb, B, K, N, ldb, p.bn);
+  return make_map(ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, p.m_box) &&
+         make_map(tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, ldb, 64, p.bn);
 }
 
 // INVARIANT: K cut into chunks of max(8, ceil(KB/8)) blocks for every M; the
@@ -1025,7 +1080,8 @@ Plan plan_bf16(const biv_gemm_desc& d) {
   p.tiles = int64_t((d.N + p.bn - 1) / p.bn) * tiles_m;
   // partial mode: more than one chunk, tiles of at most 128 columns
   p.partial = partial && p.chunks > 1 && p.bn <= 128;
-  const int a_stage = p.m_box * 128, b_stage = p.bn * 128;
+  p.kpb = kpb_for(d.K);
+  const int a_stage = p.m_box * 128 * p.kpb, b_stage = p.bn * 128 * p.kpb;
   const size_t fixed = GemmSmem<128>::bytes(0, p.m_box, !p.partial);
   const size_t budget = p.partial ? kSmemBudgetPartial : kSmemBudget;
   p.stages = int(std::min<size_t>(kMaxStages, (budget - fixed) / (a_stage + b_stage)));
@@ -1064,11 +1120,12 @@ biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_g
   a.vec_ok = aligned16(d.C) && (d.ldc * eb) % 16 == 0;
   a.n_fastest = !pl.partial && d.N <= d.M;
   a.b_after_wait = b_after_wait ? 1 : 0;
+  a.kpb = pl.kpb;
   a.err = device_error_word();
   const int64_t items = pl.partial ? pl.tiles * pl.chunks : pl.tiles;
   const int sms = sm_count() > 0 ? sm_count() : 148;
   const int grid = int(std::min<int64_t>(items, sms));
-  const size_t smem = GemmSmem<BN>::bytes(pl.stages, pl.m_box, !pl.partial);
+  const size_t smem = GemmSmem<BN>::bytes(pl.stages, pl.m_box, !pl.partial, pl.kpb);
   launch_pdl(kern, grid, kGemmThreads, smem, s, ta, tb, a);
   biv_status st = check_launch("gemm_bf16");
   if (st != BIV_OK || !pl.partial || d.defer_fold) return st;
@@ -1241,8 +1298,7 @@ biv_status biv_gemm_nvfp4(const uint16_t* A, int64_t lda, const uint8_t* codes,
     if (st != BIV_OK) return st;
     d.B = dec;
     CUtensorMap ta, tb;
-    if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, f.p.m_box) ||
-        !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dec, K, N, K, 64, f.p.bn))
+    if (!make_bf16_maps(&ta, &tb, A, lda, M, dec, K, N, K, f.p))
       return set_error(BIV_ERR_CUDA, "gemm_nvfp4: tensor map encoding failed");
     // the decoded weights come from the kernel just before: no early B prefetch
     void* pws = static_cast<uint8_t*>(ws) + f.dec_bytes;
@@ -1322,8 +1378,7 @@ biv_status biv_gemm(const biv_gemm_desc* d, void* ws, size_t ws_bytes, biv_strea
       return set_error(BIV_ERR_WORKSPACE, "gemm: workspace of %zu bytes needed", p.ws_bytes);
     if (p.ws_bytes && !aligned16(ws))
       return set_error(BIV_ERR_INVALID, "gemm: workspace must be 16-byte aligned");
-    if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->A, d->K, d->M, d->lda, 64, p.m_box) ||
-        !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->B, d->K, d->N, d->ldb, 64, p.bn))
+    if (!make_bf16_maps(&ta, &tb, d->A, d->lda, d->M, d->B, d->ldb, d->N, d->K, p))
       return set_error(BIV_ERR_CUDA, "gemm: tensor map encoding failed");
     return d->c_dtype == BIV_F32 ? dispatch_bf16<true>(ta, tb, *d, p, ws, s)
                                  : dispatch_bf16<false>(ta, tb, *d, p, ws, s);
@@ -1407,9 +1462,10 @@ Plan plan_lse(const biv_gemm_desc& d) {
   p.bn = kWideN;
   p.partial = false;
   p.tiles = int64_t((d.N + p.bn - 1) / p.bn) * ((d.M + BM - 1) / BM);
+  p.kpb = kpb_for(d.K);
   const size_t fixed = GemmSmem<kWideN>::bytes(0, p.m_box, true);
   p.stages = int(std::min<size_t>(kMaxStages, (kSmemBudget - fixed) /
-                                                  (p.m_box * 128 + GemmSmem<kWideN>::B_STAGE)));
+                                                  ((p.m_box * 128 + GemmSmem<kWideN>::B_STAGE) * p.kpb)));
   return p;
 }
 
@@ -1449,8 +1505,7 @@ extern "C" biv_status biv_lm_head_logprob(const uint16_t* h, int64_t ldh, const 
     return set_error(BIV_ERR_INVALID, "lm_head_logprob: workspace must be 16-byte aligned");
   const Plan p = plan_lse(d);
   CUtensorMap ta, tb;
-  if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, K, M, ldh, 64, p.m_box) ||
-      !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, K, V, ldw, 64, p.bn))
+  if (!make_bf16_maps(&ta, &tb, h, ldh, M, W, ldw, V, K, p))
     return set_error(BIV_ERR_CUDA, "lm_head_logprob: tensor map encoding failed");
   auto kern = gemm_bf16_kernel<kWideN, true, false, true>;
   static bool attr = false;
@@ -1463,7 +1518,7 @@ extern "C" biv_status biv_lm_head_logprob(const uint16_t* h, int64_t ldh, const 
   GemmArgs a;
   memset(&a, 0, sizeof(a));
   a.M = M; a.N = V; a.K = K;
-  a.kc_blocks = p.kc_blocks; a.m_box = p.m_box; a.stages = p.stages;
+  a.kc_blocks = p.kc_blocks; a.m_box = p.m_box; a.stages = p.stages; a.kpb = p.kpb;
   a.n_fastest = V <= M;
   a.target = target;
   a.lse = static_cast<float2*>(workspace);
@@ -1473,7 +1528,7 @@ extern "C" biv_status biv_lm_head_logprob(const uint16_t* h, int64_t ldh, const 
   const int sms = sm_count() > 0 ? sm_count() : 148;
   cudaStream_t s = as_cuda(stream);
   launch_pdl(kern, int(std::min<int64_t>(p.tiles, sms)), kGemmThreads,
-             GemmSmem<kWideN>::bytes(p.stages, p.m_box, true), s, ta, tb, a);
+             GemmSmem<kWideN>::bytes(p.stages, p.m_box, true, p.kpb), s, ta, tb, a);
   st = check_launch("lm_head_logprob gemm");
   if (st != BIV_OK) return st;
   launch_pdl(lse_combine_kernel, (M + kLseWarps - 1) / kLseWarps, kLseWarps * 32, 0, s,

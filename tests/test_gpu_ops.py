@@ -525,6 +525,31 @@ def test_tcgen05_result_independent_of_tile_width(B, monkeypatch, M, N, K):
     assert rel_err(got, ref) < REL
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 2048), (64, 2048, 6144), (256, 12288, 2048),
+                                   (300, 1000, 576), (2048, 2048, 2048)])
+@pytest.mark.parametrize("fold", ["cta", "partial"])
+def test_two_block_stages_change_no_bit(B, monkeypatch, M, N, K, fold):
+    """Pipeline stages of two K blocks (3-D TMA boxes) and of one K block feed
+    the same MMAs in the same order: every output bit is the same, folded in
+    the CTA or as partials (odd chunk tails included: K 576 is 9 blocks)."""
+    g = synth.rng(M + N * 3 + K)
+    a, b = rnd_bf16(g, M, K), rnd_bf16(g, N, K, std=0.05)
+    ad, bd = dev(a), dev(b)
+    monkeypatch.setenv("BIV_GEMM_FOLD", fold)
+    outs = []
+    for kpb in ["2", "1"]:
+        monkeypatch.setenv("BIV_GEMM_KPB", kpb)
+        d = B.gemm_desc(ad, bd, torch.empty(M, N, dtype=torch.float32, device="cuda"))
+        ws = torch.empty(max(B.biv_gemm_workspace(d), 16), dtype=torch.uint8, device="cuda")
+        c = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        B.biv_gemm(B.gemm_desc(ad, bd, c), ws)
+        outs.append(bits(c))
+    assert np.array_equal(outs[0], outs[1])
+    rows = np.unique(np.r_[0, M // 2, M - 1])
+    ref = ops.gemm(a[rows].float().numpy(), b.float().numpy(), out="f32")
+    assert rel_err(outs[0].view(np.float32).reshape(M, N)[rows], ref) < REL
+
+
 # ------------------------------------------------- fused GEMM consumers --
 def _deferred_gemm(B, ad, bd, M, N, ws):
     """GEMM whose fold is left to the consumer; returns the partials (chunks
