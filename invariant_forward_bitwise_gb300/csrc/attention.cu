@@ -17,8 +17,9 @@
 // position are fully masked and leave (m, l, acc) bitwise unchanged, and
 // masked V slots are zero in shared memory.
 //
-// Loads: dense bf16 pages (D = 64 or 128) arrive by TMA, one 2-D bulk copy
-// per 64-dim half of K and V, 128-byte swizzled, completed on an mbarrier;
+// Loads: dense bf16 pages (D = 64 or 128) arrive by TMA, one 3-D bulk copy
+// per page of K and of V (its 64-dim panels back to back), 128-byte
+// swizzled, completed on an mbarrier;
 // FP8 pages (dequantised on the way in), sparse gathers and D = 80 use
 // cp.async / plain loads into padded rows.
 #include <algorithm>
@@ -265,10 +266,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     uint8_t* dst = (which ? sV : sK) + buf * KVB;
     fence_proxy_async();  // earlier generic accesses to this buffer come first
     mbar_expect_tx(bar, KVB);
-#pragma unroll
-    for (int hh = 0; hh < D / 64; ++hh)
-      tma_load_2d(smem_u32(dst + hh * 8192), which ? &a.tmV : &a.tmK, bar, h * D + hh * 64,
-                  page * kTile);
+    tma_load_3d(smem_u32(dst), which ? &a.tmV : &a.tmK, bar, 0, page * kTile, h * (D / 64));
   };
   auto load_tile = [&](int buf, int t) {
     const int tbase = lo + t * kTile;
@@ -751,11 +749,8 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         const int sk = t % STK;
         if (t >= STK && !mbar_wait(bar(K_EMPTY + sk), ((t / STK) - 1) & 1, a.err)) return false;
         mbar_expect_tx(bar(K_FULL + sk), KVB);
-        const int page = page_of(t);
-#pragma unroll
-        for (int hh = 0; hh < D / 64; ++hh)
-          tma_load_2d(smem_u32(sK + sk * KVB + hh * 8192), &a.tmK, bar(K_FULL + sk),
-                      h * D + hh * 64, page * kTile);
+        tma_load_3d(smem_u32(sK + sk * KVB), &a.tmK, bar(K_FULL + sk), 0, page_of(t) * kTile,
+                    h * (D / 64));
         ++issued_k;
         return true;
       };
@@ -765,11 +760,8 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         const int sv = t % STV;
         if (t >= STV && !mbar_wait(bar(V_EMPTY + sv), ((t / STV) - 1) & 1, a.err)) break;
         mbar_expect_tx(bar(V_FULL + sv), KVB);
-        const int page = page_of(t);
-#pragma unroll
-        for (int hh = 0; hh < D / 64; ++hh)
-          tma_load_2d(smem_u32(sV + sv * KVB + hh * 8192), &a.tmV, bar(V_FULL + sv),
-                      h * D + hh * 64, page * kTile);
+        tma_load_3d(smem_u32(sV + sv * KVB), &a.tmV, bar(V_FULL + sv), 0, page_of(t) * kTile,
+                    h * (D / 64));
         ++issued_v;
       }
     }
@@ -1158,16 +1150,19 @@ biv_status launch_decode(const biv_attn_desc& d, const AttnArgs& a, int st, cuda
   return launch_cfg<D, DS, 3, true, DS>(d, a, s);
 }
 
-// bf16 cache of one layer as a 2-D tensor [num_pages*64 slots, Hkv*D], boxes of
-// 64 slots x 64 dims (128 bytes, 128-byte swizzle)
+// bf16 cache of one layer as a 3-D tensor {64 dims, num_pages*64 slots,
+// Hkv*D/64 panels} (slot stride Hkv*D elements, panel stride 64 elements):
+// one box {64, 64, D/64} is one page of one KV head, landing as [panel][slot]
+// [128 B] with 128-byte swizzling, in a single copy (a copy per 128-byte row
+// segment is what a TMA producer pays for)
 bool make_kv_map(CUtensorMap* m, const void* base, int num_pages, int Hkv, int D) {
   auto fn = tensor_map_encoder();
   if (!fn) return false;
-  cuuint64_t dims[2] = {cuuint64_t(Hkv) * D, cuuint64_t(num_pages) * kTile};
-  cuuint64_t strides[1] = {cuuint64_t(Hkv) * D * 2};
-  cuuint32_t box[2] = {64, kTile};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  cuuint64_t dims[3] = {64, cuuint64_t(num_pages) * kTile, cuuint64_t(Hkv) * D / 64};
+  cuuint64_t strides[2] = {cuuint64_t(Hkv) * D * 2, 128};
+  cuuint32_t box[3] = {64, kTile, cuuint32_t(D / 64)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
