@@ -396,6 +396,14 @@ class KernelTimer:
     NAMES = {"decode_step": "decode step (one CUDA-graph replay: 28 layers, LM head, logprob)",
              "gemm_bf16": "prefill bf16 GEMMs (tcgen05)", "attention_prefill": "prefill attention"}
 
+    # DRAM bytes per algorithmic byte of a decode step, from ncu captures of one
+    # eager step with every sequence at position 700 (kernel_bench decode_step):
+    # 9.335 GB against 8.59 GB at batch 64, 25.78 GB against 23.99 GB at batch
+    # 256; the excess is the decode GEMMs' FP32 chunk partials.  The bench's
+    # steps mix batch sizes and contexts, so their traffic is this ratio times
+    # their own algorithmic bytes.
+    DECODE_DRAM_RATIO = (9.335 / 8.59 + 25.78 / 23.99) / 2
+
     def entry(self, k, a, peaks):
         if a["unit"] == "flop":
             ach = a["work"] / (a["ms"] / 1e3) / 1e12
@@ -406,10 +414,17 @@ class KernelTimer:
                     "peak_source": peaks["source"] + " sustained bf16"}
         ach = a["work"] / (a["ms"] / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
-        return {"kernel": self.NAMES.get(k, k), "bound": "hbm", "achieved": ach, "peak": peak,
-                "unit": "GB/s", "frac": ach / peak, "traffic": None, "launches": a["n"],
-                "ms_total": a["ms"], "algorithmic_per_launch": a["work"] / a["n"],
-                "peak_source": peaks["source"] + " hbm"}
+        out = {"kernel": self.NAMES.get(k, k), "bound": "hbm", "achieved": ach, "peak": peak,
+               "unit": "GB/s", "frac": ach / peak, "traffic": None, "launches": a["n"],
+               "ms_total": a["ms"], "algorithmic_per_launch": a["work"] / a["n"],
+               "peak_source": peaks["source"] + " hbm"}
+        if k == "decode_step":
+            out["traffic"] = self.DECODE_DRAM_RATIO * a["work"] / a["n"]
+            out["traffic_source"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one eager decode "
+                                     "step at batch 64 and 256 (position 700), per algorithmic byte "
+                                     f"({self.DECODE_DRAM_RATIO:.3f}), times this run's algorithmic "
+                                     "bytes per replay")
+        return out
 
     def summary(self, peaks):
         return {k: self.entry(k, a, peaks) for k, a in self.totals().items()}

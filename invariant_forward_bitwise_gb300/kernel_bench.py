@@ -9,9 +9,12 @@ attn_prefill (8 sequences x 1024 tokens), gemm_prefill (M 8192, N 2048,
 K 6144), gemm_qkv (M 16384, N 4096, K 2048), gemm_decode (M 64, N 2048, K 6144), lm_head (M 4096, N 151936,
 K 2048), ssd_prefill (16384 tokens, 64 heads), ssd_decode (one token), topk_indexer
 (4096 rows x 32768 scores, top 2048), moe_block (4096 tokens through the
-64-expert FP8 block) and decode_step (one decode step of the 28-layer model
+64-expert FP8 block), decode_step (one decode step of the 28-layer model
 at batch BIV_BENCH_BATCH, default 64, from its CUDA graph and eagerly; the
-eager step runs inside cudaProfilerStart/Stop for an ncu launch list).
+eager step runs inside cudaProfilerStart/Stop for an ncu launch list) and
+prefill_step (one 16384-row step of the 28-layer model: 16 sequences x 1024
+tokens, every row producing a logprob, as in the trainer recompute; one more
+step runs inside cudaProfilerStart/Stop).
 Each case times REPS calls with CUDA events after one warm-up call and
 prints the time and the rate against the case's algorithmic bytes or FLOPs;
 it is also the command that the ncu summaries in profiles/ capture.
@@ -118,6 +121,37 @@ if case == "decode_step":
               f"(weights 3.44 GB + KV {kvb/1e9:.2f} GB -> {(3.44e9 + kvb)/(ms/1e3)/1e9:.0f} GB/s)", flush=True)
     torch.cuda.cudart().cudaProfilerStart()
     dg.run(*args)
+    torch.cuda.synchronize()
+    torch.cuda.cudart().cudaProfilerStop()
+elif case == "prefill_step":
+    from invariant_forward_bitwise_gb300.model import DenseModel, PagedKV, Runner, prefill_rows
+    cfg = synth.QWEN3_1P7B
+    m = DenseModel(cfg, synth.dense_weights(cfg, seed=0), max_rows=16384, max_pos=1536)
+    Bn, ctx = 16, 1024
+    kv = PagedKV(cfg, pages=Bn * 17 + 8, max_seqs=Bn, max_pages=24)
+    for i in range(Bn):
+        kv.admit(i, ctx + 8)
+    kv.sync_table()
+    run = Runner(m)
+    toks = g.integers(0, cfg.vocab, size=(Bn, ctx + 1)).astype(np.int32)
+    seqs = [synth.Sequence(toks[i], 1) for i in range(Bn)]
+    rows = prefill_rows(seqs, list(range(Bn)), [0] * Bn, [ctx] * Bn, [0] * Bn)
+    spec = run.load_rows(kv, *rows[:5])
+    m.reserve(kv, [spec])
+    m.step(kv, spec)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        m.step(kv, spec)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    fl = 2.0 * Bn * ctx * (28 * 2048 * (4096 + 2048 + 2 * 6144 + 6144) + 2048 * cfg.vocab)
+    print(f"prefill_step 16 x 1024 rows: {ms:.2f} ms  ({Bn * ctx / (ms / 1e3):.0f} tokens/s, "
+          f"GEMM FLOPs {fl / (ms / 1e3) / 1e12:.0f} TFLOP/s over the whole step)")
+    torch.cuda.cudart().cudaProfilerStart()
+    m.step(kv, spec)
     torch.cuda.synchronize()
     torch.cuda.cudart().cudaProfilerStop()
 elif case == "topk_indexer":
