@@ -7,7 +7,7 @@ attn_decode4 (the same for 4 sequences), attn_decode_fp8 (128 sequences x 4096
 context on the e4m3 cache),
 attn_prefill (8 sequences x 1024 tokens), gemm_prefill (M 8192, N 2048,
 K 6144), gemm_qkv (M 16384, N 4096, K 2048), gemm_decode (M 64, N 2048, K 6144), lm_head (M 4096, N 151936,
-K 2048), ssd_prefill (16384 tokens, 64 heads), ssd_decode (one token), topk_indexer
+K 2048, with the log-softmax gather in its epilogue), ssd_prefill (16384 tokens, 64 heads), ssd_decode (one token), topk_indexer
 (4096 rows x 32768 scores, top 2048), moe_block (4096 tokens through the
 64-expert FP8 block), decode_step (one decode step of the 28-layer model
 at batch BIV_BENCH_BATCH, default 64, from its CUDA graph and eagerly; the
@@ -319,7 +319,14 @@ else:
                "gemm_decode": (64, 2048, 6144), "lm_head": (4096, 151936, 2048)}[case]
     a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
     b = (torch.randn(N, K, device="cuda") * 0.02).to(torch.bfloat16)
-    c = torch.empty(M, N, device="cuda", dtype=torch.float32 if case == "lm_head" else torch.bfloat16)
-    d = biv.gemm_desc(a, b, c)
-    ms = timeit(lambda: biv.biv_gemm(d))
+    if case == "lm_head":
+        # the model's LM head: the log-softmax gather in the GEMM's epilogue
+        tgt = torch.randint(0, N, (M,), dtype=torch.int32, device="cuda")
+        lp = torch.empty(M, device="cuda")
+        ws = torch.empty(biv.biv_lm_head_logprob_workspace(M, N), dtype=torch.uint8, device="cuda")
+        ms = timeit(lambda: biv.biv_lm_head_logprob(a, b, tgt, lp, ws))
+    else:
+        c = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        d = biv.gemm_desc(a, b, c)
+        ms = timeit(lambda: biv.biv_gemm(d))
     print(f"{case} M={M} N={N} K={K}: {ms*1e3:.1f} us  {2*M*N*K/(ms/1e3)/1e12:.0f} TFLOP/s  weights {N*K*2/(ms/1e3)/1e9:.0f} GB/s")
