@@ -14,7 +14,9 @@ at batch BIV_BENCH_BATCH, default 64, from its CUDA graph and eagerly; the
 eager step runs inside cudaProfilerStart/Stop for an ncu launch list) and
 prefill_step (one 16384-row step of the 28-layer model: 16 sequences x 1024
 tokens, every row producing a logprob, as in the trainer recompute; one more
-step runs inside cudaProfilerStart/Stop).
+step runs inside cudaProfilerStart/Stop) and hybrid_decode_step (one decode step of the
+Mamba-2 hybrid unit for 3 sequences, graph-timed, then eagerly inside
+cudaProfilerStart/Stop).
 Each case times REPS calls with CUDA events after one warm-up call and
 prints the time and the rate against the case's algorithmic bytes or FLOPs;
 it is also the command that the ncu summaries in profiles/ capture.
@@ -152,6 +154,56 @@ elif case == "prefill_step":
           f"GEMM FLOPs {fl / (ms / 1e3) / 1e12:.0f} TFLOP/s over the whole step)")
     torch.cuda.cudart().cudaProfilerStart()
     m.step(kv, spec)
+    torch.cuda.synchronize()
+    torch.cuda.cudart().cudaProfilerStop()
+elif case == "hybrid_decode_step":
+    # one decode step of the Mamba-2 hybrid unit (d 2560, NVFP4 linear layers)
+    # for 3 sequences after a 1024-token prefill each; graph-timed, then one
+    # eager step inside cudaProfilerStart/Stop
+    from invariant_forward_bitwise_gb300.hybrid import HybridModel, new_kv
+    cfg = synth.HYBRID
+    W = synth.device_hybrid_weights(cfg, 9)
+    S, L = 3, 1024
+    m = HybridModel(cfg, W, max_rows=4096, max_seqs=S, max_pos=L + 64)
+    kv = new_kv(cfg, S, L + 64)
+    toks = g.integers(0, cfg.vocab, size=(S, L + 2)).astype(np.int32)
+    for i in range(S):
+        kv.admit(i, L + 2)
+        m.reset_slot(i)
+    kv.sync_table()
+
+    def rows(ps, n):
+        seq, pos, ids = [], [], []
+        for i in range(S):
+            for p in range(ps, ps + n):
+                seq.append(i)
+                pos.append(p)
+                ids.append(int(toks[i][p]))
+        return seq, pos, ids, list(range(len(ids))), [int(toks[s_][p + 1]) for s_, p in zip(seq, pos)]
+
+    spec = m.load(kv, *rows(0, L))
+    m.step(kv, spec)
+    dspec = dict(T=S, nqblocks=S, max_rows_per_block=1, max_ctx=L + 64, T_lm=S, max_n=1)
+    m.load(kv, *rows(L, 1))
+    m.step(kv, dspec)
+    gr = torch.cuda.CUDAGraph()
+    st = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(st)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(gr):
+            m.step(kv, dspec)
+    st.wait_stream(side)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        gr.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    print(f"hybrid_decode_step graph, 3 sequences: {e0.elapsed_time(e1) / reps * 1e3:.1f} us")
+    torch.cuda.cudart().cudaProfilerStart()
+    m.step(kv, dspec)
     torch.cuda.synchronize()
     torch.cuda.cudart().cudaProfilerStop()
 elif case == "topk_indexer":
