@@ -7,19 +7,22 @@
 // copied to shared memory with cp.async while the CTA works on the previous
 // row, so the HBM read overlaps the selection.  Thread t then keeps 32 keys
 // in registers: in round r (0..7) the four consecutive positions
-// 4096 r + 4 t + e (e = 0..3).  Scores become order-preserving 32-bit keys
-// (+0 and -0 map to one key; -inf and positions past valid_len are
-// excluded).
+// 4096 r + 4 t + e (e = 0..3).  Scores become order-preserving 32-bit keys:
+// +0 and -0 map to one key, and NaN, -inf and the positions past valid_len
+// (filled with -inf in shared memory) all map to the key of -inf, which lies
+// below every bin the selection can choose and is never selected.
 //
-// The k-th largest key is bracketed by range refinement: the current key
-// range [lo, hi] is cut into at most 4096 power-of-two-wide bins, a shared
-// histogram counts the keys per bin, and a block scan over the bins in
-// descending order finds the bin holding the rem-th largest key, which
-// becomes the next range (32 -> 20 -> 8 -> 0 bits of width: at most three
-// rounds reach one key value).  The first round runs over every key; when
-// the chosen bin holds at most 1024 keys they are copied to a candidate list
-// in shared memory and the remaining rounds run over that list (one
-// candidate per thread).  Refinement stops once the chosen bin's keys are
+// The k-th largest key is bracketed by range refinement.  The first round
+// counts every key in a 4096-bin histogram of its top 12 bits while the keys
+// are formed; a block scan over the bins in descending order finds the bin
+// holding the k-th largest key, which becomes the key range [lo, hi].  Each
+// later round cuts the current range into at most 4096 power-of-two-wide
+// bins and narrows it the same way (20 -> 8 -> 0 bits of width: at most
+// three rounds reach one key value).  When the first bin holds at most 1024
+// keys they are copied to a candidate list in shared memory and the later
+// rounds run over that list (one candidate per thread) with 256 bins, which
+// one warp scans (20 -> 12 -> 4 -> 0 bits); otherwise they run over the
+// registers.  Refinement stops once the chosen bin's keys are
 // exactly the ones still wanted, or the bin is one key value, whose lowest
 // positions then fill the remaining slots.
 //
@@ -29,13 +32,17 @@
 // from per-(round, warp) counts scanned over the block and per-lane counts
 // scanned over the warp.  Only integer counts decide the result, so it is
 // unique and independent of scheduling.
+//
+// The kernel is bound by instruction issue, so the per-row block scans run
+// on warp shuffles (one barrier each) and every narrowing step clears the
+// histogram it has read, ready for the next round or row.
 #include "common.cuh"
 
 namespace biv {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
+constexpr int kWarps = kThreads / 32;       // 32: one warp-sum per lane
 constexpr int kRounds = 8;                  // float4 rounds per thread
 constexpr int kPer = 4 * kRounds;           // keys per thread
 constexpr int kRoundSpan = 4 * kThreads;    // positions per round
@@ -43,67 +50,46 @@ constexpr int kMaxN = kThreads * kPer;      // 32768
 constexpr int kBinBits = 12;
 constexpr int kBins = 1 << kBinBits;        // 4096
 constexpr int kBinsPerThread = kBins / kThreads;
+constexpr uint32_t kNegInfKey = 0x007FFFFFu;   // the key of -inf (and of NaN)
+// the first round's bins below this one hold no key but -inf's
+constexpr int kFirstValidBin = int((kNegInfKey + 1u) >> (32 - kBinBits));
+// Rounds after the first: a 2^20-wide bin needs two more (2^8, then one key);
+// the bound only guards the loop.
+constexpr int kMaxRefine = 4;
+static_assert(kWarps == 32 && kBinsPerThread == 4, "scan and histogram layout");
 
+// Order-preserving key of a score: -0 + 0 = +0 gives -0 the key of +0, and
+// the IEEE maximum with -inf turns NaN into -inf (finite values, infinities
+// and subnormals pass both unchanged).
 __device__ __forceinline__ uint32_t order_key(float s) {
-  if (s == 0.f) s = 0.f;  // -0 -> +0
-  const uint32_t u = __float_as_uint(s);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  const uint32_t u = __float_as_uint(fmaxf(s + 0.0f, -INFINITY));
+  return u ^ (uint32_t(int32_t(u) >> 31) | 0x80000000u);
 }
 
 // position of key slot q (= 4 r + e) of thread t
 __device__ __forceinline__ int slot_pos(int q, int t) { return (q >> 2) * kRoundSpan + 4 * t + (q & 3); }
 
-// Exclusive scan of one value per thread over the CTA in thread order; also
-// returns the total.  Uses wsum[kWarps]; two barriers.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint32_t x = v;
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) wsum[warp] = x;
-  __syncthreads();
-  uint32_t pre = 0, tot = 0;
-#pragma unroll 8
-  for (int w = 0; w < kWarps; ++w) {
-    const uint32_t c = wsum[w];
-    pre += w < warp ? c : 0u;
-    tot += c;
-  }
-  __syncthreads();  // wsum may be reused after this
-  total = tot;
-  return pre + x - v;
+  return x;
 }
 
-// Block-wide sum, min and max (a thread without a valid key passes ~0 and 0).
-__device__ __forceinline__ void block_count_range(uint32_t cnt, uint32_t mn, uint32_t mx,
-                                                  uint32_t* red, uint32_t& tot, uint32_t& kmin,
-                                                  uint32_t& kmax) {
+// Exclusive scan of one value per thread over the CTA in thread order; also
+// returns the total.  One barrier, after which wsum is read by every warp: a
+// caller must pass another barrier before the next scan writes wsum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-  if (lane == 0) {
-    red[warp] = cnt;
-    red[kWarps + warp] = mn;
-    red[2 * kWarps + warp] = mx;
-  }
+  const uint32_t x = warp_incl_scan(v, lane);
+  if (lane == 31) wsum[warp] = x;
   __syncthreads();
-  tot = 0;
-  kmin = 0xffffffffu;
-  kmax = 0;
-#pragma unroll 8
-  for (int w = 0; w < kWarps; ++w) {
-    tot += red[w];
-    kmin = min(kmin, red[kWarps + w]);
-    kmax = max(kmax, red[2 * kWarps + w]);
-  }
-  __syncthreads();  // red may be reused after this
+  const uint32_t ws = wsum[lane];
+  const uint32_t wi = warp_incl_scan(ws, lane);
+  total = __shfl_sync(0xffffffffu, wi, 31);
+  return __shfl_sync(0xffffffffu, wi - ws, warp) + x - v;
 }
 
 struct Range {
@@ -118,10 +104,15 @@ __device__ __forceinline__ int bin_shift(const Range& g) {
 }
 
 // After the histogram of the current range is complete in hist[]: find the
-// bin holding the rem-th largest key and narrow the range to it.  Every
-// thread returns the same new range.  Barriers: 3.
-__device__ __forceinline__ void narrow(Range& g, int shift, uint32_t* hist, uint32_t* wsum,
-                                       uint32_t* s_sel) {
+// bin holding the rem-th largest key and narrow the range to it (only when
+// the range holds at least rem keys).  Every thread returns the same new
+// range and the number of keys the histogram held, and hist[] is zero again.
+// Barriers: 2; s_sel is free again once the caller has passed one more.
+// FIRST: the first round (bins of the top 12 key bits), whose bins below
+// kFirstValidBin are not counted.
+template <bool FIRST = false>
+__device__ __forceinline__ uint32_t narrow(Range& g, int shift, uint32_t* hist, uint32_t* wsum,
+                                          uint32_t* s_sel) {
   const int tid = threadIdx.x;
   const int nb = int((g.hi - g.lo) >> shift) + 1;
   // descending bin order: thread t owns bins nb-1-4t .. nb-4-4t
@@ -129,28 +120,34 @@ __device__ __forceinline__ void narrow(Range& g, int shift, uint32_t* hist, uint
 #pragma unroll
   for (int d = 0; d < kBinsPerThread; ++d) {
     const int b = nb - 1 - (kBinsPerThread * tid + d);
-    c[d] = b >= 0 ? hist[b] : 0u;
+    c[d] = b >= (FIRST ? kFirstValidBin : 0) ? hist[b] : 0u;
     sum += c[d];
   }
   uint32_t tot;
-  uint32_t above = block_excl_scan(sum, wsum, tot);
+  uint32_t above = block_excl_scan(sum, wsum, tot);   // every bin has been read
+  reinterpret_cast<uint4*>(hist)[tid] = make_uint4(0u, 0u, 0u, 0u);
+  const bool pick = g.rem <= tot;
+  if (pick) {
 #pragma unroll
-  for (int d = 0; d < kBinsPerThread; ++d) {
-    if (above < g.rem && g.rem <= above + c[d]) {
-      s_sel[0] = uint32_t(nb - 1 - (kBinsPerThread * tid + d));
-      s_sel[1] = above;
-      s_sel[2] = c[d];
+    for (int d = 0; d < kBinsPerThread; ++d) {
+      if (above < g.rem && g.rem <= above + c[d]) {
+        s_sel[0] = uint32_t(nb - 1 - (kBinsPerThread * tid + d));
+        s_sel[1] = above;
+        s_sel[2] = c[d];
+      }
+      above += c[d];
     }
-    above += c[d];
   }
   __syncthreads();
-  const uint32_t b = s_sel[0];
-  g.rem -= s_sel[1];
-  g.in_bin = s_sel[2];
-  const uint32_t nlo = g.lo + (b << shift), width_m1 = (1u << shift) - 1u;
-  if (g.hi - nlo > width_m1) g.hi = nlo + width_m1;  // no wrap: nlo + width_m1 < hi
-  g.lo = nlo;
-  __syncthreads();  // s_sel and hist are free again
+  if (pick) {
+    const uint32_t b = s_sel[0];
+    g.rem -= s_sel[1];
+    g.in_bin = s_sel[2];
+    const uint32_t nlo = g.lo + (b << shift), width_m1 = (1u << shift) - 1u;
+    if (g.hi - nlo > width_m1) g.hi = nlo + width_m1;  // no wrap: nlo + width_m1 < hi
+    g.lo = nlo;
+  }
+  return tot;
 }
 
 __device__ __forceinline__ bool range_done(const Range& g) {
@@ -161,13 +158,10 @@ __device__ __forceinline__ bool range_done(const Range& g) {
 __device__ __forceinline__ void refine_regs(Range& g, const uint32_t (&key)[kPer], uint32_t* hist,
                                             uint32_t* wsum, uint32_t* s_sel) {
   const int shift = bin_shift(g);
-#pragma unroll
-  for (int b = threadIdx.x; b < kBins; b += kThreads) hist[b] = 0;
-  __syncthreads();
   const uint32_t span = g.hi - g.lo;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
-    const uint32_t d = key[q] - g.lo;  // keys below lo wrap above span
+    const uint32_t d = key[q] - g.lo;  // keys below lo (-inf's too) wrap above span
     if (d <= span) atomicAdd(hist + (d >> shift), 1u);
   }
   __syncthreads();
@@ -175,25 +169,60 @@ __device__ __forceinline__ void refine_regs(Range& g, const uint32_t (&key)[kPer
 }
 
 // One refinement round over the candidate list (thread t holds candidate t
-// when t < count; ck = its key).
+// when t < count; ck = its key): at most 256 bins, counted by every thread
+// and scanned by warp 0 alone (lane L owns the descending bins nb-1-8L ..
+// nb-8-8L), which then clears them.  Barriers: 2.
+constexpr int kCandBinBits = 8;
+constexpr int kCandBins = 1 << kCandBinBits;
 __device__ __forceinline__ void refine_cands(Range& g, bool has, uint32_t ck, uint32_t* hist,
-                                             uint32_t* wsum, uint32_t* s_sel) {
-  const int shift = bin_shift(g);
-#pragma unroll
-  for (int b = threadIdx.x; b < kBins; b += kThreads) hist[b] = 0;
-  __syncthreads();
+                                             uint32_t* s_sel) {
+  const int shift = max(0, 32 - __clz(g.hi - g.lo) - kCandBinBits);
   if (has && ck >= g.lo && ck <= g.hi) atomicAdd(hist + ((ck - g.lo) >> shift), 1u);
   __syncthreads();
-  narrow(g, shift, hist, wsum, s_sel);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int nb = int((g.hi - g.lo) >> shift) + 1;
+    uint32_t c[kCandBins / 32], sum = 0;
+#pragma unroll
+    for (int d = 0; d < kCandBins / 32; ++d) {
+      const int b = nb - 1 - ((kCandBins / 32) * lane + d);
+      c[d] = b >= 0 ? hist[b] : 0u;
+      sum += c[d];
+    }
+    const uint32_t incl = warp_incl_scan(sum, lane);
+    uint32_t above = incl - sum;
+    if (above < g.rem && g.rem <= incl) {
+#pragma unroll
+      for (int d = 0; d < kCandBins / 32; ++d) {
+        if (above < g.rem && g.rem <= above + c[d]) {
+          s_sel[0] = uint32_t(nb - 1 - ((kCandBins / 32) * lane + d));
+          s_sel[1] = above;
+          s_sel[2] = c[d];
+        }
+        above += c[d];
+      }
+    }
+    __syncwarp();
+    reinterpret_cast<uint4*>(hist)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(hist)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  const uint32_t b = s_sel[0];
+  g.rem -= s_sel[1];
+  g.in_bin = s_sel[2];
+  const uint32_t nlo = g.lo + (b << shift), width_m1 = (1u << shift) - 1u;
+  if (g.hi - nlo > width_m1) g.hi = nlo + width_m1;
+  g.lo = nlo;
 }
 
 // Output slots of the set bits of `mask` (bit q = key slot q of this thread)
 // in ascending position order.  tab: kRounds * kWarps words.  On return
 // tab[r * kWarps + w] = chosen positions before round r's warp-w block, and
-// lane_pre[r] = chosen positions of lanes < this lane in round r.  Also
-// returns the total.  Barriers: 3.
+// byte r of the pair pre (rounds 0..3 in pre[0], 4..7 in pre[1]) = chosen
+// positions of lanes < this lane in round r.  Also returns the total.
+// Barriers: 3 (tab may be rewritten once the caller has passed one more).
 __device__ __forceinline__ uint32_t ordered_slots(uint32_t mask, uint32_t* tab, uint32_t* wsum,
-                                                  uint32_t (&lane_pre)[kRounds]) {
+                                                  uint32_t (&pre)[2]) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // per-round counts (0..4) packed as 8-bit fields, four rounds per word: a
   // warp prefix is at most 128, so the fields never carry into each other
@@ -210,18 +239,18 @@ __device__ __forceinline__ uint32_t ordered_slots(uint32_t mask, uint32_t* tab, 
       if (lane >= o) x[h] += y;
     }
   }
+  // fields never borrow: each inclusive count is at least its own
+  pre[0] = x[0] - c[0];
+  pre[1] = x[1] - c[1];
+  if (lane == 31) {
 #pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
-    const int sh = 8 * (r & 3);
-    const uint32_t incl = (x[r >> 2] >> sh) & 255u;
-    lane_pre[r] = incl - ((c[r >> 2] >> sh) & 255u);
-    if (lane == 31) tab[r * kWarps + warp] = incl;
+    for (int r = 0; r < kRounds; ++r) tab[r * kWarps + warp] = (x[r >> 2] >> (8 * (r & 3))) & 255u;
   }
   __syncthreads();
   const uint32_t v = tid < kRounds * kWarps ? tab[tid] : 0u;
   uint32_t total;
-  const uint32_t pre = block_excl_scan(v, wsum, total);
-  if (tid < kRounds * kWarps) tab[tid] = pre;
+  const uint32_t before = block_excl_scan(v, wsum, total);
+  if (tid < kRounds * kWarps) tab[tid] = before;
   __syncthreads();
   return total;
 }
@@ -240,7 +269,7 @@ __device__ __forceinline__ int row_valid(const int32_t* valid_len, int row, int 
 }
 
 // Start the copy of a row's valid scores into buf (16-byte pieces where the
-// row allows them).
+// row allows them); the positions past them are set to -inf.
 template <bool VEC>
 __device__ __forceinline__ void prefetch_row(float* buf, const float* __restrict__ scores,
                                              int64_t ld, int row, int nv) {
@@ -252,8 +281,12 @@ __device__ __forceinline__ void prefetch_row(float* buf, const float* __restrict
       cp_async16(buf + j0, src + j0);
     } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (j0 + e < nv) cp_async4(buf + j0 + e, src + j0 + e);
+      for (int e = 0; e < 4; ++e) {
+        if (j0 + e < nv)
+          cp_async4(buf + j0 + e, src + j0 + e);
+        else
+          buf[j0 + e] = -INFINITY;
+      }
     }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -263,26 +296,34 @@ template <bool VEC>
 __global__ void __launch_bounds__(kThreads, 1)
     topk_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ valid_len,
                 int rows, int n, int k, int32_t* __restrict__ idx) {
-  extern __shared__ float4 rowbuf4[];         // one row of scores (kMaxN floats)
+  extern __shared__ float4 rowbuf4[];                // one row of scores (kMaxN floats)
   float* rowbuf = reinterpret_cast<float*>(rowbuf4);
-  __shared__ uint32_t hist[kBins];            // bin counts; reused as the slot table
-  __shared__ uint32_t wsum[3 * kWarps];
-  __shared__ uint32_t s_sel[4];
-  __shared__ uint32_t cand_key[kThreads];     // candidate list
+  __shared__ __align__(16) uint32_t hist[kBins];     // bin counts, zero between rounds
+  __shared__ uint32_t tab[kRounds * kWarps];         // output slot table
+  __shared__ uint32_t wsum[kWarps];
+  __shared__ uint32_t s_sel[3];
+  __shared__ uint32_t s_cnt;                         // candidates gathered
+  __shared__ uint32_t cand_key[kThreads];            // candidate list
   __shared__ uint32_t cand_pos[kThreads];
-  __shared__ uint32_t tie_bits[kThreads];     // chosen candidates, as thread-slot masks
+  __shared__ uint32_t tie_bits[kThreads];            // chosen candidates, as thread-slot masks
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  reinterpret_cast<uint4*>(hist)[tid] = make_uint4(0u, 0u, 0u, 0u);
   int row = blockIdx.x;
   int nv_next = row < rows ? row_valid(valid_len, row, n) : 0;
   if (row < rows) prefetch_row<VEC>(rowbuf, scores, ld, row, nv_next);
+  // The first round counts only the bins from lbin up: the bin below the
+  // one this CTA's previous row chose (its rows are alike, as the causal
+  // rows of one indexer are).  Keys below never reach the histogram, which
+  // relieves the shared-memory atomics; a row with fewer than k keys from
+  // lbin up is counted again in full.  lbin changes the time, not the result.
+  uint32_t lbin = 0;
   for (; row < rows; row += gridDim.x) {
-    const int nv = nv_next;
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();  // the row is in shared memory; the previous row's tables are free
 
+    // keys, and the first round's histogram of their top 12 bits
     uint32_t key[kPer];
-    uint32_t cnt = 0, mn = 0xffffffffu, mx = 0;
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
       const int j0 = r * kRoundSpan + 4 * tid;
@@ -290,114 +331,127 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float v[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const uint32_t kk = (j0 + e < nv && v[e] != -INFINITY) ? order_key(v[e]) : 0u;
+        const uint32_t kk = order_key(v[e]);
         key[4 * r + e] = kk;
-        if (kk != 0) {
-          ++cnt;
-          mn = min(mn, kk);
-          mx = max(mx, kk);
-        }
+        const uint32_t b = kk >> (32 - kBinBits);
+        if (b >= lbin) atomicAdd(hist + b, 1u);
       }
     }
-    __syncthreads();  // every thread holds its keys: the buffer takes the next row
-    if (row + int(gridDim.x) < rows) {
-      nv_next = row_valid(valid_len, row + gridDim.x, n);
-      prefetch_row<VEC>(rowbuf, scores, ld, row + gridDim.x, nv_next);
+    __syncthreads();  // keys in registers; histogram complete
+    // the next row goes to the buffer once this row's candidates are read
+    // from it (or at once when no candidate list is built)
+    auto start_next = [&]() {
+      if (row + int(gridDim.x) < rows) {
+        nv_next = row_valid(valid_len, row + gridDim.x, n);
+        prefetch_row<VEC>(rowbuf, scores, ld, row + gridDim.x, nv_next);
+      }
+    };
+    if (tid == 0) s_cnt = 0u;
+    tie_bits[tid] = 0u;
+    Range g{0u, 0xffffffffu, uint32_t(k), 0u};
+    uint32_t total_valid = narrow<true>(g, 32 - kBinBits, hist, wsum, s_sel);
+    if (total_valid <= uint32_t(k) && lbin > uint32_t(kFirstValidBin)) {
+      // at most k keys from lbin up: count every key (the test below must
+      // see the whole row's count before it selects every valid key)
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) atomicAdd(hist + (key[q] >> (32 - kBinBits)), 1u);
+      __syncthreads();
+      g = Range{0u, 0xffffffffu, uint32_t(k), 0u};   // the filtered pass may have narrowed it
+      total_valid = narrow<true>(g, 32 - kBinBits, hist, wsum, s_sel);
     }
-    uint32_t total_valid;
-    Range g;
-    block_count_range(cnt, mn, mx, wsum, total_valid, g.lo, g.hi);
-    g.rem = uint32_t(k);
-    g.in_bin = total_valid;
+    lbin = total_valid >= uint32_t(k) ? (g.lo >> (32 - kBinBits)) - 1u : 0u;
 
     uint32_t sel = 0;  // bit q: key slot q chosen
     if (total_valid <= uint32_t(k)) {
+      start_next();
 #pragma unroll
-      for (int q = 0; q < kPer; ++q) sel |= uint32_t(key[q] != 0) << q;
-    } else {
-      if (!range_done(g)) refine_regs(g, key, hist, wsum, s_sel);
-      if (!range_done(g) && g.in_bin <= uint32_t(kThreads)) {
-        // the bin's keys as a candidate list (list order is irrelevant: every
-        // later decision is by key, then by position)
-        if (tid == 0) s_sel[3] = 0;
-        tie_bits[tid] = 0;
-        __syncthreads();
-        // keys above the bin are chosen whatever the later rounds decide
-        const uint32_t lo1 = g.lo, span1 = g.hi - g.lo;
+      for (int q = 0; q < kPer; ++q) sel |= uint32_t(key[q] > kNegInfKey) << q;
+    } else if (!range_done(g) && g.in_bin <= uint32_t(kThreads)) {
+      // the bin's keys as a candidate list (list order is irrelevant: every
+      // later decision is by key, then by position); keys above the bin are
+      // chosen whatever the later rounds decide
+      const uint32_t lo1 = g.lo, hi1 = g.hi, span1 = hi1 - lo1;
+      uint32_t cm = 0;   // bit q: key slot q is a candidate
 #pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-          const uint32_t d = key[q] - lo1;
-          if (d <= span1) {
-            const uint32_t s = atomicAdd(s_sel + 3, 1u);
-            cand_key[s] = key[q];
-            cand_pos[s] = uint32_t(slot_pos(q, tid));
-          }
-          sel |= uint32_t(key[q] > lo1 && d > span1) << q;
-        }
-        __syncthreads();
-        const uint32_t nc = g.in_bin;
-        const bool has = uint32_t(tid) < nc;
-        const uint32_t ck = has ? cand_key[tid] : 0u, cp = has ? cand_pos[tid] : 0u;
-        while (!range_done(g)) refine_cands(g, has, ck, hist, wsum, s_sel);
-        bool take = has && ck > g.hi;
-        if (has && ck >= g.lo && ck <= g.hi) {
-          if (g.in_bin == g.rem) {
-            take = true;
-          } else {  // one key value: the lowest positions win
-            uint32_t before = 0;
-            for (uint32_t c = 0; c < nc; ++c) before += (cand_key[c] == ck && cand_pos[c] < cp);
-            take = before < g.rem;
-          }
-        }
-        if (take) {
-          const uint32_t r = cp / kRoundSpan, w = cp % kRoundSpan;
-          atomicOr(tie_bits + w / 4, 1u << (4 * r + (w & 3)));
-        }
-        __syncthreads();
-        sel |= tie_bits[tid];
-      } else {
-        // more than 1024 keys share the bin: refine over the registers
-        while (!range_done(g)) refine_regs(g, key, hist, wsum, s_sel);
-        uint32_t eq = 0;
-#pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-          sel |= uint32_t(key[q] > g.hi) << q;
-          eq |= uint32_t(key[q] >= g.lo && key[q] <= g.hi) << q;
-        }
+      for (int q = 0; q < kPer; ++q) {
+        cm |= uint32_t(key[q] - lo1 <= span1) << q;
+        sel |= uint32_t(key[q] > hi1) << q;
+      }
+      if (cm) {   // one slot reservation per thread; keys re-read from the row
+        uint32_t s = atomicAdd(&s_cnt, uint32_t(__popc(cm)));
+        do {
+          const int q = __ffs(cm) - 1;
+          cm &= cm - 1u;
+          const int pos = slot_pos(q, tid);
+          cand_key[s] = order_key(rowbuf[pos]);
+          cand_pos[s] = uint32_t(pos);
+          ++s;
+        } while (cm);
+      }
+      __syncthreads();
+      start_next();
+      const uint32_t nc = g.in_bin;
+      const bool has = uint32_t(tid) < nc;
+      const uint32_t ck = has ? cand_key[tid] : 0u, cp = has ? cand_pos[tid] : 0u;
+      for (int it = 0; it < kMaxRefine && !range_done(g); ++it)
+        refine_cands(g, has, ck, hist, s_sel);
+      bool take = has && ck > g.hi;
+      if (has && ck >= g.lo && ck <= g.hi) {
         if (g.in_bin == g.rem) {
-          sel |= eq;
-        } else {  // one key value: its lowest `rem` positions
-          uint32_t lane_pre[kRounds];
-          ordered_slots(eq, hist, wsum, lane_pre);
+          take = true;
+        } else {  // one key value: the lowest positions win
+          uint32_t before = 0;
+          for (uint32_t c = 0; c < nc; ++c) before += (cand_key[c] == ck && cand_pos[c] < cp);
+          take = before < g.rem;
+        }
+      }
+      if (take) {
+        const uint32_t r = cp / kRoundSpan, w = cp % kRoundSpan;
+        atomicOr(tie_bits + w / 4, 1u << (4 * r + (w & 3)));
+      }
+      __syncthreads();
+      sel |= tie_bits[tid];
+    } else {
+      // more than 1024 keys share the bin (or it is already decided): refine
+      // over the registers
+      start_next();
+      for (int it = 0; it < kMaxRefine && !range_done(g); ++it)
+        refine_regs(g, key, hist, wsum, s_sel);
+      uint32_t eq = 0;
 #pragma unroll
-          for (int r = 0; r < kRounds; ++r) {
-            uint32_t rank = hist[r * kWarps + warp] + lane_pre[r];
+      for (int q = 0; q < kPer; ++q) {
+        sel |= uint32_t(key[q] > g.hi) << q;
+        eq |= uint32_t(key[q] >= g.lo && key[q] <= g.hi) << q;
+      }
+      if (g.in_bin == g.rem) {
+        sel |= eq;
+      } else {  // one key value: its lowest `rem` positions
+        uint32_t pre[2];
+        ordered_slots(eq, tab, wsum, pre);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int q = 4 * r + e;
-              if ((eq >> q) & 1u) {
-                if (rank < g.rem) sel |= 1u << q;
-                ++rank;
-              }
+        for (int r = 0; r < kRounds; ++r) {
+          uint32_t rank = tab[r * kWarps + warp] + ((pre[r >> 2] >> (8 * (r & 3))) & 255u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int q = 4 * r + e;
+            if ((eq >> q) & 1u) {
+              if (rank < g.rem) sel |= 1u << q;
+              ++rank;
             }
           }
-          __syncthreads();  // the slot table is rebuilt below
         }
+        __syncthreads();  // the slot table is rebuilt below
       }
     }
 
-    uint32_t lane_pre[kRounds];
-    const uint32_t total_sel = ordered_slots(sel, hist, wsum, lane_pre);
+    uint32_t pre[2];
+    const uint32_t total_sel = ordered_slots(sel, tab, wsum, pre);
     int32_t* out = idx + int64_t(row) * k;
-#pragma unroll
-    for (int r = 0; r < kRounds; ++r) {
-      const uint32_t nib = (sel >> (4 * r)) & 15u;
-      if (nib) {
-        uint32_t slot = hist[r * kWarps + warp] + lane_pre[r];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if ((nib >> e) & 1u) out[slot++] = r * kRoundSpan + 4 * tid + e;
-      }
+    for (uint32_t m = sel; m; m &= m - 1u) {   // this thread's chosen slots
+      const int q = __ffs(m) - 1, r = q >> 2;
+      const uint32_t slot = tab[r * kWarps + warp] + ((pre[r >> 2] >> (8 * (r & 3))) & 255u) +
+                            __popc(sel & ((1u << q) - 1u) & (15u << (4 * r)));
+      out[slot] = r * kRoundSpan + 4 * tid + (q & 3);
     }
     for (int s2 = int(total_sel) + tid; s2 < k; s2 += kThreads) out[s2] = -1;
   }  // rows

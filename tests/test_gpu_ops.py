@@ -394,6 +394,52 @@ def test_topk_range_refinement_distributions(B):
     assert np.array_equal(idx.cpu().numpy(), ops.topk_positions(s, nv, k))
 
 
+def test_topk_many_rows_per_cta(B):
+    """More rows than SMs, so each persistent CTA selects several rows in turn
+    and its first round starts from the previous row's bin: rows whose scale
+    jumps by 1e6 either way, rows with fewer than k valid scores, exactly k,
+    and one key value follow one another; every row equals the oracle's."""
+    g = synth.rng(18)
+    R, n, k = 1400, 4096, 256
+    s = synth.normal_f32(g, (R, n))
+    scale = np.float32(10.0) ** g.choice([-6, -3, 0, 0, 0, 3, 6], size=R).astype(np.float32)
+    s *= scale[:, None]
+    s[::9] += np.float32(50.0)
+    s[5::11] = np.round(s[5::11])                     # ties at the threshold
+    s[7::13] = 2.5                                    # one key value
+    nv = np.full(R, n, np.int32)
+    nv[3::7] = g.integers(0, 2 * k, size=nv[3::7].size)   # some below k, some above
+    nv[4::17] = k
+    idx = torch.empty(R, k, dtype=torch.int32, device="cuda")
+    B.biv_topk(dev(s), dev(nv), k, idx)
+    got, ref = idx.cpu().numpy(), ops.topk_positions(s, nv, k)
+    bad = np.nonzero((got != ref).any(axis=1))[0]
+    assert bad.size == 0, f"rows differ: {bad[:20]} (of {bad.size})"
+
+
+def test_topk_nan_never_chosen(B):
+    """NaN scores of either sign and any payload are never chosen, as in the
+    oracle (a NaN is not greater than -inf); the rest of the row is selected
+    as if they were -inf."""
+    g = synth.rng(17)
+    R, n, k = 4, 3000, 200
+    s = synth.normal_f32(g, (R, n))
+    nan_bits = np.array([0x7FC00000, 0x7F800001, 0x7FFFFFFF, 0xFFC00000, 0xFF800001, 0xFFFFFFFF],
+                        np.uint32)
+    for r in range(R):
+        pos = g.choice(n, size=300 + 100 * r, replace=False)
+        s[r, pos] = nan_bits[g.integers(0, nan_bits.size, pos.size)].view(np.float32)
+    s[3, 150:] = np.uint32(0x7FC00000).view(np.float32)   # fewer than k non-NaN scores
+    nv = np.full(R, n, np.int32)
+    idx = torch.empty(R, k, dtype=torch.int32, device="cuda")
+    B.biv_topk(dev(s), dev(nv), k, idx)
+    got = idx.cpu().numpy()
+    assert np.array_equal(got, ops.topk_positions(s, nv, k))
+    for r in range(R):
+        chosen = got[r][got[r] >= 0]
+        assert not np.isnan(s[r, chosen]).any()
+
+
 def test_router_topk(B):
     g = synth.rng(16)
     R, E, k = 300, 64, 6
