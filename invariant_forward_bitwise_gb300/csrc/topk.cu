@@ -4,8 +4,10 @@
 // order, so the same set is always accumulated in the same order).
 //
 // Persistent CTAs of 1024 threads, one row at a time.  A row's scores are
-// copied to shared memory with cp.async while the CTA works on the previous
-// row, so the HBM read overlaps the selection.  Thread t then keeps 32 keys
+// copied to shared memory while the CTA works on the previous row, so the
+// HBM read overlaps the selection: by a few bulk copies issued by one thread
+// when rows are 16-byte aligned (8192 per-thread 16-byte copies kept the
+// load/store unit busy through the whole selection), else by cp.async.  Thread t then keeps 32 keys
 // in registers: in round r (0..7) the four consecutive positions
 // 4096 r + 4 t + e (e = 0..3).  Scores become order-preserving 32-bit keys:
 // +0 and -0 map to one key, and NaN, -inf and the positions past valid_len
@@ -268,34 +270,51 @@ __device__ __forceinline__ int row_valid(const int32_t* valid_len, int row, int 
   return min(max(valid_len[row], 0), n);
 }
 
-// Start the copy of a row's valid scores into buf (16-byte pieces where the
-// row allows them); the positions past them are set to -inf.
+constexpr int kBulkChunk = 4096;   // floats per bulk copy
+
+// Start the copy of a row's valid scores into buf; the positions past them
+// are set to -inf.  VEC (16-byte aligned rows): bulk copies of the first
+// nv & ~3 scores by thread 0, completing on mbarrier `bar`, and plain loads
+// of the rest; the caller has ordered every read of buf before this call
+// with a barrier.  Otherwise: cp.async, 4 or 16 bytes per copy.
 template <bool VEC>
 __device__ __forceinline__ void prefetch_row(float* buf, const float* __restrict__ scores,
-                                             int64_t ld, int row, int nv) {
+                                             int64_t ld, int row, int nv, uint32_t bar) {
   const float* src = scores + int64_t(row) * ld;
+  if constexpr (VEC) {
+    const int nv4 = nv & ~3;
+    if (threadIdx.x == 0) {
+      fence_proxy_async();
+      mbar_expect_tx(bar, uint32_t(nv4) * 4u);
+      for (int off = 0; off < nv4; off += kBulkChunk)
+        bulk_load(smem_u32(buf + off), src + off, uint32_t(min(kBulkChunk, nv4 - off)) * 4u, bar);
+    }
+    for (int j = nv4 + threadIdx.x; j < kMaxN; j += kThreads) buf[j] = j < nv ? __ldg(src + j) : -INFINITY;
+  } else {
+    const bool a16 = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
 #pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
-    const int j0 = r * kRoundSpan + 4 * threadIdx.x;
-    if (VEC && j0 + 3 < nv) {
-      cp_async16(buf + j0, src + j0);
-    } else {
+    for (int r = 0; r < kRounds; ++r) {
+      const int j0 = r * kRoundSpan + 4 * threadIdx.x;
+      if (a16 && j0 + 3 < nv) {
+        cp_async16(buf + j0, src + j0);
+      } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (j0 + e < nv)
-          cp_async4(buf + j0 + e, src + j0 + e);
-        else
-          buf[j0 + e] = -INFINITY;
+        for (int e = 0; e < 4; ++e) {
+          if (j0 + e < nv)
+            cp_async4(buf + j0 + e, src + j0 + e);
+          else
+            buf[j0 + e] = -INFINITY;
+        }
       }
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads, 1)
     topk_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ valid_len,
-                int rows, int n, int k, int32_t* __restrict__ idx) {
+                int rows, int n, int k, int32_t* __restrict__ idx, int* err) {
   extern __shared__ float4 rowbuf4[];                // one row of scores (kMaxN floats)
   float* rowbuf = reinterpret_cast<float*>(rowbuf4);
   __shared__ __align__(16) uint32_t hist[kBins];     // bin counts, zero between rounds
@@ -306,12 +325,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t cand_key[kThreads];            // candidate list
   __shared__ uint32_t cand_pos[kThreads];
   __shared__ uint32_t tie_bits[kThreads];            // chosen candidates, as thread-slot masks
+  __shared__ __align__(8) uint64_t row_bar;          // bulk copies of the next row landed
 
   const int tid = threadIdx.x, warp = tid >> 5;
   reinterpret_cast<uint4*>(hist)[tid] = make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t bar = smem_u32(&row_bar);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
   int row = blockIdx.x;
   int nv_next = row < rows ? row_valid(valid_len, row, n) : 0;
-  if (row < rows) prefetch_row<VEC>(rowbuf, scores, ld, row, nv_next);
+  if (row < rows) prefetch_row<VEC>(rowbuf, scores, ld, row, nv_next, bar);
+  uint32_t parity = 0;
   // The first round counts only the bins from lbin up: the bin below the
   // one this CTA's previous row chose (its rows are alike, as the causal
   // rows of one indexer are).  Keys below never reach the histogram, which
@@ -319,8 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // lbin up is counted again in full.  lbin changes the time, not the result.
   uint32_t lbin = 0;
   for (; row < rows; row += gridDim.x) {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncthreads();  // the row is in shared memory; the previous row's tables are free
+    bool landed = true;
+    if (VEC)
+      landed = mbar_wait(bar, parity, err);
+    else
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    parity ^= 1u;
+    // the row is in shared memory; the previous row's tables are free
+    if (!__syncthreads_and(landed)) return;
 
     // keys, and the first round's histogram of their top 12 bits
     uint32_t key[kPer];
@@ -343,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto start_next = [&]() {
       if (row + int(gridDim.x) < rows) {
         nv_next = row_valid(valid_len, row + gridDim.x, n);
-        prefetch_row<VEC>(rowbuf, scores, ld, row + gridDim.x, nv_next);
+        prefetch_row<VEC>(rowbuf, scores, ld, row + gridDim.x, nv_next, bar);
       }
     };
     if (tid == 0) s_cnt = 0u;
@@ -483,7 +516,7 @@ biv_status biv_topk(const float* scores, int64_t ld, const int32_t* valid_len, i
   }
   const int sms = sm_count() > 0 ? sm_count() : 148;
   kern<<<std::min(rows, sms), kThreads, kRowBytes, as_cuda(stream)>>>(scores, ld, valid_len, rows,
-                                                                     n, k, idx);
+                                                                     n, k, idx, device_error_word());
   return check_launch("topk");
 }
 
