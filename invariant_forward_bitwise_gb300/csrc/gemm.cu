@@ -36,10 +36,15 @@ struct Fp8Cfg {
   static constexpr int BK = 128;                      // 128 e4m3 = one 128-byte swizzle row
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (160 * 1024) / STAGE > 8 ? 8 : (160 * 1024) / STAGE;
+  static constexpr int STAGE = A_BYTES + B_BYTES;     // one K block of A and of B
+  static constexpr int BLOCKS = 4;                    // K blocks in the ring (kpb per stage)
   static constexpr int TMEM_COLS = 2 * BN;            // two accumulator buffers
-  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+  static constexpr int MAX_GROUPS = 1024;
+  static constexpr int EPI_WARPS = 16;                // lane quarter x 64-column quarter
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int SMEM =
+      BLOCKS * STAGE + 1024 + (2 * BLOCKS + 4) * 8 + 16 + 2 * (MAX_GROUPS + 1) * 4;
+  static_assert(BN == 4 * 64, "each epilogue warp promotes one 64-column quarter");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -526,64 +531,80 @@ __global__ void __launch_bounds__(256) gemm_fold_kernel(const float* __restrict_
 }
 
 // ------------------------------------------------------------- FP8 kernel --
-// 6 warps: warp 0 = TMA producer, warp 1 = MMA issuer (+TMEM owner),
-// warps 2..5 = promotion/epilogue (lane quarter = warp % 4).  For each
-// 128-wide K block the MMA writes a fresh FP32 partial into one of two TMEM
-// buffers; the epilogue warps fold it into registers as
-// acc = fma(sa*sb, partial, acc), blocks in ascending order.
-// grid (ceil(N/BN), tiles over groups).
+// Block-scaled e4m3 GEMM (per 128-wide K block: a scale per A row and one per
+// 128 x 128 block of B), optionally grouped (expert g's rows
+// [offs[g], offs[g+1]) of A against its weights, rows [g N, g N + N) of B).
+// Persistent CTAs walk 128 x 256 tiles, the M tiles of all groups in group
+// order, N tiles fastest.
+// Pipeline: when K is a whole number of 128-wide blocks, a stage holds
+// kpb = 2 K blocks, brought by one 3-D copy per operand (two stages of
+// 96 KB; otherwise four stages of one block).  TMA moves about twice the
+// bytes per SM clock with two 128-byte panels per row as with one (measured
+// on GB300), and one-panel copies left the MMA waiting.
+// Warps: 0 = TMA producer, 1 = MMA issuer and TMEM owner, 2..17 =
+// promotion/epilogue (lane quarter = warp % 4, 64-column quarter =
+// (warp - 2) / 4).  For each K block the MMA writes a fresh FP32 partial into
+// one of two TMEM buffers and the epilogue warps fold it into registers as
+// acc = fma(sa * sb, partial, acc), blocks in ascending order, while the MMA
+// fills the other buffer; a tile's store overlaps the next tile's first
+// MMAs.  64 running sums a thread keep the promotion loop in registers (with
+// 128, in eight warps, it spilled to local memory).
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(Fp8Cfg<BN>::THREADS, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     uint16_t* C, int64_t ldc, int M, int N, int K, const float* __restrict__ sa,
                     int64_t ld_sa, const float* __restrict__ sb, const int32_t* __restrict__ offs,
-                    int groups, int vec_ok, int* err) {
+                    int groups, int vec_ok, int kpb, int* err) {
   using Cfg = Fp8Cfg<BN>;
-  constexpr int S = Cfg::STAGES;
+  const int S = Cfg::BLOCKS / kpb;                    // stages of kpb K blocks
   extern __shared__ uint8_t smem_raw[];
-  // locate this CTA's (group, row range)
-  int g = 0, m0 = blockIdx.y * BM, m_end = M;
-  if (groups > 1) {
-    int before = 0;
-    g = -1;
-    for (int gg = 0; gg < groups; ++gg) {
-      const int lo = offs[gg], hi = offs[gg + 1];
-      const int nt = (hi - lo + BM - 1) / BM;
-      if (int(blockIdx.y) < before + nt) {
-        g = gg;
-        m0 = lo + (int(blockIdx.y) - before) * BM;
-        m_end = hi;
-        break;
-      }
-      before += nt;
-    }
-    if (g < 0) return;  // uniform early exit: nothing allocated yet
-  }
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + S * Cfg::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
-  const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
+  uint8_t* sA = smem;                                 // [S][kpb] A blocks
+  uint8_t* sB = smem + Cfg::BLOCKS * Cfg::A_BYTES;    // [S][kpb] B blocks
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::BLOCKS * Cfg::STAGE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * Cfg::BLOCKS + 4);
+  int* tpre = reinterpret_cast<int*>(tmem_slot + 4);   // [groups + 1]: M tiles before group g
+  int* goff = tpre + Cfg::MAX_GROUPS + 1;                // [groups + 1]: offs, in shared memory
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + Cfg::BLOCKS);
+  const uint32_t tfull0 = smem_u32(bars + 2 * Cfg::BLOCKS);
+  const uint32_t tempty0 = smem_u32(bars + 2 * Cfg::BLOCKS + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN;
   const int KB = (K + Cfg::BK - 1) / Cfg::BK;
   const int NB = (N + 127) / 128;
+  const int tiles_n = (N + BN - 1) / BN;
+  const int a_stage = kpb * Cfg::A_BYTES, b_stage = kpb * Cfg::B_BYTES;
 
-  if (threadIdx.x == 0) {
+  if (warp == 0) {   // tile prefix over the groups
+    int run = 0;
+    for (int g0 = 0; g0 < groups; g0 += 32) {
+      const int gg = g0 + lane;
+      int nt = 0;
+      if (gg < groups)
+        nt = groups > 1 ? (max(offs[gg + 1] - offs[gg], 0) + BM - 1) / BM : (M + BM - 1) / BM;
+      int incl = nt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (gg < groups) tpre[gg + 1] = run + incl;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tpre[0] = 0;
+    for (int gg = lane; gg <= groups; gg += 32) goff[gg] = groups > 1 ? offs[gg] : (gg ? M : 0);
+  }
+  if (threadIdx.x == 32) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(tfull0 + 8 * j, 1);
-      mbar_init(tempty0 + 8 * j, 4);
+      mbar_init(tempty0 + 8 * j, Cfg::EPI_WARPS);
     }
     fence_barrier_init();
   }
-  __syncwarp();
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
     tmem_relinquish();
@@ -592,72 +613,128 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int items = tpre[groups] * tiles_n;
+  // M tile mt -> its group (the last group whose tiles start at or before
+  // mt: empty groups are skipped), first row and row bound
+  auto locate = [&](int mt, int& g, int& m0, int& m_end) {
+    int lo = 0, hi = groups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tpre[mid] <= mt) lo = mid; else hi = mid - 1;
+    }
+    g = lo;
+    m0 = goff[g] + (mt - tpre[g]) * BM;
+    m_end = goff[g + 1];
+  };
 
   int issued = 0;
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    for (int i = 0; i < KB; ++i) {
-      const int s = i % S;
-      if (i >= S && !mbar_wait(empty0 + 8 * s, ((i / S) - 1) & 1, err)) break;
-      mbar_expect_tx(full0 + 8 * s, Cfg::STAGE);
-      tma_load_2d(smem_u32(sA + s * Cfg::A_BYTES), &tmA, full0 + 8 * s, i * Cfg::BK, m0);
-      tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full0 + 8 * s, i * Cfg::BK, g * N + n0);
-      issued = i + 1;
+    bool ok = true;
+    for (int t = blockIdx.x; t < items && ok; t += gridDim.x) {
+      int g, m0, m_end;
+      locate(t / tiles_n, g, m0, m_end);
+      const int n0 = (t % tiles_n) * BN;
+      for (int kb = 0; kb < KB; kb += kpb) {
+        const int s = issued % S;
+        if (issued >= S && !mbar_wait(empty0 + 8 * s, ((issued / S) - 1) & 1, err)) {
+          ok = false;
+          break;
+        }
+        // a 3-D copy past the last K block fills zeros and counts its bytes
+        mbar_expect_tx(full0 + 8 * s, uint32_t(a_stage + b_stage));
+        const uint32_t fb = full0 + 8 * s;
+        if (kpb == 2) {
+          tma_load_3d(smem_u32(sA + s * a_stage), &tmA, fb, 0, m0, kb);
+          tma_load_3d(smem_u32(sB + s * b_stage), &tmB, fb, 0, g * N + n0, kb);
+        } else {
+          tma_load_2d(smem_u32(sA + s * a_stage), &tmA, fb, kb * Cfg::BK, m0);
+          tma_load_2d(smem_u32(sB + s * b_stage), &tmB, fb, kb * Cfg::BK, g * N + n0);
+        }
+        ++issued;
+      }
     }
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc = idesc_mma(0u, BM, BN);
-    for (int i = 0; i < KB; ++i) {
-      const int s = i % S, j = i & 1;
-      if (i >= 2 && !mbar_wait(tempty0 + 8 * j, ((i >> 1) - 1) & 1, err)) break;
-      if (!mbar_wait(full0 + 8 * s, (i / S) & 1, err)) break;
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(sA + s * Cfg::A_BYTES);
-      const uint32_t b0 = smem_u32(sB + s * Cfg::B_BYTES);
+    int it = 0, st = 0;   // K blocks, stages consumed
+    bool ok = true;
+    for (int t = blockIdx.x; t < items && ok; t += gridDim.x) {
+      for (int kb = 0; kb < KB && ok; kb += kpb, ++st) {
+        const int s = st % S;
+        if (!mbar_wait(full0 + 8 * s, (st / S) & 1, err)) {
+          ok = false;
+          break;
+        }
+        for (int b = 0; b < kpb && kb + b < KB; ++b, ++it) {
+          const int j = it & 1;
+          if (it >= 2 && !mbar_wait(tempty0 + 8 * j, ((it >> 1) - 1) & 1, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * a_stage + b * Cfg::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + s * b_stage + b * Cfg::B_BYTES);
 #pragma unroll
-      for (int kk = 0; kk < Cfg::BK / 32; ++kk)
-        umma_f8(tmem + j * BN, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
-                kk != 0 ? 1u : 0u);
-      umma_commit(empty0 + 8 * s);
-      umma_commit(tfull0 + 8 * j);
+          for (int kk = 0; kk < Cfg::BK / 32; ++kk)
+            umma_f8(tmem + j * BN, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
+                    kk != 0 ? 1u : 0u);
+          umma_commit(tfull0 + 8 * j);
+        }
+        umma_commit(empty0 + 8 * s);
+      }
     }
   } else if (warp >= 2) {
-    const int q = warp & 3;
-    const int row = m0 + q * 32 + lane;
-    const bool live = row < m_end && row < M;
-    const float* sbg = sb + int64_t(g) * NB * KB + int64_t(n0 / 128) * KB;
-    float acc[BN];
-#pragma unroll
-    for (int c = 0; c < BN; ++c) acc[c] = 0.f;
+    const int q = warp & 3, cq = (warp - 2) >> 2;
+    int it = 0;
     bool ok = true;
-    for (int i = 0; i < KB && ok; ++i) {
-      const int j = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * j, (i >> 1) & 1, err))) {
-        ok = false;
-        break;
+    for (int t = blockIdx.x; t < items && ok; t += gridDim.x) {
+      int g, m0, m_end;
+      locate(t / tiles_n, g, m0, m_end);
+      const int nh = (t % tiles_n) * BN + cq * 64;   // this warp's first column
+      const int row = m0 + q * 32 + lane;
+      const bool live = row < m_end && row < M;
+      const bool hlive = nh < N;
+      const float* sbh = sb + (int64_t(g) * NB + (hlive ? nh / 128 : 0)) * KB;
+      float acc[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+      // block kb + 1's scales are loaded while block kb is promoted
+      const float* sar = sa + int64_t(live ? row : 0) * ld_sa;
+      float a_nx = live ? sar[0] : 0.f, b_nx = hlive ? sbh[0] : 0.f;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int j = it & 1;
+        const float scale = a_nx * b_nx;
+        if (kb + 1 < KB) {
+          a_nx = live ? sar[kb + 1] : 0.f;
+          b_nx = hlive ? sbh[kb + 1] : 0.f;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * j, (it >> 1) & 1, err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tb = tmem + j * BN + cq * 64 + (uint32_t(q * 32) << 16);
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tb + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) acc[c0 + c] = fmaf(scale, __uint_as_float(r[c]), acc[c0 + c]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8 * j);
       }
-      tc_fence_after();
-      const float scale = (live ? sa[int64_t(row) * ld_sa + i] : 0.f) * sbg[i];
-      const uint32_t tb = tmem + j * BN + (uint32_t(q * 32) << 16);
+      if (ok && live && hlive) {
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tb + c0, r);
-        tmem_ld_wait();
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t r[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) acc[c0 + c] = fmaf(scale, __uint_as_float(r[c]), acc[c0 + c]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * j);
-    }
-    if (ok && live) {
-#pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(acc[c0 + c]);
-        if (n0 + c0 < N) store_row32<false>(C, ldc, row, n0 + c0, N, r, vec_ok != 0);
+          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(acc[c0 + c]);
+          if (nh + c0 < N) store_row32<false>(C, ldc, row, nh + c0, N, r, vec_ok != 0);
+        }
       }
     }
   }
@@ -972,6 +1049,30 @@ bool make_map2k(CUtensorMap* m, const void* base, int64_t K, int64_t rows, int64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A K-major operand [rows, K] as a 3-D tensor {panel, rows, K / panel}
+// (elements): a box {panel, box_rows, 2} brings two consecutive K blocks,
+// landing as [block][row][panel] with 128-byte swizzling.  K % panel == 0.
+bool make_map_panels(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
+                     int64_t K, int64_t rows, int64_t ld, int panel, int box_rows) {
+  auto fn = tensor_map_encoder();
+  if (!fn || K % panel != 0) return false;
+  cuuint64_t dims[3] = {cuuint64_t(panel), cuuint64_t(rows), cuuint64_t(K / panel)};
+  cuuint64_t strides[2] = {cuuint64_t(ld * elem_bytes), cuuint64_t(panel * elem_bytes)};
+  cuuint32_t box[3] = {cuuint32_t(panel), cuuint32_t(box_rows), 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// FP8: two K blocks of 128 per pipeline stage when K is a whole number of
+// blocks (BIV_GEMM_KPB=1 keeps one; the tests check that neither changes a bit).
+int fp8_kpb_for(int K) {
+  const char* e = getenv("BIV_GEMM_KPB");
+  if (e && atoi(e) == 1) return 1;
+  return (K % 128 == 0 && K >= 256) ? 2 : 1;
+}
+
 struct Plan {
   int bn = 256;
   int kpb = 1;        // K blocks per pipeline stage
@@ -1149,7 +1250,7 @@ biv_status dispatch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv
 
 template <int BN>
 biv_status launch_fp8(const CUtensorMap& ta, const CUtensorMap& tb, const biv_gemm_desc& d,
-                      cudaStream_t s) {
+                      int kpb, cudaStream_t s) {
   using Cfg = Fp8Cfg<BN>;
   auto kern = gemm_fp8_kernel<BN>;
   static bool attr = false;
@@ -1161,11 +1262,15 @@ biv_status launch_fp8(const CUtensorMap& ta, const CUtensorMap& tb, const biv_ge
   }
   const int groups = d.groups > 1 ? d.groups : 1;
   const int vec_ok = aligned16(d.C) && (d.ldc * 2) % 16 == 0;
-  const int tiles_m = (d.M + BM - 1) / BM + (groups > 1 ? groups : 0);
-  dim3 grid((d.N + BN - 1) / BN, tiles_m, 1);
-  kern<<<grid, 192, Cfg::SMEM, s>>>(ta, tb, static_cast<uint16_t*>(d.C), d.ldc, d.M, d.N, d.K,
-                                    d.sa, d.ld_sa, d.sb, d.group_offsets, groups, vec_ok,
-                                    device_error_word());
+  // persistent grid: at most one CTA per SM, no more than the tiles there
+  // can be (each group rounds its rows up to whole tiles)
+  const int64_t tiles_m = (d.M + BM - 1) / BM + (groups > 1 ? groups : 0);
+  const int64_t items = tiles_m * ((d.N + BN - 1) / BN);
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items, sms)));
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(ta, tb, static_cast<uint16_t*>(d.C), d.ldc, d.M, d.N,
+                                             d.K, d.sa, d.ld_sa, d.sb, d.group_offsets, groups,
+                                             vec_ok, kpb, device_error_word());
   return check_launch("gemm_fp8");
 }
 
@@ -1191,6 +1296,8 @@ biv_status validate(const biv_gemm_desc* d) {
     if (d->c_dtype != BIV_BF16) return set_error(BIV_ERR_UNSUPPORTED, "gemm: FP8 GEMM writes bf16");
     BIV_REQUIRE(d->sa && d->sb && d->ld_sa >= (d->K + 127) / 128, "gemm: FP8 needs sa/sb");
     BIV_REQUIRE(d->groups <= 1 || d->group_offsets, "gemm: grouped needs offsets");
+    BIV_REQUIRE(d->groups <= Fp8Cfg<256>::MAX_GROUPS, "gemm: at most %d groups",
+                Fp8Cfg<256>::MAX_GROUPS);
   }
   return BIV_OK;
 }
@@ -1385,12 +1492,18 @@ biv_status biv_gemm(const biv_gemm_desc* d, void* ws, size_t ws_bytes, biv_strea
   }
   // FP8 block-scaled (optionally grouped)
   const int groups = d->groups > 1 ? d->groups : 1;
-  const int bn = 128;
-  if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d->A, d->K, d->M, d->lda, 128, BM) ||
-      !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d->B, d->K, int64_t(groups) * d->N, d->ldb,
-                128, bn))
-    return set_error(BIV_ERR_CUDA, "gemm_fp8: tensor map encoding failed");
-  return launch_fp8<128>(ta, tb, *d, s);
+  constexpr int bn = 256;
+  const int kpb = fp8_kpb_for(d->K);
+  const bool maps_ok =
+      kpb == 2 ? make_map_panels(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d->A, d->K, d->M, d->lda, 128,
+                                 BM) &&
+                     make_map_panels(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d->B, d->K,
+                                     int64_t(groups) * d->N, d->ldb, 128, bn)
+               : make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d->A, d->K, d->M, d->lda, 128, BM) &&
+                     make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d->B, d->K,
+                              int64_t(groups) * d->N, d->ldb, 128, bn);
+  if (!maps_ok) return set_error(BIV_ERR_CUDA, "gemm_fp8: tensor map encoding failed");
+  return launch_fp8<bn>(ta, tb, *d, kpb, s);
 }
 
 }  // extern "C"

@@ -333,6 +333,41 @@ def test_gemm_fp8_grouped(B):
         assert rel_err(got[lo:hi], ref) < REL, e
 
 
+@pytest.mark.parametrize("G,N,K", [(1, 640, 384), (5, 512, 1408), (3, 2816, 4096)])
+def test_fp8_two_block_stages_change_no_bit(B, monkeypatch, G, N, K):
+    """FP8 stages of two 128-wide K blocks (3-D TMA boxes; an odd block count
+    leaves the last stage's second block as zero fill) and of one block feed
+    the same MMAs and the same promotions: every output bit is the same; a
+    group with no rows and N % 256 == 128 included."""
+    g = synth.rng(G * 7 + N + K)
+    counts = [0] if G == 1 else [150, 0, 300, 5, 129][:G]
+    M = 333 if G == 1 else sum(counts)
+    a = rnd_bf16(g, M, K)
+    codes_b, sb = synth.fp8_block_weights(g, G, N, K)
+    ac = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    sa = torch.empty(M, K // 128, dtype=torch.float32, device="cuda")
+    B.biv_act_quant_fp8(dev(a), ac, sa)
+    bc = dev(codes_b.view(torch.uint8).reshape(G * N, K))
+    kw = {}
+    if G > 1:
+        offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        kw = dict(group_offsets=dev(offs), groups=G, M=M)
+    outs = []
+    for kpb in ["2", "1"]:
+        monkeypatch.setenv("BIV_GEMM_KPB", kpb)
+        c = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        B.biv_gemm(B.gemm_desc(ac, bc, c, sa=sa, sb=dev(sb if G > 1 else sb[0]), **kw))
+        outs.append(bits(c))
+    assert np.array_equal(outs[0], outs[1])
+    lo = 0 if G == 1 else counts[0] + counts[1]
+    hi = M if G == 1 else lo + counts[2]
+    e = 0 if G == 1 else 2
+    ref = ops.gemm_fp8_block(ac.cpu().numpy()[lo:hi], sa.cpu().numpy()[lo:hi],
+                             synth.fp8_bits(codes_b[e]), sb[e])
+    got = outs[0].view(np.uint16).reshape(M, N)[lo:hi]
+    assert rel_err((got.astype(np.uint32) << 16).view(np.float32), ref) < REL
+
+
 # -------------------------------------------------------------------- Top-K --
 def test_topk_brute_force_ties(B):
     g = synth.rng(14)
