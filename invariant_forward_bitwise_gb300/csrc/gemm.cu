@@ -43,7 +43,7 @@ struct Fp8Cfg {
   static constexpr int EPI_WARPS = 16;                // lane quarter x 64-column quarter
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int SMEM =
-      BLOCKS * STAGE + 1024 + (2 * BLOCKS + 4) * 8 + 16 + 2 * (MAX_GROUPS + 1) * 4;
+      BLOCKS * STAGE + 1024 + (2 * BLOCKS + 4) * 8 + 16 + (MAX_GROUPS + 1) * 4;
   static_assert(BN == 4 * 64, "each epilogue warp promotes one 64-column quarter");
 };
 
@@ -564,7 +564,6 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::BLOCKS * Cfg::STAGE);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * Cfg::BLOCKS + 4);
   int* tpre = reinterpret_cast<int*>(tmem_slot + 4);   // [groups + 1]: M tiles before group g
-  int* goff = tpre + Cfg::MAX_GROUPS + 1;                // [groups + 1]: offs, in shared memory
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + Cfg::BLOCKS);
   const uint32_t tfull0 = smem_u32(bars + 2 * Cfg::BLOCKS);
   const uint32_t tempty0 = smem_u32(bars + 2 * Cfg::BLOCKS + 2);
@@ -592,7 +591,6 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::THREADS, 1)
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) tpre[0] = 0;
-    for (int gg = lane; gg <= groups; gg += 32) goff[gg] = groups > 1 ? offs[gg] : (gg ? M : 0);
   }
   if (threadIdx.x == 32) {
     for (int s = 0; s < S; ++s) {
@@ -623,8 +621,8 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::THREADS, 1)
       if (tpre[mid] <= mt) lo = mid; else hi = mid - 1;
     }
     g = lo;
-    m0 = goff[g] + (mt - tpre[g]) * BM;
-    m_end = goff[g + 1];
+    m0 = (groups > 1 ? offs[g] : 0) + (mt - tpre[g]) * BM;
+    m_end = groups > 1 ? offs[g + 1] : M;
   };
 
   int issued = 0;
@@ -699,16 +697,9 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::THREADS, 1)
       float acc[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) acc[c] = 0.f;
-      // block kb + 1's scales are loaded while block kb is promoted
-      const float* sar = sa + int64_t(live ? row : 0) * ld_sa;
-      float a_nx = live ? sar[0] : 0.f, b_nx = hlive ? sbh[0] : 0.f;
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int j = it & 1;
-        const float scale = a_nx * b_nx;
-        if (kb + 1 < KB) {
-          a_nx = live ? sar[kb + 1] : 0.f;
-          b_nx = hlive ? sbh[kb + 1] : 0.f;
-        }
+        const float scale = (live ? sa[int64_t(row) * ld_sa + kb] : 0.f) * (hlive ? sbh[kb] : 0.f);
         if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * j, (it >> 1) & 1, err))) {
           ok = false;
           break;
