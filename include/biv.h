@@ -318,13 +318,20 @@ biv_status biv_gemm(const biv_gemm_desc* desc, void* workspace, size_t workspace
 biv_status biv_act_quant_fp8(const uint16_t* x, int64_t x_stride, int rows, int K,
                              uint8_t* codes, float* scales, biv_stream_t stream);
 
+/* biv_silu_mul followed by biv_act_quant_fp8 of its result, in one pass:
+ * gate_up = [g | u] bf16 [rows, 2I] (row stride gu_stride >= 2I); codes
+ * uint8 [rows, I] and scales float32 [rows, ceil(I/128)] are bit for bit what
+ * the two calls write (the bf16 activation is not stored).  I % 16 == 0. */
+biv_status biv_silu_mul_quant_fp8(const uint16_t* gate_up, int64_t gu_stride, int rows, int I,
+                                  uint8_t* codes, float* scales, biv_stream_t stream);
+
 /* -------------------------------------------------------------- Top-K ---
  * Sparse-attention selection ("Finish RL Training Faster", section
  * "让训练前向使用推理的数值": fixed tie-break and fixed position order): per row
  * r, among indices j < valid_len[r] with scores[r, j] > -inf, the k largest
  * scores, equal scores resolved toward the LOWER index; the chosen indices
  * are written to idx int32 [rows, k] in ASCENDING index order, padded with
- * -1.  -0.0 and +0.0 compare equal; NaN scores are not allowed.
+ * -1.  -0.0 and +0.0 compare equal; a NaN score is never chosen.
  * 0 < k <= n <= 32768, ld >= n. */
 biv_status biv_topk(const float* scores, int64_t ld, const int32_t* valid_len, int rows, int n,
                     int k, int32_t* idx, biv_stream_t stream);

@@ -24,7 +24,7 @@ EXPORTS = [
     "biv_rope_table", "biv_qk_norm_rope", "biv_kv_store_bf16", "biv_kv_fp8_quant", "biv_qkv_finalize", "biv_silu_mul_partials",
     "biv_kv_fp8_gather", "biv_attention_workspace", "biv_attention", "biv_attention_noalloc",
     "biv_gemm_workspace", "biv_gemm_partials", "biv_gemm",
-    "biv_act_quant_fp8", "biv_topk", "biv_router_topk", "biv_moe_dispatch", "biv_gather_rows",
+    "biv_act_quant_fp8", "biv_silu_mul_quant_fp8", "biv_topk", "biv_router_topk", "biv_moe_dispatch", "biv_gather_rows",
     "biv_moe_combine", "biv_logprob", "biv_lm_head_logprob_workspace", "biv_lm_head_logprob",
     "biv_ssd_workspace", "biv_ssd_scan",
     "biv_causal_conv1d", "biv_gated_rmsnorm", "biv_nvfp4_dequant",
@@ -144,6 +144,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "biv_attention_noalloc": ([P, P], I),
         "biv_gemm_workspace": ([P, P], I), "biv_gemm": ([P, P, C.c_size_t, P], I),
         "biv_act_quant_fp8": ([P, I64, I, I, P, P, P], I),
+        "biv_silu_mul_quant_fp8": ([P, I64, I, I, P, P, P], I),
         "biv_topk": ([P, I64, P, I, I, I, P, P], I),
         "biv_router_topk": ([P, I64, I, I, I, P, P, P], I),
         "biv_moe_dispatch": ([P, I, I, I, P, P, P, P], I),
@@ -375,6 +376,12 @@ def biv_gemm(desc: GemmDesc, ws: Optional[torch.Tensor] = None, stream=None):
 def biv_act_quant_fp8(x, codes, scales, stream=None):
     _check(load().biv_act_quant_fp8(_p(x), _rs(x), x.shape[0], x.shape[1], _p(codes), _p(scales),
                                     _stream(stream)), "biv_act_quant_fp8")
+
+
+def biv_silu_mul_quant_fp8(gate_up, codes, scales, stream=None):
+    _check(load().biv_silu_mul_quant_fp8(_p(gate_up), _rs(gate_up), gate_up.shape[0],
+                                         codes.shape[1], _p(codes), _p(scales), _stream(stream)),
+           "biv_silu_mul_quant_fp8")
 
 
 def biv_topk(scores, valid_len, k, idx, stream=None):

@@ -559,6 +559,48 @@ __global__ void act_quant_kernel(const uint16_t* __restrict__ x, int64_t xs, int
   if (lane == 0) scales[int64_t(row) * groups + g] = sc;
 }
 
+// SiLU-mul and the activation quantisation of its result in one pass: each
+// value is the bf16 silu_mul_kernel stores, quantised as act_quant_kernel
+// quantises it (the bf16 activation itself is not written).  One warp per
+// (row, 128-wide group).
+__global__ void silu_mul_quant_kernel(const uint16_t* __restrict__ gu, int64_t gs, int rows, int I,
+                                      uint8_t* __restrict__ codes, float* __restrict__ scales) {
+  pdl_wait();     // stream predecessor done, its writes visible
+  pdl_trigger();
+  const int groups = (I + 127) / 128;
+  const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= int64_t(rows) * groups) return;
+  const int row = int(gw / groups), g = int(gw % groups);
+  const uint16_t* gr = gu + int64_t(row) * gs;
+  float v[4];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = g * 128 + lane * 4 + i;
+    if (j < I) {
+      const float gv = bf2f(gr[j]), uv = bf2f(gr[I + j]);
+      v[i] = bf2f(f2bf((gv / (1.0f + expf(-gv))) * uv));
+    } else {
+      v[i] = 0.f;
+    }
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = warp_max(amax);
+  const float sc = amax == 0.f ? 1.0f : amax / 448.0f;
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) packed |= uint32_t(f2e4m3(v[i] / sc)) << (8 * i);
+  uint8_t* dst = codes + int64_t(row) * I + g * 128 + lane * 4;
+  if (g * 128 + lane * 4 + 4 <= I) {
+    *reinterpret_cast<uint32_t*>(dst) = packed;
+  } else {
+    for (int i = 0; i < 4; ++i)
+      if (g * 128 + lane * 4 + i < I) dst[i] = uint8_t(packed >> (8 * i));
+  }
+  if (lane == 0) scales[int64_t(row) * groups + g] = sc;
+}
+
 // -------------------------------------------------------------- logprob ----
 // One CTA of 512 threads per row.  Thread t folds float4 chunks t, t+512, ...
 // into an online (max, sumexp) pair; pairs are then merged by a warp xor tree
@@ -982,6 +1024,18 @@ biv_status biv_act_quant_fp8(const uint16_t* x, int64_t xs, int rows, int K, uin
   act_quant_kernel<<<unsigned((warps * 32 + 255) / 256), 256, 0, as_cuda(stream)>>>(
       x, xs, rows, K, codes, scales);
   return check_launch("act_quant_fp8");
+}
+
+biv_status biv_silu_mul_quant_fp8(const uint16_t* gu, int64_t gs, int rows, int I, uint8_t* codes,
+                                  float* scales, biv_stream_t stream) {
+  BIV_REQUIRE(rows >= 0 && I > 0 && I % 16 == 0, "silu_mul_quant_fp8: I=%d must be a multiple of 16",
+              I);
+  if (rows == 0) return BIV_OK;
+  BIV_REQUIRE(gu && codes && scales && gs >= 2 * int64_t(I), "silu_mul_quant_fp8: bad arguments");
+  const int64_t warps = int64_t(rows) * ((I + 127) / 128);
+  launch_pdl(silu_mul_quant_kernel, unsigned((warps * 32 + 255) / 256), 256, 0, as_cuda(stream), gu,
+             gs, rows, I, codes, scales);
+  return check_launch("silu_mul_quant_fp8");
 }
 
 biv_status biv_logprob(const float* z, int64_t ld, const int32_t* target, int T, int V, float* lp,

@@ -125,7 +125,6 @@ class ExpertParallelMoE:
         self.aq = torch.empty(R, d, **u8)
         self.as_ = torch.empty(R, kb(d), **f32)
         self.sgu_out = torch.empty(T, I2, **bf)
-        self.sact = torch.empty(T, I, **bf)
         self.sactq = torch.empty(T, I, **u8)
         self.sacts = torch.empty(T, kb(I), **f32)
         self.shared = torch.empty(T, d, **bf)
@@ -135,15 +134,13 @@ class ExpertParallelMoE:
         """Grouped FP8 MLPs of the local experts over n grouped rows."""
         dev = aq.device
         gu = torch.empty(n, self.I2, dtype=torch.bfloat16, device=dev)
-        act = torch.empty(n, self.I, dtype=torch.bfloat16, device=dev)
         actq = torch.empty(n, self.I, dtype=torch.uint8, device=dev)
         acts = torch.empty(n, (self.I + 127) // 128, dtype=torch.float32, device=dev)
         y = torch.empty(n, self.d, dtype=torch.bfloat16, device=dev)
         if n:
             biv.biv_gemm(biv.gemm_desc(aq, self.wgu, gu, sa=as_, sb=self.sgu, group_offsets=offsets_dev,
                                        groups=self.epr, M=n))
-            biv.biv_silu_mul(gu, act)
-            biv.biv_act_quant_fp8(act, actq, acts)
+            biv.biv_silu_mul_quant_fp8(gu, actq, acts)
             biv.biv_gemm(biv.gemm_desc(actq, self.wd, y, sa=acts, sb=self.sd, group_offsets=offsets_dev,
                                        groups=self.epr, M=n))
         return y
@@ -184,8 +181,7 @@ class ExpertParallelMoE:
         y = self.r.exchange_rows(y_recv, recv_splits, send_splits)
         # shared expert on this rank's tokens, then the FP32 fixed-slot merge
         biv.biv_gemm(biv.gemm_desc(self.hq[:T], self.sh_gu, self.sgu_out[:T], sa=self.hs[:T], sb=self.sh_sgu))
-        biv.biv_silu_mul(self.sgu_out[:T], self.sact[:T])
-        biv.biv_act_quant_fp8(self.sact[:T], self.sactq[:T], self.sacts[:T])
+        biv.biv_silu_mul_quant_fp8(self.sgu_out[:T], self.sactq[:T], self.sacts[:T])
         biv.biv_gemm(biv.gemm_desc(self.sactq[:T], self.sh_d, self.shared[:T], sa=self.sacts[:T], sb=self.sh_sd))
         biv.biv_moe_combine(y, self.src[:R], self.w[:T], self.shared[:T], self.out[:T])
         return self.out[:T]

@@ -57,12 +57,10 @@ class MoEBlock:
         self.aq = torch.empty(R, d, **u8)
         self.as_ = torch.empty(R, (d + 127) // 128, **f32)
         self.gu = torch.empty(R, I2, **bf)
-        self.act = torch.empty(R, I, **bf)
         self.actq = torch.empty(R, I, **u8)
         self.acts = torch.empty(R, (I + 127) // 128, **f32)
         self.y = torch.empty(R, d, **bf)
         self.sgu_out = torch.empty(T, I2, **bf)
-        self.sact = torch.empty(T, I, **bf)
         self.sactq = torch.empty(T, I, **u8)
         self.sacts = torch.empty(T, (I + 127) // 128, **f32)
         self.shared = torch.empty(T, d, **bf)
@@ -81,14 +79,12 @@ class MoEBlock:
         # routed experts: grouped FP8 GEMMs over the dispatched rows
         biv.biv_gemm(biv.gemm_desc(self.aq[:R], self.wgu, self.gu[:R], sa=self.as_[:R], sb=self.sgu,
                                    group_offsets=self.offs, groups=E, M=R))
-        biv.biv_silu_mul(self.gu[:R], self.act[:R])
-        biv.biv_act_quant_fp8(self.act[:R], self.actq[:R], self.acts[:R])
+        biv.biv_silu_mul_quant_fp8(self.gu[:R], self.actq[:R], self.acts[:R])
         biv.biv_gemm(biv.gemm_desc(self.actq[:R], self.wd, self.y[:R], sa=self.acts[:R], sb=self.sd,
                                    group_offsets=self.offs, groups=E, M=R))
         # shared expert on every token
         biv.biv_gemm(biv.gemm_desc(self.hq[:T], self.sh_gu, self.sgu_out[:T], sa=self.hs[:T], sb=self.sh_sgu))
-        biv.biv_silu_mul(self.sgu_out[:T], self.sact[:T])
-        biv.biv_act_quant_fp8(self.sact[:T], self.sactq[:T], self.sacts[:T])
+        biv.biv_silu_mul_quant_fp8(self.sgu_out[:T], self.sactq[:T], self.sacts[:T])
         biv.biv_gemm(biv.gemm_desc(self.sactq[:T], self.sh_d, self.shared[:T], sa=self.sacts[:T], sb=self.sh_sd))
         # FP32 fixed-slot merge
         biv.biv_moe_combine(self.y, self.src[:R], self.w[:T], self.shared[:T], self.out[:T])

@@ -309,6 +309,30 @@ def test_gemm_fp8_block_scaled_parity(B):
     assert np.array_equal(bits(one), bits(c[150:151]))
 
 
+@pytest.mark.parametrize("rows,I", [(1, 1408), (300, 1408), (7, 144)])
+def test_silu_mul_quant_equals_two_calls(B, rows, I):
+    """The fused SiLU-mul + FP8 activation quantisation writes the codes and
+    scales of biv_silu_mul followed by biv_act_quant_fp8, bit for bit (a
+    ragged last group included); they are the oracle's quantisation of that
+    bf16 activation, which is within the SiLU-mul tolerance of the oracle's."""
+    g = synth.rng(rows + I)
+    gu = rnd_bf16(g, rows, 2 * I)
+    gu[0, :I] = 0.0                                   # an all-zero first row: scale 1
+    gud = dev(gu)
+    act = torch.empty(rows, I, dtype=torch.bfloat16, device="cuda")
+    q2 = torch.empty(rows, I, dtype=torch.uint8, device="cuda")
+    s2 = torch.empty(rows, (I + 127) // 128, dtype=torch.float32, device="cuda")
+    B.biv_silu_mul(gud, act)
+    B.biv_act_quant_fp8(act, q2, s2)
+    q1 = torch.full((rows, I), 0xAB, dtype=torch.uint8, device="cuda")
+    s1 = torch.full((rows, (I + 127) // 128), float("nan"), dtype=torch.float32, device="cuda")
+    B.biv_silu_mul_quant_fp8(gud, q1, s1)
+    assert np.array_equal(bits(q1), bits(q2)) and np.array_equal(bits(s1), bits(s2))
+    rq, rs = ops.act_quant_fp8(host_f32(act))
+    assert np.array_equal(q1.cpu().numpy(), rq) and np.array_equal(s1.cpu().numpy(), rs)
+    assert rel_err(host_f32(act), ops.silu_mul(gu.float().numpy())) < REL
+
+
 def test_gemm_fp8_grouped(B):
     g = synth.rng(13)
     G, N, K = 4, 256, 384
