@@ -527,78 +527,79 @@ __global__ void kv_fp8_gather_kernel(const uint8_t* __restrict__ codes,
 }
 
 // ---------------------------------------------------- activation quant ----
-// One warp per (row, 128-wide group).
+// Half a warp per (row, 128-wide group), 8 values a lane (16-byte loads):
+// amax over the 16 lanes, s = amax / 448 (1 when amax = 0), codes by RNE.
+__device__ __forceinline__ float half_warp_max(float v) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Quantise the 8 values of one lane of its group (K % 16 == 0: a lane's
+// values are all in the row or none); every lane of the warp calls this for
+// the shuffles, and only lanes with `on` store: their codes, and lane % 16 ==
+// 0 the group's scale.
+__device__ __forceinline__ void quant8_store(const float (&v)[8], bool on, uint8_t* dst,
+                                             float* scale_dst, int lane) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = half_warp_max(amax);
+  const float sc = amax == 0.f ? 1.0f : amax / 448.0f;
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i >> 2] |= uint32_t(f2e4m3(v[i] / sc)) << (8 * (i & 3));
+  if (!on) return;
+  *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  if ((lane & 15) == 0) *scale_dst = sc;
+}
+
 __global__ void act_quant_kernel(const uint16_t* __restrict__ x, int64_t xs, int rows, int K,
                                  uint8_t* __restrict__ codes, float* __restrict__ scales) {
   const int groups = (K + 127) / 128;
-  const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t hw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 4;   // half warp
   const int lane = threadIdx.x & 31;
-  if (gw >= int64_t(rows) * groups) return;
-  const int row = int(gw / groups), g = int(gw % groups);
-  const uint16_t* src = x + int64_t(row) * xs + g * 128;
-  float v[4];
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int j = lane * 4 + i;
-    v[i] = (g * 128 + j < K) ? bf2f(src[j]) : 0.f;
-    amax = fmaxf(amax, fabsf(v[i]));
-  }
-  amax = warp_max(amax);
-  const float sc = amax == 0.f ? 1.0f : amax / 448.0f;
-  uint32_t packed = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) packed |= uint32_t(f2e4m3(v[i] / sc)) << (8 * i);
-  uint8_t* dst = codes + int64_t(row) * K + g * 128 + lane * 4;
-  if (g * 128 + lane * 4 + 4 <= K) {
-    *reinterpret_cast<uint32_t*>(dst) = packed;
+  const bool on = hw < int64_t(rows) * groups;   // both halves of a warp reach the shuffles
+  const int row = on ? int(hw / groups) : 0, g = on ? int(hw % groups) : 0;
+  const int c0 = g * 128 + (lane & 15) * 8;
+  const bool live = on && c0 < K;
+  float v[8];
+  if (live) {
+    unpack8(*reinterpret_cast<const uint4*>(x + int64_t(row) * xs + c0), v);
   } else {
-    for (int i = 0; i < 4; ++i)
-      if (g * 128 + lane * 4 + i < K) dst[i] = uint8_t(packed >> (8 * i));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
   }
-  if (lane == 0) scales[int64_t(row) * groups + g] = sc;
+  quant8_store(v, live, codes + int64_t(row) * K + c0, scales + int64_t(row) * groups + g, lane);
 }
 
 // SiLU-mul and the activation quantisation of its result in one pass: each
 // value is the bf16 silu_mul_kernel stores, quantised as act_quant_kernel
-// quantises it (the bf16 activation itself is not written).  One warp per
-// (row, 128-wide group).
+// quantises it (the bf16 activation itself is not written).  Half a warp per
+// (row, 128-wide group), 8 values a lane.
 __global__ void silu_mul_quant_kernel(const uint16_t* __restrict__ gu, int64_t gs, int rows, int I,
                                       uint8_t* __restrict__ codes, float* __restrict__ scales) {
   pdl_wait();     // stream predecessor done, its writes visible
   pdl_trigger();
   const int groups = (I + 127) / 128;
-  const int64_t gw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t hw = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 4;   // half warp
   const int lane = threadIdx.x & 31;
-  if (gw >= int64_t(rows) * groups) return;
-  const int row = int(gw / groups), g = int(gw % groups);
-  const uint16_t* gr = gu + int64_t(row) * gs;
-  float v[4];
-  float amax = 0.f;
+  const bool on = hw < int64_t(rows) * groups;   // both halves of a warp reach the shuffles
+  const int row = on ? int(hw / groups) : 0, g = on ? int(hw % groups) : 0;
+  const int c0 = g * 128 + (lane & 15) * 8;
+  const bool live = on && c0 < I;
+  float v[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int j = g * 128 + lane * 4 + i;
-    if (j < I) {
-      const float gv = bf2f(gr[j]), uv = bf2f(gr[I + j]);
-      v[i] = bf2f(f2bf((gv / (1.0f + expf(-gv))) * uv));
-    } else {
-      v[i] = 0.f;
-    }
-    amax = fmaxf(amax, fabsf(v[i]));
-  }
-  amax = warp_max(amax);
-  const float sc = amax == 0.f ? 1.0f : amax / 448.0f;
-  uint32_t packed = 0;
+  for (int i = 0; i < 8; ++i) v[i] = 0.f;
+  if (live) {
+    const uint16_t* gr = gu + int64_t(row) * gs;
+    float gv[8], uv[8];
+    unpack8(*reinterpret_cast<const uint4*>(gr + c0), gv);
+    unpack8(*reinterpret_cast<const uint4*>(gr + I + c0), uv);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) packed |= uint32_t(f2e4m3(v[i] / sc)) << (8 * i);
-  uint8_t* dst = codes + int64_t(row) * I + g * 128 + lane * 4;
-  if (g * 128 + lane * 4 + 4 <= I) {
-    *reinterpret_cast<uint32_t*>(dst) = packed;
-  } else {
-    for (int i = 0; i < 4; ++i)
-      if (g * 128 + lane * 4 + i < I) dst[i] = uint8_t(packed >> (8 * i));
+    for (int i = 0; i < 8; ++i) v[i] = bf2f(f2bf((gv[i] / (1.0f + expf(-gv[i]))) * uv[i]));
   }
-  if (lane == 0) scales[int64_t(row) * groups + g] = sc;
+  quant8_store(v, live, codes + int64_t(row) * I + c0, scales + int64_t(row) * groups + g, lane);
 }
 
 // -------------------------------------------------------------- logprob ----
@@ -722,56 +723,77 @@ __global__ void router_kernel(const float* __restrict__ logits, int64_t ld, int 
 }
 
 // ------------------------------------------------------------- dispatch ----
-// One CTA per expert e: count every expert's entries (shared-memory counters,
-// order-free integers), take e's start as the sum of the counts below it, then
-// walk the entries in ascending (t, s) order in blocks of 1024 and place e's
-// entries by a block-wide ballot scan, so the layout is unique.
+// One CTA per expert e.  e's first slot is the number of entries routed to
+// an expert below e (a per-thread count, then one block sum: order-free
+// integers).  Then e's entries are placed in ascending (t, s) order, 4096 per
+// round (4 consecutive entries a thread) by a block-wide scan of the hit
+// counts, so the layout is unique.
+__device__ __forceinline__ int warp_incl_scan_i(int x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
 __global__ void __launch_bounds__(1024) moe_dispatch_kernel(const int32_t* __restrict__ idx,
                                                             int n, int E,
                                                             int32_t* __restrict__ offsets,
                                                             int32_t* __restrict__ perm,
                                                             int32_t* __restrict__ src_row) {
-  extern __shared__ int sm_counts[];  // [E]
-  __shared__ int wcount[32];
+  __shared__ int wsum[32];
   __shared__ int s_start;
   const int e = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int x = tid; x < E; x += blockDim.x) sm_counts[x] = 0;
-  __syncthreads();
+  int below = 0;
   for (int i = tid; i < n; i += blockDim.x) {
     const int v = idx[i];
-    if (v >= 0 && v < E) atomicAdd(sm_counts + v, 1);
+    below += (v >= 0 && v < e) ? 1 : 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) below += __shfl_xor_sync(0xffffffffu, below, o);
+  if (lane == 0) wsum[warp] = below;
+  __syncthreads();
+  if (warp == 0) {
+    int x = wsum[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) s_start = x;
   }
   __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int x = 0; x < e; ++x) acc += sm_counts[x];
-    s_start = acc;
-    offsets[e] = acc;
-    if (e == E - 1) offsets[E] = acc + sm_counts[e];
-  }
-  __syncthreads();
-  int at = s_start;
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int base = 0; base < n; base += blockDim.x) {
-    const int i = base + tid;
-    const bool hit = i < n && idx[i] == e;
-    const uint32_t bal = __ballot_sync(0xffffffffu, hit);
-    if (lane == 0) wcount[warp] = __popc(bal);
-    __syncthreads();
-    int pre = 0, tot = 0;
-    for (int w = 0; w < 32; ++w) {
-      const int c = wcount[w];
-      pre += w < warp ? c : 0;
-      tot += c;
+  const int start = s_start;
+  int at = start;
+  for (int base = 0; base < n; base += 4 * int(blockDim.x)) {
+    const int i0 = base + 4 * tid;
+    bool hit[4];
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      hit[j] = i0 + j < n && idx[i0 + j] == e;
+      c += hit[j] ? 1 : 0;
     }
-    if (hit) {
-      const int r = at + pre + __popc(bal & lt);
-      perm[r] = i;
-      src_row[i] = r;
+    const int incl = warp_incl_scan_i(c, lane);
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    const int ws = wsum[lane];
+    const int wi = warp_incl_scan_i(ws, lane);
+    const int tot = __shfl_sync(0xffffffffu, wi, 31);
+    int r = at + __shfl_sync(0xffffffffu, wi - ws, warp) + incl - c;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (hit[j]) {
+        perm[r] = i0 + j;
+        src_row[i0 + j] = r;
+        ++r;
+      }
     }
     at += tot;
-    __syncthreads();
+    __syncthreads();   // wsum is rewritten next round
+  }
+  if (tid == 0) {
+    offsets[e] = start;
+    if (e == E - 1) offsets[E] = at;
   }
 }
 
@@ -1020,8 +1042,9 @@ biv_status biv_act_quant_fp8(const uint16_t* x, int64_t xs, int rows, int K, uin
   BIV_REQUIRE(rows >= 0 && K > 0 && K % 16 == 0, "act_quant_fp8: K=%d must be a multiple of 16", K);
   if (rows == 0) return BIV_OK;
   BIV_REQUIRE(x && codes && scales, "act_quant_fp8: null pointer");
-  const int64_t warps = int64_t(rows) * ((K + 127) / 128);
-  act_quant_kernel<<<unsigned((warps * 32 + 255) / 256), 256, 0, as_cuda(stream)>>>(
+  BIV_REQUIRE(row_ok(x, xs, 2), "act_quant_fp8: x rows must be 16-byte aligned");
+  const int64_t halves = int64_t(rows) * ((K + 127) / 128);
+  act_quant_kernel<<<unsigned((halves * 16 + 255) / 256), 256, 0, as_cuda(stream)>>>(
       x, xs, rows, K, codes, scales);
   return check_launch("act_quant_fp8");
 }
@@ -1031,10 +1054,11 @@ biv_status biv_silu_mul_quant_fp8(const uint16_t* gu, int64_t gs, int rows, int 
   BIV_REQUIRE(rows >= 0 && I > 0 && I % 16 == 0, "silu_mul_quant_fp8: I=%d must be a multiple of 16",
               I);
   if (rows == 0) return BIV_OK;
-  BIV_REQUIRE(gu && codes && scales && gs >= 2 * int64_t(I), "silu_mul_quant_fp8: bad arguments");
-  const int64_t warps = int64_t(rows) * ((I + 127) / 128);
-  launch_pdl(silu_mul_quant_kernel, unsigned((warps * 32 + 255) / 256), 256, 0, as_cuda(stream), gu,
-             gs, rows, I, codes, scales);
+  BIV_REQUIRE(gu && codes && scales && gs >= 2 * int64_t(I) && row_ok(gu, gs, 2),
+              "silu_mul_quant_fp8: bad arguments (rows must be 16-byte aligned)");
+  const int64_t halves = int64_t(rows) * ((I + 127) / 128);
+  launch_pdl(silu_mul_quant_kernel, unsigned((halves * 16 + 255) / 256), 256, 0, as_cuda(stream),
+             gu, gs, rows, I, codes, scales);
   return check_launch("silu_mul_quant_fp8");
 }
 
@@ -1065,8 +1089,7 @@ biv_status biv_moe_dispatch(const int32_t* idx, int T, int k, int E, int32_t* of
   BIV_REQUIRE(T >= 0 && k > 0 && E > 0 && E <= 4096 && int64_t(T) * k <= (1 << 20),
               "moe_dispatch: bad sizes");
   BIV_REQUIRE(idx && offsets && perm && src_row, "moe_dispatch: null pointer");
-  moe_dispatch_kernel<<<E, 1024, E * sizeof(int), as_cuda(stream)>>>(idx, T * k, E, offsets,
-                                                                    perm, src_row);
+  moe_dispatch_kernel<<<E, 1024, 0, as_cuda(stream)>>>(idx, T * k, E, offsets, perm, src_row);
   return check_launch("moe_dispatch");
 }
 
