@@ -743,30 +743,45 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::THREADS, 1)
 // [N, K/2] (element 2i in the low nibble of byte i) and one e4m3 scale per 16
 // elements [N, K/16], global scale 1.  Each K block of 64 arrives as 4 KB of
 // codes and the 16-byte scale group holding its four scales; converter warps
-// decode it to bf16 (e2m1 x scale is exact in bf16) into the same
-// 128-byte-swizzled K-major tile that TMA writes for the bf16 path, and the
-// MMA runs the identical K schedule.  Every partial, and so every output, has
-// the bits of the bf16 GEMM on the decoded weights; HBM reads 0.5625 bytes
-// per weight instead of 2.
-// Two rings: R raw stages (A box, codes, scales; ~8 KB each, deep, so that
-// enough bytes are in flight) and kFp4Dec decoded bf16 tiles (16 KB each).
-// Warps: 0 = TMA producer, 1 = MMA issuer and TMEM owner, 2..9 = converters
-// (two threads per B row), 10..13 = epilogue (TMEM lane quarters).  A
-// converter looks each code byte (two elements) up in a 256-entry table of
-// bf16 pairs at scale 1 and multiplies the pair by the block scale in bf16
-// (exact: the product has at most 6 significant bits).  The table is held in
-// 32 interleaved copies so that lane L always reads bank L (measured: one
-// shared copy cost about 340 bank conflicts per 64-wide K block).
-constexpr int kFp4CodeBytes = 128 * 32;   // a K block: 128 rows x 64 codes
-constexpr int kFp4SclBytes = 128 * 16;    // a K block: 128 rows x one 16-scale group
-constexpr int kFp4Conv = 8;               // converter warps
+// decode it to bf16 (e2m1 x scale is exact in bf16) straight into TMEM, and
+// the MMA runs with the operands swapped: the decoded weight tile (128 weight
+// rows in the 128 TMEM lanes) is the A operand, the few activation rows (the
+// TMA box in shared memory) the B operand, N = the box's rows.  D'[n][m] is
+// the bf16 path's D[m][n]: tcgen05 is operand-symmetric (measured on GB300:
+// every element of C1 = A.B^T equals C2^T = (B.A^T)^T), and the K steps run
+// in the same order, so every partial, and so every output, has the bits of
+// the bf16 GEMM on the decoded weights.  HBM reads 0.5625 bytes per weight
+// instead of 2.
+// A ring of R raw stages and kFp4Dec decoded tiles in TMEM (32 columns
+// each).  A raw stage holds kFp4Sub = 4 K blocks: the codes as one box of
+// 128-byte rows, the two 16-byte scale groups around them as one box of
+// 32-byte rows, the activations as one 3-D box of four 64-wide panels.  TMA
+// moves a few box rows per SM clock whatever their width (measured on
+// GB300), so one K block per stage, in 32- and 16-byte rows, ran at about a
+// fifth of the HBM rate.
+// Warps: 0 = TMA producer, 1 = MMA issuer and TMEM owner, 2..17 = converters
+// in four groups of four (lane quarter = warp % 4): group g decodes the K
+// blocks whose running index is g mod 4 into decoded tile g, each thread the
+// 64 elements of one weight row as 32 columns, so four K blocks are decoded
+// at once (one group at a time left the MMA waiting on the store latency);
+// 18..21 = epilogue (TMEM lane quarters: one weight row a thread, every
+// activation row of the box).  A converter looks each code byte (two elements) up in a
+// 256-entry table of bf16 pairs at scale 1 and multiplies the pair by the
+// block scale in bf16 (exact: the product has at most 6 significant bits).
+// The table is held in 32 interleaved copies so that lane L always reads
+// bank L (one shared copy cost about 340 bank conflicts per K block).
+constexpr int kFp4Sub = 4;                // K blocks per raw stage
+constexpr int kFp4CodeBytes = 128 * 128;  // a stage: 128 rows x 256 codes
+constexpr int kFp4SclBytes = 128 * 32;    // a stage: 128 rows x two 16-scale groups (at most)
+constexpr int kFp4Conv = 16;              // converter warps: four groups of four
 constexpr int kFp4Threads = 64 + 32 * kFp4Conv + 128;
-constexpr int kFp4Dec = 3;                // decoded bf16 tiles
+constexpr int kFp4Dec = 4;                // decoded tiles in TMEM, one per converter group
 constexpr int kFp4MaxRaw = 32;            // raw stages at most
+constexpr uint32_t kFp4DecCol = 0;        // TMEM: decoded tiles at columns [0, 128)
+constexpr uint32_t kFp4AccCol = 128;      // two accumulators of <= 64 columns from 128
 
 size_t fp4_smem_bytes(int raw, int m_box) {
-  return 1024 + size_t(kFp4Dec) * 128 * 128 +
-         size_t(raw) * (m_box * 128 + kFp4CodeBytes + kFp4SclBytes) + (128 - m_box) * 128 +
+  return 1024 + size_t(raw) * (kFp4Sub * m_box * 128 + kFp4CodeBytes + kFp4SclBytes) +
          (2 * kFp4MaxRaw + 2 * kFp4Dec + 4) * 8 + 16 + 256 * 32 * 4;
 }
 
@@ -779,21 +794,20 @@ __global__ void __launch_bounds__(kFp4Threads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmC,
                       const __grid_constant__ CUtensorMap tmS, const GemmArgs p) {
-  constexpr int BN = 128;
-  constexpr int B_TILE = BN * 128;
-  constexpr uint32_t kTmemCols = 256;   // two 128-column accumulators
+  constexpr int BN = 128;                 // weight rows per tile (the MMA's M)
+  constexpr uint32_t kTmemCols = 256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int R = p.stages;                                        // raw stages
-  const int a_stage = p.m_box * 128;
-  uint8_t* sB = smem;                                            // [kFp4Dec] decoded tiles
-  uint8_t* sA = sB + kFp4Dec * B_TILE;                           // [R] A boxes (+ pad)
-  uint8_t* sCode = sA + R * a_stage + (128 - p.m_box) * 128;     // [R] raw codes
+  const int a_blk = p.m_box * 128, a_stage = kFp4Sub * a_blk;
+  const int sw = min(32, p.K / 16);                              // scale bytes a row per stage
+  uint8_t* sA = smem;                                            // [R][kFp4Sub] activation boxes
+  uint8_t* sCode = sA + R * a_stage;                             // [R] raw codes
   uint8_t* sScl = sCode + R * kFp4CodeBytes;                     // [R] raw scale groups
   uint64_t* bars = reinterpret_cast<uint64_t*>(sScl + R * kFp4SclBytes);
-  // full[r]: A, codes and scales of raw stage r landed.  empty[r]: the MMA
-  // (A) and every converter warp (codes) are done with it.  dfull[b] /
-  // dempty[b]: decoded tile b written / read by the MMA.
+  // full[r]: activations, codes and scales of raw stage r landed.  empty[r]:
+  // the MMA (activations) and every converter warp (codes) are done with it.
+  // dfull[b] / dempty[b]: decoded tile b written / read by the MMA.
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kFp4MaxRaw);
   const uint32_t dfull0 = smem_u32(bars + 2 * kFp4MaxRaw);
   const uint32_t dempty0 = smem_u32(bars + 2 * kFp4MaxRaw + kFp4Dec);
@@ -821,7 +835,7 @@ __global__ void __launch_bounds__(kFp4Threads, 1)
       mbar_init(empty0 + 8 * r, 1 + kFp4Conv);
     }
     for (int b = 0; b < kFp4Dec; ++b) {
-      mbar_init(dfull0 + 8 * b, kFp4Conv);
+      mbar_init(dfull0 + 8 * b, 4);        // the four warps of converter group b
       mbar_init(dempty0 + 8 * b, 1);
     }
     for (int j = 0; j < 2; ++j) {
@@ -847,145 +861,165 @@ __global__ void __launch_bounds__(kFp4Threads, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmC);
       tma_prefetch_desc(&tmS);
-      const uint32_t tx = uint32_t(a_stage + kFp4CodeBytes + kFp4SclBytes);
-      auto load_b = [&](int r, int kb, int n0) {
+      // boxes past the end of K fill zeros and count their bytes
+      const uint32_t tx = uint32_t(a_stage + kFp4CodeBytes + 128 * sw);
+      auto load_b = [&](int r, int kb0, int n0) {
         mbar_expect_tx(full0 + 8 * r, tx);
-        tma_load_2d(smem_u32(sCode + r * kFp4CodeBytes), &tmC, full0 + 8 * r, kb * 32, n0);
-        tma_load_2d(smem_u32(sScl + r * kFp4SclBytes), &tmS, full0 + 8 * r, (kb >> 2) * 16, n0);
+        tma_load_2d(smem_u32(sCode + r * kFp4CodeBytes), &tmC, full0 + 8 * r, kb0 * 32, n0);
+        tma_load_2d(smem_u32(sScl + r * kFp4SclBytes), &tmS, full0 + 8 * r, (kb0 >> 2) * 16, n0);
       };
       // weights of the first stages before waiting for the previous kernel
       int pre = 0;
       if (blockIdx.x < items) {
         const int i = blockIdx.x, t = i / chunks, c = i % chunks;
-        const int kb0 = c * p.kc_blocks;
-        pre = min(R, min(KB, kb0 + p.kc_blocks) - kb0);
-        for (int r = 0; r < pre; ++r) load_b(r, kb0 + r, tile_n0(t));
+        const int kb_lo = c * p.kc_blocks, kb_hi = min(KB, kb_lo + p.kc_blocks);
+        for (int kb0 = kb_lo; kb0 < kb_hi && pre < R; kb0 += kFp4Sub, ++pre)
+          load_b(pre, kb0, tile_n0(t));
       }
       pdl_wait();
       bool ok = true;
       for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
         const int t = i / chunks, c = i % chunks, m0 = tile_m0(t), n0 = tile_n0(t);
         const int kb1 = min(KB, (c + 1) * p.kc_blocks);
-        for (int kb = c * p.kc_blocks; kb < kb1; ++kb) {
+        for (int kb0 = c * p.kc_blocks; kb0 < kb1; kb0 += kFp4Sub) {
           const int r = issued % R;
           if (issued >= pre) {
             if (issued >= R && !mbar_wait(empty0 + 8 * r, ((issued / R) - 1) & 1, p.err)) {
               ok = false;
               break;
             }
-            load_b(r, kb, n0);
+            load_b(r, kb0, n0);
           }
-          tma_load_2d(smem_u32(sA + r * a_stage), &tmA, full0 + 8 * r, kb * 64, m0);
+          tma_load_3d(smem_u32(sA + r * a_stage), &tmA, full0 + 8 * r, 0, m0, kb0);
           ++issued;
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_mma(1u, BM, BN);
-      int it = 0, j = 0;
+      // D'[128 weight rows x m_box activation rows]: A from TMEM, B K-major
+      const uint32_t idesc = idesc_mma(1u, BN, p.m_box);
+      int it = 0, st = 0, j = 0;   // K blocks, raw stages, work items
       bool ok = true;
       for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++j) {
         const int c = i % chunks, tb = j & 1;
         if (j >= 2 && !mbar_wait(tempty0 + 8 * tb, ((j >> 1) - 1) & 1, p.err)) break;
         tc_fence_after();
-        const uint32_t dt = tmem + tb * BN;
-        const int kb0 = c * p.kc_blocks, kb1 = min(KB, kb0 + p.kc_blocks);
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int r = it % R, b = it % kFp4Dec;
-          if (!mbar_wait(full0 + 8 * r, (it / R) & 1, p.err) ||
-              !mbar_wait(dfull0 + 8 * b, (it / kFp4Dec) & 1, p.err)) {
+        const uint32_t dt = tmem + kFp4AccCol + tb * 64;
+        const int kb_lo = c * p.kc_blocks, kb1 = min(KB, kb_lo + p.kc_blocks);
+        for (int kb0 = kb_lo; kb0 < kb1 && ok; kb0 += kFp4Sub, ++st) {
+          const int r = st % R;
+          if (!mbar_wait(full0 + 8 * r, (st / R) & 1, p.err)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + r * a_stage);
-          const uint32_t b0 = smem_u32(sB + b * B_TILE);
+          for (int kb = kb0; kb < min(kb1, kb0 + kFp4Sub); ++kb, ++it) {
+            const int b = it % kFp4Dec;
+            if (!mbar_wait(dfull0 + 8 * b, (it / kFp4Dec) & 1, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + r * a_stage + (kb - kb0) * a_blk);
+            const uint32_t w0 = tmem + kFp4DecCol + b * 32;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_f16(dt, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
-                     (kb != kb0 || kk != 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_f16_ts(dt, w0 + kk * 8, sdesc_k_sw128(a0 + kk * 32), idesc,
+                          (kb != kb_lo || kk != 0) ? 1u : 0u);
+            umma_commit(dempty0 + 8 * b);
+          }
           umma_commit(empty0 + 8 * r);
-          umma_commit(dempty0 + 8 * b);
         }
         if (ok) umma_commit(tfull0 + 8 * tb);
       }
     }
   } else if (warp < 2 + kFp4Conv) {
     // ---------------------------------------------------------- decode --
-    // two threads per B row: 16 bytes of codes (32 elements) and two scales
-    // of this K block -> half of one 128-byte swizzled bf16 row
-    const int rw = (threadIdx.x - 64) >> 1, hh = (threadIdx.x - 64) & 1;
-    int it = 0;
+    // thread: weight row 32 q + lane of the tile; group grp: the K blocks
+    // whose running index is grp mod 4, into decoded tile grp
+    const int q = warp & 3, grp = (warp - 2) >> 2;
+    const int rw = q * 32 + lane;
+    const uint32_t dst = tmem + (uint32_t(q * 32) << 16) + kFp4DecCol + grp * 32;
+    int it = 0, st = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
       const int c = i % chunks;
       const int kb1 = min(KB, (c + 1) * p.kc_blocks);
-      for (int kb = c * p.kc_blocks; kb < kb1; ++kb, ++it) {
-        const int r = it % R, b = it % kFp4Dec;
-        bool w_ok = mbar_wait(full0 + 8 * r, (it / R) & 1, p.err);
-        if (it >= kFp4Dec)
-          w_ok = w_ok && mbar_wait(dempty0 + 8 * b, ((it / kFp4Dec) - 1) & 1, p.err);
-        if (!__all_sync(0xffffffffu, w_ok)) {
+      for (int kb0 = c * p.kc_blocks; kb0 < kb1 && ok; kb0 += kFp4Sub, ++st) {
+        const int r = st % R;
+        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * r, (st / R) & 1, p.err))) {
           ok = false;
           break;
         }
-        const uint4 cv =
-            *reinterpret_cast<const uint4*>(sCode + r * kFp4CodeBytes + rw * 32 + hh * 16);
-        const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(sScl + r * kFp4SclBytes + rw * 16 +
-                                                                  (kb & 3) * 4 + hh * 2);
+        for (int kb = kb0; kb < min(kb1, kb0 + kFp4Sub); ++kb, ++it) {
+          if (it % kFp4Dec != grp) continue;
+          if (it >= kFp4Dec &&
+              !__all_sync(0xffffffffu, mbar_wait(dempty0 + 8 * grp, ((it / kFp4Dec) - 1) & 1, p.err))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // codes land 128-byte swizzled (16-byte chunk j of row r at j ^ (r % 8)):
+          // a warp's 32 rows then spread over every bank (unswizzled, all 32
+          // lanes of a 16-byte load hit the same four banks)
+          const uint8_t* crow = sCode + r * kFp4CodeBytes + rw * 128;
+          const int j0 = 2 * (kb - kb0), sx = rw & 7;
+          const uint4 c0 = *reinterpret_cast<const uint4*>(crow + ((j0 ^ sx) << 4));
+          const uint4 c1 = *reinterpret_cast<const uint4*>(crow + (((j0 + 1) ^ sx) << 4));
+          // the stage's scale row starts at group (kb0 >> 2): block kb's four
+          // scales sit (kb - 4 (kb0 >> 2)) * 4 bytes in
+          const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(
+              sScl + r * kFp4SclBytes + rw * sw + (kb - 4 * (kb0 >> 2)) * 4);
+          const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          const uint32_t* lt = lut + lane;        // this lane's copy: bank = lane
+          uint32_t o[32];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {           // 16 elements (two words) per e4m3 scale
+            const float sf = __half2float(__ushort_as_half(
+                __nv_cvt_fp8_to_halfraw(__nv_fp8_storage_t((sc4 >> (8 * g)) & 0xFFu), __NV_E4M3).x));
+            const __nv_bfloat162 s2 = __floats2bfloat162_rn(sf, sf);   // e4m3 is exact in bf16
+#pragma unroll
+            for (int wi = 2 * g; wi < 2 * g + 2; ++wi)   // 8 elements (4 columns) per word
+#pragma unroll
+              for (int by = 0; by < 4; ++by)
+                o[wi * 4 + by] = bf16x2_mul(lt[((w[wi] >> (8 * by)) & 0xFFu) << 5], s2);
+          }
+          tmem_st32(dst, o);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dfull0 + 8 * grp);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * r);   // this warp is done with raw stage r
-        uint8_t* dst = sB + b * B_TILE + (rw >> 3) * 1024 + (rw & 7) * 128;
-        const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {              // 16 elements per e4m3 scale
-          const float sf = __half2float(__ushort_as_half(
-              __nv_cvt_fp8_to_halfraw(__nv_fp8_storage_t((sc2 >> (8 * g)) & 0xFFu), __NV_E4M3).x));
-          const __nv_bfloat162 s2 = __floats2bfloat162_rn(sf, sf);   // e4m3 is exact in bf16
-#pragma unroll
-          for (int q = 2 * g; q < 2 * g + 2; ++q) {  // 8 elements (one 16-byte chunk) per word
-            const uint32_t* lt = lut + lane;      // this lane's copy: bank = lane
-            const uint4 v = make_uint4(bf16x2_mul(lt[(w[q] & 0xFFu) << 5], s2),
-                                       bf16x2_mul(lt[((w[q] >> 8) & 0xFFu) << 5], s2),
-                                       bf16x2_mul(lt[((w[q] >> 16) & 0xFFu) << 5], s2),
-                                       bf16x2_mul(lt[(w[q] >> 24) << 5], s2));
-            const int chunk = hh * 4 + q;
-            *reinterpret_cast<uint4*>(dst + ((chunk ^ (rw & 7)) << 4)) = v;
-          }
-        }
-        fence_proxy_async();   // the generic writes above feed the tensor core
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dfull0 + 8 * b);
       }
     }
   } else {
     // -------------------------------------------------------- epilogue --
+    // thread: weight row n0 + 32 q + lane; D' columns = activation rows
     const int q = warp & 3;
     int j = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++j) {
       const int t = i / chunks, c = i % chunks, m0 = tile_m0(t), n0 = tile_n0(t);
-      const int row = m0 + q * 32 + lane;
+      const int n = n0 + q * 32 + lane;
       const int tb = j & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * tb, (j >> 1) & 1, p.err))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t ta = tmem + tb * BN + (uint32_t(q * 32) << 16);
-      float* dst = row < p.M ? p.ws + (int64_t(c) * p.M + row) * p.ldp + n0 : nullptr;
-#pragma unroll
-      for (int g = 0; g < BN / 32; ++g) {
-        uint32_t v[32];
-        tmem_ld32(ta + g * 32, v);
+      const uint32_t ta = tmem + kFp4AccCol + tb * 64 + (uint32_t(q * 32) << 16);
+      float* dst = p.ws + (int64_t(c) * p.M + m0) * p.ldp + n;
+      const int rows = min(p.m_box, p.M - m0);
+      for (int g0 = 0; g0 < p.m_box; g0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(ta + g0, v);
         tmem_ld_wait();
-        if (dst) {
+        if (n < p.N) {
 #pragma unroll
-          for (int x = 0; x < 32; x += 4)
-            *reinterpret_cast<float4*>(dst + g * 32 + x) =
-                make_float4(__uint_as_float(v[x]), __uint_as_float(v[x + 1]),
-                            __uint_as_float(v[x + 2]), __uint_as_float(v[x + 3]));
+          for (int x = 0; x < 16; ++x)
+            if (g0 + x < rows) dst[int64_t(g0 + x) * p.ldp] = __uint_as_float(v[x]);
         }
       }
       tc_fence_before();
@@ -1041,15 +1075,17 @@ bool make_map2k(CUtensorMap* m, const void* base, int64_t K, int64_t rows, int64
 }
 
 // A K-major operand [rows, K] as a 3-D tensor {panel, rows, K / panel}
-// (elements): a box {panel, box_rows, 2} brings two consecutive K blocks,
-// landing as [block][row][panel] with 128-byte swizzling.  K % panel == 0.
+// (elements): a box {panel, box_rows, panels} brings that many consecutive K
+// blocks, landing as [block][row][panel] with 128-byte swizzling.
+// K % panel == 0.
 bool make_map_panels(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
-                     int64_t K, int64_t rows, int64_t ld, int panel, int box_rows) {
+                     int64_t K, int64_t rows, int64_t ld, int panel, int box_rows,
+                     int panels = 2) {
   auto fn = tensor_map_encoder();
   if (!fn || K % panel != 0) return false;
   cuuint64_t dims[3] = {cuuint64_t(panel), cuuint64_t(rows), cuuint64_t(K / panel)};
   cuuint64_t strides[2] = {cuuint64_t(ld * elem_bytes), cuuint64_t(panel * elem_bytes)};
-  cuuint32_t box[3] = {cuuint32_t(panel), cuuint32_t(box_rows), 2};
+  cuuint32_t box[3] = {cuuint32_t(panel), cuuint32_t(box_rows), cuuint32_t(panels)};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1324,7 +1360,10 @@ Fp4Plan plan_nvfp4(const biv_gemm_desc& d) {
   // the CTA (wide N, e.g. an LM head): partial and in-CTA fold give the same
   // bits, and only the native kernel reads 4-bit weights.
   const bool stream_rows = d.M <= kPartialRows && d.mode == BIV_MODE_INVARIANT;
-  f.native = d.K % 256 == 0 && ((f.p.partial && f.p.bn == 128) || stream_rows);
+  // At most 64 activation rows: the kernel's two accumulators (the box's rows
+  // as TMEM columns) and three decoded 32-column tiles share 256 columns.
+  f.native = d.K % 256 == 0 && d.M <= kPartialRows &&
+             ((f.p.partial && f.p.bn == 128) || stream_rows);
   if (f.native && !(f.p.partial && f.p.bn == 128)) {
     const int64_t tiles_m = (d.M + BM - 1) / BM;
     f.p.partial = true;
@@ -1334,7 +1373,7 @@ Fp4Plan plan_nvfp4(const biv_gemm_desc& d) {
     f.p.ws_bytes = size_t(f.p.chunks) * d.M * f.p.ldp * sizeof(float);
   }
   if (f.native) {
-    const size_t per = size_t(f.p.m_box) * 128 + kFp4CodeBytes + kFp4SclBytes;
+    const size_t per = size_t(kFp4Sub) * f.p.m_box * 128 + kFp4CodeBytes + kFp4SclBytes;
     f.stages = int(std::min<size_t>(kFp4MaxRaw, (kSmemBudget - fp4_smem_bytes(0, f.p.m_box)) / per));
     f.ws_bytes = f.p.ws_bytes;
   } else {
@@ -1405,9 +1444,11 @@ biv_status biv_gemm_nvfp4(const uint16_t* A, int64_t lda, const uint8_t* codes,
   }
   const Plan& p = f.p;
   CUtensorMap ta, tc, ts;
-  if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, p.m_box) ||
-      !make_map(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, codes, K / 2, N, K / 2, 32, 128, false) ||
-      !make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, scales, K / 16, N, K / 16, 16, 128, false))
+  if (!make_map_panels(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, p.m_box,
+                       kFp4Sub) ||
+      !make_map(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, codes, K / 2, N, K / 2, 128, 128, true) ||
+      !make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, scales, K / 16, N, K / 16,
+                std::min(32, K / 16), 128, false))
     return set_error(BIV_ERR_CUDA, "gemm_nvfp4: tensor map encoding failed");
   static bool attr = false;
   if (!attr) {
