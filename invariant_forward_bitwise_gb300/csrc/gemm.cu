@@ -160,6 +160,7 @@ struct GemmArgs {
   float2* lse;
   float* zt;
   int ngroups;
+  int ws_v8;                   // partial mode: the workspace is 32-byte aligned
   int* err;
 };
 
@@ -189,6 +190,13 @@ struct GemmSmem {
            (2 * kMaxStages + 4) * 8 + 16 + (staging ? kStagingBytes : 0);
   }
 };
+
+// 256-bit store of 8 FP32 values (32-byte aligned address)
+__device__ __forceinline__ void st_global_v8(float* dst, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
 
 // PARTIAL: the partial-mode instantiation.  Its epilogue keeps no running
 // sum, so it is compiled for half the register file; with PDL the next
@@ -370,7 +378,13 @@ __global__ void __launch_bounds__(kGemmThreads, PARTIAL ? 2 : 1)
             uint32_t v[32];
             tmem_ld32(ta + g * 32, v);
             tmem_ld_wait();
-            if (dst) {
+            if (dst && p.ws_v8) {
+              // whole 32-byte sectors per store: half-sector stores slowed
+              // the next work item's loads more (measured with a
+              // clock-stamped build)
+#pragma unroll
+              for (int x = 0; x < 32; x += 8) st_global_v8(dst + g * 32 + x, v + x);
+            } else if (dst) {
 #pragma unroll
               for (int x = 0; x < 32; x += 4)
                 *reinterpret_cast<float4*>(dst + g * 32 + x) =
@@ -1244,6 +1258,7 @@ biv_status launch_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const biv_g
   a.stages = pl.stages;
   a.partial = pl.partial ? 1 : 0;
   a.ws = pl.partial ? static_cast<float*>(ws) : nullptr;
+  a.ws_v8 = pl.partial && (reinterpret_cast<uintptr_t>(ws) & 31) == 0;
   a.ldp = pl.ldp;
   a.vec_ok = aligned16(d.C) && (d.ldc * eb) % 16 == 0;
   a.n_fastest = !pl.partial && d.N <= d.M;

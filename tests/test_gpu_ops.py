@@ -655,6 +655,28 @@ def test_two_block_stages_change_no_bit(B, monkeypatch, M, N, K, fold):
     assert rel_err(outs[0].view(np.float32).reshape(M, N)[rows], ref) < REL
 
 
+def test_partials_workspace_alignment_changes_no_bit(B, monkeypatch):
+    """Partial mode stores its FP32 partials 32 bytes at a time when the
+    workspace is 32-byte aligned and 16 bytes at a time otherwise: the
+    outputs have the same bits either way."""
+    g = synth.rng(77)
+    M, N, K = 64, 4096, 2048
+    a, b = rnd_bf16(g, M, K), rnd_bf16(g, N, K, std=0.05)
+    ad, bd = dev(a), dev(b)
+    monkeypatch.setenv("BIV_GEMM_FOLD", "partial")
+    d = B.gemm_desc(ad, bd, torch.empty(M, N, dtype=torch.float32, device="cuda"))
+    need = B.biv_gemm_workspace(d)
+    assert need > 0
+    big = torch.empty(need + 64, dtype=torch.uint8, device="cuda")
+    assert big.data_ptr() % 32 == 0
+    outs = []
+    for off in (0, 16):
+        c = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        B.biv_gemm(B.gemm_desc(ad, bd, c), big[off:off + need])
+        outs.append(bits(c))
+    assert np.array_equal(outs[0], outs[1])
+
+
 # ------------------------------------------------- fused GEMM consumers --
 def _deferred_gemm(B, ad, bd, M, N, ws):
     """GEMM whose fold is left to the consumer; returns the partials (chunks
