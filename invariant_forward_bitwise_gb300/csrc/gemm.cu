@@ -51,7 +51,15 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Store 32 consecutive FP32 accumulator columns of one row.
+// 256-bit store of eight 32-bit words (32-byte aligned address)
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// Store 32 consecutive FP32 accumulator columns of one row.  bf16 rows whose
+// 64 bytes are 32-byte aligned go out as two whole-sector stores.
 template <bool F32OUT>
 __device__ __forceinline__ void store_row32(void* C, int64_t ldc, int row, int n, int N,
                                             const uint32_t (&r)[32], bool vec_ok) {
@@ -70,7 +78,16 @@ __device__ __forceinline__ void store_row32(void* C, int64_t ldc, int row, int n
     }
   } else {
     uint16_t* dst = static_cast<uint16_t*>(C) + int64_t(row) * ldc + n;
-    if (vec_ok && n + 32 <= N) {
+    if (vec_ok && n + 32 <= N && (reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+          w[x] = pack_bf2(__uint_as_float(r[16 * h + 2 * x]), __uint_as_float(r[16 * h + 2 * x + 1]));
+        st_global_v8(dst + 16 * h, w);
+      }
+    } else if (vec_ok && n + 32 <= N) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         uint4 v;
@@ -190,13 +207,6 @@ struct GemmSmem {
            (2 * kMaxStages + 4) * 8 + 16 + (staging ? kStagingBytes : 0);
   }
 };
-
-// 256-bit store of 8 FP32 values (32-byte aligned address)
-__device__ __forceinline__ void st_global_v8(float* dst, const uint32_t* v) {
-  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
-               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
 
 // PARTIAL: the partial-mode instantiation.  Its epilogue keeps no running
 // sum, so it is compiled for half the register file; with PDL the next
