@@ -1002,25 +1002,35 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         if (!mine) continue;
         const int d0 = hf * DH + c * 32;
         if (ns == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(a.out + int64_t(row) * a.out_stride +
-                                                int64_t(head) * D + d0);
+          uint16_t* orow = a.out + int64_t(row) * a.out_stride + int64_t(head) * D + d0;
+          uint32_t pk[16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t pk[4];
+          for (int e = 0; e < 16; ++e) {
+            const float o0 = __uint_as_float(r[2 * e]) * inv_l + 0.0f;
+            const float o1 = __uint_as_float(r[2 * e + 1]) * inv_l + 0.0f;
+            pk[e] = pack_bf2(o0, o1);
+          }
+          if ((reinterpret_cast<uintptr_t>(orow) & 31) == 0) {   // whole sectors
+            st_global_v8(orow, pk);
+            st_global_v8(orow + 16, pk + 8);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float o0 = __uint_as_float(r[8 * q + 2 * e]) * inv_l + 0.0f;
-              const float o1 = __uint_as_float(r[8 * q + 2 * e + 1]) * inv_l + 0.0f;
-              pk[e] = pack_bf2(o0, o1);
-            }
-            dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
           }
         } else {
-          float4* wo = reinterpret_cast<float4*>(a.ws_o + slot * D + d0);
+          float* wrow = a.ws_o + slot * D + d0;
+          if ((reinterpret_cast<uintptr_t>(wrow) & 31) == 0) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            wo[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            for (int q = 0; q < 4; ++q) st_global_v8(wrow + 8 * q, r + 8 * q);
+          } else {
+            float4* wo = reinterpret_cast<float4*>(wrow);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              wo[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                  __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+          }
         }
       }
       if (mine && ns > 1 && hf == 0) {

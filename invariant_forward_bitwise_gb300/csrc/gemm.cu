@@ -51,13 +51,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// 256-bit store of eight 32-bit words (32-byte aligned address)
-__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* v) {
-  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
-               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-
 // Store 32 consecutive FP32 accumulator columns of one row.  bf16 rows whose
 // 64 bytes are 32-byte aligned go out as two whole-sector stores.
 template <bool F32OUT>
