@@ -398,11 +398,11 @@ class KernelTimer:
 
     # DRAM bytes per algorithmic byte of a decode step, from ncu captures of one
     # eager step with every sequence at position 700 (kernel_bench decode_step):
-    # 9.335 GB against 8.59 GB at batch 64, 25.78 GB against 23.99 GB at batch
+    # 9.337 GB against 8.59 GB at batch 64, 25.77 GB against 23.99 GB at batch
     # 256; the excess is the decode GEMMs' FP32 chunk partials.  The bench's
     # steps mix batch sizes and contexts, so their traffic is this ratio times
     # their own algorithmic bytes.
-    DECODE_DRAM_RATIO = (9.335 / 8.59 + 25.78 / 23.99) / 2
+    DECODE_DRAM_RATIO = (9.337 / 8.59 + 25.77 / 23.99) / 2
 
     def entry(self, k, a, peaks):
         if a["unit"] == "flop":
