@@ -123,6 +123,14 @@ __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
   uint4* rr = r ? reinterpret_cast<uint4*>(r + int64_t(row) * rs) : nullptr;
   float v[CPT][8];
   float ss = 0.f;
+  // the weights go out with the row's loads, not after the reduction
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  uint4 wq[CPT];
+#pragma unroll
+  for (int i = 0; i < CPT; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    wq[i] = c < chunks ? __ldg(wr + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
 #pragma unroll
   for (int i = 0; i < CPT; ++i) {
     const int c = threadIdx.x + i * kNormThreads;
@@ -149,14 +157,13 @@ __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
 #pragma unroll
   for (int i = 0; i < kNormThreads / 32; ++i) tot += warp_ss[i];
   const float inv = 1.0f / sqrtf(tot / float(d) + eps);
-  const uint4* wr = reinterpret_cast<const uint4*>(w);
   uint4* yr = reinterpret_cast<uint4*>(y + int64_t(row) * ys);
 #pragma unroll
   for (int i = 0; i < CPT; ++i) {
     const int c = threadIdx.x + i * kNormThreads;
     if (c < chunks) {
       float wv[8], o[8];
-      unpack8(__ldg(wr + c), wv);
+      unpack8(wq[i], wv);
 #pragma unroll
       for (int j = 0; j < 8; ++j) o[j] = (v[i][j] * inv) * wv[j];
       yr[c] = pack8(o);
@@ -375,6 +382,22 @@ __global__ void qkv_finalize_kernel(uint16_t* __restrict__ qkv, int64_t rs, cons
   const int kind = h < Hq ? 0 : (h < Hq + Hkv ? 1 : 2);  // q, k, v
   uint16_t* v = qkv + int64_t(t) * rs + int64_t(h) * D;
   const int half = D / 2;
+  // loads that do not depend on the values go out first, so that their
+  // latencies overlap the partials' instead of following them
+  const int p_in = kind < 2 ? pos[t] : 0;
+  const int64_t sl = kind > 0 ? slot[t] : -1;
+  const uint16_t* wn = kind == 0 ? qw : (kind == 1 ? kw : nullptr);
+  float wa[2] = {0.f, 0.f}, wb[2] = {0.f, 0.f};
+  if (wn) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int j = lane + 32 * i;
+      if (j < half) {
+        wa[i] = bf2f(wn[j]);
+        wb[i] = bf2f(wn[j + half]);
+      }
+    }
+  }
   float a[2], b[2];
   uint16_t oa[2], ob[2];
   if (!PARTIAL) {
@@ -424,8 +447,7 @@ __global__ void qkv_finalize_kernel(uint16_t* __restrict__ qkv, int64_t rs, cons
     ob[i] = f2bf(b[i]);
   }
   if (kind < 2) {
-    const uint16_t* wn = kind == 0 ? qw : kw;
-    int p = pos[t];
+    int p = p_in;
     if (p < 0 || p >= max_pos) {
       if (lane == 0) raise_error(err, kErrBadIndex);
       p = 0;
@@ -445,8 +467,8 @@ __global__ void qkv_finalize_kernel(uint16_t* __restrict__ qkv, int64_t rs, cons
       for (int i = 0; i < 2; ++i) {
         const int j = lane + 32 * i;
         if (j < half) {
-          a[i] = bf2f(f2bf((a[i] * inv) * bf2f(wn[j])));
-          b[i] = bf2f(f2bf((b[i] * inv) * bf2f(wn[j + half])));
+          a[i] = bf2f(f2bf((a[i] * inv) * wa[i]));
+          b[i] = bf2f(f2bf((b[i] * inv) * wb[i]));
         }
       }
     }
@@ -472,7 +494,6 @@ __global__ void qkv_finalize_kernel(uint16_t* __restrict__ qkv, int64_t rs, cons
     }
   }
   if (kind == 0) return;
-  const int64_t sl = slot[t];
   if (sl < 0) return;
   const int hk = h - Hq - (kind == 2 ? Hkv : 0);
   const int64_t base = (sl * Hkv + hk) * D;
