@@ -86,6 +86,12 @@ class StepSpec:
     max_ctx: int            # bound on row position + 1
     T_lm: int               # rows that produce a logprob
     attn_flops: float = 0.0  # algorithmic attention FLOPs of the step (4 * sum(ctx) * Hq * D)
+    # a step that mixes prefill blocks with single-vector (decode) blocks holds
+    # the multi-row blocks first: the first n_multi blocks (max_rows_per_block
+    # rows at most) and the rest (max_rows_single at most) go to attention as
+    # two calls, so that decode rows run the decode-shaped CTA
+    n_multi: int = 0
+    max_rows_single: int = 1
 
 
 class DenseModel:
@@ -166,16 +172,29 @@ class DenseModel:
         else:
             biv.biv_add_rmsnorm(x[:T], r, w, y, eps, stream=st)
 
-    def _attn_desc(self, kv: PagedKV, layer: int, spec: StepSpec, qblocks=None):
+    def _attn_descs(self, kv: PagedKV, layer: int, spec: StepSpec, qblocks=None):
+        """Attention call(s) of a layer: one, or two when the step mixes
+        prefill blocks with decode blocks (see StepSpec)."""
+        qb = self.qblocks if qblocks is None else qblocks
+        if 0 < spec.n_multi < spec.nqblocks:
+            return [self._attn_desc(kv, layer, spec, qb.data_ptr(), spec.n_multi,
+                                    spec.max_rows_per_block),
+                    self._attn_desc(kv, layer, spec, qb.data_ptr() + 8 * spec.n_multi,
+                                    spec.nqblocks - spec.n_multi, spec.max_rows_single)]
+        return [self._attn_desc(kv, layer, spec, qb.data_ptr(), spec.nqblocks,
+                                spec.max_rows_per_block)]
+
+    def _attn_desc(self, kv: PagedKV, layer: int, spec: StepSpec, qblocks_ptr: int, nqblocks: int,
+                   max_rows: int):
         cfg = self.cfg
         d = biv.AttnDesc()
         d.q, d.q_stride = self.qkv.data_ptr(), self.qkv.stride(0)
         d.out, d.out_stride = self.o.data_ptr(), self.o.stride(0)
         d.T, d.Hq, d.Hkv, d.D = spec.T, cfg.q_heads, cfg.kv_heads, cfg.head_dim
         d.row_seq, d.row_pos = self.row_seq.data_ptr(), self.row_pos.data_ptr()
-        d.qblocks = (self.qblocks if qblocks is None else qblocks).data_ptr()
-        d.nqblocks = spec.nqblocks
-        d.max_rows_per_block = spec.max_rows_per_block
+        d.qblocks = qblocks_ptr
+        d.nqblocks = nqblocks
+        d.max_rows_per_block = max_rows
         d.kv_dtype = biv.E4M3 if kv.fp8 else biv.BF16
         d.k_cache, d.v_cache = kv.k[layer].data_ptr(), kv.v[layer].data_ptr()
         if kv.fp8:
@@ -193,7 +212,8 @@ class DenseModel:
         need, gneed = 16, 256
         cfg = self.cfg
         for s in specs:
-            need = max(need, biv.biv_attention_workspace(self._attn_desc(kv, 0, s)))
+            for ad in self._attn_descs(kv, 0, s):
+                need = max(need, biv.biv_attention_workspace(ad))
             for (N, K) in [(cfg.qkv_width, cfg.hidden), (cfg.hidden, cfg.q_heads * cfg.head_dim),
                            (2 * cfg.intermediate, cfg.hidden), (cfg.hidden, cfg.intermediate)]:
                 d = biv.GemmDesc()
@@ -242,11 +262,13 @@ class DenseModel:
                                  self.row_pos, eps, self.slot, biv.E4M3 if kv.fp8 else biv.BF16,
                                  kv.k[l], kv.v[l], kv.ks[l] if kv.fp8 else None,
                                  kv.vs[l] if kv.fp8 else None, partials=qp, stream=st)
-            ad = self._attn_desc(kv, l, spec, qblocks)
-            need = biv.biv_attention_workspace(ad)
             t = self._timer()
             tok = t.bracket("attention_prefill", spec.attn_flops, "flop") if t and spec.attn_flops else None
-            biv.biv_attention(ad, self.ws if need else None, stream=st)
+            attn_launches = 0
+            for ad in self._attn_descs(kv, l, spec, qblocks):
+                need = biv.biv_attention_workspace(ad)
+                biv.biv_attention(ad, self.ws if need else None, stream=st)
+                attn_launches += 1 + (1 if need else 0)   # + the split merge
             if tok:
                 t.close(tok)
             op = self._gemm(self.o, W[p + "wo"], self.a, T, st, defer=defer)
@@ -267,7 +289,7 @@ class DenseModel:
             nxt = W[f"l{l + 1}.attn_norm"] if l + 1 < cfg.layers else W["final_norm"]
             self._add_rmsnorm(self.a, dp, r, nxt, y, T, eps, st)
             # qkv finalize, attention (+ split merge), 2 x add_rmsnorm, silu_mul
-            self.launches += 5 + (1 if need else 0)
+            self.launches += 4 + attn_launches
             if self.audit is not None and not torch.cuda.is_current_stream_capturing():
                 self.audit.append(("layer", l, r.clone()))
         # LM head + logprob over the rows that produce a logprob
@@ -322,6 +344,14 @@ class Runner:
         seq_slot = np.asarray(seq_slot, np.int32)
         pos = np.asarray(pos, np.int32)
         qb = qblocks_for(seq_slot, self.rows_per_block)
+        # prefill blocks first, then single-vector (decode) blocks: a mixed
+        # step runs them as two attention calls (each block is computed on its
+        # own, so the order changes no result)
+        G = m.cfg.q_heads // m.cfg.kv_heads
+        multi = qb[:, 1] * G > 16
+        n_multi = int(multi.sum())
+        if 0 < n_multi < qb.shape[0]:
+            qb = np.concatenate([qb[multi], qb[~multi]])
         slots = kv.slots(seq_slot, pos)
         if write_kv is not None:
             slots = np.where(write_kv, slots, -1)
@@ -337,8 +367,12 @@ class Runner:
         m.h2d_bytes += T * (4 + 4 + 4 + 8) + qb.size * 4 + nl * 8
         cfg = m.cfg
         attn_flops = 4.0 * float(np.sum(pos.astype(np.int64) + 1)) * cfg.q_heads * cfg.head_dim
-        return StepSpec(T=T, nqblocks=int(qb.shape[0]), max_rows_per_block=int(qb[:, 1].max()),
-                        max_ctx=int(pos.max()) + 1, T_lm=nl, attn_flops=attn_flops)
+        mixed = 0 < n_multi < qb.shape[0]
+        return StepSpec(T=T, nqblocks=int(qb.shape[0]),
+                        max_rows_per_block=int(qb[:n_multi if mixed else qb.shape[0], 1].max()),
+                        max_ctx=int(pos.max()) + 1, T_lm=nl, attn_flops=attn_flops,
+                        n_multi=n_multi if mixed else 0,
+                        max_rows_single=int(qb[n_multi:, 1].max()) if mixed else 1)
 
 
 def prefill_rows(seqs, slots, starts, ends, lm_from):
