@@ -48,10 +48,14 @@ constexpr float kLazy = 8.f;
 // per warp, the same arithmetic for every output element).
 // F8: FP8 pages; their codes and scales land in a staging area by cp.async one
 // tile ahead and are dequantised shared-to-shared into the bf16 K/V tiles.
+// One staging buffer: tile t+1's copies are issued once tile t is dequantised
+// (a second buffer was never in use, and without it four decode CTAs fit on
+// an SM instead of three).
 template <int D, int NW, int ST, bool TMA, int DS, bool F8 = false>
 struct AttnCfg {
   static_assert(DS == 1 || DS == NW, "D split: one warp per D slice");
   static_assert(!(F8 && TMA), "FP8 pages use the thread loader");
+  static_assert(!F8 || ST == 2, "FP8 pages: one staged tile in flight");
   static constexpr int LD = D + 8;                   // padded row (elements), thread-loaded tiles
   static constexpr int NV = DS > 1 ? 16 : NW * 16;   // query vectors per CTA
   static constexpr int NT = NW * 32;                 // threads per CTA
@@ -61,8 +65,11 @@ struct AttnCfg {
   static constexpr int Q_BYTES = NV * LD * 2;
   static constexpr int F8_CODES = F8 ? 2 * kTile * D : 0;          // K then V codes
   static constexpr int F8_STAGE = F8 ? F8_CODES + 2 * kTile * 4 : 0;  // + K then V scales
+  // TMA tiles are 128-byte swizzled (1024-byte aligned); thread-loaded ones
+  // need 16 bytes
+  static constexpr int ALIGN = TMA ? 1024 : 16;
   static constexpr int SMEM =
-      1024 + 2 * TST * KVB + Q_BYTES + ST * F8_STAGE + ST * kTile * 4 + 2 * ST * 8;
+      ALIGN + 2 * TST * KVB + Q_BYTES + F8_STAGE + ST * kTile * 4 + 2 * ST * 8;
   static constexpr int DK = D / 16;                  // k-steps of Q.K^T
   static constexpr int DT = D / 8;                   // n-tiles of O
   static constexpr int DTW = DT / DS;                // n-tiles of O per warp
@@ -206,14 +213,14 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
   constexpr int LD = Cfg::LD, NV = Cfg::NV, NT = Cfg::NT, KVB = Cfg::KVB;
   constexpr int DTW = Cfg::DTW;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + Cfg::ALIGN - 1) & ~uintptr_t(Cfg::ALIGN - 1));
   constexpr int TST = Cfg::TST;
   uint8_t* sK = base;                                   // [TST] stages of KVB bytes
   uint8_t* sV = base + TST * KVB;
   uint16_t* sQ = reinterpret_cast<uint16_t*>(base + 2 * TST * KVB);
-  uint8_t* sF8 = base + 2 * TST * KVB + Cfg::Q_BYTES;   // [ST] FP8 staging (F8 only)
-  int32_t* sPos = reinterpret_cast<int32_t*>(sF8 + ST * Cfg::F8_STAGE);  // [ST][64]
+  uint8_t* sF8 = base + 2 * TST * KVB + Cfg::Q_BYTES;   // FP8 staging (F8 only)
+  int32_t* sPos = reinterpret_cast<int32_t*>(sF8 + Cfg::F8_STAGE);  // [ST][64]
   // TMA: K of stage s completes on bars[s], V on bars[ST + s], so that K of
   // the next tile streams in while this tile's softmax and P.V run
   uint64_t* bars = reinterpret_cast<uint64_t*>(sPos + ST * kTile);                 // [2 ST]
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     } else {
       // raw codes (16 per copy) and scales of the tile's keys into the
       // stage's staging area; missing keys read as zero codes and scales
-      uint8_t* stg = sF8 + buf * Cfg::F8_STAGE;
+      uint8_t* stg = sF8;
       constexpr int CPR = D / 16;
       for (int i = tid; i < kTile * CPR * 2; i += NT) {
         const int which = i / (kTile * CPR);
@@ -340,7 +347,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
   };
   // FP8: the staged codes of stage buf -> bf16 K/V tiles, x = bf16(float(code) * s)
   auto dequant_stage = [&](int buf) {
-    const uint8_t* stg = sF8 + buf * Cfg::F8_STAGE;
+    const uint8_t* stg = sF8;
     const float* scl = reinterpret_cast<const float*>(stg + Cfg::F8_CODES);
     constexpr int CPR = D / 16;
     for (int i = tid; i < kTile * CPR * 2; i += NT) {
