@@ -62,7 +62,10 @@ struct AttnCfg {
   static constexpr int KVB = TMA ? kTile * D * 2 : kTile * LD * 2;  // one K or V stage
   // bf16 K/V tile stages: FP8 keeps one (its staging area holds the prefetch)
   static constexpr int TST = F8 ? 1 : ST;
-  static constexpr int Q_BYTES = NV * LD * 2;
+  // Q is read into registers once; with a D split its area then holds the
+  // S tile the warps assemble (8 n-tiles x 32 lanes x 4 FP32)
+  static constexpr int S_BYTES = DS > 1 ? 8 * 32 * 16 : 0;
+  static constexpr int Q_BYTES = NV * LD * 2 > S_BYTES ? NV * LD * 2 : S_BYTES;
   static constexpr int F8_CODES = F8 ? 2 * kTile * D : 0;          // K then V codes
   static constexpr int F8_STAGE = F8 ? F8_CODES + 2 * kTile * 4 : 0;  // + K then V scales
   // TMA tiles are 128-byte swizzled (1024-byte aligned); thread-loaded ones
@@ -438,7 +441,45 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     float s[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-    if (live) {
+    if (DS > 1) {
+      // D split: the warps share one S tile.  Warp w computes its 64 / DS keys
+      // (the same ascending-k chain per element as one warp computing all
+      // of them) and publishes them; every warp then reads the whole tile.
+      constexpr int NPW = 4 / (DS > 1 ? DS : 1);   // n-tile pairs per warp
+      float sw[2 * NPW][4];
+#pragma unroll
+      for (int i = 0; i < 2 * NPW; ++i) sw[i][0] = sw[i][1] = sw[i][2] = sw[i][3] = 0.f;
+      if (live) {
+#pragma unroll
+        for (int kk = 0; kk < Cfg::DK; ++kk) {
+          uint32_t kf[NPW][4];
+#pragma unroll
+          for (int j = 0; j < NPW; ++j) {
+            const int key = (warp * NPW + j) * 16 + (lane & 7) + (lane >> 4) * 8;
+            const int dim = kk * 16 + ((lane >> 3) & 1) * 8;
+            ldsm_x4(tK + Cfg::off(key, dim), kf[j][0], kf[j][1], kf[j][2], kf[j][3]);
+          }
+#pragma unroll
+          for (int j = 0; j < NPW; ++j) {
+            mma_bf16(sw[2 * j], qf[kk], kf[j][0], kf[j][1]);
+            mma_bf16(sw[2 * j + 1], qf[kk], kf[j][2], kf[j][3]);
+          }
+        }
+        float4* sS = reinterpret_cast<float4*>(sQ);
+#pragma unroll
+        for (int i = 0; i < 2 * NPW; ++i)
+          sS[(warp * 2 * NPW + i) * 32 + lane] = make_float4(sw[i][0], sw[i][1], sw[i][2], sw[i][3]);
+      }
+      __syncthreads();   // S published; every warp is also done with K of tile t
+      if (live) {
+        const float4* sS = reinterpret_cast<const float4*>(sQ);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const float4 v = sS[nt * 32 + lane];
+          s[nt][0] = v.x; s[nt][1] = v.y; s[nt][2] = v.z; s[nt][3] = v.w;
+        }
+      }
+    } else if (live) {
     // per k-step: all fragment loads first, then the MMAs (independent
     // accumulators back to back; each accumulator still sees ascending k)
 #pragma unroll
@@ -458,7 +499,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     }
     }  // live
     if (TMA) {
-      __syncthreads();                                  // every warp is done with K of tile t
+      if (DS == 1) __syncthreads();                     // every warp is done with K of tile t
       if (t + ST < ntiles) load_half(buf, t + ST, 0);   // its buffer takes K of tile t+ST
     }
     if (live) {
