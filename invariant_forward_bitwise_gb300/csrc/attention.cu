@@ -71,8 +71,14 @@ struct AttnCfg {
   // TMA tiles are 128-byte swizzled (1024-byte aligned); thread-loaded ones
   // need 16 bytes
   static constexpr int ALIGN = TMA ? 1024 : 16;
-  static constexpr int SMEM =
-      ALIGN + 2 * TST * KVB + Q_BYTES + F8_STAGE + ST * kTile * 4 + 2 * ST * 8;
+  static constexpr int SMEM = ALIGN + 2 * TST * KVB + Q_BYTES + F8_STAGE + ST * kTile * 4 +
+                              2 * ST * 8 + (TMA ? 0 : kTile * 4);
+  // thread-issued copies: how many of a thread's copies read their source
+  // rows before any is issued (cp.async is ordered against every other
+  // memory access, so one at a time would serialise those reads)
+  __host__ __device__ static constexpr int batch(int per) {
+    return per <= 8 ? per : per % 8 == 0 ? 8 : per % 5 == 0 ? 5 : per % 4 == 0 ? 4 : 1;
+  }
   static constexpr int DK = D / 16;                  // k-steps of Q.K^T
   static constexpr int DT = D / 8;                   // n-tiles of O
   static constexpr int DTW = DT / DS;                // n-tiles of O per warp
@@ -227,6 +233,8 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
   // TMA: K of stage s completes on bars[s], V on bars[ST + s], so that K of
   // the next tile streams in while this tile's softmax and P.V run
   uint64_t* bars = reinterpret_cast<uint64_t*>(sPos + ST * kTile);                 // [2 ST]
+  // thread loader: the cache slot of each key of the tile being loaded (-1: none)
+  int32_t* sSlot = reinterpret_cast<int32_t*>(bars + 2 * ST);                       // [64]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int blk = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
@@ -300,51 +308,65 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
         if (p >= hi) p = -1;
       }
       pos_buf[j] = p;
+      sSlot[j] = p >= 0 ? a.bt[int64_t(seq) * a.max_pages + p / kTile] * kTile + p % kTile : -1;
     }
     __syncthreads();
     uint8_t* dK = sK + (buf % TST) * KVB;
     uint8_t* dV = sV + (buf % TST) * KVB;
     if constexpr (!F8) {
       constexpr int CPR = D / 8;
-      for (int i = tid; i < kTile * CPR * 2; i += NT) {
-        const int which = i / (kTile * CPR);
-        const int rem = i % (kTile * CPR);
-        const int j = rem / CPR, c = rem % CPR;
-        const int p = pos_buf[j];
-        const uint16_t* src = static_cast<const uint16_t*>(which ? a.vc : a.kc);
-        const uint16_t* gp = src;
-        if (p >= 0) {
-          const int64_t slot = int64_t(a.bt[int64_t(seq) * a.max_pages + p / kTile]) * kTile + p % kTile;
-          gp = src + slot * kv_row + int64_t(h) * D + c * 8;
+      constexpr int PER = kTile * CPR * 2 / NT, GRP = Cfg::batch(PER);
+      static_assert(kTile * CPR * 2 % NT == 0 && PER % GRP == 0, "copies per thread");
+#pragma unroll
+      for (int g0 = 0; g0 < PER; g0 += GRP) {
+        int sl[GRP];
+#pragma unroll
+        for (int k = 0; k < GRP; ++k) sl[k] = sSlot[((tid + (g0 + k) * NT) % (kTile * CPR)) / CPR];
+#pragma unroll
+        for (int k = 0; k < GRP; ++k) {
+          const int i = tid + (g0 + k) * NT;
+          const int which = i / (kTile * CPR);
+          const int rem = i % (kTile * CPR);
+          const int j = rem / CPR, c = rem % CPR;
+          const uint16_t* gp = static_cast<const uint16_t*>(which ? a.vc : a.kc);
+          if (sl[k] >= 0) gp += int64_t(sl[k]) * kv_row + int64_t(h) * D + c * 8;
+          cp_async16(smem_u32((which ? dV : dK) + Cfg::off(j, c * 8)), gp, sl[k] >= 0);
         }
-        cp_async16(smem_u32((which ? dV : dK) + Cfg::off(j, c * 8)), gp, p >= 0);
       }
     } else {
       // raw codes (16 per copy) and scales of the tile's keys into the
-      // stage's staging area; missing keys read as zero codes and scales
+      // staging area; missing keys read as zero codes and scales
       uint8_t* stg = sF8;
       constexpr int CPR = D / 16;
-      for (int i = tid; i < kTile * CPR * 2; i += NT) {
-        const int which = i / (kTile * CPR);
-        const int rem = i % (kTile * CPR);
-        const int j = rem / CPR, c = rem % CPR;
-        const int p = pos_buf[j];
-        const uint8_t* gp = static_cast<const uint8_t*>(which ? a.vc : a.kc);
-        if (p >= 0) {
-          const int64_t slot = int64_t(a.bt[int64_t(seq) * a.max_pages + p / kTile]) * kTile + p % kTile;
-          gp += slot * kv_row + int64_t(h) * D + c * 16;
+      constexpr int PER = kTile * CPR * 2 / NT, GRP = Cfg::batch(PER);
+      static_assert(kTile * CPR * 2 % NT == 0 && PER % GRP == 0, "copies per thread");
+#pragma unroll
+      for (int g0 = 0; g0 < PER; g0 += GRP) {
+        int sl[GRP];
+#pragma unroll
+        for (int k = 0; k < GRP; ++k) sl[k] = sSlot[((tid + (g0 + k) * NT) % (kTile * CPR)) / CPR];
+#pragma unroll
+        for (int k = 0; k < GRP; ++k) {
+          const int i = tid + (g0 + k) * NT;
+          const int which = i / (kTile * CPR);
+          const int rem = i % (kTile * CPR);
+          const int j = rem / CPR, c = rem % CPR;
+          const uint8_t* gp = static_cast<const uint8_t*>(which ? a.vc : a.kc);
+          if (sl[k] >= 0) gp += int64_t(sl[k]) * kv_row + int64_t(h) * D + c * 16;
+          cp_async16(smem_u32(stg + which * kTile * D + j * D + c * 16), gp, sl[k] >= 0);
         }
-        cp_async16(smem_u32(stg + which * kTile * D + j * D + c * 16), gp, p >= 0);
       }
-      for (int i = tid; i < 2 * kTile; i += NT) {
-        const int which = i / kTile, j = i % kTile;
-        const int p = pos_buf[j];
-        const float* gp = which ? a.vs : a.ks;
-        if (p >= 0) {
-          const int64_t slot = int64_t(a.bt[int64_t(seq) * a.max_pages + p / kTile]) * kTile + p % kTile;
-          gp += slot * a.Hkv + h;
-        }
-        cp_async4(smem_u32(stg + Cfg::F8_CODES + i * 4), gp, p >= 0);
+      constexpr int SPER = 2 * kTile / NT;
+      static_assert(2 * kTile % NT == 0, "scale copies per thread");
+      int sl[SPER];
+#pragma unroll
+      for (int k = 0; k < SPER; ++k) sl[k] = sSlot[(tid + k * NT) % kTile];
+#pragma unroll
+      for (int k = 0; k < SPER; ++k) {
+        const int i = tid + k * NT;
+        const float* gp = i / kTile ? a.vs : a.ks;
+        if (sl[k] >= 0) gp += int64_t(sl[k]) * a.Hkv + h;
+        cp_async4(smem_u32(stg + Cfg::F8_CODES + i * 4), gp, sl[k] >= 0);
       }
     }
   };
@@ -353,12 +375,29 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     const uint8_t* stg = sF8;
     const float* scl = reinterpret_cast<const float*>(stg + Cfg::F8_CODES);
     constexpr int CPR = D / 16;
-    for (int i = tid; i < kTile * CPR * 2; i += NT) {
+    constexpr int PER = kTile * CPR * 2 / NT, GRP = Cfg::batch(PER);
+    // a group's codes and scales are read before any of its stores
+#pragma unroll
+    for (int g0 = 0; g0 < PER; g0 += GRP) {
+    uint4 cvs[GRP];
+    float scs[GRP];
+#pragma unroll
+    for (int k = 0; k < GRP; ++k) {
+      const int i = tid + (g0 + k) * NT;
       const int which = i / (kTile * CPR);
       const int rem = i % (kTile * CPR);
       const int j = rem / CPR, c = rem % CPR;
-      const uint4 cv = *reinterpret_cast<const uint4*>(stg + which * kTile * D + j * D + c * 16);
-      const float sc = scl[which * kTile + j];
+      cvs[k] = *reinterpret_cast<const uint4*>(stg + which * kTile * D + j * D + c * 16);
+      scs[k] = scl[which * kTile + j];
+    }
+#pragma unroll
+    for (int k = 0; k < GRP; ++k) {
+      const int i = tid + (g0 + k) * NT;
+      const int which = i / (kTile * CPR);
+      const int rem = i % (kTile * CPR);
+      const int j = rem / CPR, c = rem % CPR;
+      const uint4 cv = cvs[k];
+      const float sc = scs[k];
       const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
       uint32_t packed[8];
 #pragma unroll
@@ -373,6 +412,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
           make_uint4(packed[0], packed[1], packed[2], packed[3]);
       *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16 + 8)) =
           make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    }
     }
   };
 
@@ -1334,8 +1374,9 @@ biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
       // FP8 decode CTAs: four warps share the staged dequantisation and split
       // the head dimension in P.V (D = 80 keeps one warp: its 10 output
       // n-tiles do not split four ways)
+      // (registers capped so that four of them fit on an SM)
       constexpr int DSF = D % 64 == 0 ? 4 : 1;
-      st = small ? launch_cfg<D, DSF, 2, false, DSF, 0, true>(d, a, s)
+      st = small ? launch_cfg<D, DSF, 2, false, DSF, DSF == 4 ? 4 : 0, true>(d, a, s)
                  : launch_cfg<D, 4, 2, false, 1, 0, true>(d, a, s);
     } else {
       st = small ? launch_cfg<D, 1, 2, false>(d, a, s) : launch_cfg<D, 4, 2, false>(d, a, s);
