@@ -1279,18 +1279,23 @@ int env_int(const char* name, int lo, int hi) {
   const int v = e ? atoi(e) : 0;
   return (v >= lo && v <= hi) ? v : 0;
 }
-bool decode_grid_small(int64_t ctas) {
-  const int sms = sm_count() > 0 ? sm_count() : 148;
-  return ctas < 2 * int64_t(sms);
-}
+// Decode CTA shape by grid size (GB300, 16 q / 8 kv heads, D 128, 16 to 256
+// sequences at 300 to 1400 tokens, graph-replayed over caches larger than
+// L2): a second TMA stage pays only below one CTA per SM; four warps on the
+// head dimension are fastest from two CTAs per SM up to 1024 CTAs (up to 13%
+// over one warp; a whole 64-sequence decode step 2.52 -> 2.40 ms), two below
+// that and up to 2048, and one warp beyond, where the kernel runs at the HBM
+// rate.
 int decode_stages(int64_t ctas) {
   if (const int v = env_int("BIV_ATTN_DECODE_STAGES", 1, 3)) return v;
-  return decode_grid_small(ctas) ? 2 : 1;
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  return ctas < sms ? 2 : 1;
 }
 int decode_dsplit(int64_t ctas) {
   const int v = env_int("BIV_ATTN_DECODE_DSPLIT", 1, 4);
   if (v == 1 || v == 2 || v == 4) return v;
-  return decode_grid_small(ctas) ? 2 : 1;
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  return ctas < 2 * sms ? 2 : ctas <= 1024 ? 4 : ctas <= 2048 ? 2 : 1;
 }
 
 // q as a 3-D tensor [T][Hq][D] with boxes of 64 dims x G heads x 128/G rows:
