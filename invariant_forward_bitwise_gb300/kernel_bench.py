@@ -12,6 +12,8 @@ K 2048, with the log-softmax gather in its epilogue), ssd_prefill (16384 tokens,
 64-expert FP8 block), decode_step (one decode step of the 28-layer model
 at batch BIV_BENCH_BATCH, default 64, from its CUDA graph and eagerly; the
 eager step runs inside cudaProfilerStart/Stop for an ncu launch list) and
+fp8_serving (the FP8-KV continuous-batching workload, REPS timed
+steps; the third and fourth run inside cudaProfilerStart/Stop) and
 prefill_step (one 16384-row step of the 28-layer model: 16 sequences x 1024
 tokens, every row producing a logprob, as in the trainer recompute; one more
 step runs inside cudaProfilerStart/Stop) and hybrid_decode_step (one decode step of the
@@ -125,6 +127,32 @@ if case == "decode_step":
     dg.run(*args)
     torch.cuda.synchronize()
     torch.cuda.cudart().cudaProfilerStop()
+elif case == "fp8_serving":
+    # the FP8-KV continuous-batching workload (bench.py's configs entry) for
+    # REPS timed steps over a pool of BIV_BENCH_POOL sequences; its third and
+    # fourth model steps run inside cudaProfilerStart/Stop
+    import json
+    import bench
+    from invariant_forward_bitwise_gb300 import model as M
+    orig, count = M.DenseModel.step, [0]
+
+    def step(self, *args, **kw):
+        count[0] += 1
+        if count[0] == 3:
+            torch.cuda.synchronize()
+            torch.cuda.cudart().cudaProfilerStart()
+        r = orig(self, *args, **kw)
+        if count[0] == 4:
+            torch.cuda.synchronize()
+            torch.cuda.cudart().cudaProfilerStop()
+        return r
+
+    M.DenseModel.step = step
+    W = synth.dense_weights(synth.QWEN3_1P7B_FP8KV, seed=0)
+    r = bench.fp8_serving(W, bench.load_peaks(), steps=reps,
+                          pool=int(os.environ.get("BIV_BENCH_POOL", "256")))
+    print(f"{case}: {r['value']:.0f} tokens/s, {r['ms_per_step']:.2f} ms per step, "
+          f"roofline {r['roofline']['frac']:.3f}")
 elif case == "prefill_step":
     from invariant_forward_bitwise_gb300.model import DenseModel, PagedKV, Runner, prefill_rows
     cfg = synth.QWEN3_1P7B
