@@ -344,13 +344,19 @@ class Runner:
         seq_slot = np.asarray(seq_slot, np.int32)
         pos = np.asarray(pos, np.int32)
         qb = qblocks_for(seq_slot, self.rows_per_block)
-        # prefill blocks first, then single-vector (decode) blocks: a mixed
-        # step runs them as two attention calls (each block is computed on its
-        # own, so the order changes no result)
+        # prefill blocks first, then single-vector (decode) blocks: a step
+        # that mixes them runs them as two attention calls (each block is
+        # computed on its own, so the order changes no result).  Only when the
+        # single-vector blocks are at least as many as the others: a handful of
+        # short sequence tails in a prefill step cost less inside the prefill
+        # call than as a second call after it (measured on the rollout +
+        # recompute workload: prefill attention 686 -> 819 ms when split).
         G = m.cfg.q_heads // m.cfg.kv_heads
         multi = qb[:, 1] * G > 16
         n_multi = int(multi.sum())
-        if 0 < n_multi < qb.shape[0]:
+        if not 0 < n_multi <= qb.shape[0] - n_multi:
+            n_multi = 0
+        if n_multi:
             qb = np.concatenate([qb[multi], qb[~multi]])
         slots = kv.slots(seq_slot, pos)
         if write_kv is not None:
@@ -367,7 +373,7 @@ class Runner:
         m.h2d_bytes += T * (4 + 4 + 4 + 8) + qb.size * 4 + nl * 8
         cfg = m.cfg
         attn_flops = 4.0 * float(np.sum(pos.astype(np.int64) + 1)) * cfg.q_heads * cfg.head_dim
-        mixed = 0 < n_multi < qb.shape[0]
+        mixed = n_multi > 0
         return StepSpec(T=T, nqblocks=int(qb.shape[0]),
                         max_rows_per_block=int(qb[:n_multi if mixed else qb.shape[0], 1].max()),
                         max_ctx=int(pos.max()) + 1, T_lm=nl, attn_flops=attn_flops,
