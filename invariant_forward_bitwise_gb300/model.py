@@ -326,6 +326,24 @@ def qblocks_for(row_seq: np.ndarray, per: int) -> np.ndarray:
     return np.array(out, np.int32).reshape(-1, 2)
 
 
+def split_blocks(qb: np.ndarray, G: int):
+    """Order query blocks for attention: returns (blocks, n_multi).  When a
+    step holds both multi-row blocks (more than 16 query vectors) and at least
+    as many single-vector (decode-shaped) blocks, the multi-row blocks come
+    first and n_multi counts them: attention then runs them as two calls, the
+    decode-shaped blocks on the decode CTA.  Otherwise the blocks keep their
+    order and n_multi is 0 (one call).  A handful of short sequence tails in a
+    prefill step cost less inside the prefill call than as a second call after
+    it (measured on the rollout + recompute workload: prefill attention 686 ->
+    819 ms when split).  Each block is computed on its own, so neither the
+    order nor the split changes a result."""
+    multi = qb[:, 1] * G > 16
+    n_multi = int(multi.sum())
+    if not 0 < n_multi <= qb.shape[0] - n_multi:
+        return qb, 0
+    return np.concatenate([qb[multi], qb[~multi]]), n_multi
+
+
 class Runner:
     """Feeds host-side row batches into a DenseModel's static inputs."""
 
@@ -343,21 +361,8 @@ class Runner:
         T = len(ids)
         seq_slot = np.asarray(seq_slot, np.int32)
         pos = np.asarray(pos, np.int32)
-        qb = qblocks_for(seq_slot, self.rows_per_block)
-        # prefill blocks first, then single-vector (decode) blocks: a step
-        # that mixes them runs them as two attention calls (each block is
-        # computed on its own, so the order changes no result).  Only when the
-        # single-vector blocks are at least as many as the others: a handful of
-        # short sequence tails in a prefill step cost less inside the prefill
-        # call than as a second call after it (measured on the rollout +
-        # recompute workload: prefill attention 686 -> 819 ms when split).
-        G = m.cfg.q_heads // m.cfg.kv_heads
-        multi = qb[:, 1] * G > 16
-        n_multi = int(multi.sum())
-        if not 0 < n_multi <= qb.shape[0] - n_multi:
-            n_multi = 0
-        if n_multi:
-            qb = np.concatenate([qb[multi], qb[~multi]])
+        qb, n_multi = split_blocks(qblocks_for(seq_slot, self.rows_per_block),
+                                   m.cfg.q_heads // m.cfg.kv_heads)
         slots = kv.slots(seq_slot, pos)
         if write_kv is not None:
             slots = np.where(write_kv, slots, -1)

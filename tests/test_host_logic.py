@@ -64,3 +64,37 @@ def test_decode_buckets(model_mod):
         assert k == min(x for x in b if x >= n)                 # the smallest that fits
     with pytest.raises(ValueError):
         DG.bucket(fake, b[-1] + 1)
+
+
+def test_split_blocks_two_calls_only_when_decode_blocks_dominate(model_mod):
+    G = 2
+    # a prefill step: 64-row blocks with two short sequence tails -> one call
+    qb = np.array([(0, 64), (64, 64), (128, 5), (133, 64), (197, 3)], np.int32)
+    out, n = model_mod.split_blocks(qb, G)
+    assert n == 0 and np.array_equal(out, qb)
+    # a mixed step: one prefill chunk's blocks next to more decode rows -> the
+    # multi-row blocks first, their relative order kept, then the rest
+    qb = np.array([(0, 1), (1, 32), (33, 1), (34, 32), (66, 1), (67, 8)], np.int32)
+    out, n = model_mod.split_blocks(qb, G)
+    assert n == 2
+    assert np.array_equal(out[:2], qb[[1, 3]])
+    assert np.array_equal(out[2:], qb[[0, 2, 4, 5]])
+    # a block of 8 rows at G = 2 is 16 vectors: decode-shaped; 9 rows is not
+    assert model_mod.split_blocks(np.array([(0, 9), (9, 8)], np.int32), G)[1] == 1
+    assert model_mod.split_blocks(np.array([(0, 9), (9, 9)], np.int32), G)[1] == 0
+    # pure decode and pure prefill steps stay one call
+    for qb in (np.array([(i, 1) for i in range(7)], np.int32),
+               np.array([(0, 64), (64, 64)], np.int32)):
+        out, n = model_mod.split_blocks(qb, G)
+        assert n == 0 and np.array_equal(out, qb)
+    # every block appears exactly once, whatever the mix
+    g = np.random.default_rng(9)
+    for _ in range(50):
+        rows = g.integers(1, 65, size=g.integers(1, 40))
+        starts = np.concatenate([[0], np.cumsum(rows)[:-1]])
+        qb = np.stack([starts, rows], 1).astype(np.int32)
+        out, n = model_mod.split_blocks(qb, G)
+        assert sorted(map(tuple, out)) == sorted(map(tuple, qb))
+        if n:
+            assert np.all(out[:n, 1] * G > 16) and np.all(out[n:, 1] * G <= 16)
+            assert qb.shape[0] - n >= n
