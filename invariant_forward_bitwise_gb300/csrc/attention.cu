@@ -42,10 +42,12 @@ constexpr int kNVTc = 128;  // most query vectors a block may hold (attn_tc_kern
 constexpr float kLazy = 8.f;
 
 // NW warps per CTA, ST-stage K/V pipeline, TMA or thread-issued loads, and
-// DS: 1 = each warp owns 16 query vectors (prefill blocks); DS = NW = every
-// warp forms the same S and softmax for one group of 16 vectors and takes
-// 1/DS of the head dimension in P.V (decode blocks: shorter dependency chains
-// per warp, the same arithmetic for every output element).
+// DS: 1 = each warp owns 16 query vectors (prefill blocks); DS = NW = the
+// warps share one group of 16 vectors: each computes 64/DS keys of the score
+// tile, the tile is exchanged through shared memory, every warp runs the same
+// softmax on all of it and takes 1/DS of the head dimension in P.V (decode
+// blocks: shorter dependency chains per warp, the same arithmetic for every
+// output element).
 // F8: FP8 pages; their codes and scales land in a staging area by cp.async one
 // tile ahead and are dequantised shared-to-shared into the bf16 K/V tiles.
 // One staging buffer: tile t+1's copies are issued once tile t is dequantised
