@@ -570,7 +570,7 @@ def fp8_serving(W, peaks, steps=24, pool=256, chunk=512, seed=5):
                          "peak_source": peaks["source"]}}
 
 
-def moe_sparse_block(peaks, steps=5, warmup=3, seed=7):
+def moe_sparse_block(peaks, steps=5, warmup=3, seed=7, profile_step=False):
     """The MoE + sparse-attention block, 4096 tokens per step: indexer scores of
     4096 queries (positions 28672..32767) against a 32768-token context (one
     128-d head, FP32 out), top 2048 positions per query (lowest position wins
@@ -579,7 +579,8 @@ def moe_sparse_block(peaks, steps=5, warmup=3, seed=7):
     expert intermediate 1408, FP8 e4m3 weights with 128x128 scales) and the
     FP32 fixed-slot combine.  Inputs drawn on the device from a seeded
     generator.  Roofline: the sum of each part's lower bound over the
-    measured time."""
+    measured time.  profile_step: one more step after the timed ones, inside
+    cudaProfilerStart/Stop (for an ncu launch list)."""
     import math
     import torch
     import synth
@@ -642,6 +643,11 @@ def moe_sparse_block(peaks, steps=5, warmup=3, seed=7):
     e1.record(st)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    if profile_step:
+        torch.cuda.cudart().cudaProfilerStart()
+        step()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStop()
     bw, tf = peaks["hbm_gbs"] * 1e9, peaks["bf16_tflops_sustained"] * 1e12
     fp8 = 2.0 * tf          # FP8 dense rate: the nominal 2x of bf16
     parts = {

@@ -42,12 +42,13 @@ constexpr int kNVTc = 128;  // most query vectors a block may hold (attn_tc_kern
 constexpr float kLazy = 8.f;
 
 // NW warps per CTA, ST-stage K/V pipeline, TMA or thread-issued loads, and
-// DS: 1 = each warp owns 16 query vectors (prefill blocks); DS = NW = the
-// warps share one group of 16 vectors: each computes 64/DS keys of the score
-// tile, the tile is exchanged through shared memory, every warp runs the same
-// softmax on all of it and takes 1/DS of the head dimension in P.V (decode
-// blocks: shorter dependency chains per warp, the same arithmetic for every
-// output element).
+// DS: 1 = each warp owns 16 query vectors (prefill blocks); DS > 1 = DS
+// consecutive warps share one group of 16 vectors (NW / DS groups): each
+// computes 64/DS keys of the group's score tile, the tile is exchanged
+// through shared memory, every warp of the group runs the same softmax on all
+// of it and takes 1/DS of the head dimension in P.V (decode blocks, and the
+// 32-vector blocks of the sparse path: shorter dependency chains per warp,
+// the same arithmetic for every output element).
 // F8: FP8 pages; their codes and scales land in a staging area by cp.async one
 // tile ahead and are dequantised shared-to-shared into the bf16 K/V tiles.
 // One staging buffer: tile t+1's copies are issued once tile t is dequantised
@@ -55,18 +56,18 @@ constexpr float kLazy = 8.f;
 // an SM instead of three).
 template <int D, int NW, int ST, bool TMA, int DS, bool F8 = false>
 struct AttnCfg {
-  static_assert(DS == 1 || DS == NW, "D split: one warp per D slice");
+  static_assert(NW % DS == 0 && 4 % DS == 0, "D split: DS warps per vector group");
   static_assert(!(F8 && TMA), "FP8 pages use the thread loader");
   static_assert(!F8 || ST == 2, "FP8 pages: one staged tile in flight");
   static constexpr int LD = D + 8;                   // padded row (elements), thread-loaded tiles
-  static constexpr int NV = DS > 1 ? 16 : NW * 16;   // query vectors per CTA
+  static constexpr int NV = NW / DS * 16;            // query vectors per CTA
   static constexpr int NT = NW * 32;                 // threads per CTA
   static constexpr int KVB = TMA ? kTile * D * 2 : kTile * LD * 2;  // one K or V stage
   // bf16 K/V tile stages: FP8 keeps one (its staging area holds the prefetch)
   static constexpr int TST = F8 ? 1 : ST;
-  // Q is read into registers once; with a D split its area then holds the
-  // S tile the warps assemble (8 n-tiles x 32 lanes x 4 FP32)
-  static constexpr int S_BYTES = DS > 1 ? 8 * 32 * 16 : 0;
+  // Q is read into registers once; with a D split its area then holds each
+  // group's S tile as the warps assemble it (8 n-tiles x 32 lanes x 4 FP32)
+  static constexpr int S_BYTES = DS > 1 ? NW / DS * 8 * 32 * 16 : 0;
   static constexpr int Q_BYTES = NV * LD * 2 > S_BYTES ? NV * LD * 2 : S_BYTES;
   static constexpr int F8_CODES = F8 ? 2 * kTile * D : 0;          // K then V codes
   static constexpr int F8_STAGE = F8 ? F8_CODES + 2 * kTile * 4 : 0;  // + K then V scales
@@ -420,8 +421,8 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
 
   // per-thread rows: g and g+8 of the warp's 16 vectors (vw: their group);
   // O n-tiles dt0 .. dt0+DTW-1 of the head dimension
-  const int vw = DS > 1 ? 0 : warp;
-  const int dt0 = DS > 1 ? warp * DTW : 0;
+  const int vw = warp / DS;
+  const int dt0 = (warp % DS) * DTW;
   const int g = lane >> 2, cq = lane & 3;
   int vpos[2];
 #pragma unroll
@@ -484,10 +485,12 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
 #pragma unroll
     for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
     if (DS > 1) {
-      // D split: the warps share one S tile.  Warp w computes its 64 / DS keys
-      // (the same ascending-k chain per element as one warp computing all
-      // of them) and publishes them; every warp then reads the whole tile.
+      // D split: a group's warps share one S tile.  Warp w of the group
+      // computes its 64 / DS keys (the same ascending-k chain per element as
+      // one warp computing all of them) and publishes them; every warp of
+      // the group then reads the whole tile.
       constexpr int NPW = 4 / (DS > 1 ? DS : 1);   // n-tile pairs per warp
+      const int wg = warp % DS;                     // the warp's place in its group
       float sw[2 * NPW][4];
 #pragma unroll
       for (int i = 0; i < 2 * NPW; ++i) sw[i][0] = sw[i][1] = sw[i][2] = sw[i][3] = 0.f;
@@ -497,7 +500,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
           uint32_t kf[NPW][4];
 #pragma unroll
           for (int j = 0; j < NPW; ++j) {
-            const int key = (warp * NPW + j) * 16 + (lane & 7) + (lane >> 4) * 8;
+            const int key = (wg * NPW + j) * 16 + (lane & 7) + (lane >> 4) * 8;
             const int dim = kk * 16 + ((lane >> 3) & 1) * 8;
             ldsm_x4(tK + Cfg::off(key, dim), kf[j][0], kf[j][1], kf[j][2], kf[j][3]);
           }
@@ -507,14 +510,14 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
             mma_bf16(sw[2 * j + 1], qf[kk], kf[j][2], kf[j][3]);
           }
         }
-        float4* sS = reinterpret_cast<float4*>(sQ);
+        float4* sS = reinterpret_cast<float4*>(sQ) + vw * 8 * 32;
 #pragma unroll
         for (int i = 0; i < 2 * NPW; ++i)
-          sS[(warp * 2 * NPW + i) * 32 + lane] = make_float4(sw[i][0], sw[i][1], sw[i][2], sw[i][3]);
+          sS[(wg * 2 * NPW + i) * 32 + lane] = make_float4(sw[i][0], sw[i][1], sw[i][2], sw[i][3]);
       }
       __syncthreads();   // S published; every warp is also done with K of tile t
       if (live) {
-        const float4* sS = reinterpret_cast<const float4*>(sQ);
+        const float4* sS = reinterpret_cast<const float4*>(sQ) + vw * 8 * 32;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
           const float4 v = sS[nt * 32 + lane];
@@ -1385,8 +1388,17 @@ biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
       constexpr int DSF = D % 64 == 0 ? 4 : 1;
       st = small ? launch_cfg<D, DSF, 2, false, DSF, DSF == 4 ? 4 : 0, true>(d, a, s)
                  : launch_cfg<D, 4, 2, false, 1, 0, true>(d, a, s);
+    } else if (small) {
+      st = launch_cfg<D, 1, 2, false>(d, a, s);
+    } else if (D % 64 == 0 && d.max_rows_per_block * a.G <= 32 &&
+               !(getenv("BIV_ATTN_GROUP_DSPLIT") && atoi(getenv("BIV_ATTN_GROUP_DSPLIT")) == 0)) {
+      // blocks of 17-32 vectors (sparse rows of a 32-head MQA): two vector
+      // groups of two warps each, instead of four warps of which two are
+      // idle.  BIV_ATTN_GROUP_DSPLIT=0 keeps the four-warp CTA (tests: no
+      // bit changes).
+      st = launch_cfg<D, 4, 2, false, D % 64 == 0 ? 2 : 1>(d, a, s);
     } else {
-      st = small ? launch_cfg<D, 1, 2, false>(d, a, s) : launch_cfg<D, 4, 2, false>(d, a, s);
+      st = launch_cfg<D, 4, 2, false>(d, a, s);
     }
   }
   if (st != BIV_OK || a.nsplit_grid <= 1) return st;

@@ -13,7 +13,9 @@ K 2048, with the log-softmax gather in its epilogue), ssd_prefill (16384 tokens,
 at batch BIV_BENCH_BATCH, default 64, from its CUDA graph and eagerly; the
 eager step runs inside cudaProfilerStart/Stop for an ncu launch list) and
 fp8_serving (the FP8-KV continuous-batching workload, REPS timed
-steps; the third and fourth run inside cudaProfilerStart/Stop) and
+steps; the third and fourth run inside cudaProfilerStart/Stop),
+moe_sparse_step (the MoE + sparse-attention block workload, REPS timed steps
+and one more inside cudaProfilerStart/Stop) and
 prefill_step (one 16384-row step of the 28-layer model: 16 sequences x 1024
 tokens, every row producing a logprob, as in the trainer recompute; one more
 step runs inside cudaProfilerStart/Stop) and hybrid_decode_step (one decode step of the
@@ -152,6 +154,13 @@ elif case == "fp8_serving":
     r = bench.fp8_serving(W, bench.load_peaks(), steps=reps,
                           pool=int(os.environ.get("BIV_BENCH_POOL", "256")))
     print(f"{case}: {r['value']:.0f} tokens/s, {r['ms_per_step']:.2f} ms per step, "
+          f"roofline {r['roofline']['frac']:.3f}")
+elif case == "moe_sparse_step":
+    # the MoE + sparse-attention block workload (bench.py's configs entry):
+    # REPS timed steps, then one more inside cudaProfilerStart/Stop
+    import bench
+    r = bench.moe_sparse_block(bench.load_peaks(), steps=reps, profile_step=True)
+    print(f"{case}: {r['value']:.0f} tokens/s, {r['ms_per_step']*1e3:.1f} us per step, "
           f"roofline {r['roofline']['frac']:.3f}")
 elif case == "prefill_step":
     from invariant_forward_bitwise_gb300.model import DenseModel, PagedKV, Runner, prefill_rows

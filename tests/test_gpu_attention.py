@@ -260,6 +260,46 @@ def test_tma_loader_equals_thread_loader(B, D):
     assert np.array_equal(bits(dec), bits(a[torch.tensor(last, device="cuda")]))
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_grouped_dsplit_cta_changes_no_bit(B, monkeypatch, D):
+    """Blocks of 17-32 query vectors on the thread loader run two vector
+    groups of two warps (split keys in S, split head dimension in P.V); they
+    give the bits of the four-warp CTA: sparse MQA rows (32 heads on one KV
+    head, several 64-key tiles and splits, a short list) and dense blocks of
+    12 rows at G = 2 with ragged tails."""
+    g = synth.rng(91 + D)
+    L, Hq = 700, 32
+    pc = Paged(B, g, [L], 1, D)
+    qpos = [699, 650, 100, 5]
+    topk = 320
+    idx = np.full((len(qpos), topk), -1, np.int32)
+    for r, p in enumerate(qpos):
+        cand = g.permutation(p + 1)[:min(topk, p + 1)]
+        idx[r, :cand.size] = np.sort(cand)
+    rows = [(0, p) for p in qpos]
+    q = synth.normal_bf16(g, (len(qpos), Hq * D)).cuda()
+    blocks = [(i, 1) for i in range(len(qpos))]
+    kw = dict(kv_split=128, topk_idx=torch.from_numpy(idx).cuda(), topk=topk)
+    got = run_attn(B, pc, q, rows, blocks, Hq, **kw)
+    monkeypatch.setenv("BIV_ATTN_GROUP_DSPLIT", "0")
+    ref = run_attn(B, pc, q, rows, blocks, Hq, **kw)
+    assert np.array_equal(bits(got), bits(ref))
+    monkeypatch.delenv("BIV_ATTN_GROUP_DSPLIT")
+    # dense, thread loader: 12-row blocks of 16 q / 8 kv heads (24 vectors)
+    lens = [300, 129, 70]
+    pc2 = Paged(B, g, lens, 8, D)
+    rows2 = [(i, p) for i, n in enumerate(lens) for p in range(n)]
+    q2 = synth.normal_bf16(g, (len(rows2), 16 * D)).cuda()
+    blocks2 = blocks_of(rows2, 12)
+    got2 = run_attn(B, pc2, q2, rows2, blocks2, 16, kv_split=256, tma=False)
+    monkeypatch.setenv("BIV_ATTN_GROUP_DSPLIT", "0")
+    ref2 = run_attn(B, pc2, q2, rows2, blocks2, 16, kv_split=256, tma=False)
+    assert np.array_equal(bits(got2), bits(ref2))
+    # and both equal the one-row blocks of the same rows
+    one = run_attn(B, pc2, q2, rows2, [(i, 1) for i in range(len(rows2))], 16, kv_split=256, tma=False)
+    assert np.array_equal(bits(got2), bits(one))
+
+
 @pytest.mark.parametrize("stages,dsplit", [("1", "1"), ("2", "2"), ("3", "4"), ("1", "4")])
 @pytest.mark.parametrize("D", [64, 128])
 def test_decode_cta_shape_changes_no_bit(B, monkeypatch, stages, dsplit, D):
