@@ -1394,8 +1394,8 @@ biv_status launch(const biv_attn_desc& d, AttnArgs& a, cudaStream_t s) {
                !(getenv("BIV_ATTN_GROUP_DSPLIT") && atoi(getenv("BIV_ATTN_GROUP_DSPLIT")) == 0)) {
       // blocks of 17-32 vectors (sparse rows of a 32-head MQA): two vector
       // groups of two warps each, instead of four warps of which two are
-      // idle (GB300, the 4096-row top-2048 MQA step: 2.82 ms against 3.16;
-      // eight warps in two groups of four took 3.13).  BIV_ATTN_GROUP_DSPLIT=0
+      // idle (GB300, a 4096-token block with top-2048 MQA attention and the
+      // MoE: 2.82 ms a step against 3.16; two groups of four warps: 3.13).  BIV_ATTN_GROUP_DSPLIT=0
       // keeps the four-warp CTA (tests: no bit changes).
       st = launch_cfg<D, 4, 2, false, D % 64 == 0 ? 2 : 1>(d, a, s);
     } else {
