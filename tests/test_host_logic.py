@@ -98,3 +98,28 @@ def test_split_blocks_two_calls_only_when_decode_blocks_dominate(model_mod):
         if n:
             assert np.all(out[:n, 1] * G > 16) and np.all(out[n:, 1] * G <= 16)
             assert qb.shape[0] - n >= n
+
+
+def test_decode_step_bytes_counts_each_weight_once_and_the_kv_it_reads():
+    """The decode-step roofline's algorithmic bytes: every distinct weight
+    tensor once (a tied LM head shares the embedding), 114,688 B of K/V per
+    cached token for the Qwen3-1.7B shape in bf16 (28 layers x K and V x 8 kv
+    heads x 128 x 2 B), e4m3 codes plus one fp32 scale per token and kv head
+    for the FP8 cache, and per row its own K/V write plus the (max, sum exp)
+    pairs of its 128-logit groups."""
+    import torch
+    import bench
+    cfg = synth.QWEN3_1P7B
+    emb = torch.empty(cfg.vocab, cfg.hidden, dtype=torch.bfloat16, device="meta")
+    other = torch.empty(1000, 10, dtype=torch.bfloat16, device="meta")
+    W = {"embed": emb, "lm_head": emb, "w": other}
+    work = bench.decode_step_bytes(cfg, W)
+    wb = (cfg.vocab * cfg.hidden + 1000 * 10) * 2
+    assert work.weight_bytes == wb
+    assert work.kv_bytes_per_token == 114_688
+    groups = (cfg.vocab + 127) // 128
+    pos = [699] * 64 + [5]
+    want = wb + (64 * 700 + 6) * 114_688 + 65 * (114_688 + 2 * groups * 8)
+    assert work(pos) == float(want)
+    fp8 = bench.decode_step_bytes(synth.QWEN3_1P7B_FP8KV, W)
+    assert fp8.kv_bytes_per_token == 28 * 2 * (8 * 128 + 8 * 4)
