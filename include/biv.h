@@ -203,9 +203,9 @@ biv_status biv_kv_fp8_gather(const uint8_t* codes, const float* scales,
  * attends to keys at positions <= row_pos[t] of its sequence, read from the
  * paged cache through block_table.  Keys are visited in 64-token tiles aligned
  * to absolute positions, grouped into splits of kv_split tokens (a model
- * constant); each split keeps an online softmax (FP32), P enters P.V as a
- * bf16 hi + lo pair (about 16 significant bits), and the splits are merged
- * in ascending order in FP32.  With topk_idx != NULL (sparse attention) the
+ * constant); each split keeps an online softmax (FP32), P enters P.V as
+ * three bf16 parts hi + mid + lo that add up to the FP32 p exactly, and the
+ * splits are merged in ascending order in FP32.  With topk_idx != NULL (sparse attention) the
  * keys of row t are the positions topk_idx[t, 0..topk) (ascending, -1 =
  * none) and splits run over that list.
  * qblocks int32 [nqblocks, 2] = (first row, row count): rows of a block must
@@ -227,7 +227,10 @@ typedef struct {
   const void* v_cache;
   const float* k_scale;     /* [pages, page, Hkv] (E4M3 only) */
   const float* v_scale;
-  const int32_t* block_table; /* [nseq, max_pages] */
+  const int32_t* block_table; /* [nseq, max_pages]: page indices, 0 <= page < 2^31 / 64
+                                 (the thread loader raises the device error word on a
+                                 negative or larger entry, reads zeros for that page's
+                                 keys and leaves the outputs that see them undefined) */
   int max_pages;
   int page;                 /* must be 64 */
   int kv_split;             /* tokens per split, multiple of 64 (INVARIANT: model constant) */

@@ -311,7 +311,15 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
         if (p >= hi) p = -1;
       }
       pos_buf[j] = p;
-      sSlot[j] = p >= 0 ? a.bt[int64_t(seq) * a.max_pages + p / kTile] * kTile + p % kTile : -1;
+      int sl = -1;
+      if (p >= 0) {
+        const int pg = a.bt[int64_t(seq) * a.max_pages + p / kTile];
+        if (pg >= 0 && pg <= (INT_MAX - (kTile - 1)) / kTile)
+          sl = pg * kTile + p % kTile;
+        else
+          raise_error(a.err, kErrBadIndex);   // a page index no slot number can hold
+      }
+      sSlot[j] = sl;
     }
     __syncthreads();
     uint8_t* dK = sK + (buf % TST) * KVB;
