@@ -131,6 +131,52 @@ def test_rope_rotation_properties():
     assert abs(d1 - d2) < 0.05 * (np.abs(q).sum() * np.abs(k).max())
 
 
+def test_qk_norm_rope_is_head_norm_then_rotation():
+    g = np.random.default_rng(12)
+    T, H, D = 7, 3, 64
+    x = randn(g, T, H, D, std=3.0)
+    pos = g.integers(0, 500, size=T)
+    cos, sin = ops.rope_table(1e4, D, 512)
+    # no norm weight: RoPE alone
+    assert np.array_equal(ops.qk_norm_rope(x, pos, None, 1e-6, cos, sin), ops.rope(x, pos, cos, sin))
+    one = np.ones(D, F32)
+    # at position 0 the rotation is the identity: each head normalised on its own
+    y0 = ops.qk_norm_rope(x, np.zeros(T, np.int64), one, 1e-6, cos, sin).astype(np.float64)
+    x64 = x.astype(np.float64)
+    n = x64 / np.sqrt(np.mean(x64 * x64, axis=-1, keepdims=True) + 1e-6)
+    assert np.all(np.abs(y0 - n) <= 2 ** -8 * np.abs(n) + 1e-30)
+    # elsewhere the rotation keeps each head's RMS at 1 (a dropped sin or cos
+    # term would not)
+    y = ops.qk_norm_rope(x, pos, one, 1e-6, cos, sin).astype(np.float64)
+    assert np.all(np.abs(np.sqrt(np.mean(y * y, axis=-1)) - 1.0) < 1e-2)
+
+
+def test_kv_roundtrip_within_e4m3_half_spacing():
+    """Per (token, head): s = amax / 448, x -> bf16(e4m3(x / s) * s).  e4m3
+    keeps 3 mantissa bits, so the code is off by at most 2^-4 of the value
+    (normal codes) or 2^-10 * s (subnormal codes), and the bf16 rounding adds
+    at most 2^-8 of the result; more is a slip.  The amax element maps to code
+    448 and comes back to the bf16 rounding, and an all-zero row stays zero."""
+    g = np.random.default_rng(13)
+    T, H, D = 40, 4, 128
+    mag = np.power(10.0, g.uniform(-3, 3, size=(T, H, 1)))
+    x = (g.standard_normal((T, H, D)) * mag).astype(F32)
+    x[3, 2] = 0.0
+    rt = ops.kv_roundtrip(x).astype(np.float64)
+    x64 = x.astype(np.float64)
+    s = np.max(np.abs(x64), axis=-1, keepdims=True) / 448.0
+    e8 = np.maximum(np.abs(x64) * 2 ** -4, s * 2 ** -10)
+    bound = (e8 + 2 ** -8 * (np.abs(x64) + e8)) * (1 + 1e-5)
+    assert np.all(np.abs(rt - x64) <= bound)
+    am = np.argmax(np.abs(x64), axis=-1)[..., None]
+    ta, ra = np.take_along_axis(x64, am, -1), np.take_along_axis(rt, am, -1)
+    nz = ta != 0
+    assert np.all(np.abs(ra - ta)[nz] <= 2 ** -8 * (1 + 1e-5) * np.abs(ta)[nz])
+    assert np.all(rt[3, 2] == 0.0)
+    # finer than that: a random row is not returned unchanged
+    assert not np.array_equal(rt, x64)
+
+
 # ------------------------------------------------------------ attention ----
 def test_attention_against_torch_sdpa_causal_gqa():
     g = np.random.default_rng(7)
