@@ -5,8 +5,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.codecs import (E4M3_TABLE, bf16_round, bf16_to_f32, e4m3_to_f32,
-                           f32_to_bf16, f32_to_e4m3)
+from oracle.codecs import (E4M3_TABLE, bf16_round, bf16_to_f32, e2m1_to_f32, e4m3_to_f32,
+                           f32_to_bf16, f32_to_e4m3, nvfp4_dequant, nvfp4_unpack)
 from oracle import ops
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
@@ -120,3 +120,39 @@ def test_fp8_quant_rows_rules():
     c2, s2 = ops.fp8_quant_rows(xq)
     assert np.array_equal(ops.fp8_dequant_rows(c2, s2), ops.fp8_dequant_rows(c, s)) or \
         np.max(np.abs(ops.fp8_dequant_rows(c2, s2) - xq)) <= 2 ** -6 * np.max(np.abs(xq))
+
+
+def test_e2m1_matches_ocp_fixture():
+    got = e2m1_to_f32(np.arange(16, dtype=np.uint8))
+    n = 0
+    for code, val in _rows("e2m1_ocp_values.txt"):
+        c = int(code, 16)
+        assert got[c] == float(val) and np.signbit(got[c]) == val.startswith("-"), (code, got[c])
+        n += 1
+    assert n == 16
+    # only the low nibble is a code
+    assert np.array_equal(e2m1_to_f32(np.arange(256, dtype=np.uint8)), np.tile(got, 16))
+
+
+def test_nvfp4_unpack_low_nibble_first():
+    packed = np.array([[0x21, 0x0F, 0xA5]], np.uint8)
+    assert np.array_equal(nvfp4_unpack(packed), np.array([[1, 2, 15, 0, 5, 10]], np.uint8))
+
+
+def test_nvfp4_dequant_exact_products_on_the_bf16_grid():
+    """Every (e2m1 code, finite e4m3 scale) product is exact in FP32 and a
+    bf16 value; scale j covers the 16 elements 16j .. 16j+15 of its row."""
+    codes = np.arange(16, dtype=np.uint8)
+    scales = np.array([c for c in range(256) if np.isfinite(E4M3_TABLE[c])], np.uint8)
+    for sc in scales:
+        packed = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)[None, :]   # one block of 16
+        w = nvfp4_dequant(packed, np.array([[sc]], np.uint8))[0]
+        want = e2m1_to_f32(codes).astype(np.float64) * float(E4M3_TABLE[sc])
+        assert np.array_equal(w.astype(np.float64), want)
+        assert np.array_equal(bf16_round(w), w)
+    # block mapping: three blocks with scales 1, 2, 0.5 on the same codes
+    packed = np.tile((codes[0::2] | (codes[1::2] << 4)).astype(np.uint8), 3)[None, :]
+    s = f32_to_e4m3(np.array([[1.0, 2.0, 0.5]], np.float32))
+    w = nvfp4_dequant(packed, s)[0]
+    base = e2m1_to_f32(codes)
+    assert np.array_equal(w, np.concatenate([base, 2 * base, 0.5 * base]).astype(np.float32))
