@@ -390,40 +390,40 @@ __global__ void __launch_bounds__(NW * 32, MINB) attn_kernel(const __grid_consta
     // a group's codes and scales are read before any of its stores
 #pragma unroll
     for (int g0 = 0; g0 < PER; g0 += GRP) {
-    uint4 cvs[GRP];
-    float scs[GRP];
+      uint4 cvs[GRP];
+      float scs[GRP];
 #pragma unroll
-    for (int k = 0; k < GRP; ++k) {
-      const int i = tid + (g0 + k) * NT;
-      const int which = i / (kTile * CPR);
-      const int rem = i % (kTile * CPR);
-      const int j = rem / CPR, c = rem % CPR;
-      cvs[k] = *reinterpret_cast<const uint4*>(stg + which * kTile * D + j * D + c * 16);
-      scs[k] = scl[which * kTile + j];
-    }
-#pragma unroll
-    for (int k = 0; k < GRP; ++k) {
-      const int i = tid + (g0 + k) * NT;
-      const int which = i / (kTile * CPR);
-      const int rem = i % (kTile * CPR);
-      const int j = rem / CPR, c = rem % CPR;
-      const uint4 cv = cvs[k];
-      const float sc = scs[k];
-      const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
-      uint32_t packed[8];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f01 = e4m3x2_to_float2(uint16_t(w[q] & 0xFFFFu));
-        const float2 f23 = e4m3x2_to_float2(uint16_t(w[q] >> 16));
-        packed[2 * q] = pack_bf2(f01.x * sc, f01.y * sc);
-        packed[2 * q + 1] = pack_bf2(f23.x * sc, f23.y * sc);
+      for (int k = 0; k < GRP; ++k) {
+        const int i = tid + (g0 + k) * NT;
+        const int which = i / (kTile * CPR);
+        const int rem = i % (kTile * CPR);
+        const int j = rem / CPR, c = rem % CPR;
+        cvs[k] = *reinterpret_cast<const uint4*>(stg + which * kTile * D + j * D + c * 16);
+        scs[k] = scl[which * kTile + j];
       }
-      uint8_t* dst = (which ? sV : sK) + (buf % TST) * KVB;
-      *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16)) =
-          make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16 + 8)) =
-          make_uint4(packed[4], packed[5], packed[6], packed[7]);
-    }
+#pragma unroll
+      for (int k = 0; k < GRP; ++k) {
+        const int i = tid + (g0 + k) * NT;
+        const int which = i / (kTile * CPR);
+        const int rem = i % (kTile * CPR);
+        const int j = rem / CPR, c = rem % CPR;
+        const uint4 cv = cvs[k];
+        const float sc = scs[k];
+        const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
+        uint32_t packed[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f01 = e4m3x2_to_float2(uint16_t(w[q] & 0xFFFFu));
+          const float2 f23 = e4m3x2_to_float2(uint16_t(w[q] >> 16));
+          packed[2 * q] = pack_bf2(f01.x * sc, f01.y * sc);
+          packed[2 * q + 1] = pack_bf2(f23.x * sc, f23.y * sc);
+        }
+        uint8_t* dst = (which ? sV : sK) + (buf % TST) * KVB;
+        *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16)) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        *reinterpret_cast<uint4*>(dst + Cfg::off(j, c * 16 + 8)) =
+            make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      }
     }
   };
 
