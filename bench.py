@@ -143,7 +143,8 @@ def run_reference(args, rank):
     """The reference arm: the CPU oracle, timed on the host's cores."""
     if rank != 0:
         return
-    sample = "1 sequence (prompt 48, response 48) of the full 28-layer shape: oracle rollout + recompute per step"
+    shape = "the full 28-layer shape" if args.layers == 28 else f"the shape cut to {args.layers} layers"
+    sample = f"1 sequence (prompt 48, response 48) of {shape}: oracle rollout + recompute per step"
     for _ in range(args.warmup):
         oracle_sample(args.layers)
     times, toks = [], 0

@@ -1,6 +1,7 @@
-"""The N>1 path of bench.py on CPU: replicas over gloo, world size 2.  Each
-rank runs its own sequences; the step time is the max over ranks and the
-whole-job throughput counts every rank's tokens (no data-path collective)."""
+"""bench.py's host logic on CPU.  The N>1 path: replicas over gloo, world
+size 2.  Each rank runs its own sequences; the step time is the max over
+ranks and the whole-job throughput counts every rank's tokens (no data-path
+collective).  And the reference arm's JSON line."""
 import os
 import socket
 
@@ -44,3 +45,29 @@ def test_two_rank_replicas_max_time_and_whole_job_value():
         assert ms == 150.0
         assert value == pytest.approx(2 * 1000 / 0.150)
         assert firsts[0] != firsts[1]          # different sequences per rank
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    """The reference arm (the CPU oracle on the host's cores) prints one JSON
+    line with the contract's keys; rank 0 alone runs it."""
+    import json
+    import types
+    import bench
+    calls = []
+
+    def fake_sample(layers):
+        calls.append(layers)
+        return 96 / 2.0, 2.0, 96
+    monkeypatch.setattr(bench, "oracle_sample", fake_sample)
+    args = types.SimpleNamespace(gpus=1, steps=2, warmup=3, layers=28)
+    bench.run_reference(args, rank=1)
+    assert calls == [] and capsys.readouterr().out == ""
+    bench.run_reference(args, rank=0)
+    assert calls == [28] * 5
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["impl"] == "reference" and line["value"] == 48.0 and line["unit"] == bench.UNIT
+    assert line["metric"] == bench.METRIC and line["steps"] == 2 and line["warmup"] == 3
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == 48.0 and cb["cores"] >= 1 and "28-layer" in cb["sample"]
+    assert line["e2e"] == {"value": 48.0, "unit": bench.UNIT, "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
