@@ -312,6 +312,26 @@ def test_moe_combine_one_hot_and_order():
     assert np.allclose(ops.moe_combine(y, w2, sh), ref, rtol=2 ** -7, atol=1e-6)
 
 
+def test_moe_combine_fixed_fp32_order():
+    """The merge is one FP32 accumulator over slots 0..k-1 in order, the shared
+    expert added last.  a = 1 + 2^-8 is the midpoint between two bf16 values
+    and t = 3 * 2^-26 is three quarters of half an FP32 ulp of a: added to a
+    one at a time, each t is lost and the sum stays on the midpoint (bf16
+    rounds it to even, 1.0); two t added together first (1.5 half-ulps) push
+    the sum past it (bf16 1.0078125).  So any other order shows in the bits."""
+    a, t = F32(1 + 2 ** -8), F32(3 * 2 ** -26)
+    one = np.ones((1, 3), F32)
+    y = np.zeros((1, 3, 4), F32)
+    y[0, :, 0] = [a, t, t]            # in slot order: a, then each t lost
+    assert ops.moe_combine(y, one)[0, 0] == F32(1.0)
+    assert ops.moe_combine(y[:, ::-1], one)[0, 0] == F32(1.0078125)   # the reverse order differs
+    y2 = np.zeros((1, 2, 4), F32)
+    y2[0, :, 0] = [t, a]              # slots t, a, then the shared expert t
+    sh = np.zeros((1, 4), F32)
+    sh[0, 0] = t
+    assert ops.moe_combine(y2, one[:, :2], sh)[0, 0] == F32(1.0)
+
+
 # ---------------------------------------------------------- log-softmax ----
 def test_log_softmax_normalised_and_against_torch():
     g = np.random.default_rng(15)
