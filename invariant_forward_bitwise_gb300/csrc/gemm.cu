@@ -359,6 +359,7 @@ __global__ void __launch_bounds__(kGemmThreads, PARTIAL ? 2 : 1)
   } else {
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3, col0 = ((warp - 2) >> 2) * HALF;
+    constexpr bool kStream1 = F32OUT && !LSE && !PARTIAL;
     float r[PARTIAL ? 1 : HALF];
     int j = 0;
     bool ok = true;
@@ -395,6 +396,52 @@ __global__ void __launch_bounds__(kGemmThreads, PARTIAL ? 2 : 1)
                                 __uint_as_float(v[x + 2]), __uint_as_float(v[x + 3]));
             }
           }
+        } else if (kStream1 && item_c1(i) - item_c0(i) == 1) {
+          // FP32 output from one chunk: nothing to fold, so 32 columns at a
+          // time go from TMEM through the warp's staging block to memory,
+          // with no running sums held (the same values the fold path stores;
+          // the fold path's 128 sums a thread spill on 256-column tiles)
+          constexpr int W = F32OUT ? 4 : 8;
+          constexpr int LPR = 32 / W, RPI = 32 / LPR;
+          float* stg = staging + (warp - 2) * 32 * kStagePitch;
+          const int rows = min(32, p.M - (m0 + q * 32));   // live rows of this warp
+          const int sub = lane % LPR, rsub = lane / LPR;
+#pragma unroll 1
+          for (int blk = 0; blk < HALF / 32; ++blk) {
+            uint32_t v32[32];
+            tmem_ld32(ta + blk * 32, v32);
+            tmem_ld_wait();
+            __syncwarp();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) stg[lane * kStagePitch + x] = __uint_as_float(v32[x]);
+            __syncwarp();
+            const int n = n0 + col0 + blk * 32 + sub * W;
+#pragma unroll
+            for (int it = 0; it < 32 / RPI; ++it) {
+              const int jr = it * RPI + rsub;
+              if (jr >= rows || n >= p.N) continue;
+              float v[W];
+#pragma unroll
+              for (int e = 0; e < W; ++e) v[e] = stg[jr * kStagePitch + sub * W + e];
+              const int64_t off = int64_t(m0 + q * 32 + jr) * p.ldc + n;
+              if (p.vec_ok && n + W <= p.N) {
+                if (F32OUT)
+                  *reinterpret_cast<float4*>(static_cast<float*>(p.C) + off) =
+                      make_float4(v[0], v[1], v[2], v[3]);
+                else
+                  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.C) + off) =
+                      make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]),
+                                 pack_bf2(v[6], v[7]));
+              } else {
+                for (int e = 0; e < W && n + e < p.N; ++e) {
+                  if (F32OUT)
+                    static_cast<float*>(p.C)[off + e] = v[e];
+                  else
+                    static_cast<uint16_t*>(p.C)[off + e] = f2bf(v[e]);
+                }
+              }
+            }
+          }
         } else {
           // 16-column loads keep the running sum plus one load in registers
 #pragma unroll
@@ -417,6 +464,7 @@ __global__ void __launch_bounds__(kGemmThreads, PARTIAL ? 2 : 1)
       }
       if (partial) continue;  // gemm_fold_kernel finishes the tile
       if (!ok) break;
+      if (kStream1 && item_c1(i) - item_c0(i) == 1) continue;   // streamed above
       if constexpr (LSE) {
         static_assert(HALF == kLseGroup, "one 128-column group per epilogue thread");
         // the row's logits z[nb .. nb+nv) of this half tile: their max, then
